@@ -1,0 +1,349 @@
+"""CPU oracle for the MoE FFN hot path -- TEST INFRASTRUCTURE ONLY.
+
+A plain fp64 C implementation (moe_oracle.c) of what the path computes,
+loaded with ctypes.  Only tests/, __graft_entry__.smoke() and bench.py's
+CPU-baseline / reference leg may import this package; the CUDA product path
+never does, and the two share no code.
+
+bf16 tensors cross this boundary as uint16 bit patterns (numpy), fp32 as
+float32, indices as int32.  Every function cites the passage it follows in
+moe_oracle.c.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from typing import Sequence
+
+import numpy as np
+
+from . import build as _build
+
+_lib = None
+
+_u16p = C.POINTER(C.c_uint16)
+_u8p = C.POINTER(C.c_uint8)
+_i32p = C.POINTER(C.c_int32)
+_i64p = C.POINTER(C.c_int64)
+_f32p = C.POINTER(C.c_float)
+_f64p = C.POINTER(C.c_double)
+_i64 = C.c_int64
+_int = C.c_int
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        L.oracle_bf16_to_double.restype = C.c_double
+        L.oracle_bf16_to_double.argtypes = [C.c_uint16]
+        L.oracle_double_to_bf16.restype = C.c_uint16
+        L.oracle_double_to_bf16.argtypes = [C.c_double]
+        L.oracle_e4m3_to_double.restype = C.c_double
+        L.oracle_e4m3_to_double.argtypes = [C.c_uint8]
+        L.oracle_double_to_e4m3.restype = C.c_uint8
+        L.oracle_double_to_e4m3.argtypes = [C.c_double]
+        L.oracle_quantize_mxfp8.restype = None
+        L.oracle_quantize_mxfp8.argtypes = [_u16p, _i64, _i64, _i64, _i64, _u8p, _u8p]
+        L.oracle_route_topk.restype = None
+        L.oracle_route_topk.argtypes = [_f32p, _i64, _int, _int, _i32p, _f32p]
+        L.oracle_permute.restype = _i64
+        L.oracle_permute.argtypes = [_i32p, _i64, _int, _int, _int, _i32p, _i32p, _i64, _i32p, _i32p]
+        L.oracle_gather_rows.restype = None
+        L.oracle_gather_rows.argtypes = [_u16p, _int, _int, _i32p, _i64, _u16p]
+        pp16 = C.POINTER(_u16p)
+        pp8 = C.POINTER(_u8p)
+        L.oracle_moe_fwd.restype = None
+        L.oracle_moe_fwd.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p, pp16, pp16, pp16,
+                                     _i32p, _f32p, _int, _f64p, _f64p, _f64p, _f64p]
+        L.oracle_moe_fwd_mxfp8.restype = None
+        L.oracle_moe_fwd_mxfp8.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p,
+                                           pp8, pp8, pp8, pp8, pp8, pp8, _i32p, _f32p, _int,
+                                           _f64p, _f64p]
+        L.oracle_moe_bwd.restype = None
+        L.oracle_moe_bwd.argtypes = [_i64, _int, _int, _int, _int, _u16p, pp16, pp16, pp16,
+                                     _i32p, _f32p, _u16p, _int, _f64p, _f64p, _f64p, _f64p, _f64p]
+        L.oracle_moe_bwd_dx_tokens.restype = None
+        L.oracle_moe_bwd_dx_tokens.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p, pp16, pp16,
+                                               pp16, _i32p, _f32p, _u16p, _int, _f64p, _f64p]
+        L.oracle_moe_bwd_dw_entries.restype = None
+        L.oracle_moe_bwd_dw_entries.argtypes = [_i64, _i32p, _i32p, _i32p, _i32p, _i64, _int, _int,
+                                                _int, _int, _u16p, pp16, pp16, pp16, _i32p, _f32p,
+                                                _u16p, _int, _f64p]
+        L.oracle_unpermute_combine.restype = None
+        L.oracle_unpermute_combine.argtypes = [_u16p, _i32p, _f32p, _i64, _int, _int, _int, _f64p]
+        L.oracle_num_threads.restype = _int
+        L.oracle_num_threads.argtypes = []
+        _lib = L
+    return _lib
+
+
+# ---------------------------------------------------------------- helpers
+
+def _c(a: np.ndarray, dtype) -> np.ndarray:
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def _p(a: np.ndarray | None, ptype):
+    if a is None:
+        return None
+    return a.ctypes.data_as(ptype)
+
+
+def bf16_bits(t) -> np.ndarray:
+    """uint16 bit patterns of a bf16 torch tensor (copied to the host)."""
+    import torch
+    return t.detach().to("cpu").contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bits_to_float(b: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns -> float64 values (exact)."""
+    return (np.asarray(b, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def double_to_bf16_bits(a: np.ndarray) -> np.ndarray:
+    L = lib()
+    flat = np.asarray(a, dtype=np.float64).ravel()
+    out = np.fromiter((L.oracle_double_to_bf16(float(v)) for v in flat), dtype=np.uint16, count=flat.size)
+    return out.reshape(np.shape(a))
+
+
+def round_bf16(a: np.ndarray) -> np.ndarray:
+    """Round a float64 array to bf16 values (RNE), returned as float64."""
+    return bits_to_float(double_to_bf16_bits(a))
+
+
+def e4m3_to_double(code: int) -> float:
+    return lib().oracle_e4m3_to_double(code)
+
+
+def double_to_e4m3(v: float) -> int:
+    return lib().oracle_double_to_e4m3(v)
+
+
+def num_threads() -> int:
+    return lib().oracle_num_threads()
+
+
+class _PtrArray:
+    """Per-expert pointer array (None entries become NULL)."""
+
+    def __init__(self, arrays: Sequence[np.ndarray | None], ptype, dtype):
+        self.keep = [None if a is None else _c(a, dtype) for a in arrays]
+        self.arr = (ptype * len(self.keep))(*[(_p(a, ptype) if a is not None else ptype()) for a in self.keep])
+
+
+def _experts(W, E):
+    """Accept an [E,...] array or a sequence/dict of per-expert arrays."""
+    if isinstance(W, dict):
+        return [W.get(e) for e in range(E)]
+    if isinstance(W, np.ndarray):
+        return [W[e] for e in range(E)]
+    return list(W)
+
+
+# ---------------------------------------------------------------- A1, A2
+
+def route_topk(logits: np.ndarray, k: int):
+    """Top-k routing, softmax over the selected k (moe_oracle.c, A1)."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    lib().oracle_route_topk(_p(lg, _f32p), T, E, k, _p(idx, _i32p), _p(w, _f32p))
+    return idx, w
+
+
+def permute(topk_idx: np.ndarray, E: int, align: int = 1, rows_cap: int | None = None):
+    """Stable counting sort of routes by expert (moe_oracle.c, A2)."""
+    ti = _c(topk_idx, np.int32)
+    T, k = ti.shape
+    R = T * k
+    if rows_cap is None:
+        rows_cap = R + E * (align - 1)
+    dst = np.empty(R, np.int32)
+    src = np.empty(rows_cap, np.int32)
+    gs = np.empty(E, np.int32)
+    go = np.empty(E + 1, np.int32)
+    bad = lib().oracle_permute(_p(ti, _i32p), T, k, E, align, _p(dst, _i32p), _p(src, _i32p),
+                               rows_cap, _p(gs, _i32p), _p(go, _i32p))
+    return {"dst_of_route": dst.reshape(T, k), "src_of_row": src, "group_sizes": gs,
+            "group_offsets": go, "n_invalid": int(bad)}
+
+
+def gather_rows(x_bits: np.ndarray, k: int, src_of_row: np.ndarray, rows: int) -> np.ndarray:
+    xb = _c(x_bits, np.uint16)
+    H = xb.shape[1]
+    src = _c(src_of_row, np.int32)
+    out = np.empty((rows, H), np.uint16)
+    lib().oracle_gather_rows(_p(xb, _u16p), H, k, _p(src, _i32p), rows, _p(out, _u16p))
+    return out
+
+
+def unpermute_combine(y_perm_bits: np.ndarray, dst_of_route: np.ndarray, topk_w: np.ndarray,
+                      round_mode: int = 1) -> np.ndarray:
+    """Weighted combine in slot order (moe_oracle.c, A5)."""
+    yb = _c(y_perm_bits, np.uint16)
+    H = yb.shape[1]
+    dst = _c(dst_of_route, np.int32)
+    tw = _c(topk_w, np.float32)
+    T, k = dst.shape
+    out = np.empty((T, H))
+    lib().oracle_unpermute_combine(_p(yb, _u16p), _p(dst, _i32p), _p(tw, _f32p), T, H, k,
+                                   round_mode, _p(out, _f64p))
+    return out
+
+
+# ---------------------------------------------------------------- A3..A5
+
+def moe_fwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, tokens=None, round_mode: int = 1,
+            want_fc1: bool = False, want_h: bool = False, want_y: bool = False):
+    """Per-token forward: SwiGLU experts + weighted combine (moe_oracle.c).
+
+    Returns dict with out (float64 [n,H]) and optional per-route fc1 [n*k,2F],
+    h [n*k,F], y [n*k,H] (NaN rows for dropped routes)."""
+    xb = _c(x_bits, np.uint16)
+    T, H = xb.shape
+    ti = _c(topk_idx, np.int32)
+    tw = _c(topk_w, np.float32)
+    k = ti.shape[1]
+    wg = _experts(Wg, None if not isinstance(Wg, np.ndarray) else Wg.shape[0])
+    E = len(wg)
+    wu = _experts(Wu, E)
+    wd = _experts(Wd, E)
+    F = next(a for a in wg if a is not None).shape[1]
+    toks = None if tokens is None else _c(tokens, np.int64)
+    n = T if toks is None else toks.size
+    out = np.empty((n, H), np.float64)
+    fc1 = np.full((n * k, 2 * F), np.nan) if want_fc1 else None
+    h = np.full((n * k, F), np.nan) if want_h else None
+    y = np.full((n * k, H), np.nan) if want_y else None
+    pg, pu, pd = (_PtrArray(a, _u16p, np.uint16) for a in (wg, wu, wd))
+    lib().oracle_moe_fwd(n, _p(toks, _i64p), H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr, pd.arr,
+                         _p(ti, _i32p), _p(tw, _f32p), round_mode, _p(out, _f64p),
+                         _p(fc1, _f64p), _p(h, _f64p), _p(y, _f64p))
+    return {"out": out, "fc1": fc1, "h": h, "y": y}
+
+
+def quantize_mxfp8(in_bits: np.ndarray, n_vec: int, K: int, stride_vec: int, stride_k: int):
+    """MXFP8 (E4M3 + UE8M0 per 1x32 block along K) of n_vec vectors
+    (moe_oracle.c, oracle_quantize_mxfp8).  Returns (codes [n_vec,K],
+    scales [n_vec,K/32])."""
+    ib = _c(in_bits, np.uint16)
+    data = np.empty((n_vec, K), np.uint8)
+    scale = np.empty((n_vec, K // 32), np.uint8)
+    lib().oracle_quantize_mxfp8(_p(ib, _u16p), n_vec, K, stride_vec, stride_k,
+                                _p(data, _u8p), _p(scale, _u8p))
+    return data, scale
+
+
+def quantize_rows_mxfp8(rows_bits: np.ndarray):
+    """Quantise each row of a [n,K] bf16 matrix along K."""
+    n, K = rows_bits.shape
+    return quantize_mxfp8(rows_bits, n, K, K, 1)
+
+
+def quantize_cols_mxfp8(mat_bits: np.ndarray):
+    """Quantise each column of a [K,N] bf16 matrix along K; codes are
+    returned K-contiguous as [N,K] with scales [N,K/32]."""
+    K, N = mat_bits.shape
+    return quantize_mxfp8(mat_bits, N, K, 1, N)
+
+
+def moe_fwd_mxfp8(x_bits, Wg_q, Wg_s, Wu_q, Wu_s, Wd_q, Wd_s, topk_idx, topk_w,
+                  tokens=None, round_mode: int = 1, want_y: bool = False):
+    """MXFP8 forward for a list of tokens (moe_oracle.c, A7).  Weight codes
+    and scales are per expert (None for experts not needed): W_gate/W_up as
+    [F,H] codes with [F,H/32] scales, W_down as [H,F] codes with [H,F/32]."""
+    xb = _c(x_bits, np.uint16)
+    T, H = xb.shape
+    ti = _c(topk_idx, np.int32)
+    tw = _c(topk_w, np.float32)
+    k = ti.shape[1]
+    lists = [list(a) if not isinstance(a, dict) else a for a in (Wg_q, Wg_s, Wu_q, Wu_s, Wd_q, Wd_s)]
+    E = len(lists[0]) if not isinstance(lists[0], dict) else max(lists[0].keys()) + 1
+    lists = [_experts(a, E) for a in lists]
+    F = next(a for a in lists[0] if a is not None).shape[0]
+    toks = None if tokens is None else _c(tokens, np.int64)
+    n = T if toks is None else toks.size
+    out = np.empty((n, H), np.float64)
+    y = np.full((n * k, H), np.nan) if want_y else None
+    ptrs = [_PtrArray(a, _u8p, np.uint8) for a in lists]
+    lib().oracle_moe_fwd_mxfp8(n, _p(toks, _i64p), H, F, E, k, _p(xb, _u16p),
+                               *[p.arr for p in ptrs], _p(ti, _i32p), _p(tw, _f32p), round_mode,
+                               _p(out, _f64p), _p(y, _f64p))
+    return {"out": out, "y": y}
+
+
+# ---------------------------------------------------------------- A8
+
+def moe_bwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, round_mode: int = 1):
+    """Full backward on a small problem (moe_oracle.c, oracle_moe_bwd)."""
+    xb = _c(x_bits, np.uint16)
+    T, H = xb.shape
+    ti = _c(topk_idx, np.int32)
+    tw = _c(topk_w, np.float32)
+    db = _c(dY_bits, np.uint16)
+    k = ti.shape[1]
+    wg = _experts(Wg, Wg.shape[0] if isinstance(Wg, np.ndarray) else None)
+    E = len(wg)
+    wu, wd = _experts(Wu, E), _experts(Wd, E)
+    F = next(a for a in wg if a is not None).shape[1]
+    dx = np.empty((T, H))
+    dWg = np.empty((E, H, F))
+    dWu = np.empty((E, H, F))
+    dWd = np.empty((E, F, H))
+    dtw = np.empty((T, k))
+    pg, pu, pd = (_PtrArray(a, _u16p, np.uint16) for a in (wg, wu, wd))
+    lib().oracle_moe_bwd(T, H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr, pd.arr, _p(ti, _i32p),
+                         _p(tw, _f32p), _p(db, _u16p), round_mode, _p(dx, _f64p), _p(dWg, _f64p),
+                         _p(dWu, _f64p), _p(dWd, _f64p), _p(dtw, _f64p))
+    return {"dx": dx, "dW_gate": dWg, "dW_up": dWu, "dW_down": dWd, "d_topk_w": dtw}
+
+
+def moe_bwd_dx_tokens(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, tokens, round_mode: int = 1):
+    """dx and d_topk_w of selected tokens (moe_oracle.c)."""
+    xb = _c(x_bits, np.uint16)
+    T, H = xb.shape
+    ti = _c(topk_idx, np.int32)
+    tw = _c(topk_w, np.float32)
+    db = _c(dY_bits, np.uint16)
+    k = ti.shape[1]
+    wg = _experts(Wg, Wg.shape[0] if isinstance(Wg, np.ndarray) else None)
+    E = len(wg)
+    wu, wd = _experts(Wu, E), _experts(Wd, E)
+    F = next(a for a in wg if a is not None).shape[1]
+    toks = _c(tokens, np.int64)
+    n = toks.size
+    dx = np.empty((n, H))
+    dtw = np.empty((n, k))
+    pg, pu, pd = (_PtrArray(a, _u16p, np.uint16) for a in (wg, wu, wd))
+    lib().oracle_moe_bwd_dx_tokens(n, _p(toks, _i64p), H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr,
+                                   pd.arr, _p(ti, _i32p), _p(tw, _f32p), _p(db, _u16p), round_mode,
+                                   _p(dx, _f64p), _p(dtw, _f64p))
+    return {"dx": dx, "d_topk_w": dtw}
+
+
+def moe_bwd_dw_entries(entries, x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, round_mode: int = 1):
+    """Selected weight-gradient entries; entries = [(which, e, a, b)] with
+    which 0 = dW_gate[e,h,f], 1 = dW_up[e,h,f], 2 = dW_down[e,f,n]."""
+    ent = np.asarray(entries, dtype=np.int32).reshape(-1, 4)
+    which, ee, aa, bb = (np.ascontiguousarray(ent[:, i]) for i in range(4))
+    xb = _c(x_bits, np.uint16)
+    T, H = xb.shape
+    ti = _c(topk_idx, np.int32)
+    tw = _c(topk_w, np.float32)
+    db = _c(dY_bits, np.uint16)
+    k = ti.shape[1]
+    wg = _experts(Wg, Wg.shape[0] if isinstance(Wg, np.ndarray) else None)
+    E = len(wg)
+    wu, wd = _experts(Wu, E), _experts(Wd, E)
+    F = next(a for a in wg if a is not None).shape[1]
+    val = np.empty(len(ent))
+    pg, pu, pd = (_PtrArray(a, _u16p, np.uint16) for a in (wg, wu, wd))
+    lib().oracle_moe_bwd_dw_entries(len(ent), _p(which, _i32p), _p(ee, _i32p), _p(aa, _i32p),
+                                    _p(bb, _i32p), T, H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr,
+                                    pd.arr, _p(ti, _i32p), _p(tw, _f32p), _p(db, _u16p),
+                                    round_mode, _p(val, _f64p))
+    return val
