@@ -1,0 +1,226 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) Mixture-of-Experts FFN hot path.
+ *
+ * One GPU, one stream per call, no host synchronisation on the hot path:
+ *
+ *   moe_route_topk        router logits -> top-k expert ids and weights
+ *   moe_permute           tokens -> expert-contiguous rows, group sizes and
+ *                         offsets written on the device
+ *   moe_grouped_ffn_fwd   grouped gate/up GEMM + SwiGLU, grouped down GEMM
+ *   moe_unpermute_combine weighted top-k combine back to token order
+ *   moe_grouped_ffn_bwd   dSwiGLU + grouped dgrad / wgrad GEMMs
+ *   moe_grouped_quantize_mxfp8 / moe_grouped_ffn_fwd_mxfp8  MXFP8 path
+ *
+ * Conventions for every call:
+ *   - Pointers named in a call's doc as "device" are device pointers owned by
+ *     the caller; the library never frees or keeps them past the call, and
+ *     allocates no device memory on these paths.
+ *   - bf16 tensors are passed as moe_bf16_t (the raw 16-bit pattern).
+ *   - Matrices are dense row-major with the innermost dimension contiguous
+ *     and no padding between rows, unless stated otherwise.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without waiting.  Problem sizes that
+ *     depend on routing are read on the device, so every call can be
+ *     captured in a CUDA graph.
+ *   - Host-side argument errors return a status before anything is
+ *     enqueued.  Errors found in device data (an expert id outside [-1, E),
+ *     a wait that timed out) set bits in the device error word at offset 0
+ *     of the workspace; read it with moe_read_device_error (the one call
+ *     that synchronises).  Kernels never trap.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+typedef uint16_t moe_bf16_t;          /* bf16 bit pattern */
+typedef struct CUstream_st *moe_stream_t; /* same type as cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* a null pointer, a negative or inconsistent size */
+    MOE_ERR_UNSUPPORTED = 2,   /* a size outside what the kernels handle (alignment, limits) */
+    MOE_ERR_CUDA = 3,          /* a CUDA runtime/driver call failed (launch, encode, copy) */
+    MOE_ERR_DEVICE_DATA = 4,   /* returned by moe_read_device_error when the word is non-zero */
+    MOE_ERR_WORKSPACE = 5,     /* workspace null or smaller than moe_workspace_bytes */
+} moe_status_t;
+
+/* Bits of the device error word (uint32 at workspace offset 0). */
+#define MOE_DEVERR_BAD_EXPERT_ID 0x1u  /* a topk id outside [-1, E): route treated as dropped */
+#define MOE_DEVERR_TIMEOUT       0x2u  /* a bounded device wait gave up; outputs are invalid */
+#define MOE_DEVERR_CAPACITY      0x4u  /* routed rows exceed rows_cap; extra rows not written */
+
+/* Human-readable name of a status (static storage). */
+MOE_API const char *moe_status_string(moe_status_t status);
+
+/* ABI version of this header (incremented on incompatible changes). */
+MOE_API int moe_abi_version(void);
+
+/* ------------------------------------------------------------------ */
+/* Workspace                                                           */
+/* ------------------------------------------------------------------ */
+
+/* Bytes of device workspace that moe_permute, moe_grouped_ffn_fwd(_mxfp8)
+ * and moe_grouped_ffn_bwd need for a problem with T tokens, E experts and
+ * top-k: the error word (offset 0) plus the permutation's per-chunk expert
+ * counts.  Returns 0 for invalid sizes. */
+MOE_API size_t moe_workspace_bytes(int64_t T, int E, int k);
+
+/* Zero the error word (and any state) of a workspace, on `stream`. */
+MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* Copy the device error word to *out (synchronises `stream`).  Returns
+ * MOE_OK if the word is 0, MOE_ERR_DEVICE_DATA if any bit is set,
+ * MOE_ERR_CUDA if the copy failed. */
+MOE_API moe_status_t moe_read_device_error(const void *ws, moe_stream_t stream, uint32_t *out);
+
+/* ------------------------------------------------------------------ */
+/* A1  Top-k routing                                                    */
+/* ------------------------------------------------------------------ */
+
+/* Top-k routing over fp32 router logits ("[JAX] Expert Parallelism: JAX
+ * primitives + VJPs", commit log: fused top-k router with fp32 logits; the
+ * score function, a softmax over the k selected logits, is the workload's).
+ *
+ *   logits   device fp32 [T, E]
+ *   topk_idx device int32 [T, k] out: for each token the k experts ranked
+ *            first by (logit descending, expert id ascending); +0 and -0
+ *            are equal; NaN ranks below -inf.  Slot j is the j-th ranked.
+ *   topk_w   device fp32 [T, k] out: w_j = exp(l_j - l_0) / sum_i exp(l_i
+ *            - l_0) over the selected logits; all 0 when l_0 = -inf.
+ *
+ * Limits: 1 <= E <= 1024, 1 <= k <= min(E, 32), T >= 0 (T = 0 is a no-op).
+ * Logits must be finite or -inf for the weights to be defined.
+ * Errors: MOE_ERR_INVALID_ARG (null pointer with T > 0, negative T),
+ * MOE_ERR_UNSUPPORTED (E or k out of range), MOE_ERR_CUDA. */
+MOE_API moe_status_t moe_route_topk(const float *logits, int64_t T, int E, int k,
+                            int32_t *topk_idx, float *topk_w, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* A2  Permutation into expert-contiguous order                         */
+/* ------------------------------------------------------------------ */
+
+/* One-GPU counterpart of the expert-parallel dispatch ("[JAX] Expert
+ * Parallelism", commit log: receive buffer laid out expert-major, per-expert
+ * token counts fed to the grouped GEMM from device memory; "Add MoE +
+ * expert-parallel Python API surface, PyTorch reference, and tests":
+ * "-1 = dropped route", other ids out of range are an error).
+ *
+ * Routes are flattened r = t*k + j.  Route r with id e in [0, E) gets row
+ * group_offsets[e] + #{r' < r : id(r') == e} (stable order); each group
+ * occupies round_up(group_sizes[e], align) rows.
+ *
+ *   x             device bf16 [T, H] tokens
+ *   topk_idx      device int32 [T, k]; -1 = dropped route; an id outside
+ *                 [-1, E) sets MOE_DEVERR_BAD_EXPERT_ID and is dropped
+ *   x_perm        device bf16 [rows_cap, H] out: row dst_of_route[r] holds
+ *                 x[r / k]; padding rows (align > 1) are zero; rows past
+ *                 group_offsets[E] are not written
+ *   rows_cap      capacity of x_perm / src_of_row; must be >= T*k +
+ *                 E*(align-1) so that every route fits
+ *   dst_of_route  device int32 [T, k] out: row of each route, -1 if dropped
+ *   src_of_row    device int32 [rows_cap] out: route r of each row, -1 for
+ *                 padding rows; rows past group_offsets[E] are not written
+ *   group_sizes   device int32 [E] out: routes per expert
+ *   group_offsets device int32 [E+1] out: first row of each group;
+ *                 group_offsets[E] = rows used
+ *   ws, ws_bytes  device workspace of at least moe_workspace_bytes(T,E,k)
+ *                 bytes, initialised once with moe_workspace_init
+ *
+ * Limits: H % 8 == 0, 1 <= E <= 1024, 1 <= k <= 32, 1 <= align <= 1024.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE,
+ * MOE_ERR_CUDA; device: MOE_DEVERR_BAD_EXPERT_ID. */
+MOE_API moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx, int64_t T, int H,
+                         int E, int k, int align, moe_bf16_t *x_perm, int64_t rows_cap,
+                         int32_t *dst_of_route, int32_t *src_of_row, int32_t *group_sizes,
+                         int32_t *group_offsets, void *ws, size_t ws_bytes,
+                         moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* A3 + A4  Grouped expert FFN, forward                                 */
+/* ------------------------------------------------------------------ */
+
+/* For every expert e and every row i in [group_offsets[e], group_offsets[e+1]):
+ *   g = x_perm[i] W_gate[e],  u = x_perm[i] W_up[e]     (fp32 accumulation)
+ *   h[i] = bf16(silu(g) * u)                            (SwiGLU, fp32)
+ *   y_perm[i] = h[i] W_down[e]                          (fp32 accumulation, fp32 result)
+ * ("Add MoE + expert-parallel Python API surface, PyTorch reference, and
+ * tests", Summary: local SwiGLU experts silu(gate) * up, the fc1_c stash;
+ * "[Draft][JAX] MoE block optimization", diagram: fused grouped GEMM and
+ * SwiGLU, then the down projection.)
+ *
+ *   x_perm        device bf16 [rows_cap, H] (from moe_permute)
+ *   W_gate, W_up  device bf16 [E, H, F]
+ *   W_down        device bf16 [E, F, H]
+ *   group_offsets device int32 [E+1] (from moe_permute); read on the device
+ *   rows_cap      rows of x_perm / h / y_perm; group_offsets[E] <= rows_cap
+ *   h             device bf16 [rows_cap, F] out (rows of groups only)
+ *   y_perm        device fp32 [rows_cap, H] out (rows of groups only); kept in
+ *                 fp32 so that the combine adds unrounded expert outputs
+ *   fc1_c         device bf16 [rows_cap, 2F] out, or NULL: the pre-SwiGLU
+ *                 accumulators rounded to bf16, gate in columns [0, F) and
+ *                 up in [F, 2F); needed by moe_grouped_ffn_bwd
+ *   ws, ws_bytes  workspace (error word)
+ *
+ * Limits: H % 128 == 0, F % 128 == 0, 1 <= E <= 1024, rows_cap < 2^31.
+ * Rows outside every group are neither read into results nor written.
+ * Errors: MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE,
+ * MOE_ERR_CUDA; device: MOE_DEVERR_TIMEOUT. */
+MOE_API moe_status_t moe_grouped_ffn_fwd(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                 const moe_bf16_t *W_up, const moe_bf16_t *W_down,
+                                 const int32_t *group_offsets, int E, int H, int F,
+                                 int64_t rows_cap, moe_bf16_t *h, float *y_perm,
+                                 moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                 moe_stream_t stream);
+
+/* The two halves of moe_grouped_ffn_fwd, callable on their own (same
+ * arguments, same limits and errors):
+ *   moe_grouped_fc1_swiglu  x_perm -> h (and the optional fc1_c stash)
+ *   moe_grouped_fc2         h -> y_perm */
+MOE_API moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                            const moe_bf16_t *W_up, const int32_t *group_offsets,
+                                            int E, int H, int F, int64_t rows_cap, moe_bf16_t *h,
+                                            moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                            moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_down,
+                                     const int32_t *group_offsets, int E, int H, int F,
+                                     int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
+                                     moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* A5  Weighted unpermute / combine                                     */
+/* ------------------------------------------------------------------ */
+
+/* out[t] = bf16( sum_{j<k} topk_w[t,j] * y_perm[dst_of_route[t,j]] ), the
+ * sum taken in fp32 in slot order; routes with dst -1 contribute nothing
+ * ("Add MoE + expert-parallel Python API surface, PyTorch reference, and
+ * tests", Summary: per-top-k combine; "[JAX] Expert Parallelism", sequence
+ * diagram: the combine that returns expert outputs to token order).
+ *
+ *   y_perm       device fp32 [rows, H]
+ *   dst_of_route device int32 [T, k] (from moe_permute)
+ *   topk_w       device fp32 [T, k]
+ *   out          device bf16 [T, H] out
+ *
+ * Limits: H % 8 == 0, 1 <= k <= 32.  Errors: MOE_ERR_INVALID_ARG,
+ * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *dst_of_route,
+                                   const float *topk_w, int64_t T, int H, int k,
+                                   moe_bf16_t *out, moe_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,11 @@
+"""GB300-native (sm_103a) Mixture-of-Experts FFN hot path.
+
+Python binding over the C ABI of include/moe.h.  The library is loaded on
+first use; nothing here computes on the CPU.
+"""
+from ._binding import (  # noqa: F401
+    LIB_PATH, MoeError, Permutation, Workspace, load_library, moe_grouped_fc1_swiglu, moe_grouped_fc2,
+    moe_grouped_ffn_fwd, moe_permute,
+    moe_route_topk, moe_unpermute_combine, rows_capacity,
+)
+from .layer import MoeForward, moe_forward  # noqa: F401

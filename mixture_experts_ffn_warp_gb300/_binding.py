@@ -1,0 +1,259 @@
+"""ctypes binding of the C ABI declared in include/moe.h.
+
+Argument marshalling only: every step runs in the CUDA library
+(_build/libmoe_gb300.so).  There is no CPU fallback -- if the library is
+missing or CUDA is unavailable, calls raise.  torch supplies device memory
+and the current stream.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmoe_gb300.so")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
+          4: "MOE_ERR_DEVICE_DATA", 5: "MOE_ERR_WORKSPACE"}
+DEVERR_BAD_EXPERT_ID = 0x1
+DEVERR_TIMEOUT = 0x2
+DEVERR_CAPACITY = 0x4
+
+_vp = C.c_void_p
+_i64 = C.c_int64
+_int = C.c_int
+_sz = C.c_size_t
+_st = C.c_int
+
+# name -> (restype, argtypes); mirrors include/moe.h
+SIGNATURES = {
+    "moe_status_string": (C.c_char_p, [_int]),
+    "moe_abi_version": (_int, []),
+    "moe_workspace_bytes": (_sz, [_i64, _int, _int]),
+    "moe_workspace_init": (_st, [_vp, _sz, _vp]),
+    "moe_read_device_error": (_st, [_vp, _vp, C.POINTER(C.c_uint32)]),
+    "moe_route_topk": (_st, [_vp, _i64, _int, _int, _vp, _vp, _vp]),
+    "moe_permute": (_st, [_vp, _vp, _i64, _int, _int, _int, _int, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_grouped_ffn_fwd": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_grouped_fc1_swiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "moe_grouped_fc2": (_st, [_vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
+    "moe_unpermute_combine": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp]),
+}
+
+_lib = None
+
+
+class MoeError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def load_library(path: str | None = None):
+    """Load (once) the CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError(f"CUDA library not built: {p} (run __graft_entry__.build())")
+        L = C.CDLL(p)
+        for name, (res, args) in SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != MOE_OK:
+        raise MoeError(fn, status)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype: torch.dtype, shape: tuple | None = None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} shape must be {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+# ------------------------------------------------------------------ workspace
+
+class Workspace:
+    """Device workspace (error word + permutation scratch) for T, E, k."""
+
+    def __init__(self, T: int, E: int, k: int, device=None, stream=None):
+        L = load_library()
+        n = L.moe_workspace_bytes(T, E, k)
+        if n == 0:
+            raise ValueError(f"invalid sizes T={T} E={E} k={k}")
+        self.nbytes = int(n)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        _check("moe_workspace_init", L.moe_workspace_init(_ptr(self.buf), self.nbytes, _stream(stream)))
+
+    def reset(self, stream=None):
+        _check("moe_workspace_init", load_library().moe_workspace_init(_ptr(self.buf), self.nbytes, _stream(stream)))
+
+    def read_error(self, stream=None) -> int:
+        """Device error word (synchronises the stream)."""
+        v = C.c_uint32(0)
+        st = load_library().moe_read_device_error(_ptr(self.buf), _stream(stream), C.byref(v))
+        if st not in (MOE_OK, 4):
+            raise MoeError("moe_read_device_error", st)
+        return int(v.value)
+
+
+# ------------------------------------------------------------------ A1
+
+def moe_route_topk(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None, stream=None):
+    """Top-k routing with a softmax over the selected k logits (moe.h)."""
+    _need(logits, "logits", torch.float32)
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, E]")
+    T, E = logits.shape
+    if topk_idx is None:
+        topk_idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _need(topk_idx, "topk_idx", torch.int32, (T, k), logits.device)
+    _need(topk_w, "topk_w", torch.float32, (T, k), logits.device)
+    _check("moe_route_topk", load_library().moe_route_topk(
+        _ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
+    return topk_idx, topk_w
+
+
+# ------------------------------------------------------------------ A2
+
+@dataclass
+class Permutation:
+    x_perm: torch.Tensor        # [rows_cap, H]
+    dst_of_route: torch.Tensor  # [T, k] int32
+    src_of_row: torch.Tensor    # [rows_cap] int32
+    group_sizes: torch.Tensor   # [E] int32
+    group_offsets: torch.Tensor # [E+1] int32
+    rows_cap: int
+    align: int
+
+
+def rows_capacity(T: int, k: int, E: int, align: int = 1) -> int:
+    return T * k + E * (align - 1)
+
+
+def moe_permute(x: torch.Tensor, topk_idx: torch.Tensor, E: int, ws: Workspace, align: int = 1,
+                out: Permutation | None = None, stream=None) -> Permutation:
+    """Expert-contiguous permutation with device-side group sizes (moe.h)."""
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    _need(topk_idx, "topk_idx", torch.int32, None, x.device)
+    if topk_idx.dim() != 2 or topk_idx.shape[0] != T:
+        raise ValueError(f"topk_idx must be [{T}, k]")
+    k = topk_idx.shape[1]
+    cap = rows_capacity(T, k, E, align)
+    if out is None:
+        dev = x.device
+        out = Permutation(
+            x_perm=torch.empty(cap, H, dtype=torch.bfloat16, device=dev),
+            dst_of_route=torch.empty(T, k, dtype=torch.int32, device=dev),
+            src_of_row=torch.empty(cap, dtype=torch.int32, device=dev),
+            group_sizes=torch.empty(E, dtype=torch.int32, device=dev),
+            group_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
+            rows_cap=cap, align=align)
+    _check("moe_permute", load_library().moe_permute(
+        _ptr(x), _ptr(topk_idx), T, H, E, k, align, _ptr(out.x_perm), out.rows_cap,
+        _ptr(out.dst_of_route), _ptr(out.src_of_row), _ptr(out.group_sizes), _ptr(out.group_offsets),
+        _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ A3 + A4
+
+def moe_grouped_ffn_fwd(x_perm: torch.Tensor, W_gate: torch.Tensor, W_up: torch.Tensor,
+                        W_down: torch.Tensor, group_offsets: torch.Tensor, ws: Workspace,
+                        want_fc1_c: bool = False, h=None, y_perm=None, fc1_c=None, stream=None):
+    """Grouped SwiGLU expert FFN on tcgen05 (moe.h).  Returns (h, y_perm, fc1_c)."""
+    _need(x_perm, "x_perm", torch.bfloat16)
+    rows_cap, H = x_perm.shape
+    dev = x_perm.device
+    E, H2, F = W_gate.shape
+    if H2 != H:
+        raise ValueError(f"W_gate must be [E, {H}, F]")
+    _need(W_gate, "W_gate", torch.bfloat16, (E, H, F), dev)
+    _need(W_up, "W_up", torch.bfloat16, (E, H, F), dev)
+    _need(W_down, "W_down", torch.bfloat16, (E, F, H), dev)
+    _need(group_offsets, "group_offsets", torch.int32, (E + 1,), dev)
+    if h is None:
+        h = torch.empty(rows_cap, F, dtype=torch.bfloat16, device=dev)
+    if y_perm is None:
+        y_perm = torch.empty(rows_cap, H, dtype=torch.float32, device=dev)
+    if want_fc1_c and fc1_c is None:
+        fc1_c = torch.empty(rows_cap, 2 * F, dtype=torch.bfloat16, device=dev)
+    _need(h, "h", torch.bfloat16, (rows_cap, F), dev)
+    _need(y_perm, "y_perm", torch.float32, (rows_cap, H), dev)
+    if fc1_c is not None:
+        _need(fc1_c, "fc1_c", torch.bfloat16, (rows_cap, 2 * F), dev)
+    _check("moe_grouped_ffn_fwd", load_library().moe_grouped_ffn_fwd(
+        _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(group_offsets), E, H, F, rows_cap,
+        _ptr(h), _ptr(y_perm), _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    return h, y_perm, fc1_c
+
+
+def moe_grouped_fc1_swiglu(x_perm, W_gate, W_up, group_offsets, ws: Workspace, h, fc1_c=None, stream=None):
+    """A3 alone: h = silu(x W_gate) * (x W_up) per group (moe.h)."""
+    rows_cap, H = x_perm.shape
+    E, _, F = W_gate.shape
+    _check("moe_grouped_fc1_swiglu", load_library().moe_grouped_fc1_swiglu(
+        _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(group_offsets), E, H, F, rows_cap, _ptr(h),
+        _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    return h
+
+
+def moe_grouped_fc2(h, W_down, group_offsets, ws: Workspace, y_perm, stream=None):
+    """A4 alone: y_perm = h W_down per group (moe.h)."""
+    rows_cap, F = h.shape
+    E, _, H = W_down.shape
+    _check("moe_grouped_fc2", load_library().moe_grouped_fc2(
+        _ptr(h), _ptr(W_down), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
+        _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    return y_perm
+
+
+# ------------------------------------------------------------------ A5
+
+def moe_unpermute_combine(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w: torch.Tensor,
+                          out=None, stream=None) -> torch.Tensor:
+    """out[t] = sum_j w[t,j] * y_perm[dst[t,j]] in fp32, slot order (moe.h)."""
+    _need(y_perm, "y_perm", torch.float32)
+    H = y_perm.shape[1]
+    dev = y_perm.device
+    _need(dst_of_route, "dst_of_route", torch.int32, None, dev)
+    T, k = dst_of_route.shape
+    _need(topk_w, "topk_w", torch.float32, (T, k), dev)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (T, H), dev)
+    _check("moe_unpermute_combine", load_library().moe_unpermute_combine(
+        _ptr(y_perm), _ptr(dst_of_route), _ptr(topk_w), T, H, k, _ptr(out), _stream(stream)))
+    return out

@@ -1,0 +1,52 @@
+// abi.cu -- status strings, workspace management and the device error word.
+#include "common.cuh"
+
+namespace moe {
+
+int device_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 1;
+    return n > 0 ? n : 1;
+}
+
+}  // namespace moe
+
+extern "C" {
+
+const char *moe_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_DEVICE_DATA: return "MOE_ERR_DEVICE_DATA";
+        case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+int moe_abi_version(void) { return 1; }
+
+size_t moe_workspace_bytes(int64_t T, int E, int k) {
+    if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32) return 0;
+    int64_t chunks = moe::perm_chunks(T * (int64_t)k);
+    return moe::kWsHeaderBytes + (size_t)chunks * (size_t)E * sizeof(int32_t);
+}
+
+moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!ws || ws_bytes < moe::kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    return moe::cuda_status(cudaMemsetAsync(ws, 0, moe::kWsHeaderBytes, (cudaStream_t)stream));
+}
+
+moe_status_t moe_read_device_error(const void *ws, moe_stream_t stream, uint32_t *out) {
+    if (!ws || !out) return MOE_ERR_INVALID_ARG;
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, (cudaStream_t)stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    *out = v;
+    return v ? MOE_ERR_DEVICE_DATA : MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// combine.cu -- A5: weighted unpermute / combine back to token order.
+//
+// One warp per token; each lane owns 8-column slices of the row (two 16-byte
+// fp32 loads per slot, one 16-byte bf16 store) and accumulates
+// w_j * y_perm[dst_j] over the k slots in slot order in fp32.  All slot loads
+// of a slice are issued before the FMAs, and each lane keeps several slices
+// in flight.  ("Add MoE + expert-parallel Python API surface, PyTorch
+// reference, and tests", Summary: per-top-k combine.)
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kCombineWarps = 8;
+
+struct F8 {
+    float4 a, b;
+};
+
+__device__ __forceinline__ void fma8(float (&acc)[8], float w, const F8 &v) {
+    acc[0] = fmaf(w, v.a.x, acc[0]);
+    acc[1] = fmaf(w, v.a.y, acc[1]);
+    acc[2] = fmaf(w, v.a.z, acc[2]);
+    acc[3] = fmaf(w, v.a.w, acc[3]);
+    acc[4] = fmaf(w, v.b.x, acc[4]);
+    acc[5] = fmaf(w, v.b.y, acc[5]);
+    acc[6] = fmaf(w, v.b.z, acc[6]);
+    acc[7] = fmaf(w, v.b.w, acc[7]);
+}
+
+__device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
+    uint4 r;
+    __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&r);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    return r;
+}
+
+template <int KMAX>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+combine_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ dst_of_route,
+               const float *__restrict__ topk_w, int64_t T, int k, int slices,
+               uint4 *__restrict__ out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_dst = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+        my_dst = dst_of_route[t * k + lane];
+        my_w = topk_w[t * k + lane];
+    }
+    int dst[KMAX];
+    float w[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        dst[j] = __shfl_sync(0xFFFFFFFFu, my_dst, j);
+        w[j] = __shfl_sync(0xFFFFFFFFu, my_w, j);
+        if (j >= k) dst[j] = -1;
+    }
+    constexpr int U = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);   // slices in flight per lane
+    for (int s0 = lane; s0 < slices; s0 += 32 * U) {
+        F8 val[U][KMAX];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (dst[j] >= 0 && s0 + 32 * u < slices) {
+                    const float4 *src = y_perm + ((int64_t)dst[j] * slices + s0 + 32 * u) * 2;
+                    val[u][j].a = __ldg(src);
+                    val[u][j].b = __ldg(src + 1);
+                }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (s0 + 32 * u >= slices) break;
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (dst[j] >= 0) fma8(acc, w[j], val[u][j]);
+            out[t * slices + s0 + 32 * u] = pack8(acc);
+        }
+    }
+}
+
+template <int KMAX>
+cudaError_t launch(const float *y, const int32_t *dst, const float *w, int64_t T, int k, int slices,
+                   moe_bf16_t *out, cudaStream_t s) {
+    const int64_t blocks = (T + kCombineWarps - 1) / kCombineWarps;
+    combine_kernel<KMAX><<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(
+        reinterpret_cast<const float4 *>(y), dst, w, T, k, slices, reinterpret_cast<uint4 *>(out));
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *dst_of_route,
+                                              const float *topk_w, int64_t T, int H, int k,
+                                              moe_bf16_t *out, moe_stream_t stream) {
+    if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
+    if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!y_perm || !dst_of_route || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int sl = H / 8;
+    cudaError_t e;
+    if (k <= 1) e = moe::launch<1>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
+    else if (k <= 2) e = moe::launch<2>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
+    else if (k <= 4) e = moe::launch<4>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
+    else if (k <= 8) e = moe::launch<8>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
+    else if (k <= 16) e = moe::launch<16>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
+    else e = moe::launch<32>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
+    return moe::cuda_status(e);
+}

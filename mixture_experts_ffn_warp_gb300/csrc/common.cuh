@@ -1,0 +1,36 @@
+// common.cuh -- shared host/device helpers of the CUDA path (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Workspace layout: [0, 256) header (uint32 error word at offset 0), then the
+// permutation's per-chunk expert counts.
+constexpr size_t kWsHeaderBytes = 256;
+
+// Routes per chunk of the permutation's counting pass.
+constexpr int kPermWarps = 8;
+constexpr int kPermSteps = 32;
+constexpr int kPermChunk = kPermWarps * 32 * kPermSteps;   // 8192 routes
+
+inline int64_t perm_chunks(int64_t R) { return (R + kPermChunk - 1) / kPermChunk; }
+
+inline uint32_t *ws_error_word(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
+
+inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// Status of the last launch on this thread (clears the sticky-free error).
+inline moe_status_t launch_status() { return cuda_status(cudaGetLastError()); }
+
+int device_sm_count();
+
+__device__ __forceinline__ void raise_device_error(uint32_t *err, uint32_t bits) {
+    if (err) atomicOr(err, bits);
+}
+
+}  // namespace moe

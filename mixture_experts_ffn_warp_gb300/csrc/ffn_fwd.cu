@@ -1,0 +1,90 @@
+// ffn_fwd.cu -- A3 + A4: grouped gate/up GEMM with SwiGLU epilogue, then the
+// grouped down projection, both on tcgen05 with group sizes read on the device.
+#include "gemm_launch.cuh"
+
+using namespace moe;
+using gg::Op;
+
+namespace {
+
+moe_status_t check_common(int E, int H, int F, int64_t rows_cap, void *ws, size_t ws_bytes) {
+    if (E < 1 || H < 1 || F < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
+    if (E > gg::kMaxE || H % 128 != 0 || F % 128 != 0 || rows_cap >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int64_t mblock_bound(int64_t rows_cap, int E) { return (rows_cap + gg::BM - 1) / gg::BM + E; }
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                               const moe_bf16_t *W_up, const int32_t *group_offsets,
+                                               int E, int H, int F, int64_t rows_cap, moe_bf16_t *h,
+                                               moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                               moe_stream_t stream) {
+    moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
+    if (st != MOE_OK || rows_cap == 0) return st;
+    if (!x_perm || !W_gate || !W_up || !group_offsets || !h) return MOE_ERR_INVALID_ARG;
+    // [rows, H] x [H, F] (gate | up) -> h [rows, F]; 128 gate + 128 up columns per tile
+    CUtensorMap tA, tB0, tB1;
+    if (!tmap_bf16_2d(&tA, x_perm, H, rows_cap, H, 64, 128) ||
+        !tmap_bf16_3d(&tB0, W_gate, F, H, E, 64, 64) || !tmap_bf16_3d(&tB1, W_up, F, H, E, 64, 64))
+        return MOE_ERR_UNSUPPORTED;
+    gg::Args a{};
+    a.group_offsets = group_offsets;
+    a.E = E;
+    a.N = F;
+    a.K = H;
+    a.n_tiles = F / 128;
+    a.rows_cap = rows_cap;
+    a.out0 = reinterpret_cast<__nv_bfloat16 *>(h);
+    a.ld0 = F;
+    a.out1 = reinterpret_cast<__nv_bfloat16 *>(fc1_c);
+    a.ld1 = 2 * (int64_t)F;
+    a.err = ws_error_word(ws);
+    return gg::launch<Op::FC1_SWIGLU, 256>(tA, tB0, tB1, a, mblock_bound(rows_cap, E) * a.n_tiles,
+                                           (cudaStream_t)stream);
+}
+
+extern "C" moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_down,
+                                        const int32_t *group_offsets, int E, int H, int F,
+                                        int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
+                                        moe_stream_t stream) {
+    moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
+    if (st != MOE_OK || rows_cap == 0) return st;
+    if (!h || !W_down || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
+    // h [rows, F] x W_down [F, H] -> y_perm [rows, H]
+    const int bn = (H % 256 == 0) ? 256 : 128;
+    CUtensorMap tA, tB;
+    if (!tmap_bf16_2d(&tA, h, F, rows_cap, F, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, 64))
+        return MOE_ERR_UNSUPPORTED;
+    gg::Args b{};
+    b.group_offsets = group_offsets;
+    b.E = E;
+    b.N = H;
+    b.K = F;
+    b.n_tiles = H / bn;
+    b.rows_cap = rows_cap;
+    b.out_f32 = y_perm;
+    b.ld0 = H;
+    b.err = ws_error_word(ws);
+    const int64_t bound = mblock_bound(rows_cap, E) * b.n_tiles;
+    if (bn == 256) return gg::launch<Op::FC2, 256>(tA, tB, tB, b, bound, (cudaStream_t)stream);
+    return gg::launch<Op::FC2, 128>(tA, tB, tB, b, bound, (cudaStream_t)stream);
+}
+
+extern "C" moe_status_t moe_grouped_ffn_fwd(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                            const moe_bf16_t *W_up, const moe_bf16_t *W_down,
+                                            const int32_t *group_offsets, int E, int H, int F,
+                                            int64_t rows_cap, moe_bf16_t *h, float *y_perm,
+                                            moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                            moe_stream_t stream) {
+    moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
+    if (st != MOE_OK || rows_cap == 0) return st;
+    if (!x_perm || !W_gate || !W_up || !W_down || !group_offsets || !h || !y_perm) return MOE_ERR_INVALID_ARG;
+    st = moe_grouped_fc1_swiglu(x_perm, W_gate, W_up, group_offsets, E, H, F, rows_cap, h, fc1_c, ws,
+                                ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    return moe_grouped_fc2(h, W_down, group_offsets, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
+}

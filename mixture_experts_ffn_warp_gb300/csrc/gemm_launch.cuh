@@ -1,0 +1,31 @@
+// gemm_launch.cuh -- host launch of one grouped GEMM op (persistent grid, one CTA per SM).
+#pragma once
+
+#include "grouped_gemm.cuh"
+#include "tmap.cuh"
+
+namespace moe {
+namespace gg {
+
+template <Op OP, int BN>
+moe_status_t launch(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorMap &b1, const Args &args,
+                    int64_t tiles_bound, cudaStream_t s) {
+    using C = Cfg<OP, BN>;
+    if (tiles_bound <= 0) return MOE_OK;
+    auto kern = grouped_gemm_kernel<OP, BN>;
+    static int configured_dev = -1;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (configured_dev != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        configured_dev = dev;
+    }
+    const int64_t sms = device_sm_count();
+    const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
+    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(a, b0, b1, args);
+    return launch_status();
+}
+
+}  // namespace gg
+}  // namespace moe

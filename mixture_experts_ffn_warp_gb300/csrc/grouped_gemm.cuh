@@ -1,0 +1,529 @@
+// grouped_gemm.cuh -- persistent, warp-specialised grouped GEMM on tcgen05 for the
+// expert FFN (forward and backward).
+//
+// One CTA per SM, 6 warps:
+//   warp 0      TMA producer (one lane): A and B tiles -> a ring of smem stages
+//   warp 1      MMA issuer (lane 0 issues tcgen05.mma, M=128 x N=BN x K=16);
+//               fp32 accumulators live in TMEM, double-buffered
+//   warps 2..5  epilogue: tcgen05.ld -> fused activation -> bf16 stores
+// Tiles are scheduled on the device from group_offsets (no host round trip).
+//
+// Ops (A row = one permuted route unless stated):
+//   FC1_SWIGLU     h = silu(x W_gate) * (x W_up)        M-grouped, K = H
+//   FC2            y = h W_down                         M-grouped, K = F
+//   DGRAD_DSWIGLU  dh = dy W_down^T, then dSwiGLU       M-grouped, K = H
+//   DGRAD_FC1      dx = dg W_gate^T + du W_up^T          M-grouped, K = 2F
+//   WGRAD_DOWN     dW_down[e] = h_e^T dy_e              K-grouped (K = rows of e)
+//   WGRAD_GATEUP   [dW_gate|dW_up][e] = x_e^T [dg|du]_e K-grouped
+// ("Add MoE + expert-parallel Python API surface, PyTorch reference, and
+// tests", Summary: SwiGLU experts, fc1_c stash, backward; "[Draft][JAX] MoE
+// block optimization": fused grouped GEMM + SwiGLU and grouped_gemm_dswiglu;
+// "[JAX] Expert Parallelism": zero wgrad for experts with no tokens.)
+#pragma once
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace moe {
+namespace gg {
+
+enum class Op : int { FC1_SWIGLU, FC2, DGRAD_DSWIGLU, DGRAD_FC1, WGRAD_DOWN, WGRAD_GATEUP };
+
+constexpr int BM = 128;
+constexpr int BK = 64;             // bf16 K elements per stage (one 128-byte swizzle row)
+constexpr int UMMA_K = 16;
+constexpr int kThreads = 192;
+constexpr int kMaxE = 1024;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+template <Op OP>
+struct Traits {
+    static constexpr bool k_grouped = (OP == Op::WGRAD_DOWN || OP == Op::WGRAD_GATEUP);
+    static constexpr bool a_mn = k_grouped;                       // A is MN-major only for wgrad
+    static constexpr bool b_mn = (OP == Op::FC1_SWIGLU || OP == Op::FC2 || k_grouped);
+    static constexpr bool b_two = (OP == Op::FC1_SWIGLU || OP == Op::DGRAD_FC1);
+};
+
+struct Args {
+    const int32_t *group_offsets;   // [E+1]
+    int E;
+    int M;            // K-grouped: rows of each expert's output matrix
+    int N;            // output columns (FC1: F; FC2: H; DSWIGLU: F; DGRAD_FC1: H; WGRAD: N)
+    int K;            // M-grouped contraction length
+    int n_tiles;      // tiles along N
+    int m_tiles;      // K-grouped: tiles along M
+    int k_split;      // DGRAD_FC1: K index where B switches from W_gate to W_up (= F)
+    int n_split;      // WGRAD_GATEUP: column where output switches from out0 to out1 (= F)
+    int64_t rows_cap; // rows of the permuted tensors
+    __nv_bfloat16 *out0;
+    float *out_f32;        // FC2: the fp32 expert output y_perm (row pitch ld0)
+    int64_t ld0;
+    __nv_bfloat16 *out1;   // FC1: fc1_c stash (nullable); WGRAD_GATEUP: dW_up
+    int64_t ld1;
+    const __nv_bfloat16 *aux;   // DSWIGLU: fc1_c
+    int64_t ld_aux;
+    int64_t expert_stride;      // K-grouped: elements between experts' outputs
+    uint32_t *err;
+};
+
+template <Op OP, int BN>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;   // + alignment slack
+    // output columns produced per tile
+    static constexpr int OUT_COLS = (OP == Op::FC1_SWIGLU) ? BN / 2 : BN;
+};
+
+__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+
+__device__ __forceinline__ void store_bf16x32(__nv_bfloat16 *dst, const float (&v)[32]) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 pk;
+        __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(v[8 * q + 2 * i], v[8 * q + 2 * i + 1]);
+        d[q] = pk;
+    }
+}
+
+__device__ __forceinline__ void load_bf16x32(const __nv_bfloat16 *src, float (&v)[32]) {
+    const uint4 *s = reinterpret_cast<const uint4 *>(src);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint4 pk = __ldg(s + q);
+        const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&pk);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float2 f = __bfloat1622float2(p[i]);
+            v[8 * q + 2 * i] = f.x;
+            v[8 * q + 2 * i + 1] = f.y;
+        }
+    }
+}
+
+struct Tile {
+    int e;
+    int m0;      // M-grouped: first row in the permuted tensor; K-grouped: row in the expert's output
+    int m_end;   // M-grouped: end of the group's rows
+    int n0;      // first output column
+    int kb;      // number of K blocks
+    int k_row0;  // K-grouped: first permuted row of the group
+    int k_rows;  // K-grouped: rows of the group
+};
+
+template <Op OP, int BN>
+__device__ __forceinline__ Tile decode_tile(int t, const Args &a, const int *s_off, const int *s_start) {
+    using TR = Traits<OP>;
+    Tile tl;
+    if constexpr (TR::k_grouped) {
+        const int per = a.m_tiles * a.n_tiles;
+        tl.e = t / per;
+        const int local = t - tl.e * per;
+        const int mb = local % a.m_tiles, nb = local / a.m_tiles;
+        tl.m0 = mb * BM;
+        tl.m_end = a.M;
+        tl.n0 = nb * BN;
+        const int r0 = s_off[tl.e], r1 = s_off[tl.e + 1];
+        tl.k_row0 = r0;
+        tl.k_rows = r1 > r0 ? r1 - r0 : 0;
+        tl.kb = (tl.k_rows + BK - 1) / BK;
+    } else {
+        // largest e with s_start[e] <= t
+        int lo = 0, hi = a.E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_start[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        tl.e = lo;
+        const int rows = s_off[lo + 1] - s_off[lo];
+        const int nmb = (rows + BM - 1) / BM;
+        const int local = t - s_start[lo];
+        const int mb = local % nmb, nb = local / nmb;
+        tl.m0 = s_off[lo] + mb * BM;
+        tl.m_end = s_off[lo + 1];
+        tl.n0 = nb * Cfg<OP, BN>::OUT_COLS;
+        tl.kb = (a.K + BK - 1) / BK;
+        tl.k_row0 = 0;
+        tl.k_rows = 0;
+    }
+    return tl;
+}
+
+template <Op OP, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                    const __grid_constant__ CUtensorMap tmB1, const Args args) {
+    using TR = Traits<OP>;
+    using C = Cfg<OP, BN>;
+    constexpr int S = C::STAGES;
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[S], empty_bar[S], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_off[kMaxE + 1];
+    __shared__ int s_start[kMaxE + 1];
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t smem_base = sm100::smem_u32(smem);
+
+    // ---------------------------------------------------------------- setup
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            sm100::mbar_init(&full_bar[s], 1);
+            sm100::mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            sm100::mbar_init(&tfull_bar[b], 1);
+            sm100::mbar_init(&tempty_bar[b], 4 * 32);
+        }
+        sm100::mbar_init(&drain_bar, 1);
+        s_abort = 0;
+        sm100::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        sm100::prefetch_tmap(&tmA);
+        sm100::prefetch_tmap(&tmB0);
+        if constexpr (TR::b_two) sm100::prefetch_tmap(&tmB1);
+    }
+    if (warp == 1) {
+        sm100::tmem_alloc(&s_tmem_base, C::TMEM_COLS);
+        sm100::tmem_relinquish();
+    }
+    const int E = args.E;
+    for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = args.group_offsets[i];
+    __syncthreads();
+    if (warp == 2) {
+        // s_start[e] = tiles before expert e (M-grouped: m-blocks x n_tiles)
+        const int seg = (E + 31) / 32;
+        const int e0 = lane * seg;
+        int sum = 0;
+        for (int i = 0; i < seg; ++i) {
+            const int e = e0 + i;
+            if (e < E) {
+                int tiles;
+                if constexpr (TR::k_grouped) {
+                    tiles = args.m_tiles * args.n_tiles;
+                } else {
+                    int rows = s_off[e + 1] - s_off[e];
+                    if (rows < 0) rows = 0;
+                    tiles = ((rows + BM - 1) / BM) * args.n_tiles;
+                }
+                sum += tiles;
+            }
+        }
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - sum;
+        for (int i = 0; i < seg; ++i) {
+            const int e = e0 + i;
+            if (e < E) {
+                s_start[e] = run;
+                int tiles;
+                if constexpr (TR::k_grouped) {
+                    tiles = args.m_tiles * args.n_tiles;
+                } else {
+                    int rows = s_off[e + 1] - s_off[e];
+                    if (rows < 0) rows = 0;
+                    tiles = ((rows + BM - 1) / BM) * args.n_tiles;
+                }
+                run += tiles;
+            }
+        }
+        if (lane == 31) s_start[E] = incl;
+    }
+    sm100::tc_fence_before();
+    __syncthreads();
+    sm100::tc_fence_after();
+    const uint32_t tmem_base = s_tmem_base;
+    const int total_tiles = s_start[E];
+    volatile int *abort = &s_abort;
+
+    if (warp == 0) {
+        // ============================================================ producer
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+                const Tile tl = decode_tile<OP, BN>(t, args, s_off, s_start);
+                for (int kb = 0; kb < tl.kb; ++kb) {
+                    if (!sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                    const uint32_t sb = sa + C::A_BYTES;
+                    uint64_t *fb = &full_bar[stage];
+                    sm100::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                    const int k0 = kb * BK;
+                    if constexpr (TR::k_grouped) {
+                        const int krow = tl.k_row0 + k0;
+                        sm100::tma_load_2d(sa, &tmA, fb, tl.m0, krow);
+                        sm100::tma_load_2d(sa + 8192, &tmA, fb, tl.m0 + 64, krow);
+#pragma unroll
+                        for (int i = 0; i < BN / 64; ++i) sm100::tma_load_2d(sb + i * 8192, &tmB0, fb, tl.n0 + 64 * i, krow);
+                    } else {
+                        sm100::tma_load_2d(sa, &tmA, fb, k0, tl.m0);
+                        if constexpr (OP == Op::FC1_SWIGLU) {
+                            // gate columns [n0, n0+BN/2) then up columns, each as 64-wide MN chunks
+#pragma unroll
+                            for (int i = 0; i < BN / 128; ++i) {
+                                sm100::tma_load_3d(sb + i * 8192, &tmB0, fb, tl.n0 + 64 * i, k0, tl.e);
+                                sm100::tma_load_3d(sb + (BN / 128 + i) * 8192, &tmB1, fb, tl.n0 + 64 * i, k0, tl.e);
+                            }
+                        } else if constexpr (OP == Op::FC2) {
+#pragma unroll
+                            for (int i = 0; i < BN / 64; ++i) sm100::tma_load_3d(sb + i * 8192, &tmB0, fb, tl.n0 + 64 * i, k0, tl.e);
+                        } else if constexpr (OP == Op::DGRAD_DSWIGLU) {
+                            sm100::tma_load_3d(sb, &tmB0, fb, k0, tl.n0, tl.e);
+                        } else {   // DGRAD_FC1: K in [0, F) from W_gate, [F, 2F) from W_up
+                            if (k0 < args.k_split) sm100::tma_load_3d(sb, &tmB0, fb, k0, tl.n0, tl.e);
+                            else sm100::tma_load_3d(sb, &tmB1, fb, k0 - args.k_split, tl.n0, tl.e);
+                        }
+                    }
+                    ++issued;
+                    if (++stage == S) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // let the copies already issued land before the CTA exits
+                int st = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < S && i < issued; ++i) {
+                    if (--st < 0) { st = S - 1; ph ^= 1u; }
+                    int dummy = 0;
+                    sm100::mbar_wait(&full_bar[st], ph, &dummy, nullptr, 10000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer
+        constexpr uint32_t IDESC = sm100::idesc_bf16(BM, BN, TR::a_mn, TR::b_mn);
+        int stage = 0;
+        uint32_t phase = 0;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        bool ok = true;
+        bool issued_any = false;
+        for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
+            const Tile tl = decode_tile<OP, BN>(t, args, s_off, s_start);
+            if (tl.kb == 0) continue;   // empty K range: the epilogue writes zeros
+            const bool got_acc = sm100::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, kWaitLimitNs);
+            if (__any_sync(0xFFFFFFFFu, !got_acc)) { ok = false; break; }
+            sm100::tc_fence_after();
+            const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < tl.kb; ++kb) {
+                const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, kWaitLimitNs);
+                if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
+                const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
+                const uint32_t sb = sa + C::A_BYTES;
+                if constexpr (TR::k_grouped) {
+                    // zero the K rows past the group's end (they belong to the next group)
+                    const int valid = tl.k_rows - kb * BK;
+                    if (valid < BK) {
+                        uint8_t *pa = smem + stage * C::STAGE_BYTES;
+                        const int nbox = 2 + BN / 64;
+                        const int zrows = BK - valid;
+                        for (int i = lane; i < nbox * zrows * 8; i += 32) {
+                            const int box = i / (zrows * 8);
+                            const int rem = i - box * zrows * 8;
+                            const int row = valid + rem / 8, c16 = rem % 8;
+                            *reinterpret_cast<uint4 *>(pa + box * 8192 + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        sm100::fence_proxy_async_smem();
+                        __syncwarp();
+                    }
+                }
+                sm100::tc_fence_after();
+                if (lane == 0) {
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        uint64_t ad, bd;
+                        if constexpr (TR::a_mn) ad = sm100::sdesc_sw128(sa + kk * 2048, 8192, 1024);
+                        else ad = sm100::sdesc_sw128(sa + kk * 32, 16, 1024);
+                        if constexpr (TR::b_mn) bd = sm100::sdesc_sw128(sb + kk * 2048, 8192, 1024);
+                        else bd = sm100::sdesc_sw128(sb + kk * 32, 16, 1024);
+                        sm100::mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    sm100::mma_commit(&empty_bar[stage]);
+                    issued_any = true;
+                }
+                __syncwarp();
+                if (++stage == S) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (lane == 0) sm100::mma_commit(&tfull_bar[acc]);
+            __syncwarp();
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        if (!ok && issued_any && lane == 0) {
+            // drain: wait for the MMAs already issued before TMEM is released
+            sm100::mma_commit(&drain_bar);
+            int dummy = 0;
+            sm100::mbar_wait(&drain_bar, 0, &dummy, nullptr, 10000000ull);
+        }
+        __syncwarp();
+    } else {
+        // ============================================================ epilogue
+        const int q = warp & 3;            // TMEM lane quarter this warp may access
+        const int r = q * 32 + lane;       // accumulator row of this thread
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
+            const Tile tl = decode_tile<OP, BN>(t, args, s_off, s_start);
+            if constexpr (TR::k_grouped) {
+                const int row = tl.m0 + r;
+                const size_t eoff = (size_t)tl.e * (size_t)args.expert_stride;
+                if (tl.kb == 0) {
+                    // expert with no routes: its weight gradient is exactly zero
+                    float z[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) z[i] = 0.0f;
+                    for (int c = 0; c < BN; c += 32) {
+                        const int n = tl.n0 + c;
+                        if (n >= args.N) break;
+                        if (OP == Op::WGRAD_GATEUP && n >= args.n_split)
+                            store_bf16x32(args.out1 + eoff + (size_t)row * args.ld1 + (n - args.n_split), z);
+                        else
+                            store_bf16x32(args.out0 + eoff + (size_t)row * args.ld0 + n, z);
+                    }
+                    continue;
+                }
+            }
+            const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, kWaitLimitNs);
+            if (__any_sync(0xFFFFFFFFu, !got)) break;
+            sm100::tc_fence_after();
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+
+            if constexpr (OP == Op::FC1_SWIGLU) {
+                const int64_t row = tl.m0 + r;
+                const bool valid = row < tl.m_end && row < args.rows_cap;
+#pragma unroll 1
+                for (int c = 0; c < BN / 2; c += 32) {
+                    uint32_t g[32], u[32];
+                    sm100::tmem_ld32(tacc + c, g);
+                    sm100::tmem_ld32(tacc + BN / 2 + c, u);
+                    sm100::tmem_ld_wait();
+                    const int n = tl.n0 + c;
+                    if (valid && n < args.N) {
+                        float hv[32], gv[32], uv[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            gv[i] = __uint_as_float(g[i]);
+                            uv[i] = __uint_as_float(u[i]);
+                            hv[i] = silu_f(gv[i]) * uv[i];
+                        }
+                        store_bf16x32(args.out0 + row * args.ld0 + n, hv);
+                        if (args.out1) {
+                            store_bf16x32(args.out1 + row * args.ld1 + n, gv);
+                            store_bf16x32(args.out1 + row * args.ld1 + args.N + n, uv);
+                        }
+                    }
+                }
+            } else if constexpr (OP == Op::DGRAD_DSWIGLU) {
+                const int64_t row = tl.m0 + r;
+                const bool valid = row < tl.m_end && row < args.rows_cap;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t d[32];
+                    sm100::tmem_ld32(tacc + c, d);
+                    sm100::tmem_ld_wait();
+                    const int n = tl.n0 + c;
+                    if (valid && n < args.N) {
+                        float gv[32], uv[32], dg[32], du[32];
+                        load_bf16x32(args.aux + row * args.ld_aux + n, gv);
+                        load_bf16x32(args.aux + row * args.ld_aux + args.N + n, uv);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float dh = __uint_as_float(d[i]);
+                            const float s = 1.0f / (1.0f + __expf(-gv[i]));
+                            dg[i] = dh * uv[i] * s * (1.0f + gv[i] * (1.0f - s));
+                            du[i] = dh * gv[i] * s;
+                        }
+                        store_bf16x32(args.out0 + row * args.ld0 + n, dg);
+                        store_bf16x32(args.out0 + row * args.ld0 + args.N + n, du);
+                    }
+                }
+            } else if constexpr (TR::k_grouped) {
+                const int row = tl.m0 + r;
+                const size_t eoff = (size_t)tl.e * (size_t)args.expert_stride;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t d[32];
+                    sm100::tmem_ld32(tacc + c, d);
+                    sm100::tmem_ld_wait();
+                    const int n = tl.n0 + c;
+                    if (n < args.N) {
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(d[i]);
+                        if (OP == Op::WGRAD_GATEUP && n >= args.n_split)
+                            store_bf16x32(args.out1 + eoff + (size_t)row * args.ld1 + (n - args.n_split), v);
+                        else
+                            store_bf16x32(args.out0 + eoff + (size_t)row * args.ld0 + n, v);
+                    }
+                }
+            } else if constexpr (OP == Op::FC2) {   // fp32 store of the expert output
+                const int64_t row = tl.m0 + r;
+                const bool valid = row < tl.m_end && row < args.rows_cap;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t d[32];
+                    sm100::tmem_ld32(tacc + c, d);
+                    sm100::tmem_ld_wait();
+                    const int n = tl.n0 + c;
+                    if (valid && n < args.N) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(args.out_f32 + row * args.ld0 + n);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            dst[q] = make_uint4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+                    }
+                }
+            } else {   // DGRAD_FC1: plain bf16 store
+                const int64_t row = tl.m0 + r;
+                const bool valid = row < tl.m_end && row < args.rows_cap;
+#pragma unroll 1
+                for (int c = 0; c < BN; c += 32) {
+                    uint32_t d[32];
+                    sm100::tmem_ld32(tacc + c, d);
+                    sm100::tmem_ld_wait();
+                    const int n = tl.n0 + c;
+                    if (valid && n < args.N) {
+                        float v[32];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(d[i]);
+                        store_bf16x32(args.out0 + row * args.ld0 + n, v);
+                    }
+                }
+            }
+            sm100::tc_fence_before();
+            sm100::mbar_arrive(&tempty_bar[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    // ---------------------------------------------------------------- teardown
+    sm100::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        sm100::tc_fence_after();
+        sm100::tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+}  // namespace gg
+}  // namespace moe

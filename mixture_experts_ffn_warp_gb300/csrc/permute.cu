@@ -1,0 +1,235 @@
+// permute.cu -- A2: sync-free permutation of tokens into expert-contiguous rows.
+//
+// Three launches on one stream, no host round trip:
+//   1. count:   each 8192-route chunk counts its routes per expert and gives
+//               every route its stable rank among the chunk's routes to the
+//               same expert (warp match + per-warp running counts);
+//   2. scan:    one block turns the chunk counts into group sizes, (aligned)
+//               group offsets and each chunk's first row per expert;
+//   3. scatter: one warp per token writes dst_of_route / src_of_row and
+//               copies the token's row once from HBM into its k destinations
+//               with 16-byte loads and stores.
+// (One-GPU counterpart of the expert-major dispatch layout with device-side
+// group sizes: "[JAX] Expert Parallelism: JAX primitives + VJPs", commit log;
+// "MoE training optimization": problem sizes supplied from device buffers.)
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kScanThreads = 1024;
+constexpr int kScatterWarps = 8;
+
+__global__ void __launch_bounds__(kPermWarps * 32)
+permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E,
+                     int32_t *__restrict__ local_rank, int32_t *__restrict__ chunk_counts,
+                     uint32_t *err) {
+    extern __shared__ int32_t s_cnt[];   // [kPermWarps][E] running counts
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) s_cnt[i] = 0;
+    __syncthreads();
+
+    const int64_t chunk0 = (int64_t)blockIdx.x * kPermChunk;
+    const int64_t w0 = chunk0 + (int64_t)warp * 32 * kPermSteps;
+    int32_t *cnt = s_cnt + warp * E;
+    const unsigned lt_mask = (1u << lane) - 1u;
+    for (int step = 0; step < kPermSteps; ++step) {
+        const int64_t r = w0 + step * 32 + lane;
+        int e = -1;
+        if (r < R) {
+            e = topk_idx[r];
+            if (e < -1 || e >= E) {
+                raise_device_error(err, MOE_DEVERR_BAD_EXPERT_ID);
+                e = -1;
+            }
+        }
+        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+        int rank = -1;
+        if (e >= 0) rank = cnt[e] + __popc(peers & lt_mask);
+        __syncwarp();
+        if (e >= 0 && (peers & lt_mask) == 0) cnt[e] += __popc(peers);   // leader of the peer group
+        __syncwarp();
+        if (r < R) local_rank[r] = rank;
+    }
+    __syncthreads();
+    // exclusive scan over warps per expert -> rank offset of each warp; chunk totals
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        int run = 0;
+        for (int w = 0; w < kPermWarps; ++w) {
+            int c = s_cnt[w * E + e];
+            s_cnt[w * E + e] = run;
+            run += c;
+        }
+        chunk_counts[(int64_t)blockIdx.x * E + e] = run;
+    }
+    __syncthreads();
+    // add the warp offsets to this chunk's ranks
+    for (int step = 0; step < kPermSteps; ++step) {
+        const int64_t r = w0 + step * 32 + lane;
+        if (r < R) {
+            int rank = local_rank[r];
+            if (rank >= 0) {
+                int e = topk_idx[r];
+                local_rank[r] = rank + s_cnt[warp * E + e];
+            }
+        }
+    }
+}
+
+// Group sizes, aligned offsets, and per-chunk first rows (in place of the counts).
+__global__ void __launch_bounds__(kScanThreads)
+permute_scan_kernel(int32_t *__restrict__ chunk_counts, int64_t chunks, int E, int align,
+                    int32_t *__restrict__ group_sizes, int32_t *__restrict__ group_offsets) {
+    __shared__ int32_t s_warp[kScanThreads / 32];
+    const int e = threadIdx.x;
+    int total = 0;
+    if (e < E) {
+#pragma unroll 8
+        for (int64_t c = 0; c < chunks; ++c) total += chunk_counts[c * E + e];
+    }
+    const int padded = e < E ? (total + align - 1) / align * align : 0;
+    // block exclusive scan of padded sizes
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int incl = padded;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) s_warp[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int v = s_warp[lane];
+        int vi = v;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int o = __shfl_up_sync(0xFFFFFFFFu, vi, off);
+            if (lane >= off) vi += o;
+        }
+        s_warp[lane] = vi - v;
+    }
+    __syncthreads();
+    const int excl = incl - padded + s_warp[warp];
+    if (e < E) {
+        group_sizes[e] = total;
+        group_offsets[e] = excl;
+        if (e == E - 1) group_offsets[E] = excl + padded;
+        int run = excl;
+        for (int64_t c = 0; c < chunks; ++c) {
+            int v = chunk_counts[c * E + e];
+            chunk_counts[c * E + e] = run;
+            run += v;
+        }
+    }
+}
+
+// One warp per token: maps, then the row copied once into its k rows.
+__global__ void __launch_bounds__(kScatterWarps * 32)
+permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
+                       int64_t T, int k, int E, int row_vecs,
+                       const int32_t *__restrict__ chunk_first, int32_t *__restrict__ dst_of_route,
+                       int32_t *__restrict__ src_of_row, uint4 *__restrict__ x_perm,
+                       int64_t rows_cap, uint32_t *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_dst = -1;
+    if (lane < k) {
+        const int64_t r = t * k + lane;
+        const int rank = dst_of_route[r];     // local rank written by the count pass
+        if (rank >= 0) {
+            const int e = topk_idx[r];
+            const int64_t row = (int64_t)chunk_first[(r / kPermChunk) * E + e] + rank;
+            if (row < rows_cap) {
+                my_dst = (int)row;
+                src_of_row[row] = (int32_t)r;
+            } else {
+                raise_device_error(err, MOE_DEVERR_CAPACITY);
+            }
+        }
+        dst_of_route[r] = my_dst;
+    }
+    int dst[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) dst[j] = j < k ? __shfl_sync(0xFFFFFFFFu, my_dst, j) : -1;
+    const uint4 *src = x + t * row_vecs;
+    constexpr int U = 4;   // 16-byte vectors in flight per lane
+    for (int v0 = lane; v0 < row_vecs; v0 += 32 * U) {
+        uint4 val[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (v0 + 32 * u < row_vecs) val[u] = __ldg(src + v0 + 32 * u);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < k && dst[j] >= 0) {
+                uint4 *d = x_perm + (int64_t)dst[j] * row_vecs;
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (v0 + 32 * u < row_vecs) d[v0 + 32 * u] = val[u];
+            }
+        }
+    }
+}
+
+// Padding rows of aligned groups: src_of_row = -1 and zero data.
+__global__ void permute_pad_kernel(const int32_t *__restrict__ group_sizes,
+                                   const int32_t *__restrict__ group_offsets, int E, int row_vecs,
+                                   int32_t *__restrict__ src_of_row, uint4 *__restrict__ x_perm,
+                                   int64_t rows_cap) {
+    const int e = blockIdx.x;
+    const int64_t first = (int64_t)group_offsets[e] + group_sizes[e];
+    const int64_t last = group_offsets[e + 1] < rows_cap ? group_offsets[e + 1] : rows_cap;
+    for (int64_t row = first; row < last; ++row) {
+        if (threadIdx.x == 0) src_of_row[row] = -1;
+        for (int v = threadIdx.x; v < row_vecs; v += blockDim.x)
+            x_perm[row * row_vecs + v] = make_uint4(0, 0, 0, 0);
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx, int64_t T, int H,
+                                    int E, int k, int align, moe_bf16_t *x_perm, int64_t rows_cap,
+                                    int32_t *dst_of_route, int32_t *src_of_row,
+                                    int32_t *group_sizes, int32_t *group_offsets, void *ws,
+                                    size_t ws_bytes, moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || H < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || E > 1024 || k < 1 || k > 32 || align < 1 || align > 1024 || H % 8 != 0)
+        return MOE_ERR_UNSUPPORTED;
+    if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
+    const int64_t R = T * (int64_t)k;
+    if (rows_cap < R + (int64_t)E * (align - 1)) return MOE_ERR_INVALID_ARG;
+    if (rows_cap >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !topk_idx || !x_perm || !dst_of_route || !src_of_row))
+        return MOE_ERR_INVALID_ARG;
+    const size_t need = moe_workspace_bytes(T, E, k);
+    if (!ws || ws_bytes < need || need == 0) return MOE_ERR_WORKSPACE;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t *err = ws_error_word(ws);
+    int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsHeaderBytes);
+    const int64_t chunks = perm_chunks(R);
+    if (chunks > 0) {
+        permute_count_kernel<<<(unsigned)chunks, kPermWarps * 32, kPermWarps * E * sizeof(int32_t), s>>>(
+            topk_idx, R, E, dst_of_route, counts, err);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    permute_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, chunks, E, align, group_sizes, group_offsets);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    const int row_vecs = H / 8;
+    if (T > 0) {
+        const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
+        permute_scatter_kernel<<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(
+            reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts, dst_of_route,
+            src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, err);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    if (align > 1) {
+        permute_pad_kernel<<<E, 256, 0, s>>>(group_sizes, group_offsets, E, row_vecs, src_of_row,
+                                             reinterpret_cast<uint4 *>(x_perm), rows_cap);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}

@@ -1,0 +1,65 @@
+// tmap.cuh -- host-side TMA tensor-map encoding (driver entry point fetched at run time).
+#pragma once
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace moe {
+
+inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// Tiled map over a row-major tensor of `dtype` elements of `elem_bytes`
+// bytes: dims[0] is the contiguous dimension; strides_bytes[i] is the byte
+// stride of dims[i+1].  128-byte swizzle, zero fill out of bounds.
+inline bool encode_tmap(CUtensorMap *m, CUtensorMapDataType dtype, int rank, const void *base,
+                        const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
+                        CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+    auto fn = tmap_encoder();
+    if (!fn) return false;
+    if (reinterpret_cast<uintptr_t>(base) % 16 != 0) return false;
+    cuuint64_t d[5], st[4];
+    cuuint32_t b[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        b[i] = box[i];
+        es[i] = 1;
+    }
+    for (int i = 0; i + 1 < rank; ++i) st[i] = strides_bytes[i];
+    CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void *>(base), d, st, b, es,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+// 2-D bf16 matrix [outer, inner] with row pitch `ld` elements.
+inline bool tmap_bf16_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
+                         uint32_t box_inner, uint32_t box_outer) {
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {ld * 2};
+    const uint32_t box[2] = {box_inner, box_outer};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box);
+}
+
+// 3-D bf16 tensor [d2, d1, d0] (d0 contiguous), densely packed.
+inline bool tmap_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2,
+                         uint32_t box0, uint32_t box1) {
+    const uint64_t dims[3] = {d0, d1, d2};
+    const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+    const uint32_t box[3] = {box0, box1, 1};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
+}
+
+}  // namespace moe

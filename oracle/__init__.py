@@ -72,7 +72,9 @@ def lib():
                                                 _int, _int, _u16p, pp16, pp16, pp16, _i32p, _f32p,
                                                 _u16p, _int, _f64p]
         L.oracle_unpermute_combine.restype = None
-        L.oracle_unpermute_combine.argtypes = [_u16p, _i32p, _f32p, _i64, _int, _int, _int, _f64p]
+        L.oracle_unpermute_combine.argtypes = [_f32p, _i32p, _f32p, _i64, _int, _int, _int, _f64p]
+        L.oracle_round_bf16_array.restype = None
+        L.oracle_round_bf16_array.argtypes = [_f64p, _i64, _f64p]
         L.oracle_num_threads.restype = _int
         L.oracle_num_threads.argtypes = []
         _lib = L
@@ -111,7 +113,10 @@ def double_to_bf16_bits(a: np.ndarray) -> np.ndarray:
 
 def round_bf16(a: np.ndarray) -> np.ndarray:
     """Round a float64 array to bf16 values (RNE), returned as float64."""
-    return bits_to_float(double_to_bf16_bits(a))
+    src = _c(a, np.float64)
+    out = np.empty_like(src)
+    lib().oracle_round_bf16_array(_p(src, _f64p), src.size, _p(out, _f64p))
+    return out
 
 
 def e4m3_to_double(code: int) -> float:
@@ -137,6 +142,8 @@ class _PtrArray:
 def _experts(W, E):
     """Accept an [E,...] array or a sequence/dict of per-expert arrays."""
     if isinstance(W, dict):
+        if E is None:
+            E = max(W.keys()) + 1
         return [W.get(e) for e in range(E)]
     if isinstance(W, np.ndarray):
         return [W[e] for e in range(E)]
@@ -181,16 +188,16 @@ def gather_rows(x_bits: np.ndarray, k: int, src_of_row: np.ndarray, rows: int) -
     return out
 
 
-def unpermute_combine(y_perm_bits: np.ndarray, dst_of_route: np.ndarray, topk_w: np.ndarray,
+def unpermute_combine(y_perm: np.ndarray, dst_of_route: np.ndarray, topk_w: np.ndarray,
                       round_mode: int = 1) -> np.ndarray:
-    """Weighted combine in slot order (moe_oracle.c, A5)."""
-    yb = _c(y_perm_bits, np.uint16)
+    """Weighted combine in slot order of fp32 expert outputs (moe_oracle.c, A5)."""
+    yb = _c(y_perm, np.float32)
     H = yb.shape[1]
     dst = _c(dst_of_route, np.int32)
     tw = _c(topk_w, np.float32)
     T, k = dst.shape
     out = np.empty((T, H))
-    lib().oracle_unpermute_combine(_p(yb, _u16p), _p(dst, _i32p), _p(tw, _f32p), T, H, k,
+    lib().oracle_unpermute_combine(_p(yb, _f32p), _p(dst, _i32p), _p(tw, _f32p), T, H, k,
                                    round_mode, _p(out, _f64p))
     return out
 

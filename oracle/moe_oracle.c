@@ -25,9 +25,13 @@
  *     (same cudnn-frontend page, BlockScaledTensor: block_size 32 for mxfp8).
  *
  * Arithmetic is double.  round_mode = 1 rounds to bf16 exactly where the
- * GPU path stores a bf16 tensor (h, y, out, dy_perm, dg/du, dx_perm, dx, dW);
+ * GPU path stores a bf16 tensor (h, out, dy_perm, dg/du, dx_perm, dx, dW; the
+ * expert output y is stored in fp32 by the path and is not rounded here);
  * round_mode = 0 keeps every intermediate in double (used to pin the
- * formulas against fp64 autograd).  Readings of points the pages leave open
+ * formulas against fp64 autograd); round_mode = 2 rounds the stored
+ * intermediates (h, dy_perm, dg/du, dx_perm) but returns the final
+ * outputs (out, dx, dW) unrounded, so that a bf16 output of the GPU can be
+ * compared with the exact value of the same arithmetic.  Readings of points the pages leave open
  * (tie-break, NaN order, MX scale rule) are stated at each function.
  */
 #include <math.h>
@@ -73,7 +77,11 @@ uint16_t oracle_double_to_bf16(double x)
 }
 
 static double bf(double x) { return oracle_bf16_to_double(oracle_double_to_bf16(x)); }
+/* Rounding of a stored intermediate (round_mode 1 and 2) and of a final
+ * output (round_mode 1 only: mode 2 returns the exact value of the final
+ * sum, computed from intermediates rounded where the path stores them). */
 static double rnd(double x, int round_mode) { return round_mode ? bf(x) : x; }
+static double rnd_out(double x, int round_mode) { return round_mode == 1 ? bf(x) : x; }
 
 /* OCP FP8 E4M3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no
  * infinities, NaN = S.1111.111, largest finite 448 = S.1111.110. */
@@ -276,7 +284,7 @@ void oracle_gather_rows(const uint16_t *x, int H, int k, const int32_t *src_of_r
 
 /* A5 on its own: out[t] = sum_j w[t,j] * y_perm[dst_of_route[t,j]] in slot
  * order, dropped routes (-1) skipped (double; bf16 in round_mode 1). */
-void oracle_unpermute_combine(const uint16_t *y_perm, const int32_t *dst_of_route,
+void oracle_unpermute_combine(const float *y_perm, const int32_t *dst_of_route,
                               const float *topk_w, int64_t T, int H, int k,
                               int round_mode, double *out)
 {
@@ -287,9 +295,9 @@ void oracle_unpermute_combine(const uint16_t *y_perm, const int32_t *dst_of_rout
             int32_t row = dst_of_route[t * k + j];
             if (row < 0) continue;
             double w = (double)topk_w[t * k + j];
-            for (int n = 0; n < H; ++n) o[n] += w * oracle_bf16_to_double(y_perm[(int64_t)row * H + n]);
+            for (int n = 0; n < H; ++n) o[n] += w * (double)y_perm[(int64_t)row * H + n];
         }
-        for (int n = 0; n < H; ++n) o[n] = rnd(o[n], round_mode);
+        for (int n = 0; n < H; ++n) o[n] = rnd_out(o[n], round_mode);
     }
 }
 
@@ -301,7 +309,8 @@ static double silu(double g) { return g / (1.0 + exp(-g)); }
 static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
 
 /* g = x Wg, u = x Wu (double), h = silu(g) * u (bf16 in round_mode 1),
- * y = h Wd (bf16 in round_mode 1).  Wg, Wu are [H,F]; Wd is [F,H]. */
+ * y = h Wd (kept unrounded: the path stores y in fp32).  Wg, Wu are [H,F];
+ * Wd is [F,H]. */
 static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t *Wu,
                          const uint16_t *Wd, int H, int F, int round_mode,
                          double *g, double *u, double *h, double *y)
@@ -321,7 +330,7 @@ static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t 
         const uint16_t *wd = Wd + (int64_t)f * H;
         for (int n = 0; n < H; ++n) y[n] += h[f] * oracle_bf16_to_double(wd[n]);
     }
-    for (int n = 0; n < H; ++n) y[n] = rnd(y[n], round_mode);
+
 }
 
 /* ------------------------------------------------------------------ */
@@ -357,7 +366,7 @@ void oracle_moe_fwd(int64_t n_tokens, const int64_t *tokens, int H, int F, int E
             if (h_out) memcpy(h_out + ri * F, h, sizeof(double) * F);
             if (y_out) memcpy(y_out + ri * H, y, sizeof(double) * H);
         }
-        for (int n = 0; n < H; ++n) o[n] = rnd(o[n], round_mode);
+        for (int n = 0; n < H; ++n) o[n] = rnd_out(o[n], round_mode);
         free(g);
     }
 }
@@ -370,7 +379,8 @@ void oracle_moe_fwd(int64_t n_tokens, const int64_t *tokens, int H, int F, int E
  * block along K) and dequantised exactly: x along H; W_gate / W_up given as
  * quantised K-major [F][H] codes with scales [F][H/32]; W_down as quantised
  * [H][F] codes with scales [H][F/32]; h = silu(g)*u quantised along F from
- * its unrounded value.  y is bf16 (round_mode 1), out is bf16. */
+ * its unrounded value.  y is kept unrounded (fp32 on the path); out is bf16
+ * in round_mode 1. */
 void oracle_moe_fwd_mxfp8(int64_t n_tokens, const int64_t *tokens, int H, int F, int E, int k,
                           const uint16_t *x,
                           const uint8_t *const *Wg_q, const uint8_t *const *Wg_s,
@@ -410,13 +420,13 @@ void oracle_moe_fwd_mxfp8(int64_t n_tokens, const int64_t *tokens, int H, int F,
                 double s = 0.0;
                 const uint8_t *qd = Wd_q[e] + (int64_t)n * F, *cd = Wd_s[e] + (int64_t)n * (F / 32);
                 for (int f = 0; f < F; ++f) s += h[f] * ldexp(oracle_e4m3_to_double(qd[f]), (int)cd[f / 32] - 127);
-                y[n] = rnd(s, round_mode);
+                y[n] = s;
             }
             double w = (double)topk_w[t * k + j];
             for (int n = 0; n < H; ++n) o[n] += w * y[n];
             if (y_out) memcpy(y_out + (i * k + j) * H, y, sizeof(double) * H);
         }
-        for (int n = 0; n < H; ++n) o[n] = rnd(o[n], round_mode);
+        for (int n = 0; n < H; ++n) o[n] = rnd_out(o[n], round_mode);
         free(xq);
         free(xd);
     }
@@ -499,10 +509,10 @@ void oracle_moe_bwd(int64_t T, int H, int F, int E, int k, const uint16_t *x,
             for (int f = 0; f < F; ++f)
                 for (int n = 0; n < H; ++n) wd[(int64_t)f * H + n] += h[f] * dy[n];
         }
-        for (int n = 0; n < H; ++n) dx[t * H + n] = rnd(acc[n], round_mode);
+        for (int n = 0; n < H; ++n) dx[t * H + n] = rnd_out(acc[n], round_mode);
     }
     free(g);
-    if (round_mode) {
+    if (round_mode == 1) {
         for (int64_t i = 0; i < (int64_t)E * H * F; ++i) {
             dWg[i] = bf(dWg[i]);
             dWu[i] = bf(dWu[i]);
@@ -537,7 +547,7 @@ void oracle_moe_bwd_dx_tokens(int64_t n_tokens, const int64_t *tokens, int H, in
                       round_mode, dy, dg, du, dxr);
             for (int n = 0; n < H; ++n) o[n] += dxr[n];
         }
-        for (int n = 0; n < H; ++n) o[n] = rnd(o[n], round_mode);
+        for (int n = 0; n < H; ++n) o[n] = rnd_out(o[n], round_mode);
         free(g);
     }
 }
@@ -587,7 +597,7 @@ void oracle_moe_bwd_dw_entries(int64_t n_entries, const int32_t *which, const in
                 acc += oracle_bf16_to_double(xr[hn]) * d;
             }
         }
-        val[q] = rnd(acc, round_mode);
+        val[q] = rnd_out(acc, round_mode);
     }
 }
 
@@ -598,4 +608,10 @@ int oracle_num_threads(void)
 #else
     return 1;
 #endif
+}
+
+/* Round n doubles to bf16 values (returned as doubles). */
+void oracle_round_bf16_array(const double *in, int64_t n, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = bf(in[i]);
 }

@@ -1,0 +1,60 @@
+"""Shared helpers for the GPU parity tests: seeded inputs on the device, host
+copies for the oracle, and the tolerance checks."""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from mixture_experts_ffn_warp_gb300.synthetic import MoeShape, make_inputs
+
+# Floating-point bar: max |err| <= 2e-2 * RMS(reference) for bf16 outputs with
+# fp32 accumulation; 6e-2 * RMS for MXFP8 against an oracle that applies the
+# same quantisation.
+TOL_BF16 = 2e-2
+TOL_MXFP8 = 6e-2
+
+
+def bits(t: torch.Tensor) -> np.ndarray:
+    return oracle.bf16_bits(t)
+
+
+def to_f64(t: torch.Tensor) -> np.ndarray:
+    return t.detach().float().cpu().double().numpy()
+
+
+def assert_close_rms(got, ref, tol=TOL_BF16, what=""):
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    err = float(np.abs(got - ref).max()) if got.size else 0.0
+    assert err <= tol * rms, f"{what}: max|err| {err:.3e} > {tol} * RMS {rms:.3e}"
+    return err / rms if rms > 0 else 0.0
+
+
+def assert_close_ulp(got, ref, what="", slack=2e-3):
+    """Element-wise check of a stored bf16 intermediate against the oracle that
+    rounds at the same point: the two may round a value on either side of a
+    bf16 rounding boundary (fp32 vs fp64 accumulation), so each element may
+    differ by one bf16 ulp (2^-7 relative, at most) plus a small absolute
+    slack of `slack` * RMS for the accumulation-order difference."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    bound = 2.0 ** -7 * np.abs(ref) + slack * rms
+    bad = np.abs(got - ref) > bound
+    assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond 1 ulp + {slack}*RMS; " \
+                          f"worst {float(np.abs(got - ref).max()):.3e} (RMS {rms:.3e})"
+
+
+def gpu_inputs(shape: MoeShape, seed: int = 0, with_dy=None):
+    return make_inputs(shape, device="cuda", seed=seed, with_dy=with_dy)
+
+
+def host_experts(W: torch.Tensor, experts) -> dict:
+    """Copy selected experts of a [E, a, b] bf16 device tensor to host bits."""
+    return {int(e): bits(W[int(e)]) for e in experts}

@@ -271,7 +271,7 @@ def test_identity_experts_return_input():
     idx, w = oracle.route_topk(lg, 6)
     p = oracle.permute(idx, 64)
     xb = oracle.bf16_bits(inp["x"][:512])
-    xp = oracle.gather_rows(xb, 6, p["src_of_row"], idx.size)
+    xp = oracle.bits_to_float(oracle.gather_rows(xb, 6, p["src_of_row"], idx.size)).astype(np.float32)
     out = oracle.unpermute_combine(xp, p["dst_of_route"], w, round_mode=0)
     x = oracle.bits_to_float(xb)
     s = w.astype(np.float64).sum(1, keepdims=True)
@@ -282,8 +282,7 @@ def test_identity_experts_return_input():
 
 
 def test_combine_slot_weights_and_drops():
-    y = np.array([[1.0, 2.0], [10.0, -4.0], [0.5, 0.25]])
-    yb = oracle.double_to_bf16_bits(y)
+    yb = np.array([[1.0, 2.0], [10.0, -4.0], [0.5, 0.25]], np.float32)
     dst = np.array([[1, 0], [-1, 2]], np.int32)
     w = np.array([[0.25, 0.75], [0.9, 2.0]], np.float32)
     out = oracle.unpermute_combine(yb, dst, w, round_mode=0)
@@ -503,3 +502,16 @@ def test_mxfp8_forward_close_to_exact_on_random_inputs():
     rms = np.sqrt((ex["out"] ** 2).mean())
     rel = np.sqrt(((mx["out"] - ex["out"]) ** 2).mean()) / rms
     assert 1e-3 < rel < 0.15
+
+
+def test_round_mode_2_is_mode_1_before_the_final_rounding():
+    inp, idx, w, b = _rand_problem(15, T=20, H=32, F=64, E=4, k=2)
+    f1 = oracle.moe_fwd(b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, round_mode=1, want_y=True)
+    f2 = oracle.moe_fwd(b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, round_mode=2, want_y=True)
+    assert np.array_equal(f1["y"], f2["y"])                      # same intermediates
+    assert np.array_equal(oracle.round_bf16(f2["out"]), f1["out"])
+    assert not np.array_equal(f2["out"], f1["out"])
+    g1 = oracle.moe_bwd(b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, b["dY"], round_mode=1)
+    g2 = oracle.moe_bwd(b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, b["dY"], round_mode=2)
+    for n in ("dx", "dW_gate", "dW_up", "dW_down"):
+        assert np.array_equal(oracle.round_bf16(g2[n]), g1[n]), n
