@@ -147,6 +147,33 @@ MOE_API moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx, i
                          int32_t *group_offsets, void *ws, size_t ws_bytes,
                          moe_stream_t stream);
 
+/* moe_permute for callers that cannot allocate device memory.  The pages
+ * have no counterpart of this call; it exists for hosts whose device memory
+ * is owned by someone else -- a framework's caching allocator or a fixed
+ * arena sized up front, where a stray cudaMalloc breaks the memory budget --
+ * and for plain C or plugin callers with no way to manage a workspace buffer.
+ *
+ * Same arguments, results and limits as moe_permute, except:
+ *   - no workspace: the scratch (error word and per-chunk expert counts)
+ *     lives in a fixed 256 KiB array inside this library's device image,
+ *     resident on every GPU that loads the library until the process exits;
+ *   - problems whose scratch exceeds it are rejected with
+ *     MOE_ERR_UNSUPPORTED: ceil(T*k / 8192) * E must be <= 65472;
+ *   - error_word: device uint32 out (nullable) that receives this call's
+ *     device error bits (MOE_DEVERR_*), stream-ordered after the call.
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).  The first call on each device looks up the array's device
+ * address (cudaGetSymbolAddress) with that device current; make that first
+ * call before any stream capture.  Every call shares the one array, so calls
+ * that overlap on the GPU (for example on two streams at once) race and give
+ * undefined results; serialise them. */
+MOE_API moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const int32_t *topk_idx, int64_t T,
+                                                int H, int E, int k, int align, moe_bf16_t *x_perm,
+                                                int64_t rows_cap, int32_t *dst_of_route,
+                                                int32_t *src_of_row, int32_t *group_sizes,
+                                                int32_t *group_offsets, uint32_t *error_word,
+                                                moe_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* A3 + A4  Grouped expert FFN, forward                                 */
 /* ------------------------------------------------------------------ */

@@ -38,6 +38,8 @@ SIGNATURES = {
     "moe_read_device_error": (_st, [_vp, _vp, C.POINTER(C.c_uint32)]),
     "moe_route_topk": (_st, [_vp, _i64, _int, _int, _vp, _vp, _vp]),
     "moe_permute": (_st, [_vp, _vp, _i64, _int, _int, _int, _int, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_permute_static_scratch": (_st, [_vp, _vp, _i64, _int, _int, _int, _int, _vp, _i64, _vp, _vp, _vp, _vp,
+                                         _vp, _vp]),
     "moe_grouped_ffn_fwd": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_fc1_swiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_fc2": (_st, [_vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),

@@ -233,3 +233,98 @@ extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx
     }
     return MOE_OK;
 }
+
+// ---------------------------------------------------------------------------
+// moe_permute_static_scratch: the same permutation for callers that cannot
+// allocate device memory.  Its scratch (error word + per-chunk expert counts)
+// is a fixed array in this library's device image instead of a workspace.
+// ---------------------------------------------------------------------------
+
+#include <mutex>
+
+namespace moe {
+namespace {
+
+// 256 KiB: a 256-byte header (error word at offset 0) and room for
+// (256 KiB - 256) / 4 = 65472 per-chunk counts, i.e. chunks * E <= 65472
+// with 8192 routes per chunk.  Every GPU that loads the library keeps this
+// array resident until the process exits.
+constexpr size_t kStaticScratchBytes = 256 * 1024;
+static __device__ __align__(256) unsigned char g_permute_scratch[kStaticScratchBytes];
+
+constexpr int kMaxScratchDevices = 128;
+std::mutex g_scratch_lock;
+void *g_scratch_addr[kMaxScratchDevices];   // device address of the array, per device
+
+// Device address of the array on the current device, looked up once per
+// device (the host-side name is only a stand-in and must not reach a kernel).
+moe_status_t static_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> guard(g_scratch_lock);
+    if (!g_scratch_addr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return MOE_OK;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const int32_t *topk_idx, int64_t T,
+                                                   int H, int E, int k, int align, moe_bf16_t *x_perm,
+                                                   int64_t rows_cap, int32_t *dst_of_route,
+                                                   int32_t *src_of_row, int32_t *group_sizes,
+                                                   int32_t *group_offsets, uint32_t *error_word,
+                                                   moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || H < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || E > 1024 || k < 1 || k > 32 || align < 1 || align > 1024 || H % 8 != 0)
+        return MOE_ERR_UNSUPPORTED;
+    if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
+    const int64_t R = T * (int64_t)k;
+    if (rows_cap < R + (int64_t)E * (align - 1)) return MOE_ERR_INVALID_ARG;
+    if (rows_cap >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !topk_idx || !x_perm || !dst_of_route || !src_of_row))
+        return MOE_ERR_INVALID_ARG;
+    const int64_t chunks = perm_chunks(R);
+    if (kWsHeaderBytes + (size_t)chunks * (size_t)E * sizeof(int32_t) > kStaticScratchBytes)
+        return MOE_ERR_UNSUPPORTED;   // problem needs more than the fixed scratch array
+
+    void *scratch = nullptr;
+    moe_status_t st = static_scratch(&scratch);
+    if (st != MOE_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t *err = static_cast<uint32_t *>(scratch);
+    int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(scratch) + kWsHeaderBytes);
+    // the error word starts at zero on every call; the counts are fully rewritten
+    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (chunks > 0) {
+        permute_count_kernel<<<(unsigned)chunks, kPermWarps * 32, kPermWarps * E * sizeof(int32_t), s>>>(
+            topk_idx, R, E, dst_of_route, counts, err);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    permute_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, chunks, E, align, group_sizes, group_offsets);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    const int row_vecs = H / 8;
+    if (T > 0) {
+        const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
+        permute_scatter_kernel<<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(
+            reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts, dst_of_route,
+            src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, err);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    if (align > 1) {
+        permute_pad_kernel<<<E, 256, 0, s>>>(group_sizes, group_offsets, E, row_vecs, src_of_row,
+                                             reinterpret_cast<uint4 *>(x_perm), rows_cap);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    if (error_word &&
+        cudaMemcpyAsync(error_word, err, sizeof(uint32_t), cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    return MOE_OK;
+}
