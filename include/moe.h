@@ -246,6 +246,69 @@ MOE_API moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *d
                                    const float *topk_w, int64_t T, int H, int k,
                                    moe_bf16_t *out, moe_stream_t stream);
 
+/* ------------------------------------------------------------------ */
+/* A8  Backward                                                         */
+/* ------------------------------------------------------------------ */
+
+/* Backward of the expert FFN and the combine ("Add MoE + expert-parallel
+ * Python API surface, PyTorch reference, and tests", Summary: the backward
+ * re-dispatches gradient rows along the forward routes, recomputes SwiGLU
+ * from the bf16 fc1_c stash, returns FP32 weight gradients and the route
+ * (top-k weight) gradients; "[Draft][JAX] MoE block optimization": fused
+ * grouped_gemm_dswiglu; "[JAX] Expert Parallelism", commit log: the wgrad of
+ * an expert with no tokens is zero, never uninitialised).  For route
+ * r = (t, j) -> expert e at permuted row i = dst_of_route[t, j]:
+ *   dy_perm[i] = bf16(w[t,j] dY[t]);          d_topk_w[t,j] = <dY[t], y_perm[i]>
+ *   dh = dy_perm[i] W_down[e]^T (fp32);       g, u = fc1_c[i] (bf16 stash)
+ *   dgu[i] = bf16([dh u s (1 + g (1 - s)) | dh g s]),  s = sigmoid(g)
+ *   dx_perm[i] = dgu[i] [W_gate[e]; W_up[e]]^T (fp32)
+ *   dx[t] = bf16(sum_j dx_perm[row(t,j)])
+ *   dW_down[e] = sum_i h[i]^T dy_perm[i];  [dW_gate|dW_up][e] = sum_i x_perm[i]^T dgu[i]
+ *     (fp32, over the rows of group e; experts with no rows get exact zeros)
+ * Shapes: dY, dx bf16 [T, H]; x_perm, dy_perm bf16 [rows_cap, H]; h bf16
+ * [rows_cap, F]; fc1_c, dgu bf16 [rows_cap, 2F]; y_perm, dx_perm fp32
+ * [rows_cap, H]; dW_gate, dW_up fp32 [E, H, F]; dW_down fp32 [E, F, H];
+ * d_topk_w fp32 [T, k] (nullable; y_perm may then be NULL).  dy_perm, dgu
+ * and dx_perm are caller-owned scratch.  group_sizes/group_offsets/
+ * dst_of_route are the forward's (moe_permute); padding rows (align > 1)
+ * get zero gradient rows.  Limits: H % 128 == 0, F % 128 == 0, E <= 1024,
+ * 1 <= k <= 32.  Errors as for the forward calls. */
+MOE_API moe_status_t moe_grouped_ffn_bwd(
+    const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
+    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const float *y_perm,
+    const int32_t *dst_of_route, const int32_t *group_sizes, const int32_t *group_offsets,
+    const float *topk_w, int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm,
+    moe_bf16_t *dgu, float *dx_perm, moe_bf16_t *dx, float *dW_gate, float *dW_up, float *dW_down,
+    float *d_topk_w, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* The steps of moe_grouped_ffn_bwd, callable on their own (same arguments,
+ * limits and errors; each reads what the previous steps wrote):
+ *   moe_combine_bwd               dY -> dy_perm (+ zero padding rows), d_topk_w
+ *   moe_grouped_dgrad_fc2_dswiglu dy_perm, fc1_c -> dgu
+ *   moe_grouped_dgrad_fc1         dgu -> dx_perm
+ *   moe_grouped_wgrad             x_perm, h, dy_perm, dgu -> dW_gate, dW_up, dW_down
+ *   moe_unpermute_sum             dx_perm -> dx */
+MOE_API moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const float *y_perm, const int32_t *dst_of_route,
+                                     const float *topk_w, const int32_t *group_sizes,
+                                     const int32_t *group_offsets, int64_t T, int H, int E, int k,
+                                     int64_t rows_cap, moe_bf16_t *dy_perm, float *d_topk_w,
+                                     moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down,
+                                                   const moe_bf16_t *fc1_c, const int32_t *group_offsets,
+                                                   int E, int H, int F, int64_t rows_cap, moe_bf16_t *dgu,
+                                                   void *ws, size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_bf16_t *W_gate,
+                                           const moe_bf16_t *W_up, const int32_t *group_offsets, int E,
+                                           int H, int F, int64_t rows_cap, float *dx_perm, void *ws,
+                                           size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf16_t *h,
+                                       const moe_bf16_t *dy_perm, const moe_bf16_t *dgu,
+                                       const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap,
+                                       float *dW_gate, float *dW_up, float *dW_down, void *ws,
+                                       size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *dst_of_route, int64_t T, int H,
+                                       int k, moe_bf16_t *dx, moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -8,4 +8,8 @@ from ._binding import (  # noqa: F401
     moe_grouped_ffn_fwd, moe_permute,
     moe_route_topk, moe_unpermute_combine, rows_capacity,
 )
-from .layer import MoeForward, moe_forward  # noqa: F401
+from ._binding import (  # noqa: F401
+    moe_combine_bwd, moe_grouped_dgrad_fc1, moe_grouped_dgrad_fc2_dswiglu, moe_grouped_ffn_bwd,
+    moe_grouped_wgrad, moe_unpermute_sum,
+)
+from .layer import MoeBackward, MoeForward, moe_forward  # noqa: F401

@@ -44,6 +44,12 @@ SIGNATURES = {
     "moe_grouped_fc1_swiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_fc2": (_st, [_vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_unpermute_combine": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp]),
+    "moe_grouped_ffn_bwd": (_st, [_vp] * 12 + [_i64, _int, _int, _int, _int, _i64] + [_vp] * 8 + [_vp, _sz, _vp]),
+    "moe_combine_bwd": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _i64, _vp, _vp, _vp]),
+    "moe_grouped_dgrad_fc2_dswiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
+    "moe_grouped_dgrad_fc1": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
+    "moe_grouped_wgrad": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_unpermute_sum": (_st, [_vp, _vp, _i64, _int, _int, _vp, _vp]),
 }
 
 _lib = None
@@ -258,4 +264,85 @@ def moe_unpermute_combine(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk
     _need(out, "out", torch.bfloat16, (T, H), dev)
     _check("moe_unpermute_combine", load_library().moe_unpermute_combine(
         _ptr(y_perm), _ptr(dst_of_route), _ptr(topk_w), T, H, k, _ptr(out), _stream(stream)))
+    return out
+
+
+# ------------------------------------------------------------------ A8 backward steps
+
+def moe_combine_bwd(dY, y_perm, perm: "Permutation", topk_w, dy_perm, d_topk_w=None, stream=None):
+    """dy_perm = w * dY scattered to the forward rows; d_topk_w = <dY, y> (moe.h)."""
+    T, H = dY.shape
+    k = perm.dst_of_route.shape[1]
+    E = perm.group_sizes.shape[0]
+    _check("moe_combine_bwd", load_library().moe_combine_bwd(
+        _ptr(dY), _ptr(y_perm), _ptr(perm.dst_of_route), _ptr(topk_w), _ptr(perm.group_sizes),
+        _ptr(perm.group_offsets), T, H, E, k, perm.rows_cap, _ptr(dy_perm), _ptr(d_topk_w), _stream(stream)))
+
+
+def moe_grouped_dgrad_fc2_dswiglu(dy_perm, W_down, fc1_c, group_offsets, ws: Workspace, dgu, stream=None):
+    """dgu = dSwiGLU(dy_perm W_down^T) from the fc1_c stash (moe.h)."""
+    rows_cap, H = dy_perm.shape
+    E, F, _ = W_down.shape
+    _check("moe_grouped_dgrad_fc2_dswiglu", load_library().moe_grouped_dgrad_fc2_dswiglu(
+        _ptr(dy_perm), _ptr(W_down), _ptr(fc1_c), _ptr(group_offsets), E, H, F, rows_cap, _ptr(dgu),
+        _ptr(ws.buf), ws.nbytes, _stream(stream)))
+
+
+def moe_grouped_dgrad_fc1(dgu, W_gate, W_up, group_offsets, ws: Workspace, dx_perm, stream=None):
+    """dx_perm = [dg|du] [W_gate; W_up]^T per group (moe.h)."""
+    rows_cap = dgu.shape[0]
+    E, H, F = W_gate.shape
+    _check("moe_grouped_dgrad_fc1", load_library().moe_grouped_dgrad_fc1(
+        _ptr(dgu), _ptr(W_gate), _ptr(W_up), _ptr(group_offsets), E, H, F, rows_cap, _ptr(dx_perm),
+        _ptr(ws.buf), ws.nbytes, _stream(stream)))
+
+
+def moe_grouped_wgrad(x_perm, h, dy_perm, dgu, group_offsets, ws: Workspace, dW_gate, dW_up, dW_down,
+                      stream=None):
+    """fp32 weight gradients per expert, K = the group's rows (moe.h)."""
+    rows_cap, H = x_perm.shape
+    E, _, F = dW_gate.shape
+    _check("moe_grouped_wgrad", load_library().moe_grouped_wgrad(
+        _ptr(x_perm), _ptr(h), _ptr(dy_perm), _ptr(dgu), _ptr(group_offsets), E, H, F, rows_cap,
+        _ptr(dW_gate), _ptr(dW_up), _ptr(dW_down), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+
+
+def moe_unpermute_sum(dx_perm, dst_of_route, dx, stream=None):
+    """dx[t] = sum_j dx_perm[dst[t,j]] (moe.h)."""
+    T, k = dst_of_route.shape
+    H = dx_perm.shape[1]
+    _check("moe_unpermute_sum", load_library().moe_unpermute_sum(
+        _ptr(dx_perm), _ptr(dst_of_route), T, H, k, _ptr(dx), _stream(stream)))
+
+
+def moe_grouped_ffn_bwd(dY, x_perm, W_gate, W_up, W_down, fc1_c, h, y_perm, perm: "Permutation", topk_w,
+                        ws: Workspace, want_d_topk_w: bool = True, stream=None):
+    """The whole backward in one call (moe.h); allocates its outputs and scratch.
+    Returns dict(dx, dW_gate, dW_up, dW_down, d_topk_w)."""
+    dev = dY.device
+    T, H = dY.shape
+    E, _, F = W_gate.shape
+    k = perm.dst_of_route.shape[1]
+    cap = perm.rows_cap
+    for name, t, dt, shp in (("dY", dY, torch.bfloat16, (T, H)), ("x_perm", x_perm, torch.bfloat16, (cap, H)),
+                             ("W_gate", W_gate, torch.bfloat16, (E, H, F)), ("W_up", W_up, torch.bfloat16, (E, H, F)),
+                             ("W_down", W_down, torch.bfloat16, (E, F, H)),
+                             ("fc1_c", fc1_c, torch.bfloat16, (cap, 2 * F)), ("h", h, torch.bfloat16, (cap, F)),
+                             ("y_perm", y_perm, torch.float32, (cap, H)), ("topk_w", topk_w, torch.float32, (T, k))):
+        _need(t, name, dt, shp, dev)
+    out = {
+        "dx": torch.empty(T, H, dtype=torch.bfloat16, device=dev),
+        "dW_gate": torch.empty(E, H, F, dtype=torch.float32, device=dev),
+        "dW_up": torch.empty(E, H, F, dtype=torch.float32, device=dev),
+        "dW_down": torch.empty(E, F, H, dtype=torch.float32, device=dev),
+        "d_topk_w": torch.empty(T, k, dtype=torch.float32, device=dev) if want_d_topk_w else None,
+    }
+    dy_perm = torch.empty(cap, H, dtype=torch.bfloat16, device=dev)
+    dgu = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev)
+    dx_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
+    _check("moe_grouped_ffn_bwd", load_library().moe_grouped_ffn_bwd(
+        _ptr(dY), _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(fc1_c), _ptr(h), _ptr(y_perm),
+        _ptr(perm.dst_of_route), _ptr(perm.group_sizes), _ptr(perm.group_offsets), _ptr(topk_w),
+        T, H, F, E, k, cap, _ptr(dy_perm), _ptr(dgu), _ptr(dx_perm), _ptr(out["dx"]), _ptr(out["dW_gate"]),
+        _ptr(out["dW_up"]), _ptr(out["dW_down"]), _ptr(out["d_topk_w"]), _ptr(ws.buf), ws.nbytes, _stream(stream)))
     return out

@@ -48,7 +48,7 @@ combine_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ ds
     float my_w = 0.0f;
     if (lane < k) {
         my_dst = dst_of_route[t * k + lane];
-        my_w = topk_w[t * k + lane];
+        my_w = topk_w ? topk_w[t * k + lane] : 1.0f;   // no weights: plain sum over the slots
     }
     int dst[KMAX];
     float w[KMAX];
@@ -92,6 +92,18 @@ cudaError_t launch(const float *y, const int32_t *dst, const float *w, int64_t T
 }
 
 }  // namespace
+
+cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int64_t T, int H, int k,
+                         moe_bf16_t *out, cudaStream_t s) {
+    const int sl = H / 8;
+    if (k <= 1) return launch<1>(y, dst, w, T, k, sl, out, s);
+    if (k <= 2) return launch<2>(y, dst, w, T, k, sl, out, s);
+    if (k <= 4) return launch<4>(y, dst, w, T, k, sl, out, s);
+    if (k <= 8) return launch<8>(y, dst, w, T, k, sl, out, s);
+    if (k <= 16) return launch<16>(y, dst, w, T, k, sl, out, s);
+    return launch<32>(y, dst, w, T, k, sl, out, s);
+}
+
 }  // namespace moe
 
 extern "C" moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *dst_of_route,
@@ -101,14 +113,5 @@ extern "C" moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t
     if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!y_perm || !dst_of_route || !topk_w || !out) return MOE_ERR_INVALID_ARG;
-    cudaStream_t s = (cudaStream_t)stream;
-    const int sl = H / 8;
-    cudaError_t e;
-    if (k <= 1) e = moe::launch<1>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
-    else if (k <= 2) e = moe::launch<2>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
-    else if (k <= 4) e = moe::launch<4>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
-    else if (k <= 8) e = moe::launch<8>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
-    else if (k <= 16) e = moe::launch<16>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
-    else e = moe::launch<32>(y_perm, dst_of_route, topk_w, T, k, sl, out, s);
-    return moe::cuda_status(e);
+    return moe::cuda_status(moe::combine_rows(y_perm, dst_of_route, topk_w, T, H, k, out, (cudaStream_t)stream));
 }

@@ -29,6 +29,10 @@ inline moe_status_t launch_status() { return cuda_status(cudaGetLastError()); }
 
 int device_sm_count();
 
+// out[t] = bf16(sum_j w[t,j] * y[dst[t,j]]) over fp32 rows of y (w == nullptr: weights 1).
+cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int64_t T, int H, int k,
+                         moe_bf16_t *out, cudaStream_t s);
+
 __device__ __forceinline__ void raise_device_error(uint32_t *err, uint32_t bits) {
     if (err) atomicOr(err, bits);
 }

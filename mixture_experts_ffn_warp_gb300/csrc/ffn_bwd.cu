@@ -1,0 +1,296 @@
+// ffn_bwd.cu -- A8: backward of the expert FFN and of the combine.
+//
+//   B1 combine_bwd      dy_perm[row(t,j)] = bf16(w[t,j] * dY[t]); d_topk_w[t,j] = <dY[t], y(t,j)>
+//   B2+B3 dgrad FC2     dh = dy_perm W_down^T (fp32 in TMEM), then dSwiGLU from the fc1_c
+//                       stash in the epilogue: dg = dh*u*s*(1+g*(1-s)), du = dh*g*s -> bf16
+//   B4 dgrad FC1        dx_perm = [dg|du] [W_gate; W_up]^T (K = 2F), fp32
+//   B5 wgrad            dW_down[e] = h_e^T dy_e;  dW_gate|dW_up[e] = x_e^T [dg|du]_e  (fp32;
+//                       K = the rows of group e, read on the device; 0-token experts -> 0)
+//   B6 unpermute-sum    dx[t] = bf16(sum_j dx_perm[row(t,j)])
+// ("Add MoE + expert-parallel Python API surface, PyTorch reference, and tests",
+// Summary: backward re-dispatches gradient rows along the forward routes, recomputes
+// SwiGLU from the fc1_c stash, returns FP32 weight gradients and route gradients;
+// "[Draft][JAX] MoE block optimization": grouped_gemm_dswiglu; "[JAX] Expert
+// Parallelism", commit log: zero-filled wgrad of experts with no tokens.)
+#include "gemm_launch.cuh"
+
+using namespace moe;
+using gg::Op;
+
+namespace {
+
+constexpr int kBwdWarps = 8;
+
+template <int KMAX>
+__global__ void __launch_bounds__(kBwdWarps * 32)
+combine_bwd_kernel(const uint4 *__restrict__ dY, const float4 *__restrict__ y_perm,
+                   const int32_t *__restrict__ dst_of_route, const float *__restrict__ topk_w, int64_t T,
+                   int k, int slices, uint4 *__restrict__ dy_perm, float *__restrict__ d_topk_w) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_dst = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+        my_dst = dst_of_route[t * k + lane];
+        my_w = topk_w[t * k + lane];
+    }
+    int dst[KMAX];
+    float w[KMAX], dot[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        dst[j] = __shfl_sync(0xFFFFFFFFu, my_dst, j);
+        w[j] = __shfl_sync(0xFFFFFFFFu, my_w, j);
+        if (j >= k) dst[j] = -1;
+        dot[j] = 0.0f;
+    }
+    const bool want_dot = d_topk_w != nullptr;
+    for (int s = lane; s < slices; s += 32) {
+        const uint4 g = __ldg(dY + t * slices + s);
+        const __nv_bfloat162 *gp = reinterpret_cast<const __nv_bfloat162 *>(&g);
+        float d[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(gp[i]);
+            d[2 * i] = f.x;
+            d[2 * i + 1] = f.y;
+        }
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {
+            if (dst[j] < 0) continue;
+            uint4 o;
+            __nv_bfloat162 *op = reinterpret_cast<__nv_bfloat162 *>(&o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) op[i] = __floats2bfloat162_rn(w[j] * d[2 * i], w[j] * d[2 * i + 1]);
+            dy_perm[(int64_t)dst[j] * slices + s] = o;
+            if (want_dot) {
+                const float4 *yr = y_perm + ((int64_t)dst[j] * slices + s) * 2;
+                const float4 a = __ldg(yr), b = __ldg(yr + 1);
+                dot[j] += d[0] * a.x + d[1] * a.y + d[2] * a.z + d[3] * a.w + d[4] * b.x + d[5] * b.y +
+                          d[6] * b.z + d[7] * b.w;
+            }
+        }
+    }
+    if (!want_dot) return;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        float v = dot[j];
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, off);
+        if (lane == 0 && j < k) d_topk_w[t * k + j] = dst[j] >= 0 ? v : 0.0f;
+    }
+}
+
+// Padding rows of aligned groups get a zero gradient row (never uninitialised memory).
+__global__ void zero_pad_rows_kernel(const int32_t *__restrict__ group_sizes,
+                                     const int32_t *__restrict__ group_offsets, int row_vecs,
+                                     uint4 *__restrict__ rows, int64_t rows_cap) {
+    const int e = blockIdx.x;
+    const int64_t first = (int64_t)group_offsets[e] + group_sizes[e];
+    const int64_t last = group_offsets[e + 1] < rows_cap ? group_offsets[e + 1] : rows_cap;
+    for (int64_t row = first; row < last; ++row)
+        for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) rows[row * row_vecs + v] = make_uint4(0, 0, 0, 0);
+}
+
+template <int KMAX>
+cudaError_t launch_combine_bwd(const moe_bf16_t *dY, const float *y_perm, const int32_t *dst, const float *w,
+                               int64_t T, int H, int k, moe_bf16_t *dy_perm, float *d_topk_w, cudaStream_t s) {
+    const int64_t blocks = (T + kBwdWarps - 1) / kBwdWarps;
+    combine_bwd_kernel<KMAX><<<(unsigned)blocks, kBwdWarps * 32, 0, s>>>(
+        reinterpret_cast<const uint4 *>(dY), reinterpret_cast<const float4 *>(y_perm), dst, w, T, k, H / 8,
+        reinterpret_cast<uint4 *>(dy_perm), d_topk_w);
+    return cudaGetLastError();
+}
+
+moe_status_t check_sizes(int E, int H, int F, int64_t rows_cap, void *ws, size_t ws_bytes) {
+    if (E < 1 || H < 1 || F < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
+    if (E > gg::kMaxE || H % 128 != 0 || F % 128 != 0 || rows_cap >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+    if (!ws || ws_bytes < kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+int64_t mblock_bound(int64_t rows_cap, int E) { return (rows_cap + gg::BM - 1) / gg::BM + E; }
+
+}  // namespace
+
+extern "C" moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const float *y_perm, const int32_t *dst_of_route,
+                                        const float *topk_w, const int32_t *group_sizes,
+                                        const int32_t *group_offsets, int64_t T, int H, int E, int k,
+                                        int64_t rows_cap, moe_bf16_t *dy_perm, float *d_topk_w,
+                                        moe_stream_t stream) {
+    if (T < 0 || H < 1 || E < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
+    if (k < 1 || k > 32 || H % 8 != 0 || E > gg::kMaxE) return MOE_ERR_UNSUPPORTED;
+    if (!group_sizes || !group_offsets || !dy_perm) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!dY || !dst_of_route || !topk_w || (d_topk_w && !y_perm))) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (T > 0) {
+        cudaError_t e;
+        if (k <= 1) e = launch_combine_bwd<1>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
+        else if (k <= 2) e = launch_combine_bwd<2>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
+        else if (k <= 4) e = launch_combine_bwd<4>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
+        else if (k <= 8) e = launch_combine_bwd<8>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
+        else if (k <= 16) e = launch_combine_bwd<16>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
+        else e = launch_combine_bwd<32>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
+        if (e != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    zero_pad_rows_kernel<<<E, 256, 0, s>>>(group_sizes, group_offsets, H / 8, reinterpret_cast<uint4 *>(dy_perm),
+                                           rows_cap);
+    return launch_status();
+}
+
+extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down,
+                                                      const moe_bf16_t *fc1_c, const int32_t *group_offsets,
+                                                      int E, int H, int F, int64_t rows_cap, moe_bf16_t *dgu,
+                                                      void *ws, size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
+    if (st != MOE_OK || rows_cap == 0) return st;
+    if (!dy_perm || !W_down || !fc1_c || !group_offsets || !dgu) return MOE_ERR_INVALID_ARG;
+    const int bn = (F % 256 == 0) ? 256 : 128;
+    // A = dy_perm [rows, H] (K-major), B = W_down[e] as [F rows][H] (K-major)
+    CUtensorMap tA, tB;
+    if (!tmap_bf16_2d(&tA, dy_perm, H, rows_cap, H, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, bn))
+        return MOE_ERR_UNSUPPORTED;
+    gg::Args a{};
+    a.group_offsets = group_offsets;
+    a.E = E;
+    a.N = F;
+    a.K = H;
+    a.n_tiles = F / bn;
+    a.rows_cap = rows_cap;
+    a.out0 = reinterpret_cast<__nv_bfloat16 *>(dgu);
+    a.ld0 = 2 * (int64_t)F;
+    a.aux = reinterpret_cast<const __nv_bfloat16 *>(fc1_c);
+    a.ld_aux = 2 * (int64_t)F;
+    a.err = ws_error_word(ws);
+    const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
+    if (bn == 256) return gg::launch<Op::DGRAD_DSWIGLU, 256>(tA, tB, tB, a, bound, (cudaStream_t)stream);
+    return gg::launch<Op::DGRAD_DSWIGLU, 128>(tA, tB, tB, a, bound, (cudaStream_t)stream);
+}
+
+extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_bf16_t *W_gate,
+                                              const moe_bf16_t *W_up, const int32_t *group_offsets, int E, int H,
+                                              int F, int64_t rows_cap, float *dx_perm, void *ws, size_t ws_bytes,
+                                              moe_stream_t stream) {
+    moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
+    if (st != MOE_OK || rows_cap == 0) return st;
+    if (!dgu || !W_gate || !W_up || !group_offsets || !dx_perm) return MOE_ERR_INVALID_ARG;
+    const int bn = (H % 256 == 0) ? 256 : 128;
+    // A = [dg | du] [rows, 2F] (K-major), B = W_gate[e] / W_up[e] as [H rows][F] (K-major)
+    CUtensorMap tA, tB0, tB1;
+    if (!tmap_bf16_2d(&tA, dgu, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F, 64, 128) ||
+        !tmap_bf16_3d(&tB0, W_gate, F, H, E, 64, bn) || !tmap_bf16_3d(&tB1, W_up, F, H, E, 64, bn))
+        return MOE_ERR_UNSUPPORTED;
+    gg::Args a{};
+    a.group_offsets = group_offsets;
+    a.E = E;
+    a.N = H;
+    a.K = 2 * F;
+    a.k_split = F;
+    a.n_tiles = H / bn;
+    a.rows_cap = rows_cap;
+    a.out_f32 = dx_perm;
+    a.ld0 = H;
+    a.err = ws_error_word(ws);
+    const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
+    if (bn == 256) return gg::launch<Op::DGRAD_FC1, 256>(tA, tB0, tB1, a, bound, (cudaStream_t)stream);
+    return gg::launch<Op::DGRAD_FC1, 128>(tA, tB0, tB1, a, bound, (cudaStream_t)stream);
+}
+
+extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf16_t *h, const moe_bf16_t *dy_perm,
+                                          const moe_bf16_t *dgu, const int32_t *group_offsets, int E, int H, int F,
+                                          int64_t rows_cap, float *dW_gate, float *dW_up, float *dW_down, void *ws,
+                                          size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    if (!group_offsets || !dW_gate || !dW_up || !dW_down) return MOE_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (rows_cap == 0) {   // no rows at all: every expert's gradient is zero
+        const size_t n = (size_t)E * H * F * sizeof(float);
+        if (cudaMemsetAsync(dW_gate, 0, n, s) != cudaSuccess || cudaMemsetAsync(dW_up, 0, n, s) != cudaSuccess ||
+            cudaMemsetAsync(dW_down, 0, n, s) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        return MOE_OK;
+    }
+    if (!x_perm || !h || !dy_perm || !dgu) return MOE_ERR_INVALID_ARG;
+    const uint64_t rows = (uint64_t)rows_cap;
+    {   // dW_down[e] [F, H] = h_e^T dy_e: A = h (MN-major), B = dy_perm (MN-major)
+        const int bn = (H % 256 == 0) ? 256 : 128;
+        CUtensorMap tA, tB;
+        if (!tmap_bf16_2d(&tA, h, F, rows, F, 64, 64) || !tmap_bf16_2d(&tB, dy_perm, H, rows, H, 64, 64))
+            return MOE_ERR_UNSUPPORTED;
+        gg::Args a{};
+        a.group_offsets = group_offsets;
+        a.E = E;
+        a.M = F;
+        a.N = H;
+        a.m_tiles = F / gg::BM;
+        a.n_tiles = H / bn;
+        a.rows_cap = rows_cap;
+        a.out_f32 = dW_down;
+        a.ld0 = H;
+        a.expert_stride = (int64_t)F * H;
+        a.err = ws_error_word(ws);
+        const int64_t tiles = (int64_t)E * a.m_tiles * a.n_tiles;
+        st = (bn == 256) ? gg::launch<Op::WGRAD_DOWN, 256>(tA, tB, tB, a, tiles, s)
+                         : gg::launch<Op::WGRAD_DOWN, 128>(tA, tB, tB, a, tiles, s);
+        if (st != MOE_OK) return st;
+    }
+    {   // [dW_gate | dW_up][e] [H, 2F] = x_e^T [dg | du]_e: A = x_perm (MN-major), B = dgu (MN-major)
+        CUtensorMap tA, tB;
+        if (!tmap_bf16_2d(&tA, x_perm, H, rows, H, 64, 64) ||
+            !tmap_bf16_2d(&tB, dgu, 2 * (uint64_t)F, rows, 2 * (uint64_t)F, 64, 64))
+            return MOE_ERR_UNSUPPORTED;
+        gg::Args a{};
+        a.group_offsets = group_offsets;
+        a.E = E;
+        a.M = H;
+        a.N = 2 * F;
+        a.n_split = F;
+        a.m_tiles = H / gg::BM;
+        a.n_tiles = 2 * F / 256;
+        a.rows_cap = rows_cap;
+        a.out_f32 = dW_gate;
+        a.ld0 = F;
+        a.out1_f32 = dW_up;
+        a.ld1 = F;
+        a.expert_stride = (int64_t)H * F;
+        a.err = ws_error_word(ws);
+        const int64_t tiles = (int64_t)E * a.m_tiles * a.n_tiles;
+        return gg::launch<Op::WGRAD_GATEUP, 256>(tA, tB, tB, a, tiles, s);
+    }
+}
+
+extern "C" moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *dst_of_route, int64_t T, int H, int k,
+                                          moe_bf16_t *dx, moe_stream_t stream) {
+    if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
+    if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!dx_perm || !dst_of_route || !dx) return MOE_ERR_INVALID_ARG;
+    return cuda_status(combine_rows(dx_perm, dst_of_route, nullptr, T, H, k, dx, (cudaStream_t)stream));
+}
+
+extern "C" moe_status_t moe_grouped_ffn_bwd(
+    const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
+    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const float *y_perm,
+    const int32_t *dst_of_route, const int32_t *group_sizes, const int32_t *group_offsets, const float *topk_w,
+    int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm, moe_bf16_t *dgu,
+    float *dx_perm, moe_bf16_t *dx, float *dW_gate, float *dW_up, float *dW_down, float *d_topk_w, void *ws,
+    size_t ws_bytes, moe_stream_t stream) {
+    moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
+    if (st != MOE_OK) return st;
+    st = moe_combine_bwd(dY, y_perm, dst_of_route, topk_w, group_sizes, group_offsets, T, H, E, k, rows_cap,
+                         dy_perm, d_topk_w, stream);
+    if (st != MOE_OK) return st;
+    if (rows_cap > 0) {
+        st = moe_grouped_dgrad_fc2_dswiglu(dy_perm, W_down, fc1_c, group_offsets, E, H, F, rows_cap, dgu, ws,
+                                           ws_bytes, stream);
+        if (st != MOE_OK) return st;
+        st = moe_grouped_dgrad_fc1(dgu, W_gate, W_up, group_offsets, E, H, F, rows_cap, dx_perm, ws, ws_bytes,
+                                   stream);
+        if (st != MOE_OK) return st;
+    }
+    st = moe_grouped_wgrad(x_perm, h, dy_perm, dgu, group_offsets, E, H, F, rows_cap, dW_gate, dW_up, dW_down, ws,
+                           ws_bytes, stream);
+    if (st != MOE_OK) return st;
+    return moe_unpermute_sum(dx_perm, dst_of_route, T, H, k, dx, stream);
+}

@@ -55,10 +55,11 @@ struct Args {
     int k_split;      // DGRAD_FC1: K index where B switches from W_gate to W_up (= F)
     int n_split;      // WGRAD_GATEUP: column where output switches from out0 to out1 (= F)
     int64_t rows_cap; // rows of the permuted tensors
-    __nv_bfloat16 *out0;
-    float *out_f32;        // FC2: the fp32 expert output y_perm (row pitch ld0)
+    __nv_bfloat16 *out0;   // FC1: h; DSWIGLU: [dg | du]
+    float *out_f32;        // FC2: y_perm; DGRAD_FC1: dx_perm; WGRAD: dW_down / dW_gate (row pitch ld0)
     int64_t ld0;
-    __nv_bfloat16 *out1;   // FC1: fc1_c stash (nullable); WGRAD_GATEUP: dW_up
+    __nv_bfloat16 *out1;   // FC1: fc1_c stash (nullable)
+    float *out1_f32;       // WGRAD_GATEUP: dW_up (row pitch ld1)
     int64_t ld1;
     const __nv_bfloat16 *aux;   // DSWIGLU: fc1_c
     int64_t ld_aux;
@@ -389,16 +390,15 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const size_t eoff = (size_t)tl.e * (size_t)args.expert_stride;
                 if (tl.kb == 0) {
                     // expert with no routes: its weight gradient is exactly zero
-                    float z[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) z[i] = 0.0f;
                     for (int c = 0; c < BN; c += 32) {
                         const int n = tl.n0 + c;
                         if (n >= args.N) break;
-                        if (OP == Op::WGRAD_GATEUP && n >= args.n_split)
-                            store_bf16x32(args.out1 + eoff + (size_t)row * args.ld1 + (n - args.n_split), z);
-                        else
-                            store_bf16x32(args.out0 + eoff + (size_t)row * args.ld0 + n, z);
+                        float *dst = (OP == Op::WGRAD_GATEUP && n >= args.n_split)
+                                         ? args.out1_f32 + eoff + (size_t)row * args.ld1 + (n - args.n_split)
+                                         : args.out_f32 + eoff + (size_t)row * args.ld0 + n;
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) d4[q] = make_uint4(0, 0, 0, 0);
                     }
                     continue;
                 }
@@ -457,7 +457,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         store_bf16x32(args.out0 + row * args.ld0 + args.N + n, du);
                     }
                 }
-            } else if constexpr (TR::k_grouped) {
+            } else if constexpr (TR::k_grouped) {   // fp32 weight gradient of expert e
                 const int row = tl.m0 + r;
                 const size_t eoff = (size_t)tl.e * (size_t)args.expert_stride;
 #pragma unroll 1
@@ -467,16 +467,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     sm100::tmem_ld_wait();
                     const int n = tl.n0 + c;
                     if (n < args.N) {
-                        float v[32];
+                        float *dst = (OP == Op::WGRAD_GATEUP && n >= args.n_split)
+                                         ? args.out1_f32 + eoff + (size_t)row * args.ld1 + (n - args.n_split)
+                                         : args.out_f32 + eoff + (size_t)row * args.ld0 + n;
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(d[i]);
-                        if (OP == Op::WGRAD_GATEUP && n >= args.n_split)
-                            store_bf16x32(args.out1 + eoff + (size_t)row * args.ld1 + (n - args.n_split), v);
-                        else
-                            store_bf16x32(args.out0 + eoff + (size_t)row * args.ld0 + n, v);
+                        for (int q = 0; q < 8; ++q)
+                            d4[q] = make_uint4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
                     }
                 }
-            } else if constexpr (OP == Op::FC2) {   // fp32 store of the expert output
+            } else {   // FC2 (y_perm) and DGRAD_FC1 (dx_perm): fp32 rows of the group
+                static_assert(OP == Op::FC2 || OP == Op::DGRAD_FC1, "unhandled op");
                 const int64_t row = tl.m0 + r;
                 const bool valid = row < tl.m_end && row < args.rows_cap;
 #pragma unroll 1
@@ -490,22 +491,6 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                         for (int q = 0; q < 8; ++q)
                             dst[q] = make_uint4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
-                    }
-                }
-            } else {   // DGRAD_FC1: plain bf16 store
-                const int64_t row = tl.m0 + r;
-                const bool valid = row < tl.m_end && row < args.rows_cap;
-#pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
-                    uint32_t d[32];
-                    sm100::tmem_ld32(tacc + c, d);
-                    sm100::tmem_ld_wait();
-                    const int n = tl.n0 + c;
-                    if (valid && n < args.N) {
-                        float v[32];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(d[i]);
-                        store_bf16x32(args.out0 + row * args.ld0 + n, v);
                     }
                 }
             }

@@ -33,23 +33,28 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E,
     const int64_t w0 = chunk0 + (int64_t)warp * 32 * kPermSteps;
     int32_t *cnt = s_cnt + warp * E;
     const unsigned lt_mask = (1u << lane) - 1u;
+    // all of this warp's route ids first (independent loads), then the ranks from registers
+    int ev[kPermSteps], rk[kPermSteps];
+#pragma unroll
     for (int step = 0; step < kPermSteps; ++step) {
         const int64_t r = w0 + step * 32 + lane;
-        int e = -1;
-        if (r < R) {
-            e = topk_idx[r];
-            if (e < -1 || e >= E) {
-                raise_device_error(err, MOE_DEVERR_BAD_EXPERT_ID);
-                e = -1;
-            }
+        ev[step] = r < R ? __ldg(topk_idx + r) : -1;
+    }
+#pragma unroll
+    for (int step = 0; step < kPermSteps; ++step) {
+        int e = ev[step];
+        if (e < -1 || e >= E) {
+            raise_device_error(err, MOE_DEVERR_BAD_EXPERT_ID);
+            e = -1;
         }
+        ev[step] = e;
         const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
         int rank = -1;
         if (e >= 0) rank = cnt[e] + __popc(peers & lt_mask);
         __syncwarp();
         if (e >= 0 && (peers & lt_mask) == 0) cnt[e] += __popc(peers);   // leader of the peer group
         __syncwarp();
-        if (r < R) local_rank[r] = rank;
+        rk[step] = rank;
     }
     __syncthreads();
     // exclusive scan over warps per expert -> rank offset of each warp; chunk totals
@@ -64,15 +69,10 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E,
     }
     __syncthreads();
     // add the warp offsets to this chunk's ranks
+#pragma unroll
     for (int step = 0; step < kPermSteps; ++step) {
         const int64_t r = w0 + step * 32 + lane;
-        if (r < R) {
-            int rank = local_rank[r];
-            if (rank >= 0) {
-                int e = topk_idx[r];
-                local_rank[r] = rank + s_cnt[warp * E + e];
-            }
-        }
+        if (r < R) local_rank[r] = rk[step] >= 0 ? rk[step] + s_cnt[warp * E + ev[step]] : -1;
     }
 }
 

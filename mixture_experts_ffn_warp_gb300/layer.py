@@ -10,8 +10,10 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import (Permutation, Workspace, moe_grouped_fc1_swiglu, moe_grouped_fc2, moe_permute,
-                       moe_route_topk, moe_unpermute_combine, rows_capacity)
+from ._binding import (Permutation, Workspace, moe_combine_bwd, moe_grouped_dgrad_fc1,
+                       moe_grouped_dgrad_fc2_dswiglu, moe_grouped_fc1_swiglu, moe_grouped_fc2,
+                       moe_grouped_wgrad, moe_permute, moe_route_topk, moe_unpermute_combine,
+                       moe_unpermute_sum, rows_capacity)
 
 
 class MoeForward:
@@ -74,3 +76,54 @@ def moe_forward(x, logits, W_gate, W_up, W_down, k: int, align: int = 1, keep_fc
     E, _, F = W_gate.shape
     m = MoeForward(T, H, F, E, k, x.device, align, keep_fc1_c)
     return m(x, logits, W_gate, W_up, W_down), m
+
+
+class MoeBackward:
+    """Pre-allocated backward for a MoeForward built with keep_fc1_c=True.
+
+    Produces dx (bf16), fp32 dW_gate / dW_up / dW_down and fp32 d_topk_w,
+    following the backward contract of "Add MoE + expert-parallel Python API
+    surface, PyTorch reference, and tests" (FP32 weight and route gradients)."""
+
+    def __init__(self, fwd: MoeForward, want_d_topk_w: bool = True):
+        if fwd.fc1_c is None:
+            raise ValueError("the forward must keep the fc1_c stash (keep_fc1_c=True)")
+        self.fwd = fwd
+        T, H, F, E, k, dev, cap = fwd.T, fwd.H, fwd.F, fwd.E, fwd.k, fwd.device, fwd.rows_cap
+        self.dy_perm = torch.empty(cap, H, dtype=torch.bfloat16, device=dev)
+        self.dgu = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev)
+        self.dx_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
+        self.dx = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.dW_gate = torch.empty(E, H, F, dtype=torch.float32, device=dev)
+        self.dW_up = torch.empty(E, H, F, dtype=torch.float32, device=dev)
+        self.dW_down = torch.empty(E, F, H, dtype=torch.float32, device=dev)
+        self.d_topk_w = torch.empty(T, k, dtype=torch.float32, device=dev) if want_d_topk_w else None
+
+    def combine_bwd(self, dY, stream=None):
+        f = self.fwd
+        moe_combine_bwd(dY, f.y_perm, f.perm, f.topk_w, self.dy_perm, self.d_topk_w, stream=stream)
+
+    def dgrad_fc2(self, W_down, stream=None):
+        f = self.fwd
+        moe_grouped_dgrad_fc2_dswiglu(self.dy_perm, W_down, f.fc1_c, f.perm.group_offsets, f.ws, self.dgu,
+                                      stream=stream)
+
+    def dgrad_fc1(self, W_gate, W_up, stream=None):
+        f = self.fwd
+        moe_grouped_dgrad_fc1(self.dgu, W_gate, W_up, f.perm.group_offsets, f.ws, self.dx_perm, stream=stream)
+
+    def wgrad(self, stream=None):
+        f = self.fwd
+        moe_grouped_wgrad(f.perm.x_perm, f.h, self.dy_perm, self.dgu, f.perm.group_offsets, f.ws, self.dW_gate,
+                          self.dW_up, self.dW_down, stream=stream)
+
+    def unpermute_sum(self, stream=None):
+        moe_unpermute_sum(self.dx_perm, self.fwd.perm.dst_of_route, self.dx, stream=stream)
+
+    def __call__(self, dY, W_gate, W_up, W_down, stream=None):
+        self.combine_bwd(dY, stream)
+        self.dgrad_fc2(W_down, stream)
+        self.dgrad_fc1(W_gate, W_up, stream)
+        self.wgrad(stream)
+        self.unpermute_sum(stream)
+        return self.dx

@@ -25,11 +25,12 @@
  *     (same cudnn-frontend page, BlockScaledTensor: block_size 32 for mxfp8).
  *
  * Arithmetic is double.  round_mode = 1 rounds to bf16 exactly where the
- * GPU path stores a bf16 tensor (h, out, dy_perm, dg/du, dx_perm, dx, dW; the
- * expert output y is stored in fp32 by the path and is not rounded here);
+ * GPU path stores a bf16 tensor (h, out, dy_perm, dg/du, dx; the expert output
+ * y, dx_perm and the weight gradients are fp32 on the path and are not
+ * rounded here);
  * round_mode = 0 keeps every intermediate in double (used to pin the
  * formulas against fp64 autograd); round_mode = 2 rounds the stored
- * intermediates (h, dy_perm, dg/du, dx_perm) but returns the final
+ * intermediates (h, dy_perm, dg/du) but returns the final
  * outputs (out, dx, dW) unrounded, so that a bf16 output of the GPU can be
  * compared with the exact value of the same arithmetic.  Readings of points the pages leave open
  * (tie-break, NaN order, MX scale rule) are stated at each function.
@@ -442,7 +443,7 @@ void oracle_moe_fwd_mxfp8(int64_t n_tokens, const int64_t *tokens, int H, int F,
  *   with G, U = the fc1_c stash (bf16 of g, u) in round_mode 1, else g, u:
  *   dg    = dh * U * s * (1 + G * (1 - s)),  s = sigmoid(G)   (bf16 in mode 1)
  *   du    = dh * G * s                                      (bf16 in mode 1)
- *   dxr   = dg Wg^T + du Wu^T                       (bf16 in round_mode 1)
+ *   dxr   = dg Wg^T + du Wu^T                       (unrounded: fp32 on the path)
  * g, u, h are the forward values of the route. */
 static void route_bwd(const uint16_t *dYt, double w, const double *g, const double *u,
                       const uint16_t *Wg, const uint16_t *Wu, const uint16_t *Wd,
@@ -465,7 +466,7 @@ static void route_bwd(const uint16_t *dYt, double w, const double *g, const doub
         double s = 0.0;
         for (int f = 0; f < F; ++f)
             s += dg[f] * oracle_bf16_to_double(wg[f]) + du[f] * oracle_bf16_to_double(wu[f]);
-        dxr[i] = rnd(s, round_mode);
+        dxr[i] = s;
     }
 }
 
@@ -512,13 +513,7 @@ void oracle_moe_bwd(int64_t T, int H, int F, int E, int k, const uint16_t *x,
         for (int n = 0; n < H; ++n) dx[t * H + n] = rnd_out(acc[n], round_mode);
     }
     free(g);
-    if (round_mode == 1) {
-        for (int64_t i = 0; i < (int64_t)E * H * F; ++i) {
-            dWg[i] = bf(dWg[i]);
-            dWu[i] = bf(dWu[i]);
-            dWd[i] = bf(dWd[i]);
-        }
-    }
+    /* the weight gradients are fp32 on the path: no bf16 rounding in any mode */
 }
 
 /* dx and d_topk_w for a list of tokens (any problem size): dx[i] (double
@@ -597,7 +592,7 @@ void oracle_moe_bwd_dw_entries(int64_t n_entries, const int32_t *which, const in
                 acc += oracle_bf16_to_double(xr[hn]) * d;
             }
         }
-        val[q] = rnd_out(acc, round_mode);
+        val[q] = acc;   /* fp32 on the path: not rounded */
     }
 }
 

@@ -442,8 +442,8 @@ def test_sampled_backward_functions_agree_with_full():
     ents = [(0, 1, 3, 4), (1, 2, 0, 31), (2, 3, 7, 9), (2, 0, 31, 0)]
     vals = oracle.moe_bwd_dw_entries(ents, b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, b["dY"])
     ref = [full["dW_gate"][1, 3, 4], full["dW_up"][2, 0, 31], full["dW_down"][3, 7, 9], full["dW_down"][0, 31, 0]]
-    # same definition, summed in a different order: equal to double precision before rounding
-    assert np.allclose(vals, ref, rtol=2.0 ** -7, atol=0)
+    # same definition, summed in a different order
+    assert np.allclose(vals, ref, rtol=1e-12, atol=0)
 
 
 # ------------------------------------------------------------ A7 MXFP8 forward
@@ -513,5 +513,6 @@ def test_round_mode_2_is_mode_1_before_the_final_rounding():
     assert not np.array_equal(f2["out"], f1["out"])
     g1 = oracle.moe_bwd(b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, b["dY"], round_mode=1)
     g2 = oracle.moe_bwd(b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, b["dY"], round_mode=2)
-    for n in ("dx", "dW_gate", "dW_up", "dW_down"):
-        assert np.array_equal(oracle.round_bf16(g2[n]), g1[n]), n
+    assert np.array_equal(oracle.round_bf16(g2["dx"]), g1["dx"])
+    for n in ("dW_gate", "dW_up", "dW_down"):                   # fp32 on the path: never rounded
+        assert np.array_equal(g2[n], g1[n]), n
