@@ -247,6 +247,83 @@ MOE_API moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *d
                                    moe_bf16_t *out, moe_stream_t stream);
 
 /* ------------------------------------------------------------------ */
+/* A6 + A7  MXFP8 path                                                  */
+/* ------------------------------------------------------------------ */
+
+/* MXFP8 = E4M3 elements with one UE8M0 scale per 32 consecutive elements along
+ * the contraction dimension K ("Add MoE + expert-parallel Python API surface,
+ * PyTorch reference, and tests", BlockScaledTensor: block size 32 for mxfp8;
+ * "MoE training optimization": grouped MXFP8 quantize and grouped GEMM).
+ * Scale of a block with maximum magnitude amax: the smallest 2^X with
+ * amax / 2^X <= 448 (X = floor(log2 amax) - 8, +1 when amax's significand
+ * exceeds 1.75), clamped to [-127, 127], stored as X + 127 (amax = 0 -> 0).
+ * Elements: v / 2^X rounded to nearest even onto E4M3, saturated to +-448.
+ *
+ * Scale layouts:
+ *   row-major    uint8 [rows][K/32]
+ *   tile layout  the block-scaled MMA's operand layout.  Rows are cut into
+ *                128-row tiles per group (tile ids run over the groups in
+ *                order, ceil(rows_g / 128) tiles per group); each tile has one
+ *                512-byte atom per 128 K elements, atoms ordered [tile][K/128],
+ *                byte (m % 32) * 16 + (m / 32) * 4 + (kb % 4) for tile row m
+ *                and 32-block kb.  Size: moe_mx_tile_scale_bytes(rows_cap, E, K).
+ *   weights      [E][K/128][N/128] atoms of the same form, m = n % 128. */
+MOE_API size_t moe_mx_tile_scale_bytes(int64_t rows_cap, int E, int K);
+
+/* A6: quantise rows of a bf16 [rows, K] matrix along K.  data: uint8
+ * [rows, K] out.  scale_rowmajor (nullable): [rows][K/32] out.  scale_tiles
+ * (nullable): tile-layout scales of the groups given by group_offsets [G+1]
+ * (required with scale_tiles; ws must then hold 256 + 4*(G+1) bytes).  At
+ * least one scale output.  Limits: K % 128 == 0, G <= 1024. */
+MOE_API moe_status_t moe_grouped_quantize_mxfp8(const moe_bf16_t *in, int64_t rows, int K,
+                                                const int32_t *group_offsets, int G, uint8_t *data,
+                                                uint8_t *scale_rowmajor, uint8_t *scale_tiles, void *ws,
+                                                size_t ws_bytes, moe_stream_t stream);
+
+/* Quantise expert weights W bf16 [E, K, N] (N contiguous) along K: data uint8
+ * [E, N, K] (K contiguous, the K-major operand of the MMA), scales in the
+ * weights' tile layout ([E][K/128][N/128] atoms, E*K*N/32 bytes).  For
+ * W_gate / W_up pass K = H, N = F; for W_down K = F, N = H.  Limits:
+ * K % 128 == 0, N % 128 == 0. */
+MOE_API moe_status_t moe_quantize_weights_mxfp8(const moe_bf16_t *W, int E, int K, int N, uint8_t *data,
+                                                uint8_t *scales, moe_stream_t stream);
+
+/* moe_permute with the rows quantised to MXFP8 on the way (each token row is
+ * read once): x_q uint8 [rows_cap, H] out (row dst_of_route[r] holds the
+ * E4M3 codes of x[r / k]), x_sf tile-layout scales out
+ * (moe_mx_tile_scale_bytes(rows_cap, E, H) bytes).  Other arguments and
+ * outputs as moe_permute with align = 1.  Limits: H % 128 == 0. */
+MOE_API moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *topk_idx, int64_t T, int H, int E,
+                                       int k, uint8_t *x_q, uint8_t *x_sf, int64_t rows_cap,
+                                       int32_t *dst_of_route, int32_t *src_of_row, int32_t *group_sizes,
+                                       int32_t *group_offsets, void *ws, size_t ws_bytes, moe_stream_t stream);
+
+/* A7: the grouped FFN on MXFP8 operands with block-scaled tcgen05 MMAs, fp32
+ * accumulation:
+ *   h = silu(x W_gate) * (x W_up) (fp32), quantised to MXFP8 along F:
+ *       h_q uint8 [rows_cap, F], h_sf tile layout (moe_mx_tile_scale_bytes(rows_cap, E, F))
+ *   y_perm = h W_down, fp32 [rows_cap, H]
+ * x_q / x_sf from moe_permute_mxfp8; Wg_q, Wu_q uint8 [E, F, H] and Wd_q
+ * uint8 [E, H, F] with scales from moe_quantize_weights_mxfp8.  All scale
+ * pointers 16-byte aligned.  Limits: H % 128 == 0, F % 128 == 0, E <= 1024.
+ * moe_grouped_fc1_swiglu_mxfp8 and moe_grouped_fc2_mxfp8 are the two halves. */
+MOE_API moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,
+                                               const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,
+                                               const uint8_t *Wd_q, const uint8_t *Wd_sf,
+                                               const int32_t *group_offsets, int E, int H, int F,
+                                               int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf, float *y_perm,
+                                               void *ws, size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,
+                                                  const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,
+                                                  const int32_t *group_offsets, int E, int H, int F,
+                                                  int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf, void *ws,
+                                                  size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
+                                           const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H, int F,
+                                           int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
+                                           moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
 /* A8  Backward                                                         */
 /* ------------------------------------------------------------------ */
 

@@ -12,4 +12,8 @@ from ._binding import (  # noqa: F401
     moe_combine_bwd, moe_grouped_dgrad_fc1, moe_grouped_dgrad_fc2_dswiglu, moe_grouped_ffn_bwd,
     moe_grouped_wgrad, moe_unpermute_sum,
 )
-from .layer import MoeBackward, MoeForward, moe_forward  # noqa: F401
+from ._binding import (  # noqa: F401
+    PermutationMX, moe_grouped_fc1_swiglu_mxfp8, moe_grouped_fc2_mxfp8, moe_grouped_quantize_mxfp8,
+    moe_permute_mxfp8, moe_quantize_weights_mxfp8, mx_tile_scale_bytes,
+)
+from .layer import MoeBackward, MoeForward, MoeForwardMX, MxWeights, moe_forward  # noqa: F401

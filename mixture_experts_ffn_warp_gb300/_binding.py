@@ -50,6 +50,14 @@ SIGNATURES = {
     "moe_grouped_dgrad_fc1": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_grouped_wgrad": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_unpermute_sum": (_st, [_vp, _vp, _i64, _int, _int, _vp, _vp]),
+    "moe_mx_tile_scale_bytes": (_sz, [_i64, _int, _int]),
+    "moe_grouped_quantize_mxfp8": (_st, [_vp, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_quantize_weights_mxfp8": (_st, [_vp, _int, _int, _int, _vp, _vp, _vp]),
+    "moe_permute_mxfp8": (_st, [_vp, _vp, _i64, _int, _int, _int, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _sz,
+                                _vp]),
+    "moe_grouped_ffn_fwd_mxfp8": (_st, [_vp] * 9 + [_int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_grouped_fc1_swiglu_mxfp8": (_st, [_vp] * 7 + [_int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "moe_grouped_fc2_mxfp8": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -346,3 +354,95 @@ def moe_grouped_ffn_bwd(dY, x_perm, W_gate, W_up, W_down, fc1_c, h, y_perm, perm
         T, H, F, E, k, cap, _ptr(dy_perm), _ptr(dgu), _ptr(dx_perm), _ptr(out["dx"]), _ptr(out["dW_gate"]),
         _ptr(out["dW_up"]), _ptr(out["dW_down"]), _ptr(out["d_topk_w"]), _ptr(ws.buf), ws.nbytes, _stream(stream)))
     return out
+
+
+# ------------------------------------------------------------------ A6 + A7 MXFP8
+
+def mx_tile_scale_bytes(rows_cap: int, E: int, K: int) -> int:
+    return int(load_library().moe_mx_tile_scale_bytes(rows_cap, E, K))
+
+
+def moe_grouped_quantize_mxfp8(x: torch.Tensor, group_offsets=None, ws: Workspace | None = None,
+                               rowmajor: bool = True, tiles: bool = False, stream=None):
+    """MXFP8 of each row of a bf16 [rows, K] matrix along K (moe.h).  Returns
+    (data uint8 [rows, K], row-major scales [rows, K/32] or None, tile-layout
+    scales or None)."""
+    _need(x, "x", torch.bfloat16)
+    rows, K = x.shape
+    dev = x.device
+    data = torch.empty(rows, K, dtype=torch.uint8, device=dev)
+    srm = torch.empty(rows, K // 32, dtype=torch.uint8, device=dev) if rowmajor else None
+    stl = None
+    G = 0
+    if tiles:
+        G = group_offsets.shape[0] - 1
+        stl = torch.zeros(mx_tile_scale_bytes(rows, G, K), dtype=torch.uint8, device=dev)
+    _check("moe_grouped_quantize_mxfp8", load_library().moe_grouped_quantize_mxfp8(
+        _ptr(x), rows, K, _ptr(group_offsets), G, _ptr(data), _ptr(srm), _ptr(stl),
+        _ptr(ws.buf) if ws is not None else None, ws.nbytes if ws is not None else 0, _stream(stream)))
+    return data, srm, stl
+
+
+def moe_quantize_weights_mxfp8(W: torch.Tensor, stream=None):
+    """MXFP8 of expert weights [E, K, N] along K -> (data uint8 [E, N, K],
+    scales in the weights' tile layout, uint8 [E*K*N/32]) (moe.h)."""
+    _need(W, "W", torch.bfloat16)
+    E, K, N = W.shape
+    data = torch.empty(E, N, K, dtype=torch.uint8, device=W.device)
+    scales = torch.empty(E * K * N // 32, dtype=torch.uint8, device=W.device)
+    _check("moe_quantize_weights_mxfp8", load_library().moe_quantize_weights_mxfp8(
+        _ptr(W), E, K, N, _ptr(data), _ptr(scales), _stream(stream)))
+    return data, scales
+
+
+@dataclass
+class PermutationMX:
+    x_q: torch.Tensor           # [rows_cap, H] uint8 (E4M3)
+    x_sf: torch.Tensor          # tile-layout scales, uint8
+    dst_of_route: torch.Tensor
+    src_of_row: torch.Tensor
+    group_sizes: torch.Tensor
+    group_offsets: torch.Tensor
+    rows_cap: int
+
+
+def moe_permute_mxfp8(x: torch.Tensor, topk_idx: torch.Tensor, E: int, ws: Workspace,
+                      out: PermutationMX | None = None, stream=None) -> PermutationMX:
+    """Permutation with the rows quantised to MXFP8 on the way (moe.h)."""
+    _need(x, "x", torch.bfloat16)
+    T, H = x.shape
+    k = topk_idx.shape[1]
+    cap = T * k
+    if out is None:
+        dev = x.device
+        out = PermutationMX(
+            x_q=torch.empty(cap, H, dtype=torch.uint8, device=dev),
+            x_sf=torch.zeros(mx_tile_scale_bytes(cap, E, H), dtype=torch.uint8, device=dev),
+            dst_of_route=torch.empty(T, k, dtype=torch.int32, device=dev),
+            src_of_row=torch.empty(cap, dtype=torch.int32, device=dev),
+            group_sizes=torch.empty(E, dtype=torch.int32, device=dev),
+            group_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev), rows_cap=cap)
+    _check("moe_permute_mxfp8", load_library().moe_permute_mxfp8(
+        _ptr(x), _ptr(topk_idx), T, H, E, k, _ptr(out.x_q), _ptr(out.x_sf), out.rows_cap, _ptr(out.dst_of_route),
+        _ptr(out.src_of_row), _ptr(out.group_sizes), _ptr(out.group_offsets), _ptr(ws.buf), ws.nbytes,
+        _stream(stream)))
+    return out
+
+
+def moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, ws: Workspace, h_q, h_sf,
+                                 stream=None):
+    """A3 on MXFP8 operands; h quantised to MXFP8 along F (moe.h)."""
+    rows_cap, H = x_q.shape
+    E, F, _ = Wg_q.shape
+    _check("moe_grouped_fc1_swiglu_mxfp8", load_library().moe_grouped_fc1_swiglu_mxfp8(
+        _ptr(x_q), _ptr(x_sf), _ptr(Wg_q), _ptr(Wg_sf), _ptr(Wu_q), _ptr(Wu_sf), _ptr(group_offsets), E, H, F,
+        rows_cap, _ptr(h_q), _ptr(h_sf), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+
+
+def moe_grouped_fc2_mxfp8(h_q, h_sf, Wd_q, Wd_sf, group_offsets, ws: Workspace, y_perm, stream=None):
+    """A4 on MXFP8 operands, fp32 output (moe.h)."""
+    rows_cap, F = h_q.shape
+    E, H, _ = Wd_q.shape
+    _check("moe_grouped_fc2_mxfp8", load_library().moe_grouped_fc2_mxfp8(
+        _ptr(h_q), _ptr(h_sf), _ptr(Wd_q), _ptr(Wd_sf), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
+        _ptr(ws.buf), ws.nbytes, _stream(stream)))

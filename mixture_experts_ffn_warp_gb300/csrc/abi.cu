@@ -31,7 +31,12 @@ int moe_abi_version(void) { return 1; }
 size_t moe_workspace_bytes(int64_t T, int E, int k) {
     if (T < 0 || E < 1 || E > 1024 || k < 1 || k > 32) return 0;
     int64_t chunks = moe::perm_chunks(T * (int64_t)k);
-    return moe::kWsHeaderBytes + (size_t)chunks * (size_t)E * sizeof(int32_t);
+    return moe::kWsHeaderBytes + moe::ws_counts_bytes(chunks, E) + moe::ws_mtile_bytes(E);
+}
+
+size_t moe_mx_tile_scale_bytes(int64_t rows_cap, int E, int K) {
+    if (rows_cap < 0 || E < 1 || K < 128 || K % 128 != 0) return 0;
+    return (size_t)((rows_cap + 127) / 128 + E) * (size_t)(K / 128) * 512;
 }
 
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {

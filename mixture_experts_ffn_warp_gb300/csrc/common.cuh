@@ -20,6 +20,16 @@ constexpr int kPermChunk = kPermWarps * 32 * kPermSteps;   // 8192 routes
 
 inline int64_t perm_chunks(int64_t R) { return (R + kPermChunk - 1) / kPermChunk; }
 
+// Workspace layout after the header: per-chunk expert counts, then (for the
+// MXFP8 path) each group's first 128-row M-tile id, [E+1] int32.
+inline size_t ws_counts_bytes(int64_t chunks, int E) {
+    return ((size_t)chunks * (size_t)E * sizeof(int32_t) + 15) / 16 * 16;
+}
+inline size_t ws_mtile_bytes(int E) { return ((size_t)(E + 1) * sizeof(int32_t) + 15) / 16 * 16; }
+
+// mtile_start[g] = sum over g' < g of ceil(rows(g') / 128) from group offsets (one block, G <= 1024).
+__global__ void mtile_prefix_kernel(const int32_t *__restrict__ group_offsets, int G, int32_t *__restrict__ mtile_start);
+
 inline uint32_t *ws_error_word(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
 
 inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }

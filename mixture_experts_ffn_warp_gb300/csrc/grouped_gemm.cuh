@@ -1,36 +1,43 @@
 // grouped_gemm.cuh -- persistent, warp-specialised grouped GEMM on tcgen05 for the
-// expert FFN (forward and backward).
+// expert FFN (forward, backward and the MXFP8 forward).
 //
 // One CTA per SM, 6 warps:
-//   warp 0      TMA producer (one lane): A and B tiles -> a ring of smem stages
-//   warp 1      MMA issuer (lane 0 issues tcgen05.mma, M=128 x N=BN x K=16);
-//               fp32 accumulators live in TMEM, double-buffered
-//   warps 2..5  epilogue: tcgen05.ld -> fused activation -> bf16 stores
+//   warp 0      TMA producer (one lane): A and B tiles (and, for MXFP8, their
+//               block scales) -> a ring of smem stages
+//   warp 1      MMA issuer (lane 0 issues tcgen05.mma, M=128 x N=BN; K=16 per
+//               instruction for bf16, K=32 for E4M3); fp32 accumulators live in
+//               TMEM (double-buffered for bf16, single for MXFP8, whose scales
+//               take the other half of TMEM)
+//   warps 2..5  epilogue: tcgen05.ld -> fused activation -> stores
 // Tiles are scheduled on the device from group_offsets (no host round trip).
 //
 // Ops (A row = one permuted route unless stated):
 //   FC1_SWIGLU     h = silu(x W_gate) * (x W_up)        M-grouped, K = H
-//   FC2            y = h W_down                         M-grouped, K = F
+//   FC2            y = h W_down (fp32 out)              M-grouped, K = F
 //   DGRAD_DSWIGLU  dh = dy W_down^T, then dSwiGLU       M-grouped, K = H
-//   DGRAD_FC1      dx = dg W_gate^T + du W_up^T          M-grouped, K = 2F
-//   WGRAD_DOWN     dW_down[e] = h_e^T dy_e              K-grouped (K = rows of e)
+//   DGRAD_FC1      dx = dg W_gate^T + du W_up^T (fp32)   M-grouped, K = 2F
+//   WGRAD_DOWN     dW_down[e] = h_e^T dy_e (fp32)        K-grouped (K = rows of e)
 //   WGRAD_GATEUP   [dW_gate|dW_up][e] = x_e^T [dg|du]_e K-grouped
+//   FC1_MX         FC1_SWIGLU on MXFP8 operands; h is quantised to MXFP8 (along F)
+//                  in the epilogue, scales written in the MMA tile layout
+//   FC2_MX         FC2 on MXFP8 operands (fp32 out)
 // ("Add MoE + expert-parallel Python API surface, PyTorch reference, and
-// tests", Summary: SwiGLU experts, fc1_c stash, backward; "[Draft][JAX] MoE
-// block optimization": fused grouped GEMM + SwiGLU and grouped_gemm_dswiglu;
-// "[JAX] Expert Parallelism": zero wgrad for experts with no tokens.)
+// tests", Summary: SwiGLU experts, fc1_c stash, backward, MXFP8 operands;
+// "[Draft][JAX] MoE block optimization": fused grouped GEMM + SwiGLU and
+// grouped_gemm_dswiglu; "[JAX] Expert Parallelism": zero wgrad for experts
+// with no tokens; "MoE training optimization": MXFP8 grouped GEMM.)
 #pragma once
 
 #include "common.cuh"
+#include "mx.cuh"
 #include "sm100.cuh"
 
 namespace moe {
 namespace gg {
 
-enum class Op : int { FC1_SWIGLU, FC2, DGRAD_DSWIGLU, DGRAD_FC1, WGRAD_DOWN, WGRAD_GATEUP };
+enum class Op : int { FC1_SWIGLU, FC2, DGRAD_DSWIGLU, DGRAD_FC1, WGRAD_DOWN, WGRAD_GATEUP, FC1_MX, FC2_MX };
 
 constexpr int BM = 128;
-constexpr int BK = 64;             // bf16 K elements per stage (one 128-byte swizzle row)
 constexpr int UMMA_K = 16;
 constexpr int kThreads = 192;
 constexpr int kMaxE = 1024;
@@ -38,10 +45,13 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 template <Op OP>
 struct Traits {
+    static constexpr bool mx = (OP == Op::FC1_MX || OP == Op::FC2_MX);
     static constexpr bool k_grouped = (OP == Op::WGRAD_DOWN || OP == Op::WGRAD_GATEUP);
     static constexpr bool a_mn = k_grouped;                       // A is MN-major only for wgrad
     static constexpr bool b_mn = (OP == Op::FC1_SWIGLU || OP == Op::FC2 || k_grouped);
-    static constexpr bool b_two = (OP == Op::FC1_SWIGLU || OP == Op::DGRAD_FC1);
+    static constexpr bool b_two = (OP == Op::FC1_SWIGLU || OP == Op::DGRAD_FC1 || OP == Op::FC1_MX);
+    static constexpr bool swiglu = (OP == Op::FC1_SWIGLU || OP == Op::FC1_MX);
+    static constexpr int BK = mx ? 128 : 64;   // K elements per stage: one 128-byte swizzle row
 };
 
 struct Args {
@@ -64,19 +74,32 @@ struct Args {
     const __nv_bfloat16 *aux;   // DSWIGLU: fc1_c
     int64_t ld_aux;
     int64_t expert_stride;      // K-grouped: elements between experts' outputs
+    // MXFP8: A scales in tile layout [mtile][K/128][512]; B scales [E][K/128][N_B/128][512]
+    const uint8_t *sfa;
+    const uint8_t *sfb0;
+    const uint8_t *sfb1;
+    int nb_rows;          // MXFP8: rows (N) of each expert's B matrix
+    uint8_t *out_q;       // FC1_MX: quantised h [rows, N] (E4M3)
+    uint8_t *out_sf;      // FC1_MX: h scales in tile layout [mtile][N/128][512]
     uint32_t *err;
 };
 
 template <Op OP, int BN>
 struct Cfg {
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BN * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr bool MX = Traits<OP>::mx;
+    static constexpr int A_BYTES = BM * 128;
+    static constexpr int B_BYTES = BN * 128;
+    static constexpr int SF_BYTES = MX ? 512 + (BN / 128) * 512 : 0;
+    static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + SF_BYTES + 1023) / 1024 * 1024;
     static constexpr int STAGES = (BN == 256) ? 4 : 6;
-    static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+    static constexpr int ACC_BUFS = MX ? 1 : 2;
+    static constexpr int TMEM_COLS = MX ? 512 : ((2 * BN <= 256) ? 256 : 512);
+    static constexpr int SF_COL0 = BN;                          // MXFP8 scale slots after the accumulator
+    static constexpr int SF_COLS = 4 + 4 * (BN / 128);          // per stage: A (4) + B (4 per 128 rows)
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;   // + alignment slack
     // output columns produced per tile
-    static constexpr int OUT_COLS = (OP == Op::FC1_SWIGLU) ? BN / 2 : BN;
+    static constexpr int OUT_COLS = Traits<OP>::swiglu ? BN / 2 : BN;
+    static_assert(!MX || SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM overflow");
 };
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
@@ -108,6 +131,12 @@ __device__ __forceinline__ void load_bf16x32(const __nv_bfloat16 *src, float (&v
     }
 }
 
+__device__ __forceinline__ void store_f32x32(float *dst, const uint32_t (&d)[32]) {
+    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) d4[q] = make_uint4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+}
+
 struct Tile {
     int e;
     int m0;      // M-grouped: first row in the permuted tensor; K-grouped: row in the expert's output
@@ -116,6 +145,7 @@ struct Tile {
     int kb;      // number of K blocks
     int k_row0;  // K-grouped: first permuted row of the group
     int k_rows;  // K-grouped: rows of the group
+    int mtile;   // M-grouped: global 128-row tile id (expert-major), the MXFP8 scale tile
 };
 
 template <Op OP, int BN>
@@ -133,7 +163,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Args &a, const int *s_o
         const int r0 = s_off[tl.e], r1 = s_off[tl.e + 1];
         tl.k_row0 = r0;
         tl.k_rows = r1 > r0 ? r1 - r0 : 0;
-        tl.kb = (tl.k_rows + BK - 1) / BK;
+        tl.kb = (tl.k_rows + TR::BK - 1) / TR::BK;
+        tl.mtile = 0;
     } else {
         // largest e with s_start[e] <= t
         int lo = 0, hi = a.E - 1;
@@ -149,9 +180,10 @@ __device__ __forceinline__ Tile decode_tile(int t, const Args &a, const int *s_o
         tl.m0 = s_off[lo] + mb * BM;
         tl.m_end = s_off[lo + 1];
         tl.n0 = nb * Cfg<OP, BN>::OUT_COLS;
-        tl.kb = (a.K + BK - 1) / BK;
+        tl.kb = (a.K + TR::BK - 1) / TR::BK;
         tl.k_row0 = 0;
         tl.k_rows = 0;
+        tl.mtile = s_start[lo] / a.n_tiles + mb;
     }
     return tl;
 }
@@ -163,6 +195,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     using TR = Traits<OP>;
     using C = Cfg<OP, BN>;
     constexpr int S = C::STAGES;
+    constexpr int NACC = C::ACC_BUFS;
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full_bar[S], empty_bar[S], tfull_bar[2], tempty_bar[2], drain_bar;
@@ -205,21 +238,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // s_start[e] = tiles before expert e (M-grouped: m-blocks x n_tiles)
         const int seg = (E + 31) / 32;
         const int e0 = lane * seg;
-        int sum = 0;
-        for (int i = 0; i < seg; ++i) {
-            const int e = e0 + i;
-            if (e < E) {
-                int tiles;
-                if constexpr (TR::k_grouped) {
-                    tiles = args.m_tiles * args.n_tiles;
-                } else {
-                    int rows = s_off[e + 1] - s_off[e];
-                    if (rows < 0) rows = 0;
-                    tiles = ((rows + BM - 1) / BM) * args.n_tiles;
-                }
-                sum += tiles;
+        auto tiles_of = [&](int e) {
+            if constexpr (TR::k_grouped) {
+                return args.m_tiles * args.n_tiles;
+            } else {
+                int rows = s_off[e + 1] - s_off[e];
+                if (rows < 0) rows = 0;
+                return ((rows + BM - 1) / BM) * args.n_tiles;
             }
-        }
+        };
+        int sum = 0;
+        for (int i = 0; i < seg; ++i)
+            if (e0 + i < E) sum += tiles_of(e0 + i);
         int incl = sum;
 #pragma unroll
         for (int off = 1; off < 32; off <<= 1) {
@@ -228,18 +258,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         int run = incl - sum;
         for (int i = 0; i < seg; ++i) {
-            const int e = e0 + i;
-            if (e < E) {
-                s_start[e] = run;
-                int tiles;
-                if constexpr (TR::k_grouped) {
-                    tiles = args.m_tiles * args.n_tiles;
-                } else {
-                    int rows = s_off[e + 1] - s_off[e];
-                    if (rows < 0) rows = 0;
-                    tiles = ((rows + BM - 1) / BM) * args.n_tiles;
-                }
-                run += tiles;
+            if (e0 + i < E) {
+                s_start[e0 + i] = run;
+                run += tiles_of(e0 + i);
             }
         }
         if (lane == 31) s_start[E] = incl;
@@ -268,9 +289,28 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
                     const uint32_t sb = sa + C::A_BYTES;
                     uint64_t *fb = &full_bar[stage];
-                    sm100::mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-                    const int k0 = kb * BK;
-                    if constexpr (TR::k_grouped) {
+                    sm100::mbar_arrive_expect_tx(fb, C::A_BYTES + C::B_BYTES + C::SF_BYTES);
+                    const int k0 = kb * TR::BK;
+                    if constexpr (TR::mx) {
+                        // E4M3 rows are K-contiguous: A [rows, K], B [E][N_B rows][K]
+                        const uint32_t ssf = sb + C::B_BYTES;
+                        const int kblocks = args.K / 128;
+                        sm100::tma_load_2d(sa, &tmA, fb, k0, tl.m0);
+                        sm100::bulk_load(ssf, args.sfa + ((int64_t)tl.mtile * kblocks + kb) * 512, 512, fb);
+                        const int nblk = args.nb_rows / 128;
+                        const int64_t sfb_atom = ((int64_t)tl.e * kblocks + kb) * nblk;
+                        if constexpr (OP == Op::FC1_MX) {
+                            // 128 gate rows then 128 up rows of the weights, with their scale atoms
+                            sm100::tma_load_3d(sb, &tmB0, fb, k0, tl.n0, tl.e);
+                            sm100::tma_load_3d(sb + 16384, &tmB1, fb, k0, tl.n0, tl.e);
+                            sm100::bulk_load(ssf + 512, args.sfb0 + (sfb_atom + tl.n0 / 128) * 512, 512, fb);
+                            sm100::bulk_load(ssf + 1024, args.sfb1 + (sfb_atom + tl.n0 / 128) * 512, 512, fb);
+                        } else {
+                            sm100::tma_load_3d(sb, &tmB0, fb, k0, tl.n0, tl.e);
+                            sm100::bulk_load(ssf + 512, args.sfb0 + (sfb_atom + tl.n0 / 128) * 512,
+                                             (BN / 128) * 512, fb);
+                        }
+                    } else if constexpr (TR::k_grouped) {
                         const int krow = tl.k_row0 + k0;
                         sm100::tma_load_2d(sa, &tmA, fb, tl.m0, krow);
                         sm100::tma_load_2d(sa + 8192, &tmA, fb, tl.m0 + 64, krow);
@@ -312,7 +352,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
     } else if (warp == 1) {
         // ============================================================ MMA issuer
-        constexpr uint32_t IDESC = sm100::idesc_bf16(BM, BN, TR::a_mn, TR::b_mn);
+        constexpr uint32_t IDESC = TR::mx ? sm100::idesc_mxf8(BM, BN) : sm100::idesc_bf16(BM, BN, TR::a_mn, TR::b_mn);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -333,11 +373,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const uint32_t sb = sa + C::A_BYTES;
                 if constexpr (TR::k_grouped) {
                     // zero the K rows past the group's end (they belong to the next group)
-                    const int valid = tl.k_rows - kb * BK;
-                    if (valid < BK) {
+                    const int valid = tl.k_rows - kb * TR::BK;
+                    if (valid < TR::BK) {
                         uint8_t *pa = smem + stage * C::STAGE_BYTES;
                         const int nbox = 2 + BN / 64;
-                        const int zrows = BK - valid;
+                        const int zrows = TR::BK - valid;
                         for (int i = lane; i < nbox * zrows * 8; i += 32) {
                             const int box = i / (zrows * 8);
                             const int rem = i - box * zrows * 8;
@@ -350,14 +390,32 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 }
                 sm100::tc_fence_after();
                 if (lane == 0) {
+                    if constexpr (TR::mx) {
+                        // scales of this stage: smem atoms -> TMEM slot of the stage, then 4 MMAs of
+                        // K = 32 with scale ids 0..3 (the 4 bytes of each TMEM scale word)
+                        const uint32_t ssf = sb + C::B_BYTES;
+                        const uint32_t tsf = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
+                        sm100::tmem_cp_32x128b_x4(tsf, sm100::sdesc_plain(ssf));
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        uint64_t ad, bd;
-                        if constexpr (TR::a_mn) ad = sm100::sdesc_sw128(sa + kk * 2048, 8192, 1024);
-                        else ad = sm100::sdesc_sw128(sa + kk * 32, 16, 1024);
-                        if constexpr (TR::b_mn) bd = sm100::sdesc_sw128(sb + kk * 2048, 8192, 1024);
-                        else bd = sm100::sdesc_sw128(sb + kk * 32, 16, 1024);
-                        sm100::mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        for (int j = 0; j < BN / 128; ++j)
+                            sm100::tmem_cp_32x128b_x4(tsf + 4 + 4 * j, sm100::sdesc_plain(ssf + 512 + 512 * j));
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = sm100::sdesc_sw128(sa + kk * 32, 16, 1024);
+                            const uint64_t bd = sm100::sdesc_sw128(sb + kk * 32, 16, 1024);
+                            sm100::mma_mxf8(d_tmem, ad, bd, IDESC | sm100::idesc_sf_ids(kk, kk), tsf, tsf + 4,
+                                            (kb | kk) != 0 ? 1u : 0u);
+                        }
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < TR::BK / UMMA_K; ++kk) {
+                            uint64_t ad, bd;
+                            if constexpr (TR::a_mn) ad = sm100::sdesc_sw128(sa + kk * 2048, 8192, 1024);
+                            else ad = sm100::sdesc_sw128(sa + kk * 32, 16, 1024);
+                            if constexpr (TR::b_mn) bd = sm100::sdesc_sw128(sb + kk * 2048, 8192, 1024);
+                            else bd = sm100::sdesc_sw128(sb + kk * 32, 16, 1024);
+                            sm100::mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        }
                     }
                     sm100::mma_commit(&empty_bar[stage]);
                     issued_any = true;
@@ -368,7 +426,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (!ok) break;
             if (lane == 0) sm100::mma_commit(&tfull_bar[acc]);
             __syncwarp();
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
         }
         if (!ok && issued_any && lane == 0) {
             // drain: wait for the MMAs already issued before TMEM is released
@@ -398,7 +456,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                          : args.out_f32 + eoff + (size_t)row * args.ld0 + n;
                         uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                        for (int q = 0; q < 8; ++q) d4[q] = make_uint4(0, 0, 0, 0);
+                        for (int q4 = 0; q4 < 8; ++q4) d4[q4] = make_uint4(0, 0, 0, 0);
                     }
                     continue;
                 }
@@ -408,7 +466,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             sm100::tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
 
-            if constexpr (OP == Op::FC1_SWIGLU) {
+            if constexpr (TR::swiglu) {
                 const int64_t row = tl.m0 + r;
                 const bool valid = row < tl.m_end && row < args.rows_cap;
 #pragma unroll 1
@@ -419,17 +477,30 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     sm100::tmem_ld_wait();
                     const int n = tl.n0 + c;
                     if (valid && n < args.N) {
-                        float hv[32], gv[32], uv[32];
+                        float hv[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            gv[i] = __uint_as_float(g[i]);
-                            uv[i] = __uint_as_float(u[i]);
-                            hv[i] = silu_f(gv[i]) * uv[i];
-                        }
-                        store_bf16x32(args.out0 + row * args.ld0 + n, hv);
-                        if (args.out1) {
-                            store_bf16x32(args.out1 + row * args.ld1 + n, gv);
-                            store_bf16x32(args.out1 + row * args.ld1 + args.N + n, uv);
+                        for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+                        if constexpr (OP == Op::FC1_MX) {
+                            // h quantised along F: this thread's 32 columns are one MX block
+                            const int X = mx::scale_exp(mx::amax32(hv));
+                            uint4 lo, hi;
+                            mx::quantize32(hv, X, lo, hi);
+                            uint4 *dq = reinterpret_cast<uint4 *>(args.out_q + row * args.ld0 + n);
+                            dq[0] = lo;
+                            dq[1] = hi;
+                            args.out_sf[mx::tile_sf_offset(tl.mtile, args.N / 128, r, n / 32)] = (uint8_t)(X + 127);
+                        } else {
+                            store_bf16x32(args.out0 + row * args.ld0 + n, hv);
+                            if (args.out1) {
+                                float gv[32], uv[32];
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    gv[i] = __uint_as_float(g[i]);
+                                    uv[i] = __uint_as_float(u[i]);
+                                }
+                                store_bf16x32(args.out1 + row * args.ld1 + n, gv);
+                                store_bf16x32(args.out1 + row * args.ld1 + args.N + n, uv);
+                            }
                         }
                     }
                 }
@@ -470,14 +541,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         float *dst = (OP == Op::WGRAD_GATEUP && n >= args.n_split)
                                          ? args.out1_f32 + eoff + (size_t)row * args.ld1 + (n - args.n_split)
                                          : args.out_f32 + eoff + (size_t)row * args.ld0 + n;
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            d4[q] = make_uint4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
+                        store_f32x32(dst, d);
                     }
                 }
-            } else {   // FC2 (y_perm) and DGRAD_FC1 (dx_perm): fp32 rows of the group
-                static_assert(OP == Op::FC2 || OP == Op::DGRAD_FC1, "unhandled op");
+            } else {   // FC2, FC2_MX (y_perm) and DGRAD_FC1 (dx_perm): fp32 rows of the group
+                static_assert(OP == Op::FC2 || OP == Op::FC2_MX || OP == Op::DGRAD_FC1, "unhandled op");
                 const int64_t row = tl.m0 + r;
                 const bool valid = row < tl.m_end && row < args.rows_cap;
 #pragma unroll 1
@@ -486,17 +554,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     sm100::tmem_ld32(tacc + c, d);
                     sm100::tmem_ld_wait();
                     const int n = tl.n0 + c;
-                    if (valid && n < args.N) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(args.out_f32 + row * args.ld0 + n);
-#pragma unroll
-                        for (int q = 0; q < 8; ++q)
-                            dst[q] = make_uint4(d[4 * q], d[4 * q + 1], d[4 * q + 2], d[4 * q + 3]);
-                    }
+                    if (valid && n < args.N) store_f32x32(args.out_f32 + row * args.ld0 + n, d);
                 }
             }
             sm100::tc_fence_before();
             sm100::mbar_arrive(&tempty_bar[acc]);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
         }
     }
 

@@ -328,3 +328,123 @@ extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const in
         return MOE_ERR_CUDA;
     return MOE_OK;
 }
+
+// ---------------------------------------------------------------------------
+// moe_permute_mxfp8: the same permutation with the rows quantised to MXFP8 on
+// the way (x is read once; each route gets E4M3 bytes and its scales in the
+// MMA tile layout of its group).  ("[Draft][JAX] MoE block optimization",
+// diagram: quantise before gather.)
+// ---------------------------------------------------------------------------
+
+#include "mx.cuh"
+
+namespace moe {
+namespace {
+
+__global__ void __launch_bounds__(kScatterWarps * 32)
+permute_scatter_mx_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx, int64_t T, int k,
+                          int E, int H, const int32_t *__restrict__ chunk_first,
+                          const int32_t *__restrict__ group_offsets, const int32_t *__restrict__ mtile_start,
+                          int32_t *__restrict__ dst_of_route, int32_t *__restrict__ src_of_row,
+                          uint8_t *__restrict__ x_q, uint8_t *__restrict__ x_sf, int64_t rows_cap, uint32_t *err) {
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_dst = -1, my_tile = 0, my_m = 0;
+    if (lane < k) {
+        const int64_t r = t * k + lane;
+        const int rank = dst_of_route[r];     // local rank written by the count pass
+        if (rank >= 0) {
+            const int e = topk_idx[r];
+            const int64_t row = (int64_t)chunk_first[(r / kPermChunk) * E + e] + rank;
+            if (row < rows_cap) {
+                my_dst = (int)row;
+                src_of_row[row] = (int32_t)r;
+                const int i = (int)(row - group_offsets[e]);
+                my_tile = mtile_start[e] + i / 128;
+                my_m = i % 128;
+            } else {
+                raise_device_error(err, MOE_DEVERR_CAPACITY);
+            }
+        }
+        dst_of_route[r] = my_dst;
+    }
+    int dst[32], tile[32], mm[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        dst[j] = j < k ? __shfl_sync(0xFFFFFFFFu, my_dst, j) : -1;
+        tile[j] = __shfl_sync(0xFFFFFFFFu, my_tile, j);
+        mm[j] = __shfl_sync(0xFFFFFFFFu, my_m, j);
+    }
+    const int nb = H / 32, kb128 = H / 128;
+    const uint4 *src = x + t * (H / 8);
+    for (int b = lane; b < nb; b += 32) {
+        float v[32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 p = __ldg(src + b * 4 + q);
+            const __nv_bfloat162 *hp = reinterpret_cast<const __nv_bfloat162 *>(&p);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __bfloat1622float2(hp[i]);
+                v[8 * q + 2 * i] = f.x;
+                v[8 * q + 2 * i + 1] = f.y;
+            }
+        }
+        const int X = mx::scale_exp(mx::amax32(v));
+        uint4 lo, hi;
+        mx::quantize32(v, X, lo, hi);
+        const uint8_t byte = (uint8_t)(X + 127);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < k && dst[j] >= 0) {
+                uint4 *d = reinterpret_cast<uint4 *>(x_q + (int64_t)dst[j] * H) + 2 * b;
+                d[0] = lo;
+                d[1] = hi;
+                x_sf[mx::tile_sf_offset(tile[j], kb128, mm[j], b)] = byte;
+            }
+        }
+    }
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *topk_idx, int64_t T, int H, int E,
+                                          int k, uint8_t *x_q, uint8_t *x_sf, int64_t rows_cap,
+                                          int32_t *dst_of_route, int32_t *src_of_row, int32_t *group_sizes,
+                                          int32_t *group_offsets, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || H < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
+    if (E < 1 || E > 1024 || k < 1 || k > 32 || H % 128 != 0) return MOE_ERR_UNSUPPORTED;
+    if (!group_sizes || !group_offsets) return MOE_ERR_INVALID_ARG;
+    const int64_t R = T * (int64_t)k;
+    if (rows_cap < R) return MOE_ERR_INVALID_ARG;
+    if (rows_cap >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
+    if (T > 0 && (!x || !topk_idx || !x_q || !x_sf || !dst_of_route || !src_of_row)) return MOE_ERR_INVALID_ARG;
+    const size_t need = moe_workspace_bytes(T, E, k);
+    if (!ws || ws_bytes < need || need == 0) return MOE_ERR_WORKSPACE;
+
+    cudaStream_t s = (cudaStream_t)stream;
+    uint32_t *err = ws_error_word(ws);
+    const int64_t chunks = perm_chunks(R);
+    int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsHeaderBytes);
+    int32_t *mtile = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsHeaderBytes + ws_counts_bytes(chunks, E));
+    if (chunks > 0) {
+        permute_count_kernel<<<(unsigned)chunks, kPermWarps * 32, kPermWarps * E * sizeof(int32_t), s>>>(
+            topk_idx, R, E, dst_of_route, counts, err);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    permute_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, chunks, E, 1, group_sizes, group_offsets);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    mtile_prefix_kernel<<<1, 1024, 0, s>>>(group_offsets, E, mtile);
+    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (T > 0) {
+        const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
+        permute_scatter_mx_kernel<<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(
+            reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, H, counts, group_offsets, mtile, dst_of_route,
+            src_of_row, x_q, x_sf, rows_cap, err);
+        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    }
+    return MOE_OK;
+}

@@ -92,6 +92,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *m, 
         : "memory");
 }
 
+// Plain bulk copy global -> shared (both 16-byte aligned, size a multiple of 16),
+// completing as transaction bytes on `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Generic-proxy shared-memory writes -> visible to the async proxy (tcgen05.mma).
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -125,6 +134,25 @@ __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64
         "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+// D[tmem] (+)= (A * scaleA) (B * scaleB): E4M3 operands with UE8M0 block scales in TMEM
+// (one scale per 32 K elements; the scale id in the instruction descriptor picks the
+// byte of each 32-bit TMEM scale word), fp32 accumulator, one CTA.
+__device__ __forceinline__ void mma_mxf8(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Copy a 32-row x 16-byte smem block into 4 TMEM columns of all four lane quarters
+// (row i -> lane i of each quarter).  Ordered before later tcgen05.mma of this thread.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
 // Arrive on `bar` once every tcgen05 operation issued so far by this thread completes.
@@ -170,6 +198,23 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
     return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) |
            ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Descriptor of an unswizzled smem block of 16-byte rows (8-row groups 128 B apart),
+// the source of tcgen05.cp.
+__device__ __forceinline__ uint64_t sdesc_plain(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+           (1ull << 46);
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scales: A/B format E4M3 (0) at bits
+// 7 and 10, K-major, N >> 3 at bit 17, scale format UE8M0 (1) at bit 23, M >> 4 at bit 24;
+// the B / A scale ids go to bits [4,6) / [29,31) (idesc_sf_ids).
+__host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N) {
+    return ((uint32_t)(N >> 3) << 17) | (1u << 23) | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_sf_ids(int a_id, int b_id) {
+    return ((uint32_t)b_id << 4) | ((uint32_t)a_id << 29);
 }
 
 }  // namespace sm100

@@ -62,4 +62,22 @@ inline bool tmap_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t
     return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
 }
 
+// 2-D byte matrix [outer, inner] with row pitch `ld` bytes (E4M3 data).
+inline bool tmap_u8_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
+                       uint32_t box_inner, uint32_t box_outer) {
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {ld};
+    const uint32_t box[2] = {box_inner, box_outer};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box);
+}
+
+// 3-D byte tensor [d2, d1, d0] (d0 contiguous), densely packed.
+inline bool tmap_u8_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d1, uint64_t d2, uint32_t box0,
+                       uint32_t box1) {
+    const uint64_t dims[3] = {d0, d1, d2};
+    const uint64_t strides[2] = {d0, d0 * d1};
+    const uint32_t box[3] = {box0, box1, 1};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box);
+}
+
 }  // namespace moe

@@ -10,7 +10,9 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import (Permutation, Workspace, moe_combine_bwd, moe_grouped_dgrad_fc1,
+from ._binding import (Permutation, PermutationMX, Workspace, moe_combine_bwd, moe_grouped_dgrad_fc1,
+                       moe_grouped_fc1_swiglu_mxfp8, moe_grouped_fc2_mxfp8, moe_permute_mxfp8,
+                       moe_quantize_weights_mxfp8, mx_tile_scale_bytes,
                        moe_grouped_dgrad_fc2_dswiglu, moe_grouped_fc1_swiglu, moe_grouped_fc2,
                        moe_grouped_wgrad, moe_permute, moe_route_topk, moe_unpermute_combine,
                        moe_unpermute_sum, rows_capacity)
@@ -127,3 +129,64 @@ class MoeBackward:
         self.wgrad(stream)
         self.unpermute_sum(stream)
         return self.dx
+
+
+class MxWeights:
+    """Expert weights quantised once to MXFP8 (K-major codes + tile-layout scales)."""
+
+    def __init__(self, W_gate, W_up, W_down, stream=None):
+        self.Wg_q, self.Wg_sf = moe_quantize_weights_mxfp8(W_gate, stream)   # [E, F, H]
+        self.Wu_q, self.Wu_sf = moe_quantize_weights_mxfp8(W_up, stream)
+        self.Wd_q, self.Wd_sf = moe_quantize_weights_mxfp8(W_down, stream)   # [E, H, F]
+
+
+class MoeForwardMX:
+    """Pre-allocated MXFP8 forward: route -> quantising permute -> block-scaled
+    FC1 + SwiGLU (h to MXFP8) -> block-scaled FC2 -> combine (bf16 out)."""
+
+    def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda"):
+        self.T, self.H, self.F, self.E, self.k = T, H, F, E, k
+        dev = torch.device(device)
+        self.device = dev
+        self.ws = Workspace(T, E, k, dev)
+        cap = T * k
+        self.rows_cap = cap
+        self.topk_idx = torch.empty(T, k, dtype=torch.int32, device=dev)
+        self.topk_w = torch.empty(T, k, dtype=torch.float32, device=dev)
+        self.perm = PermutationMX(
+            x_q=torch.empty(cap, H, dtype=torch.uint8, device=dev),
+            x_sf=torch.zeros(mx_tile_scale_bytes(cap, E, H), dtype=torch.uint8, device=dev),
+            dst_of_route=torch.empty(T, k, dtype=torch.int32, device=dev),
+            src_of_row=torch.empty(cap, dtype=torch.int32, device=dev),
+            group_sizes=torch.empty(E, dtype=torch.int32, device=dev),
+            group_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev), rows_cap=cap)
+        self.h_q = torch.empty(cap, F, dtype=torch.uint8, device=dev)
+        self.h_sf = torch.zeros(mx_tile_scale_bytes(cap, E, F), dtype=torch.uint8, device=dev)
+        self.y_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
+        self.out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+
+    def route(self, logits, stream=None):
+        moe_route_topk(logits, self.k, self.topk_idx, self.topk_w, stream=stream)
+
+    def permute(self, x, stream=None):
+        moe_permute_mxfp8(x, self.topk_idx, self.E, self.ws, out=self.perm, stream=stream)
+
+    def fc1(self, w: MxWeights, stream=None):
+        p = self.perm
+        moe_grouped_fc1_swiglu_mxfp8(p.x_q, p.x_sf, w.Wg_q, w.Wg_sf, w.Wu_q, w.Wu_sf, p.group_offsets, self.ws,
+                                     self.h_q, self.h_sf, stream=stream)
+
+    def fc2(self, w: MxWeights, stream=None):
+        moe_grouped_fc2_mxfp8(self.h_q, self.h_sf, w.Wd_q, w.Wd_sf, self.perm.group_offsets, self.ws, self.y_perm,
+                              stream=stream)
+
+    def combine(self, stream=None):
+        moe_unpermute_combine(self.y_perm, self.perm.dst_of_route, self.topk_w, out=self.out, stream=stream)
+
+    def __call__(self, x, logits, w: MxWeights, stream=None):
+        self.route(logits, stream)
+        self.permute(x, stream)
+        self.fc1(w, stream)
+        self.fc2(w, stream)
+        self.combine(stream)
+        return self.out
