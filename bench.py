@@ -1,11 +1,16 @@
-"""Benchmark of the single-GPU MoE FFN forward hot path on GB300.
+"""Benchmark of the single-GPU MoE FFN hot path on GB300.
 
-A step = route (A1) + permute (A2) + grouped FC1+SwiGLU (A3) + grouped FC2
-(A4) + combine (A5) over one batch of seeded synthetic inputs resident in
-HBM.  Default workload: fine_grained (T=4096, H=2048, F=1408, E=64, top-6).
+A step is one pass of the whole hot path over one batch of seeded synthetic
+inputs resident in HBM:
+  bf16 forward   route -> permute -> grouped FC1+SwiGLU -> grouped FC2 -> combine
+  mixtral        the forward, then the backward (combine bwd, FC2 dgrad + dSwiGLU,
+                 FC1 dgrad, grouped wgrad, unpermute-sum)
+  dsv3_mxfp8     route -> quantising permute -> block-scaled FC1 (h to MXFP8) ->
+                 block-scaled FC2 -> combine; weights quantised once, untimed
+Default workload: fine_grained (T=4096, H=2048, F=1408, E=64, top-6).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
-    python bench.py --impl reference ...     # the CPU oracle, timed on the host cores
+    python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs an independent
 replica of the workload on its own GPU (the path needs no collective); the
@@ -28,12 +33,12 @@ sys.path.insert(0, ROOT)
 METRIC = "MoE layer tokens/s & grouped-GEMM TFLOP/s (% of GB300 peak); permute/combine GB/s"
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
+FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 
-
-# DRAM traffic (read + write bytes per launch) of the dominant kernel (grouped FC1 + SwiGLU),
-# from one ncu capture per workload (profiles/<workload>_fwd_kernels.md), with a hash of the
-# kernel sources the capture was taken on.  Reported as null once those sources change.
-PROFILED_TRAFFIC = {"fine_grained": (900.8e6, "c26e88ae9aa42def")}
+# DRAM traffic (read + write bytes per launch) of a workload's dominant kernel from one
+# ncu capture (profiles/), with a hash of the kernel sources it was taken on.  Reported as
+# null once those sources change.
+PROFILED_TRAFFIC = {("fine_grained", "fc1_swiglu"): (900.8e6, "c26e88ae9aa42def")}
 KERNEL_SOURCES = ["common.cuh", "sm100.cuh", "grouped_gemm.cuh", "gemm_launch.cuh", "tmap.cuh", "ffn_fwd.cu"]
 
 
@@ -46,14 +51,14 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
-    t = PROFILED_TRAFFIC.get(workload)
+def profiled_traffic(workload: str, kernel: str):
+    t = PROFILED_TRAFFIC.get((workload, kernel))
     if t is None or t[1] != kernel_source_hash():
         return None
     return t[0]
 
 
-def _peaks():
+def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
         with open(p) as f:
@@ -66,10 +71,8 @@ def _peaks():
 # ------------------------------------------------------------------ distributed plumbing
 
 def dist_env():
-    ws = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return ws, rank, local
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
 
 
 def init_dist(backend: str):
@@ -104,11 +107,13 @@ def barrier(device=None):
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons, started before the
+    warm-up and stopped after the timed steps."""
 
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
          "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
          "clocks_event_reasons.sw_power_cap")
+    NAMES = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
 
     def __init__(self, gpu_index: int):
         self.idx = gpu_index
@@ -124,27 +129,24 @@ class ClockSampler:
             self.thread.start()
         except (OSError, FileNotFoundError):
             self.proc = None
+        t0 = time.time()
+        while self.proc is not None and not self.lines and time.time() - t0 < 3.0:
+            time.sleep(0.01)
 
     def _read(self):
         for line in self.proc.stdout:
             self.lines.append(line.strip())
 
-    def wait_first(self, limit_s: float = 3.0):
-        t0 = time.time()
-        while self.proc is not None and not self.lines and time.time() - t0 < limit_s:
-            time.sleep(0.01)
-
     def stop(self) -> dict:
         if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        sm, mx, power, reasons = [], [], [], set()
         for ln in self.lines:
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
@@ -152,96 +154,220 @@ class ClockSampler:
             try:
                 sm.append(float(parts[1]))
                 mx.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[4:8]):
+            for n, v in zip(self.NAMES, parts[4:8]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ------------------------------------------------------------------ workload bookkeeping
+# ------------------------------------------------------------------ workloads
 
-def work(shape):
-    """Algorithmic FLOPs and bytes of one forward step."""
+class Group:
+    """One timed kernel group of a step: its launches and its algorithmic work."""
+
+    def __init__(self, name, run, flop=0.0, nbytes=0.0, launches=1, fp8=False):
+        self.name, self.run, self.flop, self.nbytes, self.launches, self.fp8 = name, run, flop, nbytes, launches, fp8
+
+
+def build_workload(shape, dev, stream):
+    """Inputs, pre-allocated layer objects and the step's kernel groups."""
+    import torch
+    from mixture_experts_ffn_warp_gb300 import MoeBackward, MoeForward, MoeForwardMX, MxWeights
+    from mixture_experts_ffn_warp_gb300.synthetic import make_inputs
+
     T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
     R = T * k
-    return {
-        "fc1_flop": 4.0 * R * H * F,
-        # FC1 reads x_perm and W_gate/W_up of the experts that received routes, writes h
-        "fc1_bytes": R * H * 2 + 2 * E * H * F * 2 + R * F * 2,
-        "fc2_flop": 2.0 * R * H * F,
-        "permute_bytes": T * H * 2 + R * H * 2 + R * 8 + E * 8,
-        "combine_bytes": R * H * 4 + T * H * 2 + R * 8,   # fp32 expert outputs in, bf16 out
-        "route_bytes": T * E * 4 + R * 8,
-    }
+    inp = make_inputs(shape, device=dev, with_dy=shape.backward)
+    w = {"inp": inp, "shape": shape}
+    if shape.mxfp8:
+        mw = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"], stream)
+        m = MoeForwardMX(T, H, F, E, k, device=dev)
+        w.update(layer=m, mw=mw)
+        m(inp["x"], inp["logits"], mw, stream)
+    else:
+        m = MoeForward(T, H, F, E, k, device=dev, keep_fc1_c=shape.backward)
+        w.update(layer=m)
+        m(inp["x"], inp["logits"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
+        if shape.backward:
+            w["bwd"] = MoeBackward(m)
+    torch.cuda.synchronize(dev)
+    active = int((m.perm.group_sizes > 0).sum().item())     # experts whose weights are read
+    w["active_experts"] = active
+    wbytes = active * H * F * (1 if shape.mxfp8 else 2) * (1 + (1 / 32 if shape.mxfp8 else 0))
+
+    g = [Group("route", lambda: m.route(inp["logits"], stream), nbytes=T * E * 4 + R * 8)]
+    if shape.mxfp8:
+        mw = w["mw"]
+        g += [
+            Group("permute_mxfp8", lambda: m.permute(inp["x"], stream),
+                  nbytes=T * H * 2 + R * H * (1 + 1 / 32) + R * 8, launches=4),
+            Group("fc1_swiglu_mxfp8", lambda: m.fc1(mw, stream), flop=4.0 * R * H * F,
+                  nbytes=R * H * (1 + 1 / 32) + 2 * wbytes + R * F * (1 + 1 / 32), fp8=True),
+            Group("fc2_mxfp8", lambda: m.fc2(mw, stream), flop=2.0 * R * H * F,
+                  nbytes=R * F * (1 + 1 / 32) + wbytes + R * H * 4, fp8=True),
+        ]
+    else:
+        stash = R * 2 * F * 2 if shape.backward else 0
+        g += [
+            Group("permute", lambda: m.permute(inp["x"], stream), nbytes=T * H * 2 + R * H * 2 + R * 8,
+                  launches=3),
+            Group("fc1_swiglu", lambda: m.fc1(inp["W_gate"], inp["W_up"], stream), flop=4.0 * R * H * F,
+                  nbytes=R * H * 2 + 2 * wbytes + R * F * 2 + stash),
+            Group("fc2", lambda: m.fc2(inp["W_down"], stream), flop=2.0 * R * H * F,
+                  nbytes=R * F * 2 + wbytes + R * H * 4),
+        ]
+    g.append(Group("combine", lambda: m.combine(stream), nbytes=R * H * 4 + T * H * 2 + R * 8))
+    if shape.backward:
+        b = w["bwd"]
+        g += [
+            Group("combine_bwd", lambda: b.combine_bwd(inp["dY"], stream),
+                  nbytes=T * H * 2 + R * H * 4 + R * H * 2 + R * 8, launches=2),
+            Group("dgrad_fc2_dswiglu", lambda: b.dgrad_fc2(inp["W_down"], stream), flop=2.0 * R * H * F,
+                  nbytes=R * H * 2 + wbytes + R * 2 * F * 2 * 2),
+            Group("dgrad_fc1", lambda: b.dgrad_fc1(inp["W_gate"], inp["W_up"], stream), flop=4.0 * R * H * F,
+                  nbytes=R * 2 * F * 2 + 2 * wbytes + R * H * 4),
+            Group("wgrad", lambda: b.wgrad(stream), flop=6.0 * R * H * F,
+                  nbytes=R * (F + H + H + 2 * F) * 2 + 3 * E * H * F * 4, launches=2),
+            Group("unpermute_sum", lambda: b.unpermute_sum(stream), nbytes=R * H * 4 + T * H * 2 + R * 8),
+        ]
+    w["groups"] = g
+    return w
 
 
-# ------------------------------------------------------------------ CPU oracle baseline
+def e2e_step(w, host, stream):
+    """One step through the public layer API, inputs copied from pinned host
+    memory and the result copied back (inside the timed region)."""
+    inp, m, shape = w["inp"], w["layer"], w["shape"]
+    host["x_d"].copy_(host["x"], non_blocking=True)
+    host["lg_d"].copy_(host["lg"], non_blocking=True)
+    if shape.mxfp8:
+        m(host["x_d"], host["lg_d"], w["mw"], stream)
+    else:
+        m(host["x_d"], host["lg_d"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
+    host["out"].copy_(m.out, non_blocking=True)
+    if shape.backward:
+        host["dy_d"].copy_(host["dy"], non_blocking=True)
+        w["bwd"](host["dy_d"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
+        host["dx"].copy_(w["bwd"].dx, non_blocking=True)
 
-def oracle_sample_rate(shape, inp_cpu, target_s: float, max_tokens: int = 4096):
-    """Tokens/s of the oracle's per-token forward on a bounded sample of tokens,
-    plus its routing + permutation over all tokens."""
+
+def e2e_buffers(w):
+    import torch
+    inp, shape = w["inp"], w["shape"]
+    host = {"x": inp["x"].cpu().pin_memory(), "lg": inp["logits"].cpu().pin_memory(),
+            "out": torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory(),
+            "x_d": torch.empty_like(inp["x"]), "lg_d": torch.empty_like(inp["logits"])}
+    h2d = shape.T * shape.H * 2 + shape.T * shape.E * 4
+    d2h = shape.T * shape.H * 2
+    if shape.backward:
+        host.update(dy=inp["dY"].cpu().pin_memory(), dy_d=torch.empty_like(inp["dY"]),
+                    dx=torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory())
+        h2d += shape.T * shape.H * 2
+        d2h += shape.T * shape.H * 2
+    return host, h2d, d2h
+
+
+# ------------------------------------------------------------------ CPU oracle
+
+def oracle_sample(shape, inp_dev, n_tokens: int, it: int = 0):
+    """Run the oracle on a sample of n_tokens tokens of the workload (routing and
+    permutation over all tokens; the expert FFN -- and for mixtral the backward,
+    for dsv3_mxfp8 the MXFP8 arithmetic -- on the sampled tokens).  Weights of
+    the experts the sample touches are copied to the host (and, for MXFP8,
+    quantised by the oracle) before the clock starts.  Returns (seconds, tokens)."""
     import numpy as np
     import oracle
-    lg = inp_cpu["logits"].numpy()
+    T, k = shape.T, shape.k
+    lg = inp_dev["logits"].cpu().numpy()
+    idx_all, w_all = oracle.route_topk(lg, k)
+    toks = (np.arange(n_tokens) * max(1, T // n_tokens) + it) % T
+    experts = np.unique(idx_all[toks])
+    x_rows = oracle.bf16_bits(inp_dev["x"].index_select(0, _long(inp_dev, toks)))
+    wts = {n: {int(e): oracle.bf16_bits(inp_dev[n][int(e)]) for e in experts} for n in ("W_gate", "W_up", "W_down")}
+    idx_s, w_s = idx_all[toks], w_all[toks]
+    if shape.mxfp8:
+        q = {n: {} for n in ("gq", "gs", "uq", "us", "dq", "ds")}
+        for e in experts:
+            e = int(e)
+            q["gq"][e], q["gs"][e] = oracle.quantize_cols_mxfp8(wts["W_gate"][e])
+            q["uq"][e], q["us"][e] = oracle.quantize_cols_mxfp8(wts["W_up"][e])
+            q["dq"][e], q["ds"][e] = oracle.quantize_cols_mxfp8(wts["W_down"][e])
+    dy_rows = oracle.bf16_bits(inp_dev["dY"].index_select(0, _long(inp_dev, toks))) if shape.backward else None
     t0 = time.perf_counter()
-    idx, w = oracle.route_topk(lg, shape.k)
+    idx, w = oracle.route_topk(lg, k)
     oracle.permute(idx, shape.E)
-    t_route = time.perf_counter() - t0
-    xb = oracle.bf16_bits(inp_cpu["x"])
-    Wg, Wu, Wd = inp_cpu["Wg_bits"], inp_cpu["Wu_bits"], inp_cpu["Wd_bits"]
-    n = 8
-    spent, done = 0.0, 0
-    while True:
-        toks = np.arange(done, min(done + n, shape.T, max_tokens))
-        if toks.size == 0:
-            break
-        t0 = time.perf_counter()
-        oracle.moe_fwd(xb, Wg, Wu, Wd, idx, w, tokens=toks)
-        spent += time.perf_counter() - t0
-        done += toks.size
-        if spent >= target_s or done >= min(shape.T, max_tokens):
-            break
-        n = min(4 * n, max(8, int(toks.size * (target_s - spent) / max(spent, 1e-3))))
-    # tokens/s for the whole path: per-token FFN rate, plus routing amortised over T
-    per_token = spent / done
-    total = per_token * shape.T + t_route
-    return shape.T / total, done, spent + t_route, oracle.num_threads()
+    if shape.mxfp8:
+        oracle.moe_fwd_mxfp8(x_rows, q["gq"], q["gs"], q["uq"], q["us"], q["dq"], q["ds"], idx_s, w_s)
+    else:
+        oracle.moe_fwd(x_rows, wts["W_gate"], wts["W_up"], wts["W_down"], idx_s, w_s)
+        if shape.backward:
+            oracle.moe_bwd(x_rows, _dense(wts["W_gate"], shape.E), _dense(wts["W_up"], shape.E),
+                           _dense(wts["W_down"], shape.E), idx_s, w_s, dy_rows)
+    return time.perf_counter() - t0, n_tokens
 
 
-def cpu_inputs(inp):
+def _long(inp_dev, toks):
+    import torch
+    return torch.from_numpy(toks.astype("int64")).to(inp_dev["x"].device)
+
+
+def _dense(d: dict, E: int):
+    """Per-expert dict -> list; experts the sample does not route to get a zero
+    placeholder (never read by the oracle)."""
+    import numpy as np
+    zero = np.zeros_like(next(iter(d.values())))
+    return [d[e] if e in d else zero for e in range(E)]
+
+
+def cpu_baseline(shape, inp_dev, target_s: float):
+    """The oracle as it stands on the host cores, on a bounded token sample."""
     import oracle
-    c = {"logits": inp["logits"].cpu(), "x": inp["x"].cpu()}
-    c["Wg_bits"] = oracle.bf16_bits(inp["W_gate"])
-    c["Wu_bits"] = oracle.bf16_bits(inp["W_up"])
-    c["Wd_bits"] = oracle.bf16_bits(inp["W_down"])
-    return c
+    n = 2 if (shape.backward or shape.mxfp8) else 8
+    spent, done = 0.0, 0
+    while spent < target_s and done < shape.T:
+        dt, m = oracle_sample(shape, inp_dev, n, it=done)
+        spent += dt
+        done += m
+        if spent < target_s:
+            n = max(1, min(4 * n, int(m * (target_s - spent) / max(dt, 1e-3))))
+    return {"value": done / spent, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{done} of {shape.T} tokens in {spent:.1f} s: routing + permutation over all tokens, "
+                      f"the per-token fp64 oracle ({'forward + backward' if shape.backward else 'MXFP8 forward' if shape.mxfp8 else 'forward'}) on the sample"}
+
+
+# ------------------------------------------------------------------ arms
+
+def workload_shape(args):
+    """The named workload, with sizes overridden by --shape (a smaller case of the
+    same kernels, e.g. for profiling)."""
+    import dataclasses
+    from mixture_experts_ffn_warp_gb300.synthetic import CONFIGS
+    shape = CONFIGS[args.config]
+    if args.shape:
+        kw = {kv.split("=")[0].strip(): int(kv.split("=")[1]) for kv in args.shape.split(",") if kv.strip()}
+        shape = dataclasses.replace(shape, name=shape.name + "_" + "_".join(f"{a}{b}" for a, b in kw.items()), **kw)
+    return shape
 
 
 def run_reference(args):
-    """The oracle as it stands, on the host cores, bounded sample per step."""
-    import numpy as np
+    """The oracle as it stands, on the host cores, a bounded token sample per step."""
+    import torch
     import oracle
     from mixture_experts_ffn_warp_gb300.synthetic import CONFIGS, make_inputs
-    ws, rank, _ = dist_env()
+    _, rank, _ = dist_env()
     if rank != 0:
         return 0
-    shape = CONFIGS[args.config]
-    inp = make_inputs(shape, device="cpu")
-    c = cpu_inputs(inp)
-    lg = c["logits"].numpy()
-    xb = oracle.bf16_bits(c["x"])
-    sample = max(1, min(shape.T, args.ref_tokens))
+    shape = workload_shape(args)
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = make_inputs(shape, device=dev, with_dy=shape.backward)
+    sample = max(1, min(shape.T, args.ref_tokens if args.ref_tokens else (2 if shape.backward or shape.mxfp8 else 16)))
     times = []
     for it in range(args.warmup + args.steps):
-        toks = (np.arange(sample) * (shape.T // sample) + it) % shape.T
-        t0 = time.perf_counter()
-        idx, w = oracle.route_topk(lg, shape.k)
-        oracle.permute(idx, shape.E)
-        oracle.moe_fwd(xb, c["Wg_bits"], c["Wu_bits"], c["Wd_bits"], idx, w, tokens=toks)
-        dt = time.perf_counter() - t0
+        dt, _ = oracle_sample(shape, inp, sample, it=it)
         if it >= args.warmup:
             times.append(dt)
     ms = 1e3 * statistics.mean(times)
@@ -260,150 +386,120 @@ def run_reference(args):
     return 0
 
 
-# ------------------------------------------------------------------ GPU arm
-
 def run_gpu(args):
     import torch
-    from mixture_experts_ffn_warp_gb300 import MoeForward
-    from mixture_experts_ffn_warp_gb300.synthetic import CONFIGS, make_inputs
+    from mixture_experts_ffn_warp_gb300.synthetic import CONFIGS
 
-    backend = "nccl" if torch.cuda.is_available() else "gloo"
-    world, rank = init_dist(backend)
-    _, _, local = dist_env()
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA GPU (no CPU fallback)")
+    world, rank = init_dist("nccl")
+    _, _, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    shape = CONFIGS[args.config]
-    W = work(shape)
-    peaks = _peaks()
-
-    inp = make_inputs(shape, device=dev, with_dy=False)
-    m = MoeForward(shape.T, shape.H, shape.F, shape.E, shape.k, device=dev)
+    shape = workload_shape(args)
+    pk = peaks()
     stream = torch.cuda.Stream(device=dev)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
-
-    def step():
-        m.route(inp["logits"], stream)
-        m.permute(inp["x"], stream)
-        m.fc1(inp["W_gate"], inp["W_up"], stream)
-        m.fc2(inp["W_down"], stream)
-        m.combine(stream)
-
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    # clocks are sampled from the start of the warm-up to the end of the timed steps
+
+    with torch.cuda.stream(stream):
+        w = build_workload(shape, dev, stream)
+    groups = w["groups"]
+    m = w["layer"]
+
     clocks = ClockSampler(local)
     clocks.start()
-    clocks.wait_first()
     with torch.cuda.stream(stream):
         for _ in range(args.warmup):
-            step()
+            for g in groups:
+                g.run()
         stream.synchronize()
         if m.ws.read_error(stream) != 0:
             raise RuntimeError("device error word set during warm-up")
-
         barrier(dev)
         torch.cuda.synchronize(dev)
         marks = []
         for it in range(args.steps):
             flush.fill_(float(it % 7))           # evict L2 between steps (outside the events)
-            e = [ev() for _ in range(5)]
+            e = [ev() for _ in range(len(groups) + 1)]
             e[0].record(stream)
-            m.route(inp["logits"], stream)
-            m.permute(inp["x"], stream)
-            e[1].record(stream)
-            m.fc1(inp["W_gate"], inp["W_up"], stream)
-            e[2].record(stream)
-            m.fc2(inp["W_down"], stream)
-            e[3].record(stream)
-            m.combine(stream)
-            e[4].record(stream)
+            for i, g in enumerate(groups):
+                g.run()
+                e[i + 1].record(stream)
             marks.append(e)
         torch.cuda.synchronize(dev)
         barrier(dev)
-        clk = clocks.stop()
+    clk = clocks.stop()
+    if m.ws.read_error(stream) != 0:
+        raise RuntimeError("device error word set during the timed steps")
 
-        seg = {"route_permute": [], "fc1": [], "fc2": [], "combine": [], "step": []}
-        for e in marks:
-            seg["route_permute"].append(e[0].elapsed_time(e[1]))
-            seg["fc1"].append(e[1].elapsed_time(e[2]))
-            seg["fc2"].append(e[2].elapsed_time(e[3]))
-            seg["combine"].append(e[3].elapsed_time(e[4]))
-            seg["step"].append(e[0].elapsed_time(e[4]))
-        ms_step = max_over_ranks(statistics.mean(seg["step"]), dev)
-        mean = {k: statistics.mean(v) for k, v in seg.items()}
-        if m.ws.read_error(stream) != 0:
-            raise RuntimeError("device error word set during the timed steps")
+    per = {g.name: statistics.mean(e[i].elapsed_time(e[i + 1]) for e in marks) for i, g in enumerate(groups)}
+    step_ms = statistics.mean(e[0].elapsed_time(e[-1]) for e in marks)
+    ms_step = max_over_ranks(step_ms, dev)
 
-        # separate route / permute split (same launches, timed apart once per step)
-        rp = []
-        for _ in range(max(3, args.steps // 2)):
-            flush.fill_(1.0)
-            e = [ev() for _ in range(3)]
-            e[0].record(stream)
-            m.route(inp["logits"], stream)
-            e[1].record(stream)
-            m.permute(inp["x"], stream)
-            e[2].record(stream)
-            rp.append((e[0], e[1], e[2]))
-        torch.cuda.synchronize(dev)
-        t_route = statistics.mean(a.elapsed_time(b) for a, b, _ in rp)
-        t_perm = statistics.mean(b.elapsed_time(c) for _, b, c in rp)
-
-        # ---------------- end to end through the public API with host buffers
-        x_h = inp["x"].cpu().pin_memory()
-        lg_h = inp["logits"].cpu().pin_memory()
-        out_h = torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory()
-        x_d = torch.empty_like(inp["x"])
-        lg_d = torch.empty_like(inp["logits"])
-        e2e_times = []
+    # end to end through the layer API with host buffers
+    host, h2d, d2h = e2e_buffers(w)
+    e2e_t = []
+    with torch.cuda.stream(stream):
         for it in range(args.warmup + args.steps):
             flush.fill_(2.0)
-            e0, e1 = ev(), ev()
-            e0.record(stream)
-            x_d.copy_(x_h, non_blocking=True)
-            lg_d.copy_(lg_h, non_blocking=True)
-            m(x_d, lg_d, inp["W_gate"], inp["W_up"], inp["W_down"], stream=stream)
-            out_h.copy_(m.out, non_blocking=True)
-            e1.record(stream)
+            a, b = ev(), ev()
+            a.record(stream)
+            e2e_step(w, host, stream)
+            b.record(stream)
             if it >= args.warmup:
-                e2e_times.append((e0, e1))
+                e2e_t.append((a, b))
         torch.cuda.synchronize(dev)
-        ms_e2e = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_times), dev)
+    ms_e2e = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_t), dev)
 
+    def peak_flops(g):
+        return pk["bf16_tflops"] * (FP8_OVER_BF16 if g.fp8 else 1.0)
+
+    rates = {}
+    for g in groups:
+        t = per[g.name] / 1e3
+        r = {"ms": per[g.name], "gbs": g.nbytes / t / 1e9}
+        if g.flop:
+            r["tflops"] = g.flop / t / 1e12
+            r["frac_tensor"] = r["tflops"] / peak_flops(g)
+        r["frac_hbm"] = r["gbs"] / pk["hbm_gbs"]
+        rates[g.name] = r
+    dom = max(groups, key=lambda g: per[g.name])
+    t_dom = per[dom.name] / 1e3
+    ridge = peak_flops(dom) * 1e12 / (pk["hbm_gbs"] * 1e9)
+    tensor_bound = dom.flop > 0 and dom.flop / dom.nbytes >= ridge
+    if tensor_bound:
+        roof = {"bound": "tensor", "achieved": dom.flop / t_dom / 1e12, "peak": peak_flops(dom), "unit": "TFLOP/s",
+                "peak_source": f"{pk['source']} bf16 dense burst" + (" x 2 (nominal fp8/bf16)" if dom.fp8 else "")}
+    else:
+        roof = {"bound": "hbm", "achieved": dom.nbytes / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "peak_source": f"{pk['source']} HBM copy"}
+    roof.update(kernel=dom.name, frac=roof["achieved"] / roof["peak"], traffic=profiled_traffic(shape.name, dom.name),
+                algorithmic_bytes=dom.nbytes, algorithmic_flop=dom.flop)
+
+    ffn = [g for g in groups if g.flop]
+    ffn_flop = sum(g.flop for g in ffn)
+    ffn_ms = sum(per[g.name] for g in ffn)
     tokens = shape.T * world
-    value = tokens / (ms_step / 1e3)
-    fc1_tflops = W["fc1_flop"] / (mean["fc1"] / 1e3) / 1e12
-    ffn_tflops = (W["fc1_flop"] + W["fc2_flop"]) / ((mean["fc1"] + mean["fc2"]) / 1e3) / 1e12
     line = {
-        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "metric": METRIC, "value": tokens / (ms_step / 1e3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, BASELINE shapes and distributions)",
-        "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
-                   "k": shape.k, "l2": "flushed between steps (256 MiB write outside the timed events)"},
-        "breakdown_ms": {"route": t_route, "permute": t_perm, "fc1_swiglu": mean["fc1"], "fc2": mean["fc2"],
-                         "combine": mean["combine"]},
-        "ffn_tflops": ffn_tflops,
-        "ffn_frac_of_bf16_peak": ffn_tflops / peaks["bf16_tflops"],
-        "permute_gbs": W["permute_bytes"] / (t_perm / 1e3) / 1e9,
-        "combine_gbs": W["combine_bytes"] / (mean["combine"] / 1e3) / 1e9,
-        "roofline": {"kernel": "grouped_gemm FC1_SWIGLU", "bound": "tensor", "achieved": fc1_tflops,
-                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s", "frac": fc1_tflops / peaks["bf16_tflops"],
-                     "peak_source": f"{peaks['source']} bf16 dense burst",
-                     "traffic": profiled_traffic(shape.name),
-                     "algorithmic_bytes": W["fc1_bytes"]},
+        "vs_baseline": None, "dtype": "mxfp8" if shape.mxfp8 else "bf16",
+        "data": "synthetic (seeded; BASELINE shapes and distributions)",
+        "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k,
+                   "pass": "forward+backward" if shape.backward else "forward",
+                   "active_experts": w["active_experts"],
+                   "l2": "flushed between steps (256 MiB write outside the timed events)"},
+        "kernels": rates,
+        "ffn_tflops": ffn_flop / (ffn_ms / 1e3) / 1e12,
+        "ffn_frac_of_peak": ffn_flop / (ffn_ms / 1e3) / 1e12 / (pk["bf16_tflops"] * (FP8_OVER_BF16 if shape.mxfp8 else 1)),
+        "roofline": roof,
         "clocks": clk,
-        "gpu_launches": 7 * args.steps,
-        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT,
-                "h2d_bytes_per_step": shape.T * shape.H * 2 + shape.T * shape.E * 4,
-                "d2h_bytes_per_step": shape.T * shape.H * 2},
+        "gpu_launches": args.steps * sum(g.launches for g in groups),
+        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        c = cpu_inputs({k: v for k, v in inp.items()})
-        rate, done, spent, cores = oracle_sample_rate(shape, c, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": cores, "kind": "oracle",
-                                "sample": f"{done} of {shape.T} tokens through the per-token fp64 oracle in "
-                                          f"{spent:.1f} s (routing + permutation over all tokens), scaled to T"}
+        line["cpu_baseline"] = cpu_baseline(shape, w["inp"], args.cpu_seconds)
     if rank == 0:
         print(json.dumps(line), flush=True)
     import torch.distributed as dist
@@ -415,15 +511,18 @@ def run_gpu(args):
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="fine_grained")
+    ap.add_argument("--config", default="fine_grained",
+                    choices=["tiny", "fine_grained", "mixtral", "skewed", "dsv3_mxfp8"])
+    ap.add_argument("--shape", default="",
+                    help="override sizes of the workload, e.g. 'T=2048,F=4096' (same kind of pass)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--ref-tokens", type=int, default=64)
+    ap.add_argument("--ref-tokens", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
-    if args.warmup < 3 and args.impl == "ours":
+    if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
