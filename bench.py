@@ -204,7 +204,7 @@ def build_workload(shape, dev, stream):
         mw = w["mw"]
         g += [
             Group("permute_mxfp8", lambda: m.permute(inp["x"], stream),
-                  nbytes=T * H * 2 + R * H * (1 + 1 / 32) + R * 8, launches=4),
+                  nbytes=T * H * 2 + R * H * (1 + 1 / 32) + R * 8, launches=2),
             Group("fc1_swiglu_mxfp8", lambda: m.fc1(mw, stream), flop=4.0 * R * H * F,
                   nbytes=R * H * (1 + 1 / 32) + 2 * wbytes + R * F * (1 + 1 / 32), fp8=True),
             Group("fc2_mxfp8", lambda: m.fc2(mw, stream), flop=2.0 * R * H * F,
@@ -214,7 +214,7 @@ def build_workload(shape, dev, stream):
         stash = R * 2 * F * 2 if shape.backward else 0
         g += [
             Group("permute", lambda: m.permute(inp["x"], stream), nbytes=T * H * 2 + R * H * 2 + R * 8,
-                  launches=3),
+                  launches=2),
             Group("fc1_swiglu", lambda: m.fc1(inp["W_gate"], inp["W_up"], stream), flop=4.0 * R * H * F,
                   nbytes=R * H * 2 + 2 * wbytes + R * F * 2 + stash),
             Group("fc2", lambda: m.fc2(inp["W_down"], stream), flop=2.0 * R * H * F,

@@ -31,6 +31,9 @@ inline size_t ws_mtile_bytes(int E) { return ((size_t)(E + 1) * sizeof(int32_t) 
 __global__ void mtile_prefix_kernel(const int32_t *__restrict__ group_offsets, int G, int32_t *__restrict__ mtile_start);
 
 inline uint32_t *ws_error_word(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
+// Blocks of the permutation's counting pass that have finished (header offset 4); the last
+// one to finish runs the scan and sets it back to zero.
+inline uint32_t *ws_done_counter(void *ws) { return reinterpret_cast<uint32_t *>(ws) + 1; }
 
 inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 

@@ -1,12 +1,12 @@
 // permute.cu -- A2: sync-free permutation of tokens into expert-contiguous rows.
 //
-// Three launches on one stream, no host round trip:
+// Two launches on one stream, no host round trip:
 //   1. count:   each 8192-route chunk counts its routes per expert and gives
 //               every route its stable rank among the chunk's routes to the
-//               same expert (warp match + per-warp running counts);
-//   2. scan:    one block turns the chunk counts into group sizes, (aligned)
-//               group offsets and each chunk's first row per expert;
-//   3. scatter: one warp per token writes dst_of_route / src_of_row and
+//               same expert (warp match + per-warp running counts); the last
+//               block to finish turns the chunk counts into group sizes,
+//               (aligned) group offsets and each chunk's first row per expert;
+//   2. scatter: one warp per token writes dst_of_route / src_of_row and
 //               copies the token's row once from HBM into its k destinations
 //               with 16-byte loads and stores.
 // (One-GPU counterpart of the expert-major dispatch layout with device-side
@@ -17,14 +17,86 @@
 namespace moe {
 namespace {
 
-constexpr int kScanThreads = 1024;
 constexpr int kScatterWarps = 8;
 
+// Group sizes, aligned offsets, each chunk's first row per expert (in place of
+// the chunk counts) and, if mtile_start != nullptr, each group's first 128-row
+// M-tile: one block (>= 256 threads), each thread owning up to 4 consecutive experts.
+__device__ void scan_groups(int32_t *chunk_counts, int64_t chunks, int E, int align, int32_t *group_sizes,
+                            int32_t *group_offsets, int32_t *mtile_start) {
+    __shared__ int32_t s_wsum[32], s_wtile[32];
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (E + nt - 1) / nt;
+    const int e0 = tid * per;
+    int tot[4] = {0, 0, 0, 0};
+    int pad_sum = 0, tile_sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = e0 + i;
+        if (i < per && e < E) {
+#pragma unroll 8
+            for (int64_t c = 0; c < chunks; ++c) tot[i] += __ldcg(chunk_counts + c * E + e);
+            const int padded = (tot[i] + align - 1) / align * align;
+            pad_sum += padded;
+            tile_sum += (padded + 127) / 128;
+        }
+    }
+    int incl = pad_sum, tincl = tile_sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off), ot = __shfl_up_sync(0xFFFFFFFFu, tincl, off);
+        if (lane >= off) { incl += o; tincl += ot; }
+    }
+    if (lane == 31) { s_wsum[warp] = incl; s_wtile[warp] = tincl; }
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = (nt + 31) / 32;
+        int v = lane < nw ? s_wsum[lane] : 0, vt = lane < nw ? s_wtile[lane] : 0;
+        int vi = v, vti = vt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, vi, off), ot = __shfl_up_sync(0xFFFFFFFFu, vti, off);
+            if (lane >= off) { vi += o; vti += ot; }
+        }
+        if (lane < nw) { s_wsum[lane] = vi - v; s_wtile[lane] = vti - vt; }
+    }
+    __syncthreads();
+    int run = incl - pad_sum + s_wsum[warp];
+    int trun = tincl - tile_sum + s_wtile[warp];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = e0 + i;
+        if (i < per && e < E) {
+            group_sizes[e] = tot[i];
+            group_offsets[e] = run;
+            if (mtile_start) mtile_start[e] = trun;
+            int r2 = run;
+            for (int64_t c = 0; c < chunks; ++c) {
+                const int v = __ldcg(chunk_counts + c * E + e);
+                chunk_counts[c * E + e] = r2;
+                r2 += v;
+            }
+            const int padded = (tot[i] + align - 1) / align * align;
+            run += padded;
+            trun += (padded + 127) / 128;
+            if (e == E - 1) {
+                group_offsets[E] = run;
+                if (mtile_start) mtile_start[E] = trun;
+            }
+        }
+    }
+}
+
+// Counting pass: per 8192-route chunk, stable ranks (warp match + per-warp running
+// counts) and per-expert chunk counts; the last block to finish runs scan_groups,
+// so that offsets are ready when the kernel ends (no separate scan launch).
 __global__ void __launch_bounds__(kPermWarps * 32)
-permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E,
+permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E, int align,
                      int32_t *__restrict__ local_rank, int32_t *__restrict__ chunk_counts,
-                     uint32_t *err) {
+                     int32_t *__restrict__ group_sizes, int32_t *__restrict__ group_offsets,
+                     int32_t *__restrict__ mtile_start, uint32_t *done, uint32_t *err) {
     extern __shared__ int32_t s_cnt[];   // [kPermWarps][E] running counts
+    __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) s_cnt[i] = 0;
     __syncthreads();
@@ -74,53 +146,36 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E,
         const int64_t r = w0 + step * 32 + lane;
         if (r < R) local_rank[r] = rk[step] >= 0 ? rk[step] + s_cnt[warp * E + ev[step]] : -1;
     }
+    // the last block to finish turns all chunk counts into offsets
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    scan_groups(chunk_counts, gridDim.x, E, align, group_sizes, group_offsets, mtile_start);
+    if (threadIdx.x == 0) *done = 0u;
 }
 
-// Group sizes, aligned offsets, and per-chunk first rows (in place of the counts).
-__global__ void __launch_bounds__(kScanThreads)
+// The scan alone, for an empty problem (no counting blocks).
+__global__ void __launch_bounds__(256)
 permute_scan_kernel(int32_t *__restrict__ chunk_counts, int64_t chunks, int E, int align,
-                    int32_t *__restrict__ group_sizes, int32_t *__restrict__ group_offsets) {
-    __shared__ int32_t s_warp[kScanThreads / 32];
-    const int e = threadIdx.x;
-    int total = 0;
-    if (e < E) {
-#pragma unroll 8
-        for (int64_t c = 0; c < chunks; ++c) total += chunk_counts[c * E + e];
-    }
-    const int padded = e < E ? (total + align - 1) / align * align : 0;
-    // block exclusive scan of padded sizes
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int incl = padded;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-        int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
-        if (lane >= off) incl += o;
-    }
-    if (lane == 31) s_warp[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        int v = s_warp[lane];
-        int vi = v;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            int o = __shfl_up_sync(0xFFFFFFFFu, vi, off);
-            if (lane >= off) vi += o;
-        }
-        s_warp[lane] = vi - v;
-    }
-    __syncthreads();
-    const int excl = incl - padded + s_warp[warp];
-    if (e < E) {
-        group_sizes[e] = total;
-        group_offsets[e] = excl;
-        if (e == E - 1) group_offsets[E] = excl + padded;
-        int run = excl;
-        for (int64_t c = 0; c < chunks; ++c) {
-            int v = chunk_counts[c * E + e];
-            chunk_counts[c * E + e] = run;
-            run += v;
-        }
-    }
+                    int32_t *__restrict__ group_sizes, int32_t *__restrict__ group_offsets,
+                    int32_t *__restrict__ mtile_start) {
+    scan_groups(chunk_counts, chunks, E, align, group_sizes, group_offsets, mtile_start);
+}
+
+// Counting pass with the scan in its last block (or the scan alone for R = 0).
+moe_status_t count_and_scan(const int32_t *topk_idx, int64_t R, int E, int align, int32_t *local_rank,
+                            int32_t *counts, int32_t *group_sizes, int32_t *group_offsets, int32_t *mtile,
+                            uint32_t *done, uint32_t *err, cudaStream_t s) {
+    const int64_t chunks = perm_chunks(R);
+    if (chunks > 0)
+        permute_count_kernel<<<(unsigned)chunks, kPermWarps * 32, kPermWarps * E * sizeof(int32_t), s>>>(
+            topk_idx, R, E, align, local_rank, counts, group_sizes, group_offsets, mtile, done, err);
+    else
+        permute_scan_kernel<<<1, 256, 0, s>>>(counts, 0, E, align, group_sizes, group_offsets, mtile);
+    return launch_status();
 }
 
 // One warp per token: maps, then the row copied once into its k rows.
@@ -211,13 +266,9 @@ extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx
     uint32_t *err = ws_error_word(ws);
     int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsHeaderBytes);
     const int64_t chunks = perm_chunks(R);
-    if (chunks > 0) {
-        permute_count_kernel<<<(unsigned)chunks, kPermWarps * 32, kPermWarps * E * sizeof(int32_t), s>>>(
-            topk_idx, R, E, dst_of_route, counts, err);
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    }
-    permute_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, chunks, E, align, group_sizes, group_offsets);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (count_and_scan(topk_idx, R, E, align, dst_of_route, counts, group_sizes, group_offsets, nullptr,
+                       ws_done_counter(ws), err, s) != MOE_OK)
+        return MOE_ERR_CUDA;
     const int row_vecs = H / 8;
     if (T > 0) {
         const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
@@ -301,15 +352,12 @@ extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const in
     cudaStream_t s = (cudaStream_t)stream;
     uint32_t *err = static_cast<uint32_t *>(scratch);
     int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(scratch) + kWsHeaderBytes);
-    // the error word starts at zero on every call; the counts are fully rewritten
-    if (cudaMemsetAsync(err, 0, sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (chunks > 0) {
-        permute_count_kernel<<<(unsigned)chunks, kPermWarps * 32, kPermWarps * E * sizeof(int32_t), s>>>(
-            topk_idx, R, E, dst_of_route, counts, err);
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    }
-    permute_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, chunks, E, align, group_sizes, group_offsets);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    // the error word and the finished-blocks counter start at zero on every call; the
+    // counts are fully rewritten
+    if (cudaMemsetAsync(err, 0, 2 * sizeof(uint32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (count_and_scan(topk_idx, R, E, align, dst_of_route, counts, group_sizes, group_offsets, nullptr,
+                       err + 1, err, s) != MOE_OK)
+        return MOE_ERR_CUDA;
     const int row_vecs = H / 8;
     if (T > 0) {
         const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
@@ -430,15 +478,9 @@ extern "C" moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *to
     const int64_t chunks = perm_chunks(R);
     int32_t *counts = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsHeaderBytes);
     int32_t *mtile = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsHeaderBytes + ws_counts_bytes(chunks, E));
-    if (chunks > 0) {
-        permute_count_kernel<<<(unsigned)chunks, kPermWarps * 32, kPermWarps * E * sizeof(int32_t), s>>>(
-            topk_idx, R, E, dst_of_route, counts, err);
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    }
-    permute_scan_kernel<<<1, kScanThreads, 0, s>>>(counts, chunks, E, 1, group_sizes, group_offsets);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    mtile_prefix_kernel<<<1, 1024, 0, s>>>(group_offsets, E, mtile);
-    if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
+    if (count_and_scan(topk_idx, R, E, 1, dst_of_route, counts, group_sizes, group_offsets, mtile,
+                       ws_done_counter(ws), err, s) != MOE_OK)
+        return MOE_ERR_CUDA;
     if (T > 0) {
         const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
         permute_scatter_mx_kernel<<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(
