@@ -158,7 +158,7 @@ MOE_API moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx, i
  *     lives in a fixed 256 KiB array inside this library's device image,
  *     resident on every GPU that loads the library until the process exits;
  *   - problems whose scratch exceeds it are rejected with
- *     MOE_ERR_UNSUPPORTED: ceil(T*k / 8192) * E must be <= 65472;
+ *     MOE_ERR_UNSUPPORTED: ceil(T*k / 2048) * E must be <= 65472;
  *   - error_word: device uint32 out (nullable) that receives this call's
  *     device error bits (MOE_DEVERR_*), stream-ordered after the call.
  * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
@@ -280,11 +280,15 @@ MOE_API moe_status_t moe_grouped_quantize_mxfp8(const moe_bf16_t *in, int64_t ro
                                                 uint8_t *scale_rowmajor, uint8_t *scale_tiles, void *ws,
                                                 size_t ws_bytes, moe_stream_t stream);
 
-/* Quantise expert weights W bf16 [E, K, N] (N contiguous) along K: data uint8
- * [E, N, K] (K contiguous, the K-major operand of the MMA), scales in the
- * weights' tile layout ([E][K/128][N/128] atoms, E*K*N/32 bytes).  For
- * W_gate / W_up pass K = H, N = F; for W_down K = F, N = H.  Limits:
- * K % 128 == 0, N % 128 == 0. */
+/* Quantise expert weights W bf16 [E, K, N] (N contiguous) along K.  data:
+ * E*K*N bytes of E4M3 codes as the MMA's K-major operand, tiled: one
+ * contiguous 16 KB block per (expert, 128 K elements, 128 rows n), blocks
+ * ordered [E][K/128][N/128]; inside a block row r = n % 128 takes 128 bytes
+ * (the codes of k % 128 = 0..127) with its 16-byte chunk j stored at chunk
+ * j ^ (r % 8) (the 128-byte swizzle), so each block is one bulk copy.
+ * scales: the weights' tile layout ([E][K/128][N/128] 512-byte atoms,
+ * E*K*N/32 bytes).  For W_gate / W_up pass K = H, N = F; for W_down K = F,
+ * N = H.  Limits: K % 128 == 0, N % 128 == 0. */
 MOE_API moe_status_t moe_quantize_weights_mxfp8(const moe_bf16_t *W, int E, int K, int N, uint8_t *data,
                                                 uint8_t *scales, moe_stream_t stream);
 
@@ -303,9 +307,9 @@ MOE_API moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *topk_
  *   h = silu(x W_gate) * (x W_up) (fp32), quantised to MXFP8 along F:
  *       h_q uint8 [rows_cap, F], h_sf tile layout (moe_mx_tile_scale_bytes(rows_cap, E, F))
  *   y_perm = h W_down, fp32 [rows_cap, H]
- * x_q / x_sf from moe_permute_mxfp8; Wg_q, Wu_q uint8 [E, F, H] and Wd_q
- * uint8 [E, H, F] with scales from moe_quantize_weights_mxfp8.  All scale
- * pointers 16-byte aligned.  Limits: H % 128 == 0, F % 128 == 0, E <= 1024.
+ * x_q / x_sf from moe_permute_mxfp8; Wg_q, Wu_q (K = H, N = F) and Wd_q
+ * (K = F, N = H) with their scales from moe_quantize_weights_mxfp8.  All code
+ * and scale pointers 16-byte aligned.  Limits: H % 128 == 0, F % 128 == 0, E <= 1024.
  * moe_grouped_fc1_swiglu_mxfp8 and moe_grouped_fc2_mxfp8 are the two halves. */
 MOE_API moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,
                                                const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,

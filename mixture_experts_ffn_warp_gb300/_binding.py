@@ -384,11 +384,13 @@ def moe_grouped_quantize_mxfp8(x: torch.Tensor, group_offsets=None, ws: Workspac
 
 
 def moe_quantize_weights_mxfp8(W: torch.Tensor, stream=None):
-    """MXFP8 of expert weights [E, K, N] along K -> (data uint8 [E, N, K],
-    scales in the weights' tile layout, uint8 [E*K*N/32]) (moe.h)."""
+    """MXFP8 of expert weights [E, K, N] along K -> (codes, scales), both uint8
+    flat arrays in the MMA tile layout (moe.h): codes in 16 KB pre-swizzled
+    blocks of 128 rows n x 128 K bytes, scales in 512-byte atoms, both ordered
+    [E][K/128][N/128]."""
     _need(W, "W", torch.bfloat16)
     E, K, N = W.shape
-    data = torch.empty(E, N, K, dtype=torch.uint8, device=W.device)
+    data = torch.empty(E * N * K, dtype=torch.uint8, device=W.device)
     scales = torch.empty(E * K * N // 32, dtype=torch.uint8, device=W.device)
     _check("moe_quantize_weights_mxfp8", load_library().moe_quantize_weights_mxfp8(
         _ptr(W), E, K, N, _ptr(data), _ptr(scales), _stream(stream)))
@@ -433,7 +435,8 @@ def moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offs
                                  stream=None):
     """A3 on MXFP8 operands; h quantised to MXFP8 along F (moe.h)."""
     rows_cap, H = x_q.shape
-    E, F, _ = Wg_q.shape
+    E = group_offsets.shape[0] - 1
+    F = h_q.shape[1]
     _check("moe_grouped_fc1_swiglu_mxfp8", load_library().moe_grouped_fc1_swiglu_mxfp8(
         _ptr(x_q), _ptr(x_sf), _ptr(Wg_q), _ptr(Wg_sf), _ptr(Wu_q), _ptr(Wu_sf), _ptr(group_offsets), E, H, F,
         rows_cap, _ptr(h_q), _ptr(h_sf), _ptr(ws.buf), ws.nbytes, _stream(stream)))
@@ -442,7 +445,8 @@ def moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offs
 def moe_grouped_fc2_mxfp8(h_q, h_sf, Wd_q, Wd_sf, group_offsets, ws: Workspace, y_perm, stream=None):
     """A4 on MXFP8 operands, fp32 output (moe.h)."""
     rows_cap, F = h_q.shape
-    E, H, _ = Wd_q.shape
+    E = group_offsets.shape[0] - 1
+    H = y_perm.shape[1]
     _check("moe_grouped_fc2_mxfp8", load_library().moe_grouped_fc2_mxfp8(
         _ptr(h_q), _ptr(h_sf), _ptr(Wd_q), _ptr(Wd_sf), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
         _ptr(ws.buf), ws.nbytes, _stream(stream)))

@@ -15,8 +15,8 @@ constexpr size_t kWsHeaderBytes = 256;
 
 // Routes per chunk of the permutation's counting pass.
 constexpr int kPermWarps = 8;
-constexpr int kPermSteps = 32;
-constexpr int kPermChunk = kPermWarps * 32 * kPermSteps;   // 8192 routes
+constexpr int kPermSteps = 8;
+constexpr int kPermChunk = kPermWarps * 32 * kPermSteps;   // 2048 routes
 
 inline int64_t perm_chunks(int64_t R) { return (R + kPermChunk - 1) / kPermChunk; }
 

@@ -1,6 +1,8 @@
 // ffn_mx.cu -- A7: the grouped expert FFN on MXFP8 operands (E4M3 data, UE8M0 scales
 // per 32 K elements) with block-scaled tcgen05 MMAs.  FC1 quantises h to MXFP8
-// along F in its epilogue; FC2 writes fp32 expert outputs.
+// along F in its epilogue; FC2 writes fp32 expert outputs.  Activation tiles come
+// in by TMA; weight tiles (pre-swizzled 16 KB blocks from moe_quantize_weights_mxfp8)
+// and all scale atoms by plain bulk copies.
 #include "gemm_launch.cuh"
 
 using namespace moe;
@@ -30,11 +32,10 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const u
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!x_q || !x_sf || !Wg_q || !Wg_sf || !Wu_q || !Wu_sf || !group_offsets || !h_q || !h_sf)
         return MOE_ERR_INVALID_ARG;
-    if (!aligned16(x_sf) || !aligned16(Wg_sf) || !aligned16(Wu_sf)) return MOE_ERR_UNSUPPORTED;
-    CUtensorMap tA, tB0, tB1;
-    if (!tmap_u8_2d(&tA, x_q, H, rows_cap, H, 128, 128) || !tmap_u8_3d(&tB0, Wg_q, H, F, E, 128, 128) ||
-        !tmap_u8_3d(&tB1, Wu_q, H, F, E, 128, 128))
+    if (!aligned16(x_sf) || !aligned16(Wg_sf) || !aligned16(Wu_sf) || !aligned16(Wg_q) || !aligned16(Wu_q))
         return MOE_ERR_UNSUPPORTED;
+    CUtensorMap tA;
+    if (!tmap_u8_2d(&tA, x_q, H, rows_cap, H, 128, 128)) return MOE_ERR_UNSUPPORTED;
     gg::Args a{};
     a.group_offsets = group_offsets;
     a.E = E;
@@ -45,12 +46,14 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const u
     a.sfa = x_sf;
     a.sfb0 = Wg_sf;
     a.sfb1 = Wu_sf;
+    a.b0_tiles = Wg_q;
+    a.b1_tiles = Wu_q;
     a.nb_rows = F;
     a.out_q = h_q;
     a.ld0 = F;
     a.out_sf = h_sf;
     a.err = ws_error_word(ws);
-    return gg::launch<Op::FC1_MX, 256>(tA, tB0, tB1, a, mblock_bound(rows_cap, E) * a.n_tiles, (cudaStream_t)stream);
+    return gg::launch<Op::FC1_MX, 256>(tA, tA, tA, a, mblock_bound(rows_cap, E) * a.n_tiles, (cudaStream_t)stream);
 }
 
 extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
@@ -60,11 +63,10 @@ extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t 
     moe_status_t st = check_mx(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!h_q || !h_sf || !Wd_q || !Wd_sf || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
-    if (!aligned16(h_sf) || !aligned16(Wd_sf)) return MOE_ERR_UNSUPPORTED;
+    if (!aligned16(h_sf) || !aligned16(Wd_sf) || !aligned16(Wd_q)) return MOE_ERR_UNSUPPORTED;
     const int bn = (H % 256 == 0) ? 256 : 128;
-    CUtensorMap tA, tB;
-    if (!tmap_u8_2d(&tA, h_q, F, rows_cap, F, 128, 128) || !tmap_u8_3d(&tB, Wd_q, F, H, E, 128, bn))
-        return MOE_ERR_UNSUPPORTED;
+    CUtensorMap tA;
+    if (!tmap_u8_2d(&tA, h_q, F, rows_cap, F, 128, 128)) return MOE_ERR_UNSUPPORTED;
     gg::Args a{};
     a.group_offsets = group_offsets;
     a.E = E;
@@ -74,13 +76,14 @@ extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t 
     a.rows_cap = rows_cap;
     a.sfa = h_sf;
     a.sfb0 = Wd_sf;
+    a.b0_tiles = Wd_q;
     a.nb_rows = H;
     a.out_f32 = y_perm;
     a.ld0 = H;
     a.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
-    if (bn == 256) return gg::launch<Op::FC2_MX, 256>(tA, tB, tB, a, bound, (cudaStream_t)stream);
-    return gg::launch<Op::FC2_MX, 128>(tA, tB, tB, a, bound, (cudaStream_t)stream);
+    if (bn == 256) return gg::launch<Op::FC2_MX, 256>(tA, tA, tA, a, bound, (cudaStream_t)stream);
+    return gg::launch<Op::FC2_MX, 128>(tA, tA, tA, a, bound, (cudaStream_t)stream);
 }
 
 extern "C" moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,

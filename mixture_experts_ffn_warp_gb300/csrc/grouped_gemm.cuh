@@ -78,6 +78,8 @@ struct Args {
     const uint8_t *sfa;
     const uint8_t *sfb0;
     const uint8_t *sfb1;
+    const uint8_t *b0_tiles;   // MXFP8: weight codes in 16 KB pre-swizzled blocks [E][K/128][N_B/128]
+    const uint8_t *b1_tiles;   // FC1_MX: the W_up codes
     int nb_rows;          // MXFP8: rows (N) of each expert's B matrix
     uint8_t *out_q;       // FC1_MX: quantised h [rows, N] (E4M3)
     uint8_t *out_sf;      // FC1_MX: h scales in tile layout [mtile][N/128][512]
@@ -297,18 +299,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         const int kblocks = args.K / 128;
                         sm100::tma_load_2d(sa, &tmA, fb, k0, tl.m0);
                         sm100::bulk_load(ssf, args.sfa + ((int64_t)tl.mtile * kblocks + kb) * 512, 512, fb);
+                        // weights: contiguous pre-swizzled 16 KB code blocks and 512-byte scale
+                        // atoms, both ordered [E][K/128][N/128] -> plain bulk copies
                         const int nblk = args.nb_rows / 128;
-                        const int64_t sfb_atom = ((int64_t)tl.e * kblocks + kb) * nblk;
+                        const int64_t blk = ((int64_t)tl.e * kblocks + kb) * nblk + tl.n0 / 128;
                         if constexpr (OP == Op::FC1_MX) {
-                            // 128 gate rows then 128 up rows of the weights, with their scale atoms
-                            sm100::tma_load_3d(sb, &tmB0, fb, k0, tl.n0, tl.e);
-                            sm100::tma_load_3d(sb + 16384, &tmB1, fb, k0, tl.n0, tl.e);
-                            sm100::bulk_load(ssf + 512, args.sfb0 + (sfb_atom + tl.n0 / 128) * 512, 512, fb);
-                            sm100::bulk_load(ssf + 1024, args.sfb1 + (sfb_atom + tl.n0 / 128) * 512, 512, fb);
+                            // 128 gate rows then 128 up rows, with their scale atoms
+                            sm100::bulk_load(sb, args.b0_tiles + blk * 16384, 16384, fb);
+                            sm100::bulk_load(sb + 16384, args.b1_tiles + blk * 16384, 16384, fb);
+                            sm100::bulk_load(ssf + 512, args.sfb0 + blk * 512, 512, fb);
+                            sm100::bulk_load(ssf + 1024, args.sfb1 + blk * 512, 512, fb);
                         } else {
-                            sm100::tma_load_3d(sb, &tmB0, fb, k0, tl.n0, tl.e);
-                            sm100::bulk_load(ssf + 512, args.sfb0 + (sfb_atom + tl.n0 / 128) * 512,
-                                             (BN / 128) * 512, fb);
+                            sm100::bulk_load(sb, args.b0_tiles + blk * 16384, (BN / 128) * 16384, fb);
+                            sm100::bulk_load(ssf + 512, args.sfb0 + blk * 512, (BN / 128) * 512, fb);
                         }
                     } else if constexpr (TR::k_grouped) {
                         const int krow = tl.k_row0 + k0;

@@ -1,9 +1,9 @@
 // permute.cu -- A2: sync-free permutation of tokens into expert-contiguous rows.
 //
 // Two launches on one stream, no host round trip:
-//   1. count:   each 8192-route chunk counts its routes per expert and gives
+//   1. count:   each 2048-route chunk counts its routes per expert and gives
 //               every route its stable rank among the chunk's routes to the
-//               same expert (warp match + per-warp running counts); the last
+//               same expert (bit-sliced warp ballots + per-warp running counts); the last
 //               block to finish turns the chunk counts into group sizes,
 //               (aligned) group offsets and each chunk's first row per expert;
 //   2. scatter: one warp per token writes dst_of_route / src_of_row and
@@ -87,7 +87,7 @@ __device__ void scan_groups(int32_t *chunk_counts, int64_t chunks, int E, int al
     }
 }
 
-// Counting pass: per 8192-route chunk, stable ranks (warp match + per-warp running
+// Counting pass: per 2048-route chunk, stable ranks (warp ballots + per-warp running
 // counts) and per-expert chunk counts; the last block to finish runs scan_groups,
 // so that offsets are ready when the kernel ends (no separate scan launch).
 __global__ void __launch_bounds__(kPermWarps * 32)
@@ -105,6 +105,7 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E, int
     const int64_t w0 = chunk0 + (int64_t)warp * 32 * kPermSteps;
     int32_t *cnt = s_cnt + warp * E;
     const unsigned lt_mask = (1u << lane) - 1u;
+    const int id_bits = 32 - __clz(E);
     // all of this warp's route ids first (independent loads), then the ranks from registers
     int ev[kPermSteps], rk[kPermSteps];
 #pragma unroll
@@ -120,7 +121,13 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E, int
             e = -1;
         }
         ev[step] = e;
-        const unsigned peers = __match_any_sync(0xFFFFFFFFu, e);
+        // lanes holding the same id: AND of the ballots of each bit of e + 1 (in [0, E])
+        unsigned peers = 0xFFFFFFFFu;
+        const unsigned v = (unsigned)(e + 1);
+        for (int b = 0; b < id_bits; ++b) {
+            const unsigned bal = __ballot_sync(0xFFFFFFFFu, (v >> b) & 1u);
+            peers &= ((v >> b) & 1u) ? bal : ~bal;
+        }
         int rank = -1;
         if (e >= 0) rank = cnt[e] + __popc(peers & lt_mask);
         __syncwarp();
@@ -298,7 +305,7 @@ namespace {
 
 // 256 KiB: a 256-byte header (error word at offset 0) and room for
 // (256 KiB - 256) / 4 = 65472 per-chunk counts, i.e. chunks * E <= 65472
-// with 8192 routes per chunk.  Every GPU that loads the library keeps this
+// with 2048 routes per chunk.  Every GPU that loads the library keeps this
 // array resident until the process exits.
 constexpr size_t kStaticScratchBytes = 256 * 1024;
 static __device__ __align__(256) unsigned char g_permute_scratch[kStaticScratchBytes];

@@ -113,7 +113,10 @@ quantize_rows_kernel(const __nv_bfloat16 *__restrict__ in, int64_t rows, int K,
 
 // Weights: W[e] is [K, N] (N contiguous).  Block (e, n-tile of 64, k-block of 32):
 // stage [32][64] bf16 in smem, each of 64 threads quantises one column's 32 values,
-// writes 32 bytes of data[e][n][k..k+32) and one scale byte.
+// writes the 32 codes of (n, k..k+32) and one scale byte.  Codes go to the tiled
+// layout: for every (expert, 128 K bytes, 128 rows n) one contiguous 16 KB block of
+// 128 rows x 128 bytes, 16-byte chunk j of row r stored at chunk j ^ (r % 8) (the
+// 128-byte swizzle of the MMA's K-major operand), blocks ordered [E][K/128][N/128].
 __global__ void __launch_bounds__(64)
 quantize_weights_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N, uint8_t *__restrict__ data,
                         uint8_t *__restrict__ scales) {
@@ -130,12 +133,13 @@ quantize_weights_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N, uint8
     uint4 lo, hi;
     mx::quantize32(v, X, lo, hi);
     const int n = n0 + t;
-    uint4 *d = reinterpret_cast<uint4 *>(data + ((int64_t)e * N + n) * K + (int64_t)kb * 32);
-    d[0] = lo;
-    d[1] = hi;
-    // atoms ordered [e][K/128][N/128], tile row = n % 128
+    // atoms and code blocks ordered [e][K/128][N/128], tile row = n % 128
     const int64_t atom = ((int64_t)e * (K / 128) + kb / 4) * (N / 128) + n / 128;
     const int m = n % 128;
+    uint8_t *blk = data + atom * 16384 + m * 128;
+    const int c0 = (kb % 4) * 2;   // the two 16-byte chunks of this 32-code run
+    *reinterpret_cast<uint4 *>(blk + ((c0 ^ (m % 8)) * 16)) = lo;
+    *reinterpret_cast<uint4 *>(blk + (((c0 + 1) ^ (m % 8)) * 16)) = hi;
     scales[atom * 512 + (m % 32) * 16 + (m / 32) * 4 + (kb % 4)] = (uint8_t)(X + 127);
 }
 

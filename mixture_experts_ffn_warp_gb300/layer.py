@@ -135,9 +135,9 @@ class MxWeights:
     """Expert weights quantised once to MXFP8 (K-major codes + tile-layout scales)."""
 
     def __init__(self, W_gate, W_up, W_down, stream=None):
-        self.Wg_q, self.Wg_sf = moe_quantize_weights_mxfp8(W_gate, stream)   # [E, F, H]
+        self.Wg_q, self.Wg_sf = moe_quantize_weights_mxfp8(W_gate, stream)   # K = H, N = F
         self.Wu_q, self.Wu_sf = moe_quantize_weights_mxfp8(W_up, stream)
-        self.Wd_q, self.Wd_sf = moe_quantize_weights_mxfp8(W_down, stream)   # [E, H, F]
+        self.Wd_q, self.Wd_sf = moe_quantize_weights_mxfp8(W_down, stream)   # K = F, N = H
 
 
 class MoeForwardMX:

@@ -48,8 +48,8 @@ def test_status_strings_and_version(lib):
 
 
 def test_workspace_bytes(lib):
-    # header + per-chunk counts (24576 routes -> 3 chunks of 8192) + M-tile prefix, 16-byte rounded
-    assert lib.moe_workspace_bytes(4096, 64, 6) == 256 + 3 * 64 * 4 + 272
+    # header + per-chunk counts (24576 routes -> 12 chunks of 2048) + M-tile prefix, 16-byte rounded
+    assert lib.moe_workspace_bytes(4096, 64, 6) == 256 + 12 * 64 * 4 + 272
     assert lib.moe_workspace_bytes(0, 8, 2) == 256 + 0 + 48
     assert lib.moe_workspace_bytes(10, 0, 2) == 0
     assert lib.moe_workspace_bytes(10, 8, 33) == 0

@@ -42,6 +42,16 @@ def weight_scales_rowmajor(sf: np.ndarray, E: int, K: int, N: int) -> np.ndarray
     return sf[off]
 
 
+def weight_codes_nk(data: torch.Tensor, e: int, K: int, N: int) -> np.ndarray:
+    """Codes of expert e as [N, K] from the tiled layout: 16 KB blocks ordered
+    [K/128][N/128], row r of a block holding its 16-byte chunk j at j ^ (r % 8)."""
+    blk = data[e * K * N:(e + 1) * K * N].cpu().numpy().reshape(K // 128, N // 128, 128, 8, 16)
+    r = np.arange(128)[:, None]
+    phys = np.arange(8)[None, :] ^ (r % 8)                      # [r, logical chunk] -> stored chunk
+    logical = blk[:, :, r, phys, :]                             # [KB, NB, 128, 8, 16]
+    return np.ascontiguousarray(logical.transpose(1, 2, 0, 3, 4)).reshape(N, K)
+
+
 def _special_rows(g, rows, K):
     x = torch.randn(rows, K, generator=g, device="cuda", dtype=torch.float32)
     x[0] = 0.0                                    # amax = 0 blocks
@@ -89,7 +99,7 @@ def test_quantize_weights_bit_exact():
     wb = bits(W)
     for e in range(E):
         rd, rs = oracle.quantize_cols_mxfp8(wb[e])
-        assert np.array_equal(data[e].cpu().numpy(), rd)
+        assert np.array_equal(weight_codes_nk(data, e, K, N), rd)
         assert np.array_equal(rs_all[e], rs)
 
 
@@ -169,8 +179,8 @@ def test_mxfp8_forward_dsv3_full_size_sampled():
     # the GPU's weight codes for two of those experts, bit for bit
     for e in experts[:2]:
         e = int(e)
-        assert np.array_equal(w.Wg_q[e].cpu().numpy(), q["gq"][e])
-        assert np.array_equal(w.Wd_q[e].cpu().numpy(), q["dq"][e])
+        assert np.array_equal(weight_codes_nk(w.Wg_q, e, shape.H, shape.F), q["gq"][e])
+        assert np.array_equal(weight_codes_nk(w.Wd_q, e, shape.F, shape.H), q["dq"][e])
     ref = oracle.moe_fwd_mxfp8(bits(inp["x"]), q["gq"], q["gs"], q["uq"], q["us"], q["dq"], q["ds"], idx, tw,
                                tokens=toks, round_mode=2)
     assert_close_rms(to_f64(out[torch.from_numpy(toks).cuda()]), ref["out"], tol=TOL_MXFP8, what="dsv3 out")

@@ -96,7 +96,7 @@ def test_static_scratch_reports_bad_ids_and_clears_them():
 def test_static_scratch_rejects_problems_beyond_the_array():
     L = load_library()
     nul = C.c_void_p(16)
-    # ceil(T*k / 8192) * E > 65472  ->  MOE_ERR_UNSUPPORTED before any launch
+    # ceil(T*k / 2048) * E > 65472  ->  MOE_ERR_UNSUPPORTED before any launch
     T, E, k = 600000, 1024, 1
     st = L.moe_permute_static_scratch(nul, nul, T, 64, E, k, 1, nul, T * k, nul, nul, nul, nul, None,
                                       C.c_void_p(torch.cuda.current_stream().cuda_stream))
