@@ -147,8 +147,9 @@ extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm,
     if (!dy_perm || !W_down || !fc1_c || !group_offsets || !dgu) return MOE_ERR_INVALID_ARG;
     const int bn = (F % 256 == 0) ? 256 : 128;
     // A = dy_perm [rows, H] (K-major), B = W_down[e] as [F rows][H] (K-major)
-    CUtensorMap tA, tB;
-    if (!tmap_bf16_2d(&tA, dy_perm, H, rows_cap, H, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, bn))
+    CUtensorMap tA, tB, tC;
+    if (!tmap_bf16_2d(&tA, dy_perm, H, rows_cap, H, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, bn) ||
+        !tmap_store_2d(&tC, dgu, 2, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F))
         return MOE_ERR_UNSUPPORTED;
     gg::Args a{};
     a.group_offsets = group_offsets;
@@ -163,8 +164,8 @@ extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm,
     a.ld_aux = 2 * (int64_t)F;
     a.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
-    if (bn == 256) return gg::launch<Op::DGRAD_DSWIGLU, 256>(tA, tB, tB, a, bound, (cudaStream_t)stream);
-    return gg::launch<Op::DGRAD_DSWIGLU, 128>(tA, tB, tB, a, bound, (cudaStream_t)stream);
+    if (bn == 256) return gg::launch<Op::DGRAD_DSWIGLU, 256>(tA, tB, tB, tC, tC, a, bound, (cudaStream_t)stream);
+    return gg::launch<Op::DGRAD_DSWIGLU, 128>(tA, tB, tB, tC, tC, a, bound, (cudaStream_t)stream);
 }
 
 extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_bf16_t *W_gate,
@@ -176,9 +177,10 @@ extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_b
     if (!dgu || !W_gate || !W_up || !group_offsets || !dx_perm) return MOE_ERR_INVALID_ARG;
     const int bn = (H % 256 == 0) ? 256 : 128;
     // A = [dg | du] [rows, 2F] (K-major), B = W_gate[e] / W_up[e] as [H rows][F] (K-major)
-    CUtensorMap tA, tB0, tB1;
+    CUtensorMap tA, tB0, tB1, tC;
     if (!tmap_bf16_2d(&tA, dgu, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F, 64, 128) ||
-        !tmap_bf16_3d(&tB0, W_gate, F, H, E, 64, bn) || !tmap_bf16_3d(&tB1, W_up, F, H, E, 64, bn))
+        !tmap_bf16_3d(&tB0, W_gate, F, H, E, 64, bn) || !tmap_bf16_3d(&tB1, W_up, F, H, E, 64, bn) ||
+        !tmap_store_2d(&tC, dx_perm, 4, H, rows_cap, H))
         return MOE_ERR_UNSUPPORTED;
     gg::Args a{};
     a.group_offsets = group_offsets;
@@ -192,8 +194,8 @@ extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_b
     a.ld0 = H;
     a.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
-    if (bn == 256) return gg::launch<Op::DGRAD_FC1, 256>(tA, tB0, tB1, a, bound, (cudaStream_t)stream);
-    return gg::launch<Op::DGRAD_FC1, 128>(tA, tB0, tB1, a, bound, (cudaStream_t)stream);
+    if (bn == 256) return gg::launch<Op::DGRAD_FC1, 256>(tA, tB0, tB1, tC, tC, a, bound, (cudaStream_t)stream);
+    return gg::launch<Op::DGRAD_FC1, 128>(tA, tB0, tB1, tC, tC, a, bound, (cudaStream_t)stream);
 }
 
 extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf16_t *h, const moe_bf16_t *dy_perm,
@@ -215,8 +217,9 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
     const uint64_t rows = (uint64_t)rows_cap;
     {   // dW_down[e] [F, H] = h_e^T dy_e: A = h (MN-major), B = dy_perm (MN-major)
         const int bn = (H % 256 == 0) ? 256 : 128;
-        CUtensorMap tA, tB;
-        if (!tmap_bf16_2d(&tA, h, F, rows, F, 64, 64) || !tmap_bf16_2d(&tB, dy_perm, H, rows, H, 64, 64))
+        CUtensorMap tA, tB, tC;
+        if (!tmap_bf16_2d(&tA, h, F, rows, F, 64, 64) || !tmap_bf16_2d(&tB, dy_perm, H, rows, H, 64, 64) ||
+            !tmap_store_2d(&tC, dW_down, 4, H, (uint64_t)E * F, H))
             return MOE_ERR_UNSUPPORTED;
         gg::Args a{};
         a.group_offsets = group_offsets;
@@ -231,14 +234,15 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
         a.expert_stride = (int64_t)F * H;
         a.err = ws_error_word(ws);
         const int64_t tiles = (int64_t)E * a.m_tiles * a.n_tiles;
-        st = (bn == 256) ? gg::launch<Op::WGRAD_DOWN, 256>(tA, tB, tB, a, tiles, s)
-                         : gg::launch<Op::WGRAD_DOWN, 128>(tA, tB, tB, a, tiles, s);
+        st = (bn == 256) ? gg::launch<Op::WGRAD_DOWN, 256>(tA, tB, tB, tC, tC, a, tiles, s)
+                         : gg::launch<Op::WGRAD_DOWN, 128>(tA, tB, tB, tC, tC, a, tiles, s);
         if (st != MOE_OK) return st;
     }
     {   // [dW_gate | dW_up][e] [H, 2F] = x_e^T [dg | du]_e: A = x_perm (MN-major), B = dgu (MN-major)
-        CUtensorMap tA, tB;
+        CUtensorMap tA, tB, tC0, tC1;
         if (!tmap_bf16_2d(&tA, x_perm, H, rows, H, 64, 64) ||
-            !tmap_bf16_2d(&tB, dgu, 2 * (uint64_t)F, rows, 2 * (uint64_t)F, 64, 64))
+            !tmap_bf16_2d(&tB, dgu, 2 * (uint64_t)F, rows, 2 * (uint64_t)F, 64, 64) ||
+            !tmap_store_2d(&tC0, dW_gate, 4, F, (uint64_t)E * H, F) || !tmap_store_2d(&tC1, dW_up, 4, F, (uint64_t)E * H, F))
             return MOE_ERR_UNSUPPORTED;
         gg::Args a{};
         a.group_offsets = group_offsets;
@@ -256,7 +260,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
         a.expert_stride = (int64_t)H * F;
         a.err = ws_error_word(ws);
         const int64_t tiles = (int64_t)E * a.m_tiles * a.n_tiles;
-        return gg::launch<Op::WGRAD_GATEUP, 256>(tA, tB, tB, a, tiles, s);
+        return gg::launch<Op::WGRAD_GATEUP, 256>(tA, tB, tB, tC0, tC1, a, tiles, s);
     }
 }
 

@@ -27,9 +27,13 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const m
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!x_perm || !W_gate || !W_up || !group_offsets || !h) return MOE_ERR_INVALID_ARG;
     // [rows, H] x [H, F] (gate | up) -> h [rows, F]; 128 gate + 128 up columns per tile
-    CUtensorMap tA, tB0, tB1;
+    CUtensorMap tA, tB0, tB1, tC0, tC1;
     if (!tmap_bf16_2d(&tA, x_perm, H, rows_cap, H, 64, 128) ||
-        !tmap_bf16_3d(&tB0, W_gate, F, H, E, 64, 64) || !tmap_bf16_3d(&tB1, W_up, F, H, E, 64, 64))
+        !tmap_bf16_3d(&tB0, W_gate, F, H, E, 64, 64) || !tmap_bf16_3d(&tB1, W_up, F, H, E, 64, 64) ||
+        !tmap_store_2d(&tC0, h, 2, F, rows_cap, F))
+        return MOE_ERR_UNSUPPORTED;
+    tC1 = tC0;
+    if (fc1_c && !tmap_store_2d(&tC1, fc1_c, 2, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F))
         return MOE_ERR_UNSUPPORTED;
     gg::Args a{};
     a.group_offsets = group_offsets;
@@ -43,7 +47,7 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const m
     a.out1 = reinterpret_cast<__nv_bfloat16 *>(fc1_c);
     a.ld1 = 2 * (int64_t)F;
     a.err = ws_error_word(ws);
-    return gg::launch<Op::FC1_SWIGLU, 256>(tA, tB0, tB1, a, mblock_bound(rows_cap, E) * a.n_tiles,
+    return gg::launch<Op::FC1_SWIGLU, 256>(tA, tB0, tB1, tC0, tC1, a, mblock_bound(rows_cap, E) * a.n_tiles,
                                            (cudaStream_t)stream);
 }
 
@@ -56,8 +60,9 @@ extern "C" moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W
     if (!h || !W_down || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
     // h [rows, F] x W_down [F, H] -> y_perm [rows, H]
     const int bn = (H % 256 == 0) ? 256 : 128;
-    CUtensorMap tA, tB;
-    if (!tmap_bf16_2d(&tA, h, F, rows_cap, F, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, 64))
+    CUtensorMap tA, tB, tC;
+    if (!tmap_bf16_2d(&tA, h, F, rows_cap, F, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, 64) ||
+        !tmap_store_2d(&tC, y_perm, 4, H, rows_cap, H))
         return MOE_ERR_UNSUPPORTED;
     gg::Args b{};
     b.group_offsets = group_offsets;
@@ -70,8 +75,8 @@ extern "C" moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W
     b.ld0 = H;
     b.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * b.n_tiles;
-    if (bn == 256) return gg::launch<Op::FC2, 256>(tA, tB, tB, b, bound, (cudaStream_t)stream);
-    return gg::launch<Op::FC2, 128>(tA, tB, tB, b, bound, (cudaStream_t)stream);
+    if (bn == 256) return gg::launch<Op::FC2, 256>(tA, tB, tB, tC, tC, b, bound, (cudaStream_t)stream);
+    return gg::launch<Op::FC2, 128>(tA, tB, tB, tC, tC, b, bound, (cudaStream_t)stream);
 }
 
 extern "C" moe_status_t moe_grouped_ffn_fwd(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,

@@ -34,8 +34,9 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const u
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(x_sf) || !aligned16(Wg_sf) || !aligned16(Wu_sf) || !aligned16(Wg_q) || !aligned16(Wu_q))
         return MOE_ERR_UNSUPPORTED;
-    CUtensorMap tA;
-    if (!tmap_u8_2d(&tA, x_q, H, rows_cap, H, 128, 128)) return MOE_ERR_UNSUPPORTED;
+    CUtensorMap tA, tC;
+    if (!tmap_u8_2d(&tA, x_q, H, rows_cap, H, 128, 128) || !tmap_store_2d(&tC, h_q, 1, F, rows_cap, F))
+        return MOE_ERR_UNSUPPORTED;
     gg::Args a{};
     a.group_offsets = group_offsets;
     a.E = E;
@@ -53,7 +54,8 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const u
     a.ld0 = F;
     a.out_sf = h_sf;
     a.err = ws_error_word(ws);
-    return gg::launch<Op::FC1_MX, 256>(tA, tA, tA, a, mblock_bound(rows_cap, E) * a.n_tiles, (cudaStream_t)stream);
+    return gg::launch<Op::FC1_MX, 256>(tA, tA, tA, tC, tC, a, mblock_bound(rows_cap, E) * a.n_tiles,
+                                       (cudaStream_t)stream);
 }
 
 extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
@@ -65,8 +67,9 @@ extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t 
     if (!h_q || !h_sf || !Wd_q || !Wd_sf || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
     if (!aligned16(h_sf) || !aligned16(Wd_sf) || !aligned16(Wd_q)) return MOE_ERR_UNSUPPORTED;
     const int bn = (H % 256 == 0) ? 256 : 128;
-    CUtensorMap tA;
-    if (!tmap_u8_2d(&tA, h_q, F, rows_cap, F, 128, 128)) return MOE_ERR_UNSUPPORTED;
+    CUtensorMap tA, tC;
+    if (!tmap_u8_2d(&tA, h_q, F, rows_cap, F, 128, 128) || !tmap_store_2d(&tC, y_perm, 4, H, rows_cap, H))
+        return MOE_ERR_UNSUPPORTED;
     gg::Args a{};
     a.group_offsets = group_offsets;
     a.E = E;
@@ -82,8 +85,8 @@ extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t 
     a.ld0 = H;
     a.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
-    if (bn == 256) return gg::launch<Op::FC2_MX, 256>(tA, tA, tA, a, bound, (cudaStream_t)stream);
-    return gg::launch<Op::FC2_MX, 128>(tA, tA, tA, a, bound, (cudaStream_t)stream);
+    if (bn == 256) return gg::launch<Op::FC2_MX, 256>(tA, tA, tA, tC, tC, a, bound, (cudaStream_t)stream);
+    return gg::launch<Op::FC2_MX, 128>(tA, tA, tA, tC, tC, a, bound, (cudaStream_t)stream);
 }
 
 extern "C" moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,

@@ -8,7 +8,8 @@
 //               instruction for bf16, K=32 for E4M3); fp32 accumulators live in
 //               TMEM (double-buffered for bf16, single for MXFP8, whose scales
 //               take the other half of TMEM)
-//   warps 2..5  epilogue: tcgen05.ld -> fused activation -> stores
+//   warps 2..5  epilogue: tcgen05.ld -> fused activation -> swizzled smem slots ->
+//               TMA stores (row by row only for a warp whose rows cross a group end)
 // Tiles are scheduled on the device from group_offsets (no host round trip).
 //
 // Ops (A row = one permuted route unless stated):
@@ -93,12 +94,17 @@ struct Cfg {
     static constexpr int B_BYTES = BN * 128;
     static constexpr int SF_BYTES = MX ? 512 + (BN / 128) * 512 : 0;
     static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + SF_BYTES + 1023) / 1024 * 1024;
-    static constexpr int STAGES = (BN == 256) ? 4 : 6;
+    static constexpr int STG_BYTES = 4 * 4096;   // epilogue staging: 2 x 2 KB per epilogue warp
+    // dynamic shared memory: 227 KB per CTA less ~9 KB of static tables and barriers
+    static constexpr int DYN_BUDGET = 232448 - 9216;
+    static constexpr int FIT = (DYN_BUDGET - STG_BYTES - 1024) / STAGE_BYTES;
+    static constexpr int STAGES = FIT < ((BN == 256) ? 4 : 6) ? FIT : ((BN == 256) ? 4 : 6);
     static constexpr int ACC_BUFS = MX ? 1 : 2;
     static constexpr int TMEM_COLS = MX ? 512 : ((2 * BN <= 256) ? 256 : 512);
     static constexpr int SF_COL0 = BN;                          // MXFP8 scale slots after the accumulator
     static constexpr int SF_COLS = 4 + 4 * (BN / 128);          // per stage: A (4) + B (4 per 128 rows)
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;   // + alignment slack
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_BYTES + 1024;   // + alignment slack
+    static_assert(STAGES >= 2, "shared memory ring too shallow");
     // output columns produced per tile
     static constexpr int OUT_COLS = Traits<OP>::swiglu ? BN / 2 : BN;
     static_assert(!MX || SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM overflow");
@@ -193,7 +199,8 @@ __device__ __forceinline__ Tile decode_tile(int t, const Args &a, const int *s_o
 template <Op OP, int BN>
 __global__ void __launch_bounds__(kThreads, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                    const __grid_constant__ CUtensorMap tmB1, const Args args) {
+                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
+                    const __grid_constant__ CUtensorMap tmC1, const Args args) {
     using TR = Traits<OP>;
     using C = Cfg<OP, BN>;
     constexpr int S = C::STAGES;
@@ -442,6 +449,51 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // ============================================================ epilogue
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;       // accumulator row of this thread
+        // Output staging of this warp: two 2 KB slots of 32 rows x 64 bytes in the 64-byte
+        // swizzle (16-byte chunk j of row i at chunk j ^ ((i / 2) % 4): conflict-free
+        // 16-byte writes), each written back by one TMA store while the other fills.
+        uint8_t *stg = smem + S * C::STAGE_BYTES + q * 4096;
+        const uint32_t stg_s = smem_base + S * C::STAGE_BYTES + q * 4096;
+        int slot = 0;
+        auto slot_open = [&]() {
+            if (lane == 0) sm100::bulk_wait_read<1>();   // the store that last used this slot has read it
+            __syncwarp();
+        };
+        auto slot_put = [&](int j, uint4 v) {
+            *reinterpret_cast<uint4 *>(stg + slot * 2048 + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+        };
+        auto slot_store = [&](const CUtensorMap *tm, int col, int64_t row0) {
+            sm100::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                sm100::tma_store_2d(tm, stg_s + slot * 2048, col, (int)row0);
+                sm100::bulk_commit();
+            }
+            slot ^= 1;
+        };
+        auto stage_bf16x32 = [&](const float (&v)[32], const CUtensorMap *tm, int col, int64_t row0) {
+            slot_open();
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint4 pk;
+                __nv_bfloat162 *p = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) p[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+                slot_put(j, pk);
+            }
+            slot_store(tm, col, row0);
+        };
+        auto stage_f32x32 = [&](const uint32_t (&d)[32], const CUtensorMap *tm, int col, int64_t row0) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                slot_open();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    slot_put(j, make_uint4(d[16 * h + 4 * j], d[16 * h + 4 * j + 1], d[16 * h + 4 * j + 2],
+                                           d[16 * h + 4 * j + 3]));
+                slot_store(tm, col + 16 * h, row0);
+            }
+        };
         int acc = 0;
         uint32_t acc_phase = 0;
         for (int t = blockIdx.x; t < total_tiles; t += gridDim.x) {
@@ -468,6 +520,10 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if (__any_sync(0xFFFFFFFFu, !got)) break;
             sm100::tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);
+            // M-grouped: this warp's 32 rows go out through TMA when all of them belong to the
+            // group (a store box never crosses into the next group's rows); else row by row
+            const int64_t wrow0 = (int64_t)tl.m0 + q * 32;
+            const bool whole = wrow0 + 32 <= tl.m_end && wrow0 + 32 <= args.rows_cap;
 
             if constexpr (TR::swiglu) {
                 const int64_t row = tl.m0 + r;
@@ -479,30 +535,47 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     sm100::tmem_ld32(tacc + BN / 2 + c, u);
                     sm100::tmem_ld_wait();
                     const int n = tl.n0 + c;
-                    if (valid && n < args.N) {
+                    if (n < args.N && (whole || valid)) {
                         float hv[32];
 #pragma unroll
                         for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
                         if constexpr (OP == Op::FC1_MX) {
-                            // h quantised along F: this thread's 32 columns are one MX block
+                            // h quantised along F: this thread's 32 columns are one MX block; two
+                            // blocks (64 bytes of codes) fill a staging row
                             const int X = mx::scale_exp(mx::amax32(hv));
                             uint4 lo, hi;
                             mx::quantize32(hv, X, lo, hi);
-                            uint4 *dq = reinterpret_cast<uint4 *>(args.out_q + row * args.ld0 + n);
-                            dq[0] = lo;
-                            dq[1] = hi;
+                            if (whole) {
+                                const int half = (c >> 5) & 1;
+                                if (half == 0) slot_open();
+                                slot_put(2 * half, lo);
+                                slot_put(2 * half + 1, hi);
+                                if (half == 1) slot_store(&tmC0, n - 32, wrow0);
+                            } else {
+                                uint4 *dq = reinterpret_cast<uint4 *>(args.out_q + row * args.ld0 + n);
+                                dq[0] = lo;
+                                dq[1] = hi;
+                            }
                             args.out_sf[mx::tile_sf_offset(tl.mtile, args.N / 128, r, n / 32)] = (uint8_t)(X + 127);
                         } else {
-                            store_bf16x32(args.out0 + row * args.ld0 + n, hv);
-                            if (args.out1) {
-                                float gv[32], uv[32];
+                            float gv[32], uv[32];
 #pragma unroll
-                                for (int i = 0; i < 32; ++i) {
-                                    gv[i] = __uint_as_float(g[i]);
-                                    uv[i] = __uint_as_float(u[i]);
+                            for (int i = 0; i < 32; ++i) {
+                                gv[i] = __uint_as_float(g[i]);
+                                uv[i] = __uint_as_float(u[i]);
+                            }
+                            if (whole) {
+                                stage_bf16x32(hv, &tmC0, n, wrow0);
+                                if (args.out1) {
+                                    stage_bf16x32(gv, &tmC1, n, wrow0);
+                                    stage_bf16x32(uv, &tmC1, args.N + n, wrow0);
                                 }
-                                store_bf16x32(args.out1 + row * args.ld1 + n, gv);
-                                store_bf16x32(args.out1 + row * args.ld1 + args.N + n, uv);
+                            } else {
+                                store_bf16x32(args.out0 + row * args.ld0 + n, hv);
+                                if (args.out1) {
+                                    store_bf16x32(args.out1 + row * args.ld1 + n, gv);
+                                    store_bf16x32(args.out1 + row * args.ld1 + args.N + n, uv);
+                                }
                             }
                         }
                     }
@@ -516,7 +589,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     sm100::tmem_ld32(tacc + c, d);
                     sm100::tmem_ld_wait();
                     const int n = tl.n0 + c;
-                    if (valid && n < args.N) {
+                    if (n < args.N && (whole || valid)) {
                         float gv[32], uv[32], dg[32], du[32];
                         load_bf16x32(args.aux + row * args.ld_aux + n, gv);
                         load_bf16x32(args.aux + row * args.ld_aux + args.N + n, uv);
@@ -527,13 +600,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                             dg[i] = dh * uv[i] * s * (1.0f + gv[i] * (1.0f - s));
                             du[i] = dh * gv[i] * s;
                         }
-                        store_bf16x32(args.out0 + row * args.ld0 + n, dg);
-                        store_bf16x32(args.out0 + row * args.ld0 + args.N + n, du);
+                        if (whole) {
+                            stage_bf16x32(dg, &tmC0, n, wrow0);
+                            stage_bf16x32(du, &tmC0, args.N + n, wrow0);
+                        } else {
+                            store_bf16x32(args.out0 + row * args.ld0 + n, dg);
+                            store_bf16x32(args.out0 + row * args.ld0 + args.N + n, du);
+                        }
                     }
                 }
             } else if constexpr (TR::k_grouped) {   // fp32 weight gradient of expert e
-                const int row = tl.m0 + r;
-                const size_t eoff = (size_t)tl.e * (size_t)args.expert_stride;
+                // rows of the [E * M, N] view of the expert-stacked gradient
+                const int64_t grow0 = (int64_t)tl.e * args.M + tl.m0 + q * 32;
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t d[32];
@@ -541,10 +619,8 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     sm100::tmem_ld_wait();
                     const int n = tl.n0 + c;
                     if (n < args.N) {
-                        float *dst = (OP == Op::WGRAD_GATEUP && n >= args.n_split)
-                                         ? args.out1_f32 + eoff + (size_t)row * args.ld1 + (n - args.n_split)
-                                         : args.out_f32 + eoff + (size_t)row * args.ld0 + n;
-                        store_f32x32(dst, d);
+                        const bool second = OP == Op::WGRAD_GATEUP && n >= args.n_split;
+                        stage_f32x32(d, second ? &tmC1 : &tmC0, second ? n - args.n_split : n, grow0);
                     }
                 }
             } else {   // FC2, FC2_MX (y_perm) and DGRAD_FC1 (dx_perm): fp32 rows of the group
@@ -557,13 +633,19 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     sm100::tmem_ld32(tacc + c, d);
                     sm100::tmem_ld_wait();
                     const int n = tl.n0 + c;
-                    if (valid && n < args.N) store_f32x32(args.out_f32 + row * args.ld0 + n, d);
+                    if (n < args.N) {
+                        if (whole) stage_f32x32(d, &tmC0, n, wrow0);
+                        else if (valid) store_f32x32(args.out_f32 + row * args.ld0 + n, d);
+                    }
                 }
             }
             sm100::tc_fence_before();
             sm100::mbar_arrive(&tempty_bar[acc]);
             if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
         }
+        // every TMA store of this warp has finished before the CTA can exit
+        if (lane == 0) sm100::bulk_wait_all();
+        __syncwarp();
     }
 
     // ---------------------------------------------------------------- teardown

@@ -23,7 +23,7 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tmap_encoder() {
 
 // Tiled map over a row-major tensor of `dtype` elements of `elem_bytes`
 // bytes: dims[0] is the contiguous dimension; strides_bytes[i] is the byte
-// stride of dims[i+1].  128-byte swizzle, zero fill out of bounds.
+// stride of dims[i+1].  128-byte swizzle unless given, zero fill out of bounds.
 inline bool encode_tmap(CUtensorMap *m, CUtensorMapDataType dtype, int rank, const void *base,
                         const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                         CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
@@ -60,6 +60,20 @@ inline bool tmap_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t
     const uint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
     const uint32_t box[3] = {box0, box1, 1};
     return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
+}
+
+// Store map of the GEMM epilogue: 2-D row-major [outer, inner] of `elem_bytes`-byte
+// elements (bf16, fp32 or bytes), row pitch `ld` elements; boxes of 64 bytes x 32 rows
+// in the 64-byte swizzle (the epilogue's staging slots).
+inline bool tmap_store_2d(CUtensorMap *m, const void *base, int elem_bytes, uint64_t inner, uint64_t outer,
+                          uint64_t ld) {
+    const CUtensorMapDataType dt = elem_bytes == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {ld * (uint64_t)elem_bytes};
+    const uint32_t box[2] = {(uint32_t)(64 / elem_bytes), 32};
+    return encode_tmap(m, dt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // 2-D byte matrix [outer, inner] with row pitch `ld` bytes (E4M3 data).
