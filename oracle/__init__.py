@@ -48,6 +48,10 @@ def lib():
         L.oracle_quantize_mxfp8.argtypes = [_u16p, _i64, _i64, _i64, _i64, _u8p, _u8p]
         L.oracle_route_topk.restype = None
         L.oracle_route_topk.argtypes = [_f32p, _i64, _int, _int, _i32p, _f32p]
+        L.oracle_route_topk_sigmoid.restype = None
+        L.oracle_route_topk_sigmoid.argtypes = [_f32p, _f32p, _i64, _int, _int, _int, _i32p, _f32p]
+        L.oracle_route_topk_bwd.restype = None
+        L.oracle_route_topk_bwd.argtypes = [_f32p, _i32p, _f32p, _i64, _int, _int, _int, _int, _f64p]
         L.oracle_permute.restype = _i64
         L.oracle_permute.argtypes = [_i32p, _i64, _int, _int, _int, _i32p, _i32p, _i64, _i32p, _i32p]
         L.oracle_gather_rows.restype = None
@@ -160,6 +164,36 @@ def route_topk(logits: np.ndarray, k: int):
     w = np.empty((T, k), np.float32)
     lib().oracle_route_topk(_p(lg, _f32p), T, E, k, _p(idx, _i32p), _p(w, _f32p))
     return idx, w
+
+
+def route_topk_sigmoid(logits: np.ndarray, k: int, bias: np.ndarray | None = None, normalize: bool = True):
+    """Top-k routing on sigmoid scores with an optional expert routing bias
+    (selection only); weights = selected scores / (sum + 1e-20) when normalize."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    b = None if bias is None else _c(bias, np.float32)
+    idx = np.empty((T, k), np.int32)
+    w = np.empty((T, k), np.float32)
+    lib().oracle_route_topk_sigmoid(_p(lg, _f32p), None if b is None else _p(b, _f32p), T, E, k, int(normalize),
+                                    _p(idx, _i32p), _p(w, _f32p))
+    return idx, w
+
+
+SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1
+
+
+def route_topk_bwd(logits: np.ndarray, topk_idx: np.ndarray, d_topk_w: np.ndarray, score_fn: int,
+                   normalize: bool = True) -> np.ndarray:
+    """d_logits [T, E] (float64) of the router for the given selection."""
+    lg = _c(logits, np.float32)
+    T, E = lg.shape
+    ti = _c(topk_idx, np.int32)
+    k = ti.shape[1]
+    g = _c(d_topk_w, np.float32)
+    out = np.empty((T, E), np.float64)
+    lib().oracle_route_topk_bwd(_p(lg, _f32p), _p(ti, _i32p), _p(g, _f32p), T, E, k, int(score_fn), int(normalize),
+                                _p(out, _f64p))
+    return out
 
 
 def permute(topk_idx: np.ndarray, E: int, align: int = 1, rows_cap: int | None = None):

@@ -231,6 +231,103 @@ void oracle_route_topk(const float *logits, int64_t T, int E, int k,
 }
 
 /* ------------------------------------------------------------------ */
+/* Router variant: sigmoid scores with an expert routing bias            */
+/* ------------------------------------------------------------------ */
+
+static double sigmoid_d(double x) { return 1.0 / (1.0 + exp(-x)); }
+
+/* Sigmoid score function of the fused top-k router ("[JAX] Expert
+ * Parallelism: JAX primitives + VJPs", commit log: sigmoid scores, the
+ * expert routing bias of the sigmoid-bias configurations, and the kernel's
+ * normalisation weights / (sum + 1e-20)).  Readings: the score of expert e
+ * is s_e = sigmoid(l_e); the bias takes part in the selection only (key
+ * s_e + b_e, larger first, equal keys to the lower id); the weights are the
+ * unbiased scores of the selected experts, divided by (their sum + 1e-20)
+ * when normalize != 0.  bias may be NULL (all zero).  A NaN logit ranks
+ * last.  Keys and weights in double. */
+void oracle_route_topk_sigmoid(const float *logits, const float *bias, int64_t T, int E, int k,
+                               int normalize, int32_t *topk_idx, float *topk_w)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        double *key = (double *)malloc((size_t)E * sizeof(double));
+        unsigned char *taken = (unsigned char *)calloc((size_t)E, 1);
+        for (int e = 0; e < E; ++e)
+            key[e] = isnan(l[e]) ? NAN : sigmoid_d((double)l[e]) + (bias ? (double)bias[e] : 0.0);
+        double s[64], sum = 0.0;
+        for (int j = 0; j < k; ++j) {
+            int best = -1;
+            for (int e = 0; e < E; ++e) {
+                if (taken[e]) continue;
+                if (best < 0) { best = e; continue; }
+                int nb = isnan(key[best]), ne = isnan(key[e]);
+                if (nb && !ne) best = e;
+                else if (!nb && !ne && key[e] > key[best]) best = e;
+            }
+            taken[best] = 1;
+            topk_idx[t * k + j] = best;
+            s[j] = isnan(l[best]) ? 0.0 : sigmoid_d((double)l[best]);
+            sum += s[j];
+        }
+        for (int j = 0; j < k; ++j)
+            topk_w[t * k + j] = (float)(normalize ? s[j] / (sum + 1e-20) : s[j]);
+        free(taken);
+        free(key);
+    }
+}
+
+/* Router backward: d_logits [T, E] (double) from d_topk_w [T, k] for the
+ * selection topk_idx (ids outside [0, E) are skipped), following the router's
+ * VJP ("[JAX] Expert Parallelism: JAX primitives + VJPs", commit log:
+ * fused_topk_with_score_function_bwd produces the fp32 logits cotangent).
+ * The weights are recomputed in double from the logits; unselected experts
+ * get 0 (the selection is piecewise constant), and so does the bias.
+ *   score_fn 0 (softmax over the k selected):  dl_j = w_j (g_j - sum_i w_i g_i)
+ *   score_fn 1 (sigmoid s_j):  normalize: ds_j = (g_j - sum_i w_i g_i) / (S + 1e-20),
+ *                              else ds_j = g_j;  dl_j = ds_j s_j (1 - s_j)      */
+void oracle_route_topk_bwd(const float *logits, const int32_t *topk_idx, const float *d_topk_w,
+                           int64_t T, int E, int k, int score_fn, int normalize, double *d_logits)
+{
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const float *l = logits + t * E;
+        double *dl = d_logits + t * E;
+        for (int e = 0; e < E; ++e) dl[e] = 0.0;
+        double w[64], s[64], g[64];
+        int id[64], n = 0;
+        for (int j = 0; j < k; ++j) {
+            int e = topk_idx[t * k + j];
+            if (e < 0 || e >= E) continue;
+            id[n] = e;
+            g[n] = (double)d_topk_w[t * k + j];
+            ++n;
+        }
+        if (n == 0) continue;
+        if (score_fn == 0) {
+            double lmax = -INFINITY, sum = 0.0;
+            for (int j = 0; j < n; ++j)
+                if ((double)l[id[j]] > lmax) lmax = (double)l[id[j]];
+            if (isinf(lmax) && lmax < 0) continue;   /* all weights 0, no gradient */
+            for (int j = 0; j < n; ++j) { w[j] = exp((double)l[id[j]] - lmax); sum += w[j]; }
+            double gw = 0.0;
+            for (int j = 0; j < n; ++j) { w[j] /= sum; gw += w[j] * g[j]; }
+            for (int j = 0; j < n; ++j) dl[id[j]] += w[j] * (g[j] - gw);
+        } else {
+            double S = 0.0;
+            for (int j = 0; j < n; ++j) { s[j] = sigmoid_d((double)l[id[j]]); S += s[j]; }
+            double gw = 0.0;
+            if (normalize)
+                for (int j = 0; j < n; ++j) gw += g[j] * s[j] / (S + 1e-20);
+            for (int j = 0; j < n; ++j) {
+                double ds = normalize ? (g[j] - gw) / (S + 1e-20) : g[j];
+                dl[id[j]] += ds * s[j] * (1.0 - s[j]);
+            }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------ */
 /* A2: permutation into expert-contiguous order                         */
 /* ------------------------------------------------------------------ */
 
