@@ -3,8 +3,9 @@
 A step is one pass of the whole hot path over one batch of seeded synthetic
 inputs resident in HBM:
   bf16 forward   route -> permute -> grouped FC1+SwiGLU -> grouped FC2 -> combine
-  mixtral        the forward, then the backward (combine bwd, FC2 dgrad + dSwiGLU,
-                 FC1 dgrad, grouped wgrad, unpermute-sum)
+  mixtral        the forward, then the backward (combine bwd, router bwd to the
+                 logits, FC2 dgrad + dSwiGLU, FC1 dgrad, grouped wgrad, unpermute-sum)
+  --router sigmoid  routes on sigmoid scores + a seeded expert routing bias
   dsv3_mxfp8     route -> quantising permute -> block-scaled FC1 (h to MXFP8) ->
                  block-scaled FC2 -> combine; weights quantised once, untimed
 Default workload: fine_grained (T=4096, H=2048, F=1408, E=64, top-6).
@@ -181,19 +182,21 @@ def build_workload(shape, dev, stream):
 
     T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
     R = T * k
-    inp = make_inputs(shape, device=dev, with_dy=shape.backward)
+    sigmoid = shape.router == "sigmoid"
+    inp = make_inputs(shape, device=dev, with_dy=shape.backward, with_expert_bias=sigmoid)
     w = {"inp": inp, "shape": shape}
     if shape.mxfp8:
         mw = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"], stream)
-        m = MoeForwardMX(T, H, F, E, k, device=dev)
+        m = MoeForwardMX(T, H, F, E, k, device=dev, router=shape.router, expert_bias=inp.get("expert_bias"))
         w.update(layer=m, mw=mw)
         m(inp["x"], inp["logits"], mw, stream)
     else:
-        m = MoeForward(T, H, F, E, k, device=dev, keep_fc1_c=shape.backward)
+        m = MoeForward(T, H, F, E, k, device=dev, keep_fc1_c=shape.backward,
+                       router="sigmoid" if sigmoid else "softmax", expert_bias=inp.get("expert_bias"))
         w.update(layer=m)
         m(inp["x"], inp["logits"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
         if shape.backward:
-            w["bwd"] = MoeBackward(m)
+            w["bwd"] = MoeBackward(m, want_d_logits=True)
     torch.cuda.synchronize(dev)
     active = int((m.perm.group_sizes > 0).sum().item())     # experts whose weights are read
     w["active_experts"] = active
@@ -226,6 +229,7 @@ def build_workload(shape, dev, stream):
         g += [
             Group("combine_bwd", lambda: b.combine_bwd(inp["dY"], stream),
                   nbytes=T * H * 2 + R * H * 4 + R * H * 2 + R * 8, launches=2),
+            Group("route_bwd", lambda: b.router_bwd(inp["logits"], stream), nbytes=R * 4 + R * 8 + T * E * 4),
             Group("dgrad_fc2_dswiglu", lambda: b.dgrad_fc2(inp["W_down"], stream), flop=2.0 * R * H * F,
                   nbytes=R * H * 2 + wbytes + R * 2 * F * 2 * 2),
             Group("dgrad_fc1", lambda: b.dgrad_fc1(inp["W_gate"], inp["W_up"], stream), flop=4.0 * R * H * F,
@@ -251,7 +255,7 @@ def e2e_step(w, host, stream):
     host["out"].copy_(m.out, non_blocking=True)
     if shape.backward:
         host["dy_d"].copy_(host["dy"], non_blocking=True)
-        w["bwd"](host["dy_d"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
+        w["bwd"](host["dy_d"], inp["W_gate"], inp["W_up"], inp["W_down"], stream, logits=host["lg_d"])
         host["dx"].copy_(w["bwd"].dx, non_blocking=True)
 
 
@@ -283,7 +287,12 @@ def oracle_sample(shape, inp_dev, n_tokens: int, it: int = 0):
     import oracle
     T, k = shape.T, shape.k
     lg = inp_dev["logits"].cpu().numpy()
-    idx_all, w_all = oracle.route_topk(lg, k)
+    bias = inp_dev["expert_bias"].cpu().numpy() if shape.router == "sigmoid" else None
+
+    def route():
+        return oracle.route_topk_sigmoid(lg, k, bias) if bias is not None else oracle.route_topk(lg, k)
+
+    idx_all, w_all = route()
     toks = (np.arange(n_tokens) * max(1, T // n_tokens) + it) % T
     experts = np.unique(idx_all[toks])
     x_rows = oracle.bf16_bits(inp_dev["x"].index_select(0, _long(inp_dev, toks)))
@@ -298,15 +307,17 @@ def oracle_sample(shape, inp_dev, n_tokens: int, it: int = 0):
             q["dq"][e], q["ds"][e] = oracle.quantize_cols_mxfp8(wts["W_down"][e])
     dy_rows = oracle.bf16_bits(inp_dev["dY"].index_select(0, _long(inp_dev, toks))) if shape.backward else None
     t0 = time.perf_counter()
-    idx, w = oracle.route_topk(lg, k)
+    idx, w = route()
     oracle.permute(idx, shape.E)
     if shape.mxfp8:
         oracle.moe_fwd_mxfp8(x_rows, q["gq"], q["gs"], q["uq"], q["us"], q["dq"], q["ds"], idx_s, w_s)
     else:
         oracle.moe_fwd(x_rows, wts["W_gate"], wts["W_up"], wts["W_down"], idx_s, w_s)
         if shape.backward:
-            oracle.moe_bwd(x_rows, _dense(wts["W_gate"], shape.E), _dense(wts["W_up"], shape.E),
-                           _dense(wts["W_down"], shape.E), idx_s, w_s, dy_rows)
+            g = oracle.moe_bwd(x_rows, _dense(wts["W_gate"], shape.E), _dense(wts["W_up"], shape.E),
+                               _dense(wts["W_down"], shape.E), idx_s, w_s, dy_rows)
+            oracle.route_topk_bwd(lg[toks], idx_s, g["d_topk_w"].astype("float32"),
+                                  oracle.SCORE_SIGMOID if bias is not None else oracle.SCORE_SOFTMAX)
     return time.perf_counter() - t0, n_tokens
 
 
@@ -351,6 +362,8 @@ def workload_shape(args):
     if args.shape:
         kw = {kv.split("=")[0].strip(): int(kv.split("=")[1]) for kv in args.shape.split(",") if kv.strip()}
         shape = dataclasses.replace(shape, name=shape.name + "_" + "_".join(f"{a}{b}" for a, b in kw.items()), **kw)
+    if args.router != "softmax":
+        shape = dataclasses.replace(shape, name=shape.name + "_" + args.router, router=args.router)
     return shape
 
 
@@ -364,7 +377,7 @@ def run_reference(args):
         return 0
     shape = workload_shape(args)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = make_inputs(shape, device=dev, with_dy=shape.backward)
+    inp = make_inputs(shape, device=dev, with_dy=shape.backward, with_expert_bias=shape.router == "sigmoid")
     sample = max(1, min(shape.T, args.ref_tokens if args.ref_tokens else (2 if shape.backward or shape.mxfp8 else 16)))
     times = []
     for it in range(args.warmup + args.steps):
@@ -378,7 +391,7 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
-                   "k": shape.k, "tokens_per_step": sample},
+                   "k": shape.k, "router": shape.router, "tokens_per_step": sample},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"{sample} of {shape.T} tokens per step (routing and permutation over all tokens)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -488,7 +501,7 @@ def run_gpu(args):
         "vs_baseline": None, "dtype": "mxfp8" if shape.mxfp8 else "bf16",
         "data": "synthetic (seeded; BASELINE shapes and distributions)",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k,
-                   "pass": "forward+backward" if shape.backward else "forward",
+                   "router": shape.router, "pass": "forward+backward" if shape.backward else "forward",
                    "active_experts": w["active_experts"],
                    "l2": "flushed between steps (256 MiB write outside the timed events)"},
         "kernels": rates,
@@ -518,6 +531,8 @@ def main(argv=None):
                     choices=["tiny", "fine_grained", "mixtral", "skewed", "dsv3_mxfp8"])
     ap.add_argument("--shape", default="",
                     help="override sizes of the workload, e.g. 'T=2048,F=4096' (same kind of pass)")
+    ap.add_argument("--router", default="softmax", choices=["softmax", "sigmoid"],
+                    help="score function of the routing step (sigmoid: + a seeded expert routing bias)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -4,6 +4,8 @@
  * One GPU, one stream per call, no host synchronisation on the hot path:
  *
  *   moe_route_topk        router logits -> top-k expert ids and weights
+ *                         (moe_route_topk_sigmoid: sigmoid scores + routing
+ *                         bias; moe_route_topk_bwd: the logits gradient)
  *   moe_permute           tokens -> expert-contiguous rows, group sizes and
  *                         offsets written on the device
  *   moe_grouped_ffn_fwd   grouped gate/up GEMM + SwiGLU, grouped down GEMM
@@ -106,6 +108,53 @@ MOE_API moe_status_t moe_read_device_error(const void *ws, moe_stream_t stream, 
  * MOE_ERR_UNSUPPORTED (E or k out of range), MOE_ERR_CUDA. */
 MOE_API moe_status_t moe_route_topk(const float *logits, int64_t T, int E, int k,
                             int32_t *topk_idx, float *topk_w, moe_stream_t stream);
+
+/* Sigmoid variant of the top-k router ("[JAX] Expert Parallelism: JAX
+ * primitives + VJPs", commit log: sigmoid scores, the expert routing bias of
+ * the sigmoid-bias configurations, and the kernel's weights / (sum + 1e-20)
+ * normalisation).
+ *
+ *   logits      device fp32 [T, E]; score s_e = sigmoid(l_e) in fp32
+ *   expert_bias device fp32 [E] or NULL (all zero): added to the scores for
+ *               the selection only
+ *   normalize   0: w_j = s_j;  else w_j = s_j / (sum of the k selected s + 1e-20)
+ *   topk_idx    device int32 [T, k] out: the k experts ranked first by
+ *               (s_e + b_e descending, expert id ascending); a NaN logit ranks
+ *               last (its weight is 0)
+ *   topk_w      device fp32 [T, k] out: the weights above (never NaN for
+ *               finite or -inf logits: all-zero scores give zero weights)
+ *
+ * Limits and errors as moe_route_topk. */
+MOE_API moe_status_t moe_route_topk_sigmoid(const float *logits, const float *expert_bias, int64_t T, int E,
+                                            int k, int normalize, int32_t *topk_idx, float *topk_w,
+                                            moe_stream_t stream);
+
+#define MOE_SCORE_SOFTMAX 0   /* moe_route_topk */
+#define MOE_SCORE_SIGMOID 1   /* moe_route_topk_sigmoid */
+
+/* Router backward: the fp32 logits cotangent from the weights' cotangent
+ * ("[JAX] Expert Parallelism: JAX primitives + VJPs", commit log: the
+ * router's backward gives an fp32 cotangent of the fp32-promoted logits).
+ * The selection is taken as given (piecewise constant: unselected experts and
+ * the routing bias get no gradient); the weights are recomputed in fp32 from
+ * the logits over the valid selected ids.
+ *
+ *   logits    device fp32 [T, E] (the forward's input)
+ *   topk_idx  device int32 [T, k] (the forward's selection); ids outside
+ *             [0, E) are skipped (no logit receives their gradient)
+ *   d_topk_w  device fp32 [T, k] (e.g. from moe_combine_bwd)
+ *   score_fn  MOE_SCORE_SOFTMAX: dl_j = w_j (g_j - sum_i w_i g_i)
+ *             MOE_SCORE_SIGMOID: ds_j = normalize ? (g_j - sum_i w_i g_i) /
+ *             (S + 1e-20) : g_j, dl_j = ds_j s_j (1 - s_j), S = sum of the
+ *             selected scores
+ *   d_logits  device fp32 [T, E] out, dense: 0 where not selected; an expert
+ *             selected twice receives the sum
+ *
+ * Limits as moe_route_topk.  Errors: MOE_ERR_INVALID_ARG (null pointer with
+ * T > 0, negative T, unknown score_fn), MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
+MOE_API moe_status_t moe_route_topk_bwd(const float *logits, const int32_t *topk_idx, const float *d_topk_w,
+                                        int64_t T, int E, int k, int score_fn, int normalize, float *d_logits,
+                                        moe_stream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* A2  Permutation into expert-contiguous order                         */

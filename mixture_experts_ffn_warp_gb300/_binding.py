@@ -37,6 +37,8 @@ SIGNATURES = {
     "moe_workspace_init": (_st, [_vp, _sz, _vp]),
     "moe_read_device_error": (_st, [_vp, _vp, C.POINTER(C.c_uint32)]),
     "moe_route_topk": (_st, [_vp, _i64, _int, _int, _vp, _vp, _vp]),
+    "moe_route_topk_sigmoid": (_st, [_vp, _vp, _i64, _int, _int, _int, _vp, _vp, _vp]),
+    "moe_route_topk_bwd": (_st, [_vp, _vp, _vp, _i64, _int, _int, _int, _int, _vp, _vp]),
     "moe_permute": (_st, [_vp, _vp, _i64, _int, _int, _int, _int, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_permute_static_scratch": (_st, [_vp, _vp, _i64, _int, _int, _int, _int, _vp, _i64, _vp, _vp, _vp, _vp,
                                          _vp, _vp]),
@@ -159,6 +161,50 @@ def moe_route_topk(logits: torch.Tensor, k: int, topk_idx=None, topk_w=None, str
     _check("moe_route_topk", load_library().moe_route_topk(
         _ptr(logits), T, E, k, _ptr(topk_idx), _ptr(topk_w), _stream(stream)))
     return topk_idx, topk_w
+
+
+SCORE_SOFTMAX, SCORE_SIGMOID = 0, 1   # moe.h MOE_SCORE_*
+
+
+def moe_route_topk_sigmoid(logits: torch.Tensor, k: int, expert_bias=None, normalize: bool = True, topk_idx=None,
+                           topk_w=None, stream=None):
+    """Top-k routing on sigmoid scores; the expert routing bias takes part in the
+    selection only; weights / (sum + 1e-20) when normalize (moe.h)."""
+    _need(logits, "logits", torch.float32)
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, E]")
+    T, E = logits.shape
+    if expert_bias is not None:
+        _need(expert_bias, "expert_bias", torch.float32, (E,), logits.device)
+    if topk_idx is None:
+        topk_idx = torch.empty(T, k, dtype=torch.int32, device=logits.device)
+    if topk_w is None:
+        topk_w = torch.empty(T, k, dtype=torch.float32, device=logits.device)
+    _need(topk_idx, "topk_idx", torch.int32, (T, k), logits.device)
+    _need(topk_w, "topk_w", torch.float32, (T, k), logits.device)
+    _check("moe_route_topk_sigmoid", load_library().moe_route_topk_sigmoid(
+        _ptr(logits), _ptr(expert_bias), T, E, k, int(bool(normalize)), _ptr(topk_idx), _ptr(topk_w),
+        _stream(stream)))
+    return topk_idx, topk_w
+
+
+def moe_route_topk_bwd(logits: torch.Tensor, topk_idx: torch.Tensor, d_topk_w: torch.Tensor, score_fn: int,
+                       normalize: bool = True, d_logits=None, stream=None):
+    """fp32 logits gradient of the router for the given selection (moe.h)."""
+    _need(logits, "logits", torch.float32)
+    if logits.dim() != 2:
+        raise ValueError("logits must be [T, E]")
+    T, E = logits.shape
+    k = topk_idx.shape[1] if topk_idx.dim() == 2 else -1
+    _need(topk_idx, "topk_idx", torch.int32, (T, k), logits.device)
+    _need(d_topk_w, "d_topk_w", torch.float32, (T, k), logits.device)
+    if d_logits is None:
+        d_logits = torch.empty(T, E, dtype=torch.float32, device=logits.device)
+    _need(d_logits, "d_logits", torch.float32, (T, E), logits.device)
+    _check("moe_route_topk_bwd", load_library().moe_route_topk_bwd(
+        _ptr(logits), _ptr(topk_idx), _ptr(d_topk_w), T, E, k, int(score_fn), int(bool(normalize)),
+        _ptr(d_logits), _stream(stream)))
+    return d_logits
 
 
 # ------------------------------------------------------------------ A2

@@ -10,7 +10,8 @@ from __future__ import annotations
 
 import torch
 
-from ._binding import (Permutation, PermutationMX, Workspace, moe_combine_bwd, moe_grouped_dgrad_fc1,
+from ._binding import (SCORE_SIGMOID, SCORE_SOFTMAX, Permutation, PermutationMX, Workspace, moe_combine_bwd,
+                       moe_grouped_dgrad_fc1, moe_route_topk_bwd, moe_route_topk_sigmoid,
                        moe_grouped_fc1_swiglu_mxfp8, moe_grouped_fc2_mxfp8, moe_permute_mxfp8,
                        moe_quantize_weights_mxfp8, mx_tile_scale_bytes,
                        moe_grouped_dgrad_fc2_dswiglu, moe_grouped_fc1_swiglu, moe_grouped_fc2,
@@ -19,11 +20,18 @@ from ._binding import (Permutation, PermutationMX, Workspace, moe_combine_bwd, m
 
 
 class MoeForward:
-    """Pre-allocated forward pass for fixed (T, H, F, E, k)."""
+    """Pre-allocated forward pass for fixed (T, H, F, E, k).
+
+    router: "softmax" (softmax over the k selected logits) or "sigmoid" (sigmoid
+    scores; `expert_bias` [E] fp32 takes part in the selection only; weights
+    normalised by their sum + 1e-20 when `normalize`)."""
 
     def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", align: int = 1,
-                 keep_fc1_c: bool = False):
+                 keep_fc1_c: bool = False, router: str = "softmax", expert_bias=None, normalize: bool = True):
+        if router not in ("softmax", "sigmoid"):
+            raise ValueError("router must be 'softmax' or 'sigmoid'")
         self.T, self.H, self.F, self.E, self.k, self.align = T, H, F, E, k, align
+        self.router, self.expert_bias, self.normalize = router, expert_bias, normalize
         dev = torch.device(device)
         self.device = dev
         self.ws = Workspace(T, E, k, dev)
@@ -45,7 +53,11 @@ class MoeForward:
 
     # the steps, each one launch group on the current stream
     def route(self, logits, stream=None):
-        moe_route_topk(logits, self.k, self.topk_idx, self.topk_w, stream=stream)
+        if self.router == "sigmoid":
+            moe_route_topk_sigmoid(logits, self.k, self.expert_bias, self.normalize, self.topk_idx, self.topk_w,
+                                   stream=stream)
+        else:
+            moe_route_topk(logits, self.k, self.topk_idx, self.topk_w, stream=stream)
 
     def permute(self, x, stream=None):
         moe_permute(x, self.topk_idx, self.E, self.ws, self.align, out=self.perm, stream=stream)
@@ -85,9 +97,13 @@ class MoeBackward:
 
     Produces dx (bf16), fp32 dW_gate / dW_up / dW_down and fp32 d_topk_w,
     following the backward contract of "Add MoE + expert-parallel Python API
-    surface, PyTorch reference, and tests" (FP32 weight and route gradients)."""
+    surface, PyTorch reference, and tests" (FP32 weight and route gradients);
+    with want_d_logits also the fp32 router-logits gradient ("[JAX] Expert
+    Parallelism: JAX primitives + VJPs", commit log: the router backward)."""
 
-    def __init__(self, fwd: MoeForward, want_d_topk_w: bool = True):
+    def __init__(self, fwd: MoeForward, want_d_topk_w: bool = True, want_d_logits: bool = False):
+        if want_d_logits and not want_d_topk_w:
+            raise ValueError("the logits gradient needs d_topk_w")
         if fwd.fc1_c is None:
             raise ValueError("the forward must keep the fc1_c stash (keep_fc1_c=True)")
         self.fwd = fwd
@@ -100,6 +116,7 @@ class MoeBackward:
         self.dW_up = torch.empty(E, H, F, dtype=torch.float32, device=dev)
         self.dW_down = torch.empty(E, F, H, dtype=torch.float32, device=dev)
         self.d_topk_w = torch.empty(T, k, dtype=torch.float32, device=dev) if want_d_topk_w else None
+        self.d_logits = torch.empty(T, E, dtype=torch.float32, device=dev) if want_d_logits else None
 
     def combine_bwd(self, dY, stream=None):
         f = self.fwd
@@ -122,8 +139,18 @@ class MoeBackward:
     def unpermute_sum(self, stream=None):
         moe_unpermute_sum(self.dx_perm, self.fwd.perm.dst_of_route, self.dx, stream=stream)
 
-    def __call__(self, dY, W_gate, W_up, W_down, stream=None):
+    def router_bwd(self, logits, stream=None):
+        f = self.fwd
+        moe_route_topk_bwd(logits, f.topk_idx, self.d_topk_w, SCORE_SIGMOID if f.router == "sigmoid" else SCORE_SOFTMAX,
+                           f.normalize, self.d_logits, stream=stream)
+
+    def __call__(self, dY, W_gate, W_up, W_down, stream=None, logits=None):
+        """logits: the forward's router logits, needed for d_logits."""
+        if self.d_logits is not None and logits is None:
+            raise ValueError("the logits gradient needs the forward's logits")
         self.combine_bwd(dY, stream)
+        if self.d_logits is not None:
+            self.router_bwd(logits, stream)
         self.dgrad_fc2(W_down, stream)
         self.dgrad_fc1(W_gate, W_up, stream)
         self.wgrad(stream)
@@ -142,10 +169,15 @@ class MxWeights:
 
 class MoeForwardMX:
     """Pre-allocated MXFP8 forward: route -> quantising permute -> block-scaled
-    FC1 + SwiGLU (h to MXFP8) -> block-scaled FC2 -> combine (bf16 out)."""
+    FC1 + SwiGLU (h to MXFP8) -> block-scaled FC2 -> combine (bf16 out).
+    router / expert_bias / normalize as for MoeForward."""
 
-    def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda"):
+    def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", router: str = "softmax",
+                 expert_bias=None, normalize: bool = True):
+        if router not in ("softmax", "sigmoid"):
+            raise ValueError("router must be 'softmax' or 'sigmoid'")
         self.T, self.H, self.F, self.E, self.k = T, H, F, E, k
+        self.router, self.expert_bias, self.normalize = router, expert_bias, normalize
         dev = torch.device(device)
         self.device = dev
         self.ws = Workspace(T, E, k, dev)
@@ -165,8 +197,7 @@ class MoeForwardMX:
         self.y_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
         self.out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
 
-    def route(self, logits, stream=None):
-        moe_route_topk(logits, self.k, self.topk_idx, self.topk_w, stream=stream)
+    route = MoeForward.route
 
     def permute(self, x, stream=None):
         moe_permute_mxfp8(x, self.topk_idx, self.E, self.ws, out=self.perm, stream=stream)

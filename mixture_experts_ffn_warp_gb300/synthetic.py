@@ -39,6 +39,7 @@ class MoeShape:
     skew: bool = False
     backward: bool = False
     mxfp8: bool = False
+    router: str = "softmax"   # or "sigmoid" (sigmoid scores + expert routing bias)
 
     @property
     def R(self) -> int:
@@ -76,11 +77,13 @@ def skew_bias(E: int, seed: int = 0) -> torch.Tensor:
 
 
 def make_inputs(shape: MoeShape, device="cpu", seed: int = 0, with_dy: bool | None = None,
-                weights: bool = True) -> dict[str, torch.Tensor]:
+                weights: bool = True, with_expert_bias: bool = False) -> dict[str, torch.Tensor]:
     """Draw the inputs of one workload on `device`.
 
     Returns a dict with logits fp32 [T,E], x bf16 [T,H], W_gate/W_up bf16
-    [E,H,F], W_down bf16 [E,F,H] and (if requested) dY bf16 [T,H].  Weights are
+    [E,H,F], W_down bf16 [E,F,H] and (if requested) dY bf16 [T,H] and an
+    expert routing bias fp32 [E] ~ N(0, 0.05^2) for the sigmoid router, drawn
+    last so that the other tensors do not depend on it.  Weights are
     drawn one expert at a time so that large workloads never hold an fp32
     copy of the whole weight set.
     """
@@ -103,4 +106,6 @@ def make_inputs(shape: MoeShape, device="cpu", seed: int = 0, with_dy: bool | No
             out[name] = w
     if with_dy:
         out["dY"] = torch.randn(T, H, generator=g, device=device, dtype=torch.bfloat16)
+    if with_expert_bias:
+        out["expert_bias"] = torch.randn(E, generator=g, device=device, dtype=torch.float32) * 0.05
     return out

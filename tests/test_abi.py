@@ -63,6 +63,14 @@ def test_host_validation_before_launch(lib):
     assert lib.moe_route_topk(nul, -1, 8, 2, nul, nul, nul) == 1
     assert lib.moe_route_topk(nul, 0, 8, 2, nul, nul, nul) == 0          # empty: no-op
     assert lib.moe_route_topk(nul, 5, 8, 2, nul, nul, nul) == 1          # null pointers
+    # sigmoid router and router backward
+    assert lib.moe_route_topk_sigmoid(nul, nul, 10, 8, 9, 1, nul, nul, nul) == 2
+    assert lib.moe_route_topk_sigmoid(nul, nul, 0, 8, 2, 1, nul, nul, nul) == 0
+    assert lib.moe_route_topk_sigmoid(nul, nul, 5, 8, 2, 1, nul, nul, nul) == 1
+    fk = C.c_void_p(16)
+    assert lib.moe_route_topk_bwd(fk, fk, fk, 5, 8, 2, 7, 1, fk, nul) == 1       # unknown score function
+    assert lib.moe_route_topk_bwd(fk, fk, fk, 5, 2000, 2, 0, 1, fk, nul) == 2    # E > 1024
+    assert lib.moe_route_topk_bwd(fk, nul, fk, 5, 8, 2, 1, 1, fk, nul) == 1      # null pointer
     # permute: H % 8, capacity, workspace
     assert lib.moe_permute(nul, nul, 4, 12, 4, 2, 1, nul, 8, nul, nul, nul, nul, nul, 0, nul) == 2
     assert lib.moe_permute(nul, nul, 4, 16, 4, 2, 1, nul, 7, nul, nul, nul, nul, nul, 0, nul) == 1
