@@ -345,7 +345,8 @@ MOE_API moe_status_t moe_quantize_weights_mxfp8(const moe_bf16_t *W, int E, int 
  * read once): x_q uint8 [rows_cap, H] out (row dst_of_route[r] holds the
  * E4M3 codes of x[r / k]), x_sf tile-layout scales out
  * (moe_mx_tile_scale_bytes(rows_cap, E, H) bytes).  Other arguments and
- * outputs as moe_permute with align = 1.  Limits: H % 128 == 0. */
+ * outputs as moe_permute with align = 1.  Limits: H % 128 == 0; x 16-byte,
+ * x_q 8-byte and x_sf 4-byte aligned (else MOE_ERR_UNSUPPORTED). */
 MOE_API moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *topk_idx, int64_t T, int H, int E,
                                        int k, uint8_t *x_q, uint8_t *x_sf, int64_t rows_cap,
                                        int32_t *dst_of_route, int32_t *src_of_row, int32_t *group_sizes,

@@ -52,6 +52,21 @@ __device__ __forceinline__ void quantize32(const float (&v)[32], int X, uint4 &l
     hi = make_uint4(w[4], w[5], w[6], w[7]);
 }
 
+// Quantise 8 values to E4M3 with block exponent X (a quarter of a block); packs 8 bytes.
+__device__ __forceinline__ uint2 quantize8(const float (&v)[8], int X) {
+    const float s = inv_pow2(X);
+    uint32_t w[2];
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const __nv_fp8x2_storage_t p0 =
+            __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i] * s, v[4 * i + 1] * s), __NV_SATFINITE, __NV_E4M3);
+        const __nv_fp8x2_storage_t p1 =
+            __nv_cvt_float2_to_fp8x2(make_float2(v[4 * i + 2] * s, v[4 * i + 3] * s), __NV_SATFINITE, __NV_E4M3);
+        w[i] = (uint32_t)p0 | ((uint32_t)p1 << 16);
+    }
+    return make_uint2(w[0], w[1]);
+}
+
 __device__ __forceinline__ float amax32(const float (&v)[32]) {
     float a = 0.0f;
 #pragma unroll

@@ -185,7 +185,8 @@ moe_status_t count_and_scan(const int32_t *topk_idx, int64_t R, int E, int align
     return launch_status();
 }
 
-// One warp per token: maps, then the row copied once into its k rows.
+// One warp per token: maps, then the row copied once into its k rows (KMAX >= k).
+template <int KMAX>
 __global__ void __launch_bounds__(kScatterWarps * 32)
 permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
                        int64_t T, int k, int E, int row_vecs,
@@ -211,9 +212,9 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
         }
         dst_of_route[r] = my_dst;
     }
-    int dst[32];
+    int dst[KMAX];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) dst[j] = j < k ? __shfl_sync(0xFFFFFFFFu, my_dst, j) : -1;
+    for (int j = 0; j < KMAX; ++j) dst[j] = j < k ? __shfl_sync(0xFFFFFFFFu, my_dst, j) : -1;
     const uint4 *src = x + t * row_vecs;
     constexpr int U = 4;   // 16-byte vectors in flight per lane
     for (int v0 = lane; v0 < row_vecs; v0 += 32 * U) {
@@ -222,7 +223,7 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
         for (int u = 0; u < U; ++u)
             if (v0 + 32 * u < row_vecs) val[u] = __ldg(src + v0 + 32 * u);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < KMAX; ++j) {
             if (j < k && dst[j] >= 0) {
                 uint4 *d = x_perm + (int64_t)dst[j] * row_vecs;
 #pragma unroll
@@ -231,6 +232,22 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
             }
         }
     }
+}
+
+void launch_scatter(int64_t blocks, cudaStream_t s, const uint4 *x, const int32_t *topk_idx, int64_t T, int k,
+                    int E, int row_vecs, const int32_t *chunk_first, int32_t *dst_of_route, int32_t *src_of_row,
+                    uint4 *x_perm, int64_t rows_cap, uint32_t *err) {
+#define MOE_SCATTER(KM)                                                                                        \
+    permute_scatter_kernel<KM><<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(x, topk_idx, T, k, E, row_vecs,  \
+                                                                              chunk_first, dst_of_route,         \
+                                                                              src_of_row, x_perm, rows_cap, err)
+    if (k <= 1) MOE_SCATTER(1);
+    else if (k <= 2) MOE_SCATTER(2);
+    else if (k <= 4) MOE_SCATTER(4);
+    else if (k <= 8) MOE_SCATTER(8);
+    else if (k <= 16) MOE_SCATTER(16);
+    else MOE_SCATTER(32);
+#undef MOE_SCATTER
 }
 
 // Padding rows of aligned groups: src_of_row = -1 and zero data.
@@ -279,9 +296,8 @@ extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx
     const int row_vecs = H / 8;
     if (T > 0) {
         const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
-        permute_scatter_kernel<<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(
-            reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts, dst_of_route,
-            src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, err);
+        launch_scatter(blocks, s, reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts,
+                       dst_of_route, src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, err);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     if (align > 1) {
@@ -368,9 +384,8 @@ extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const in
     const int row_vecs = H / 8;
     if (T > 0) {
         const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
-        permute_scatter_kernel<<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(
-            reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts, dst_of_route,
-            src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, err);
+        launch_scatter(blocks, s, reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts,
+                       dst_of_route, src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, err);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     if (align > 1) {
@@ -396,6 +411,8 @@ extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const in
 namespace moe {
 namespace {
 
+// KMAX >= k: the per-token route arrays stay in registers of that size.
+template <int KMAX>
 __global__ void __launch_bounds__(kScatterWarps * 32)
 permute_scatter_mx_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx, int64_t T, int k,
                           int E, int H, const int32_t *__restrict__ chunk_first,
@@ -424,39 +441,60 @@ permute_scatter_mx_kernel(const uint4 *__restrict__ x, const int32_t *__restrict
         }
         dst_of_route[r] = my_dst;
     }
-    int dst[32], tile[32], mm[32];
+    int dst[KMAX], tile[KMAX], mm[KMAX];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
+    for (int j = 0; j < KMAX; ++j) {
         dst[j] = j < k ? __shfl_sync(0xFFFFFFFFu, my_dst, j) : -1;
         tile[j] = __shfl_sync(0xFFFFFFFFu, my_tile, j);
         mm[j] = __shfl_sync(0xFFFFFFFFu, my_m, j);
     }
-    const int nb = H / 32, kb128 = H / 128;
+    // Four lanes share one 32-element block (8 bf16 each), so every load and every
+    // code store of the warp is 512 / 256 contiguous bytes; the block maximum takes
+    // two shuffles and one lane in four packs its group's scale bytes into a word.
+    const int kb128 = H / 128;
     const uint4 *src = x + t * (H / 8);
-    for (int b = lane; b < nb; b += 32) {
-        float v[32];
+    constexpr int U = 4;                       // 256-element slices in flight per lane
+    for (int base = 0; base < H; base += 256 * U) {
+        uint4 raw[U];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const uint4 p = __ldg(src + b * 4 + q);
-            const __nv_bfloat162 *hp = reinterpret_cast<const __nv_bfloat162 *>(&p);
+        for (int u = 0; u < U; ++u) {
+            const int e0 = base + u * 256 + lane * 8;
+            raw[u] = e0 < H ? __ldg(src + e0 / 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int e0 = base + u * 256 + lane * 8;
+            float v[8];
+            const __nv_bfloat162 *hp = reinterpret_cast<const __nv_bfloat162 *>(&raw[u]);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float2 f = __bfloat1622float2(hp[i]);
-                v[8 * q + 2 * i] = f.x;
-                v[8 * q + 2 * i + 1] = f.y;
+                v[2 * i] = f.x;
+                v[2 * i + 1] = f.y;
             }
-        }
-        const int X = mx::scale_exp(mx::amax32(v));
-        uint4 lo, hi;
-        mx::quantize32(v, X, lo, hi);
-        const uint8_t byte = (uint8_t)(X + 127);
+            float a = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            if (j < k && dst[j] >= 0) {
-                uint4 *d = reinterpret_cast<uint4 *>(x_q + (int64_t)dst[j] * H) + 2 * b;
-                d[0] = lo;
-                d[1] = hi;
-                x_sf[mx::tile_sf_offset(tile[j], kb128, mm[j], b)] = byte;
+            for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(v[i]));
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+            a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+            const int X = mx::scale_exp(a);
+            const uint2 q = mx::quantize8(v, X);
+            // scale bytes of the 4 blocks of this half-warp (blocks kb0 .. kb0+3), one word
+            const uint32_t byte = (uint32_t)(X + 127);
+            const int g0 = lane & 16;
+            const uint32_t word = __shfl_sync(0xFFFFFFFFu, byte, g0) | (__shfl_sync(0xFFFFFFFFu, byte, g0 + 4) << 8) |
+                                  (__shfl_sync(0xFFFFFFFFu, byte, g0 + 8) << 16) |
+                                  (__shfl_sync(0xFFFFFFFFu, byte, g0 + 12) << 24);
+            if (e0 < H) {
+                const int kb0 = (base + u * 256) / 32 + (lane >> 4) * 4;
+#pragma unroll
+                for (int j = 0; j < KMAX; ++j) {
+                    if (j < k && dst[j] >= 0) {
+                        *reinterpret_cast<uint2 *>(x_q + (int64_t)dst[j] * H + e0) = q;
+                        if ((lane & 15) == 0)
+                            *reinterpret_cast<uint32_t *>(x_sf + mx::tile_sf_offset(tile[j], kb128, mm[j], kb0)) = word;
+                    }
+                }
             }
         }
     }
@@ -477,6 +515,9 @@ extern "C" moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *to
     if (rows_cap < R) return MOE_ERR_INVALID_ARG;
     if (rows_cap >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
     if (T > 0 && (!x || !topk_idx || !x_q || !x_sf || !dst_of_route || !src_of_row)) return MOE_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(x) % 16 || reinterpret_cast<uintptr_t>(x_q) % 8 ||
+        reinterpret_cast<uintptr_t>(x_sf) % 4)
+        return MOE_ERR_UNSUPPORTED;
     const size_t need = moe_workspace_bytes(T, E, k);
     if (!ws || ws_bytes < need || need == 0) return MOE_ERR_WORKSPACE;
 
@@ -490,9 +531,17 @@ extern "C" moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *to
         return MOE_ERR_CUDA;
     if (T > 0) {
         const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
-        permute_scatter_mx_kernel<<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(
-            reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, H, counts, group_offsets, mtile, dst_of_route,
-            src_of_row, x_q, x_sf, rows_cap, err);
+#define MOE_SCATTER_MX(KM)                                                                                   \
+    permute_scatter_mx_kernel<KM><<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(                                  \
+        reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, H, counts, group_offsets, mtile, dst_of_route,       \
+        src_of_row, x_q, x_sf, rows_cap, err)
+        if (k <= 1) MOE_SCATTER_MX(1);
+        else if (k <= 2) MOE_SCATTER_MX(2);
+        else if (k <= 4) MOE_SCATTER_MX(4);
+        else if (k <= 8) MOE_SCATTER_MX(8);
+        else if (k <= 16) MOE_SCATTER_MX(16);
+        else MOE_SCATTER_MX(32);
+#undef MOE_SCATTER_MX
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     return MOE_OK;
