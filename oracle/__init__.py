@@ -58,6 +58,9 @@ def lib():
         L.oracle_gather_rows.argtypes = [_u16p, _int, _int, _i32p, _i64, _u16p]
         pp16 = C.POINTER(_u16p)
         pp8 = C.POINTER(_u8p)
+        L.oracle_moe_fwd_w.restype = None
+        L.oracle_moe_fwd_w.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p, pp16, pp16, pp16,
+                                       _i32p, _f32p, _int, _int, _f64p, _f64p, _f64p, _f64p]
         L.oracle_moe_fwd.restype = None
         L.oracle_moe_fwd.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p, pp16, pp16, pp16,
                                      _i32p, _f32p, _int, _f64p, _f64p, _f64p, _f64p]
@@ -238,10 +241,14 @@ def unpermute_combine(y_perm: np.ndarray, dst_of_route: np.ndarray, topk_w: np.n
 
 # ---------------------------------------------------------------- A3..A5
 
+WEIGHT_IN_COMBINE, WEIGHT_IN_FC1, WEIGHT_IN_FC2 = 0, 1, 2
+
+
 def moe_fwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, tokens=None, round_mode: int = 1,
-            want_fc1: bool = False, want_h: bool = False, want_y: bool = False):
+            want_fc1: bool = False, want_h: bool = False, want_y: bool = False, weight_at: int = 0):
     """Per-token forward: SwiGLU experts + weighted combine (moe_oracle.c).
 
+    weight_at: where the router weight is applied (WEIGHT_IN_COMBINE, _FC1, _FC2).
     Returns dict with out (float64 [n,H]) and optional per-route fc1 [n*k,2F],
     h [n*k,F], y [n*k,H] (NaN rows for dropped routes)."""
     xb = _c(x_bits, np.uint16)
@@ -261,9 +268,9 @@ def moe_fwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, tokens=None, round_mode: int =
     h = np.full((n * k, F), np.nan) if want_h else None
     y = np.full((n * k, H), np.nan) if want_y else None
     pg, pu, pd = (_PtrArray(a, _u16p, np.uint16) for a in (wg, wu, wd))
-    lib().oracle_moe_fwd(n, _p(toks, _i64p), H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr, pd.arr,
-                         _p(ti, _i32p), _p(tw, _f32p), round_mode, _p(out, _f64p),
-                         _p(fc1, _f64p), _p(h, _f64p), _p(y, _f64p))
+    lib().oracle_moe_fwd_w(n, _p(toks, _i64p), H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr, pd.arr,
+                           _p(ti, _i32p), _p(tw, _f32p), round_mode, int(weight_at), _p(out, _f64p),
+                           _p(fc1, _f64p), _p(h, _f64p), _p(y, _f64p))
     return {"out": out, "fc1": fc1, "h": h, "y": y}
 
 

@@ -409,8 +409,10 @@ static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
 /* g = x Wg, u = x Wu (double), h = silu(g) * u (bf16 in round_mode 1),
  * y = h Wd (kept unrounded: the path stores y in fp32).  Wg, Wu are [H,F];
  * Wd is [F,H]. */
+/* One route through one expert: g, u, h = rnd(hw * silu(g) * u) and y = h Wd (hw = 1
+ * except when the router weight is applied in the FC1 epilogue). */
 static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t *Wu,
-                         const uint16_t *Wd, int H, int F, int round_mode,
+                         const uint16_t *Wd, int H, int F, int round_mode, double hw,
                          double *g, double *u, double *h, double *y)
 {
     for (int f = 0; f < F; ++f) { g[f] = 0.0; u[f] = 0.0; }
@@ -422,7 +424,7 @@ static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t 
             u[f] += xv * oracle_bf16_to_double(wu[f]);
         }
     }
-    for (int f = 0; f < F; ++f) h[f] = rnd(silu(g[f]) * u[f], round_mode);
+    for (int f = 0; f < F; ++f) h[f] = rnd(hw * (silu(g[f]) * u[f]), round_mode);
     for (int n = 0; n < H; ++n) y[n] = 0.0;
     for (int f = 0; f < F; ++f) {
         const uint16_t *wd = Wd + (int64_t)f * H;
@@ -441,10 +443,19 @@ static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t 
  * [i*k + j]: fc1 (double [.., 2F], g then u, unrounded), h [.., F], y [.., H];
  * rows of dropped routes are left untouched.  Weights are given per expert
  * (Wg[e], Wu[e]: [H,F]; Wd[e]: [F,H]); only routed experts are read. */
-void oracle_moe_fwd(int64_t n_tokens, const int64_t *tokens, int H, int F, int E, int k,
-                    const uint16_t *x, const uint16_t *const *Wg, const uint16_t *const *Wu,
-                    const uint16_t *const *Wd, const int32_t *topk_idx, const float *topk_w,
-                    int round_mode, double *out, double *fc1, double *h_out, double *y_out)
+/* Where the router weight w of a route is applied ("Add MoE + expert-parallel Python
+ * API surface, PyTorch reference, and tests", Summary: the router weight in the FC1 or
+ * FC2 epilogue; "[JAX] Expert Parallelism", commit log: apply_topk_weights_early):
+ *   weight_at 0  in the combine: out = sum_j w_j y_j            (late, the default)
+ *   weight_at 1  in FC1:  h_j = rnd(w_j silu(g) u), out = sum_j y_j
+ *   weight_at 2  in FC2:  y_j <- w_j y_j,           out = sum_j y_j
+ * All three are the same function in exact arithmetic; they differ in where the
+ * rounding of h falls (weight_at 1 rounds the weighted h).  y_out holds the
+ * per-route y as the path stores it (weighted for 1 and 2). */
+void oracle_moe_fwd_w(int64_t n_tokens, const int64_t *tokens, int H, int F, int E, int k,
+                      const uint16_t *x, const uint16_t *const *Wg, const uint16_t *const *Wu,
+                      const uint16_t *const *Wd, const int32_t *topk_idx, const float *topk_w,
+                      int round_mode, int weight_at, double *out, double *fc1, double *h_out, double *y_out)
 {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_tokens; ++i) {
@@ -456,9 +467,12 @@ void oracle_moe_fwd(int64_t n_tokens, const int64_t *tokens, int H, int F, int E
         for (int j = 0; j < k; ++j) {
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) continue;
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, g, u, h, y);
-            double w = (double)topk_w[t * k + j];
-            for (int n = 0; n < H; ++n) o[n] += w * y[n];
+            const double w = (double)topk_w[t * k + j];
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, weight_at == 1 ? w : 1.0, g, u, h, y);
+            if (weight_at == 2)
+                for (int n = 0; n < H; ++n) y[n] *= w;
+            const double wc = weight_at == 0 ? w : 1.0;
+            for (int n = 0; n < H; ++n) o[n] += wc * y[n];
             int64_t ri = i * k + j;
             if (fc1) { memcpy(fc1 + ri * 2 * F, g, sizeof(double) * F); memcpy(fc1 + ri * 2 * F + F, u, sizeof(double) * F); }
             if (h_out) memcpy(h_out + ri * F, h, sizeof(double) * F);
@@ -467,6 +481,15 @@ void oracle_moe_fwd(int64_t n_tokens, const int64_t *tokens, int H, int F, int E
         for (int n = 0; n < H; ++n) o[n] = rnd_out(o[n], round_mode);
         free(g);
     }
+}
+
+void oracle_moe_fwd(int64_t n_tokens, const int64_t *tokens, int H, int F, int E, int k,
+                    const uint16_t *x, const uint16_t *const *Wg, const uint16_t *const *Wu,
+                    const uint16_t *const *Wd, const int32_t *topk_idx, const float *topk_w,
+                    int round_mode, double *out, double *fc1, double *h_out, double *y_out)
+{
+    oracle_moe_fwd_w(n_tokens, tokens, H, F, E, k, x, Wg, Wu, Wd, topk_idx, topk_w, round_mode, 0, out, fc1,
+                     h_out, y_out);
 }
 
 /* ------------------------------------------------------------------ */
@@ -589,7 +612,7 @@ void oracle_moe_bwd(int64_t T, int H, int F, int E, int k, const uint16_t *x,
         for (int j = 0; j < k; ++j) {
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) { d_topk_w[t * k + j] = 0.0; continue; }
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, g, u, h, y);
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, g, u, h, y);
             double dw = 0.0;
             for (int n = 0; n < H; ++n) dw += oracle_bf16_to_double(dY[t * H + n]) * y[n];
             d_topk_w[t * k + j] = dw;
@@ -631,7 +654,7 @@ void oracle_moe_bwd_dx_tokens(int64_t n_tokens, const int64_t *tokens, int H, in
         for (int j = 0; j < k; ++j) {
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) { d_topk_w[i * k + j] = 0.0; continue; }
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, g, u, h, y);
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, g, u, h, y);
             double dw = 0.0;
             for (int n = 0; n < H; ++n) dw += oracle_bf16_to_double(dY[t * H + n]) * y[n];
             d_topk_w[i * k + j] = dw;
