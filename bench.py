@@ -5,9 +5,10 @@ inputs resident in HBM:
   bf16 forward   route -> permute -> grouped FC1+SwiGLU -> grouped FC2 -> combine
   mixtral        the forward, then the backward (combine bwd, router bwd to the
                  logits, FC2 dgrad + dSwiGLU, FC1 dgrad, grouped wgrad, unpermute-sum)
-  --router sigmoid  routes on sigmoid scores + a seeded expert routing bias
   dsv3_mxfp8     route -> quantising permute -> block-scaled FC1 (h to MXFP8) ->
                  block-scaled FC2 -> combine; weights quantised once, untimed
+Variants: --router sigmoid (sigmoid scores + a seeded expert routing bias);
+--weight-at fc1|fc2 (the router weight applied in the FC1 / FC2 epilogue).
 Default workload: fine_grained (T=4096, H=2048, F=1408, E=64, top-6).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
@@ -192,7 +193,8 @@ def build_workload(shape, dev, stream):
         m(inp["x"], inp["logits"], mw, stream)
     else:
         m = MoeForward(T, H, F, E, k, device=dev, keep_fc1_c=shape.backward,
-                       router="sigmoid" if sigmoid else "softmax", expert_bias=inp.get("expert_bias"))
+                       router="sigmoid" if sigmoid else "softmax", expert_bias=inp.get("expert_bias"),
+                       weight_at=shape.weight_at)
         w.update(layer=m)
         m(inp["x"], inp["logits"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
         if shape.backward:
@@ -312,7 +314,8 @@ def oracle_sample(shape, inp_dev, n_tokens: int, it: int = 0):
     if shape.mxfp8:
         oracle.moe_fwd_mxfp8(x_rows, q["gq"], q["gs"], q["uq"], q["us"], q["dq"], q["ds"], idx_s, w_s)
     else:
-        oracle.moe_fwd(x_rows, wts["W_gate"], wts["W_up"], wts["W_down"], idx_s, w_s)
+        oracle.moe_fwd(x_rows, wts["W_gate"], wts["W_up"], wts["W_down"], idx_s, w_s,
+                       weight_at={"combine": 0, "fc1": 1, "fc2": 2}[shape.weight_at])
         if shape.backward:
             g = oracle.moe_bwd(x_rows, _dense(wts["W_gate"], shape.E), _dense(wts["W_up"], shape.E),
                                _dense(wts["W_down"], shape.E), idx_s, w_s, dy_rows)
@@ -364,6 +367,10 @@ def workload_shape(args):
         shape = dataclasses.replace(shape, name=shape.name + "_" + "_".join(f"{a}{b}" for a, b in kw.items()), **kw)
     if args.router != "softmax":
         shape = dataclasses.replace(shape, name=shape.name + "_" + args.router, router=args.router)
+    if args.weight_at != "combine":
+        if shape.backward or shape.mxfp8:
+            raise SystemExit("--weight-at fc1/fc2 applies to the bf16 forward workloads")
+        shape = dataclasses.replace(shape, name=shape.name + "_w" + args.weight_at, weight_at=args.weight_at)
     return shape
 
 
@@ -501,7 +508,8 @@ def run_gpu(args):
         "vs_baseline": None, "dtype": "mxfp8" if shape.mxfp8 else "bf16",
         "data": "synthetic (seeded; BASELINE shapes and distributions)",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k,
-                   "router": shape.router, "pass": "forward+backward" if shape.backward else "forward",
+                   "router": shape.router, "weight_at": shape.weight_at,
+                   "pass": "forward+backward" if shape.backward else "forward",
                    "active_experts": w["active_experts"],
                    "l2": "flushed between steps (256 MiB write outside the timed events)"},
         "kernels": rates,
@@ -533,6 +541,8 @@ def main(argv=None):
                     help="override sizes of the workload, e.g. 'T=2048,F=4096' (same kind of pass)")
     ap.add_argument("--router", default="softmax", choices=["softmax", "sigmoid"],
                     help="score function of the routing step (sigmoid: + a seeded expert routing bias)")
+    ap.add_argument("--weight-at", default="combine", choices=["combine", "fc1", "fc2"],
+                    help="where the router weight is applied (bf16 forward workloads)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -274,6 +274,31 @@ MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_do
                                      int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
                                      moe_stream_t stream);
 
+/* The same two steps with the router weight applied early ("Add MoE +
+ * expert-parallel Python API surface, PyTorch reference, and tests", Summary:
+ * the router weight in the FC1 or FC2 epilogue; "[JAX] Expert Parallelism",
+ * commit log: apply_topk_weights_early).  Row `row` of the permuted tensors
+ * belongs to route src_of_row[row] (from moe_permute; -1 = padding row, weight
+ * 0) and is scaled by topk_w[src_of_row[row]] (topk_w fp32 [T, k] read flat):
+ *   moe_grouped_fc1_swiglu_weighted   h = bf16(w * silu(g) * u); fc1_c (if
+ *                                      not NULL) keeps the unweighted g | u
+ *   moe_grouped_fc2_weighted          y_perm = w * (h W_down) in fp32
+ * Combine such outputs with moe_unpermute_combine(..., topk_w = NULL, ...).
+ * The three placements are one function in exact arithmetic; the FC1 one
+ * rounds the weighted h to bf16.  Forward only: moe_grouped_ffn_bwd assumes
+ * the weight is applied in the combine.  Other arguments, limits and errors as
+ * above; src_of_row / topk_w NULL with rows_cap > 0 is MOE_ERR_INVALID_ARG. */
+MOE_API moe_status_t moe_grouped_fc1_swiglu_weighted(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                                     const moe_bf16_t *W_up, const int32_t *group_offsets,
+                                                     const int32_t *src_of_row, const float *topk_w, int E,
+                                                     int H, int F, int64_t rows_cap, moe_bf16_t *h,
+                                                     moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                                     moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_fc2_weighted(const moe_bf16_t *h, const moe_bf16_t *W_down,
+                                              const int32_t *group_offsets, const int32_t *src_of_row,
+                                              const float *topk_w, int E, int H, int F, int64_t rows_cap,
+                                              float *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* A5  Weighted unpermute / combine                                     */
 /* ------------------------------------------------------------------ */
@@ -286,7 +311,8 @@ MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_do
  *
  *   y_perm       device fp32 [rows, H]
  *   dst_of_route device int32 [T, k] (from moe_permute)
- *   topk_w       device fp32 [T, k]
+ *   topk_w       device fp32 [T, k], or NULL for weights 1 (the plain sum, when
+ *                the router weight was already applied in FC1 or FC2)
  *   out          device bf16 [T, H] out
  *
  * Limits: H % 8 == 0, 1 <= k <= 32.  Errors: MOE_ERR_INVALID_ARG,

@@ -45,6 +45,9 @@ SIGNATURES = {
     "moe_grouped_ffn_fwd": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_fc1_swiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_fc2": (_st, [_vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
+    "moe_grouped_fc1_swiglu_weighted": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp,
+                                              _sz, _vp]),
+    "moe_grouped_fc2_weighted": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_unpermute_combine": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp]),
     "moe_grouped_ffn_bwd": (_st, [_vp] * 12 + [_i64, _int, _int, _int, _int, _i64] + [_vp] * 8 + [_vp, _sz, _vp]),
     "moe_combine_bwd": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _i64, _vp, _vp, _vp]),
@@ -282,37 +285,54 @@ def moe_grouped_ffn_fwd(x_perm: torch.Tensor, W_gate: torch.Tensor, W_up: torch.
     return h, y_perm, fc1_c
 
 
-def moe_grouped_fc1_swiglu(x_perm, W_gate, W_up, group_offsets, ws: Workspace, h, fc1_c=None, stream=None):
-    """A3 alone: h = silu(x W_gate) * (x W_up) per group (moe.h)."""
+def moe_grouped_fc1_swiglu(x_perm, W_gate, W_up, group_offsets, ws: Workspace, h, fc1_c=None, stream=None,
+                           route_weights=None):
+    """A3 alone: h = silu(x W_gate) * (x W_up) per group (moe.h).  route_weights =
+    (src_of_row, topk_w): h of each row scaled by its route's router weight."""
     rows_cap, H = x_perm.shape
     E, _, F = W_gate.shape
-    _check("moe_grouped_fc1_swiglu", load_library().moe_grouped_fc1_swiglu(
-        _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(group_offsets), E, H, F, rows_cap, _ptr(h),
-        _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    if route_weights is None:
+        _check("moe_grouped_fc1_swiglu", load_library().moe_grouped_fc1_swiglu(
+            _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(group_offsets), E, H, F, rows_cap, _ptr(h),
+            _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    else:
+        src, tw = route_weights
+        _check("moe_grouped_fc1_swiglu_weighted", load_library().moe_grouped_fc1_swiglu_weighted(
+            _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(group_offsets), _ptr(src), _ptr(tw), E, H, F, rows_cap,
+            _ptr(h), _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))
     return h
 
 
-def moe_grouped_fc2(h, W_down, group_offsets, ws: Workspace, y_perm, stream=None):
-    """A4 alone: y_perm = h W_down per group (moe.h)."""
+def moe_grouped_fc2(h, W_down, group_offsets, ws: Workspace, y_perm, stream=None, route_weights=None):
+    """A4 alone: y_perm = h W_down per group (moe.h).  route_weights = (src_of_row,
+    topk_w): y of each row scaled by its route's router weight."""
     rows_cap, F = h.shape
     E, _, H = W_down.shape
-    _check("moe_grouped_fc2", load_library().moe_grouped_fc2(
-        _ptr(h), _ptr(W_down), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
-        _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    if route_weights is None:
+        _check("moe_grouped_fc2", load_library().moe_grouped_fc2(
+            _ptr(h), _ptr(W_down), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
+            _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    else:
+        src, tw = route_weights
+        _check("moe_grouped_fc2_weighted", load_library().moe_grouped_fc2_weighted(
+            _ptr(h), _ptr(W_down), _ptr(group_offsets), _ptr(src), _ptr(tw), E, H, F, rows_cap, _ptr(y_perm),
+            _ptr(ws.buf), ws.nbytes, _stream(stream)))
     return y_perm
 
 
 # ------------------------------------------------------------------ A5
 
-def moe_unpermute_combine(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w: torch.Tensor,
+def moe_unpermute_combine(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w,
                           out=None, stream=None) -> torch.Tensor:
-    """out[t] = sum_j w[t,j] * y_perm[dst[t,j]] in fp32, slot order (moe.h)."""
+    """out[t] = sum_j w[t,j] * y_perm[dst[t,j]] in fp32, slot order (moe.h);
+    topk_w None: the plain sum (weights already applied in FC1 or FC2)."""
     _need(y_perm, "y_perm", torch.float32)
     H = y_perm.shape[1]
     dev = y_perm.device
     _need(dst_of_route, "dst_of_route", torch.int32, None, dev)
     T, k = dst_of_route.shape
-    _need(topk_w, "topk_w", torch.float32, (T, k), dev)
+    if topk_w is not None:
+        _need(topk_w, "topk_w", torch.float32, (T, k), dev)
     if out is None:
         out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     _need(out, "out", torch.bfloat16, (T, H), dev)

@@ -112,6 +112,6 @@ extern "C" moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t
     if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
     if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
-    if (!y_perm || !dst_of_route || !topk_w || !out) return MOE_ERR_INVALID_ARG;
+    if (!y_perm || !dst_of_route || !out) return MOE_ERR_INVALID_ARG;   // topk_w may be null: plain sum
     return moe::cuda_status(moe::combine_rows(y_perm, dst_of_route, topk_w, T, H, k, out, (cudaStream_t)stream));
 }

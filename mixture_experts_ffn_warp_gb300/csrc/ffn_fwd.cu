@@ -16,13 +16,12 @@ moe_status_t check_common(int E, int H, int F, int64_t rows_cap, void *ws, size_
 
 int64_t mblock_bound(int64_t rows_cap, int E) { return (rows_cap + gg::BM - 1) / gg::BM + E; }
 
-}  // namespace
-
-extern "C" moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
-                                               const moe_bf16_t *W_up, const int32_t *group_offsets,
-                                               int E, int H, int F, int64_t rows_cap, moe_bf16_t *h,
-                                               moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
-                                               moe_stream_t stream) {
+// FC1 + SwiGLU and FC2; topk_w / src_of_row non-null: the router weight of each row's
+// route is applied in the epilogue (to h, or to y).
+moe_status_t fc1_impl(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
+                      const int32_t *group_offsets, const int32_t *src_of_row, const float *topk_w, int E, int H,
+                      int F, int64_t rows_cap, moe_bf16_t *h, moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                      moe_stream_t stream) {
     moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!x_perm || !W_gate || !W_up || !group_offsets || !h) return MOE_ERR_INVALID_ARG;
@@ -46,15 +45,16 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const m
     a.ld0 = F;
     a.out1 = reinterpret_cast<__nv_bfloat16 *>(fc1_c);
     a.ld1 = 2 * (int64_t)F;
+    a.route_w = topk_w;
+    a.src_of_row = src_of_row;
     a.err = ws_error_word(ws);
     return gg::launch<Op::FC1_SWIGLU, 256>(tA, tB0, tB1, tC0, tC1, a, mblock_bound(rows_cap, E) * a.n_tiles,
                                            (cudaStream_t)stream);
 }
 
-extern "C" moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_down,
-                                        const int32_t *group_offsets, int E, int H, int F,
-                                        int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
-                                        moe_stream_t stream) {
+moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32_t *group_offsets,
+                      const int32_t *src_of_row, const float *topk_w, int E, int H, int F, int64_t rows_cap,
+                      float *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream) {
     moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!h || !W_down || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
@@ -73,10 +73,49 @@ extern "C" moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W
     b.rows_cap = rows_cap;
     b.out_f32 = y_perm;
     b.ld0 = H;
+    b.route_w = topk_w;
+    b.src_of_row = src_of_row;
     b.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * b.n_tiles;
     if (bn == 256) return gg::launch<Op::FC2, 256>(tA, tB, tB, tC, tC, b, bound, (cudaStream_t)stream);
     return gg::launch<Op::FC2, 128>(tA, tB, tB, tC, tC, b, bound, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                               const moe_bf16_t *W_up, const int32_t *group_offsets,
+                                               int E, int H, int F, int64_t rows_cap, moe_bf16_t *h,
+                                               moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                               moe_stream_t stream) {
+    return fc1_impl(x_perm, W_gate, W_up, group_offsets, nullptr, nullptr, E, H, F, rows_cap, h, fc1_c, ws,
+                    ws_bytes, stream);
+}
+
+extern "C" moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_down,
+                                        const int32_t *group_offsets, int E, int H, int F,
+                                        int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
+                                        moe_stream_t stream) {
+    return fc2_impl(h, W_down, group_offsets, nullptr, nullptr, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
+}
+
+extern "C" moe_status_t moe_grouped_fc1_swiglu_weighted(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                                        const moe_bf16_t *W_up, const int32_t *group_offsets,
+                                                        const int32_t *src_of_row, const float *topk_w, int E,
+                                                        int H, int F, int64_t rows_cap, moe_bf16_t *h,
+                                                        moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                                        moe_stream_t stream) {
+    if (rows_cap > 0 && (!src_of_row || !topk_w)) return MOE_ERR_INVALID_ARG;
+    return fc1_impl(x_perm, W_gate, W_up, group_offsets, src_of_row, topk_w, E, H, F, rows_cap, h, fc1_c, ws,
+                    ws_bytes, stream);
+}
+
+extern "C" moe_status_t moe_grouped_fc2_weighted(const moe_bf16_t *h, const moe_bf16_t *W_down,
+                                                 const int32_t *group_offsets, const int32_t *src_of_row,
+                                                 const float *topk_w, int E, int H, int F, int64_t rows_cap,
+                                                 float *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    if (rows_cap > 0 && (!src_of_row || !topk_w)) return MOE_ERR_INVALID_ARG;
+    return fc2_impl(h, W_down, group_offsets, src_of_row, topk_w, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
 }
 
 extern "C" moe_status_t moe_grouped_ffn_fwd(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,

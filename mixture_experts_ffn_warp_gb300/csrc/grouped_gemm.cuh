@@ -84,6 +84,10 @@ struct Args {
     int nb_rows;          // MXFP8: rows (N) of each expert's B matrix
     uint8_t *out_q;       // FC1_MX: quantised h [rows, N] (E4M3)
     uint8_t *out_sf;      // FC1_MX: h scales in tile layout [mtile][N/128][512]
+    // FC1_SWIGLU / FC2: the router weight of each row's route applied in the epilogue
+    // (h or y scaled by route_w[src_of_row[row]]; padding rows get 0); null = unweighted
+    const float *route_w;
+    const int32_t *src_of_row;
     uint32_t *err;
 };
 
@@ -533,6 +537,11 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             if constexpr (TR::swiglu) {
                 const int64_t row = tl.m0 + r;
                 const bool valid = row < tl.m_end && row < args.rows_cap;
+                float rw = 1.0f;
+                if (args.route_w) {
+                    const int src = valid ? args.src_of_row[row] : -1;
+                    rw = src >= 0 ? args.route_w[src] : 0.0f;
+                }
 #pragma unroll 1
                 for (int c = 0; c < BN / 2; c += 32) {
                     uint32_t g[32], u[32];
@@ -543,7 +552,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     if (n < args.N && (whole || valid)) {
                         float hv[32];
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]);
+                        for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]) * rw;
                         if constexpr (OP == Op::FC1_MX) {
                             // h quantised along F: this thread's 32 columns are one MX block; two
                             // blocks (64 bytes of codes) fill a staging row
@@ -632,11 +641,20 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 static_assert(OP == Op::FC2 || OP == Op::FC2_MX || OP == Op::DGRAD_FC1, "unhandled op");
                 const int64_t row = tl.m0 + r;
                 const bool valid = row < tl.m_end && row < args.rows_cap;
+                float rw = 1.0f;
+                if (args.route_w) {
+                    const int src = valid ? args.src_of_row[row] : -1;
+                    rw = src >= 0 ? args.route_w[src] : 0.0f;
+                }
 #pragma unroll 1
                 for (int c = 0; c < BN; c += 32) {
                     uint32_t d[32];
                     sm100::tmem_ld32(tacc + c, d);
                     sm100::tmem_ld_wait();
+                    if (args.route_w) {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) d[i] = __float_as_uint(__uint_as_float(d[i]) * rw);
+                    }
                     const int n = tl.n0 + c;
                     if (n < args.N) {
                         if (whole) stage_f32x32(d, &tmC0, n, wrow0);

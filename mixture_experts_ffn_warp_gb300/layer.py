@@ -24,12 +24,19 @@ class MoeForward:
 
     router: "softmax" (softmax over the k selected logits) or "sigmoid" (sigmoid
     scores; `expert_bias` [E] fp32 takes part in the selection only; weights
-    normalised by their sum + 1e-20 when `normalize`)."""
+    normalised by their sum + 1e-20 when `normalize`).
+    weight_at: where the router weight is applied: "combine" (default), "fc1"
+    (h scaled before its bf16 rounding) or "fc2" (y scaled); the early placements
+    are forward only."""
 
     def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", align: int = 1,
-                 keep_fc1_c: bool = False, router: str = "softmax", expert_bias=None, normalize: bool = True):
+                 keep_fc1_c: bool = False, router: str = "softmax", expert_bias=None, normalize: bool = True,
+                 weight_at: str = "combine"):
         if router not in ("softmax", "sigmoid"):
             raise ValueError("router must be 'softmax' or 'sigmoid'")
+        if weight_at not in ("combine", "fc1", "fc2"):
+            raise ValueError("weight_at must be 'combine', 'fc1' or 'fc2'")
+        self.weight_at = weight_at
         self.T, self.H, self.F, self.E, self.k, self.align = T, H, F, E, k, align
         self.router, self.expert_bias, self.normalize = router, expert_bias, normalize
         dev = torch.device(device)
@@ -62,19 +69,24 @@ class MoeForward:
     def permute(self, x, stream=None):
         moe_permute(x, self.topk_idx, self.E, self.ws, self.align, out=self.perm, stream=stream)
 
+    def _route_weights(self, at):
+        return (self.perm.src_of_row, self.topk_w) if self.weight_at == at else None
+
     def fc1(self, W_gate, W_up, stream=None):
         moe_grouped_fc1_swiglu(self.perm.x_perm, W_gate, W_up, self.perm.group_offsets, self.ws, self.h,
-                               self.fc1_c, stream=stream)
+                               self.fc1_c, stream=stream, route_weights=self._route_weights("fc1"))
 
     def fc2(self, W_down, stream=None):
-        moe_grouped_fc2(self.h, W_down, self.perm.group_offsets, self.ws, self.y_perm, stream=stream)
+        moe_grouped_fc2(self.h, W_down, self.perm.group_offsets, self.ws, self.y_perm, stream=stream,
+                        route_weights=self._route_weights("fc2"))
 
     def ffn(self, W_gate, W_up, W_down, stream=None):
         self.fc1(W_gate, W_up, stream)
         self.fc2(W_down, stream)
 
     def combine(self, stream=None):
-        moe_unpermute_combine(self.y_perm, self.perm.dst_of_route, self.topk_w, out=self.out, stream=stream)
+        w = self.topk_w if self.weight_at == "combine" else None
+        moe_unpermute_combine(self.y_perm, self.perm.dst_of_route, w, out=self.out, stream=stream)
 
     def __call__(self, x, logits, W_gate, W_up, W_down, stream=None) -> torch.Tensor:
         self.route(logits, stream)
@@ -106,6 +118,8 @@ class MoeBackward:
             raise ValueError("the logits gradient needs d_topk_w")
         if fwd.fc1_c is None:
             raise ValueError("the forward must keep the fc1_c stash (keep_fc1_c=True)")
+        if fwd.weight_at != "combine":
+            raise ValueError("the backward needs the router weight applied in the combine")
         self.fwd = fwd
         T, H, F, E, k, dev, cap = fwd.T, fwd.H, fwd.F, fwd.E, fwd.k, fwd.device, fwd.rows_cap
         self.dy_perm = torch.empty(cap, H, dtype=torch.bfloat16, device=dev)

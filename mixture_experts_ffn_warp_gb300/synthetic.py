@@ -40,6 +40,7 @@ class MoeShape:
     backward: bool = False
     mxfp8: bool = False
     router: str = "softmax"   # or "sigmoid" (sigmoid scores + expert routing bias)
+    weight_at: str = "combine"   # where the router weight is applied: combine, fc1 or fc2
 
     @property
     def R(self) -> int:

@@ -71,6 +71,9 @@ def test_host_validation_before_launch(lib):
     assert lib.moe_route_topk_bwd(fk, fk, fk, 5, 8, 2, 7, 1, fk, nul) == 1       # unknown score function
     assert lib.moe_route_topk_bwd(fk, fk, fk, 5, 2000, 2, 0, 1, fk, nul) == 2    # E > 1024
     assert lib.moe_route_topk_bwd(fk, nul, fk, 5, 8, 2, 1, 1, fk, nul) == 1      # null pointer
+    # weighted FC1 / FC2: route maps required
+    assert lib.moe_grouped_fc1_swiglu_weighted(fk, fk, fk, fk, nul, nul, 4, 128, 128, 8, fk, nul, fk, 4096, nul) == 1
+    assert lib.moe_grouped_fc2_weighted(fk, fk, fk, fk, nul, 4, 128, 128, 8, fk, fk, 4096, nul) == 1
     # permute: H % 8, capacity, workspace
     assert lib.moe_permute(nul, nul, 4, 12, 4, 2, 1, nul, 8, nul, nul, nul, nul, nul, 0, nul) == 2
     assert lib.moe_permute(nul, nul, 4, 16, 4, 2, 1, nul, 7, nul, nul, nul, nul, nul, 0, nul) == 1

@@ -3,7 +3,8 @@ FFN, A5 combine) against the CPU oracle, called through the C ABI.
 
 Integer outputs (expert ids, permutation maps, group sizes/offsets, copied
 rows) must match bit for bit; floating-point outputs must satisfy
-max|err| <= 2e-2 * RMS(oracle) (fp32 weights: 2e-6 absolute)."""
+max|err| <= 2e-2 * RMS(oracle) (fp32 weights: 2e-6 absolute), for the bf16 layer
+output counting the error beyond its own bf16 rounding of the exact value."""
 import numpy as np
 import pytest
 import torch
@@ -77,7 +78,7 @@ def test_forward_parity_small(name):
     # the layer output against the exact value of the same arithmetic (h rounded to bf16
     # where the path stores it, the output sum unrounded): max|err| <= 2e-2 * RMS
     exact = oracle.moe_fwd(xb, Wg, Wu, Wd, ref_idx, ref_w, round_mode=2)
-    assert_close_rms(to_f64(out), exact["out"], what="out")
+    assert_close_rms(to_f64(out), exact["out"], what="out", bf16_out=True)
     # combine on the GPU's own y_perm: fp32 slot-order sum vs the oracle's double sum
     ref_c = oracle.unpermute_combine(y_perm.cpu().numpy(), p.dst_of_route.cpu().numpy(), w.cpu().numpy(), round_mode=2)
     assert np.abs(to_f64(out) - ref_c).max() <= 2.0 ** -7 * np.abs(ref_c).max()
@@ -124,7 +125,7 @@ def test_permute_aligned_groups(align):
     out = moe_unpermute_combine(y_perm, p.dst_of_route, w)
     refo = oracle.moe_fwd(bits(inp["x"]), bits(inp["W_gate"]), bits(inp["W_up"]), bits(inp["W_down"]),
                           idx.cpu().numpy(), w.cpu().numpy(), round_mode=2)
-    assert_close_rms(to_f64(out), refo["out"], what="out")
+    assert_close_rms(to_f64(out), refo["out"], what="out", bf16_out=True)
 
 
 def test_permute_dropped_and_invalid_ids():
@@ -207,7 +208,7 @@ def test_forward_parity_full_size_sampled(name):
     Wg, Wu, Wd = (host_experts(inp[n], experts) for n in ("W_gate", "W_up", "W_down"))
     ref = oracle.moe_fwd(bits(inp["x"]), Wg, Wu, Wd, ref_idx, ref_w, tokens=toks, round_mode=2,
                          want_y=True)
-    assert_close_rms(to_f64(out[torch.from_numpy(toks).cuda()]), ref["out"], what=f"{name} out")
+    assert_close_rms(to_f64(out[torch.from_numpy(toks).cuda()]), ref["out"], what=f"{name} out", bf16_out=True)
     # the fp32 expert outputs of the sampled routes
     rows = torch.from_numpy(ref_p["dst_of_route"][toks].reshape(-1).astype(np.int64)).cuda()
     assert_close_rms(m.y_perm[rows].double().cpu().numpy(), ref["y"], what=f"{name} y_perm")
