@@ -60,7 +60,9 @@ def lib():
         pp8 = C.POINTER(_u8p)
         L.oracle_moe_fwd_w.restype = None
         L.oracle_moe_fwd_w.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p, pp16, pp16, pp16,
-                                       _i32p, _f32p, _int, _int, _f64p, _f64p, _f64p, _f64p]
+                                       _i32p, _f32p, _int, _int, _int, _f64p, _f64p, _f64p, _f64p]
+        L.oracle_mx_fake_quant.restype = None
+        L.oracle_mx_fake_quant.argtypes = [_f64p, _i64, _i64, _f64p]
         L.oracle_moe_fwd.restype = None
         L.oracle_moe_fwd.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p, pp16, pp16, pp16,
                                      _i32p, _f32p, _int, _f64p, _f64p, _f64p, _f64p]
@@ -70,14 +72,14 @@ def lib():
                                            _f64p, _f64p]
         L.oracle_moe_bwd.restype = None
         L.oracle_moe_bwd.argtypes = [_i64, _int, _int, _int, _int, _u16p, pp16, pp16, pp16,
-                                     _i32p, _f32p, _u16p, _int, _f64p, _f64p, _f64p, _f64p, _f64p]
+                                     _i32p, _f32p, _u16p, _int, _int, _f64p, _f64p, _f64p, _f64p, _f64p]
         L.oracle_moe_bwd_dx_tokens.restype = None
         L.oracle_moe_bwd_dx_tokens.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p, pp16, pp16,
-                                               pp16, _i32p, _f32p, _u16p, _int, _f64p, _f64p]
+                                               pp16, _i32p, _f32p, _u16p, _int, _int, _f64p, _f64p]
         L.oracle_moe_bwd_dw_entries.restype = None
         L.oracle_moe_bwd_dw_entries.argtypes = [_i64, _i32p, _i32p, _i32p, _i32p, _i64, _int, _int,
                                                 _int, _int, _u16p, pp16, pp16, pp16, _i32p, _f32p,
-                                                _u16p, _int, _f64p]
+                                                _u16p, _int, _int, _f64p]
         L.oracle_unpermute_combine.restype = None
         L.oracle_unpermute_combine.argtypes = [_f32p, _i32p, _f32p, _i64, _int, _int, _int, _f64p]
         L.oracle_round_bf16_array.restype = None
@@ -245,10 +247,13 @@ WEIGHT_IN_COMBINE, WEIGHT_IN_FC1, WEIGHT_IN_FC2 = 0, 1, 2
 
 
 def moe_fwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, tokens=None, round_mode: int = 1,
-            want_fc1: bool = False, want_h: bool = False, want_y: bool = False, weight_at: int = 0):
+            want_fc1: bool = False, want_h: bool = False, want_y: bool = False, weight_at: int = 0,
+            h_mx: bool = False):
     """Per-token forward: SwiGLU experts + weighted combine (moe_oracle.c).
 
     weight_at: where the router weight is applied (WEIGHT_IN_COMBINE, _FC1, _FC2).
+    h_mx: h quantised to MXFP8 along F (the MXFP8 forward's h; operands are then
+    passed as their MXFP8 round trips, see moe_bwd_mxfp8).
     Returns dict with out (float64 [n,H]) and optional per-route fc1 [n*k,2F],
     h [n*k,F], y [n*k,H] (NaN rows for dropped routes)."""
     xb = _c(x_bits, np.uint16)
@@ -269,7 +274,7 @@ def moe_fwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, tokens=None, round_mode: int =
     y = np.full((n * k, H), np.nan) if want_y else None
     pg, pu, pd = (_PtrArray(a, _u16p, np.uint16) for a in (wg, wu, wd))
     lib().oracle_moe_fwd_w(n, _p(toks, _i64p), H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr, pd.arr,
-                           _p(ti, _i32p), _p(tw, _f32p), round_mode, int(weight_at), _p(out, _f64p),
+                           _p(ti, _i32p), _p(tw, _f32p), round_mode, int(weight_at), int(h_mx), _p(out, _f64p),
                            _p(fc1, _f64p), _p(h, _f64p), _p(y, _f64p))
     return {"out": out, "fc1": fc1, "h": h, "y": y}
 
@@ -326,8 +331,9 @@ def moe_fwd_mxfp8(x_bits, Wg_q, Wg_s, Wu_q, Wu_s, Wd_q, Wd_s, topk_idx, topk_w,
 
 # ---------------------------------------------------------------- A8
 
-def moe_bwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, round_mode: int = 1):
-    """Full backward on a small problem (moe_oracle.c, oracle_moe_bwd)."""
+def moe_bwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, round_mode: int = 1, h_mx: bool = False):
+    """Full backward on a small problem (moe_oracle.c, oracle_moe_bwd).  h_mx: the
+    MXFP8 forward's h (use through moe_bwd_mxfp8)."""
     xb = _c(x_bits, np.uint16)
     T, H = xb.shape
     ti = _c(topk_idx, np.int32)
@@ -345,12 +351,13 @@ def moe_bwd(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, round_mode: int = 1):
     dtw = np.empty((T, k))
     pg, pu, pd = (_PtrArray(a, _u16p, np.uint16) for a in (wg, wu, wd))
     lib().oracle_moe_bwd(T, H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr, pd.arr, _p(ti, _i32p),
-                         _p(tw, _f32p), _p(db, _u16p), round_mode, _p(dx, _f64p), _p(dWg, _f64p),
+                         _p(tw, _f32p), _p(db, _u16p), round_mode, int(h_mx), _p(dx, _f64p), _p(dWg, _f64p),
                          _p(dWu, _f64p), _p(dWd, _f64p), _p(dtw, _f64p))
     return {"dx": dx, "dW_gate": dWg, "dW_up": dWu, "dW_down": dWd, "d_topk_w": dtw}
 
 
-def moe_bwd_dx_tokens(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, tokens, round_mode: int = 1):
+def moe_bwd_dx_tokens(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, tokens, round_mode: int = 1,
+                      h_mx: bool = False):
     """dx and d_topk_w of selected tokens (moe_oracle.c)."""
     xb = _c(x_bits, np.uint16)
     T, H = xb.shape
@@ -369,11 +376,12 @@ def moe_bwd_dx_tokens(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, tokens, rou
     pg, pu, pd = (_PtrArray(a, _u16p, np.uint16) for a in (wg, wu, wd))
     lib().oracle_moe_bwd_dx_tokens(n, _p(toks, _i64p), H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr,
                                    pd.arr, _p(ti, _i32p), _p(tw, _f32p), _p(db, _u16p), round_mode,
-                                   _p(dx, _f64p), _p(dtw, _f64p))
+                                   int(h_mx), _p(dx, _f64p), _p(dtw, _f64p))
     return {"dx": dx, "d_topk_w": dtw}
 
 
-def moe_bwd_dw_entries(entries, x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, round_mode: int = 1):
+def moe_bwd_dw_entries(entries, x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, round_mode: int = 1,
+                       h_mx: bool = False):
     """Selected weight-gradient entries; entries = [(which, e, a, b)] with
     which 0 = dW_gate[e,h,f], 1 = dW_up[e,h,f], 2 = dW_down[e,f,n]."""
     ent = np.asarray(entries, dtype=np.int32).reshape(-1, 4)
@@ -393,5 +401,73 @@ def moe_bwd_dw_entries(entries, x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, r
     lib().oracle_moe_bwd_dw_entries(len(ent), _p(which, _i32p), _p(ee, _i32p), _p(aa, _i32p),
                                     _p(bb, _i32p), T, H, F, E, k, _p(xb, _u16p), pg.arr, pu.arr,
                                     pd.arr, _p(ti, _i32p), _p(tw, _f32p), _p(db, _u16p),
-                                    round_mode, _p(val, _f64p))
+                                    round_mode, int(h_mx), _p(val, _f64p))
     return val
+
+
+# ---------------------------------------------------------------- A8 on the MXFP8 path
+
+_E4M3_TABLE = None
+
+
+def mx_dequantize(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Values of MXFP8 vectors: codes [n, K] (E4M3) times 2^(scale - 127) per 32
+    elements along K (moe_oracle.c, oracle_e4m3_to_double)."""
+    global _E4M3_TABLE
+    if _E4M3_TABLE is None:
+        _E4M3_TABLE = np.array([e4m3_to_double(c) for c in range(256)])
+    vals = _E4M3_TABLE[codes.astype(np.int64)]
+    exp = np.repeat(scales.astype(np.int64) - 127, 32, axis=-1)
+    return np.ldexp(vals, exp)
+
+
+def _exact_bf16_bits(v: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns of values that bf16 holds exactly (raises otherwise)."""
+    f32 = np.asarray(v, dtype=np.float64).astype(np.float32)
+    u = f32.view(np.uint32)
+    if not np.array_equal(f32.astype(np.float64), v) or np.any(u & 0xFFFF):
+        raise ValueError("an MXFP8 value is not exactly representable in bf16")
+    return (u >> 16).astype(np.uint16)
+
+
+def mx_roundtrip_rows(rows_bits: np.ndarray) -> np.ndarray:
+    """bf16 bits of deq(Q(row)) for each row of [n, K], quantised along K."""
+    q, sc = quantize_rows_mxfp8(rows_bits)
+    return _exact_bf16_bits(mx_dequantize(q, sc)).reshape(rows_bits.shape)
+
+
+def mx_roundtrip_cols(mat_bits: np.ndarray) -> np.ndarray:
+    """bf16 bits of deq(Q(column)) for each column of [K, N], quantised along K."""
+    q, sc = quantize_cols_mxfp8(mat_bits)          # [N, K] codes, [N, K/32] scales
+    return np.ascontiguousarray(_exact_bf16_bits(mx_dequantize(q, sc)).T)
+
+
+def mx_roundtrip_weights(Wg, Wu, Wd, experts=None):
+    """MXFP8 round trips of the expert weights along their forward contraction
+    axes: W_gate / W_up [H, F] along H, W_down [F, H] along F.  Returns three
+    per-expert lists (None for experts not in `experts`)."""
+    E = len(Wg)
+    keep = set(range(E)) if experts is None else {int(e) for e in experts}
+    f = lambda W: [mx_roundtrip_cols(np.asarray(W[e])) if e in keep else None for e in range(E)]  # noqa: E731
+    return f(Wg), f(Wu), f(Wd)
+
+
+def moe_bwd_mxfp8(x_bits, Wg, Wu, Wd, topk_idx, topk_w, dY_bits, round_mode: int = 1):
+    """Straight-through backward of the MXFP8 forward on a small problem: the bf16
+    backward (oracle_moe_bwd) on the MXFP8 round trips of x and the weights, with
+    the forward's MXFP8 h ("Add MoE + expert-parallel Python API surface, PyTorch
+    reference, and tests", Summary: quantization round-trips are straight-through).
+    Gradients are with respect to the unquantised x and weights."""
+    xq = mx_roundtrip_rows(np.asarray(x_bits))
+    wg, wu, wd = mx_roundtrip_weights(Wg, Wu, Wd)
+    return moe_bwd(xq, wg, wu, wd, topk_idx, topk_w, dY_bits, round_mode=round_mode, h_mx=True)
+
+
+def mx_fake_quant(v: np.ndarray) -> np.ndarray:
+    """Values of the MXFP8 round trip of each row of a float64 [n, K] array along K
+    (moe_oracle.c, mx_fake_quant: the rule applied to h on the MXFP8 path)."""
+    a = np.ascontiguousarray(v, dtype=np.float64)
+    n, K = a.reshape(-1, a.shape[-1]).shape
+    out = np.empty_like(a)
+    lib().oracle_mx_fake_quant(_p(a, _f64p), n, K, _p(out, _f64p))
+    return out

@@ -164,6 +164,13 @@ void oracle_quantize_mxfp8(const uint16_t *in, int64_t n_vec, int64_t K,
     }
 }
 
+/* Exported form of mx_fake_quant for n vectors of length K (in place allowed). */
+static void mx_fake_quant(const double *in, int64_t K, double *out);
+void oracle_mx_fake_quant(const double *in, int64_t n, int64_t K, double *out)
+{
+    for (int64_t i = 0; i < n; ++i) mx_fake_quant(in + i * K, K, out + i * K);
+}
+
 /* Same rule applied to a double vector (used for h on the MXFP8 path);
  * writes the dequantised values back to out[]. */
 static void mx_fake_quant(const double *in, int64_t K, double *out)
@@ -410,9 +417,11 @@ static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
  * y = h Wd (kept unrounded: the path stores y in fp32).  Wg, Wu are [H,F];
  * Wd is [F,H]. */
 /* One route through one expert: g, u, h = rnd(hw * silu(g) * u) and y = h Wd (hw = 1
- * except when the router weight is applied in the FC1 epilogue). */
+ * except when the router weight is applied in the FC1 epilogue).  h_mx != 0: the
+ * MXFP8 forward's h instead, hw * silu(g) * u quantised to MXFP8 along F and
+ * dequantised (in every round mode: the quantisation is part of that forward). */
 static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t *Wu,
-                         const uint16_t *Wd, int H, int F, int round_mode, double hw,
+                         const uint16_t *Wd, int H, int F, int round_mode, double hw, int h_mx,
                          double *g, double *u, double *h, double *y)
 {
     for (int f = 0; f < F; ++f) { g[f] = 0.0; u[f] = 0.0; }
@@ -424,7 +433,12 @@ static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t 
             u[f] += xv * oracle_bf16_to_double(wu[f]);
         }
     }
-    for (int f = 0; f < F; ++f) h[f] = rnd(hw * (silu(g[f]) * u[f]), round_mode);
+    if (h_mx) {
+        for (int f = 0; f < F; ++f) h[f] = hw * (silu(g[f]) * u[f]);
+        mx_fake_quant(h, F, h);
+    } else {
+        for (int f = 0; f < F; ++f) h[f] = rnd(hw * (silu(g[f]) * u[f]), round_mode);
+    }
     for (int n = 0; n < H; ++n) y[n] = 0.0;
     for (int f = 0; f < F; ++f) {
         const uint16_t *wd = Wd + (int64_t)f * H;
@@ -455,7 +469,8 @@ static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t 
 void oracle_moe_fwd_w(int64_t n_tokens, const int64_t *tokens, int H, int F, int E, int k,
                       const uint16_t *x, const uint16_t *const *Wg, const uint16_t *const *Wu,
                       const uint16_t *const *Wd, const int32_t *topk_idx, const float *topk_w,
-                      int round_mode, int weight_at, double *out, double *fc1, double *h_out, double *y_out)
+                      int round_mode, int weight_at, int h_mx, double *out, double *fc1, double *h_out,
+                      double *y_out)
 {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_tokens; ++i) {
@@ -468,7 +483,8 @@ void oracle_moe_fwd_w(int64_t n_tokens, const int64_t *tokens, int H, int F, int
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) continue;
             const double w = (double)topk_w[t * k + j];
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, weight_at == 1 ? w : 1.0, g, u, h, y);
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, weight_at == 1 ? w : 1.0, h_mx, g, u,
+                         h, y);
             if (weight_at == 2)
                 for (int n = 0; n < H; ++n) y[n] *= w;
             const double wc = weight_at == 0 ? w : 1.0;
@@ -488,7 +504,7 @@ void oracle_moe_fwd(int64_t n_tokens, const int64_t *tokens, int H, int F, int E
                     const uint16_t *const *Wd, const int32_t *topk_idx, const float *topk_w,
                     int round_mode, double *out, double *fc1, double *h_out, double *y_out)
 {
-    oracle_moe_fwd_w(n_tokens, tokens, H, F, E, k, x, Wg, Wu, Wd, topk_idx, topk_w, round_mode, 0, out, fc1,
+    oracle_moe_fwd_w(n_tokens, tokens, H, F, E, k, x, Wg, Wu, Wd, topk_idx, topk_w, round_mode, 0, 0, out, fc1,
                      h_out, y_out);
 }
 
@@ -594,11 +610,18 @@ static void route_bwd(const uint16_t *dYt, double w, const double *g, const doub
  * [T,H].  Outputs (double): dx [T,H] = sum_j dxr(t,j) (bf16 in mode 1);
  * dWg, dWu [E,H,F] = sum over routes of x^T dg / x^T du; dWd [E,F,H] = sum
  * over routes of h^T dy (each bf16 in mode 1); experts with no route get
- * exactly 0.  d_topk_w [T,k] = <dY[t], y(t,j)> (0 for dropped routes). */
+ * exactly 0.  d_topk_w [T,k] = <dY[t], y(t,j)> (0 for dropped routes).
+ *
+ * h_mx != 0: the straight-through backward of the MXFP8 forward ("Add MoE +
+ * expert-parallel Python API surface, PyTorch reference, and tests", Summary:
+ * quantization round-trips are straight-through).  x and the weights are then
+ * passed as their MXFP8 round trips (bf16 bit patterns of the dequantised
+ * values), h is the forward's MXFP8 h (expert_route), and every derivative
+ * treats a quantisation as the identity: the formulas above are unchanged. */
 void oracle_moe_bwd(int64_t T, int H, int F, int E, int k, const uint16_t *x,
                     const uint16_t *const *Wg, const uint16_t *const *Wu, const uint16_t *const *Wd,
                     const int32_t *topk_idx, const float *topk_w, const uint16_t *dY,
-                    int round_mode, double *dx, double *dWg, double *dWu, double *dWd,
+                    int round_mode, int h_mx, double *dx, double *dWg, double *dWu, double *dWd,
                     double *d_topk_w)
 {
     memset(dWg, 0, sizeof(double) * (size_t)E * H * F);
@@ -612,7 +635,7 @@ void oracle_moe_bwd(int64_t T, int H, int F, int E, int k, const uint16_t *x,
         for (int j = 0; j < k; ++j) {
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) { d_topk_w[t * k + j] = 0.0; continue; }
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, g, u, h, y);
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, h_mx, g, u, h, y);
             double dw = 0.0;
             for (int n = 0; n < H; ++n) dw += oracle_bf16_to_double(dY[t * H + n]) * y[n];
             d_topk_w[t * k + j] = dw;
@@ -637,11 +660,11 @@ void oracle_moe_bwd(int64_t T, int H, int F, int E, int k, const uint16_t *x,
 }
 
 /* dx and d_topk_w for a list of tokens (any problem size): dx[i] (double
- * [n_tokens, H]) and d_topk_w[i*k + j], as in oracle_moe_bwd. */
+ * [n_tokens, H]) and d_topk_w[i*k + j], as in oracle_moe_bwd (h_mx likewise). */
 void oracle_moe_bwd_dx_tokens(int64_t n_tokens, const int64_t *tokens, int H, int F, int E, int k,
                               const uint16_t *x, const uint16_t *const *Wg, const uint16_t *const *Wu,
                               const uint16_t *const *Wd, const int32_t *topk_idx, const float *topk_w,
-                              const uint16_t *dY, int round_mode, double *dx, double *d_topk_w)
+                              const uint16_t *dY, int round_mode, int h_mx, double *dx, double *d_topk_w)
 {
 #pragma omp parallel for schedule(dynamic, 1)
     for (int64_t i = 0; i < n_tokens; ++i) {
@@ -654,7 +677,7 @@ void oracle_moe_bwd_dx_tokens(int64_t n_tokens, const int64_t *tokens, int H, in
         for (int j = 0; j < k; ++j) {
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) { d_topk_w[i * k + j] = 0.0; continue; }
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, g, u, h, y);
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, h_mx, g, u, h, y);
             double dw = 0.0;
             for (int n = 0; n < H; ++n) dw += oracle_bf16_to_double(dY[t * H + n]) * y[n];
             d_topk_w[i * k + j] = dw;
@@ -677,7 +700,7 @@ void oracle_moe_bwd_dw_entries(int64_t n_entries, const int32_t *which, const in
                                int64_t T, int H, int F, int E, int k, const uint16_t *x,
                                const uint16_t *const *Wg, const uint16_t *const *Wu,
                                const uint16_t *const *Wd, const int32_t *topk_idx,
-                               const float *topk_w, const uint16_t *dY, int round_mode,
+                               const float *topk_w, const uint16_t *dY, int round_mode, int h_mx,
                                double *val)
 {
 #pragma omp parallel for schedule(dynamic, 1)
@@ -699,6 +722,21 @@ void oracle_moe_bwd_dw_entries(int64_t n_entries, const int32_t *which, const in
             double w = (double)topk_w[r];
             if (wsel == 2) {
                 double h = rnd(silu(g) * u, round_mode);
+                if (h_mx) {   /* MXFP8 h: the whole 32-wide block of f along F */
+                    double hb[32];
+                    const int f0 = f / 32 * 32;
+                    for (int c = 0; c < 32; ++c) {
+                        double gc = 0.0, uc = 0.0;
+                        for (int i = 0; i < H; ++i) {
+                            double xv = oracle_bf16_to_double(xr[i]);
+                            gc += xv * oracle_bf16_to_double(Wg[e][(int64_t)i * F + f0 + c]);
+                            uc += xv * oracle_bf16_to_double(Wu[e][(int64_t)i * F + f0 + c]);
+                        }
+                        hb[c] = silu(gc) * uc;
+                    }
+                    mx_fake_quant(hb, 32, hb);
+                    h = hb[f - f0];
+                }
                 double dy = rnd(w * oracle_bf16_to_double(dY[t * H + hn]), round_mode);
                 acc += h * dy;
             } else {
