@@ -41,6 +41,7 @@ __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ dst_of_route,
                const float *__restrict__ topk_w, int64_t T, int k, int slices,
                uint4 *__restrict__ out) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -86,8 +87,8 @@ template <int KMAX>
 cudaError_t launch(const float *y, const int32_t *dst, const float *w, int64_t T, int k, int slices,
                    moe_bf16_t *out, cudaStream_t s) {
     const int64_t blocks = (T + kCombineWarps - 1) / kCombineWarps;
-    combine_kernel<KMAX><<<(unsigned)blocks, kCombineWarps * 32, 0, s>>>(
-        reinterpret_cast<const float4 *>(y), dst, w, T, k, slices, reinterpret_cast<uint4 *>(out));
+    launch_k(combine_kernel<KMAX>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
+             reinterpret_cast<const float4 *>(y), dst, w, T, k, slices, reinterpret_cast<uint4 *>(out));
     return cudaGetLastError();
 }
 

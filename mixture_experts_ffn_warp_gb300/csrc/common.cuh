@@ -50,4 +50,36 @@ __device__ __forceinline__ void raise_device_error(uint32_t *err, uint32_t bits)
     if (err) atomicOr(err, bits);
 }
 
+// ---------------------------------------------------------------- programmatic dependent launch
+// Every kernel of the library is launched with programmatic stream serialization, so the
+// GPU may schedule it as the kernel before it on the stream drains, instead of after that
+// kernel has fully completed.  Each kernel calls pdl_wait() before its first global-memory
+// access and before any early return: griddepcontrol.wait blocks until the preceding grid
+// has completed and its writes are visible, so nothing a kernel reads or writes can race
+// with earlier work on the stream.  Only on-chip set-up (mbarriers, TMEM allocation,
+// tensor-map prefetch) runs before it.  No kernel triggers its dependents early
+// (griddepcontrol.launch_dependents): measured on the forward chain, an early trigger let
+// the next grid's CTAs occupy SMs during the whole kernel and cost more than it saved,
+// while the implicit trigger at CTA exit removes most of the launch gap.  Without the
+// launch attribute the wait is a no-op and the launch behaves as an ordinary one.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Kernel launch with programmatic stream serialization (arguments are converted to the
+// kernel's parameter types).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            Args &&...args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 }  // namespace moe

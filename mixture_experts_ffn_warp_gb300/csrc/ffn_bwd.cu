@@ -26,6 +26,7 @@ __global__ void __launch_bounds__(kBwdWarps * 32)
 combine_bwd_kernel(const uint4 *__restrict__ dY, const float4 *__restrict__ y_perm,
                    const int32_t *__restrict__ dst_of_route, const float *__restrict__ topk_w, int64_t T,
                    int k, int slices, uint4 *__restrict__ dy_perm, float *__restrict__ d_topk_w) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -85,6 +86,7 @@ combine_bwd_kernel(const uint4 *__restrict__ dY, const float4 *__restrict__ y_pe
 __global__ void zero_pad_rows_kernel(const int32_t *__restrict__ group_sizes,
                                      const int32_t *__restrict__ group_offsets, int row_vecs,
                                      uint4 *__restrict__ rows, int64_t rows_cap) {
+    pdl_wait();
     const int e = blockIdx.x;
     const int64_t first = (int64_t)group_offsets[e] + group_sizes[e];
     const int64_t last = group_offsets[e + 1] < rows_cap ? group_offsets[e + 1] : rows_cap;
@@ -96,9 +98,9 @@ template <int KMAX>
 cudaError_t launch_combine_bwd(const moe_bf16_t *dY, const float *y_perm, const int32_t *dst, const float *w,
                                int64_t T, int H, int k, moe_bf16_t *dy_perm, float *d_topk_w, cudaStream_t s) {
     const int64_t blocks = (T + kBwdWarps - 1) / kBwdWarps;
-    combine_bwd_kernel<KMAX><<<(unsigned)blocks, kBwdWarps * 32, 0, s>>>(
-        reinterpret_cast<const uint4 *>(dY), reinterpret_cast<const float4 *>(y_perm), dst, w, T, k, H / 8,
-        reinterpret_cast<uint4 *>(dy_perm), d_topk_w);
+    launch_k(combine_bwd_kernel<KMAX>, dim3((unsigned)blocks), dim3(kBwdWarps * 32), 0, s,
+             reinterpret_cast<const uint4 *>(dY), reinterpret_cast<const float4 *>(y_perm), dst, w, T, k, H / 8,
+             reinterpret_cast<uint4 *>(dy_perm), d_topk_w);
     return cudaGetLastError();
 }
 
@@ -133,8 +135,8 @@ extern "C" moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const float *y_per
         else e = launch_combine_bwd<32>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
-    zero_pad_rows_kernel<<<E, 256, 0, s>>>(group_sizes, group_offsets, H / 8, reinterpret_cast<uint4 *>(dy_perm),
-                                           rows_cap);
+    launch_k(zero_pad_rows_kernel, dim3(E), dim3(256), 0, s, group_sizes, group_offsets, H / 8,
+             reinterpret_cast<uint4 *>(dy_perm), rows_cap);
     return launch_status();
 }
 

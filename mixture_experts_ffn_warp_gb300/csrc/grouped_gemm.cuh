@@ -109,6 +109,9 @@ struct Cfg {
     static constexpr int SF_COLS = 4 + 4 * (BN / 128);          // per stage: A (4) + B (4 per 128 rows)
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + STG_BYTES + 1024;   // + alignment slack
     static_assert(STAGES >= 2, "shared memory ring too shallow");
+    // two GEMM CTAs never share an SM, so the TMEM allocation made before the programmatic
+    // launch wait never contends with a preceding GEMM still running there
+    static_assert(2 * SMEM_BYTES > 232448, "GEMM CTAs must not be co-resident");
     // output columns produced per tile
     static constexpr int OUT_COLS = Traits<OP>::swiglu ? BN / 2 : BN;
     static_assert(!MX || SF_COL0 + STAGES * SF_COLS <= TMEM_COLS, "TMEM overflow");
@@ -249,6 +252,9 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         sm100::tmem_alloc(&s_tmem_base, C::TMEM_COLS);
         sm100::tmem_relinquish();
     }
+    // everything above is on-chip set-up; from here on the kernel reads what earlier
+    // kernels on the stream wrote
+    pdl_wait();
     const int E = args.E;
     for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = args.group_offsets[i];
     __syncthreads();

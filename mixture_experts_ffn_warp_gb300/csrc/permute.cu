@@ -18,14 +18,25 @@ namespace moe {
 namespace {
 
 constexpr int kScatterWarps = 8;
+// Largest [chunks][E] count matrix the final scan stages in shared memory: 46 KB, within
+// the 48 KB a block may use without opt-in, with room for the kernel's static arrays.
+constexpr int64_t kScanSmemInts = 11776;
 
 // Group sizes, aligned offsets, each chunk's first row per expert (in place of
 // the chunk counts) and, if mtile_start != nullptr, each group's first 128-row
 // M-tile: one block (>= 256 threads), each thread owning up to 4 consecutive experts.
+// s_mat (nullable): shared memory for the whole [chunks][E] count matrix, which is then
+// read from and written back to global memory once, coalesced, instead of one column
+// per thread.
 __device__ void scan_groups(int32_t *chunk_counts, int64_t chunks, int E, int align, int32_t *group_sizes,
-                            int32_t *group_offsets, int32_t *mtile_start) {
+                            int32_t *group_offsets, int32_t *mtile_start, int32_t *s_mat) {
     __shared__ int32_t s_wsum[32], s_wtile[32];
     const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t n = chunks * E;
+    if (s_mat) {
+        for (int64_t i = tid; i < n; i += nt) s_mat[i] = __ldcg(chunk_counts + i);
+        __syncthreads();
+    }
     const int per = (E + nt - 1) / nt;
     const int e0 = tid * per;
     int tot[4] = {0, 0, 0, 0};
@@ -34,8 +45,17 @@ __device__ void scan_groups(int32_t *chunk_counts, int64_t chunks, int E, int al
     for (int i = 0; i < 4; ++i) {
         const int e = e0 + i;
         if (i < per && e < E) {
-#pragma unroll 8
-            for (int64_t c = 0; c < chunks; ++c) tot[i] += __ldcg(chunk_counts + c * E + e);
+            if (s_mat) {
+                for (int64_t c = 0; c < chunks; ++c) tot[i] += s_mat[c * E + e];
+            } else {
+                for (int64_t c0 = 0; c0 < chunks; c0 += 8) {   // 8 loads in flight
+                    int v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = c0 + u < chunks ? __ldcg(chunk_counts + (c0 + u) * E + e) : 0;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) tot[i] += v[u];
+                }
+            }
             const int padded = (tot[i] + align - 1) / align * align;
             pad_sum += padded;
             tile_sum += (padded + 127) / 128;
@@ -71,10 +91,23 @@ __device__ void scan_groups(int32_t *chunk_counts, int64_t chunks, int E, int al
             group_offsets[e] = run;
             if (mtile_start) mtile_start[e] = trun;
             int r2 = run;
-            for (int64_t c = 0; c < chunks; ++c) {
-                const int v = __ldcg(chunk_counts + c * E + e);
-                chunk_counts[c * E + e] = r2;
-                r2 += v;
+            if (s_mat) {
+                for (int64_t c = 0; c < chunks; ++c) {
+                    const int v = s_mat[c * E + e];
+                    s_mat[c * E + e] = r2;
+                    r2 += v;
+                }
+            } else {
+                for (int64_t c0 = 0; c0 < chunks; c0 += 8) {   // 8 loads in flight, then the stores
+                    int v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) v[u] = c0 + u < chunks ? __ldcg(chunk_counts + (c0 + u) * E + e) : 0;
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        if (c0 + u < chunks) chunk_counts[(c0 + u) * E + e] = r2;
+                        r2 += v[u];
+                    }
+                }
             }
             const int padded = (tot[i] + align - 1) / align * align;
             run += padded;
@@ -85,6 +118,10 @@ __device__ void scan_groups(int32_t *chunk_counts, int64_t chunks, int E, int al
             }
         }
     }
+    if (s_mat) {
+        __syncthreads();
+        for (int64_t i = tid; i < n; i += nt) chunk_counts[i] = s_mat[i];
+    }
 }
 
 // Counting pass: per 2048-route chunk, stable ranks (warp ballots + per-warp running
@@ -94,8 +131,11 @@ __global__ void __launch_bounds__(kPermWarps * 32)
 permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E, int align,
                      int32_t *__restrict__ local_rank, int32_t *__restrict__ chunk_counts,
                      int32_t *__restrict__ group_sizes, int32_t *__restrict__ group_offsets,
-                     int32_t *__restrict__ mtile_start, uint32_t *done, uint32_t *err) {
-    extern __shared__ int32_t s_cnt[];   // [kPermWarps][E] running counts
+                     int32_t *__restrict__ mtile_start, int scan_in_smem, uint32_t *done, uint32_t *err) {
+    pdl_wait();
+    // [kPermWarps][E] running counts; in the last block, the [chunks][E] count matrix when
+    // scan_in_smem (the launch then sizes this array for it)
+    extern __shared__ int32_t s_cnt[];
     __shared__ int s_last;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int i = threadIdx.x; i < kPermWarps * E; i += blockDim.x) s_cnt[i] = 0;
@@ -160,7 +200,8 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E, int
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    scan_groups(chunk_counts, gridDim.x, E, align, group_sizes, group_offsets, mtile_start);
+    scan_groups(chunk_counts, gridDim.x, E, align, group_sizes, group_offsets, mtile_start,
+                scan_in_smem ? s_cnt : nullptr);
     if (threadIdx.x == 0) *done = 0u;
 }
 
@@ -169,7 +210,8 @@ __global__ void __launch_bounds__(256)
 permute_scan_kernel(int32_t *__restrict__ chunk_counts, int64_t chunks, int E, int align,
                     int32_t *__restrict__ group_sizes, int32_t *__restrict__ group_offsets,
                     int32_t *__restrict__ mtile_start) {
-    scan_groups(chunk_counts, chunks, E, align, group_sizes, group_offsets, mtile_start);
+    pdl_wait();
+    scan_groups(chunk_counts, chunks, E, align, group_sizes, group_offsets, mtile_start, nullptr);
 }
 
 // Counting pass with the scan in its last block (or the scan alone for R = 0).
@@ -177,11 +219,18 @@ moe_status_t count_and_scan(const int32_t *topk_idx, int64_t R, int E, int align
                             int32_t *counts, int32_t *group_sizes, int32_t *group_offsets, int32_t *mtile,
                             uint32_t *done, uint32_t *err, cudaStream_t s) {
     const int64_t chunks = perm_chunks(R);
-    if (chunks > 0)
-        permute_count_kernel<<<(unsigned)chunks, kPermWarps * 32, kPermWarps * E * sizeof(int32_t), s>>>(
-            topk_idx, R, E, align, local_rank, counts, group_sizes, group_offsets, mtile, done, err);
-    else
-        permute_scan_kernel<<<1, 256, 0, s>>>(counts, 0, E, align, group_sizes, group_offsets, mtile);
+    if (chunks > 0) {
+        // the final scan stages the count matrix in shared memory when it fits
+        const int64_t mat = chunks * E;
+        const int scan_in_smem = mat <= kScanSmemInts ? 1 : 0;
+        const int64_t smem_ints = scan_in_smem && mat > (int64_t)kPermWarps * E ? mat : (int64_t)kPermWarps * E;
+        launch_k(permute_count_kernel, dim3((unsigned)chunks), dim3(kPermWarps * 32),
+                 (size_t)smem_ints * sizeof(int32_t), s, topk_idx, R, E, align, local_rank, counts, group_sizes,
+                 group_offsets, mtile, scan_in_smem, done, err);
+    } else {
+        launch_k(permute_scan_kernel, dim3(1), dim3(256), 0, s, counts, 0, E, align, group_sizes, group_offsets,
+                 mtile);
+    }
     return launch_status();
 }
 
@@ -193,6 +242,7 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
                        const int32_t *__restrict__ chunk_first, int32_t *__restrict__ dst_of_route,
                        int32_t *__restrict__ src_of_row, uint4 *__restrict__ x_perm,
                        int64_t rows_cap, uint32_t *err) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -238,9 +288,8 @@ void launch_scatter(int64_t blocks, cudaStream_t s, const uint4 *x, const int32_
                     int E, int row_vecs, const int32_t *chunk_first, int32_t *dst_of_route, int32_t *src_of_row,
                     uint4 *x_perm, int64_t rows_cap, uint32_t *err) {
 #define MOE_SCATTER(KM)                                                                                        \
-    permute_scatter_kernel<KM><<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(x, topk_idx, T, k, E, row_vecs,  \
-                                                                              chunk_first, dst_of_route,         \
-                                                                              src_of_row, x_perm, rows_cap, err)
+    launch_k(permute_scatter_kernel<KM>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s, x, topk_idx, T, k, \
+             E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, err)
     if (k <= 1) MOE_SCATTER(1);
     else if (k <= 2) MOE_SCATTER(2);
     else if (k <= 4) MOE_SCATTER(4);
@@ -255,6 +304,7 @@ __global__ void permute_pad_kernel(const int32_t *__restrict__ group_sizes,
                                    const int32_t *__restrict__ group_offsets, int E, int row_vecs,
                                    int32_t *__restrict__ src_of_row, uint4 *__restrict__ x_perm,
                                    int64_t rows_cap) {
+    pdl_wait();
     const int e = blockIdx.x;
     const int64_t first = (int64_t)group_offsets[e] + group_sizes[e];
     const int64_t last = group_offsets[e + 1] < rows_cap ? group_offsets[e + 1] : rows_cap;
@@ -301,8 +351,8 @@ extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     if (align > 1) {
-        permute_pad_kernel<<<E, 256, 0, s>>>(group_sizes, group_offsets, E, row_vecs, src_of_row,
-                                             reinterpret_cast<uint4 *>(x_perm), rows_cap);
+        launch_k(permute_pad_kernel, dim3(E), dim3(256), 0, s, group_sizes, group_offsets, E, row_vecs, src_of_row,
+                 reinterpret_cast<uint4 *>(x_perm), rows_cap);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     return MOE_OK;
@@ -389,8 +439,8 @@ extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const in
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     if (align > 1) {
-        permute_pad_kernel<<<E, 256, 0, s>>>(group_sizes, group_offsets, E, row_vecs, src_of_row,
-                                             reinterpret_cast<uint4 *>(x_perm), rows_cap);
+        launch_k(permute_pad_kernel, dim3(E), dim3(256), 0, s, group_sizes, group_offsets, E, row_vecs, src_of_row,
+                 reinterpret_cast<uint4 *>(x_perm), rows_cap);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     if (error_word &&
@@ -419,6 +469,7 @@ permute_scatter_mx_kernel(const uint4 *__restrict__ x, const int32_t *__restrict
                           const int32_t *__restrict__ group_offsets, const int32_t *__restrict__ mtile_start,
                           int32_t *__restrict__ dst_of_route, int32_t *__restrict__ src_of_row,
                           uint8_t *__restrict__ x_q, uint8_t *__restrict__ x_sf, int64_t rows_cap, uint32_t *err) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -532,9 +583,9 @@ extern "C" moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *to
     if (T > 0) {
         const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
 #define MOE_SCATTER_MX(KM)                                                                                   \
-    permute_scatter_mx_kernel<KM><<<(unsigned)blocks, kScatterWarps * 32, 0, s>>>(                                  \
-        reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, H, counts, group_offsets, mtile, dst_of_route,       \
-        src_of_row, x_q, x_sf, rows_cap, err)
+    launch_k(permute_scatter_mx_kernel<KM>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s,               \
+             reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, H, counts, group_offsets, mtile, dst_of_route, \
+             src_of_row, x_q, x_sf, rows_cap, err)
         if (k <= 1) MOE_SCATTER_MX(1);
         else if (k <= 2) MOE_SCATTER_MX(2);
         else if (k <= 4) MOE_SCATTER_MX(4);

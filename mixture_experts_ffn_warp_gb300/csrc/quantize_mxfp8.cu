@@ -17,6 +17,7 @@ namespace moe {
 
 // mtile_start[g] = sum over groups g' < g of ceil(rows(g') / 128); [G+1] entries.
 __global__ void mtile_prefix_kernel(const int32_t *__restrict__ group_offsets, int G, int32_t *__restrict__ mtile_start) {
+    pdl_wait();
     __shared__ int32_t s_warp[32];
     const int g = threadIdx.x, lane = g & 31, warp = g >> 5;
     int t = 0;
@@ -81,6 +82,7 @@ __global__ void __launch_bounds__(kQWarps * 32)
 quantize_rows_kernel(const __nv_bfloat16 *__restrict__ in, int64_t rows, int K,
                      const int32_t *__restrict__ group_offsets, int G, const int32_t *__restrict__ mtile_start,
                      uint8_t *__restrict__ data, uint8_t *__restrict__ scale_rm, uint8_t *__restrict__ scale_tiles) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t row = (int64_t)blockIdx.x * kQWarps + (threadIdx.x >> 5);
     if (row >= rows) return;
@@ -120,6 +122,7 @@ quantize_rows_kernel(const __nv_bfloat16 *__restrict__ in, int64_t rows, int K,
 __global__ void __launch_bounds__(64)
 quantize_weights_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N, uint8_t *__restrict__ data,
                         uint8_t *__restrict__ scales) {
+    pdl_wait();
     __shared__ float tileS[32][65];
     const int n0 = blockIdx.x * 64, kb = blockIdx.y, e = blockIdx.z;
     const __nv_bfloat16 *src = W + ((int64_t)e * K + (int64_t)kb * 32) * N + n0;
@@ -150,8 +153,8 @@ cudaError_t launch_quantize_rows(const __nv_bfloat16 *in, int64_t rows, int K, c
                                  cudaStream_t s) {
     if (rows <= 0) return cudaSuccess;
     const int64_t blocks = (rows + kQWarps - 1) / kQWarps;
-    quantize_rows_kernel<<<(unsigned)blocks, kQWarps * 32, 0, s>>>(in, rows, K, group_offsets, G, mtile_start, data,
-                                                                    scale_rm, scale_tiles);
+    launch_k(quantize_rows_kernel, dim3((unsigned)blocks), dim3(kQWarps * 32), 0, s, in, rows, K, group_offsets, G,
+             mtile_start, data, scale_rm, scale_tiles);
     return cudaGetLastError();
 }
 
@@ -172,7 +175,7 @@ extern "C" moe_status_t moe_grouped_quantize_mxfp8(const moe_bf16_t *in, int64_t
     int32_t *mtile = nullptr;
     if (scale_tiles) {
         mtile = reinterpret_cast<int32_t *>(static_cast<char *>(ws) + kWsHeaderBytes);
-        mtile_prefix_kernel<<<1, 1024, 0, s>>>(group_offsets, G, mtile);
+        launch_k(mtile_prefix_kernel, dim3(1), dim3(1024), 0, s, group_offsets, G, mtile);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     return cuda_status(launch_quantize_rows(reinterpret_cast<const __nv_bfloat16 *>(in), rows, K, group_offsets, G,
@@ -185,7 +188,7 @@ extern "C" moe_status_t moe_quantize_weights_mxfp8(const moe_bf16_t *W, int E, i
     if (K % 128 != 0 || N % 128 != 0 || E > 65535 || K / 32 > 65535) return MOE_ERR_UNSUPPORTED;
     if (!W || !data || !scales) return MOE_ERR_INVALID_ARG;
     dim3 grid(N / 64, K / 32, E);
-    moe::quantize_weights_kernel<<<grid, 64, 0, (cudaStream_t)stream>>>(reinterpret_cast<const __nv_bfloat16 *>(W), K,
-                                                                        N, data, scales);
+    moe::launch_k(moe::quantize_weights_kernel, grid, dim3(64), 0, (cudaStream_t)stream,
+                  reinterpret_cast<const __nv_bfloat16 *>(W), K, N, data, scales);
     return moe::launch_status();
 }

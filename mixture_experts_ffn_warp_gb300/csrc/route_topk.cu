@@ -33,6 +33,7 @@ template <int VPL, bool SIGMOID>
 __global__ void __launch_bounds__(kRouteWarps * 32)
 route_topk_kernel(const float *__restrict__ logits, const float *__restrict__ bias, int64_t T, int E, int k,
                   int normalize, int32_t *__restrict__ topk_idx, float *__restrict__ topk_w) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -112,9 +113,8 @@ template <int VPL, bool SIGMOID>
 cudaError_t launch(const float *logits, const float *bias, int64_t T, int E, int k, int normalize, int32_t *idx,
                    float *w, cudaStream_t s) {
     int64_t blocks = (T + kRouteWarps - 1) / kRouteWarps;
-    route_topk_kernel<VPL, SIGMOID><<<(unsigned)blocks, kRouteWarps * 32, 0, s>>>(logits, bias, T, E, k, normalize,
-                                                                                 idx, w);
-    return cudaGetLastError();
+    return launch_k(route_topk_kernel<VPL, SIGMOID>, dim3((unsigned)blocks), dim3(kRouteWarps * 32), 0, s, logits,
+                    bias, T, E, k, normalize, idx, w);
 }
 
 template <bool SIGMOID>
@@ -140,6 +140,7 @@ __global__ void __launch_bounds__(kRouteWarps * 32)
 route_bwd_kernel(const float *__restrict__ logits, const int32_t *__restrict__ topk_idx,
                  const float *__restrict__ d_topk_w, int64_t T, int E, int k, int normalize,
                  float *__restrict__ d_logits) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -201,7 +202,9 @@ cudaError_t dispatch_bwd(const float *logits, const int32_t *idx, const float *d
                          int normalize, float *dl, cudaStream_t s) {
     const int vpl = (E + 31) / 32;
     const unsigned blocks = (unsigned)((T + kRouteWarps - 1) / kRouteWarps);
-#define MOE_ROUTE_BWD(V) route_bwd_kernel<V, SIGMOID><<<blocks, kRouteWarps * 32, 0, s>>>(logits, idx, dw, T, E, k, normalize, dl)
+#define MOE_ROUTE_BWD(V) \
+    launch_k(route_bwd_kernel<V, SIGMOID>, dim3(blocks), dim3(kRouteWarps * 32), 0, s, logits, idx, dw, T, E, k, \
+             normalize, dl)
     if (vpl <= 1) MOE_ROUTE_BWD(1);
     else if (vpl <= 2) MOE_ROUTE_BWD(2);
     else if (vpl <= 4) MOE_ROUTE_BWD(4);
