@@ -8,7 +8,10 @@ inputs resident in HBM:
   dsv3_mxfp8     route -> quantising permute -> block-scaled FC1 (h to MXFP8) ->
                  block-scaled FC2 -> combine; weights quantised once, untimed
 Variants: --router sigmoid (sigmoid scores + a seeded expert routing bias);
---weight-at fc1|fc2 (the router weight applied in the FC1 / FC2 epilogue).
+--weight-at fc1|fc2 (the router weight applied in the FC1 / FC2 epilogue);
+--backward (forward + backward; on dsv3_mxfp8 the straight-through backward:
+MXFP8 rows dequantised, then the bf16 backward kernels on the values the
+forward's MMAs consumed, weights dequantised once with the quantisation).
 Default workload: fine_grained (T=4096, H=2048, F=1408, E=64, top-6).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
@@ -178,7 +181,7 @@ class Group:
 def build_workload(shape, dev, stream):
     """Inputs, pre-allocated layer objects and the step's kernel groups."""
     import torch
-    from mixture_experts_ffn_warp_gb300 import MoeBackward, MoeForward, MoeForwardMX, MxWeights
+    from mixture_experts_ffn_warp_gb300 import MoeBackward, MoeBackwardMX, MoeForward, MoeForwardMX, MxWeights
     from mixture_experts_ffn_warp_gb300.synthetic import make_inputs
 
     T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
@@ -188,9 +191,15 @@ def build_workload(shape, dev, stream):
     w = {"inp": inp, "shape": shape}
     if shape.mxfp8:
         mw = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"], stream)
-        m = MoeForwardMX(T, H, F, E, k, device=dev, router=shape.router, expert_bias=inp.get("expert_bias"))
+        m = MoeForwardMX(T, H, F, E, k, device=dev, router=shape.router, expert_bias=inp.get("expert_bias"),
+                         keep_fc1_c=shape.backward)
         w.update(layer=m, mw=mw)
         m(inp["x"], inp["logits"], mw, stream)
+        if shape.backward:
+            # the backward's weights: the bf16 values of the MXFP8 codes, prepared once
+            # with the quantisation (untimed)
+            w["bwd"] = MoeBackwardMX(m, want_d_logits=True)
+            w["bwd_weights"] = mw.dequantized(stream)
     else:
         m = MoeForward(T, H, F, E, k, device=dev, keep_fc1_c=shape.backward,
                        router="sigmoid" if sigmoid else "softmax", expert_bias=inp.get("expert_bias"),
@@ -211,7 +220,8 @@ def build_workload(shape, dev, stream):
             Group("permute_mxfp8", lambda: m.permute(inp["x"], stream),
                   nbytes=T * H * 2 + R * H * (1 + 1 / 32) + R * 8, launches=2),
             Group("fc1_swiglu_mxfp8", lambda: m.fc1(mw, stream), flop=4.0 * R * H * F,
-                  nbytes=R * H * (1 + 1 / 32) + 2 * wbytes + R * F * (1 + 1 / 32), fp8=True),
+                  nbytes=R * H * (1 + 1 / 32) + 2 * wbytes + R * F * (1 + 1 / 32)
+                  + (R * 2 * F * 2 if shape.backward else 0), fp8=True),
             Group("fc2_mxfp8", lambda: m.fc2(mw, stream), flop=2.0 * R * H * F,
                   nbytes=R * F * (1 + 1 / 32) + wbytes + R * H * 4, fp8=True),
         ]
@@ -228,14 +238,20 @@ def build_workload(shape, dev, stream):
     g.append(Group("combine", lambda: m.combine(stream), nbytes=R * H * 4 + T * H * 2 + R * 8))
     if shape.backward:
         b = w["bwd"]
+        # the backward's weights: bf16 (on the MXFP8 path the values of the MXFP8 codes)
+        Wg_b, Wu_b, Wd_b = w.get("bwd_weights") or (inp["W_gate"], inp["W_up"], inp["W_down"])
+        wb16 = active * H * F * 2
+        if shape.mxfp8:
+            g.append(Group("dequant_mx", lambda: b.dequantize(stream),
+                           nbytes=R * (H + F) * (1 + 1 / 32) + R * (H + F) * 2, launches=4))
         g += [
             Group("combine_bwd", lambda: b.combine_bwd(inp["dY"], stream),
                   nbytes=T * H * 2 + R * H * 4 + R * H * 2 + R * 8, launches=2),
             Group("route_bwd", lambda: b.router_bwd(inp["logits"], stream), nbytes=R * 4 + R * 8 + T * E * 4),
-            Group("dgrad_fc2_dswiglu", lambda: b.dgrad_fc2(inp["W_down"], stream), flop=2.0 * R * H * F,
-                  nbytes=R * H * 2 + wbytes + R * 2 * F * 2 * 2),
-            Group("dgrad_fc1", lambda: b.dgrad_fc1(inp["W_gate"], inp["W_up"], stream), flop=4.0 * R * H * F,
-                  nbytes=R * 2 * F * 2 + 2 * wbytes + R * H * 4),
+            Group("dgrad_fc2_dswiglu", lambda: b.dgrad_fc2(Wd_b, stream), flop=2.0 * R * H * F,
+                  nbytes=R * H * 2 + wb16 + R * 2 * F * 2 * 2),
+            Group("dgrad_fc1", lambda: b.dgrad_fc1(Wg_b, Wu_b, stream), flop=4.0 * R * H * F,
+                  nbytes=R * 2 * F * 2 + 2 * wb16 + R * H * 4),
             Group("wgrad", lambda: b.wgrad(stream), flop=6.0 * R * H * F,
                   nbytes=R * (F + H + H + 2 * F) * 2 + 3 * E * H * F * 4, launches=2),
             Group("unpermute_sum", lambda: b.unpermute_sum(stream), nbytes=R * H * 4 + T * H * 2 + R * 8),
@@ -257,7 +273,10 @@ def e2e_step(w, host, stream):
     host["out"].copy_(m.out, non_blocking=True)
     if shape.backward:
         host["dy_d"].copy_(host["dy"], non_blocking=True)
-        w["bwd"](host["dy_d"], inp["W_gate"], inp["W_up"], inp["W_down"], stream, logits=host["lg_d"])
+        if shape.mxfp8:
+            w["bwd"](host["dy_d"], w["mw"], stream, logits=host["lg_d"])
+        else:
+            w["bwd"](host["dy_d"], inp["W_gate"], inp["W_up"], inp["W_down"], stream, logits=host["lg_d"])
         host["dx"].copy_(w["bwd"].dx, non_blocking=True)
 
 
@@ -307,12 +326,21 @@ def oracle_sample(shape, inp_dev, n_tokens: int, it: int = 0):
             q["gq"][e], q["gs"][e] = oracle.quantize_cols_mxfp8(wts["W_gate"][e])
             q["uq"][e], q["us"][e] = oracle.quantize_cols_mxfp8(wts["W_up"][e])
             q["dq"][e], q["ds"][e] = oracle.quantize_cols_mxfp8(wts["W_down"][e])
+        if shape.backward:   # the backward's operands: the weights' MXFP8 round trips
+            rt = {n: {int(e): oracle.mx_roundtrip_cols(wts[n][int(e)]) for e in experts}
+                  for n in ("W_gate", "W_up", "W_down")}
     dy_rows = oracle.bf16_bits(inp_dev["dY"].index_select(0, _long(inp_dev, toks))) if shape.backward else None
     t0 = time.perf_counter()
     idx, w = route()
     oracle.permute(idx, shape.E)
     if shape.mxfp8:
         oracle.moe_fwd_mxfp8(x_rows, q["gq"], q["gs"], q["uq"], q["us"], q["dq"], q["ds"], idx_s, w_s)
+        if shape.backward:   # straight-through backward on the round-tripped operands
+            g = oracle.moe_bwd(oracle.mx_roundtrip_rows(x_rows), _dense(rt["W_gate"], shape.E),
+                               _dense(rt["W_up"], shape.E), _dense(rt["W_down"], shape.E), idx_s, w_s, dy_rows,
+                               h_mx=True)
+            oracle.route_topk_bwd(lg[toks], idx_s, g["d_topk_w"].astype("float32"),
+                                  oracle.SCORE_SIGMOID if bias is not None else oracle.SCORE_SOFTMAX)
     else:
         oracle.moe_fwd(x_rows, wts["W_gate"], wts["W_up"], wts["W_down"], idx_s, w_s,
                        weight_at={"combine": 0, "fc1": 1, "fc2": 2}[shape.weight_at])
@@ -351,7 +379,11 @@ def cpu_baseline(shape, inp_dev, target_s: float):
             n = max(1, min(4 * n, int(m * (target_s - spent) / max(dt, 1e-3))))
     return {"value": done / spent, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{done} of {shape.T} tokens in {spent:.1f} s: routing + permutation over all tokens, "
-                      f"the per-token fp64 oracle ({'forward + backward' if shape.backward else 'MXFP8 forward' if shape.mxfp8 else 'forward'}) on the sample"}
+                      f"the per-token fp64 oracle ({_pass_name(shape)}) on the sample"}
+
+
+def _pass_name(shape) -> str:
+    return ("MXFP8 " if shape.mxfp8 else "") + ("forward + backward" if shape.backward else "forward")
 
 
 # ------------------------------------------------------------------ arms
@@ -371,6 +403,8 @@ def workload_shape(args):
         if shape.backward or shape.mxfp8:
             raise SystemExit("--weight-at fc1/fc2 applies to the bf16 forward workloads")
         shape = dataclasses.replace(shape, name=shape.name + "_w" + args.weight_at, weight_at=args.weight_at)
+    if args.backward and not shape.backward:
+        shape = dataclasses.replace(shape, name=shape.name + "_fwdbwd", backward=True)
     return shape
 
 
@@ -559,6 +593,8 @@ def main(argv=None):
                     help="score function of the routing step (sigmoid: + a seeded expert routing bias)")
     ap.add_argument("--weight-at", default="combine", choices=["combine", "fc1", "fc2"],
                     help="where the router weight is applied (bf16 forward workloads)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time forward + backward (the MXFP8 workload: its straight-through backward)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--ref-tokens", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)

@@ -12,6 +12,8 @@
  *   moe_unpermute_combine weighted top-k combine back to token order
  *   moe_grouped_ffn_bwd   dSwiGLU + grouped dgrad / wgrad GEMMs
  *   moe_grouped_quantize_mxfp8 / moe_grouped_ffn_fwd_mxfp8  MXFP8 path
+ *   moe_dequantize_rows_mxfp8 / moe_dequantize_weights_mxfp8  operands of
+ *                         the MXFP8 path's straight-through backward
  *
  * Conventions for every call:
  *   - Pointers named in a call's doc as "device" are device pointers owned by
@@ -393,11 +395,15 @@ MOE_API moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint8_t
                                                const int32_t *group_offsets, int E, int H, int F,
                                                int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf, float *y_perm,
                                                void *ws, size_t ws_bytes, moe_stream_t stream);
+/* moe_grouped_fc1_swiglu_mxfp8 also writes, when fc1_c is non-NULL, the bf16
+ * stash of the fp32 accumulators g | u, bf16 [rows_cap, 2F], for the
+ * straight-through backward (moe_dequantize_rows_mxfp8 below). */
 MOE_API moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,
                                                   const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,
                                                   const int32_t *group_offsets, int E, int H, int F,
-                                                  int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf, void *ws,
-                                                  size_t ws_bytes, moe_stream_t stream);
+                                                  int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf,
+                                                  moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                                  moe_stream_t stream);
 MOE_API moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
                                            const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H, int F,
                                            int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
@@ -465,6 +471,35 @@ MOE_API moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf16_
                                        size_t ws_bytes, moe_stream_t stream);
 MOE_API moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *dst_of_route, int64_t T, int H,
                                        int k, moe_bf16_t *dx, moe_stream_t stream);
+
+/* ------------------------------------------------------------------ */
+/* A8 on the MXFP8 path: straight-through backward                      */
+/* ------------------------------------------------------------------ */
+
+/* The backward of the MXFP8 forward treats every quantisation round trip as
+ * the identity ("Add MoE + expert-parallel Python API surface, PyTorch
+ * reference, and tests", Summary: quantization round-trips are
+ * straight-through).  It is moe_grouped_ffn_bwd run on the values the forward's
+ * block-scaled MMAs consumed: x_perm and h replaced by the dequantised x_q and
+ * h_q rows, the weights by their dequantised codes, fc1_c from
+ * moe_grouped_fc1_swiglu_mxfp8.  Gradients are with respect to the
+ * unquantised x and weights.  Dequantised values (code * 2^(scale - 127)) are
+ * exact in bf16 except below 2^-133, which flushes to zero.
+ *
+ * moe_dequantize_rows_mxfp8: codes uint8 [rows, K] with tile-layout scales of
+ * the groups given by group_offsets [G+1] (as written by moe_permute_mxfp8 or
+ * moe_grouped_fc1_swiglu_mxfp8) -> out bf16 [rows, K]; rows at or past
+ * group_offsets[G] are written as zeros.  ws must hold 256 + 4*(G+1) bytes.
+ * Limits: K % 128 == 0, G <= 1024; codes and out 16-byte aligned.
+ *
+ * moe_dequantize_weights_mxfp8: the inverse of moe_quantize_weights_mxfp8's
+ * layout: tiled codes and weight scales -> W bf16 [E, K, N] (N contiguous).
+ * Limits: K % 128 == 0, N % 128 == 0; data 16-byte aligned. */
+MOE_API moe_status_t moe_dequantize_rows_mxfp8(const uint8_t *codes, const uint8_t *tile_scales,
+                                               const int32_t *group_offsets, int G, int64_t rows, int K,
+                                               moe_bf16_t *out, void *ws, size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_dequantize_weights_mxfp8(const uint8_t *data, const uint8_t *scales, int E, int K, int N,
+                                                  moe_bf16_t *W, moe_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -61,7 +61,9 @@ SIGNATURES = {
     "moe_permute_mxfp8": (_st, [_vp, _vp, _i64, _int, _int, _int, _vp, _vp, _i64, _vp, _vp, _vp, _vp, _vp, _sz,
                                 _vp]),
     "moe_grouped_ffn_fwd_mxfp8": (_st, [_vp] * 9 + [_int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "moe_grouped_fc1_swiglu_mxfp8": (_st, [_vp] * 7 + [_int, _int, _int, _i64, _vp, _vp, _vp, _sz, _vp]),
+    "moe_grouped_fc1_swiglu_mxfp8": (_st, [_vp] * 7 + [_int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_dequantize_rows_mxfp8": (_st, [_vp, _vp, _vp, _int, _i64, _int, _vp, _vp, _sz, _vp]),
+    "moe_dequantize_weights_mxfp8": (_st, [_vp, _vp, _int, _int, _int, _vp, _vp]),
     "moe_grouped_fc2_mxfp8": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
 }
 
@@ -498,14 +500,17 @@ def moe_permute_mxfp8(x: torch.Tensor, topk_idx: torch.Tensor, E: int, ws: Works
 
 
 def moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, ws: Workspace, h_q, h_sf,
-                                 stream=None):
-    """A3 on MXFP8 operands; h quantised to MXFP8 along F (moe.h)."""
+                                 fc1_c=None, stream=None):
+    """A3 on MXFP8 operands; h quantised to MXFP8 along F (moe.h).  fc1_c (bf16
+    [rows_cap, 2F], optional): the g | u stash for the backward."""
     rows_cap, H = x_q.shape
     E = group_offsets.shape[0] - 1
     F = h_q.shape[1]
+    if fc1_c is not None:
+        _need(fc1_c, "fc1_c", torch.bfloat16, (rows_cap, 2 * F))
     _check("moe_grouped_fc1_swiglu_mxfp8", load_library().moe_grouped_fc1_swiglu_mxfp8(
         _ptr(x_q), _ptr(x_sf), _ptr(Wg_q), _ptr(Wg_sf), _ptr(Wu_q), _ptr(Wu_sf), _ptr(group_offsets), E, H, F,
-        rows_cap, _ptr(h_q), _ptr(h_sf), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+        rows_cap, _ptr(h_q), _ptr(h_sf), _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))
 
 
 def moe_grouped_fc2_mxfp8(h_q, h_sf, Wd_q, Wd_sf, group_offsets, ws: Workspace, y_perm, stream=None):
@@ -516,3 +521,38 @@ def moe_grouped_fc2_mxfp8(h_q, h_sf, Wd_q, Wd_sf, group_offsets, ws: Workspace, 
     _check("moe_grouped_fc2_mxfp8", load_library().moe_grouped_fc2_mxfp8(
         _ptr(h_q), _ptr(h_sf), _ptr(Wd_q), _ptr(Wd_sf), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
         _ptr(ws.buf), ws.nbytes, _stream(stream)))
+
+
+# ------------------------------------------------------------------ A8 on the MXFP8 path
+
+def moe_dequantize_rows_mxfp8(codes: torch.Tensor, tile_scales: torch.Tensor, group_offsets: torch.Tensor,
+                              ws: Workspace, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """MXFP8 rows (codes uint8 [rows, K], tile-layout scales of the groups in
+    group_offsets) -> bf16 [rows, K], for the straight-through backward (moe.h)."""
+    _need(codes, "codes", torch.uint8)
+    _need(tile_scales, "tile_scales", torch.uint8)
+    _need(group_offsets, "group_offsets", torch.int32)
+    rows, K = codes.shape
+    G = group_offsets.shape[0] - 1
+    if out is None:
+        out = torch.empty(rows, K, dtype=torch.bfloat16, device=codes.device)
+    _need(out, "out", torch.bfloat16, (rows, K))
+    _check("moe_dequantize_rows_mxfp8", load_library().moe_dequantize_rows_mxfp8(
+        _ptr(codes), _ptr(tile_scales), _ptr(group_offsets), G, rows, K, _ptr(out), _ptr(ws.buf), ws.nbytes,
+        _stream(stream)))
+    return out
+
+
+def moe_dequantize_weights_mxfp8(data: torch.Tensor, scales: torch.Tensor, E: int, K: int, N: int,
+                                 out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Tiled MXFP8 expert weights (moe_quantize_weights_mxfp8) -> bf16 [E, K, N] (moe.h)."""
+    _need(data, "data", torch.uint8)
+    _need(scales, "scales", torch.uint8)
+    if data.numel() != E * K * N or scales.numel() != E * K * N // 32:
+        raise ValueError("data / scales do not match E, K, N")
+    if out is None:
+        out = torch.empty(E, K, N, dtype=torch.bfloat16, device=data.device)
+    _need(out, "out", torch.bfloat16, (E, K, N))
+    _check("moe_dequantize_weights_mxfp8", load_library().moe_dequantize_weights_mxfp8(
+        _ptr(data), _ptr(scales), E, K, N, _ptr(out), _stream(stream)))
+    return out

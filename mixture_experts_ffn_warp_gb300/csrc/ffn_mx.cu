@@ -26,8 +26,9 @@ bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0;
 extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,
                                                      const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,
                                                      const int32_t *group_offsets, int E, int H, int F,
-                                                     int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf, void *ws,
-                                                     size_t ws_bytes, moe_stream_t stream) {
+                                                     int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf,
+                                                     moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                                     moe_stream_t stream) {
     moe_status_t st = check_mx(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!x_q || !x_sf || !Wg_q || !Wg_sf || !Wu_q || !Wu_sf || !group_offsets || !h_q || !h_sf)
@@ -53,6 +54,8 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const u
     a.out_q = h_q;
     a.ld0 = F;
     a.out_sf = h_sf;
+    a.out1 = reinterpret_cast<__nv_bfloat16 *>(fc1_c);   // nullable: the g | u stash
+    a.ld1 = 2 * (int64_t)F;
     a.err = ws_error_word(ws);
     return gg::launch<Op::FC1_MX, 256>(tA, tA, tA, tC, tC, a, mblock_bound(rows_cap, E) * a.n_tiles,
                                        (cudaStream_t)stream);
@@ -96,7 +99,7 @@ extern "C" moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint
                                                   uint8_t *h_q, uint8_t *h_sf, float *y_perm, void *ws,
                                                   size_t ws_bytes, moe_stream_t stream) {
     moe_status_t st = moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, E, H, F,
-                                                   rows_cap, h_q, h_sf, ws, ws_bytes, stream);
+                                                   rows_cap, h_q, h_sf, nullptr, ws, ws_bytes, stream);
     if (st != MOE_OK) return st;
     return moe_grouped_fc2_mxfp8(h_q, h_sf, Wd_q, Wd_sf, group_offsets, E, H, F, rows_cap, y_perm, ws, ws_bytes,
                                  stream);

@@ -69,7 +69,7 @@ struct Args {
     __nv_bfloat16 *out0;   // FC1: h; DSWIGLU: [dg | du]
     float *out_f32;        // FC2: y_perm; DGRAD_FC1: dx_perm; WGRAD: dW_down / dW_gate (row pitch ld0)
     int64_t ld0;
-    __nv_bfloat16 *out1;   // FC1: fc1_c stash (nullable)
+    __nv_bfloat16 *out1;   // FC1, FC1_MX: fc1_c stash (nullable)
     float *out1_f32;       // WGRAD_GATEUP: dW_up (row pitch ld1)
     int64_t ld1;
     const __nv_bfloat16 *aux;   // DSWIGLU: fc1_c
@@ -577,6 +577,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                                 dq[1] = hi;
                             }
                             args.out_sf[mx::tile_sf_offset(tl.mtile, args.N / 128, r, n / 32)] = (uint8_t)(X + 127);
+                            if (args.out1) {   // bf16 stash of g | u for the straight-through backward
+                                float gv[32], uv[32];
+#pragma unroll
+                                for (int i = 0; i < 32; ++i) {
+                                    gv[i] = __uint_as_float(g[i]);
+                                    uv[i] = __uint_as_float(u[i]);
+                                }
+                                store_bf16x32(args.out1 + row * args.ld1 + n, gv);
+                                store_bf16x32(args.out1 + row * args.ld1 + args.N + n, uv);
+                            }
                         } else {
                             float gv[32], uv[32];
 #pragma unroll

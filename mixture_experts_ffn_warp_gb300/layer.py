@@ -13,6 +13,7 @@ import torch
 from ._binding import (SCORE_SIGMOID, SCORE_SOFTMAX, Permutation, PermutationMX, Workspace, moe_combine_bwd,
                        moe_grouped_dgrad_fc1, moe_route_topk_bwd, moe_route_topk_sigmoid,
                        moe_grouped_fc1_swiglu_mxfp8, moe_grouped_fc2_mxfp8, moe_permute_mxfp8,
+                       moe_dequantize_rows_mxfp8, moe_dequantize_weights_mxfp8,
                        moe_quantize_weights_mxfp8, mx_tile_scale_bytes,
                        moe_grouped_dgrad_fc2_dswiglu, moe_grouped_fc1_swiglu, moe_grouped_fc2,
                        moe_grouped_wgrad, moe_permute, moe_route_topk, moe_unpermute_combine,
@@ -176,9 +177,21 @@ class MxWeights:
     """Expert weights quantised once to MXFP8 (K-major codes + tile-layout scales)."""
 
     def __init__(self, W_gate, W_up, W_down, stream=None):
+        self.E, self.H, self.F = W_gate.shape
         self.Wg_q, self.Wg_sf = moe_quantize_weights_mxfp8(W_gate, stream)   # K = H, N = F
         self.Wu_q, self.Wu_sf = moe_quantize_weights_mxfp8(W_up, stream)
         self.Wd_q, self.Wd_sf = moe_quantize_weights_mxfp8(W_down, stream)   # K = F, N = H
+        self._deq = None
+
+    def dequantized(self, stream=None):
+        """(W_gate, W_up, W_down) as the bf16 values of their MXFP8 codes, in the
+        original layouts [E, H, F] / [E, F, H]; computed once."""
+        if self._deq is None:
+            E, H, F = self.E, self.H, self.F
+            self._deq = (moe_dequantize_weights_mxfp8(self.Wg_q, self.Wg_sf, E, H, F, stream=stream),
+                         moe_dequantize_weights_mxfp8(self.Wu_q, self.Wu_sf, E, H, F, stream=stream),
+                         moe_dequantize_weights_mxfp8(self.Wd_q, self.Wd_sf, E, F, H, stream=stream))
+        return self._deq
 
 
 class MoeForwardMX:
@@ -187,9 +200,10 @@ class MoeForwardMX:
     router / expert_bias / normalize as for MoeForward."""
 
     def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", router: str = "softmax",
-                 expert_bias=None, normalize: bool = True):
+                 expert_bias=None, normalize: bool = True, keep_fc1_c: bool = False):
         if router not in ("softmax", "sigmoid"):
             raise ValueError("router must be 'softmax' or 'sigmoid'")
+        self.weight_at = "combine"
         self.T, self.H, self.F, self.E, self.k = T, H, F, E, k
         self.router, self.expert_bias, self.normalize = router, expert_bias, normalize
         dev = torch.device(device)
@@ -210,6 +224,7 @@ class MoeForwardMX:
         self.h_sf = torch.zeros(mx_tile_scale_bytes(cap, E, F), dtype=torch.uint8, device=dev)
         self.y_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
         self.out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        self.fc1_c = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev) if keep_fc1_c else None
 
     route = MoeForward.route
 
@@ -219,7 +234,7 @@ class MoeForwardMX:
     def fc1(self, w: MxWeights, stream=None):
         p = self.perm
         moe_grouped_fc1_swiglu_mxfp8(p.x_q, p.x_sf, w.Wg_q, w.Wg_sf, w.Wu_q, w.Wu_sf, p.group_offsets, self.ws,
-                                     self.h_q, self.h_sf, stream=stream)
+                                     self.h_q, self.h_sf, fc1_c=self.fc1_c, stream=stream)
 
     def fc2(self, w: MxWeights, stream=None):
         moe_grouped_fc2_mxfp8(self.h_q, self.h_sf, w.Wd_q, w.Wd_sf, self.perm.group_offsets, self.ws, self.y_perm,
@@ -235,3 +250,44 @@ class MoeForwardMX:
         self.fc2(w, stream)
         self.combine(stream)
         return self.out
+
+
+class MoeBackwardMX(MoeBackward):
+    """Straight-through backward of a MoeForwardMX built with keep_fc1_c=True
+    ("Add MoE + expert-parallel Python API surface, PyTorch reference, and tests",
+    Summary: quantization round-trips are straight-through): the bf16 backward
+    kernels run on the values the forward's block-scaled MMAs consumed -- x and h
+    dequantised from their MXFP8 rows, the weights from their MXFP8 codes
+    (MxWeights.dequantized) -- with the g | u stash of the MXFP8 FC1.  Outputs as
+    MoeBackward (gradients with respect to the unquantised x and weights)."""
+
+    def __init__(self, fwd: MoeForwardMX, want_d_topk_w: bool = True, want_d_logits: bool = False):
+        super().__init__(fwd, want_d_topk_w, want_d_logits)
+        cap, dev = fwd.rows_cap, fwd.device
+        self.x_deq = torch.empty(cap, fwd.H, dtype=torch.bfloat16, device=dev)
+        self.h_deq = torch.empty(cap, fwd.F, dtype=torch.bfloat16, device=dev)
+
+    def dequantize(self, stream=None):
+        f = self.fwd
+        moe_dequantize_rows_mxfp8(f.perm.x_q, f.perm.x_sf, f.perm.group_offsets, f.ws, out=self.x_deq, stream=stream)
+        moe_dequantize_rows_mxfp8(f.h_q, f.h_sf, f.perm.group_offsets, f.ws, out=self.h_deq, stream=stream)
+
+    def wgrad(self, stream=None):
+        f = self.fwd
+        moe_grouped_wgrad(self.x_deq, self.h_deq, self.dy_perm, self.dgu, f.perm.group_offsets, f.ws, self.dW_gate,
+                          self.dW_up, self.dW_down, stream=stream)
+
+    def __call__(self, dY, w: MxWeights, stream=None, logits=None):
+        """logits: the forward's router logits, needed for d_logits."""
+        if self.d_logits is not None and logits is None:
+            raise ValueError("the logits gradient needs the forward's logits")
+        Wg, Wu, Wd = w.dequantized(stream)
+        self.dequantize(stream)
+        self.combine_bwd(dY, stream)
+        if self.d_logits is not None:
+            self.router_bwd(logits, stream)
+        self.dgrad_fc2(Wd, stream)
+        self.dgrad_fc1(Wg, Wu, stream)
+        self.wgrad(stream)
+        self.unpermute_sum(stream)
+        return self.dx
