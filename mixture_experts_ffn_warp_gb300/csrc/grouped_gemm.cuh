@@ -396,20 +396,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
                 const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
                 const uint32_t sb = sa + C::A_BYTES;
+                int kk_end = TR::BK / UMMA_K;   // K slices of 16 rows this stage contributes
                 if constexpr (TR::k_grouped) {
-                    // zero the K rows past the group's end (they belong to the next group)
+                    // the group ends inside this stage: only the 16-row slices holding its rows
+                    // are multiplied, and the rows of the last one past the group's end (they
+                    // belong to the next group) are zeroed in every operand box
                     const int valid = tl.k_rows - kb * TR::BK;
                     if (valid < TR::BK) {
-                        uint8_t *pa = smem + stage * C::STAGE_BYTES;
-                        const int nbox = 2 + BN / 64;
-                        const int zrows = TR::BK - valid;
-                        for (int i = lane; i < nbox * zrows * 8; i += 32) {
-                            const int box = i / (zrows * 8);
-                            const int rem = i - box * zrows * 8;
-                            const int row = valid + rem / 8, c16 = rem % 8;
-                            *reinterpret_cast<uint4 *>(pa + box * 8192 + row * 128 + c16 * 16) = make_uint4(0, 0, 0, 0);
+                        kk_end = (valid + UMMA_K - 1) / UMMA_K;
+                        const int zrows = kk_end * UMMA_K - valid;
+                        if (zrows > 0) {
+                            uint8_t *pa = smem + stage * C::STAGE_BYTES;
+                            const int nbox = 2 + BN / 64;
+                            for (int i = lane; i < nbox * zrows * 8; i += 32) {
+                                const int box = i / (zrows * 8);
+                                const int rem = i - box * zrows * 8;
+                                const int row = valid + rem / 8, c16 = rem % 8;
+                                *reinterpret_cast<uint4 *>(pa + box * 8192 + row * 128 + c16 * 16) =
+                                    make_uint4(0, 0, 0, 0);
+                            }
+                            sm100::fence_proxy_async_smem();
                         }
-                        sm100::fence_proxy_async_smem();
                         __syncwarp();
                     }
                 }
@@ -434,6 +441,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     } else {
 #pragma unroll
                         for (int kk = 0; kk < TR::BK / UMMA_K; ++kk) {
+                            if (kk >= kk_end) break;
                             uint64_t ad, bd;
                             if constexpr (TR::a_mn) ad = sm100::sdesc_sw128(sa + kk * 2048, 8192, 1024);
                             else ad = sm100::sdesc_sw128(sa + kk * 32, 16, 1024);
