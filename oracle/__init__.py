@@ -82,6 +82,8 @@ def lib():
                                                 _u16p, _int, _int, _f64p]
         L.oracle_unpermute_combine.restype = None
         L.oracle_unpermute_combine.argtypes = [_f32p, _i32p, _f32p, _i64, _int, _int, _int, _f64p]
+        L.oracle_unpermute_combine_mxfp8.restype = None
+        L.oracle_unpermute_combine_mxfp8.argtypes = [_f32p, _i32p, _f32p, _i64, _int, _int, _u8p, _u8p]
         L.oracle_round_bf16_array.restype = None
         L.oracle_round_bf16_array.argtypes = [_f64p, _i64, _f64p]
         L.oracle_num_threads.restype = _int
@@ -239,6 +241,22 @@ def unpermute_combine(y_perm: np.ndarray, dst_of_route: np.ndarray, topk_w: np.n
     lib().oracle_unpermute_combine(_p(yb, _f32p), _p(dst, _i32p), _p(tw, _f32p), T, H, k,
                                    round_mode, _p(out, _f64p))
     return out
+
+
+def unpermute_combine_mxfp8(y_perm: np.ndarray, dst_of_route: np.ndarray, topk_w: np.ndarray):
+    """The combine with an MXFP8 output (moe_oracle.c, oracle_unpermute_combine_mxfp8):
+    fp32 slot-order sum, then the MX rule along H.  Returns (codes uint8 [T, H],
+    scales uint8 [T, H/32])."""
+    yb = _c(y_perm, np.float32)
+    H = yb.shape[1]
+    dst = _c(dst_of_route, np.int32)
+    tw = _c(topk_w, np.float32)
+    T, k = dst.shape
+    codes = np.empty((T, H), np.uint8)
+    scales = np.empty((T, H // 32), np.uint8)
+    lib().oracle_unpermute_combine_mxfp8(_p(yb, _f32p), _p(dst, _i32p), _p(tw, _f32p), T, H, k,
+                                         _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
 
 
 # ---------------------------------------------------------------- A3..A5

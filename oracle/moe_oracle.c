@@ -406,6 +406,41 @@ void oracle_unpermute_combine(const float *y_perm, const int32_t *dst_of_route,
     }
 }
 
+/* The combine with an MXFP8 output encoding ("Add MoE + expert-parallel Python API
+ * surface, PyTorch reference, and tests", Summary: bf16, mxfp8 and nvfp4 public
+ * outputs as block-scaled tensors in their logical, unswizzled layout).  The sum is
+ * the combine's own: fp32, slot order, one rounding per multiply-add (fmaf), dropped
+ * routes skipped, starting from +0; its fp32 value then takes the MX rule along H:
+ * codes [T, H] (E4M3) and scales [T, H/32] (UE8M0, row-major).  The codes are
+ * decided on the fp32 value, as the kernel decides them. */
+void oracle_unpermute_combine_mxfp8(const float *y_perm, const int32_t *dst_of_route,
+                                    const float *topk_w, int64_t T, int H, int k,
+                                    uint8_t *codes, uint8_t *scales)
+{
+    float *acc = (float *)malloc(sizeof(float) * (size_t)H);
+    for (int64_t t = 0; t < T; ++t) {
+        for (int n = 0; n < H; ++n) acc[n] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            int32_t row = dst_of_route[t * k + j];
+            if (row < 0) continue;
+            const float w = topk_w[t * k + j];
+            for (int n = 0; n < H; ++n) acc[n] = fmaf(w, y_perm[(int64_t)row * H + n], acc[n]);
+        }
+        for (int b = 0; b < H / 32; ++b) {
+            double amax = 0.0;
+            for (int i = 0; i < 32; ++i) {
+                double a = fabs((double)acc[b * 32 + i]);
+                if (a > amax) amax = a;
+            }
+            int X = mx_scale_exp(amax);
+            scales[t * (H / 32) + b] = (uint8_t)(X + 127);
+            for (int i = 0; i < 32; ++i)
+                codes[t * H + b * 32 + i] = oracle_double_to_e4m3(ldexp((double)acc[b * 32 + i], -X));
+        }
+    }
+    free(acc);
+}
+
 /* ------------------------------------------------------------------ */
 /* A3/A4: one route through one expert                                  */
 /* ------------------------------------------------------------------ */
