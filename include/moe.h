@@ -323,6 +323,18 @@ MOE_API moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *d
                                    const float *topk_w, int64_t T, int H, int k,
                                    moe_bf16_t *out, moe_stream_t stream);
 
+/* The combine with the output encoded as MXFP8 along H ("Add MoE + expert-parallel
+ * Python API surface, PyTorch reference, and tests", Summary: mxfp8 public outputs
+ * as block-scaled tensors, logical unswizzled layout): the fp32 slot-order sum of
+ * moe_unpermute_combine, then per 32 consecutive elements of a token row the MX
+ * rule of the MXFP8 section below.  out_q: device uint8 [T, H] (E4M3 codes);
+ * out_sf: device uint8 [T, H/32] (UE8M0 scale bytes, row-major).  topk_w may be
+ * NULL (plain sum).  Limits: H % 32 == 0, 1 <= k <= 32; y_perm 16-byte and out_q
+ * 8-byte aligned. */
+MOE_API moe_status_t moe_unpermute_combine_mxfp8(const float *y_perm, const int32_t *dst_of_route,
+                                                 const float *topk_w, int64_t T, int H, int k, uint8_t *out_q,
+                                                 uint8_t *out_sf, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* A6 + A7  MXFP8 path                                                  */
 /* ------------------------------------------------------------------ */

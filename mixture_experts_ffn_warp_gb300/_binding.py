@@ -63,6 +63,7 @@ SIGNATURES = {
     "moe_grouped_ffn_fwd_mxfp8": (_st, [_vp] * 9 + [_int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_fc1_swiglu_mxfp8": (_st, [_vp] * 7 + [_int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_dequantize_rows_mxfp8": (_st, [_vp, _vp, _vp, _int, _i64, _int, _vp, _vp, _sz, _vp]),
+    "moe_unpermute_combine_mxfp8": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp, _vp]),
     "moe_dequantize_weights_mxfp8": (_st, [_vp, _vp, _int, _int, _int, _vp, _vp]),
     "moe_grouped_fc2_mxfp8": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
 }
@@ -556,3 +557,23 @@ def moe_dequantize_weights_mxfp8(data: torch.Tensor, scales: torch.Tensor, E: in
     _check("moe_dequantize_weights_mxfp8", load_library().moe_dequantize_weights_mxfp8(
         _ptr(data), _ptr(scales), E, K, N, _ptr(out), _stream(stream)))
     return out
+
+
+def moe_unpermute_combine_mxfp8(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w, out_q=None, out_sf=None,
+                                stream=None):
+    """The combine with an MXFP8 output (moe.h): (codes uint8 [T, H], scales uint8 [T, H/32])."""
+    _need(y_perm, "y_perm", torch.float32)
+    _need(dst_of_route, "dst_of_route", torch.int32)
+    T, k = dst_of_route.shape
+    H = y_perm.shape[1]
+    if topk_w is not None:
+        _need(topk_w, "topk_w", torch.float32, (T, k))
+    if out_q is None:
+        out_q = torch.empty(T, H, dtype=torch.uint8, device=y_perm.device)
+    if out_sf is None:
+        out_sf = torch.empty(T, H // 32, dtype=torch.uint8, device=y_perm.device)
+    _need(out_q, "out_q", torch.uint8, (T, H))
+    _need(out_sf, "out_sf", torch.uint8, (T, H // 32))
+    _check("moe_unpermute_combine_mxfp8", load_library().moe_unpermute_combine_mxfp8(
+        _ptr(y_perm), _ptr(dst_of_route), _ptr(topk_w), T, H, k, _ptr(out_q), _ptr(out_sf), _stream(stream)))
+    return out_q, out_sf

@@ -7,6 +7,7 @@
 // in flight.  ("Add MoE + expert-parallel Python API surface, PyTorch
 // reference, and tests", Summary: per-top-k combine.)
 #include "common.cuh"
+#include "mx.cuh"
 
 namespace moe {
 namespace {
@@ -92,6 +93,72 @@ cudaError_t launch(const float *y, const int32_t *dst, const float *w, int64_t T
     return cudaGetLastError();
 }
 
+// As combine_kernel, with the output encoded as MXFP8 along H: four consecutive lanes hold
+// the 32 columns of one block (8 each), take its maximum with two shuffles and quantise
+// their fp32 sums; one lane in four writes the block's scale byte.  Every lane runs the
+// shuffles (a block's lanes are all in range or all out, H % 32 == 0).
+template <int KMAX>
+__global__ void __launch_bounds__(kCombineWarps * 32)
+combine_mx_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ dst_of_route,
+                  const float *__restrict__ topk_w, int64_t T, int k, int slices, uint2 *__restrict__ out_q,
+                  uint8_t *__restrict__ out_sf) {
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t t = (int64_t)blockIdx.x * kCombineWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    int my_dst = -1;
+    float my_w = 0.0f;
+    if (lane < k) {
+        my_dst = dst_of_route[t * k + lane];
+        my_w = topk_w ? topk_w[t * k + lane] : 1.0f;
+    }
+    int dst[KMAX];
+    float w[KMAX];
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        dst[j] = __shfl_sync(0xFFFFFFFFu, my_dst, j);
+        w[j] = __shfl_sync(0xFFFFFFFFu, my_w, j);
+        if (j >= k) dst[j] = -1;
+    }
+    for (int s0 = 0; s0 < slices; s0 += 32) {
+        const int s = s0 + lane;
+        const bool in = s < slices;
+        F8 val[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)
+            if (in && dst[j] >= 0) {
+                const float4 *src = y_perm + ((int64_t)dst[j] * slices + s) * 2;
+                val[j].a = __ldg(src);
+                val[j].b = __ldg(src + 1);
+            }
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (in) {
+#pragma unroll
+            for (int j = 0; j < KMAX; ++j)
+                if (dst[j] >= 0) fma8(acc, w[j], val[j]);
+        }
+        float a = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a = fmaxf(a, fabsf(acc[i]));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 1));
+        a = fmaxf(a, __shfl_xor_sync(0xFFFFFFFFu, a, 2));
+        const int X = mx::scale_exp(a);
+        if (in) {
+            out_q[t * slices + s] = mx::quantize8(acc, X);
+            if ((lane & 3) == 0) out_sf[t * (slices / 4) + s / 4] = (uint8_t)(X + 127);
+        }
+    }
+}
+
+template <int KMAX>
+cudaError_t launch_mx(const float *y, const int32_t *dst, const float *w, int64_t T, int k, int slices,
+                      uint8_t *out_q, uint8_t *out_sf, cudaStream_t s) {
+    const int64_t blocks = (T + kCombineWarps - 1) / kCombineWarps;
+    launch_k(combine_mx_kernel<KMAX>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
+             reinterpret_cast<const float4 *>(y), dst, w, T, k, slices, reinterpret_cast<uint2 *>(out_q), out_sf);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
 cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int64_t T, int H, int k,
@@ -115,4 +182,26 @@ extern "C" moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t
     if (T == 0) return MOE_OK;
     if (!y_perm || !dst_of_route || !out) return MOE_ERR_INVALID_ARG;   // topk_w may be null: plain sum
     return moe::cuda_status(moe::combine_rows(y_perm, dst_of_route, topk_w, T, H, k, out, (cudaStream_t)stream));
+}
+
+extern "C" moe_status_t moe_unpermute_combine_mxfp8(const float *y_perm, const int32_t *dst_of_route,
+                                                    const float *topk_w, int64_t T, int H, int k, uint8_t *out_q,
+                                                    uint8_t *out_sf, moe_stream_t stream) {
+    using namespace moe;
+    if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
+    if (k < 1 || k > 32 || H % 32 != 0) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!y_perm || !dst_of_route || !out_q || !out_sf) return MOE_ERR_INVALID_ARG;   // topk_w may be null
+    if (reinterpret_cast<uintptr_t>(y_perm) % 16 || reinterpret_cast<uintptr_t>(out_q) % 8)
+        return MOE_ERR_UNSUPPORTED;
+    cudaStream_t s = (cudaStream_t)stream;
+    const int sl = H / 8;
+    cudaError_t e;
+    if (k <= 1) e = launch_mx<1>(y_perm, dst_of_route, topk_w, T, k, sl, out_q, out_sf, s);
+    else if (k <= 2) e = launch_mx<2>(y_perm, dst_of_route, topk_w, T, k, sl, out_q, out_sf, s);
+    else if (k <= 4) e = launch_mx<4>(y_perm, dst_of_route, topk_w, T, k, sl, out_q, out_sf, s);
+    else if (k <= 8) e = launch_mx<8>(y_perm, dst_of_route, topk_w, T, k, sl, out_q, out_sf, s);
+    else if (k <= 16) e = launch_mx<16>(y_perm, dst_of_route, topk_w, T, k, sl, out_q, out_sf, s);
+    else e = launch_mx<32>(y_perm, dst_of_route, topk_w, T, k, sl, out_q, out_sf, s);
+    return cuda_status(e);
 }

@@ -13,7 +13,7 @@ import torch
 from ._binding import (SCORE_SIGMOID, SCORE_SOFTMAX, Permutation, PermutationMX, Workspace, moe_combine_bwd,
                        moe_grouped_dgrad_fc1, moe_route_topk_bwd, moe_route_topk_sigmoid,
                        moe_grouped_fc1_swiglu_mxfp8, moe_grouped_fc2_mxfp8, moe_permute_mxfp8,
-                       moe_dequantize_rows_mxfp8, moe_dequantize_weights_mxfp8,
+                       moe_dequantize_rows_mxfp8, moe_dequantize_weights_mxfp8, moe_unpermute_combine_mxfp8,
                        moe_quantize_weights_mxfp8, mx_tile_scale_bytes,
                        moe_grouped_dgrad_fc2_dswiglu, moe_grouped_fc1_swiglu, moe_grouped_fc2,
                        moe_grouped_wgrad, moe_permute, moe_route_topk, moe_unpermute_combine,
@@ -28,11 +28,13 @@ class MoeForward:
     normalised by their sum + 1e-20 when `normalize`).
     weight_at: where the router weight is applied: "combine" (default), "fc1"
     (h scaled before its bf16 rounding) or "fc2" (y scaled); the early placements
-    are forward only."""
+    are forward only.
+    out_format: "bf16" (out [T, H]) or "mxfp8" (out_q E4M3 [T, H] + out_sf UE8M0
+    [T, H/32], the block-scaled output of the same fp32 combine sum)."""
 
     def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", align: int = 1,
                  keep_fc1_c: bool = False, router: str = "softmax", expert_bias=None, normalize: bool = True,
-                 weight_at: str = "combine"):
+                 weight_at: str = "combine", out_format: str = "bf16"):
         if router not in ("softmax", "sigmoid"):
             raise ValueError("router must be 'softmax' or 'sigmoid'")
         if weight_at not in ("combine", "fc1", "fc2"):
@@ -57,7 +59,7 @@ class MoeForward:
         self.h = torch.empty(cap, F, dtype=torch.bfloat16, device=dev)
         self.y_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
         self.fc1_c = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev) if keep_fc1_c else None
-        self.out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        _output_buffers(self, out_format, T, H, dev)
 
     # the steps, each one launch group on the current stream
     def route(self, logits, stream=None):
@@ -86,15 +88,36 @@ class MoeForward:
         self.fc2(W_down, stream)
 
     def combine(self, stream=None):
-        w = self.topk_w if self.weight_at == "combine" else None
-        moe_unpermute_combine(self.y_perm, self.perm.dst_of_route, w, out=self.out, stream=stream)
+        _combine(self, self.topk_w if self.weight_at == "combine" else None, stream)
 
-    def __call__(self, x, logits, W_gate, W_up, W_down, stream=None) -> torch.Tensor:
+    def __call__(self, x, logits, W_gate, W_up, W_down, stream=None):
+        """Returns out (bf16) or, with out_format "mxfp8", (out_q, out_sf)."""
         self.route(logits, stream)
         self.permute(x, stream)
         self.ffn(W_gate, W_up, W_down, stream)
         self.combine(stream)
-        return self.out
+        return self.out if self.out_format == "bf16" else (self.out_q, self.out_sf)
+
+
+def _output_buffers(m, out_format: str, T: int, H: int, dev):
+    if out_format not in ("bf16", "mxfp8"):
+        raise ValueError("out_format must be 'bf16' or 'mxfp8'")
+    m.out_format = out_format
+    m.out = m.out_q = m.out_sf = None
+    if out_format == "bf16":
+        m.out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    else:
+        if H % 32:
+            raise ValueError("an MXFP8 output needs H % 32 == 0")
+        m.out_q = torch.empty(T, H, dtype=torch.uint8, device=dev)
+        m.out_sf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+
+
+def _combine(m, w, stream):
+    if m.out_format == "bf16":
+        moe_unpermute_combine(m.y_perm, m.perm.dst_of_route, w, out=m.out, stream=stream)
+    else:
+        moe_unpermute_combine_mxfp8(m.y_perm, m.perm.dst_of_route, w, out_q=m.out_q, out_sf=m.out_sf, stream=stream)
 
 
 def moe_forward(x, logits, W_gate, W_up, W_down, k: int, align: int = 1, keep_fc1_c: bool = False):
@@ -200,7 +223,7 @@ class MoeForwardMX:
     router / expert_bias / normalize as for MoeForward."""
 
     def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", router: str = "softmax",
-                 expert_bias=None, normalize: bool = True, keep_fc1_c: bool = False):
+                 expert_bias=None, normalize: bool = True, keep_fc1_c: bool = False, out_format: str = "bf16"):
         if router not in ("softmax", "sigmoid"):
             raise ValueError("router must be 'softmax' or 'sigmoid'")
         self.weight_at = "combine"
@@ -223,7 +246,7 @@ class MoeForwardMX:
         self.h_q = torch.empty(cap, F, dtype=torch.uint8, device=dev)
         self.h_sf = torch.zeros(mx_tile_scale_bytes(cap, E, F), dtype=torch.uint8, device=dev)
         self.y_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
-        self.out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+        _output_buffers(self, out_format, T, H, dev)
         self.fc1_c = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev) if keep_fc1_c else None
 
     route = MoeForward.route
@@ -241,15 +264,16 @@ class MoeForwardMX:
                               stream=stream)
 
     def combine(self, stream=None):
-        moe_unpermute_combine(self.y_perm, self.perm.dst_of_route, self.topk_w, out=self.out, stream=stream)
+        _combine(self, self.topk_w, stream)
 
     def __call__(self, x, logits, w: MxWeights, stream=None):
+        """Returns out (bf16) or, with out_format "mxfp8", (out_q, out_sf)."""
         self.route(logits, stream)
         self.permute(x, stream)
         self.fc1(w, stream)
         self.fc2(w, stream)
         self.combine(stream)
-        return self.out
+        return self.out if self.out_format == "bf16" else (self.out_q, self.out_sf)
 
 
 class MoeBackwardMX(MoeBackward):

@@ -49,6 +49,31 @@ def assert_close_rms(got, ref, tol=TOL_BF16, what="", bf16_out=False):
     return err / rms if rms > 0 else 0.0
 
 
+def e4m3_half_step(ref, scale_bytes) -> np.ndarray:
+    """Half the spacing of the MXFP8 grid at each value of `ref` [rows, K] given the
+    blocks' UE8M0 scale bytes [rows, K/32]: 2^(floor(log2 |v|) - 4) for normal E4M3
+    codes (3 mantissa bits), at least half the subnormal step 2^(X - 10)."""
+    ref = np.abs(np.asarray(ref, dtype=np.float64))
+    X = np.repeat(np.asarray(scale_bytes).astype(np.int64) - 127, 32, axis=-1)
+    _, e = np.frexp(ref)                 # ref = m * 2^e, m in [0.5, 1)
+    return np.maximum(np.ldexp(1.0, e - 5), np.ldexp(1.0, X - 10))
+
+
+def assert_close_rms_mx(got, ref, scale_bytes, tol=TOL_MXFP8, what=""):
+    """max |got - ref| <= tol * RMS(ref) for an MXFP8-encoded output compared with the
+    exact value, the bar applied to the error beyond the encoding's own rounding of that
+    value (half an E4M3 step at the block's scale), as for bf16 outputs."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    dev = np.maximum(np.abs(got - ref) - e4m3_half_step(ref, scale_bytes), 0.0)
+    err = float(dev.max()) if got.size else 0.0
+    assert err <= tol * rms, f"{what}: max|err| beyond the encoding {err:.3e} > {tol} * RMS {rms:.3e}"
+    return err / rms if rms > 0 else 0.0
+
+
 def assert_close_ulp(got, ref, what="", slack=2e-3):
     """Element-wise check of a stored bf16 intermediate against the oracle that
     rounds at the same point: the two may round a value on either side of a
