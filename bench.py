@@ -191,23 +191,27 @@ def build_workload(shape, dev, stream):
     w = {"inp": inp, "shape": shape}
     if shape.mxfp8:
         mw = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"], stream)
-        m = MoeForwardMX(T, H, F, E, k, device=dev, router=shape.router, expert_bias=inp.get("expert_bias"),
-                         keep_fc1_c=shape.backward)
+        w["make_layer"] = lambda: MoeForwardMX(T, H, F, E, k, device=dev, router=shape.router,  # noqa: E731
+                                               expert_bias=inp.get("expert_bias"), keep_fc1_c=shape.backward)
+        w["make_bwd"] = lambda f: MoeBackwardMX(f, want_d_logits=True)  # noqa: E731
+        m = w["make_layer"]()
         w.update(layer=m, mw=mw)
         m(inp["x"], inp["logits"], mw, stream)
         if shape.backward:
             # the backward's weights: the bf16 values of the MXFP8 codes, prepared once
             # with the quantisation (untimed)
-            w["bwd"] = MoeBackwardMX(m, want_d_logits=True)
+            w["bwd"] = w["make_bwd"](m)
             w["bwd_weights"] = mw.dequantized(stream)
     else:
-        m = MoeForward(T, H, F, E, k, device=dev, keep_fc1_c=shape.backward,
-                       router="sigmoid" if sigmoid else "softmax", expert_bias=inp.get("expert_bias"),
-                       weight_at=shape.weight_at)
+        w["make_layer"] = lambda: MoeForward(T, H, F, E, k, device=dev, keep_fc1_c=shape.backward,  # noqa: E731
+                                             router="sigmoid" if sigmoid else "softmax",
+                                             expert_bias=inp.get("expert_bias"), weight_at=shape.weight_at)
+        w["make_bwd"] = lambda f: MoeBackward(f, want_d_logits=True)  # noqa: E731
+        m = w["make_layer"]()
         w.update(layer=m)
         m(inp["x"], inp["logits"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
         if shape.backward:
-            w["bwd"] = MoeBackward(m, want_d_logits=True)
+            w["bwd"] = w["make_bwd"](m)
     torch.cuda.synchronize(dev)
     active = int((m.perm.group_sizes > 0).sum().item())     # experts whose weights are read
     w["active_experts"] = active
@@ -260,40 +264,45 @@ def build_workload(shape, dev, stream):
     return w
 
 
-def e2e_step(w, host, stream):
-    """One step through the public layer API, inputs copied from pinned host
-    memory and the result copied back (inside the timed region)."""
-    inp, m, shape = w["inp"], w["layer"], w["shape"]
-    host["x_d"].copy_(host["x"], non_blocking=True)
-    host["lg_d"].copy_(host["lg"], non_blocking=True)
-    if shape.mxfp8:
-        m(host["x_d"], host["lg_d"], w["mw"], stream)
-    else:
-        m(host["x_d"], host["lg_d"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
-    host["out"].copy_(m.out, non_blocking=True)
-    if shape.backward:
-        host["dy_d"].copy_(host["dy"], non_blocking=True)
-        if shape.mxfp8:
-            w["bwd"](host["dy_d"], w["mw"], stream, logits=host["lg_d"])
-        else:
-            w["bwd"](host["dy_d"], inp["W_gate"], inp["W_up"], inp["W_down"], stream, logits=host["lg_d"])
-        host["dx"].copy_(w["bwd"].dx, non_blocking=True)
-
-
-def e2e_buffers(w):
+def e2e_pipeline(w, flush=None):
+    """The public HostPipeline over two slots of the workload's layer (slot 0 is the
+    layer the device-resident steps use): pinned host inputs are copied in, the
+    step runs, and its result (and for a backward workload dx) is copied back, the
+    copies of neighbouring steps overlapping compute.  flush (a device buffer) is
+    rewritten inside every step's compute when the step's weights would fit in the
+    L2.  Returns (pipeline, host inputs, host outputs, H2D bytes, D2H bytes)."""
     import torch
+    from mixture_experts_ffn_warp_gb300 import HostPipeline
     inp, shape = w["inp"], w["shape"]
-    host = {"x": inp["x"].cpu().pin_memory(), "lg": inp["logits"].cpu().pin_memory(),
-            "out": torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory(),
-            "x_d": torch.empty_like(inp["x"]), "lg_d": torch.empty_like(inp["logits"])}
-    h2d = shape.T * shape.H * 2 + shape.T * shape.E * 4
-    d2h = shape.T * shape.H * 2
-    if shape.backward:
-        host.update(dy=inp["dY"].cpu().pin_memory(), dy_d=torch.empty_like(inp["dY"]),
-                    dx=torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory())
-        h2d += shape.T * shape.H * 2
-        d2h += shape.T * shape.H * 2
-    return host, h2d, d2h
+    layers = [w["layer"], w["make_layer"]()]
+    bwds = [w["bwd"], w["make_bwd"](layers[1])] if shape.backward else None
+    names = ["x", "logits"] + (["dY"] if shape.backward else [])
+    slots = [{n: torch.empty_like(inp[n]) for n in names} for _ in layers]
+    weights = w.get("mw")
+
+    def run(bi, s):
+        if flush is not None:
+            flush.fill_(1.0)
+        d, m = slots[bi], layers[bi]
+        if shape.mxfp8:
+            m(d["x"], d["logits"], weights, s)
+        else:
+            m(d["x"], d["logits"], inp["W_gate"], inp["W_up"], inp["W_down"], s)
+        if shape.backward:
+            if shape.mxfp8:
+                bwds[bi](d["dY"], weights, s, logits=d["logits"])
+            else:
+                bwds[bi](d["dY"], inp["W_gate"], inp["W_up"], inp["W_down"], s, logits=d["logits"])
+
+    def outputs(bi):
+        return [layers[bi].out] + ([bwds[bi].dx] if shape.backward else [])
+
+    pipe = HostPipeline(slots, run, outputs)
+    host_in = {n: inp[n].cpu().pin_memory() for n in names}
+    host_out = [torch.empty(shape.T, shape.H, dtype=torch.bfloat16).pin_memory() for _ in outputs(0)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    return pipe, host_in, host_out, h2d, d2h
 
 
 # ------------------------------------------------------------------ CPU oracle
@@ -505,20 +514,25 @@ def run_gpu(args):
     step_ms = statistics.mean(a.elapsed_time(b) for a, b in steps)
     ms_step = max_over_ranks(step_ms, dev)
 
-    # end to end through the layer API with host buffers
-    host, h2d, d2h = e2e_buffers(w)
-    e2e_t = []
-    with torch.cuda.stream(stream):
-        for it in range(args.warmup + args.steps):
-            flush.fill_(2.0)
-            a, b = ev(), ev()
-            a.record(stream)
-            e2e_step(w, host, stream)
-            b.record(stream)
-            if it >= args.warmup:
-                e2e_t.append((a, b))
-        torch.cuda.synchronize(dev)
-    ms_e2e = max_over_ranks(statistics.mean(a.elapsed_time(b) for a, b in e2e_t), dev)
+    # end to end through the public pipeline API: every step copies its inputs in from
+    # pinned host memory and its result back; neighbouring steps overlap copies and compute
+    weights_bytes = shape.E * 3 * shape.H * shape.F * (1 if shape.mxfp8 else 2)
+    small = weights_bytes < 2 * L2_FLUSH_BYTES
+    pipe, host_in, host_out, h2d, d2h = e2e_pipeline(w, flush if small else None)
+    for _ in range(args.warmup):
+        pipe.submit(host_in, host_out)
+    torch.cuda.synchronize(dev)
+    barrier(dev)
+    t0, t1 = ev(), ev()
+    t0.record(pipe.up)
+    for _ in range(args.steps):
+        pipe.submit(host_in, host_out)
+    pipe.down.wait_event(pipe.ev_comp[(pipe.i - 1) % len(pipe.slots)])
+    t1.record(pipe.down)
+    torch.cuda.synchronize(dev)
+    if m.ws.read_error(stream) != 0:
+        raise RuntimeError("device error word set during the end-to-end steps")
+    ms_e2e = max_over_ranks(t0.elapsed_time(t1) / args.steps, dev)
 
     def peak_flops(g):
         return pk["bf16_tflops"] * (FP8_OVER_BF16 if g.fp8 else 1.0)
@@ -568,7 +582,12 @@ def run_gpu(args):
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": args.steps * sum(g.launches for g in groups),
-        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": ms_e2e,
+                "how": "HostPipeline (two slots; upload, compute and download streams): K steps from the first "
+                       "upload to the last download, each step's inputs copied from pinned host memory and its "
+                       "result copied back" + ("; L2 flushed inside every step" if small else
+                                               "; no flush: each step streams more than the L2 in weights")},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(shape, w["inp"], args.cpu_seconds)

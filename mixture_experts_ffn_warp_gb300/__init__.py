@@ -20,4 +20,5 @@ from ._binding import (  # noqa: F401
 from ._binding import (  # noqa: F401
     SCORE_SIGMOID, SCORE_SOFTMAX, moe_route_topk_bwd, moe_route_topk_sigmoid,
 )
-from .layer import MoeBackward, MoeBackwardMX, MoeForward, MoeForwardMX, MxWeights, moe_forward  # noqa: F401
+from .layer import (HostPipeline, MoeBackward, MoeBackwardMX, MoeForward, MoeForwardMX, MxWeights,  # noqa: F401
+                    moe_forward)

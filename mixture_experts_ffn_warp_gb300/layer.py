@@ -315,3 +315,55 @@ class MoeBackwardMX(MoeBackward):
         self.wgrad(stream)
         self.unpermute_sum(stream)
         return self.dx
+
+
+class HostPipeline:
+    """Batches that live in pinned host memory, run through per-slot layers with the
+    host <-> device copies of neighbouring batches overlapped with compute.
+
+    Three streams: uploads (host -> device inputs), compute, downloads (device ->
+    host results), ordered by CUDA events per slot.  With two slots, batch i+1's
+    inputs are copied in while batch i computes and batch i-1's results are copied
+    out; nothing synchronises with the host.  Per slot b:
+      upload    waits until compute has consumed the slot's previous inputs
+      compute   waits for its inputs and until the slot's previous results left
+      download  waits for the compute
+    slots[b]   dict: input name -> device tensor of slot b (the copy targets)
+    run(b, s)  enqueues slot b's compute on stream s
+    outputs(b) the device tensors of slot b whose values go back to the host"""
+
+    def __init__(self, slots, run, outputs, device=None):
+        dev = torch.device(device) if device is not None else torch.device("cuda", torch.cuda.current_device())
+        self.slots, self.run, self.outputs = slots, run, outputs
+        self.up, self.comp, self.down = (torch.cuda.Stream(device=dev) for _ in range(3))
+        n = len(slots)
+        self.ev_in = [torch.cuda.Event() for _ in range(n)]
+        self.ev_comp = [torch.cuda.Event() for _ in range(n)]
+        self.ev_out = [torch.cuda.Event() for _ in range(n)]
+        self.recorded = [False] * n
+        self.i = 0
+
+    def submit(self, host_inputs: dict, host_outputs: list):
+        """Enqueue one batch: host_inputs name -> pinned host tensor (copied into the
+        slot's device tensor of that name), host_outputs pinned host tensors that
+        receive outputs(b) in order.  Returns without waiting."""
+        b = self.i % len(self.slots)
+        self.i += 1
+        if self.recorded[b]:
+            self.up.wait_event(self.ev_comp[b])
+        with torch.cuda.stream(self.up):
+            for name, h in host_inputs.items():
+                self.slots[b][name].copy_(h, non_blocking=True)
+            self.ev_in[b].record(self.up)
+        self.comp.wait_event(self.ev_in[b])
+        if self.recorded[b]:
+            self.comp.wait_event(self.ev_out[b])
+        with torch.cuda.stream(self.comp):
+            self.run(b, self.comp)
+            self.ev_comp[b].record(self.comp)
+        self.down.wait_event(self.ev_comp[b])
+        with torch.cuda.stream(self.down):
+            for h, d in zip(host_outputs, self.outputs(b)):
+                h.copy_(d, non_blocking=True)
+            self.ev_out[b].record(self.down)
+        self.recorded[b] = True
