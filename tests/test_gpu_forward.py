@@ -212,3 +212,36 @@ def test_forward_parity_full_size_sampled(name):
     # the fp32 expert outputs of the sampled routes
     rows = torch.from_numpy(ref_p["dst_of_route"][toks].reshape(-1).astype(np.int64)).cuda()
     assert_close_rms(m.y_perm[rows].double().cpu().numpy(), ref["y"], what=f"{name} y_perm")
+
+
+def test_route_and_permute_at_the_largest_sizes():
+    """E = 1024 experts and k = 32 (the ABI's limits): selection, weights and maps
+    against the oracle (the route kernel's widest per-lane slice, 32 values per lane)."""
+    T, E, k, H = 300, 1024, 32, 64
+    g = torch.Generator(device="cuda").manual_seed(7)
+    logits = torch.randn(T, E, generator=g, device="cuda")
+    logits[0, :40] = 0.5                     # a tied block: lowest ids first
+    x = torch.randn(T, H, generator=g, device="cuda").to(torch.bfloat16)
+    idx, w, ref_idx, _ = _route_and_check({"logits": logits}, k)
+    ws = Workspace(T, E, k)
+    p = moe_permute(x, idx, E, ws)
+    torch.cuda.synchronize()
+    assert ws.read_error() == 0
+    _check_perm(p, oracle.permute(ref_idx, E), T * k)
+    src = p.src_of_row[: T * k].long()
+    assert torch.equal(p.x_perm[: T * k], x[src // k])
+
+
+def test_every_token_to_every_expert():
+    """k = E: each expert receives every token; the forward against the oracle."""
+    shape = small_shape("kE", T=200, H=128, F=256, E=4, k=4)
+    inp = gpu_inputs(shape, with_dy=False)
+    m = MoeForward(shape.T, shape.H, shape.F, shape.E, shape.k)
+    out = m(inp["x"], inp["logits"], inp["W_gate"], inp["W_up"], inp["W_down"])
+    torch.cuda.synchronize()
+    assert m.ws.read_error() == 0
+    assert m.perm.group_sizes.cpu().tolist() == [shape.T] * shape.E
+    idx, w = m.topk_idx.cpu().numpy(), m.topk_w.cpu().numpy()
+    hb = {n: bits(inp[n]) for n in ("x", "W_gate", "W_up", "W_down")}
+    ref = oracle.moe_fwd(hb["x"], hb["W_gate"], hb["W_up"], hb["W_down"], idx, w, round_mode=2)
+    assert_close_rms(to_f64(out), ref["out"], what="k = E out", bf16_out=True)
