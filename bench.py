@@ -567,7 +567,7 @@ def run_gpu(args):
         "metric": METRIC, "value": tokens / (ms_step / 1e3), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8" if shape.mxfp8 else "bf16",
-        "data": "synthetic (seeded; BASELINE shapes and distributions)",
+        "data": "synthetic (seeded; the workload's stated shapes and distributions)",
         "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k,
                    "router": shape.router, "weight_at": shape.weight_at,
                    "pass": "forward+backward" if shape.backward else "forward",
