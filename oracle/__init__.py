@@ -61,6 +61,8 @@ def lib():
         L.oracle_moe_fwd_w.restype = None
         L.oracle_moe_fwd_w.argtypes = [_i64, _i64p, _int, _int, _int, _int, _u16p, pp16, pp16, pp16,
                                        _i32p, _f32p, _int, _int, _int, _f64p, _f64p, _f64p, _f64p]
+        L.oracle_set_swiglu_clamp.restype = None
+        L.oracle_set_swiglu_clamp.argtypes = [C.c_double] * 4
         L.oracle_mx_fake_quant.restype = None
         L.oracle_mx_fake_quant.argtypes = [_f64p, _i64, _i64, _f64p]
         L.oracle_moe_fwd.restype = None
@@ -489,3 +491,20 @@ def mx_fake_quant(v: np.ndarray) -> np.ndarray:
     out = np.empty_like(a)
     lib().oracle_mx_fake_quant(_p(a, _f64p), n, K, _p(out, _f64p))
     return out
+
+
+class swiglu_clamp:
+    """Context manager: the oracle's SwiGLU inputs clamped, g to [gate_lo, gate_hi] and u
+    to [up_lo, up_hi], inclusive bounds (moe_oracle.c, oracle_set_swiglu_clamp); the
+    clamp is off again on exit."""
+
+    def __init__(self, gate_lo=-np.inf, gate_hi=np.inf, up_lo=-np.inf, up_hi=np.inf):
+        self.bounds = (float(gate_lo), float(gate_hi), float(up_lo), float(up_hi))
+
+    def __enter__(self):
+        lib().oracle_set_swiglu_clamp(*self.bounds)
+        return self
+
+    def __exit__(self, *exc):
+        lib().oracle_set_swiglu_clamp(-np.inf, np.inf, -np.inf, np.inf)
+        return False

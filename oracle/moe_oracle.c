@@ -448,6 +448,28 @@ void oracle_unpermute_combine_mxfp8(const float *y_perm, const int32_t *dst_of_r
 static double silu(double g) { return g / (1.0 + exp(-g)); }
 static double sigmoid(double g) { return 1.0 / (1.0 + exp(-g)); }
 
+/* Optional clamp of the SwiGLU inputs ("Add MoE + expert-parallel Python API surface,
+ * PyTorch reference, and tests", Summary: local SwiGLU experts with an optional
+ * DeepSeek-style clamp; inclusive clamp bounds).  The pages give no form and no
+ * values; reading: the gate and up accumulators are clamped to caller-given
+ * intervals before SwiGLU, h = silu(clamp(g, gate_lo, gate_hi)) * clamp(u, up_lo,
+ * up_hi), and "inclusive" means a value equal to a bound is inside: its derivative
+ * passes, a value outside gets derivative 0.  +-inf bounds (the default) disable it.
+ * Set for the whole library (before any parallel region runs). */
+static double g_gate_lo = -INFINITY, g_gate_hi = INFINITY, g_up_lo = -INFINITY, g_up_hi = INFINITY;
+
+void oracle_set_swiglu_clamp(double gate_lo, double gate_hi, double up_lo, double up_hi)
+{
+    g_gate_lo = gate_lo; g_gate_hi = gate_hi; g_up_lo = up_lo; g_up_hi = up_hi;
+}
+
+static double clamp_to(double v, double lo, double hi) { return v < lo ? lo : (v > hi ? hi : v); }
+static double inside(double v, double lo, double hi) { return (v >= lo && v <= hi) ? 1.0 : 0.0; }
+static double swiglu(double g, double u)
+{
+    return silu(clamp_to(g, g_gate_lo, g_gate_hi)) * clamp_to(u, g_up_lo, g_up_hi);
+}
+
 /* g = x Wg, u = x Wu (double), h = silu(g) * u (bf16 in round_mode 1),
  * y = h Wd (kept unrounded: the path stores y in fp32).  Wg, Wu are [H,F];
  * Wd is [F,H]. */
@@ -469,10 +491,10 @@ static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t 
         }
     }
     if (h_mx) {
-        for (int f = 0; f < F; ++f) h[f] = hw * (silu(g[f]) * u[f]);
+        for (int f = 0; f < F; ++f) h[f] = hw * swiglu(g[f], u[f]);
         mx_fake_quant(h, F, h);
     } else {
-        for (int f = 0; f < F; ++f) h[f] = rnd(hw * (silu(g[f]) * u[f]), round_mode);
+        for (int f = 0; f < F; ++f) h[f] = rnd(hw * swiglu(g[f], u[f]), round_mode);
     }
     for (int n = 0; n < H; ++n) y[n] = 0.0;
     for (int f = 0; f < F; ++f) {
@@ -585,7 +607,7 @@ void oracle_moe_fwd_mxfp8(int64_t n_tokens, const int64_t *tokens, int H, int F,
                 }
                 g[f] = sg;
                 u[f] = su;
-                h[f] = silu(sg) * su;
+                h[f] = swiglu(sg, su);
             }
             mx_fake_quant(h, F, h);
             for (int n = 0; n < H; ++n) {
@@ -627,9 +649,10 @@ static void route_bwd(const uint16_t *dYt, double w, const double *g, const doub
         double dh = 0.0;
         for (int n = 0; n < H; ++n) dh += dy[n] * oracle_bf16_to_double(wd[n]);
         double G = rnd(g[f], round_mode), U = rnd(u[f], round_mode);
-        double s = sigmoid(G);
-        dg[f] = rnd(dh * U * s * (1.0 + G * (1.0 - s)), round_mode);
-        du[f] = rnd(dh * G * s, round_mode);
+        double Gc = clamp_to(G, g_gate_lo, g_gate_hi), Uc = clamp_to(U, g_up_lo, g_up_hi);
+        double s = sigmoid(Gc);
+        dg[f] = rnd(inside(G, g_gate_lo, g_gate_hi) * dh * Uc * s * (1.0 + Gc * (1.0 - s)), round_mode);
+        du[f] = rnd(inside(U, g_up_lo, g_up_hi) * dh * Gc * s, round_mode);
     }
     if (!dxr) return;
     for (int i = 0; i < H; ++i) {
@@ -756,7 +779,7 @@ void oracle_moe_bwd_dw_entries(int64_t n_entries, const int32_t *which, const in
             }
             double w = (double)topk_w[r];
             if (wsel == 2) {
-                double h = rnd(silu(g) * u, round_mode);
+                double h = rnd(swiglu(g, u), round_mode);
                 if (h_mx) {   /* MXFP8 h: the whole 32-wide block of f along F */
                     double hb[32];
                     const int f0 = f / 32 * 32;
@@ -767,7 +790,7 @@ void oracle_moe_bwd_dw_entries(int64_t n_entries, const int32_t *which, const in
                             gc += xv * oracle_bf16_to_double(Wg[e][(int64_t)i * F + f0 + c]);
                             uc += xv * oracle_bf16_to_double(Wu[e][(int64_t)i * F + f0 + c]);
                         }
-                        hb[c] = silu(gc) * uc;
+                        hb[c] = swiglu(gc, uc);
                     }
                     mx_fake_quant(hb, 32, hb);
                     h = hb[f - f0];
@@ -779,9 +802,12 @@ void oracle_moe_bwd_dw_entries(int64_t n_entries, const int32_t *which, const in
                 const uint16_t *wd = Wd[e] + (int64_t)f * H;
                 for (int n = 0; n < H; ++n)
                     dh += rnd(w * oracle_bf16_to_double(dY[t * H + n]), round_mode) * oracle_bf16_to_double(wd[n]);
-                double G = rnd(g, round_mode), U = rnd(u, round_mode), s = sigmoid(G);
-                double d = (wsel == 0) ? rnd(dh * U * s * (1.0 + G * (1.0 - s)), round_mode)
-                                       : rnd(dh * G * s, round_mode);
+                double G = rnd(g, round_mode), U = rnd(u, round_mode);
+                double Gc = clamp_to(G, g_gate_lo, g_gate_hi), Uc = clamp_to(U, g_up_lo, g_up_hi);
+                double s = sigmoid(Gc);
+                double d = (wsel == 0)
+                               ? rnd(inside(G, g_gate_lo, g_gate_hi) * dh * Uc * s * (1.0 + Gc * (1.0 - s)), round_mode)
+                               : rnd(inside(U, g_up_lo, g_up_hi) * dh * Gc * s, round_mode);
                 acc += oracle_bf16_to_double(xr[hn]) * d;
             }
         }
