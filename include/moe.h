@@ -301,6 +301,24 @@ MOE_API moe_status_t moe_grouped_fc2_weighted(const moe_bf16_t *h, const moe_bf1
                                               const float *topk_w, int E, int H, int F, int64_t rows_cap,
                                               float *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Optional clamp of the SwiGLU inputs ("Add MoE + expert-parallel Python API surface,
+ * PyTorch reference, and tests", Summary: local SwiGLU experts with an optional
+ * DeepSeek-style clamp, inclusive clamp bounds; the pages give no values, so the
+ * bounds are the caller's): the fp32 accumulators are clamped before SwiGLU,
+ *   h = bf16(silu(clamp(g, gate_lo, gate_hi)) * clamp(u, up_lo, up_hi))   (times the
+ *   route weight when src_of_row / topk_w are given, as moe_grouped_fc1_swiglu_weighted)
+ * fc1_c (nullable) stashes the unclamped g | u.  The backward of a clamped forward uses
+ * moe_grouped_dgrad_fc2_dswiglu_clamped with the same bounds: the dSwiGLU is taken at
+ * the clamped values, and an input outside its interval gets derivative 0 (a value equal
+ * to a bound is inside).  Infinite ends disable a side.  Errors: MOE_ERR_INVALID_ARG for
+ * an empty interval or a NaN bound, else as the unclamped calls. */
+MOE_API moe_status_t moe_grouped_fc1_swiglu_clamped(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                                    const moe_bf16_t *W_up, const int32_t *group_offsets,
+                                                    const int32_t *src_of_row, const float *topk_w, int E, int H,
+                                                    int F, int64_t rows_cap, float gate_lo, float gate_hi,
+                                                    float up_lo, float up_hi, moe_bf16_t *h, moe_bf16_t *fc1_c,
+                                                    void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* A5  Weighted unpermute / combine                                     */
 /* ------------------------------------------------------------------ */
@@ -472,6 +490,11 @@ MOE_API moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm, co
                                                    const moe_bf16_t *fc1_c, const int32_t *group_offsets,
                                                    int E, int H, int F, int64_t rows_cap, moe_bf16_t *dgu,
                                                    void *ws, size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_dgrad_fc2_dswiglu_clamped(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down,
+                                                           const moe_bf16_t *fc1_c, const int32_t *group_offsets,
+                                                           int E, int H, int F, int64_t rows_cap, float gate_lo,
+                                                           float gate_hi, float up_lo, float up_hi, moe_bf16_t *dgu,
+                                                           void *ws, size_t ws_bytes, moe_stream_t stream);
 MOE_API moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_bf16_t *W_gate,
                                            const moe_bf16_t *W_up, const int32_t *group_offsets, int E,
                                            int H, int F, int64_t rows_cap, float *dx_perm, void *ws,

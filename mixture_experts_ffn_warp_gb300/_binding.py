@@ -52,6 +52,10 @@ SIGNATURES = {
     "moe_grouped_ffn_bwd": (_st, [_vp] * 12 + [_i64, _int, _int, _int, _int, _i64] + [_vp] * 8 + [_vp, _sz, _vp]),
     "moe_combine_bwd": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _i64, _vp, _vp, _vp]),
     "moe_grouped_dgrad_fc2_dswiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
+    "moe_grouped_dgrad_fc2_dswiglu_clamped": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64] + [C.c_float] * 4
+                                              + [_vp, _vp, _sz, _vp]),
+    "moe_grouped_fc1_swiglu_clamped": (_st, [_vp] * 6 + [_int, _int, _int, _i64] + [C.c_float] * 4
+                                       + [_vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_dgrad_fc1": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_grouped_wgrad": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_unpermute_sum": (_st, [_vp, _vp, _i64, _int, _int, _vp, _vp]),
@@ -289,12 +293,18 @@ def moe_grouped_ffn_fwd(x_perm: torch.Tensor, W_gate: torch.Tensor, W_up: torch.
 
 
 def moe_grouped_fc1_swiglu(x_perm, W_gate, W_up, group_offsets, ws: Workspace, h, fc1_c=None, stream=None,
-                           route_weights=None):
+                           route_weights=None, clamp=None):
     """A3 alone: h = silu(x W_gate) * (x W_up) per group (moe.h).  route_weights =
-    (src_of_row, topk_w): h of each row scaled by its route's router weight."""
+    (src_of_row, topk_w): h of each row scaled by its route's router weight.  clamp =
+    (gate_lo, gate_hi, up_lo, up_hi): the SwiGLU inputs clamped to those inclusive bounds."""
     rows_cap, H = x_perm.shape
     E, _, F = W_gate.shape
-    if route_weights is None:
+    if clamp is not None:
+        src, tw = route_weights if route_weights is not None else (None, None)
+        _check("moe_grouped_fc1_swiglu_clamped", load_library().moe_grouped_fc1_swiglu_clamped(
+            _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(group_offsets), _ptr(src), _ptr(tw), E, H, F, rows_cap,
+            *[float(v) for v in clamp], _ptr(h), _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+    elif route_weights is None:
         _check("moe_grouped_fc1_swiglu", load_library().moe_grouped_fc1_swiglu(
             _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(group_offsets), E, H, F, rows_cap, _ptr(h),
             _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))
@@ -356,10 +366,16 @@ def moe_combine_bwd(dY, y_perm, perm: "Permutation", topk_w, dy_perm, d_topk_w=N
         _ptr(perm.group_offsets), T, H, E, k, perm.rows_cap, _ptr(dy_perm), _ptr(d_topk_w), _stream(stream)))
 
 
-def moe_grouped_dgrad_fc2_dswiglu(dy_perm, W_down, fc1_c, group_offsets, ws: Workspace, dgu, stream=None):
-    """dgu = dSwiGLU(dy_perm W_down^T) from the fc1_c stash (moe.h)."""
+def moe_grouped_dgrad_fc2_dswiglu(dy_perm, W_down, fc1_c, group_offsets, ws: Workspace, dgu, stream=None, clamp=None):
+    """dgu = dSwiGLU(dy_perm W_down^T) from the fc1_c stash (moe.h); clamp: the forward's
+    SwiGLU input bounds (gate_lo, gate_hi, up_lo, up_hi)."""
     rows_cap, H = dy_perm.shape
     E, F, _ = W_down.shape
+    if clamp is not None:
+        _check("moe_grouped_dgrad_fc2_dswiglu_clamped", load_library().moe_grouped_dgrad_fc2_dswiglu_clamped(
+            _ptr(dy_perm), _ptr(W_down), _ptr(fc1_c), _ptr(group_offsets), E, H, F, rows_cap,
+            *[float(v) for v in clamp], _ptr(dgu), _ptr(ws.buf), ws.nbytes, _stream(stream)))
+        return
     _check("moe_grouped_dgrad_fc2_dswiglu", load_library().moe_grouped_dgrad_fc2_dswiglu(
         _ptr(dy_perm), _ptr(W_down), _ptr(fc1_c), _ptr(group_offsets), E, H, F, rows_cap, _ptr(dgu),
         _ptr(ws.buf), ws.nbytes, _stream(stream)))

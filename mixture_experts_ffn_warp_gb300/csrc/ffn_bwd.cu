@@ -140,10 +140,12 @@ extern "C" moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const float *y_per
     return launch_status();
 }
 
-extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down,
-                                                      const moe_bf16_t *fc1_c, const int32_t *group_offsets,
-                                                      int E, int H, int F, int64_t rows_cap, moe_bf16_t *dgu,
-                                                      void *ws, size_t ws_bytes, moe_stream_t stream) {
+namespace {
+
+// clamp (nullable): gate_lo, gate_hi, up_lo, up_hi of the forward's SwiGLU input clamp
+moe_status_t dgrad_fc2_impl(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down, const moe_bf16_t *fc1_c,
+                            const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap, moe_bf16_t *dgu,
+                            void *ws, size_t ws_bytes, moe_stream_t stream, const float *clamp) {
     moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!dy_perm || !W_down || !fc1_c || !group_offsets || !dgu) return MOE_ERR_INVALID_ARG;
@@ -164,10 +166,38 @@ extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm,
     a.ld0 = 2 * (int64_t)F;
     a.aux = reinterpret_cast<const __nv_bfloat16 *>(fc1_c);
     a.ld_aux = 2 * (int64_t)F;
+    if (clamp) {
+        a.clamp = 1;
+        a.gate_lo = clamp[0];
+        a.gate_hi = clamp[1];
+        a.up_lo = clamp[2];
+        a.up_hi = clamp[3];
+    }
     a.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
     if (bn == 256) return gg::launch<Op::DGRAD_DSWIGLU, 256>(tA, tB, tB, tC, tC, a, bound, (cudaStream_t)stream);
     return gg::launch<Op::DGRAD_DSWIGLU, 128>(tA, tB, tB, tC, tC, a, bound, (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down,
+                                                      const moe_bf16_t *fc1_c, const int32_t *group_offsets,
+                                                      int E, int H, int F, int64_t rows_cap, moe_bf16_t *dgu,
+                                                      void *ws, size_t ws_bytes, moe_stream_t stream) {
+    return dgrad_fc2_impl(dy_perm, W_down, fc1_c, group_offsets, E, H, F, rows_cap, dgu, ws, ws_bytes, stream,
+                          nullptr);
+}
+
+extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu_clamped(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down,
+                                                              const moe_bf16_t *fc1_c, const int32_t *group_offsets,
+                                                              int E, int H, int F, int64_t rows_cap, float gate_lo,
+                                                              float gate_hi, float up_lo, float up_hi,
+                                                              moe_bf16_t *dgu, void *ws, size_t ws_bytes,
+                                                              moe_stream_t stream) {
+    if (!(gate_lo <= gate_hi && up_lo <= up_hi)) return MOE_ERR_INVALID_ARG;   // also rejects NaN
+    const float c[4] = {gate_lo, gate_hi, up_lo, up_hi};
+    return dgrad_fc2_impl(dy_perm, W_down, fc1_c, group_offsets, E, H, F, rows_cap, dgu, ws, ws_bytes, stream, c);
 }
 
 extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_bf16_t *W_gate,

@@ -18,10 +18,11 @@ int64_t mblock_bound(int64_t rows_cap, int E) { return (rows_cap + gg::BM - 1) /
 
 // FC1 + SwiGLU and FC2; topk_w / src_of_row non-null: the router weight of each row's
 // route is applied in the epilogue (to h, or to y).
+// clamp (nullable): gate_lo, gate_hi, up_lo, up_hi of the SwiGLU input clamp
 moe_status_t fc1_impl(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
                       const int32_t *group_offsets, const int32_t *src_of_row, const float *topk_w, int E, int H,
                       int F, int64_t rows_cap, moe_bf16_t *h, moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
-                      moe_stream_t stream) {
+                      moe_stream_t stream, const float *clamp = nullptr) {
     moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!x_perm || !W_gate || !W_up || !group_offsets || !h) return MOE_ERR_INVALID_ARG;
@@ -47,6 +48,13 @@ moe_status_t fc1_impl(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const 
     a.ld1 = 2 * (int64_t)F;
     a.route_w = topk_w;
     a.src_of_row = src_of_row;
+    if (clamp) {
+        a.clamp = 1;
+        a.gate_lo = clamp[0];
+        a.gate_hi = clamp[1];
+        a.up_lo = clamp[2];
+        a.up_hi = clamp[3];
+    }
     a.err = ws_error_word(ws);
     return gg::launch<Op::FC1_SWIGLU, 256>(tA, tB0, tB1, tC0, tC1, a, mblock_bound(rows_cap, E) * a.n_tiles,
                                            (cudaStream_t)stream);
@@ -79,6 +87,11 @@ moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32
     const int64_t bound = mblock_bound(rows_cap, E) * b.n_tiles;
     if (bn == 256) return gg::launch<Op::FC2, 256>(tA, tB, tB, tC, tC, b, bound, (cudaStream_t)stream);
     return gg::launch<Op::FC2, 128>(tA, tB, tB, tC, tC, b, bound, (cudaStream_t)stream);
+}
+
+// Bounds of the SwiGLU clamp: each interval non-empty, no NaN (infinite ends allowed).
+bool clamp_bounds_ok(float gate_lo, float gate_hi, float up_lo, float up_hi) {
+    return gate_lo <= gate_hi && up_lo <= up_hi;   // false for any NaN
 }
 
 }  // namespace
@@ -131,4 +144,17 @@ extern "C" moe_status_t moe_grouped_ffn_fwd(const moe_bf16_t *x_perm, const moe_
                                 ws_bytes, stream);
     if (st != MOE_OK) return st;
     return moe_grouped_fc2(h, W_down, group_offsets, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
+}
+
+extern "C" moe_status_t moe_grouped_fc1_swiglu_clamped(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                                                       const moe_bf16_t *W_up, const int32_t *group_offsets,
+                                                       const int32_t *src_of_row, const float *topk_w, int E, int H,
+                                                       int F, int64_t rows_cap, float gate_lo, float gate_hi,
+                                                       float up_lo, float up_hi, moe_bf16_t *h, moe_bf16_t *fc1_c,
+                                                       void *ws, size_t ws_bytes, moe_stream_t stream) {
+    if (!clamp_bounds_ok(gate_lo, gate_hi, up_lo, up_hi)) return MOE_ERR_INVALID_ARG;
+    if (rows_cap > 0 && (src_of_row == nullptr) != (topk_w == nullptr)) return MOE_ERR_INVALID_ARG;
+    const float c[4] = {gate_lo, gate_hi, up_lo, up_hi};
+    return fc1_impl(x_perm, W_gate, W_up, group_offsets, src_of_row, topk_w, E, H, F, rows_cap, h, fc1_c, ws,
+                    ws_bytes, stream, c);
 }

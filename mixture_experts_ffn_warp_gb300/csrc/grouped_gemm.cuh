@@ -88,6 +88,10 @@ struct Args {
     // (h or y scaled by route_w[src_of_row[row]]; padding rows get 0); null = unweighted
     const float *route_w;
     const int32_t *src_of_row;
+    // FC1_SWIGLU / DGRAD_DSWIGLU: optional clamp of the SwiGLU inputs (clamp != 0): g to
+    // [gate_lo, gate_hi] and u to [up_lo, up_hi] before SwiGLU, inclusive bounds
+    int clamp;
+    float gate_lo, gate_hi, up_lo, up_hi;
     uint32_t *err;
 };
 
@@ -565,8 +569,18 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const int n = tl.n0 + c;
                     if (n < args.N && (whole || valid)) {
                         float hv[32];
+                        if (args.clamp) {
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) hv[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]) * rw;
+                            for (int i = 0; i < 32; ++i) {
+                                const float gc = fminf(fmaxf(__uint_as_float(g[i]), args.gate_lo), args.gate_hi);
+                                const float uc = fminf(fmaxf(__uint_as_float(u[i]), args.up_lo), args.up_hi);
+                                hv[i] = silu_f(gc) * uc * rw;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i)
+                                hv[i] = silu_f(__uint_as_float(g[i])) * __uint_as_float(u[i]) * rw;
+                        }
                         if constexpr (OP == Op::FC1_MX) {
                             // h quantised along F: this thread's 32 columns are one MX block; two
                             // blocks (64 bytes of codes) fill a staging row
@@ -631,12 +645,27 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         float gv[32], uv[32], dg[32], du[32];
                         load_bf16x32(args.aux + row * args.ld_aux + n, gv);
                         load_bf16x32(args.aux + row * args.ld_aux + args.N + n, uv);
+                        if (args.clamp) {   // clamped inputs; zero derivative outside the bounds
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float dh = __uint_as_float(d[i]);
-                            const float s = sigmoid_fast(gv[i]);
-                            dg[i] = dh * uv[i] * s * (1.0f + gv[i] * (1.0f - s));
-                            du[i] = dh * gv[i] * s;
+                            for (int i = 0; i < 32; ++i) {
+                                const float dh = __uint_as_float(d[i]);
+                                const float G = gv[i], U = uv[i];
+                                const float gc = fminf(fmaxf(G, args.gate_lo), args.gate_hi);
+                                const float uc = fminf(fmaxf(U, args.up_lo), args.up_hi);
+                                const float s = sigmoid_fast(gc);
+                                const bool gin = G >= args.gate_lo && G <= args.gate_hi;
+                                const bool uin = U >= args.up_lo && U <= args.up_hi;
+                                dg[i] = gin ? dh * uc * s * (1.0f + gc * (1.0f - s)) : 0.0f;
+                                du[i] = uin ? dh * gc * s : 0.0f;
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) {
+                                const float dh = __uint_as_float(d[i]);
+                                const float s = sigmoid_fast(gv[i]);
+                                dg[i] = dh * uv[i] * s * (1.0f + gv[i] * (1.0f - s));
+                                du[i] = dh * gv[i] * s;
+                            }
                         }
                         if (whole) {
                             stage_bf16x32(dg, &tmC0, n, wrow0);

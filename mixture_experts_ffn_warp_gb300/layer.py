@@ -30,16 +30,22 @@ class MoeForward:
     (h scaled before its bf16 rounding) or "fc2" (y scaled); the early placements
     are forward only.
     out_format: "bf16" (out [T, H]) or "mxfp8" (out_q E4M3 [T, H] + out_sf UE8M0
-    [T, H/32], the block-scaled output of the same fp32 combine sum)."""
+    [T, H/32], the block-scaled output of the same fp32 combine sum).
+    swiglu_clamp: None or (gate_lo, gate_hi, up_lo, up_hi): the SwiGLU inputs clamped to
+    those inclusive bounds (the optional DeepSeek-style clamp; a MoeBackward of this layer
+    uses the same bounds)."""
 
     def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", align: int = 1,
                  keep_fc1_c: bool = False, router: str = "softmax", expert_bias=None, normalize: bool = True,
-                 weight_at: str = "combine", out_format: str = "bf16"):
+                 weight_at: str = "combine", out_format: str = "bf16", swiglu_clamp=None):
         if router not in ("softmax", "sigmoid"):
             raise ValueError("router must be 'softmax' or 'sigmoid'")
         if weight_at not in ("combine", "fc1", "fc2"):
             raise ValueError("weight_at must be 'combine', 'fc1' or 'fc2'")
         self.weight_at = weight_at
+        self.swiglu_clamp = None if swiglu_clamp is None else tuple(float(v) for v in swiglu_clamp)
+        if self.swiglu_clamp is not None and len(self.swiglu_clamp) != 4:
+            raise ValueError("swiglu_clamp is (gate_lo, gate_hi, up_lo, up_hi)")
         self.T, self.H, self.F, self.E, self.k, self.align = T, H, F, E, k, align
         self.router, self.expert_bias, self.normalize = router, expert_bias, normalize
         dev = torch.device(device)
@@ -77,7 +83,8 @@ class MoeForward:
 
     def fc1(self, W_gate, W_up, stream=None):
         moe_grouped_fc1_swiglu(self.perm.x_perm, W_gate, W_up, self.perm.group_offsets, self.ws, self.h,
-                               self.fc1_c, stream=stream, route_weights=self._route_weights("fc1"))
+                               self.fc1_c, stream=stream, route_weights=self._route_weights("fc1"),
+                               clamp=self.swiglu_clamp)
 
     def fc2(self, W_down, stream=None):
         moe_grouped_fc2(self.h, W_down, self.perm.group_offsets, self.ws, self.y_perm, stream=stream,
@@ -163,7 +170,7 @@ class MoeBackward:
     def dgrad_fc2(self, W_down, stream=None):
         f = self.fwd
         moe_grouped_dgrad_fc2_dswiglu(self.dy_perm, W_down, f.fc1_c, f.perm.group_offsets, f.ws, self.dgu,
-                                      stream=stream)
+                                      stream=stream, clamp=getattr(f, "swiglu_clamp", None))
 
     def dgrad_fc1(self, W_gate, W_up, stream=None):
         f = self.fwd

@@ -74,6 +74,16 @@ def test_host_validation_before_launch(lib):
     # weighted FC1 / FC2: route maps required
     assert lib.moe_grouped_fc1_swiglu_weighted(fk, fk, fk, fk, nul, nul, 4, 128, 128, 8, fk, nul, fk, 4096, nul) == 1
     assert lib.moe_grouped_fc2_weighted(fk, fk, fk, fk, nul, 4, 128, 128, 8, fk, fk, 4096, nul) == 1
+    # SwiGLU clamp: empty interval or NaN bound rejected before anything else
+    inf, nan = float("inf"), float("nan")
+    assert lib.moe_grouped_fc1_swiglu_clamped(fk, fk, fk, fk, nul, nul, 4, 128, 128, 8, 1.0, 0.5, -inf, inf, fk, nul,
+                                              fk, 4096, nul) == 1
+    assert lib.moe_grouped_fc1_swiglu_clamped(fk, fk, fk, fk, nul, nul, 4, 128, 128, 8, -inf, inf, nan, 1.0, fk, nul,
+                                              fk, 4096, nul) == 1
+    assert lib.moe_grouped_fc1_swiglu_clamped(fk, fk, fk, fk, fk, nul, 4, 128, 128, 8, -1.0, 1.0, -1.0, 1.0, fk, nul,
+                                              fk, 4096, nul) == 1                 # half of the route maps
+    assert lib.moe_grouped_dgrad_fc2_dswiglu_clamped(fk, fk, fk, fk, 4, 128, 128, 8, 0.0, -1.0, -1.0, 1.0, fk, fk,
+                                                     4096, nul) == 1
     # permute: H % 8, capacity, workspace
     assert lib.moe_permute(nul, nul, 4, 12, 4, 2, 1, nul, 8, nul, nul, nul, nul, nul, 0, nul) == 2
     assert lib.moe_permute(nul, nul, 4, 16, 4, 2, 1, nul, 7, nul, nul, nul, nul, nul, 0, nul) == 1
