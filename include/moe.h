@@ -434,6 +434,14 @@ MOE_API moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const uint
                                                   int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf,
                                                   moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
                                                   moe_stream_t stream);
+/* moe_grouped_fc1_swiglu_mxfp8 with the SwiGLU inputs clamped (bounds and errors as
+ * moe_grouped_fc1_swiglu_clamped); the straight-through backward then uses
+ * moe_grouped_dgrad_fc2_dswiglu_clamped with the same bounds. */
+MOE_API moe_status_t moe_grouped_fc1_swiglu_mxfp8_clamped(
+    const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q, const uint8_t *Wg_sf, const uint8_t *Wu_q,
+    const uint8_t *Wu_sf, const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap, float gate_lo,
+    float gate_hi, float up_lo, float up_hi, uint8_t *h_q, uint8_t *h_sf, moe_bf16_t *fc1_c, void *ws,
+    size_t ws_bytes, moe_stream_t stream);
 MOE_API moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
                                            const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H, int F,
                                            int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,

@@ -67,6 +67,8 @@ SIGNATURES = {
     "moe_grouped_ffn_fwd_mxfp8": (_st, [_vp] * 9 + [_int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_fc1_swiglu_mxfp8": (_st, [_vp] * 7 + [_int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_dequantize_rows_mxfp8": (_st, [_vp, _vp, _vp, _int, _i64, _int, _vp, _vp, _sz, _vp]),
+    "moe_grouped_fc1_swiglu_mxfp8_clamped": (_st, [_vp] * 7 + [_int, _int, _int, _i64] + [C.c_float] * 4
+                                             + [_vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_unpermute_combine_mxfp8": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp, _vp]),
     "moe_dequantize_weights_mxfp8": (_st, [_vp, _vp, _int, _int, _int, _vp, _vp]),
     "moe_grouped_fc2_mxfp8": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
@@ -517,14 +519,21 @@ def moe_permute_mxfp8(x: torch.Tensor, topk_idx: torch.Tensor, E: int, ws: Works
 
 
 def moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, ws: Workspace, h_q, h_sf,
-                                 fc1_c=None, stream=None):
+                                 fc1_c=None, stream=None, clamp=None):
     """A3 on MXFP8 operands; h quantised to MXFP8 along F (moe.h).  fc1_c (bf16
-    [rows_cap, 2F], optional): the g | u stash for the backward."""
+    [rows_cap, 2F], optional): the g | u stash for the backward.  clamp = (gate_lo,
+    gate_hi, up_lo, up_hi): the SwiGLU inputs clamped to those inclusive bounds."""
     rows_cap, H = x_q.shape
     E = group_offsets.shape[0] - 1
     F = h_q.shape[1]
     if fc1_c is not None:
         _need(fc1_c, "fc1_c", torch.bfloat16, (rows_cap, 2 * F))
+    if clamp is not None:
+        _check("moe_grouped_fc1_swiglu_mxfp8_clamped", load_library().moe_grouped_fc1_swiglu_mxfp8_clamped(
+            _ptr(x_q), _ptr(x_sf), _ptr(Wg_q), _ptr(Wg_sf), _ptr(Wu_q), _ptr(Wu_sf), _ptr(group_offsets), E, H, F,
+            rows_cap, *[float(v) for v in clamp], _ptr(h_q), _ptr(h_sf), _ptr(fc1_c), _ptr(ws.buf), ws.nbytes,
+            _stream(stream)))
+        return
     _check("moe_grouped_fc1_swiglu_mxfp8", load_library().moe_grouped_fc1_swiglu_mxfp8(
         _ptr(x_q), _ptr(x_sf), _ptr(Wg_q), _ptr(Wg_sf), _ptr(Wu_q), _ptr(Wu_sf), _ptr(group_offsets), E, H, F,
         rows_cap, _ptr(h_q), _ptr(h_sf), _ptr(fc1_c), _ptr(ws.buf), ws.nbytes, _stream(stream)))

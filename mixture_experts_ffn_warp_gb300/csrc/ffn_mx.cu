@@ -23,12 +23,13 @@ bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0;
 
 }  // namespace
 
-extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,
-                                                     const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,
-                                                     const int32_t *group_offsets, int E, int H, int F,
-                                                     int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf,
-                                                     moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
-                                                     moe_stream_t stream) {
+namespace {
+
+// clamp (nullable): gate_lo, gate_hi, up_lo, up_hi of the SwiGLU input clamp
+moe_status_t fc1_mx_impl(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q, const uint8_t *Wg_sf,
+                         const uint8_t *Wu_q, const uint8_t *Wu_sf, const int32_t *group_offsets, int E, int H,
+                         int F, int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf, moe_bf16_t *fc1_c, void *ws,
+                         size_t ws_bytes, moe_stream_t stream, const float *clamp) {
     moe_status_t st = check_mx(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!x_q || !x_sf || !Wg_q || !Wg_sf || !Wu_q || !Wu_sf || !group_offsets || !h_q || !h_sf)
@@ -56,9 +57,39 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const u
     a.out_sf = h_sf;
     a.out1 = reinterpret_cast<__nv_bfloat16 *>(fc1_c);   // nullable: the g | u stash
     a.ld1 = 2 * (int64_t)F;
+    if (clamp) {
+        a.clamp = 1;
+        a.gate_lo = clamp[0];
+        a.gate_hi = clamp[1];
+        a.up_lo = clamp[2];
+        a.up_hi = clamp[3];
+    }
     a.err = ws_error_word(ws);
     return gg::launch<Op::FC1_MX, 256>(tA, tA, tA, tC, tC, a, mblock_bound(rows_cap, E) * a.n_tiles,
                                        (cudaStream_t)stream);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,
+                                                     const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,
+                                                     const int32_t *group_offsets, int E, int H, int F,
+                                                     int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf,
+                                                     moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
+                                                     moe_stream_t stream) {
+    return fc1_mx_impl(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, E, H, F, rows_cap, h_q, h_sf, fc1_c, ws,
+                       ws_bytes, stream, nullptr);
+}
+
+extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8_clamped(
+    const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q, const uint8_t *Wg_sf, const uint8_t *Wu_q,
+    const uint8_t *Wu_sf, const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap, float gate_lo,
+    float gate_hi, float up_lo, float up_hi, uint8_t *h_q, uint8_t *h_sf, moe_bf16_t *fc1_c, void *ws,
+    size_t ws_bytes, moe_stream_t stream) {
+    if (!(gate_lo <= gate_hi && up_lo <= up_hi)) return MOE_ERR_INVALID_ARG;   // also rejects NaN
+    const float c[4] = {gate_lo, gate_hi, up_lo, up_hi};
+    return fc1_mx_impl(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, E, H, F, rows_cap, h_q, h_sf, fc1_c, ws,
+                       ws_bytes, stream, c);
 }
 
 extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,

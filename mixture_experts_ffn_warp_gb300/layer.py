@@ -230,10 +230,12 @@ class MoeForwardMX:
     router / expert_bias / normalize as for MoeForward."""
 
     def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", router: str = "softmax",
-                 expert_bias=None, normalize: bool = True, keep_fc1_c: bool = False, out_format: str = "bf16"):
+                 expert_bias=None, normalize: bool = True, keep_fc1_c: bool = False, out_format: str = "bf16",
+                 swiglu_clamp=None):
         if router not in ("softmax", "sigmoid"):
             raise ValueError("router must be 'softmax' or 'sigmoid'")
         self.weight_at = "combine"
+        self.swiglu_clamp = None if swiglu_clamp is None else tuple(float(v) for v in swiglu_clamp)
         self.T, self.H, self.F, self.E, self.k = T, H, F, E, k
         self.router, self.expert_bias, self.normalize = router, expert_bias, normalize
         dev = torch.device(device)
@@ -264,7 +266,7 @@ class MoeForwardMX:
     def fc1(self, w: MxWeights, stream=None):
         p = self.perm
         moe_grouped_fc1_swiglu_mxfp8(p.x_q, p.x_sf, w.Wg_q, w.Wg_sf, w.Wu_q, w.Wu_sf, p.group_offsets, self.ws,
-                                     self.h_q, self.h_sf, fc1_c=self.fc1_c, stream=stream)
+                                     self.h_q, self.h_sf, fc1_c=self.fc1_c, stream=stream, clamp=self.swiglu_clamp)
 
     def fc2(self, w: MxWeights, stream=None):
         moe_grouped_fc2_mxfp8(self.h_q, self.h_sf, w.Wd_q, w.Wd_sf, self.perm.group_offsets, self.ws, self.y_perm,

@@ -84,6 +84,8 @@ def test_host_validation_before_launch(lib):
                                               fk, 4096, nul) == 1                 # half of the route maps
     assert lib.moe_grouped_dgrad_fc2_dswiglu_clamped(fk, fk, fk, fk, 4, 128, 128, 8, 0.0, -1.0, -1.0, 1.0, fk, fk,
                                                      4096, nul) == 1
+    assert lib.moe_grouped_fc1_swiglu_mxfp8_clamped(fk, fk, fk, fk, fk, fk, fk, 4, 128, 128, 8, 1.0, 0.0, -1.0, 1.0,
+                                                    fk, fk, nul, fk, 4096, nul) == 1
     # permute: H % 8, capacity, workspace
     assert lib.moe_permute(nul, nul, 4, 12, 4, 2, 1, nul, 8, nul, nul, nul, nul, nul, 0, nul) == 2
     assert lib.moe_permute(nul, nul, 4, 16, 4, 2, 1, nul, 7, nul, nul, nul, nul, nul, 0, nul) == 1

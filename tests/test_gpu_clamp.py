@@ -62,3 +62,29 @@ def test_clamp_with_weight_in_fc1():
         ref = oracle.moe_fwd(hb["x"], hb["W_gate"], hb["W_up"], hb["W_down"], idx, w, round_mode=2,
                              weight_at=oracle.WEIGHT_IN_FC1)["out"]
     assert_close_rms(to_f64(out), ref, what="clamped, weight in FC1", bf16_out=True)
+
+
+def test_clamped_mxfp8_forward_and_straight_through_backward():
+    from mixture_experts_ffn_warp_gb300 import MoeBackwardMX, MoeForwardMX, MxWeights
+    from helpers import TOL_MXFP8
+    shape = small_shape("mxclamp", T=300, H=256, F=384, E=5, k=2, backward=True, mxfp8=True)
+    clamp = (-0.3, 0.2, -0.25, 0.25)
+    inp = gpu_inputs(shape, with_dy=True)
+    mw = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"])
+    m = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k, keep_fc1_c=True, swiglu_clamp=clamp)
+    out = m(inp["x"], inp["logits"], mw)
+    b = MoeBackwardMX(m)
+    b(inp["dY"], mw)
+    torch.cuda.synchronize()
+    assert m.ws.read_error() == 0
+    idx, w = m.topk_idx.cpu().numpy(), m.topk_w.cpu().numpy()
+    hb = {n: bits(inp[n]) for n in ("x", "W_gate", "W_up", "W_down", "dY")}
+    xq = oracle.mx_roundtrip_rows(hb["x"])
+    wg, wu, wd = oracle.mx_roundtrip_weights(hb["W_gate"], hb["W_up"], hb["W_down"])
+    with oracle.swiglu_clamp(*clamp):
+        ref_out = oracle.moe_fwd(xq, wg, wu, wd, idx, w, round_mode=2, h_mx=True)["out"]
+        ref = oracle.moe_bwd_mxfp8(hb["x"], hb["W_gate"], hb["W_up"], hb["W_down"], idx, w, hb["dY"], round_mode=2)
+    assert_close_rms(to_f64(out), ref_out, tol=TOL_MXFP8, what="clamped MXFP8 out", bf16_out=True)
+    assert_close_rms(to_f64(b.dx), ref["dx"], tol=TOL_MXFP8, what="dx", bf16_out=True)
+    for n in ("dW_gate", "dW_up", "dW_down"):
+        assert_close_rms(getattr(b, n).double().cpu().numpy(), ref[n], tol=TOL_MXFP8, what=n)
