@@ -44,7 +44,8 @@ FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s
 # ncu capture (profiles/), with a hash of the kernel sources it was taken on.  Reported as
 # null once those sources change.
 PROFILED_TRAFFIC = {("fine_grained", "fc1_swiglu"): (902.7e6, "79243ae97f195135")}
-KERNEL_SOURCES = ["common.cuh", "sm100.cuh", "grouped_gemm.cuh", "gemm_launch.cuh", "tmap.cuh", "ffn_fwd.cu"]
+KERNEL_SOURCES = ["common.cuh", "sm100.cuh", "grouped_gemm.cuh", "grouped_gemm_pair.cuh", "gemm_launch.cuh", "tmap.cuh",
+                  "ffn_fwd.cu"]
 
 
 def kernel_source_hash() -> str:

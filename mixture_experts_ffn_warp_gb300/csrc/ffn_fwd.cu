@@ -1,6 +1,7 @@
 // ffn_fwd.cu -- A3 + A4: grouped gate/up GEMM with SwiGLU epilogue, then the
 // grouped down projection, both on tcgen05 with group sizes read on the device.
 #include "gemm_launch.cuh"
+#include "grouped_gemm_pair.cuh"
 
 using namespace moe;
 using gg::Op;
@@ -15,6 +16,8 @@ moe_status_t check_common(int E, int H, int F, int64_t rows_cap, void *ws, size_
 }
 
 int64_t mblock_bound(int64_t rows_cap, int E) { return (rows_cap + gg::BM - 1) / gg::BM + E; }
+// upper bound of the token blocks of the pair GEMMs over all experts
+int64_t token_block_bound(int64_t rows_cap, int E) { return (rows_cap + gp::BT - 1) / gp::BT + E; }
 
 // FC1 + SwiGLU and FC2; topk_w / src_of_row non-null: the router weight of each row's
 // route is applied in the epilogue (to h, or to y).
@@ -26,26 +29,24 @@ moe_status_t fc1_impl(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const 
     moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!x_perm || !W_gate || !W_up || !group_offsets || !h) return MOE_ERR_INVALID_ARG;
-    // [rows, H] x [H, F] (gate | up) -> h [rows, F]; 128 gate + 128 up columns per tile
-    CUtensorMap tA, tB0, tB1, tC0, tC1;
-    if (!tmap_bf16_2d(&tA, x_perm, H, rows_cap, H, 64, 128) ||
-        !tmap_bf16_3d(&tB0, W_gate, F, H, E, 64, 64) || !tmap_bf16_3d(&tB1, W_up, F, H, E, 64, 64) ||
-        !tmap_store_2d(&tC0, h, 2, F, rows_cap, F))
+    // h [rows, F] = SwiGLU(x_perm [rows, H] x (W_gate | W_up) [H, F]) on CTA pairs: per pair
+    // tile 128 gate + 128 up weight columns (M = 256) x up to 256 tokens (N)
+    CUtensorMap tW0, tW1, tX, tOut, tStash;
+    if (!tmap_bf16_3d(&tW0, W_gate, F, H, E, 64, 64) || !tmap_bf16_3d(&tW1, W_up, F, H, E, 64, 64) ||
+        !tmap_bf16_2d(&tX, x_perm, H, rows_cap, H, 64, 128) || !tmap_store_plain(&tOut, h, 2, F, rows_cap, F, 32, 16))
         return MOE_ERR_UNSUPPORTED;
-    tC1 = tC0;
-    if (fc1_c && !tmap_store_2d(&tC1, fc1_c, 2, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F))
+    tStash = tOut;
+    if (fc1_c && !tmap_store_plain(&tStash, fc1_c, 2, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F, 32, 16))
         return MOE_ERR_UNSUPPORTED;
-    gg::Args a{};
+    gp::Args a{};
     a.group_offsets = group_offsets;
     a.E = E;
-    a.N = F;
     a.K = H;
-    a.n_tiles = F / 128;
+    a.N_out = F;
+    a.n_fb = F / 128;
     a.rows_cap = rows_cap;
-    a.out0 = reinterpret_cast<__nv_bfloat16 *>(h);
-    a.ld0 = F;
-    a.out1 = reinterpret_cast<__nv_bfloat16 *>(fc1_c);
-    a.ld1 = 2 * (int64_t)F;
+    a.h = reinterpret_cast<__nv_bfloat16 *>(h);
+    a.stash = reinterpret_cast<__nv_bfloat16 *>(fc1_c);
     a.route_w = topk_w;
     a.src_of_row = src_of_row;
     if (clamp) {
@@ -56,8 +57,8 @@ moe_status_t fc1_impl(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const 
         a.up_hi = clamp[3];
     }
     a.err = ws_error_word(ws);
-    return gg::launch<Op::FC1_SWIGLU, 256>(tA, tB0, tB1, tC0, tC1, a, mblock_bound(rows_cap, E) * a.n_tiles,
-                                           (cudaStream_t)stream);
+    return gp::launch<gp::Op::FC1>(tW0, tW1, tX, tOut, tStash, a, token_block_bound(rows_cap, E) * a.n_fb,
+                                   (cudaStream_t)stream);
 }
 
 moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32_t *group_offsets,
@@ -67,7 +68,27 @@ moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!h || !W_down || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
     // h [rows, F] x W_down [F, H] -> y_perm [rows, H]
-    const int bn = (H % 256 == 0) ? 256 : 128;
+    if (H % 256 == 0) {
+        // CTA pairs: 256 output columns (M) x up to 256 tokens (N) per pair tile
+        CUtensorMap tW, tX, tOut;
+        if (!tmap_bf16_3d(&tW, W_down, H, F, E, 64, 64) || !tmap_bf16_2d(&tX, h, F, rows_cap, F, 64, 128) ||
+            !tmap_store_plain(&tOut, y_perm, 4, H, rows_cap, H, 32, 16))
+            return MOE_ERR_UNSUPPORTED;
+        gp::Args a{};
+        a.group_offsets = group_offsets;
+        a.E = E;
+        a.K = F;
+        a.N_out = H;
+        a.n_fb = H / 256;
+        a.rows_cap = rows_cap;
+        a.y = y_perm;
+        a.route_w = topk_w;
+        a.src_of_row = src_of_row;
+        a.err = ws_error_word(ws);
+        return gp::launch<gp::Op::FC2>(tW, tW, tX, tOut, tOut, a, token_block_bound(rows_cap, E) * a.n_fb,
+                                       (cudaStream_t)stream);
+    }
+    const int bn = 128;
     CUtensorMap tA, tB, tC;
     if (!tmap_bf16_2d(&tA, h, F, rows_cap, F, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, 64) ||
         !tmap_store_2d(&tC, y_perm, 4, H, rows_cap, H))
@@ -85,7 +106,6 @@ moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32
     b.src_of_row = src_of_row;
     b.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * b.n_tiles;
-    if (bn == 256) return gg::launch<Op::FC2, 256>(tA, tB, tB, tC, tC, b, bound, (cudaStream_t)stream);
     return gg::launch<Op::FC2, 128>(tA, tB, tB, tC, tC, b, bound, (cudaStream_t)stream);
 }
 

@@ -1,0 +1,561 @@
+// grouped_gemm_pair.cuh -- the expert FFN's forward GEMMs (FC1 + SwiGLU, FC2) on CTA
+// pairs, with the routed tokens on the MMA's N axis.
+//
+// Each thread-block cluster of two CTAs (one per SM of an SM pair) computes one pair tile
+// at a time: 256 expert-weight rows (M, 128 per CTA) x up to 256 tokens (N) of one
+// expert, K = the contraction length, with tcgen05.mma.cta_group::2 (M = 256, K = 16).
+// Per 64-wide K step a CTA loads 16 KB of weights (its 128 M rows, MN-major: the weight
+// matrices' own layout) and 16 KB of tokens (its half of N, K-major rows of the permuted
+// activations), 32 KB in all against 48 KB for a one-CTA 128 x 256 tile of the same MMA
+// work, so six stages fit in shared memory.  Putting tokens on N makes an expert's last,
+// partial token block cost its own width rounded up to 16 tokens rather than a whole
+// 128-row tile.
+//
+// Roles (192 threads per CTA):
+//   warp 0      TMA producer in each CTA (one lane): its weight rows and its half of the
+//               token rows; completion is counted on the first CTA's `full` barrier
+//   warp 1      MMA issuer (one lane of the first CTA only); TMEM (512 columns, two
+//               accumulators of up to 256 columns) allocated by warp 1 of both CTAs
+//   warps 2..5  epilogue in each CTA: tcgen05.ld of its 128 lanes -> SwiGLU / scaling ->
+//               shared-memory staging -> TMA stores (row by row only at an expert's last
+//               token block)
+//
+// FC1: CTA c of the pair holds, for the 128 features [128 fb, 128 fb + 128) of the tile,
+// gate rows of features 128 fb + 64 c + [0, 64) in TMEM lanes 0..63 and the up rows of the
+// same features in lanes 64..127.  The warps of lanes 0..31 (gate) and 64..95 (up) pair up
+// through shared memory: each hands the other half of a 32-token chunk, and both finish
+// h = silu(g) * u for 16 tokens.
+// FC2: CTA c holds output columns 256 fb + 128 c + [0, 128) in its 128 lanes.
+//
+// Tile order: expert, feature block, token block (fastest), so the clusters working at
+// the same time share weight blocks and token rows in the L2.  Cluster i takes in round r
+// the tile r * G + (i + r) mod G (G clusters): the rotation spreads the cheaper last token
+// blocks of the experts evenly over the clusters.
+// ("Add MoE + expert-parallel Python API surface, PyTorch reference, and tests", Summary:
+// SwiGLU experts, fc1_c stash, router weight in an FFN epilogue, DeepSeek-style clamp;
+// "[Draft][JAX] MoE block optimization": grouped GEMM with the SwiGLU fused.)
+#pragma once
+
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace moe {
+namespace gp {
+
+enum class Op : int { FC1, FC2 };
+
+constexpr int kThreads = 192;
+constexpr int BT = 256;                  // tokens per pair tile (N), 128 rows loaded per CTA
+constexpr int kMaxE = 1024;
+constexpr int A_BYTES = 128 * 128;       // 128 weight rows x 64 K (two 64-wide MN chunks)
+constexpr int B_BYTES = 128 * 128;       // 128 token rows x 64 K
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int STAGES = 6;
+constexpr int TMEM_COLS = 512;           // two accumulators of BT fp32 columns
+constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
+
+// Epilogue shared memory: FC1 exchange buffers (2 warp pairs x 2 chunk parities x 2
+// directions x 16 tokens x 32 features fp32 = 16 KB) and output staging, two slots per
+// epilogue warp of 16 token rows (FC1 bf16 rows of 64 B, FC2 fp32 rows of 128 B).
+template <Op OP>
+struct PCfg {
+    static constexpr int XBUF_BYTES = OP == Op::FC1 ? 2 * 2 * 2 * 16 * 32 * 4 : 0;
+    static constexpr int SLOT_BYTES = OP == Op::FC1 ? 16 * 64 : 16 * 128;
+    static constexpr int STG_BYTES = 4 * 2 * SLOT_BYTES;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + XBUF_BYTES + STG_BYTES + 1024;   // + alignment slack
+    // with the static tables (~8.4 KB) within the 227 KB a CTA may use
+    static_assert(SMEM_BYTES + 8 * 1024 + 512 <= 232448, "shared memory budget");
+};
+
+struct Args {
+    const int32_t *group_offsets;   // [E+1]
+    int E;
+    int K;             // contraction length: FC1 H, FC2 F
+    int N_out;         // output columns: FC1 F, FC2 H
+    int n_fb;          // feature blocks per expert: FC1 F / 128, FC2 H / 256
+    int64_t rows_cap;  // rows of the permuted tensors
+    __nv_bfloat16 *h;        // FC1: h [rows, F]
+    __nv_bfloat16 *stash;    // FC1: [g | u] bf16 [rows, 2F] (nullable)
+    float *y;                // FC2: y_perm [rows, H]
+    // router weight of each row's route applied in the epilogue (padding rows get 0); null = unweighted
+    const float *route_w;
+    const int32_t *src_of_row;
+    // FC1: optional clamp of the SwiGLU inputs, inclusive bounds (clamp != 0)
+    int clamp;
+    float gate_lo, gate_hi, up_lo, up_hi;
+    uint32_t *err;
+};
+
+struct PTile {
+    int e, fb;
+    int t0;       // first permuted row of the token block
+    int nvalid;   // rows of the block that belong to the expert (1..BT)
+    int n;        // MMA N: nvalid rounded up to 16
+};
+
+// pair tile p -> (expert, feature block, token block); s_start[e] = tiles before expert e
+__device__ __forceinline__ PTile decode(int p, const Args &a, const int *s_off, const int *s_start) {
+    int lo = 0, hi = a.E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_start[mid] <= p) lo = mid; else hi = mid - 1;
+    }
+    PTile t;
+    t.e = lo;
+    const int rows = s_off[lo + 1] - s_off[lo];
+    const int ntb = (rows + BT - 1) / BT;
+    const int local = p - s_start[lo];
+    t.fb = local / ntb;
+    const int tb = local - t.fb * ntb;
+    t.t0 = s_off[lo] + tb * BT;
+    const int left = rows - tb * BT;
+    t.nvalid = left < BT ? left : BT;
+    t.n = (t.nvalid + 15) & ~15;
+    return t;
+}
+
+__device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// Tile of round r for cluster `cid` of G (-1 past the end).
+__device__ __forceinline__ int round_tile(int r, int cid, int G, int total) {
+    const int p = r * G + (cid + r) % G;
+    return p < total ? p : -1;
+}
+
+template <Op OP>
+__global__ void __launch_bounds__(kThreads, 1)
+pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant__ CUtensorMap tmW1,
+                 const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmOut,
+                 const __grid_constant__ CUtensorMap tmStash, const Args args) {
+    using PC = PCfg<OP>;
+    constexpr int XBUF_BYTES = PC::XBUF_BYTES, SLOT_BYTES = PC::SLOT_BYTES;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
+    __shared__ uint64_t xbar[2][2];   // FC1 exchange: [warp pair][chunk parity], 64 arrivals
+    __shared__ uint32_t s_tmem_base;
+    __shared__ int s_off[kMaxE + 1];
+    __shared__ int s_start[kMaxE + 1];
+    __shared__ volatile int s_abort;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = sm100::cluster_ctarank();
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t smem_base = sm100::smem_u32(smem);
+
+    // ---------------------------------------------------------------- set-up (on chip)
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            sm100::mbar_init(&full_bar[s], 1);
+            sm100::mbar_init(&empty_bar[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            sm100::mbar_init(&tfull_bar[b], 1);
+            sm100::mbar_init(&tempty_bar[b], 2 * 4);   // one lane of each epilogue warp of both CTAs
+        }
+        sm100::mbar_init(&drain_bar, 1);
+        for (int i = 0; i < 4; ++i) sm100::mbar_init(&xbar[i >> 1][i & 1], 64);
+        s_abort = 0;
+        sm100::fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        sm100::prefetch_tmap(&tmW0);
+        if constexpr (OP == Op::FC1) sm100::prefetch_tmap(&tmW1);
+        sm100::prefetch_tmap(&tmX);
+    }
+    if (warp == 1) {
+        sm100::tmem_alloc_pair(&s_tmem_base, TMEM_COLS);
+        sm100::tmem_relinquish_pair();
+    }
+    // both CTAs' barriers are initialised before either CTA touches the other's
+    sm100::tc_fence_before();
+    sm100::cluster_sync();
+    sm100::tc_fence_after();
+
+    // from here on the kernel reads what earlier kernels on the stream wrote
+    pdl_wait();
+    const int E = args.E;
+    for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = args.group_offsets[i];
+    __syncthreads();
+    if (warp == 2) {
+        // s_start[e] = pair tiles before expert e (feature blocks x token blocks)
+        const int seg = (E + 31) / 32;
+        const int e0 = lane * seg;
+        auto tiles_of = [&](int e) {
+            int rows = s_off[e + 1] - s_off[e];
+            if (rows < 0) rows = 0;
+            return ((rows + BT - 1) / BT) * args.n_fb;
+        };
+        int sum = 0;
+        for (int i = 0; i < seg; ++i)
+            if (e0 + i < E) sum += tiles_of(e0 + i);
+        int incl = sum;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, incl, off);
+            if (lane >= off) incl += o;
+        }
+        int run = incl - sum;
+        for (int i = 0; i < seg; ++i) {
+            if (e0 + i < E) {
+                s_start[e0 + i] = run;
+                run += tiles_of(e0 + i);
+            }
+        }
+        if (lane == 31) s_start[E] = incl;
+    }
+    sm100::tc_fence_before();
+    __syncthreads();
+    sm100::tc_fence_after();
+    const uint32_t tmem_base = s_tmem_base;
+    const int total = s_start[E];
+    const int G = (int)(gridDim.x >> 1), cid = (int)(blockIdx.x >> 1);
+    const int rounds = (total + G - 1) / G;
+    const int kblocks = args.K / 64;
+    volatile int *abort = &s_abort;
+
+    if (warp == 0) {
+        // ============================================================ producer (both CTAs)
+        if (lane == 0) {
+            const uint32_t full0 = sm100::cluster_addr(&full_bar[0], 0);   // the first CTA's barriers
+            int stage = 0;
+            uint32_t phase = 0;
+            int issued = 0;
+            bool ok = true;
+            for (int r = 0; r < rounds && ok; ++r) {
+                const int p = round_tile(r, cid, G, total);
+                if (p < 0) continue;
+                const PTile tl = decode(p, args, s_off, s_start);
+                const int trow = tl.t0 + (int)rank * (tl.n >> 1);   // this CTA's half of the tokens
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+                    const uint32_t fb_c = full0 + (uint32_t)(stage * sizeof(uint64_t));
+                    if (rank == 0) sm100::mbar_arrive_expect_tx(&full_bar[stage], 2 * STAGE_BYTES);
+                    const int k0 = kb * 64;
+                    if constexpr (OP == Op::FC1) {
+                        // 64 gate then 64 up feature columns of W [E][K][F] (MN-major chunks)
+                        const int f0 = tl.fb * 128 + (int)rank * 64;
+                        sm100::tma_load_3d_pair(sa, &tmW0, fb_c, f0, k0, tl.e);
+                        sm100::tma_load_3d_pair(sa + 8192, &tmW1, fb_c, f0, k0, tl.e);
+                    } else {
+                        // 128 output columns of W_down [E][K][H]
+                        const int c0 = tl.fb * 256 + (int)rank * 128;
+                        sm100::tma_load_3d_pair(sa, &tmW0, fb_c, c0, k0, tl.e);
+                        sm100::tma_load_3d_pair(sa + 8192, &tmW0, fb_c, c0 + 64, k0, tl.e);
+                    }
+                    sm100::tma_load_2d_pair(sb, &tmX, fb_c, k0, trow);
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) {
+                // the CTA's copies in flight land before it can exit: its own stages are
+                // free again once the first CTA's MMAs (or its drain) release them
+                int st = stage;
+                uint32_t ph = phase;
+                for (int i = 0; i < STAGES && i < issued; ++i) {
+                    if (--st < 0) { st = STAGES - 1; ph ^= 1u; }
+                    int dummy = 0;
+                    sm100::mbar_wait(&empty_bar[st], ph, &dummy, nullptr, 10000000ull);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ============================================================ MMA issuer (first CTA)
+        // The whole warp runs the loop and computes the operand descriptors (warp-uniform
+        // values); one elected lane issues the MMAs and their commits.  Measured: the same
+        // loop with the descriptor arithmetic inside a one-lane branch issued an MMA every
+        // ~170 cycles, below the tensor pipe's rate.
+        if (rank == 0) {
+            const uint64_t a_desc0 = sm100::sdesc_sw128(smem_base, 8192, 1024);            // MN-major weights
+            const uint64_t b_desc0 = sm100::sdesc_sw128(smem_base + A_BYTES, 16, 1024);    // K-major tokens
+            constexpr uint64_t A_KSTEP = 2048 >> 4, B_KSTEP = 32 >> 4, STAGE_STEP = STAGE_BYTES >> 4;
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            bool ok = true, issued_any = false;
+            for (int r = 0; r < rounds && ok; ++r) {
+                const int p = round_tile(r, cid, G, total);
+                if (p < 0) continue;
+                const PTile tl = decode(p, args, s_off, s_start);
+                const uint32_t idesc = sm100::idesc_bf16(256, tl.n, true, false);
+                const bool got_acc =
+                    sm100::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, kWaitLimitNs);
+                if (__any_sync(0xFFFFFFFFu, !got_acc)) { ok = false; break; }
+                sm100::tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BT);
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, kWaitLimitNs);
+                    if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
+                    sm100::tc_fence_after();
+                    const uint64_t ad = a_desc0 + (uint64_t)stage * STAGE_STEP;
+                    const uint64_t bd = b_desc0 + (uint64_t)stage * STAGE_STEP;
+                    if (sm100::elect_one()) {
+                        sm100::mma_bf16_pair(d_tmem, ad, bd, idesc, kb != 0 ? 1u : 0u);
+                        sm100::mma_bf16_pair(d_tmem, ad + A_KSTEP, bd + B_KSTEP, idesc, 1u);
+                        sm100::mma_bf16_pair(d_tmem, ad + 2 * A_KSTEP, bd + 2 * B_KSTEP, idesc, 1u);
+                        sm100::mma_bf16_pair(d_tmem, ad + 3 * A_KSTEP, bd + 3 * B_KSTEP, idesc, 1u);
+                        sm100::mma_commit_pair(&empty_bar[stage], 0x3);
+                    }
+                    __syncwarp();
+                    issued_any = true;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                if (sm100::elect_one()) sm100::mma_commit_pair(&tfull_bar[acc], 0x3);
+                __syncwarp();
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+            }
+            if (!ok && issued_any && sm100::elect_one()) {
+                // drain: the MMAs already issued finish before TMEM is released
+                sm100::mma_commit_pair(&drain_bar, 0x1);
+                int dummy = 0;
+                sm100::mbar_wait(&drain_bar, 0, &dummy, nullptr, 10000000ull);
+            }
+            __syncwarp();
+        }
+    } else {
+        // ============================================================ epilogue (both CTAs)
+        const int q = warp & 3;              // TMEM lane quarter of this warp
+        const uint32_t tempty0 = sm100::cluster_addr(&tempty_bar[0], 0);
+        uint8_t *stg = smem + STAGES * STAGE_BYTES + XBUF_BYTES + q * 2 * SLOT_BYTES;
+        const uint32_t stg_s = smem_base + STAGES * STAGE_BYTES + XBUF_BYTES + q * 2 * SLOT_BYTES;
+        int slot = 0;
+        auto slot_open = [&]() {
+            if (lane == 0) sm100::bulk_wait_read<1>();   // the store that last read this slot is done
+            __syncwarp();
+        };
+        auto slot_store = [&](const CUtensorMap *tm, int col, int row) {
+            sm100::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                sm100::tma_store_2d(tm, stg_s + slot * SLOT_BYTES, col, row);
+                sm100::bulk_commit();
+            }
+            slot ^= 1;
+        };
+        // 16 tokens x 32 bf16 features (this thread's feature = lane): staged as 64-byte
+        // token rows (pairs of lanes swap values so that every store is a 32-bit word)
+        auto put_bf16x16 = [&](const float (&v)[16]) {
+            uint32_t *w = reinterpret_cast<uint32_t *>(stg + slot * SLOT_BYTES);
+#pragma unroll
+            for (int t = 0; t < 16; t += 2) {
+                const float send = (lane & 1) ? v[t] : v[t + 1];
+                const float recv = __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+                __nv_bfloat162 pk;
+                int row;
+                if (lane & 1) { pk = __floats2bfloat162_rn(recv, v[t + 1]); row = t + 1; }
+                else { pk = __floats2bfloat162_rn(v[t], recv); row = t; }
+                w[row * 16 + (lane >> 1)] = *reinterpret_cast<uint32_t *>(&pk);
+            }
+        };
+        // store 16 tokens (rows row0 ..) of one feature column block; nv of them valid
+        auto store_bf16x16 = [&](const float (&v)[16], const CUtensorMap *tm, __nv_bfloat16 *base, int64_t ld,
+                                 int col, int row0, int nv) {
+            if (nv >= 16) {
+                slot_open();
+                put_bf16x16(v);
+                slot_store(tm, col, row0);
+            } else if (nv > 0) {
+#pragma unroll
+                for (int t = 0; t < 16; ++t)
+                    if (t < nv) base[(int64_t)(row0 + t) * ld + col + lane] = __float2bfloat16_rn(v[t]);
+            }
+        };
+        auto route_weight = [&](int row, bool valid) {
+            const int src = valid ? args.src_of_row[row] : -1;
+            return src >= 0 ? args.route_w[src] : 0.0f;
+        };
+
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        int chunk_parity = 0;
+        uint32_t xphase = 0;   // bit b: parity of the next wait on xbar[pair][b]
+        bool alive = true;
+        for (int r = 0; r < rounds && alive; ++r) {
+            const int p = round_tile(r, cid, G, total);
+            if (p < 0) continue;
+            const PTile tl = decode(p, args, s_off, s_start);
+            const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, kWaitLimitNs);
+            if (__any_sync(0xFFFFFFFFu, !got)) break;
+            sm100::tc_fence_after();
+            const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
+
+            if constexpr (OP == Op::FC1) {
+                const int pr = q & 1;                  // feature half of this warp
+                const bool gate = q < 2;               // lanes 0..63 gate, 64..127 up
+                const int F = args.N_out;
+                const int fcol = tl.fb * 128 + (int)rank * 64 + pr * 32;   // first of this warp's 32 features
+                float *xg = reinterpret_cast<float *>(smem + STAGES * STAGE_BYTES) + pr * 2048;   // 8 KB per pair
+#pragma unroll 1
+                for (int c0 = 0; c0 < tl.n; c0 += 32) {
+                    uint32_t raw[32];
+                    sm100::tmem_ld32(tacc + c0, raw);
+                    sm100::tmem_ld_wait();
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+                    if (args.stash) {   // unclamped g (gate warps) or u (up warps), bf16
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf) {
+                            float sv[16];
+#pragma unroll
+                            for (int i = 0; i < 16; ++i) sv[i] = v[16 * hf + i];
+                            store_bf16x16(sv, &tmStash, args.stash, 2 * (int64_t)F, gate ? fcol : F + fcol,
+                                          tl.t0 + c0 + 16 * hf, tl.nvalid - c0 - 16 * hf);
+                        }
+                    }
+                    if (args.clamp) {
+                        const float lo = gate ? args.gate_lo : args.up_lo, hi = gate ? args.gate_hi : args.up_hi;
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = fminf(fmaxf(v[i], lo), hi);
+                    }
+                    // exchange: the gate warp keeps tokens 0..15 of the chunk and hands over
+                    // 16..31; the up warp the other way round
+                    float *xb = xg + chunk_parity * 1024;   // [direction][16 tokens][32 lanes]
+                    if (gate) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) xb[t * 32 + lane] = v[16 + t];
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) xb[512 + t * 32 + lane] = v[t];
+                    }
+                    uint64_t *xbr = &xbar[pr][chunk_parity];
+                    sm100::mbar_arrive(xbr);
+                    const bool xok = sm100::mbar_wait(xbr, (xphase >> chunk_parity) & 1u, abort, args.err, kWaitLimitNs);
+                    xphase ^= 1u << chunk_parity;
+                    if (__any_sync(0xFFFFFFFFu, !xok)) { alive = false; break; }
+                    float hv[16];
+                    if (gate) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) hv[t] = silu(v[t]) * xb[512 + t * 32 + lane];
+                    } else {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) hv[t] = silu(xb[t * 32 + lane]) * v[16 + t];
+                    }
+                    chunk_parity ^= 1;
+                    const int tok0 = c0 + (gate ? 0 : 16);          // first token of this warp's 16
+                    const int nv = tl.nvalid - tok0;
+                    if (args.route_w) {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) hv[t] *= route_weight(tl.t0 + tok0 + t, t < nv);
+                    }
+                    store_bf16x16(hv, &tmOut, args.h, F, fcol, tl.t0 + tok0, nv);
+                }
+                if (!alive) break;
+            } else {
+                const int H = args.N_out;
+                const int hcol = tl.fb * 256 + (int)rank * 128 + q * 32;   // this warp's 32 output columns
+#pragma unroll 1
+                for (int c0 = 0; c0 < tl.n; c0 += 32) {
+                    uint32_t raw[32];
+                    sm100::tmem_ld32(tacc + c0, raw);
+                    sm100::tmem_ld_wait();
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        const int tok0 = c0 + 16 * hf;
+                        const int nv = tl.nvalid - tok0;
+                        float v[16];
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) v[t] = __uint_as_float(raw[16 * hf + t]);
+                        if (args.route_w) {
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) v[t] *= route_weight(tl.t0 + tok0 + t, t < nv);
+                        }
+                        if (nv >= 16) {
+                            slot_open();
+                            float *w = reinterpret_cast<float *>(stg + slot * SLOT_BYTES);
+#pragma unroll
+                            for (int t = 0; t < 16; ++t) w[t * 32 + lane] = v[t];   // 128-byte token rows
+                            slot_store(&tmOut, hcol, tl.t0 + tok0);
+                        } else if (nv > 0) {
+#pragma unroll
+                            for (int t = 0; t < 16; ++t)
+                                if (t < nv) args.y[(int64_t)(tl.t0 + tok0 + t) * H + hcol + lane] = v[t];
+                        }
+                    }
+                }
+            }
+            sm100::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) sm100::mbar_arrive_cluster(tempty0 + (uint32_t)(acc * sizeof(uint64_t)));
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+        // every TMA store of this warp has finished before the CTA can exit
+        if (lane == 0) sm100::bulk_wait_all();
+        __syncwarp();
+    }
+
+    // ---------------------------------------------------------------- teardown
+    sm100::tc_fence_before();
+    __syncthreads();
+    sm100::cluster_sync();   // no arrive or copy of one CTA still targets the other
+    if (warp == 1) {
+        sm100::tc_fence_after();
+        sm100::tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace gp
+}  // namespace moe
+
+namespace moe {
+namespace gp {
+
+// Host launch: clusters of two CTAs, as many as can be resident at once (the schedule is
+// persistent), at most one per pair tile; programmatic stream serialization as every
+// kernel of the library.
+template <Op OP>
+moe_status_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensorMap &x, const CUtensorMap &out,
+                    const CUtensorMap &stash, const Args &args, int64_t tiles_bound, cudaStream_t s) {
+    if (tiles_bound <= 0) return MOE_OK;
+    auto kern = pair_gemm_kernel<OP>;
+    constexpr int smem = PCfg<OP>::SMEM_BYTES;
+    static int configured_dev = -1;
+    static int max_clusters = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    if (configured_dev != dev) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        cudaLaunchConfig_t q{};
+        q.gridDim = dim3(2);
+        q.blockDim = dim3(kThreads);
+        q.dynamicSmemBytes = smem;
+        cudaLaunchAttribute qa[1];
+        qa[0].id = cudaLaunchAttributeClusterDimension;
+        qa[0].val.clusterDim.x = 2;
+        qa[0].val.clusterDim.y = 1;
+        qa[0].val.clusterDim.z = 1;
+        q.attrs = qa;
+        q.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
+        max_clusters = n;
+        configured_dev = dev;
+    }
+    const int64_t G = tiles_bound < max_clusters ? tiles_bound : max_clusters;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3((unsigned)(2 * G));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[2];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 2;
+    if (cudaLaunchKernelEx(&cfg, kern, w0, w1, x, out, stash, args) != cudaSuccess) return MOE_ERR_CUDA;
+    return launch_status();
+}
+
+}  // namespace gp
+}  // namespace moe

@@ -76,6 +76,18 @@ inline bool tmap_store_2d(CUtensorMap *m, const void *base, int elem_bytes, uint
     return encode_tmap(m, dt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
+// Store map without swizzle: 2-D row-major [outer, inner] of `elem_bytes`-byte elements
+// (bf16 or fp32), row pitch `ld` elements, boxes of box_inner x box_rows (dense rows in
+// shared memory).
+inline bool tmap_store_plain(CUtensorMap *m, const void *base, int elem_bytes, uint64_t inner, uint64_t outer,
+                             uint64_t ld, uint32_t box_inner, uint32_t box_rows) {
+    const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint64_t dims[2] = {inner, outer};
+    const uint64_t strides[1] = {ld * (uint64_t)elem_bytes};
+    const uint32_t box[2] = {box_inner, box_rows};
+    return encode_tmap(m, dt, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
 // 2-D byte matrix [outer, inner] with row pitch `ld` bytes (E4M3 data).
 inline bool tmap_u8_2d(CUtensorMap *m, const void *base, uint64_t inner, uint64_t outer, uint64_t ld,
                        uint32_t box_inner, uint32_t box_outer) {

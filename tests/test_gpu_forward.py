@@ -27,6 +27,8 @@ SMALL = {
     "dense": small_shape("dense", T=200, H=128, F=128, E=1, k=1),
     # many experts, several empty
     "many": small_shape("many", T=512, H=128, F=128, E=64, k=4, skew=True),
+    # ~1000 rows per expert: several 256-token blocks per expert and a ragged last block
+    "blocks": small_shape("blocks", T=1500, H=256, F=256, E=3, k=2),
 }
 
 
