@@ -4,7 +4,7 @@
 // One CTA per SM, 6 warps:
 //   warp 0      TMA producer (one lane): A and B tiles (and, for MXFP8, their
 //               block scales) -> a ring of smem stages
-//   warp 1      MMA issuer (lane 0 issues tcgen05.mma, M=128 x N=BN; K=16 per
+//   warp 1      MMA issuer (one elected lane issues tcgen05.mma, M=128 x N=BN; K=16 per
 //               instruction for bf16, K=32 for E4M3); fp32 accumulators live in
 //               TMEM (double-buffered for bf16, single for MXFP8, whose scales
 //               take the other half of TMEM)
@@ -382,6 +382,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1) {
         // ============================================================ MMA issuer
         constexpr uint32_t IDESC = TR::mx ? sm100::idesc_mxf8(BM, BN) : sm100::idesc_bf16(BM, BN, TR::a_mn, TR::b_mn);
+        // stage-0 operand descriptors; a K step of 16 (bf16) or 32 (E4M3) elements moves the
+        // start address by 32 bytes (K-major) or one 2 KB group of 16 rows (MN-major)
+        const uint64_t a_desc0 = TR::a_mn ? sm100::sdesc_sw128(smem_base, 8192, 1024) : sm100::sdesc_sw128(smem_base, 16, 1024);
+        const uint64_t b_desc0 = TR::b_mn ? sm100::sdesc_sw128(smem_base + C::A_BYTES, 8192, 1024)
+                                          : sm100::sdesc_sw128(smem_base + C::A_BYTES, 16, 1024);
+        constexpr uint64_t A_KSTEP = TR::a_mn ? (2048 >> 4) : (32 >> 4);
+        constexpr uint64_t B_KSTEP = TR::b_mn ? (2048 >> 4) : (32 >> 4);
         int stage = 0;
         uint32_t phase = 0;
         int acc = 0;
@@ -425,47 +432,51 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
                 sm100::tc_fence_after();
-                if (lane == 0) {
-                    if constexpr (TR::mx) {
+                // descriptors of this stage computed by the whole warp (warp-uniform values);
+                // one elected lane issues
+                const uint64_t ad = a_desc0 + (uint64_t)stage * (C::STAGE_BYTES >> 4);
+                const uint64_t bd = b_desc0 + (uint64_t)stage * (C::STAGE_BYTES >> 4);
+                if constexpr (TR::mx) {
+                    const uint32_t ssf = sb + C::B_BYTES;
+                    const uint32_t tsf = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
+                    if (sm100::elect_one()) {
                         // scales of this stage: smem atoms -> TMEM slot of the stage, then 4 MMAs of
                         // K = 32 with scale ids 0..3 (the 4 bytes of each TMEM scale word)
-                        const uint32_t ssf = sb + C::B_BYTES;
-                        const uint32_t tsf = tmem_base + C::SF_COL0 + stage * C::SF_COLS;
                         sm100::tmem_cp_32x128b_x4(tsf, sm100::sdesc_plain(ssf));
 #pragma unroll
                         for (int j = 0; j < BN / 128; ++j)
                             sm100::tmem_cp_32x128b_x4(tsf + 4 + 4 * j, sm100::sdesc_plain(ssf + 512 + 512 * j));
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) {
-                            const uint64_t ad = sm100::sdesc_sw128(sa + kk * 32, 16, 1024);
-                            const uint64_t bd = sm100::sdesc_sw128(sb + kk * 32, 16, 1024);
-                            sm100::mma_mxf8(d_tmem, ad, bd, IDESC | sm100::idesc_sf_ids(kk, kk), tsf, tsf + 4,
-                                            (kb | kk) != 0 ? 1u : 0u);
-                        }
-                    } else {
-#pragma unroll
-                        for (int kk = 0; kk < TR::BK / UMMA_K; ++kk) {
-                            if (kk >= kk_end) break;
-                            uint64_t ad, bd;
-                            if constexpr (TR::a_mn) ad = sm100::sdesc_sw128(sa + kk * 2048, 8192, 1024);
-                            else ad = sm100::sdesc_sw128(sa + kk * 32, 16, 1024);
-                            if constexpr (TR::b_mn) bd = sm100::sdesc_sw128(sb + kk * 2048, 8192, 1024);
-                            else bd = sm100::sdesc_sw128(sb + kk * 32, 16, 1024);
-                            sm100::mma_bf16(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
-                        }
+                        for (int kk = 0; kk < 4; ++kk)
+                            sm100::mma_mxf8(d_tmem, ad + kk * A_KSTEP, bd + kk * B_KSTEP,
+                                            IDESC | sm100::idesc_sf_ids(kk, kk), tsf, tsf + 4, (kb | kk) != 0 ? 1u : 0u);
+                        sm100::mma_commit(&empty_bar[stage]);
                     }
-                    sm100::mma_commit(&empty_bar[stage]);
-                    issued_any = true;
+                } else {
+                    if (sm100::elect_one()) {
+                        if (kk_end == TR::BK / UMMA_K) {
+#pragma unroll
+                            for (int kk = 0; kk < TR::BK / UMMA_K; ++kk)
+                                sm100::mma_bf16(d_tmem, ad + kk * A_KSTEP, bd + kk * B_KSTEP, IDESC,
+                                                (kb | kk) != 0 ? 1u : 0u);
+                        } else {
+                            for (int kk = 0; kk < kk_end; ++kk)
+                                sm100::mma_bf16(d_tmem, ad + kk * A_KSTEP, bd + kk * B_KSTEP, IDESC,
+                                                (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        sm100::mma_commit(&empty_bar[stage]);
+                    }
                 }
+                issued_any = true;
                 __syncwarp();
                 if (++stage == S) { stage = 0; phase ^= 1u; }
             }
             if (!ok) break;
-            if (lane == 0) sm100::mma_commit(&tfull_bar[acc]);
+            if (sm100::elect_one()) sm100::mma_commit(&tfull_bar[acc]);
             __syncwarp();
             if (++acc == NACC) { acc = 0; acc_phase ^= 1u; }
         }
-        if (!ok && issued_any && lane == 0) {
+        if (!ok && issued_any && sm100::elect_one()) {
             // drain: wait for the MMAs already issued before TMEM is released
             sm100::mma_commit(&drain_bar);
             int dummy = 0;
