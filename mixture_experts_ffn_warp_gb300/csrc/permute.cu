@@ -18,9 +18,9 @@ namespace moe {
 namespace {
 
 constexpr int kScatterWarps = 8;
-// Largest [chunks][E] count matrix the final scan stages in shared memory: 46 KB, within
-// the 48 KB a block may use without opt-in, with room for the kernel's static arrays.
-constexpr int64_t kScanSmemInts = 11776;
+// Largest [chunks][E] count matrix the final scan stages in shared memory: 39 KB, within the
+// 48 KB a block may use without opt-in next to the counting kernel's static arrays (8.7 KB).
+constexpr int64_t kScanSmemInts = 9984;
 
 // Group sizes, aligned offsets, each chunk's first row per expert (in place of
 // the chunk counts) and, if mtile_start != nullptr, each group's first 128-row
@@ -124,6 +124,117 @@ __device__ void scan_groups(int32_t *chunk_counts, int64_t chunks, int E, int al
     }
 }
 
+// Column split of a [C][E] int matrix in shared memory over the block (E <= blockDim.x):
+// thread (e = tid % E, j = tid / E) with j < J = min(blockDim.x / E, 32) takes rows
+// [c0, c1) of column e, so the lanes of a warp read consecutive columns (no bank
+// conflicts); the J partial sums of a column meet in s_part.  Returns the column's
+// exclusive prefix before row c0 and its total.
+struct ColSplit {
+    int e, j, c0, c1, pre, tot;
+    bool act;
+};
+
+__device__ ColSplit column_split(const int32_t *s_mat, int C, int E, int32_t *s_part) {
+    ColSplit r;
+    const int nt = blockDim.x, tid = threadIdx.x;
+    const int J = nt / E < 32 ? nt / E : 32;
+    r.e = tid % E;
+    r.j = tid / E;
+    r.act = r.j < J;
+    const int per = (C + J - 1) / J;
+    r.c0 = r.j * per < C ? r.j * per : C;
+    r.c1 = r.c0 + per < C ? r.c0 + per : C;
+    int seg = 0;
+    if (r.act)
+        for (int c = r.c0; c < r.c1; ++c) seg += s_mat[c * E + r.e];
+    if (r.act) s_part[r.j * E + r.e] = seg;
+    __syncthreads();
+    r.pre = 0;
+    r.tot = 0;
+    if (r.act) {
+        for (int q = 0; q < J; ++q) {
+            const int v = s_part[q * E + r.e];
+            if (q < r.j) r.pre += v;
+            r.tot += v;
+        }
+    }
+    __syncthreads();   // s_part may be reused
+    return r;
+}
+
+// scan_groups for a count matrix staged in shared memory, with E <= blockDim.x (column
+// split as above; the exclusive scan over the experts is a block scan).  Same results as
+// scan_groups.
+__device__ void scan_groups_smem(int32_t *chunk_counts, int C, int E, int align, int32_t *group_sizes,
+                                 int32_t *group_offsets, int32_t *mtile_start, int32_t *s_mat) {
+    __shared__ int32_t s_wsum[32], s_wtile[32], s_first[1025], s_part[1024];
+    const int nt = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int n = C * E;
+    for (int base = 0; base < n; base += 8 * nt) {   // 8 loads in flight per thread, then the stores
+        int v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * nt + tid;
+            v[u] = i < n ? __ldcg(chunk_counts + i) : 0;
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int i = base + u * nt + tid;
+            if (i < n) s_mat[i] = v[u];
+        }
+    }
+    __syncthreads();
+    const ColSplit cs = column_split(s_mat, C, E, s_part);
+    // exclusive scan over the experts: thread e (j == 0) holds expert e's padded size
+    const bool head = cs.act && cs.j == 0;
+    const int padded = head ? (cs.tot + align - 1) / align * align : 0;
+    const int tiles = head ? (padded + 127) / 128 : 0;
+    int pi = padded, ti = tiles;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int o = __shfl_up_sync(0xFFFFFFFFu, pi, off), ot = __shfl_up_sync(0xFFFFFFFFu, ti, off);
+        if (lane >= off) { pi += o; ti += ot; }
+    }
+    if (lane == 31) { s_wsum[warp] = pi; s_wtile[warp] = ti; }
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = (nt + 31) / 32;
+        const int v = lane < nw ? s_wsum[lane] : 0, vt = lane < nw ? s_wtile[lane] : 0;
+        int vi = v, vti = vt;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int o = __shfl_up_sync(0xFFFFFFFFu, vi, off), ot = __shfl_up_sync(0xFFFFFFFFu, vti, off);
+            if (lane >= off) { vi += o; vti += ot; }
+        }
+        if (lane < nw) { s_wsum[lane] = vi - v; s_wtile[lane] = vti - vt; }
+    }
+    __syncthreads();
+    if (head) {
+        const int e = cs.e;
+        const int off0 = pi - padded + s_wsum[warp], t0 = ti - tiles + s_wtile[warp];
+        group_sizes[e] = cs.tot;
+        group_offsets[e] = off0;
+        if (mtile_start) mtile_start[e] = t0;
+        s_first[e] = off0;
+        if (e == E - 1) {
+            group_offsets[E] = off0 + padded;
+            if (mtile_start) mtile_start[E] = t0 + tiles;
+        }
+    }
+    __syncthreads();
+    // each chunk's first row per expert, in place of the counts
+    if (cs.act) {
+        int run = s_first[cs.e] + cs.pre;
+        for (int c = cs.c0; c < cs.c1; ++c) {
+            const int v = s_mat[c * E + cs.e];
+            s_mat[c * E + cs.e] = run;
+            run += v;
+        }
+    }
+    __syncthreads();
+    for (int i = tid; i < n; i += nt) chunk_counts[i] = s_mat[i];
+}
+
 // Counting pass: per 2048-route chunk, stable ranks (warp ballots + per-warp running
 // counts) and per-expert chunk counts; the last block to finish runs scan_groups,
 // so that offsets are ready when the kernel ends (no separate scan launch).
@@ -200,8 +311,11 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E, int
     __syncthreads();
     if (!s_last) return;
     __threadfence();
-    scan_groups(chunk_counts, gridDim.x, E, align, group_sizes, group_offsets, mtile_start,
-                scan_in_smem ? s_cnt : nullptr);
+    if (scan_in_smem && E <= (int)blockDim.x)
+        scan_groups_smem(chunk_counts, gridDim.x, E, align, group_sizes, group_offsets, mtile_start, s_cnt);
+    else
+        scan_groups(chunk_counts, gridDim.x, E, align, group_sizes, group_offsets, mtile_start,
+                    scan_in_smem ? s_cnt : nullptr);
     if (threadIdx.x == 0) *done = 0u;
 }
 
@@ -551,6 +665,26 @@ permute_scatter_mx_kernel(const uint4 *__restrict__ x, const int32_t *__restrict
     }
 }
 
+// The quantising scatter (KMAX >= k).
+moe_status_t launch_scatter_mx(cudaStream_t s, const moe_bf16_t *x, const int32_t *topk_idx, int64_t T, int k, int E,
+                               int H, const int32_t *counts, const int32_t *group_offsets,
+                               const int32_t *mtile, int32_t *dst_of_route, int32_t *src_of_row, uint8_t *x_q,
+                               uint8_t *x_sf, int64_t rows_cap, uint32_t *err) {
+    const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
+#define MOE_SCATTER_MX(KM)                                                                                   \
+    launch_k(permute_scatter_mx_kernel<KM>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s,               \
+             reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, H, counts, group_offsets, mtile, \
+             dst_of_route, src_of_row, x_q, x_sf, rows_cap, err)
+    if (k <= 1) MOE_SCATTER_MX(1);
+    else if (k <= 2) MOE_SCATTER_MX(2);
+    else if (k <= 4) MOE_SCATTER_MX(4);
+    else if (k <= 8) MOE_SCATTER_MX(8);
+    else if (k <= 16) MOE_SCATTER_MX(16);
+    else MOE_SCATTER_MX(32);
+#undef MOE_SCATTER_MX
+    return launch_status();
+}
+
 }  // namespace
 }  // namespace moe
 
@@ -580,20 +714,8 @@ extern "C" moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *to
     if (count_and_scan(topk_idx, R, E, 1, dst_of_route, counts, group_sizes, group_offsets, mtile,
                        ws_done_counter(ws), err, s) != MOE_OK)
         return MOE_ERR_CUDA;
-    if (T > 0) {
-        const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
-#define MOE_SCATTER_MX(KM)                                                                                   \
-    launch_k(permute_scatter_mx_kernel<KM>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s,               \
-             reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, H, counts, group_offsets, mtile, dst_of_route, \
-             src_of_row, x_q, x_sf, rows_cap, err)
-        if (k <= 1) MOE_SCATTER_MX(1);
-        else if (k <= 2) MOE_SCATTER_MX(2);
-        else if (k <= 4) MOE_SCATTER_MX(4);
-        else if (k <= 8) MOE_SCATTER_MX(8);
-        else if (k <= 16) MOE_SCATTER_MX(16);
-        else MOE_SCATTER_MX(32);
-#undef MOE_SCATTER_MX
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    }
+    if (T > 0 && launch_scatter_mx(s, x, topk_idx, T, k, E, H, counts, group_offsets, mtile, dst_of_route, src_of_row,
+                                   x_q, x_sf, rows_cap, err) != MOE_OK)
+        return MOE_ERR_CUDA;
     return MOE_OK;
 }
