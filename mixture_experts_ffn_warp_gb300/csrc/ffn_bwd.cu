@@ -13,6 +13,7 @@
 // "[Draft][JAX] MoE block optimization": grouped_gemm_dswiglu; "[JAX] Expert
 // Parallelism", commit log: zero-filled wgrad of experts with no tokens.)
 #include "gemm_launch.cuh"
+#include "grouped_gemm_pair.cuh"
 
 using namespace moe;
 using gg::Op;
@@ -112,6 +113,8 @@ moe_status_t check_sizes(int E, int H, int F, int64_t rows_cap, void *ws, size_t
 }
 
 int64_t mblock_bound(int64_t rows_cap, int E) { return (rows_cap + gg::BM - 1) / gg::BM + E; }
+// upper bound of the token blocks of the pair GEMMs over all experts
+int64_t token_block_bound(int64_t rows_cap, int E) { return (rows_cap + gp::BT - 1) / gp::BT + E; }
 
 }  // namespace
 
@@ -207,7 +210,27 @@ extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_b
     moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!dgu || !W_gate || !W_up || !group_offsets || !dx_perm) return MOE_ERR_INVALID_ARG;
-    const int bn = (H % 256 == 0) ? 256 : 128;
+    if (H % 256 == 0) {
+        // CTA pairs: 256 rows of W_gate / W_up (hidden units) x up to 256 tokens per pair tile
+        CUtensorMap tW0, tW1, tX, tOut;
+        if (!tmap_bf16_3d(&tW0, W_gate, F, H, E, 64, 128) || !tmap_bf16_3d(&tW1, W_up, F, H, E, 64, 128) ||
+            !tmap_bf16_2d(&tX, dgu, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F, 64, 128) ||
+            !tmap_store_plain(&tOut, dx_perm, 4, H, rows_cap, H, 32, 16))
+            return MOE_ERR_UNSUPPORTED;
+        gp::Args a{};
+        a.group_offsets = group_offsets;
+        a.E = E;
+        a.K = 2 * F;
+        a.k_split = F;
+        a.N_out = H;
+        a.n_fb = H / 256;
+        a.rows_cap = rows_cap;
+        a.y = dx_perm;
+        a.err = ws_error_word(ws);
+        return gp::launch<gp::Op::DGRAD_FC1>(tW0, tW1, tX, tOut, tOut, a, token_block_bound(rows_cap, E) * a.n_fb,
+                                             (cudaStream_t)stream);
+    }
+    const int bn = 128;
     // A = [dg | du] [rows, 2F] (K-major), B = W_gate[e] / W_up[e] as [H rows][F] (K-major)
     CUtensorMap tA, tB0, tB1, tC;
     if (!tmap_bf16_2d(&tA, dgu, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F, 64, 128) ||
@@ -226,7 +249,6 @@ extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_b
     a.ld0 = H;
     a.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
-    if (bn == 256) return gg::launch<Op::DGRAD_FC1, 256>(tA, tB0, tB1, tC, tC, a, bound, (cudaStream_t)stream);
     return gg::launch<Op::DGRAD_FC1, 128>(tA, tB0, tB1, tC, tC, a, bound, (cudaStream_t)stream);
 }
 

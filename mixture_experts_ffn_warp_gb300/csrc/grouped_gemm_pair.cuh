@@ -42,7 +42,14 @@
 namespace moe {
 namespace gp {
 
-enum class Op : int { FC1, FC2 };
+enum class Op : int { FC1, FC2, DGRAD_FC1 };
+
+// DGRAD_FC1 (the backward's dx_perm = [dg|du] [W_gate; W_up]^T, M = H, K = 2F, fp32 out)
+// reads the weights K-major: their rows are the MMA's M rows.  (The dSwiGLU dgrad stays on
+// the one-CTA kernel: with tokens on N its epilogue must transpose the token-major stash
+// and outputs through shared memory, and measured slower.)
+template <Op OP>
+constexpr bool a_kmajor() { return OP == Op::DGRAD_FC1; }
 
 constexpr int kThreads = 192;
 constexpr int BT = 256;                  // tokens per pair tile (N), 128 rows loaded per CTA
@@ -70,13 +77,14 @@ struct PCfg {
 struct Args {
     const int32_t *group_offsets;   // [E+1]
     int E;
-    int K;             // contraction length: FC1 H, FC2 F
-    int N_out;         // output columns: FC1 F, FC2 H
-    int n_fb;          // feature blocks per expert: FC1 F / 128, FC2 H / 256
+    int K;             // contraction length: FC1 H, FC2 F, DGRAD_FC1 2F
+    int N_out;         // output columns: FC1 F, FC2 H, DGRAD_FC1 H
+    int n_fb;          // feature blocks per expert: FC1 F / 128, others (output columns) / 256
+    int k_split;       // DGRAD_FC1: K index where the weights switch from W_gate to W_up (= F)
     int64_t rows_cap;  // rows of the permuted tensors
     __nv_bfloat16 *h;        // FC1: h [rows, F]
     __nv_bfloat16 *stash;    // FC1: [g | u] bf16 [rows, 2F] (nullable)
-    float *y;                // FC2: y_perm [rows, H]
+    float *y;                // FC2: y_perm [rows, H]; DGRAD_FC1: dx_perm [rows, H]
     // router weight of each row's route applied in the epilogue (padding rows get 0); null = unweighted
     const float *route_w;
     const int32_t *src_of_row;
@@ -93,7 +101,11 @@ struct PTile {
     int n;        // MMA N: nvalid rounded up to 16
 };
 
-// pair tile p -> (expert, feature block, token block); s_start[e] = tiles before expert e
+// pair tile p -> (expert, feature block, token block); s_start[e] = tiles before expert e.
+// An expert's rows are cut into ceil(rows / BT) blocks of equal width (rounded up to 16):
+// an expert of 400 tokens gets blocks of 208 + 192 rather than 256 + 144, so no block is
+// so narrow that its MMAs finish faster than one thread issues them, and the blocks cost
+// alike under the static schedule.
 __device__ __forceinline__ PTile decode(int p, const Args &a, const int *s_off, const int *s_start) {
     int lo = 0, hi = a.E - 1;
     while (lo < hi) {
@@ -104,12 +116,13 @@ __device__ __forceinline__ PTile decode(int p, const Args &a, const int *s_off, 
     t.e = lo;
     const int rows = s_off[lo + 1] - s_off[lo];
     const int ntb = (rows + BT - 1) / BT;
+    const int bs = ((rows + ntb - 1) / ntb + 15) & ~15;   // <= BT
     const int local = p - s_start[lo];
     t.fb = local / ntb;
     const int tb = local - t.fb * ntb;
-    t.t0 = s_off[lo] + tb * BT;
-    const int left = rows - tb * BT;
-    t.nvalid = left < BT ? left : BT;
+    t.t0 = s_off[lo] + tb * bs;
+    const int left = rows - tb * bs;
+    t.nvalid = left < bs ? left : bs;
     t.n = (t.nvalid + 15) & ~15;
     return t;
 }
@@ -159,7 +172,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
     }
     if (warp == 0 && lane == 0) {
         sm100::prefetch_tmap(&tmW0);
-        if constexpr (OP == Op::FC1) sm100::prefetch_tmap(&tmW1);
+        if constexpr (OP == Op::FC1 || OP == Op::DGRAD_FC1) sm100::prefetch_tmap(&tmW1);
         sm100::prefetch_tmap(&tmX);
     }
     if (warp == 1) {
@@ -240,6 +253,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                         const int f0 = tl.fb * 128 + (int)rank * 64;
                         sm100::tma_load_3d_pair(sa, &tmW0, fb_c, f0, k0, tl.e);
                         sm100::tma_load_3d_pair(sa + 8192, &tmW1, fb_c, f0, k0, tl.e);
+                    } else if constexpr (OP == Op::DGRAD_FC1) {
+                        // 128 rows (hidden units) of W_gate [E][H][F] for K < F, then of W_up
+                        const int r0 = tl.fb * 256 + (int)rank * 128;
+                        if (k0 < args.k_split) sm100::tma_load_3d_pair(sa, &tmW0, fb_c, k0, r0, tl.e);
+                        else sm100::tma_load_3d_pair(sa, &tmW1, fb_c, k0 - args.k_split, r0, tl.e);
                     } else {
                         // 128 output columns of W_down [E][K][H]
                         const int c0 = tl.fb * 256 + (int)rank * 128;
@@ -270,9 +288,12 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
         // loop with the descriptor arithmetic inside a one-lane branch issued an MMA every
         // ~170 cycles, below the tensor pipe's rate.
         if (rank == 0) {
-            const uint64_t a_desc0 = sm100::sdesc_sw128(smem_base, 8192, 1024);            // MN-major weights
-            const uint64_t b_desc0 = sm100::sdesc_sw128(smem_base + A_BYTES, 16, 1024);    // K-major tokens
-            constexpr uint64_t A_KSTEP = 2048 >> 4, B_KSTEP = 32 >> 4, STAGE_STEP = STAGE_BYTES >> 4;
+            // weights MN-major (forward) or K-major (dgrad); tokens K-major
+            const uint64_t a_desc0 = a_kmajor<OP>() ? sm100::sdesc_sw128(smem_base, 16, 1024)
+                                                    : sm100::sdesc_sw128(smem_base, 8192, 1024);
+            const uint64_t b_desc0 = sm100::sdesc_sw128(smem_base + A_BYTES, 16, 1024);
+            constexpr uint64_t A_KSTEP = a_kmajor<OP>() ? (32 >> 4) : (2048 >> 4), B_KSTEP = 32 >> 4,
+                               STAGE_STEP = STAGE_BYTES >> 4;
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -282,7 +303,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                 const int p = round_tile(r, cid, G, total);
                 if (p < 0) continue;
                 const PTile tl = decode(p, args, s_off, s_start);
-                const uint32_t idesc = sm100::idesc_bf16(256, tl.n, true, false);
+                const uint32_t idesc = sm100::idesc_bf16(256, tl.n, !a_kmajor<OP>(), false);
                 const bool got_acc =
                     sm100::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, kWaitLimitNs);
                 if (__any_sync(0xFFFFFFFFu, !got_acc)) { ok = false; break; }
@@ -447,7 +468,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                     store_bf16x16(hv, &tmOut, args.h, F, fcol, tl.t0 + tok0, nv);
                 }
                 if (!alive) break;
-            } else {
+            } else {   // FC2 (y_perm) and DGRAD_FC1 (dx_perm): fp32 rows
                 const int H = args.N_out;
                 const int hcol = tl.fb * 256 + (int)rank * 128 + q * 32;   // this warp's 32 output columns
 #pragma unroll 1

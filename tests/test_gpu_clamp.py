@@ -17,6 +17,9 @@ pytestmark = pytest.mark.gpu
 SHAPES = {
     "ragged": (small_shape("ragged", T=300, H=256, F=384, E=5, k=2, backward=True), (-0.3, 0.2, -0.25, 0.25)),
     "many": (small_shape("many", T=512, H=128, F=128, E=64, k=4, skew=True, backward=True), (-np.inf, 0.1, -0.1, 0.15)),
+    # H a multiple of 256: the FC1 dgrad runs on CTA pairs, the 256-wide dSwiGLU dgrad tiles;
+    # ~450 rows per expert, two token blocks each
+    "pairs": (small_shape("pairs", T=900, H=256, F=512, E=4, k=2, backward=True), (-0.3, 0.2, -0.25, 0.25)),
 }
 
 
