@@ -27,8 +27,8 @@
 // h = silu(g) * u for 16 tokens.
 // FC2: CTA c holds output columns 256 fb + 128 c + [0, 128) in its 128 lanes.
 //
-// Tile order: expert, feature block, token block (fastest), so the clusters working at
-// the same time share weight blocks and token rows in the L2.  Cluster i takes in round r
+// Tile order: expert, band of up to 16 token blocks, feature block, token block (fastest), so
+// the clusters working at the same time share weight blocks and token rows in the L2.  Cluster i takes in round r
 // the tile r * G + (i + r) mod G (G clusters): the rotation spreads the cheaper last token
 // blocks of the experts evenly over the clusters.
 // ("Add MoE + expert-parallel Python API surface, PyTorch reference, and tests", Summary:
@@ -101,6 +101,12 @@ struct PTile {
     int n;        // MMA N: nvalid rounded up to 16
 };
 
+// Token blocks per band of the tile order: the ~76 clusters working at once then cover about
+// 5 feature blocks x 16 token blocks of an expert (tens of MB of weights and token rows, held
+// in the L2), instead of one feature block x all token blocks of an expert with many tokens,
+// whose token rows would stream from DRAM again for every feature block.
+constexpr int kBandBlocks = 16;
+
 // pair tile p -> (expert, feature block, token block); s_start[e] = tiles before expert e.
 // An expert's rows are cut into ceil(rows / BT) blocks of equal width (rounded up to 16):
 // an expert of 400 tokens gets blocks of 208 + 192 rather than 256 + 144, so no block is
@@ -117,9 +123,15 @@ __device__ __forceinline__ PTile decode(int p, const Args &a, const int *s_off, 
     const int rows = s_off[lo + 1] - s_off[lo];
     const int ntb = (rows + BT - 1) / BT;
     const int bs = ((rows + ntb - 1) / ntb + 15) & ~15;   // <= BT
+    // within the expert: bands of up to kBandBlocks token blocks, in each band the feature
+    // block outer and the token block fastest
     const int local = p - s_start[lo];
-    t.fb = local / ntb;
-    const int tb = local - t.fb * ntb;
+    const int band_tiles = kBandBlocks * a.n_fb;
+    const int band = local / band_tiles;
+    const int bsz = ntb - band * kBandBlocks < kBandBlocks ? ntb - band * kBandBlocks : kBandBlocks;
+    const int in_band = local - band * band_tiles;
+    t.fb = in_band / bsz;
+    const int tb = band * kBandBlocks + (in_band - t.fb * bsz);
     t.t0 = s_off[lo] + tb * bs;
     const int left = rows - tb * bs;
     t.nvalid = left < bs ? left : bs;
