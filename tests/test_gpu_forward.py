@@ -29,6 +29,10 @@ SMALL = {
     "many": small_shape("many", T=512, H=128, F=128, E=64, k=4, skew=True),
     # ~1000 rows per expert: several 256-token blocks per expert and a ragged last block
     "blocks": small_shape("blocks", T=1500, H=256, F=256, E=3, k=2),
+    # the largest expert count: most of the 1024 experts get 0-3 rows (tiles of 16-token MMAs)
+    "e1024": small_shape("e1024", T=600, H=256, F=256, E=1024, k=4),
+    # ~4700 rows per expert: more than 16 token blocks, so two bands of the pair GEMM's tile order
+    "bands": small_shape("bands", T=7000, H=256, F=256, E=3, k=2),
 }
 
 
