@@ -269,6 +269,41 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
     }
     if (!x_perm || !h || !dy_perm || !dgu) return MOE_ERR_INVALID_ARG;
     const uint64_t rows = (uint64_t)rows_cap;
+    if (H % 256 == 0 && F % 256 == 0 && rows_cap >= 1024 * (int64_t)E) {
+        // CTA pairs (256 x 256 gradient tiles) when the experts hold enough rows that each tile's
+        // K loop outweighs its epilogue (the 32 fp32 columns x 256 rows it stores per CTA)
+        for (int which = 0; which < 2; ++which) {
+            const bool down = which == 0;
+            // dW_down[e] [F, H] = h_e^T dy_e;  [dW_gate | dW_up][e] [H, 2F] = x_e^T [dg | du]_e
+            const moe_bf16_t *A = down ? h : x_perm, *B = down ? dy_perm : dgu;
+            const int M = down ? F : H, N = down ? H : 2 * F;
+            CUtensorMap tA, tB, tC0, tC1;
+            if (!tmap_bf16_2d(&tA, A, M, rows, M, 64, 64) || !tmap_bf16_2d(&tB, B, N, rows, N, 64, 64))
+                return MOE_ERR_UNSUPPORTED;
+            if (down ? !tmap_store_2d(&tC0, dW_down, 4, H, (uint64_t)E * F, H)
+                     : (!tmap_store_2d(&tC0, dW_gate, 4, F, (uint64_t)E * H, F) ||
+                        !tmap_store_2d(&tC1, dW_up, 4, F, (uint64_t)E * H, F)))
+                return MOE_ERR_UNSUPPORTED;
+            if (down) tC1 = tC0;
+            gp::Args a{};
+            a.group_offsets = group_offsets;
+            a.E = E;
+            a.M = M;
+            a.nt_m = M / 256;
+            a.nt_n = N / 256;
+            a.m_fastest = a.nt_m <= a.nt_n ? 1 : 0;   // the smaller dimension fastest: a small L2 working set
+            a.n_split = down ? 0 : F;
+            a.a_rows = reinterpret_cast<const __nv_bfloat16 *>(A);
+            a.lda = M;
+            a.b_rows = reinterpret_cast<const __nv_bfloat16 *>(B);
+            a.ldb = N;
+            a.rows_cap = rows_cap;
+            a.err = ws_error_word(ws);
+            st = gp::launch<gp::Op::WGRAD>(tA, tA, tB, tC0, tC1, a, (int64_t)E * a.nt_m * a.nt_n, s);
+            if (st != MOE_OK) return st;
+        }
+        return MOE_OK;
+    }
     {   // dW_down[e] [F, H] = h_e^T dy_e: A = h (MN-major), B = dy_perm (MN-major)
         const int bn = (H % 256 == 0) ? 256 : 128;
         CUtensorMap tA, tB, tC;

@@ -42,7 +42,7 @@
 namespace moe {
 namespace gp {
 
-enum class Op : int { FC1, FC2, DGRAD_FC1 };
+enum class Op : int { FC1, FC2, DGRAD_FC1, WGRAD };
 
 // DGRAD_FC1 (the backward's dx_perm = [dg|du] [W_gate; W_up]^T, M = H, K = 2F, fp32 out)
 // reads the weights K-major: their rows are the MMA's M rows.  (The dSwiGLU dgrad stays on
@@ -50,6 +50,14 @@ enum class Op : int { FC1, FC2, DGRAD_FC1 };
 // and outputs through shared memory, and measured slower.)
 template <Op OP>
 constexpr bool a_kmajor() { return OP == Op::DGRAD_FC1; }
+
+// WGRAD (the backward's weight gradients, K-grouped: K = the rows of each expert):
+//   dW_down[e] = h_e^T dy_e          M = F, N = H
+//   [dW_gate|dW_up][e] = x_e^T [dg|du]_e   M = H, N = 2F (columns >= F go to dW_up)
+// Both operands come MN-major from the permuted row tensors; the pair MMAs cover the
+// expert's rows in whole 16-row slices loaded by TMA, then one more slice holding the last
+// (rows mod 16) rows zero-padded, written into the stage by the producer warps of both CTAs,
+// so no row of the next expert is ever multiplied.
 
 constexpr int kThreads = 192;
 constexpr int BT = 256;                  // tokens per pair tile (N), 128 rows loaded per CTA
@@ -67,11 +75,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 template <Op OP>
 struct PCfg {
     static constexpr int XBUF_BYTES = OP == Op::FC1 ? 2 * 2 * 2 * 16 * 32 * 4 : 0;
-    static constexpr int SLOT_BYTES = OP == Op::FC1 ? 16 * 64 : 16 * 128;
+    static constexpr int SLOT_BYTES = OP == Op::FC1 ? 16 * 64 : 16 * 128;   // WGRAD: 32 rows x 64 B
     static constexpr int STG_BYTES = 4 * 2 * SLOT_BYTES;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + XBUF_BYTES + STG_BYTES + 1024;   // + alignment slack
-    // with the static tables (~8.4 KB) within the 227 KB a CTA may use
-    static_assert(SMEM_BYTES + 8 * 1024 + 512 <= 232448, "shared memory budget");
+    // WGRAD: the K-tail buffer, outside the ring: 2 operands x 2 MN chunks x 16 K rows x 128 B
+    static constexpr int TAIL_BYTES = OP == Op::WGRAD ? 2 * 2 * 16 * 128 : 0;
+    static constexpr int SMEM_BYTES =
+        STAGES * STAGE_BYTES + XBUF_BYTES + STG_BYTES + TAIL_BYTES + 1024;   // + alignment slack
+    // with the static tables and barriers (9 KB) within the 227 KB a CTA may use
+    static_assert(SMEM_BYTES + 9 * 1024 + 512 <= 232448, "shared memory budget");
 };
 
 struct Args {
@@ -81,6 +92,14 @@ struct Args {
     int N_out;         // output columns: FC1 F, FC2 H, DGRAD_FC1 H
     int n_fb;          // feature blocks per expert: FC1 F / 128, others (output columns) / 256
     int k_split;       // DGRAD_FC1: K index where the weights switch from W_gate to W_up (= F)
+    // WGRAD: rows M of each expert's gradient, 256-blocks along M and N, the tile order
+    // within an expert (M blocks fastest or N blocks fastest), the column where the output
+    // switches to the second matrix (0: none), and the operands' row tensors for the K tail
+    int M, nt_m, nt_n, m_fastest, n_split;
+    const __nv_bfloat16 *a_rows;   // [rows, M]
+    int64_t lda;
+    const __nv_bfloat16 *b_rows;   // [rows, N]
+    int64_t ldb;
     int64_t rows_cap;  // rows of the permuted tensors
     __nv_bfloat16 *h;        // FC1: h [rows, F]
     __nv_bfloat16 *stash;    // FC1: [g | u] bf16 [rows, 2F] (nullable)
@@ -139,6 +158,32 @@ __device__ __forceinline__ PTile decode(int p, const Args &a, const int *s_off, 
     return t;
 }
 
+struct WTile {
+    int e, m0, n0;
+    int row0;     // the expert's first permuted row
+    int rows;     // its rows
+    int full16;   // rows in whole 16-row slices (multiplied by the MMAs)
+    int kblocks;  // 64-row K blocks holding them
+};
+
+__device__ __forceinline__ WTile decode_w(int p, const Args &a, const int *s_off) {
+    WTile t;
+    const int per = a.nt_m * a.nt_n;
+    t.e = p / per;
+    const int l = p - t.e * per;
+    int mb, nb;
+    if (a.m_fastest) { mb = l % a.nt_m; nb = l / a.nt_m; }
+    else { nb = l % a.nt_n; mb = l / a.nt_n; }
+    t.m0 = mb * 256;
+    t.n0 = nb * 256;
+    t.row0 = s_off[t.e];
+    const int r = s_off[t.e + 1] - t.row0;
+    t.rows = r > 0 ? r : 0;
+    t.full16 = t.rows & ~15;
+    t.kblocks = (t.full16 + 63) / 64;
+    return t;
+}
+
 __device__ __forceinline__ float silu(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // Tile of round r for cluster `cid` of G (-1 past the end).
@@ -157,6 +202,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ uint64_t full_bar[STAGES], empty_bar[STAGES], tfull_bar[2], tempty_bar[2], drain_bar;
     __shared__ uint64_t xbar[2][2];   // FC1 exchange: [warp pair][chunk parity], 64 arrivals
+    // WGRAD: both CTAs' K tails written (the first CTA's, 2 arrivals); the tail buffer free
+    // again (each CTA's, the pair MMA's commit)
+    __shared__ uint64_t tail_full, tail_empty;
     __shared__ uint32_t s_tmem_base;
     __shared__ int s_off[kMaxE + 1];
     __shared__ int s_start[kMaxE + 1];
@@ -179,6 +227,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
         }
         sm100::mbar_init(&drain_bar, 1);
         for (int i = 0; i < 4; ++i) sm100::mbar_init(&xbar[i >> 1][i & 1], 64);
+        sm100::mbar_init(&tail_full, 2);
+        sm100::mbar_init(&tail_empty, 1);
         s_abort = 0;
         sm100::fence_mbar_init();
     }
@@ -206,6 +256,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
         const int seg = (E + 31) / 32;
         const int e0 = lane * seg;
         auto tiles_of = [&](int e) {
+            if constexpr (OP == Op::WGRAD) return args.nt_m * args.nt_n;
             int rows = s_off[e + 1] - s_off[e];
             if (rows < 0) rows = 0;
             return ((rows + BT - 1) / BT) * args.n_fb;
@@ -238,7 +289,87 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
     const int kblocks = args.K / 64;
     volatile int *abort = &s_abort;
 
-    if (warp == 0) {
+    if (warp == 0 && OP == Op::WGRAD) {
+        // ============================================================ producer, WGRAD (both CTAs)
+        // Lane 0 issues the TMA loads of the whole 16-row slices: this CTA's 128 gradient rows
+        // (two 64-wide MN chunks of the A rows) and 128 gradient columns (of the B rows), 64
+        // K rows (tokens) per stage.  An expert's last (rows mod 16) rows go into the tail
+        // buffer, written by the whole warp: rows zero-padded to a 16-row slice in the MMA's
+        // swizzled layout, so the pair MMAs never multiply a row of the next expert.  The tail
+        // buffer sits outside the ring, so it takes no stage from the loads' lead over the MMAs.
+        const uint32_t full0 = sm100::cluster_addr(&full_bar[0], 0);
+        const uint32_t tail_full0 = sm100::cluster_addr(&tail_full, 0);
+        uint8_t *tbuf = smem + STAGES * STAGE_BYTES + XBUF_BYTES + PC::STG_BYTES;
+        int stage = 0;
+        uint32_t phase = 0, tphase = 0;
+        int issued = 0;
+        bool ok = true;
+        for (int r = 0; r < rounds && ok; ++r) {
+            const int p = round_tile(r, cid, G, total);
+            if (p < 0) continue;
+            const WTile tl = decode_w(p, args, s_off);
+            const int ntail = tl.rows - tl.full16;
+            const int m0 = tl.m0 + (int)rank * 128, n0 = tl.n0 + (int)rank * 128;
+            // the tail's 2 operands x 2 chunks x 16 K rows x 8 16-byte pieces, 16 per lane: loaded
+            // into registers before the whole slices, so that their latency overlaps those stages
+            uint4 tv[16];
+            {
+                const int64_t trow0 = (int64_t)tl.row0 + tl.full16;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int opnd = i >> 3, j = (i >> 2) & 1, k = 4 * (i & 3) + (lane >> 3), c16 = lane & 7;
+                    tv[i] = make_uint4(0, 0, 0, 0);
+                    if (k < ntail)
+                        tv[i] = __ldg(reinterpret_cast<const uint4 *>(
+                            opnd == 0 ? args.a_rows + (trow0 + k) * args.lda + m0 + j * 64 + c16 * 8
+                                      : args.b_rows + (trow0 + k) * args.ldb + n0 + j * 64 + c16 * 8));
+                }
+            }
+            for (int kb = 0; kb < tl.kblocks; ++kb) {
+                bool got = true;
+                if (lane == 0) got = sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, kWaitLimitNs);
+                if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) { ok = false; break; }
+                if (lane == 0) {
+                    const uint32_t sa = smem_base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+                    const uint32_t fb_c = full0 + (uint32_t)(stage * sizeof(uint64_t));
+                    if (rank == 0) sm100::mbar_arrive_expect_tx(&full_bar[stage], 2 * STAGE_BYTES);
+                    const int krow = tl.row0 + kb * 64;
+                    sm100::tma_load_2d_pair(sa, &tmW0, fb_c, m0, krow);
+                    sm100::tma_load_2d_pair(sa + 8192, &tmW0, fb_c, m0 + 64, krow);
+                    sm100::tma_load_2d_pair(sb, &tmX, fb_c, n0, krow);
+                    sm100::tma_load_2d_pair(sb + 8192, &tmX, fb_c, n0 + 64, krow);
+                }
+                ++issued;
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            if (ntail > 0) {
+                // the previous tail has been multiplied; then the layout the TMA loads give
+                // (128-byte swizzle), with the MN chunks 16 K rows apart
+                bool got = true;
+                if (lane == 0) got = sm100::mbar_wait(&tail_empty, tphase ^ 1u, abort, args.err, kWaitLimitNs);
+                if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) { ok = false; break; }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int opnd = i >> 3, j = (i >> 2) & 1, k = 4 * (i & 3) + (lane >> 3), c16 = lane & 7;
+                    *reinterpret_cast<uint4 *>(tbuf + opnd * 4096 + j * 2048 + k * 128 + ((c16 ^ (k & 7)) << 4)) = tv[i];
+                }
+                sm100::fence_proxy_async_smem();   // the generic writes -> the MMA's async proxy
+                __syncwarp();
+                if (lane == 0) sm100::mbar_arrive_cluster(tail_full0);
+                tphase ^= 1u;
+            }
+        }
+        if (!ok && lane == 0) {
+            int st = stage;
+            uint32_t ph = phase;
+            for (int i = 0; i < STAGES && i < issued; ++i) {
+                if (--st < 0) { st = STAGES - 1; ph ^= 1u; }
+                int dummy = 0;
+                sm100::mbar_wait(&empty_bar[st], ph, &dummy, nullptr, 10000000ull);
+            }
+        }
+    } else if (warp == 0) {
         // ============================================================ producer (both CTAs)
         if (lane == 0) {
             const uint32_t full0 = sm100::cluster_addr(&full_bar[0], 0);   // the first CTA's barriers
@@ -246,7 +377,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int r = 0; r < rounds && ok; ++r) {
+            for (int r = 0; r < rounds && ok && OP != Op::WGRAD; ++r) {
                 const int p = round_tile(r, cid, G, total);
                 if (p < 0) continue;
                 const PTile tl = decode(p, args, s_off, s_start);
@@ -311,7 +442,66 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
             int acc = 0;
             uint32_t acc_phase = 0;
             bool ok = true, issued_any = false;
-            for (int r = 0; r < rounds && ok; ++r) {
+            if constexpr (OP == Op::WGRAD) {
+                // both operands MN-major; only the whole 16-row slices of the expert's rows
+                const uint64_t wa0 = sm100::sdesc_sw128(smem_base, 8192, 1024);
+                const uint64_t wb0 = sm100::sdesc_sw128(smem_base + A_BYTES, 8192, 1024);
+                constexpr uint64_t KSTEP = 2048 >> 4;
+                constexpr uint32_t idesc = sm100::idesc_bf16(256, 256, true, true);
+                // the tail buffer: MN chunks 16 K rows (2048 B) apart
+                const uint32_t tbuf_s = smem_base + STAGES * STAGE_BYTES + PC::XBUF_BYTES + PC::STG_BYTES;
+                const uint64_t ta = sm100::sdesc_sw128(tbuf_s, 2048, 1024);
+                const uint64_t tb = sm100::sdesc_sw128(tbuf_s + 4096, 2048, 1024);
+                uint32_t tphase = 0;
+                for (int r = 0; r < rounds && ok; ++r) {
+                    const int p = round_tile(r, cid, G, total);
+                    if (p < 0) continue;
+                    const WTile tl = decode_w(p, args, s_off);
+                    const int ntail = tl.rows - tl.full16;
+                    if (tl.rows == 0) continue;   // the epilogue writes this tile's zeros alone
+                    const bool got_acc =
+                        sm100::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, kWaitLimitNs);
+                    if (__any_sync(0xFFFFFFFFu, !got_acc)) { ok = false; break; }
+                    sm100::tc_fence_after();
+                    const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BT);
+                    for (int kb = 0; kb < tl.kblocks; ++kb) {
+                        const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, kWaitLimitNs);
+                        if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
+                        sm100::tc_fence_after();
+                        const uint64_t ad = wa0 + (uint64_t)stage * STAGE_STEP;
+                        const uint64_t bd = wb0 + (uint64_t)stage * STAGE_STEP;
+                        const int left = (tl.full16 - kb * 64) >> 4;   // 16-row slices left
+                        const int kk_end = left < 4 ? left : 4;
+                        if (sm100::elect_one()) {
+                            for (int kk = 0; kk < kk_end; ++kk)
+                                sm100::mma_bf16_pair(d_tmem, ad + kk * KSTEP, bd + kk * KSTEP, idesc,
+                                                     (kb | kk) != 0 ? 1u : 0u);
+                            sm100::mma_commit_pair(&empty_bar[stage], 0x3);
+                        }
+                        __syncwarp();
+                        issued_any = true;
+                        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    }
+                    if (!ok) break;
+                    if (ntail > 0) {   // the zero-padded tail written by both producers
+                        const bool got =
+                            sm100::mbar_wait_cluster(&tail_full, tphase, abort, args.err, kWaitLimitNs);
+                        if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
+                        tphase ^= 1u;
+                        sm100::tc_fence_after();
+                        if (sm100::elect_one()) {
+                            sm100::mma_bf16_pair(d_tmem, ta, tb, idesc, tl.kblocks > 0 ? 1u : 0u);
+                            sm100::mma_commit_pair(&tail_empty, 0x3);
+                        }
+                        __syncwarp();
+                        issued_any = true;
+                    }
+                    if (sm100::elect_one()) sm100::mma_commit_pair(&tfull_bar[acc], 0x3);
+                    __syncwarp();
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                }
+            }
+            for (int r = 0; r < rounds && ok && OP != Op::WGRAD; ++r) {
                 const int p = round_tile(r, cid, G, total);
                 if (p < 0) continue;
                 const PTile tl = decode(p, args, s_off, s_start);
@@ -409,6 +599,60 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
         int chunk_parity = 0;
         uint32_t xphase = 0;   // bit b: parity of the next wait on xbar[pair][b]
         bool alive = true;
+        if constexpr (OP == Op::WGRAD) {
+            // this thread's gradient row; 32 fp32 columns at a time staged as 32 rows x 64 B
+            // (64-byte swizzle) and stored by TMA in boxes of 16 columns x 32 rows
+            auto put_w = [&](int j, uint4 v) {
+                *reinterpret_cast<uint4 *>(stg + slot * SLOT_BYTES + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+            };
+            for (int r = 0; r < rounds && alive; ++r) {
+                const int p = round_tile(r, cid, G, total);
+                if (p < 0) continue;
+                const WTile tl = decode_w(p, args, s_off);
+                const bool mma = tl.rows > 0;   // else an expert without rows: exact zeros
+                if (mma) {
+                    const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, kWaitLimitNs);
+                    if (__any_sync(0xFFFFFFFFu, !got)) break;
+                    sm100::tc_fence_after();
+                }
+                const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
+                const int64_t grow0 = (int64_t)tl.e * args.M + tl.m0 + (int)rank * 128 + q * 32;
+#pragma unroll 1
+                for (int c0 = 0; c0 < 256; c0 += 32) {
+                    float v[32];
+                    if (mma) {
+                        uint32_t raw[32];
+                        sm100::tmem_ld32(tacc + c0, raw);
+                        sm100::tmem_ld_wait();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(raw[i]);
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                    }
+                    const int ncol = tl.n0 + c0;
+                    const bool second = args.n_split > 0 && ncol >= args.n_split;
+                    const int col = second ? ncol - args.n_split : ncol;
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf) {
+                        slot_open();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j)
+                            put_w(j, make_uint4(__float_as_uint(v[16 * hf + 4 * j]), __float_as_uint(v[16 * hf + 4 * j + 1]),
+                                                __float_as_uint(v[16 * hf + 4 * j + 2]),
+                                                __float_as_uint(v[16 * hf + 4 * j + 3])));
+                        slot_store(second ? &tmStash : &tmOut, col + 16 * hf, (int)grow0);
+                    }
+                }
+                if (mma) {
+                    sm100::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) sm100::mbar_arrive_cluster(tempty0 + (uint32_t)(acc * sizeof(uint64_t)));
+                    if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                }
+            }
+            alive = false;   // the loop below is the other ops'
+        }
         for (int r = 0; r < rounds && alive; ++r) {
             const int p = round_tile(r, cid, G, total);
             if (p < 0) continue;

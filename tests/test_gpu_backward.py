@@ -10,7 +10,7 @@ import pytest
 import torch
 
 import oracle
-from mixture_experts_ffn_warp_gb300 import MoeBackward, MoeForward, moe_grouped_ffn_bwd
+from mixture_experts_ffn_warp_gb300 import MoeBackward, MoeForward, Workspace, moe_grouped_ffn_bwd, moe_grouped_wgrad
 from mixture_experts_ffn_warp_gb300.synthetic import CONFIGS, small_shape
 from helpers import assert_close_rms, assert_close_ulp, bits, gpu_inputs, host_experts, to_f64
 
@@ -26,6 +26,10 @@ SHAPES = {
     "f1408": small_shape("f1408", T=1024, H=256, F=1408, E=4, k=2, backward=True),
     # many experts, several with no routes
     "many": small_shape("many", T=512, H=128, F=128, E=64, k=4, skew=True, backward=True),
+    # >= 1024 rows per expert: the weight gradients on CTA pairs, with ragged K tails
+    "pair_wgrad": small_shape("pair_wgrad", T=2200, H=256, F=256, E=4, k=2, backward=True),
+    # the same with a Zipf-like load and one expert without routes
+    "pair_wgrad_skew": small_shape("pair_wgrad_skew", T=4500, H=256, F=256, E=8, k=2, skew=True, backward=True),
 }
 
 
@@ -130,3 +134,39 @@ def test_backward_parity_mixtral_full_size_sampled():
         rms = float(t.double().pow(2).mean().sqrt())
         err = max(abs(got[i] - vals[i]) for i in sel_w)
         assert err <= 2e-2 * rms, f"dW[{which}] max|err| {err:.3e} > 2e-2 * RMS {rms:.3e}"
+
+
+def test_wgrad_group_sizes_on_cta_pairs():
+    """moe_grouped_wgrad on chosen group sizes (0 rows, fewer than 16, whole 16-row slices,
+    ragged tails; >= 1024 rows per expert on average, so the CTA-pair kernel runs): each
+    expert's gradients against the fp64 products of its rows."""
+    H, F = 256, 512
+    sizes = [0, 5, 16, 1100, 4077, 1000, 37, 2000]
+    E, R = len(sizes), sum(sizes)
+    assert R >= 1024 * E
+    g = torch.Generator(device="cuda").manual_seed(11)
+    x = torch.randn(R, H, generator=g, device="cuda").to(torch.bfloat16)
+    h = torch.randn(R, F, generator=g, device="cuda").to(torch.bfloat16)
+    dy = torch.randn(R, H, generator=g, device="cuda").to(torch.bfloat16)
+    dgu = torch.randn(R, 2 * F, generator=g, device="cuda").to(torch.bfloat16)
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(sizes)]), dtype=torch.int32, device="cuda")
+    dWg = torch.full((E, H, F), float("nan"), device="cuda")
+    dWu = torch.full((E, H, F), float("nan"), device="cuda")
+    dWd = torch.full((E, F, H), float("nan"), device="cuda")
+    ws = Workspace(R, E, 1)
+    moe_grouped_wgrad(x, h, dy, dgu, offs, ws, dWg, dWu, dWd)
+    torch.cuda.synchronize()
+    assert ws.read_error() == 0
+    xd, hd, dyd, dgud = (t.double().cpu() for t in (x, h, dy, dgu))
+    o = offs.cpu().tolist()
+    for e in range(E):
+        r0, r1 = o[e], o[e + 1]
+        want = {"dW_down": hd[r0:r1].T @ dyd[r0:r1], "dW_gate": xd[r0:r1].T @ dgud[r0:r1, :F],
+                "dW_up": xd[r0:r1].T @ dgud[r0:r1, F:]}
+        for n, got in (("dW_down", dWd[e]), ("dW_gate", dWg[e]), ("dW_up", dWu[e])):
+            got = got.double().cpu()
+            if sizes[e] == 0:
+                assert torch.count_nonzero(got) == 0, (e, n)
+                continue
+            err = (got - want[n]).abs().max().item()
+            assert err <= 1e-4 * want[n].abs().max().item(), (e, n, err)   # fp32 accumulation
