@@ -57,12 +57,18 @@ __device__ __forceinline__ void raise_device_error(uint32_t *err, uint32_t bits)
 // access and before any early return: griddepcontrol.wait blocks until the preceding grid
 // has completed and its writes are visible, so nothing a kernel reads or writes can race
 // with earlier work on the stream.  Only on-chip set-up (mbarriers, TMEM allocation,
-// tensor-map prefetch) runs before it.  No kernel triggers its dependents early
-// (griddepcontrol.launch_dependents): measured on the forward chain, an early trigger let
-// the next grid's CTAs occupy SMs during the whole kernel and cost more than it saved,
-// while the implicit trigger at CTA exit removes most of the launch gap.  Without the
-// launch attribute the wait is a no-op and the launch behaves as an ordinary one.
+// tensor-map prefetch) runs before it.  Only the permutation's counting pass triggers its
+// dependent early (griddepcontrol.launch_dependents, right after its own wait): it runs a
+// few CTAs, so the scatter's CTAs fill the idle SMs and load their token rows meanwhile.
+// Measured on the forward chain, an early trigger in every kernel let the next grid's CTAs
+// occupy SMs during the whole kernel and cost more than it saved, while the implicit
+// trigger at CTA exit removes most of the launch gap.  Without the launch attribute the
+// wait is a no-op and the launch behaves as an ordinary one.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Lets the next kernel on the stream be scheduled before this one ends.  Called after
+// pdl_wait(), so a dependent that starts early knows that every grid before this one has
+// completed: what those grids wrote may be read before the dependent's own wait.
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Kernel launch with programmatic stream serialization (arguments are converted to the
 // kernel's parameter types).

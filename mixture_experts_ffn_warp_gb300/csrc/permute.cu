@@ -244,6 +244,7 @@ permute_count_kernel(const int32_t *__restrict__ topk_idx, int64_t R, int E, int
                      int32_t *__restrict__ group_sizes, int32_t *__restrict__ group_offsets,
                      int32_t *__restrict__ mtile_start, int scan_in_smem, uint32_t *done, uint32_t *err) {
     pdl_wait();
+    pdl_trigger();   // the scatter's CTAs may start loading token rows on the idle SMs
     // [kPermWarps][E] running counts; in the last block, the [chunks][E] count matrix when
     // scan_in_smem (the launch then sizes this array for it)
     extern __shared__ int32_t s_cnt[];
@@ -348,7 +349,12 @@ moe_status_t count_and_scan(const int32_t *topk_idx, int64_t R, int E, int align
     return launch_status();
 }
 
-// One warp per token: maps, then the row copied once into its k rows (KMAX >= k).
+// One warp per token: maps, then the row copied once into its k rows (KMAX >= k).  The
+// kernel runs after the counting pass, which triggers it early: the token row's first
+// 32 * kPreVecs 16-byte vectors are loaded before the wait (x was complete before the counting
+// pass passed its own wait; the loads go to the L2, the point of coherence, past the SM's L1),
+// the maps after it.
+constexpr int kPreVecs = 8;
 template <int KMAX>
 __global__ void __launch_bounds__(kScatterWarps * 32)
 permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
@@ -356,9 +362,16 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
                        const int32_t *__restrict__ chunk_first, int32_t *__restrict__ dst_of_route,
                        int32_t *__restrict__ src_of_row, uint4 *__restrict__ x_perm,
                        int64_t rows_cap, uint32_t *err) {
-    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
+    const uint4 *src = x + (t < T ? t : 0) * row_vecs;
+    uint4 pre[kPreVecs];
+    if (t < T) {
+#pragma unroll
+        for (int u = 0; u < kPreVecs; ++u)
+            if (lane + 32 * u < row_vecs) pre[u] = __ldcg(src + lane + 32 * u);   // from the L2, not L1
+    }
+    pdl_wait();
     if (t >= T) return;
     int my_dst = -1;
     if (lane < k) {
@@ -379,9 +392,17 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
     int dst[KMAX];
 #pragma unroll
     for (int j = 0; j < KMAX; ++j) dst[j] = j < k ? __shfl_sync(0xFFFFFFFFu, my_dst, j) : -1;
-    const uint4 *src = x + t * row_vecs;
+#pragma unroll
+    for (int j = 0; j < KMAX; ++j) {
+        if (j < k && dst[j] >= 0) {
+            uint4 *d = x_perm + (int64_t)dst[j] * row_vecs;
+#pragma unroll
+            for (int u = 0; u < kPreVecs; ++u)
+                if (lane + 32 * u < row_vecs) d[lane + 32 * u] = pre[u];
+        }
+    }
     constexpr int U = 4;   // 16-byte vectors in flight per lane
-    for (int v0 = lane; v0 < row_vecs; v0 += 32 * U) {
+    for (int v0 = lane + 32 * kPreVecs; v0 < row_vecs; v0 += 32 * U) {
         uint4 val[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
