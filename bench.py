@@ -217,6 +217,7 @@ def build_workload(shape, dev, stream):
     active = int((m.perm.group_sizes > 0).sum().item())     # experts whose weights are read
     w["active_experts"] = active
     wbytes = active * H * F * (1 if shape.mxfp8 else 2) * (1 + (1 / 32 if shape.mxfp8 else 0))
+    ysz = m.y_perm.element_size()   # fp32 rows; bf16 on the MXFP8 forward without a backward
 
     g = [Group("route", lambda: m.route(inp["logits"], stream), nbytes=T * E * 4 + R * 8)]
     if shape.mxfp8:
@@ -228,7 +229,7 @@ def build_workload(shape, dev, stream):
                   nbytes=R * H * (1 + 1 / 32) + 2 * wbytes + R * F * (1 + 1 / 32)
                   + (R * 2 * F * 2 if shape.backward else 0), fp8=True),
             Group("fc2_mxfp8", lambda: m.fc2(mw, stream), flop=2.0 * R * H * F,
-                  nbytes=R * F * (1 + 1 / 32) + wbytes + R * H * 4, fp8=True),
+                  nbytes=R * F * (1 + 1 / 32) + wbytes + R * H * ysz, fp8=True),
         ]
     else:
         stash = R * 2 * F * 2 if shape.backward else 0
@@ -238,9 +239,9 @@ def build_workload(shape, dev, stream):
             Group("fc1_swiglu", lambda: m.fc1(inp["W_gate"], inp["W_up"], stream), flop=4.0 * R * H * F,
                   nbytes=R * H * 2 + 2 * wbytes + R * F * 2 + stash),
             Group("fc2", lambda: m.fc2(inp["W_down"], stream), flop=2.0 * R * H * F,
-                  nbytes=R * F * 2 + wbytes + R * H * 4),
+                  nbytes=R * F * 2 + wbytes + R * H * ysz),
         ]
-    g.append(Group("combine", lambda: m.combine(stream), nbytes=R * H * 4 + T * H * 2 + R * 8))
+    g.append(Group("combine", lambda: m.combine(stream), nbytes=R * H * ysz + T * H * 2 + R * 8))
     if shape.backward:
         b = w["bwd"]
         # the backward's weights: bf16 (on the MXFP8 path the values of the MXFP8 codes)

@@ -340,6 +340,12 @@ MOE_API moe_status_t moe_grouped_fc1_swiglu_clamped(const moe_bf16_t *x_perm, co
 MOE_API moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *dst_of_route,
                                    const float *topk_w, int64_t T, int H, int k,
                                    moe_bf16_t *out, moe_stream_t stream);
+/* moe_unpermute_combine over bf16 y_perm rows (moe_grouped_fc2_mxfp8_ybf16): each
+ * slot's values widened to fp32, the same fp32 slot-order sum and bf16 output.
+ * y_perm 16-byte aligned; limits and errors as moe_unpermute_combine. */
+MOE_API moe_status_t moe_unpermute_combine_ybf16(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
+                                                 const float *topk_w, int64_t T, int H, int k,
+                                                 moe_bf16_t *out, moe_stream_t stream);
 
 /* The combine with the output encoded as MXFP8 along H ("Add MoE + expert-parallel
  * Python API surface, PyTorch reference, and tests", Summary: mxfp8 public outputs
@@ -446,6 +452,17 @@ MOE_API moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_
                                            const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H, int F,
                                            int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
                                            moe_stream_t stream);
+/* moe_grouped_fc2_mxfp8 with y_perm stored as bf16 [rows_cap, H] (the fp32
+ * accumulators rounded to nearest even), for moe_unpermute_combine_ybf16.  The
+ * pages' expert outputs are bf16 ("[JAX] Expert Parallelism: JAX primitives +
+ * VJPs", commit log: 2-byte combine slots; the fp32 island around SwiGLU dropped
+ * as wasted bandwidth).  On the MXFP8 path the E4M3 rounding of the operands
+ * dominates the error, and the bf16 rows halve what FC2 writes and the combine
+ * reads.  y_perm 16-byte aligned; limits and errors as moe_grouped_fc2_mxfp8. */
+MOE_API moe_status_t moe_grouped_fc2_mxfp8_ybf16(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
+                                                 const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H,
+                                                 int F, int64_t rows_cap, moe_bf16_t *y_perm, void *ws,
+                                                 size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* A8  Backward                                                         */

@@ -49,6 +49,7 @@ SIGNATURES = {
                                               _sz, _vp]),
     "moe_grouped_fc2_weighted": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_unpermute_combine": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp]),
+    "moe_unpermute_combine_ybf16": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp]),
     "moe_grouped_ffn_bwd": (_st, [_vp] * 12 + [_i64, _int, _int, _int, _int, _i64] + [_vp] * 8 + [_vp, _sz, _vp]),
     "moe_combine_bwd": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _i64, _vp, _vp, _vp]),
     "moe_grouped_dgrad_fc2_dswiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
@@ -72,6 +73,7 @@ SIGNATURES = {
     "moe_unpermute_combine_mxfp8": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp, _vp]),
     "moe_dequantize_weights_mxfp8": (_st, [_vp, _vp, _int, _int, _int, _vp, _vp]),
     "moe_grouped_fc2_mxfp8": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
+    "moe_grouped_fc2_mxfp8_ybf16": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -356,6 +358,24 @@ def moe_unpermute_combine(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk
     return out
 
 
+def moe_unpermute_combine_ybf16(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w,
+                                out=None, stream=None) -> torch.Tensor:
+    """moe_unpermute_combine over bf16 y_perm rows (moe_grouped_fc2_mxfp8_ybf16; moe.h)."""
+    _need(y_perm, "y_perm", torch.bfloat16)
+    H = y_perm.shape[1]
+    dev = y_perm.device
+    _need(dst_of_route, "dst_of_route", torch.int32, None, dev)
+    T, k = dst_of_route.shape
+    if topk_w is not None:
+        _need(topk_w, "topk_w", torch.float32, (T, k), dev)
+    if out is None:
+        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    _need(out, "out", torch.bfloat16, (T, H), dev)
+    _check("moe_unpermute_combine_ybf16", load_library().moe_unpermute_combine_ybf16(
+        _ptr(y_perm), _ptr(dst_of_route), _ptr(topk_w), T, H, k, _ptr(out), _stream(stream)))
+    return out
+
+
 # ------------------------------------------------------------------ A8 backward steps
 
 def moe_combine_bwd(dY, y_perm, perm: "Permutation", topk_w, dy_perm, d_topk_w=None, stream=None):
@@ -545,6 +565,17 @@ def moe_grouped_fc2_mxfp8(h_q, h_sf, Wd_q, Wd_sf, group_offsets, ws: Workspace, 
     E = group_offsets.shape[0] - 1
     H = y_perm.shape[1]
     _check("moe_grouped_fc2_mxfp8", load_library().moe_grouped_fc2_mxfp8(
+        _ptr(h_q), _ptr(h_sf), _ptr(Wd_q), _ptr(Wd_sf), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
+        _ptr(ws.buf), ws.nbytes, _stream(stream)))
+
+
+def moe_grouped_fc2_mxfp8_ybf16(h_q, h_sf, Wd_q, Wd_sf, group_offsets, ws: Workspace, y_perm, stream=None):
+    """A4 on MXFP8 operands, y_perm stored as bf16 (moe.h)."""
+    rows_cap, F = h_q.shape
+    E = group_offsets.shape[0] - 1
+    _need(y_perm, "y_perm", torch.bfloat16, None, h_q.device)
+    H = y_perm.shape[1]
+    _check("moe_grouped_fc2_mxfp8_ybf16", load_library().moe_grouped_fc2_mxfp8_ybf16(
         _ptr(h_q), _ptr(h_sf), _ptr(Wd_q), _ptr(Wd_sf), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
         _ptr(ws.buf), ws.nbytes, _stream(stream)))
 

@@ -1,7 +1,7 @@
 // combine.cu -- A5: weighted unpermute / combine back to token order.
 //
 // One warp per token; each lane owns 8-column slices of the row (two 16-byte
-// fp32 loads per slot, one 16-byte bf16 store) and accumulates
+// fp32 loads per slot, or one of bf16 rows; one 16-byte bf16 store) and accumulates
 // w_j * y_perm[dst_j] over the k slots in slot order in fp32.  All slot loads
 // of a slice are issued before the FMAs, and each lane keeps several slices
 // in flight.  ("Add MoE + expert-parallel Python API surface, PyTorch
@@ -37,9 +37,45 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
     return r;
 }
 
-template <int KMAX>
+// An 8-column slice of a y_perm row as loaded (two 16-byte fp32 loads, or one 16-byte load of
+// bf16 values, widened only at the FMA), and the slices each lane keeps in flight: as many
+// bytes per lane for bf16 rows as for fp32 ones.
+template <typename Y>
+struct Slice;
+template <>
+struct Slice<float4> {
+    using Raw = F8;
+    template <int KMAX>
+    static constexpr int kInFlight = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);
+    __device__ static Raw load(const float4 *y, int64_t slice) {
+        Raw v;
+        v.a = __ldg(y + slice * 2);
+        v.b = __ldg(y + slice * 2 + 1);
+        return v;
+    }
+    __device__ static void fma(float (&acc)[8], float w, const Raw &v) { fma8(acc, w, v); }
+};
+template <>
+struct Slice<uint4> {
+    using Raw = uint4;
+    template <int KMAX>
+    static constexpr int kInFlight = KMAX <= 2 ? 8 : (KMAX <= 4 ? 4 : (KMAX <= 8 ? 2 : 1));
+    __device__ static Raw load(const uint4 *y, int64_t slice) { return __ldg(y + slice); }
+    __device__ static void fma(float (&acc)[8], float w, const Raw &raw) {
+        const __nv_bfloat162 *p = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 f = __bfloat1622float2(p[i]);
+            acc[2 * i] = fmaf(w, f.x, acc[2 * i]);
+            acc[2 * i + 1] = fmaf(w, f.y, acc[2 * i + 1]);
+        }
+    }
+};
+
+// Y = float4 (fp32 y_perm rows) or uint4 (bf16 rows, the MXFP8 forward's option).
+template <int KMAX, typename Y>
 __global__ void __launch_bounds__(kCombineWarps * 32)
-combine_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ dst_of_route,
+combine_kernel(const Y *__restrict__ y_perm, const int32_t *__restrict__ dst_of_route,
                const float *__restrict__ topk_w, int64_t T, int k, int slices,
                uint4 *__restrict__ out) {
     pdl_wait();
@@ -60,36 +96,34 @@ combine_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ ds
         w[j] = __shfl_sync(0xFFFFFFFFu, my_w, j);
         if (j >= k) dst[j] = -1;
     }
-    constexpr int U = KMAX <= 2 ? 4 : (KMAX <= 4 ? 2 : 1);   // slices in flight per lane
+    using S = Slice<Y>;
+    constexpr int U = S::template kInFlight<KMAX>;   // slices in flight per lane
     for (int s0 = lane; s0 < slices; s0 += 32 * U) {
-        F8 val[U][KMAX];
+        typename S::Raw val[U][KMAX];
 #pragma unroll
         for (int u = 0; u < U; ++u)
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (dst[j] >= 0 && s0 + 32 * u < slices) {
-                    const float4 *src = y_perm + ((int64_t)dst[j] * slices + s0 + 32 * u) * 2;
-                    val[u][j].a = __ldg(src);
-                    val[u][j].b = __ldg(src + 1);
-                }
+                if (dst[j] >= 0 && s0 + 32 * u < slices)
+                    val[u][j] = S::load(y_perm, (int64_t)dst[j] * slices + s0 + 32 * u);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (s0 + 32 * u >= slices) break;
             float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (dst[j] >= 0) fma8(acc, w[j], val[u][j]);
+                if (dst[j] >= 0) S::fma(acc, w[j], val[u][j]);
             out[t * slices + s0 + 32 * u] = pack8(acc);
         }
     }
 }
 
-template <int KMAX>
-cudaError_t launch(const float *y, const int32_t *dst, const float *w, int64_t T, int k, int slices,
+template <int KMAX, typename Y>
+cudaError_t launch(const Y *y, const int32_t *dst, const float *w, int64_t T, int k, int slices,
                    moe_bf16_t *out, cudaStream_t s) {
     const int64_t blocks = (T + kCombineWarps - 1) / kCombineWarps;
-    launch_k(combine_kernel<KMAX>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
-             reinterpret_cast<const float4 *>(y), dst, w, T, k, slices, reinterpret_cast<uint4 *>(out));
+    launch_k(combine_kernel<KMAX, Y>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s, y, dst, w, T, k,
+             slices, reinterpret_cast<uint4 *>(out));
     return cudaGetLastError();
 }
 
@@ -161,8 +195,9 @@ cudaError_t launch_mx(const float *y, const int32_t *dst, const float *w, int64_
 
 }  // namespace
 
-cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int64_t T, int H, int k,
-                         moe_bf16_t *out, cudaStream_t s) {
+template <typename Y>
+cudaError_t combine_rows_t(const Y *y, const int32_t *dst, const float *w, int64_t T, int H, int k,
+                           moe_bf16_t *out, cudaStream_t s) {
     const int sl = H / 8;
     if (k <= 1) return launch<1>(y, dst, w, T, k, sl, out, s);
     if (k <= 2) return launch<2>(y, dst, w, T, k, sl, out, s);
@@ -170,6 +205,11 @@ cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int
     if (k <= 8) return launch<8>(y, dst, w, T, k, sl, out, s);
     if (k <= 16) return launch<16>(y, dst, w, T, k, sl, out, s);
     return launch<32>(y, dst, w, T, k, sl, out, s);
+}
+
+cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int64_t T, int H, int k,
+                         moe_bf16_t *out, cudaStream_t s) {
+    return combine_rows_t(reinterpret_cast<const float4 *>(y), dst, w, T, H, k, out, s);
 }
 
 }  // namespace moe
@@ -182,6 +222,17 @@ extern "C" moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t
     if (T == 0) return MOE_OK;
     if (!y_perm || !dst_of_route || !out) return MOE_ERR_INVALID_ARG;   // topk_w may be null: plain sum
     return moe::cuda_status(moe::combine_rows(y_perm, dst_of_route, topk_w, T, H, k, out, (cudaStream_t)stream));
+}
+
+extern "C" moe_status_t moe_unpermute_combine_ybf16(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
+                                                    const float *topk_w, int64_t T, int H, int k,
+                                                    moe_bf16_t *out, moe_stream_t stream) {
+    if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
+    if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+    if (T == 0) return MOE_OK;
+    if (!y_perm || !dst_of_route || !out) return MOE_ERR_INVALID_ARG;   // topk_w may be null: plain sum
+    return moe::cuda_status(moe::combine_rows_t(reinterpret_cast<const uint4 *>(y_perm), dst_of_route, topk_w, T,
+                                                H, k, out, (cudaStream_t)stream));
 }
 
 extern "C" moe_status_t moe_unpermute_combine_mxfp8(const float *y_perm, const int32_t *dst_of_route,

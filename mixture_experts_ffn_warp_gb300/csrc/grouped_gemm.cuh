@@ -66,7 +66,7 @@ struct Args {
     int k_split;      // DGRAD_FC1: K index where B switches from W_gate to W_up (= F)
     int n_split;      // WGRAD_GATEUP: column where output switches from out0 to out1 (= F)
     int64_t rows_cap; // rows of the permuted tensors
-    __nv_bfloat16 *out0;   // FC1: h; DSWIGLU: [dg | du]
+    __nv_bfloat16 *out0;   // FC1: h; DSWIGLU: [dg | du]; FC2_MX: y_perm in bf16 (else out_f32)
     float *out_f32;        // FC2: y_perm; DGRAD_FC1: dx_perm; WGRAD: dW_down / dW_gate (row pitch ld0)
     int64_t ld0;
     __nv_bfloat16 *out1;   // FC1, FC1_MX: fc1_c stash (nullable)
@@ -702,6 +702,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                 }
             } else {   // FC2, FC2_MX (y_perm) and DGRAD_FC1 (dx_perm): fp32 rows of the group
+                       // (FC2_MX with out0 set: bf16 rows)
                 static_assert(OP == Op::FC2 || OP == Op::FC2_MX || OP == Op::DGRAD_FC1, "unhandled op");
                 const int64_t row = tl.m0 + r;
                 const bool valid = row < tl.m_end && row < args.rows_cap;
@@ -721,8 +722,16 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     const int n = tl.n0 + c;
                     if (n < args.N) {
-                        if (whole) stage_f32x32(d, &tmC0, n, wrow0);
-                        else if (valid) store_f32x32(args.out_f32 + row * args.ld0 + n, d);
+                        if (OP == Op::FC2_MX && args.out0) {
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(d[i]);
+                            if (whole) stage_bf16x32(v, &tmC0, n, wrow0);
+                            else if (valid) store_bf16x32(args.out0 + row * args.ld0 + n, v);
+                        } else {
+                            if (whole) stage_f32x32(d, &tmC0, n, wrow0);
+                            else if (valid) store_f32x32(args.out_f32 + row * args.ld0 + n, d);
+                        }
                     }
                 }
             }

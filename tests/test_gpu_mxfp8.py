@@ -11,7 +11,7 @@ import torch
 import oracle
 from mixture_experts_ffn_warp_gb300 import (MoeForwardMX, MxWeights, Workspace, moe_grouped_quantize_mxfp8,
                                             moe_permute, moe_permute_mxfp8, moe_quantize_weights_mxfp8,
-                                            moe_route_topk)
+                                            moe_route_topk, moe_unpermute_combine)
 from mixture_experts_ffn_warp_gb300.synthetic import CONFIGS, small_shape
 from helpers import TOL_MXFP8, assert_close_rms, bits, gpu_inputs, to_f64
 
@@ -184,3 +184,25 @@ def test_mxfp8_forward_dsv3_full_size_sampled():
     ref = oracle.moe_fwd_mxfp8(bits(inp["x"]), q["gq"], q["gs"], q["uq"], q["us"], q["dq"], q["ds"], idx, tw,
                                tokens=toks, round_mode=2)
     assert_close_rms(to_f64(out[torch.from_numpy(toks).cuda()]), ref["out"], tol=TOL_MXFP8, what="dsv3 out", bf16_out=True)
+
+
+def test_mxfp8_bf16_y_perm_is_the_rounded_fp32_one():
+    """The MXFP8 forward stores y_perm in bf16 unless it keeps what the backward reads:
+    the same inputs through both layers give the bf16 rows as the round-to-nearest-even
+    of the fp32 rows, bit for bit, and the combine over bf16 rows equals the fp32
+    combine of the same values widened (one fp32 slot-order sum)."""
+    shape = small_shape("ybf16", T=600, H=256, F=384, E=6, k=3, mxfp8=True)
+    inp = gpu_inputs(shape, with_dy=False)
+    w = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"])
+    m16 = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k)
+    m32 = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k, keep_fc1_c=True)
+    assert m16.y_perm.dtype == torch.bfloat16 and m32.y_perm.dtype == torch.float32
+    out16 = m16(inp["x"], inp["logits"], w)
+    m32(inp["x"], inp["logits"], w)
+    torch.cuda.synchronize()
+    assert m16.ws.read_error() == 0 and m32.ws.read_error() == 0
+    rows = int(m16.perm.group_offsets[-1].item())
+    assert rows == shape.T * shape.k
+    assert torch.equal(m16.y_perm[:rows], m32.y_perm[:rows].to(torch.bfloat16))
+    ref = moe_unpermute_combine(m16.y_perm.float(), m16.perm.dst_of_route, m16.topk_w)
+    assert torch.equal(out16, ref)
