@@ -1,5 +1,6 @@
 // grouped_gemm_pair.cuh -- the expert FFN's forward GEMMs (FC1 + SwiGLU, FC2) on CTA
-// pairs, with the routed tokens on the MMA's N axis.
+// pairs, with the routed tokens on the MMA's N axis; the backward's FC1 dgrad and weight
+// gradients on the same kernel (below).
 //
 // Each thread-block cluster of two CTAs (one per SM of an SM pair) computes one pair tile
 // at a time: 256 expert-weight rows (M, 128 per CTA) x up to 256 tokens (N) of one
@@ -56,8 +57,8 @@ constexpr bool a_kmajor() { return OP == Op::DGRAD_FC1; }
 //   [dW_gate|dW_up][e] = x_e^T [dg|du]_e   M = H, N = 2F (columns >= F go to dW_up)
 // Both operands come MN-major from the permuted row tensors; the pair MMAs cover the
 // expert's rows in whole 16-row slices loaded by TMA, then one more slice holding the last
-// (rows mod 16) rows zero-padded, written into the stage by the producer warps of both CTAs,
-// so no row of the next expert is ever multiplied.
+// (rows mod 16) rows zero-padded, written by the producer warps of both CTAs into an 8 KB
+// tail buffer outside the ring, so no row of the next expert is ever multiplied.
 
 constexpr int kThreads = 192;
 constexpr int BT = 256;                  // tokens per pair tile (N), 128 rows loaded per CTA
