@@ -65,6 +65,13 @@ typedef enum {
 #define MOE_DEVERR_TIMEOUT       0x2u  /* a bounded device wait gave up; outputs are invalid */
 #define MOE_DEVERR_CAPACITY      0x4u  /* routed rows exceed rows_cap; extra rows not written */
 
+/* Alignment: the kernels move 16-byte vectors.  The row tensors of moe_permute (x, x_perm),
+ * moe_permute_static_scratch, moe_unpermute_combine(_ybf16) (y_perm, out), moe_combine_bwd
+ * (dY, y_perm, dy_perm), moe_unpermute_sum (dx_perm, dx), moe_grouped_quantize_mxfp8 (in,
+ * data) and moe_quantize_weights_mxfp8 (data) must start on a 16-byte boundary; the
+ * GEMMs' operands and outputs must too (their TMA descriptors).  A misaligned pointer gives
+ * MOE_ERR_UNSUPPORTED before anything is launched. */
+
 /* Human-readable name of a status (static storage). */
 MOE_API const char *moe_status_string(moe_status_t status);
 

@@ -221,6 +221,7 @@ extern "C" moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t
     if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!y_perm || !dst_of_route || !out) return MOE_ERR_INVALID_ARG;   // topk_w may be null: plain sum
+    if (!moe::all_aligned16({y_perm, out})) return MOE_ERR_UNSUPPORTED;
     return moe::cuda_status(moe::combine_rows(y_perm, dst_of_route, topk_w, T, H, k, out, (cudaStream_t)stream));
 }
 
@@ -231,6 +232,7 @@ extern "C" moe_status_t moe_unpermute_combine_ybf16(const moe_bf16_t *y_perm, co
     if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!y_perm || !dst_of_route || !out) return MOE_ERR_INVALID_ARG;   // topk_w may be null: plain sum
+    if (!moe::all_aligned16({y_perm, out})) return MOE_ERR_UNSUPPORTED;
     return moe::cuda_status(moe::combine_rows_t(reinterpret_cast<const uint4 *>(y_perm), dst_of_route, topk_w, T,
                                                 H, k, out, (cudaStream_t)stream));
 }

@@ -1,6 +1,8 @@
 // common.cuh -- shared host/device helpers of the CUDA path (not part of the ABI).
 #pragma once
 
+#include <initializer_list>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -19,6 +21,14 @@ constexpr int kPermSteps = 8;
 constexpr int kPermChunk = kPermWarps * 32 * kPermSteps;   // 2048 routes
 
 inline int64_t perm_chunks(int64_t R) { return (R + kPermChunk - 1) / kPermChunk; }
+
+// True when every pointer is 16-byte aligned (null counts as aligned): the row kernels move
+// 16-byte vectors, so an entry point returns MOE_ERR_UNSUPPORTED before launching on anything else.
+inline bool all_aligned16(std::initializer_list<const void *> ps) {
+    for (const void *p : ps)
+        if (reinterpret_cast<uintptr_t>(p) % 16) return false;
+    return true;
+}
 
 // Workspace layout after the header: per-chunk expert counts, then (for the
 // MXFP8 path) each group's first 128-row M-tile id, [E+1] int32.

@@ -127,6 +127,7 @@ extern "C" moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const float *y_per
     if (k < 1 || k > 32 || H % 8 != 0 || E > gg::kMaxE) return MOE_ERR_UNSUPPORTED;
     if (!group_sizes || !group_offsets || !dy_perm) return MOE_ERR_INVALID_ARG;
     if (T > 0 && (!dY || !dst_of_route || !topk_w || (d_topk_w && !y_perm))) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({dY, y_perm, dy_perm})) return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
     if (T > 0) {
         cudaError_t e;
@@ -359,6 +360,7 @@ extern "C" moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *d
     if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
     if (!dx_perm || !dst_of_route || !dx) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({dx_perm, dx})) return MOE_ERR_UNSUPPORTED;
     return cuda_status(combine_rows(dx_perm, dst_of_route, nullptr, T, H, k, dx, (cudaStream_t)stream));
 }
 

@@ -468,6 +468,7 @@ extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx
     if (rows_cap >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
     if (T > 0 && (!x || !topk_idx || !x_perm || !dst_of_route || !src_of_row))
         return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({x, x_perm})) return MOE_ERR_UNSUPPORTED;
     const size_t need = moe_workspace_bytes(T, E, k);
     if (!ws || ws_bytes < need || need == 0) return MOE_ERR_WORKSPACE;
 
@@ -550,6 +551,7 @@ extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const in
     if (rows_cap >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
     if (T > 0 && (!x || !topk_idx || !x_perm || !dst_of_route || !src_of_row))
         return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({x, x_perm})) return MOE_ERR_UNSUPPORTED;
     const int64_t chunks = perm_chunks(R);
     if (kWsHeaderBytes + (size_t)chunks * (size_t)E * sizeof(int32_t) > kStaticScratchBytes)
         return MOE_ERR_UNSUPPORTED;   // problem needs more than the fixed scratch array

@@ -169,6 +169,7 @@ extern "C" moe_status_t moe_grouped_quantize_mxfp8(const moe_bf16_t *in, int64_t
     if (K % 128 != 0 || rows >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
     if (rows == 0) return MOE_OK;
     if (!in || !data || (!scale_rowmajor && !scale_tiles)) return MOE_ERR_INVALID_ARG;
+    if (!all_aligned16({in, data})) return MOE_ERR_UNSUPPORTED;
     if (scale_tiles && (!group_offsets || G < 1 || G > 1024)) return MOE_ERR_INVALID_ARG;
     if (scale_tiles && (!ws || ws_bytes < kWsHeaderBytes + (size_t)(G + 1) * sizeof(int32_t))) return MOE_ERR_WORKSPACE;
     cudaStream_t s = (cudaStream_t)stream;
@@ -187,6 +188,7 @@ extern "C" moe_status_t moe_quantize_weights_mxfp8(const moe_bf16_t *W, int E, i
     if (E < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
     if (K % 128 != 0 || N % 128 != 0 || E > 65535 || K / 32 > 65535) return MOE_ERR_UNSUPPORTED;
     if (!W || !data || !scales) return MOE_ERR_INVALID_ARG;
+    if (!moe::all_aligned16({data})) return MOE_ERR_UNSUPPORTED;   // 16-byte stores of the code blocks
     dim3 grid(N / 64, K / 32, E);
     moe::launch_k(moe::quantize_weights_kernel, grid, dim3(64), 0, (cudaStream_t)stream,
                   reinterpret_cast<const __nv_bfloat16 *>(W), K, N, data, scales);

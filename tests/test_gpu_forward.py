@@ -251,3 +251,33 @@ def test_every_token_to_every_expert():
     hb = {n: bits(inp[n]) for n in ("x", "W_gate", "W_up", "W_down")}
     ref = oracle.moe_fwd(hb["x"], hb["W_gate"], hb["W_up"], hb["W_down"], idx, w, round_mode=2)
     assert_close_rms(to_f64(out), ref["out"], what="k = E out", bf16_out=True)
+
+
+def test_misaligned_row_pointers_are_refused_before_launch():
+    """Entry points whose kernels move 16-byte vectors return MOE_ERR_UNSUPPORTED for a
+    row pointer off a 16-byte boundary, without launching (the error word stays 0)."""
+    import ctypes as C
+    from mixture_experts_ffn_warp_gb300 import Workspace, _binding
+    L = _binding.load_library()
+    T, H, E, k = 64, 128, 8, 2
+    dev = torch.device("cuda")
+    x = torch.zeros(T * H + 8, dtype=torch.bfloat16, device=dev)
+    xp = torch.zeros(T * k * H + 8, dtype=torch.bfloat16, device=dev)
+    idx = torch.zeros(T, k, dtype=torch.int32, device=dev)
+    maps = [torch.zeros(n, dtype=torch.int32, device=dev) for n in (T * k, T * k, E, E + 1)]
+    ws = Workspace(T, E, k)
+    off = lambda t, b: C.c_void_p(t.data_ptr() + b)   # noqa: E731
+    unsupported = 2
+    st = L.moe_permute(off(x, 2), C.c_void_p(idx.data_ptr()), T, H, E, k, 1, C.c_void_p(xp.data_ptr()), T * k,
+                       *[C.c_void_p(m.data_ptr()) for m in maps], C.c_void_p(ws.buf.data_ptr()), ws.nbytes, None)
+    assert st == unsupported
+    y = torch.zeros(T * k * H + 4, dtype=torch.float32, device=dev)
+    out = torch.zeros(T * H + 8, dtype=torch.bfloat16, device=dev)
+    st = L.moe_unpermute_combine(off(y, 4), C.c_void_p(maps[0].data_ptr()), None, T, H, k,
+                                 C.c_void_p(out.data_ptr()), None)
+    assert st == unsupported
+    st = L.moe_unpermute_combine_ybf16(C.c_void_p(xp.data_ptr()), C.c_void_p(maps[0].data_ptr()), None, T, H, k,
+                                       off(out, 8), None)
+    assert st == unsupported
+    torch.cuda.synchronize()
+    assert ws.read_error() == 0
