@@ -97,6 +97,15 @@ def test_host_validation_before_launch(lib):
     # combine
     assert lib.moe_unpermute_combine(nul, nul, nul, 3, 12, 2, nul, nul) == 2
     assert lib.moe_unpermute_combine(nul, nul, nul, 3, 16, 2, nul, nul) == 1
+    # row pointers off a 16-byte boundary (the kernels move 16-byte vectors): refused
+    # before the workspace check and before any launch
+    mis = C.c_void_p(24)
+    assert lib.moe_permute(mis, fake, 4, 16, 4, 2, 1, fake, 8, fake, fake, fake, fake, nul, 0, nul) == 2
+    assert lib.moe_permute(fake, fake, 4, 16, 4, 2, 1, mis, 8, fake, fake, fake, fake, nul, 0, nul) == 2
+    assert lib.moe_unpermute_combine(mis, fake, nul, 3, 16, 2, fake, nul) == 2
+    assert lib.moe_unpermute_combine(fake, fake, nul, 3, 16, 2, mis, nul) == 2
+    assert lib.moe_unpermute_combine_ybf16(mis, fake, nul, 3, 16, 2, fake, nul) == 2
+    assert lib.moe_unpermute_sum(mis, fake, 3, 16, 2, fake, nul) == 2
 
 
 def test_product_path_has_no_oracle_dependency():
