@@ -351,11 +351,10 @@ moe_status_t count_and_scan(const int32_t *topk_idx, int64_t R, int E, int align
 
 // One warp per token: maps, then the row copied once into its k rows (KMAX >= k).  The
 // kernel runs after the counting pass, which triggers it early: the token row's first
-// 32 * kPreVecs 16-byte vectors are loaded before the wait (x was complete before the counting
+// 32 * PRE 16-byte vectors are loaded before the wait (x was complete before the counting
 // pass passed its own wait; the loads go to the L2, the point of coherence, past the SM's L1),
-// the maps after it.
-constexpr int kPreVecs = 8;
-template <int KMAX>
+// the maps after it.  PRE = 8 (4 KB rows: H <= 2048), 16 for wider rows.
+template <int KMAX, int PRE>
 __global__ void __launch_bounds__(kScatterWarps * 32)
 permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
                        int64_t T, int k, int E, int row_vecs,
@@ -365,10 +364,10 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
     const uint4 *src = x + (t < T ? t : 0) * row_vecs;
-    uint4 pre[kPreVecs];
+    uint4 pre[PRE];
     if (t < T) {
 #pragma unroll
-        for (int u = 0; u < kPreVecs; ++u)
+        for (int u = 0; u < PRE; ++u)
             if (lane + 32 * u < row_vecs) pre[u] = __ldcg(src + lane + 32 * u);   // from the L2, not L1
     }
     pdl_wait();
@@ -397,12 +396,12 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
         if (j < k && dst[j] >= 0) {
             uint4 *d = x_perm + (int64_t)dst[j] * row_vecs;
 #pragma unroll
-            for (int u = 0; u < kPreVecs; ++u)
+            for (int u = 0; u < PRE; ++u)
                 if (lane + 32 * u < row_vecs) d[lane + 32 * u] = pre[u];
         }
     }
     constexpr int U = 4;   // 16-byte vectors in flight per lane
-    for (int v0 = lane + 32 * kPreVecs; v0 < row_vecs; v0 += 32 * U) {
+    for (int v0 = lane + 32 * PRE; v0 < row_vecs; v0 += 32 * U) {
         uint4 val[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
@@ -423,8 +422,11 @@ void launch_scatter(int64_t blocks, cudaStream_t s, const uint4 *x, const int32_
                     int E, int row_vecs, const int32_t *chunk_first, int32_t *dst_of_route, int32_t *src_of_row,
                     uint4 *x_perm, int64_t rows_cap, uint32_t *err) {
 #define MOE_SCATTER(KM)                                                                                        \
-    launch_k(permute_scatter_kernel<KM>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s, x, topk_idx, T, k, \
-             E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, err)
+    (row_vecs > 256                                                                                            \
+         ? launch_k(permute_scatter_kernel<KM, 16>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s, x,   \
+                    topk_idx, T, k, E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, err)   \
+         : launch_k(permute_scatter_kernel<KM, 8>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s, x,    \
+                    topk_idx, T, k, E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, err))
     if (k <= 1) MOE_SCATTER(1);
     else if (k <= 2) MOE_SCATTER(2);
     else if (k <= 4) MOE_SCATTER(4);
