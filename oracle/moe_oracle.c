@@ -25,12 +25,16 @@
  *     (same cudnn-frontend page, BlockScaledTensor: block_size 32 for mxfp8).
  *
  * Arithmetic is double.  round_mode = 1 rounds to bf16 exactly where the
- * GPU path stores a bf16 tensor (h, out, dy_perm, dg/du, dx; the expert output
- * y, dx_perm and the weight gradients are fp32 on the path and are not
- * rounded here);
+ * GPU path stores a bf16 tensor (h, the expert output y, out, dy_perm, dg/du,
+ * dx; dx_perm and the weight gradients are fp32 on the path and are not
+ * rounded here).  The rounding points of the forward are the benchmark
+ * configuration's: h = bf16(silu(g) u) and y = bf16(h W_down), the pages'
+ * expert outputs travelling in 2-byte slots ("[JAX] Expert Parallelism: JAX
+ * primitives + VJPs", commit log: the fp32 island around silu and multiply
+ * dropped, bf16 combine slots);
  * round_mode = 0 keeps every intermediate in double (used to pin the
  * formulas against fp64 autograd); round_mode = 2 rounds the stored
- * intermediates (h, dy_perm, dg/du) but returns the final
+ * intermediates (h, y, dy_perm, dg/du) but returns the final
  * outputs (out, dx, dW) unrounded, so that a bf16 output of the GPU can be
  * compared with the exact value of the same arithmetic.  Readings of points the pages leave open
  * (tie-break, NaN order, MX scale rule) are stated at each function.
@@ -470,15 +474,15 @@ static double swiglu(double g, double u)
     return silu(clamp_to(g, g_gate_lo, g_gate_hi)) * clamp_to(u, g_up_lo, g_up_hi);
 }
 
-/* g = x Wg, u = x Wu (double), h = silu(g) * u (bf16 in round_mode 1),
- * y = h Wd (kept unrounded: the path stores y in fp32).  Wg, Wu are [H,F];
- * Wd is [F,H]. */
-/* One route through one expert: g, u, h = rnd(hw * silu(g) * u) and y = h Wd (hw = 1
- * except when the router weight is applied in the FC1 epilogue).  h_mx != 0: the
- * MXFP8 forward's h instead, hw * silu(g) * u quantised to MXFP8 along F and
- * dequantised (in every round mode: the quantisation is part of that forward). */
+/* One route through one expert: g = x Wg, u = x Wu (double), h = rnd(hw * silu(g) * u)
+ * and y = rnd(yw * (h Wd)), both stored bf16 on the path (rounded in round_mode 1
+ * and 2).  hw = w when the router weight is applied in the FC1 epilogue, yw = w when
+ * it is applied in the FC2 epilogue (the fp32 product is what the path rounds), else
+ * 1.  h_mx != 0: the MXFP8 forward's h instead, hw * silu(g) * u quantised to MXFP8
+ * along F and dequantised (in every round mode: the quantisation is part of that
+ * forward).  Wg, Wu are [H,F]; Wd is [F,H]. */
 static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t *Wu,
-                         const uint16_t *Wd, int H, int F, int round_mode, double hw, int h_mx,
+                         const uint16_t *Wd, int H, int F, int round_mode, double hw, double yw, int h_mx,
                          double *g, double *u, double *h, double *y)
 {
     for (int f = 0; f < F; ++f) { g[f] = 0.0; u[f] = 0.0; }
@@ -501,7 +505,7 @@ static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t 
         const uint16_t *wd = Wd + (int64_t)f * H;
         for (int n = 0; n < H; ++n) y[n] += h[f] * oracle_bf16_to_double(wd[n]);
     }
-
+    for (int n = 0; n < H; ++n) y[n] = rnd(yw * y[n], round_mode);
 }
 
 /* ------------------------------------------------------------------ */
@@ -519,10 +523,11 @@ static void expert_route(const uint16_t *xr, const uint16_t *Wg, const uint16_t 
  * FC2 epilogue; "[JAX] Expert Parallelism", commit log: apply_topk_weights_early):
  *   weight_at 0  in the combine: out = sum_j w_j y_j            (late, the default)
  *   weight_at 1  in FC1:  h_j = rnd(w_j silu(g) u), out = sum_j y_j
- *   weight_at 2  in FC2:  y_j <- w_j y_j,           out = sum_j y_j
+ *   weight_at 2  in FC2:  y_j = rnd(w_j (h_j Wd)),  out = sum_j y_j
  * All three are the same function in exact arithmetic; they differ in where the
- * rounding of h falls (weight_at 1 rounds the weighted h).  y_out holds the
- * per-route y as the path stores it (weighted for 1 and 2). */
+ * roundings of h and y fall (weight_at 1 rounds the weighted h, weight_at 2 the
+ * weighted y).  y_out holds the per-route y as the path stores it (weighted for 1
+ * and 2). */
 void oracle_moe_fwd_w(int64_t n_tokens, const int64_t *tokens, int H, int F, int E, int k,
                       const uint16_t *x, const uint16_t *const *Wg, const uint16_t *const *Wu,
                       const uint16_t *const *Wd, const int32_t *topk_idx, const float *topk_w,
@@ -540,10 +545,8 @@ void oracle_moe_fwd_w(int64_t n_tokens, const int64_t *tokens, int H, int F, int
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) continue;
             const double w = (double)topk_w[t * k + j];
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, weight_at == 1 ? w : 1.0, h_mx, g, u,
-                         h, y);
-            if (weight_at == 2)
-                for (int n = 0; n < H; ++n) y[n] *= w;
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, weight_at == 1 ? w : 1.0,
+                         weight_at == 2 ? w : 1.0, h_mx, g, u, h, y);
             const double wc = weight_at == 0 ? w : 1.0;
             for (int n = 0; n < H; ++n) o[n] += wc * y[n];
             int64_t ri = i * k + j;
@@ -573,8 +576,8 @@ void oracle_moe_fwd(int64_t n_tokens, const int64_t *tokens, int H, int F, int E
  * block along K) and dequantised exactly: x along H; W_gate / W_up given as
  * quantised K-major [F][H] codes with scales [F][H/32]; W_down as quantised
  * [H][F] codes with scales [H][F/32]; h = silu(g)*u quantised along F from
- * its unrounded value.  y is kept unrounded (fp32 on the path); out is bf16
- * in round_mode 1. */
+ * its unrounded value.  y is stored bf16 (rounded in round_mode 1 and 2); out
+ * is bf16 in round_mode 1. */
 void oracle_moe_fwd_mxfp8(int64_t n_tokens, const int64_t *tokens, int H, int F, int E, int k,
                           const uint16_t *x,
                           const uint8_t *const *Wg_q, const uint8_t *const *Wg_s,
@@ -614,7 +617,7 @@ void oracle_moe_fwd_mxfp8(int64_t n_tokens, const int64_t *tokens, int H, int F,
                 double s = 0.0;
                 const uint8_t *qd = Wd_q[e] + (int64_t)n * F, *cd = Wd_s[e] + (int64_t)n * (F / 32);
                 for (int f = 0; f < F; ++f) s += h[f] * ldexp(oracle_e4m3_to_double(qd[f]), (int)cd[f / 32] - 127);
-                y[n] = s;
+                y[n] = rnd(s, round_mode);
             }
             double w = (double)topk_w[t * k + j];
             for (int n = 0; n < H; ++n) o[n] += w * y[n];
@@ -668,7 +671,8 @@ static void route_bwd(const uint16_t *dYt, double w, const double *g, const doub
  * [T,H].  Outputs (double): dx [T,H] = sum_j dxr(t,j) (bf16 in mode 1);
  * dWg, dWu [E,H,F] = sum over routes of x^T dg / x^T du; dWd [E,F,H] = sum
  * over routes of h^T dy (each bf16 in mode 1); experts with no route get
- * exactly 0.  d_topk_w [T,k] = <dY[t], y(t,j)> (0 for dropped routes).
+ * exactly 0.  d_topk_w [T,k] = <dY[t], y(t,j)> with y as the forward stores it
+ * (bf16 in round_mode 1 and 2; 0 for dropped routes).
  *
  * h_mx != 0: the straight-through backward of the MXFP8 forward ("Add MoE +
  * expert-parallel Python API surface, PyTorch reference, and tests", Summary:
@@ -693,7 +697,7 @@ void oracle_moe_bwd(int64_t T, int H, int F, int E, int k, const uint16_t *x,
         for (int j = 0; j < k; ++j) {
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) { d_topk_w[t * k + j] = 0.0; continue; }
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, h_mx, g, u, h, y);
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, 1.0, h_mx, g, u, h, y);
             double dw = 0.0;
             for (int n = 0; n < H; ++n) dw += oracle_bf16_to_double(dY[t * H + n]) * y[n];
             d_topk_w[t * k + j] = dw;
@@ -735,7 +739,7 @@ void oracle_moe_bwd_dx_tokens(int64_t n_tokens, const int64_t *tokens, int H, in
         for (int j = 0; j < k; ++j) {
             int32_t e = topk_idx[t * k + j];
             if (e < 0 || e >= E) { d_topk_w[i * k + j] = 0.0; continue; }
-            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, h_mx, g, u, h, y);
+            expert_route(x + t * H, Wg[e], Wu[e], Wd[e], H, F, round_mode, 1.0, 1.0, h_mx, g, u, h, y);
             double dw = 0.0;
             for (int n = 0; n < H; ++n) dw += oracle_bf16_to_double(dY[t * H + n]) * y[n];
             d_topk_w[i * k + j] = dw;

@@ -368,6 +368,32 @@ def test_forward_vs_torch_fp64_multi_expert():
     assert np.abs(r1["out"] - r["out"]).max() <= 2e-2 * rms
 
 
+def test_forward_rounding_points_vs_torch_bf16_stores():
+    """round_mode 1 stores h and the expert output y in bf16 and rounds the output: an
+    independent torch implementation that casts to bf16 (torch's own RNE conversion) at
+    exactly those three points gives the same values.  A rounding point left out or moved
+    (y unrounded, h rounded after Wd, out rounded per slot) changes many elements."""
+    inp, idx, w, b = _rand_problem(16, T=40, H=64, F=96, E=6, k=3)
+    r = oracle.moe_fwd(b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, round_mode=1,
+                       want_h=True, want_y=True)
+    x = inp["x"].double()
+    T, k = idx.shape
+    out = torch.zeros(T, x.shape[1], dtype=torch.float64)
+    bf = lambda v: v.to(torch.bfloat16).double()  # noqa: E731
+    for t in range(T):
+        for j in range(k):
+            e = int(idx[t, j])
+            hr = bf(torch.nn.functional.silu(x[t] @ inp["W_gate"][e].double()) * (x[t] @ inp["W_up"][e].double()))
+            yr = bf(hr @ inp["W_down"][e].double())
+            assert np.array_equal(r["h"][t * k + j], hr.numpy())
+            assert np.array_equal(r["y"][t * k + j], yr.numpy())
+            out[t] += float(w[t, j]) * yr
+    assert np.array_equal(r["out"], bf(out).numpy())
+    # the unrounded y differs from the stored one: the rounding point is really there
+    r0 = oracle.moe_fwd(b["x"], b["W_gate"], b["W_up"], b["W_down"], idx, w, round_mode=0, want_y=True)
+    assert not np.array_equal(r0["y"], r["y"])
+
+
 def test_zero_token_experts_contribute_nothing():
     inp, idx, w, b = _rand_problem(8, T=32, H=32, F=64, E=8, k=2)
     idx = np.where(idx >= 6, idx - 6, idx).astype(np.int32)      # experts 6, 7 get no tokens

@@ -54,6 +54,22 @@ def test_fc1_placement_rounds_the_weighted_h():
     assert np.array_equal(got, ref)
 
 
+def test_fc2_placement_rounds_the_weighted_y():
+    """round_mode 1: y = bf16(w * (h Wd)) on the (rounded, unweighted) h, rounded by
+    torch's own bf16 conversion of the product, not w times a rounded y."""
+    b, idx, w = _case()
+    base = _fwd(b, idx, w, round_mode=1, want_h=True, want_y=True)
+    got = _fwd(b, idx, w, round_mode=1, want_h=True, want_y=True, weight_at=oracle.WEIGHT_IN_FC2)
+    assert np.array_equal(got["h"], base["h"])
+    hr = torch.from_numpy(base["h"])
+    wd = torch.from_numpy(oracle.bits_to_float(b["W_down"]))
+    y_exact = torch.stack([hr[r] @ wd[int(idx.flat[r])] for r in range(idx.size)])
+    wr = torch.from_numpy(w.reshape(-1, 1).astype(np.float64))
+    ref = (wr * y_exact).to(torch.bfloat16).double().numpy()
+    assert np.array_equal(got["y"], ref)
+    assert not np.array_equal(got["y"], (wr.numpy() * base["y"]))
+
+
 def test_unit_weights_make_the_placements_identical():
     """k = 1: the softmax over one logit is exactly 1, so every placement gives the same
     bits even with bf16 rounding."""
