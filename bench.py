@@ -12,7 +12,8 @@ Variants: --router sigmoid (sigmoid scores + a seeded expert routing bias);
 --backward (forward + backward; on dsv3_mxfp8 the straight-through backward:
 MXFP8 rows dequantised, then the bf16 backward kernels on the values the
 forward's MMAs consumed, weights dequantised once with the quantisation).
-Default workload: fine_grained (T=4096, H=2048, F=1408, E=64, top-6).
+Default workload: mixtral forward + backward (T=8192, H=4096, F=14336, E=8, top-2), the
+largest workload that fits one GPU and the one the tensor-core target is stated on.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME]
     python bench.py --impl reference ...   # the CPU oracle, timed on the host cores
@@ -217,7 +218,7 @@ def build_workload(shape, dev, stream):
     active = int((m.perm.group_sizes > 0).sum().item())     # experts whose weights are read
     w["active_experts"] = active
     wbytes = active * H * F * (1 if shape.mxfp8 else 2) * (1 + (1 / 32 if shape.mxfp8 else 0))
-    ysz = m.y_perm.element_size()   # fp32 rows; bf16 on the MXFP8 forward without a backward
+    ysz = m.y_perm.element_size()   # bf16 expert outputs
 
     g = [Group("route", lambda: m.route(inp["logits"], stream), nbytes=T * E * 4 + R * 8)]
     if shape.mxfp8:
@@ -252,7 +253,7 @@ def build_workload(shape, dev, stream):
                            nbytes=R * (H + F) * (1 + 1 / 32) + R * (H + F) * 2, launches=4))
         g += [
             Group("combine_bwd", lambda: b.combine_bwd(inp["dY"], stream),
-                  nbytes=T * H * 2 + R * H * 4 + R * H * 2 + R * 8, launches=2),
+                  nbytes=T * H * 2 + R * H * ysz + R * H * 2 + R * 8, launches=2),
             Group("route_bwd", lambda: b.router_bwd(inp["logits"], stream), nbytes=R * 4 + R * 8 + T * E * 4),
             Group("dgrad_fc2_dswiglu", lambda: b.dgrad_fc2(Wd_b, stream), flop=2.0 * R * H * F,
                   nbytes=R * H * 2 + wb16 + R * 2 * F * 2 * 2),
@@ -419,6 +420,15 @@ def workload_shape(args):
     return shape
 
 
+def workload_config(shape, active_experts: int) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    return {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k,
+            "router": shape.router, "weight_at": shape.weight_at,
+            "pass": ("MXFP8 " if shape.mxfp8 else "") + ("forward+backward" if shape.backward else "forward"),
+            "active_experts": active_experts,
+            "l2": "GPU arm: L2 flushed between timed steps (256 MiB write outside the timed events)"}
+
+
 def run_reference(args):
     """The oracle as it stands, on the host cores, a bounded token sample per step."""
     import torch
@@ -431,6 +441,12 @@ def run_reference(args):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     inp = make_inputs(shape, device=dev, with_dy=shape.backward, with_expert_bias=shape.router == "sigmoid")
     sample = max(1, min(shape.T, args.ref_tokens if args.ref_tokens else (2 if shape.backward or shape.mxfp8 else 16)))
+    lg = inp["logits"].cpu().numpy()
+    if shape.router == "sigmoid":
+        idx_all, _ = oracle.route_topk_sigmoid(lg, shape.k, inp["expert_bias"].cpu().numpy())
+    else:
+        idx_all, _ = oracle.route_topk(lg, shape.k)
+    active = int(len(set(int(e) for e in idx_all.reshape(-1) if e >= 0)))
     times = []
     for it in range(args.warmup + args.steps):
         dt, _ = oracle_sample(shape, inp, sample, it=it)
@@ -442,8 +458,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E,
-                   "k": shape.k, "router": shape.router, "tokens_per_step": sample},
+        "config": workload_config(shape, active),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"{sample} of {shape.T} tokens per step (routing and permutation over all tokens)"},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -570,11 +585,7 @@ def run_gpu(args):
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "mxfp8" if shape.mxfp8 else "bf16",
         "data": "synthetic (seeded; the workload's stated shapes and distributions)",
-        "config": {"workload": shape.name, "T": shape.T, "H": shape.H, "F": shape.F, "E": shape.E, "k": shape.k,
-                   "router": shape.router, "weight_at": shape.weight_at,
-                   "pass": "forward+backward" if shape.backward else "forward",
-                   "active_experts": w["active_experts"],
-                   "l2": "flushed between steps (256 MiB write outside the timed events)"},
+        "config": workload_config(shape, w["active_experts"]),
         "kernels": rates,
         "kernels_note": "per kernel group: a second pass of the same steps with an event after each group "
                         "(events between groups stop a launch from overlapping the previous group's tail, so "
@@ -606,7 +617,7 @@ def main(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--config", default="fine_grained",
+    ap.add_argument("--config", default="mixtral",
                     choices=["tiny", "fine_grained", "mixtral", "skewed", "dsv3_mxfp8"])
     ap.add_argument("--shape", default="",
                     help="override sizes of the workload, e.g. 'T=2048,F=4096' (same kind of pass)")

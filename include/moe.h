@@ -66,7 +66,7 @@ typedef enum {
 #define MOE_DEVERR_CAPACITY      0x4u  /* routed rows exceed rows_cap; extra rows not written */
 
 /* Alignment: the kernels move 16-byte vectors.  The row tensors of moe_permute (x, x_perm),
- * moe_permute_static_scratch, moe_unpermute_combine(_ybf16) (y_perm, out), moe_combine_bwd
+ * moe_permute_static_scratch, moe_unpermute_combine (y_perm, out), moe_combine_bwd
  * (dY, y_perm, dy_perm), moe_unpermute_sum (dx_perm, dx), moe_grouped_quantize_mxfp8 (in,
  * data) and moe_quantize_weights_mxfp8 (data) must start on a 16-byte boundary; the
  * GEMMs' operands and outputs must too (their TMA descriptors).  A misaligned pointer gives
@@ -221,10 +221,12 @@ MOE_API moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx, i
  *     device error bits (MOE_DEVERR_*), stream-ordered after the call.
  * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
  * routine).  The first call on each device looks up the array's device
- * address (cudaGetSymbolAddress) with that device current; make that first
- * call before any stream capture.  Every call shares the one array, so calls
- * that overlap on the GPU (for example on two streams at once) race and give
- * undefined results; serialise them. */
+ * address (cudaGetSymbolAddress) with that device current, and the lookup is
+ * repeated when the device's current context is no longer the one the address
+ * was taken in (after cudaDeviceReset, or under another context); make the
+ * first call in each context before any stream capture.  Every call shares
+ * the one array, so calls that overlap on the GPU (for example on two
+ * streams at once) race and give undefined results; serialise them. */
 MOE_API moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const int32_t *topk_idx, int64_t T,
                                                 int H, int E, int k, int align, moe_bf16_t *x_perm,
                                                 int64_t rows_cap, int32_t *dst_of_route,
@@ -239,7 +241,7 @@ MOE_API moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const int32
 /* For every expert e and every row i in [group_offsets[e], group_offsets[e+1]):
  *   g = x_perm[i] W_gate[e],  u = x_perm[i] W_up[e]     (fp32 accumulation)
  *   h[i] = bf16(silu(g) * u)                            (SwiGLU, fp32)
- *   y_perm[i] = h[i] W_down[e]                          (fp32 accumulation, fp32 result)
+ *   y_perm[i] = bf16(h[i] W_down[e])                    (fp32 accumulation)
  * ("Add MoE + expert-parallel Python API surface, PyTorch reference, and
  * tests", Summary: local SwiGLU experts silu(gate) * up, the fc1_c stash;
  * "[Draft][JAX] MoE block optimization", diagram: fused grouped GEMM and
@@ -251,8 +253,10 @@ MOE_API moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const int32
  *   group_offsets device int32 [E+1] (from moe_permute); read on the device
  *   rows_cap      rows of x_perm / h / y_perm; group_offsets[E] <= rows_cap
  *   h             device bf16 [rows_cap, F] out (rows of groups only)
- *   y_perm        device fp32 [rows_cap, H] out (rows of groups only); kept in
- *                 fp32 so that the combine adds unrounded expert outputs
+ *   y_perm        device bf16 [rows_cap, H] out (rows of groups only): the
+ *                 expert outputs in 2-byte slots, as the pages' combine carries
+ *                 them ("[JAX] Expert Parallelism: JAX primitives + VJPs",
+ *                 commit log)
  *   fc1_c         device bf16 [rows_cap, 2F] out, or NULL: the pre-SwiGLU
  *                 accumulators rounded to bf16, gate in columns [0, F) and
  *                 up in [F, 2F); needed by moe_grouped_ffn_bwd
@@ -265,7 +269,7 @@ MOE_API moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const int32
 MOE_API moe_status_t moe_grouped_ffn_fwd(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
                                  const moe_bf16_t *W_up, const moe_bf16_t *W_down,
                                  const int32_t *group_offsets, int E, int H, int F,
-                                 int64_t rows_cap, moe_bf16_t *h, float *y_perm,
+                                 int64_t rows_cap, moe_bf16_t *h, moe_bf16_t *y_perm,
                                  moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
                                  moe_stream_t stream);
 
@@ -280,7 +284,7 @@ MOE_API moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const moe_
                                             moe_stream_t stream);
 MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_down,
                                      const int32_t *group_offsets, int E, int H, int F,
-                                     int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
+                                     int64_t rows_cap, moe_bf16_t *y_perm, void *ws, size_t ws_bytes,
                                      moe_stream_t stream);
 
 /* The same two steps with the router weight applied early ("Add MoE +
@@ -291,10 +295,10 @@ MOE_API moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_do
  * 0) and is scaled by topk_w[src_of_row[row]] (topk_w fp32 [T, k] read flat):
  *   moe_grouped_fc1_swiglu_weighted   h = bf16(w * silu(g) * u); fc1_c (if
  *                                      not NULL) keeps the unweighted g | u
- *   moe_grouped_fc2_weighted          y_perm = w * (h W_down) in fp32
+ *   moe_grouped_fc2_weighted          y_perm = bf16(w * (h W_down)), the product in fp32
  * Combine such outputs with moe_unpermute_combine(..., topk_w = NULL, ...).
  * The three placements are one function in exact arithmetic; the FC1 one
- * rounds the weighted h to bf16.  Forward only: moe_grouped_ffn_bwd assumes
+ * rounds the weighted h to bf16, the FC2 one the weighted y.  Forward only: moe_grouped_ffn_bwd assumes
  * the weight is applied in the combine.  Other arguments, limits and errors as
  * above; src_of_row / topk_w NULL with rows_cap > 0 is MOE_ERR_INVALID_ARG. */
 MOE_API moe_status_t moe_grouped_fc1_swiglu_weighted(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
@@ -306,7 +310,7 @@ MOE_API moe_status_t moe_grouped_fc1_swiglu_weighted(const moe_bf16_t *x_perm, c
 MOE_API moe_status_t moe_grouped_fc2_weighted(const moe_bf16_t *h, const moe_bf16_t *W_down,
                                               const int32_t *group_offsets, const int32_t *src_of_row,
                                               const float *topk_w, int E, int H, int F, int64_t rows_cap,
-                                              float *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
+                                              moe_bf16_t *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream);
 
 /* Optional clamp of the SwiGLU inputs ("Add MoE + expert-parallel Python API surface,
  * PyTorch reference, and tests", Summary: local SwiGLU experts with an optional
@@ -336,7 +340,7 @@ MOE_API moe_status_t moe_grouped_fc1_swiglu_clamped(const moe_bf16_t *x_perm, co
  * tests", Summary: per-top-k combine; "[JAX] Expert Parallelism", sequence
  * diagram: the combine that returns expert outputs to token order).
  *
- *   y_perm       device fp32 [rows, H]
+ *   y_perm       device bf16 [rows, H] (each value widened exactly to fp32)
  *   dst_of_route device int32 [T, k] (from moe_permute)
  *   topk_w       device fp32 [T, k], or NULL for weights 1 (the plain sum, when
  *                the router weight was already applied in FC1 or FC2)
@@ -344,15 +348,9 @@ MOE_API moe_status_t moe_grouped_fc1_swiglu_clamped(const moe_bf16_t *x_perm, co
  *
  * Limits: H % 8 == 0, 1 <= k <= 32.  Errors: MOE_ERR_INVALID_ARG,
  * MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA. */
-MOE_API moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *dst_of_route,
+MOE_API moe_status_t moe_unpermute_combine(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                    const float *topk_w, int64_t T, int H, int k,
                                    moe_bf16_t *out, moe_stream_t stream);
-/* moe_unpermute_combine over bf16 y_perm rows (moe_grouped_fc2_mxfp8_ybf16): each
- * slot's values widened to fp32, the same fp32 slot-order sum and bf16 output.
- * y_perm 16-byte aligned; limits and errors as moe_unpermute_combine. */
-MOE_API moe_status_t moe_unpermute_combine_ybf16(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
-                                                 const float *topk_w, int64_t T, int H, int k,
-                                                 moe_bf16_t *out, moe_stream_t stream);
 
 /* The combine with the output encoded as MXFP8 along H ("Add MoE + expert-parallel
  * Python API surface, PyTorch reference, and tests", Summary: mxfp8 public outputs
@@ -362,7 +360,7 @@ MOE_API moe_status_t moe_unpermute_combine_ybf16(const moe_bf16_t *y_perm, const
  * out_sf: device uint8 [T, H/32] (UE8M0 scale bytes, row-major).  topk_w may be
  * NULL (plain sum).  Limits: H % 32 == 0, 1 <= k <= 32; y_perm 16-byte and out_q
  * 8-byte aligned. */
-MOE_API moe_status_t moe_unpermute_combine_mxfp8(const float *y_perm, const int32_t *dst_of_route,
+MOE_API moe_status_t moe_unpermute_combine_mxfp8(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                                  const float *topk_w, int64_t T, int H, int k, uint8_t *out_q,
                                                  uint8_t *out_sf, moe_stream_t stream);
 
@@ -427,7 +425,7 @@ MOE_API moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *topk_
  * accumulation:
  *   h = silu(x W_gate) * (x W_up) (fp32), quantised to MXFP8 along F:
  *       h_q uint8 [rows_cap, F], h_sf tile layout (moe_mx_tile_scale_bytes(rows_cap, E, F))
- *   y_perm = h W_down, fp32 [rows_cap, H]
+ *   y_perm = bf16(h W_down) [rows_cap, H]
  * x_q / x_sf from moe_permute_mxfp8; Wg_q, Wu_q (K = H, N = F) and Wd_q
  * (K = F, N = H) with their scales from moe_quantize_weights_mxfp8.  All code
  * and scale pointers 16-byte aligned.  Limits: H % 128 == 0, F % 128 == 0, E <= 1024.
@@ -436,7 +434,7 @@ MOE_API moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint8_t
                                                const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,
                                                const uint8_t *Wd_q, const uint8_t *Wd_sf,
                                                const int32_t *group_offsets, int E, int H, int F,
-                                               int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf, float *y_perm,
+                                               int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf, moe_bf16_t *y_perm,
                                                void *ws, size_t ws_bytes, moe_stream_t stream);
 /* moe_grouped_fc1_swiglu_mxfp8 also writes, when fc1_c is non-NULL, the bf16
  * stash of the fp32 accumulators g | u, bf16 [rows_cap, 2F], for the
@@ -457,19 +455,8 @@ MOE_API moe_status_t moe_grouped_fc1_swiglu_mxfp8_clamped(
     size_t ws_bytes, moe_stream_t stream);
 MOE_API moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
                                            const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H, int F,
-                                           int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
+                                           int64_t rows_cap, moe_bf16_t *y_perm, void *ws, size_t ws_bytes,
                                            moe_stream_t stream);
-/* moe_grouped_fc2_mxfp8 with y_perm stored as bf16 [rows_cap, H] (the fp32
- * accumulators rounded to nearest even), for moe_unpermute_combine_ybf16.  The
- * pages' expert outputs are bf16 ("[JAX] Expert Parallelism: JAX primitives +
- * VJPs", commit log: 2-byte combine slots; the fp32 island around SwiGLU dropped
- * as wasted bandwidth).  On the MXFP8 path the E4M3 rounding of the operands
- * dominates the error, and the bf16 rows halve what FC2 writes and the combine
- * reads.  y_perm 16-byte aligned; limits and errors as moe_grouped_fc2_mxfp8. */
-MOE_API moe_status_t moe_grouped_fc2_mxfp8_ybf16(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
-                                                 const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H,
-                                                 int F, int64_t rows_cap, moe_bf16_t *y_perm, void *ws,
-                                                 size_t ws_bytes, moe_stream_t stream);
 
 /* ------------------------------------------------------------------ */
 /* A8  Backward                                                         */
@@ -491,7 +478,7 @@ MOE_API moe_status_t moe_grouped_fc2_mxfp8_ybf16(const uint8_t *h_q, const uint8
  *   dW_down[e] = sum_i h[i]^T dy_perm[i];  [dW_gate|dW_up][e] = sum_i x_perm[i]^T dgu[i]
  *     (fp32, over the rows of group e; experts with no rows get exact zeros)
  * Shapes: dY, dx bf16 [T, H]; x_perm, dy_perm bf16 [rows_cap, H]; h bf16
- * [rows_cap, F]; fc1_c, dgu bf16 [rows_cap, 2F]; y_perm, dx_perm fp32
+ * [rows_cap, F]; fc1_c, dgu bf16 [rows_cap, 2F]; y_perm bf16 and dx_perm fp32
  * [rows_cap, H]; dW_gate, dW_up fp32 [E, H, F]; dW_down fp32 [E, F, H];
  * d_topk_w fp32 [T, k] (nullable; y_perm may then be NULL).  dy_perm, dgu
  * and dx_perm are caller-owned scratch.  group_sizes/group_offsets/
@@ -500,7 +487,7 @@ MOE_API moe_status_t moe_grouped_fc2_mxfp8_ybf16(const uint8_t *h_q, const uint8
  * 1 <= k <= 32.  Errors as for the forward calls. */
 MOE_API moe_status_t moe_grouped_ffn_bwd(
     const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
-    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const float *y_perm,
+    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const moe_bf16_t *y_perm,
     const int32_t *dst_of_route, const int32_t *group_sizes, const int32_t *group_offsets,
     const float *topk_w, int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm,
     moe_bf16_t *dgu, float *dx_perm, moe_bf16_t *dx, float *dW_gate, float *dW_up, float *dW_down,
@@ -513,7 +500,7 @@ MOE_API moe_status_t moe_grouped_ffn_bwd(
  *   moe_grouped_dgrad_fc1         dgu -> dx_perm
  *   moe_grouped_wgrad             x_perm, h, dy_perm, dgu -> dW_gate, dW_up, dW_down
  *   moe_unpermute_sum             dx_perm -> dx */
-MOE_API moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const float *y_perm, const int32_t *dst_of_route,
+MOE_API moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                      const float *topk_w, const int32_t *group_sizes,
                                      const int32_t *group_offsets, int64_t T, int H, int E, int k,
                                      int64_t rows_cap, moe_bf16_t *dy_perm, float *d_topk_w,

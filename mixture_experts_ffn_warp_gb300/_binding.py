@@ -49,7 +49,6 @@ SIGNATURES = {
                                               _sz, _vp]),
     "moe_grouped_fc2_weighted": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_unpermute_combine": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp]),
-    "moe_unpermute_combine_ybf16": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp]),
     "moe_grouped_ffn_bwd": (_st, [_vp] * 12 + [_i64, _int, _int, _int, _int, _i64] + [_vp] * 8 + [_vp, _sz, _vp]),
     "moe_combine_bwd": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _i64, _vp, _vp, _vp]),
     "moe_grouped_dgrad_fc2_dswiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
@@ -73,7 +72,6 @@ SIGNATURES = {
     "moe_unpermute_combine_mxfp8": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp, _vp]),
     "moe_dequantize_weights_mxfp8": (_st, [_vp, _vp, _int, _int, _int, _vp, _vp]),
     "moe_grouped_fc2_mxfp8": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
-    "moe_grouped_fc2_mxfp8_ybf16": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -283,11 +281,11 @@ def moe_grouped_ffn_fwd(x_perm: torch.Tensor, W_gate: torch.Tensor, W_up: torch.
     if h is None:
         h = torch.empty(rows_cap, F, dtype=torch.bfloat16, device=dev)
     if y_perm is None:
-        y_perm = torch.empty(rows_cap, H, dtype=torch.float32, device=dev)
+        y_perm = torch.empty(rows_cap, H, dtype=torch.bfloat16, device=dev)
     if want_fc1_c and fc1_c is None:
         fc1_c = torch.empty(rows_cap, 2 * F, dtype=torch.bfloat16, device=dev)
     _need(h, "h", torch.bfloat16, (rows_cap, F), dev)
-    _need(y_perm, "y_perm", torch.float32, (rows_cap, H), dev)
+    _need(y_perm, "y_perm", torch.bfloat16, (rows_cap, H), dev)
     if fc1_c is not None:
         _need(fc1_c, "fc1_c", torch.bfloat16, (rows_cap, 2 * F), dev)
     _check("moe_grouped_ffn_fwd", load_library().moe_grouped_ffn_fwd(
@@ -321,10 +319,11 @@ def moe_grouped_fc1_swiglu(x_perm, W_gate, W_up, group_offsets, ws: Workspace, h
 
 
 def moe_grouped_fc2(h, W_down, group_offsets, ws: Workspace, y_perm, stream=None, route_weights=None):
-    """A4 alone: y_perm = h W_down per group (moe.h).  route_weights = (src_of_row,
+    """A4 alone: y_perm = bf16(h W_down) per group (moe.h).  route_weights = (src_of_row,
     topk_w): y of each row scaled by its route's router weight."""
     rows_cap, F = h.shape
     E, _, H = W_down.shape
+    _need(y_perm, "y_perm", torch.bfloat16, (rows_cap, H), h.device)
     if route_weights is None:
         _check("moe_grouped_fc2", load_library().moe_grouped_fc2(
             _ptr(h), _ptr(W_down), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
@@ -341,9 +340,9 @@ def moe_grouped_fc2(h, W_down, group_offsets, ws: Workspace, y_perm, stream=None
 
 def moe_unpermute_combine(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w,
                           out=None, stream=None) -> torch.Tensor:
-    """out[t] = sum_j w[t,j] * y_perm[dst[t,j]] in fp32, slot order (moe.h);
-    topk_w None: the plain sum (weights already applied in FC1 or FC2)."""
-    _need(y_perm, "y_perm", torch.float32)
+    """out[t] = sum_j w[t,j] * y_perm[dst[t,j]] in fp32, slot order, over bf16 expert
+    outputs (moe.h); topk_w None: the plain sum (weights already applied in FC1 or FC2)."""
+    _need(y_perm, "y_perm", torch.bfloat16)
     H = y_perm.shape[1]
     dev = y_perm.device
     _need(dst_of_route, "dst_of_route", torch.int32, None, dev)
@@ -358,29 +357,14 @@ def moe_unpermute_combine(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk
     return out
 
 
-def moe_unpermute_combine_ybf16(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w,
-                                out=None, stream=None) -> torch.Tensor:
-    """moe_unpermute_combine over bf16 y_perm rows (moe_grouped_fc2_mxfp8_ybf16; moe.h)."""
-    _need(y_perm, "y_perm", torch.bfloat16)
-    H = y_perm.shape[1]
-    dev = y_perm.device
-    _need(dst_of_route, "dst_of_route", torch.int32, None, dev)
-    T, k = dst_of_route.shape
-    if topk_w is not None:
-        _need(topk_w, "topk_w", torch.float32, (T, k), dev)
-    if out is None:
-        out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    _need(out, "out", torch.bfloat16, (T, H), dev)
-    _check("moe_unpermute_combine_ybf16", load_library().moe_unpermute_combine_ybf16(
-        _ptr(y_perm), _ptr(dst_of_route), _ptr(topk_w), T, H, k, _ptr(out), _stream(stream)))
-    return out
-
-
 # ------------------------------------------------------------------ A8 backward steps
 
 def moe_combine_bwd(dY, y_perm, perm: "Permutation", topk_w, dy_perm, d_topk_w=None, stream=None):
-    """dy_perm = w * dY scattered to the forward rows; d_topk_w = <dY, y> (moe.h)."""
+    """dy_perm = w * dY scattered to the forward rows; d_topk_w = <dY, y> over the bf16
+    expert outputs y_perm (moe.h)."""
     T, H = dY.shape
+    if y_perm is not None:
+        _need(y_perm, "y_perm", torch.bfloat16, None, dY.device)
     k = perm.dst_of_route.shape[1]
     E = perm.group_sizes.shape[0]
     _check("moe_combine_bwd", load_library().moe_combine_bwd(
@@ -443,7 +427,7 @@ def moe_grouped_ffn_bwd(dY, x_perm, W_gate, W_up, W_down, fc1_c, h, y_perm, perm
                              ("W_gate", W_gate, torch.bfloat16, (E, H, F)), ("W_up", W_up, torch.bfloat16, (E, H, F)),
                              ("W_down", W_down, torch.bfloat16, (E, F, H)),
                              ("fc1_c", fc1_c, torch.bfloat16, (cap, 2 * F)), ("h", h, torch.bfloat16, (cap, F)),
-                             ("y_perm", y_perm, torch.float32, (cap, H)), ("topk_w", topk_w, torch.float32, (T, k))):
+                             ("y_perm", y_perm, torch.bfloat16, (cap, H)), ("topk_w", topk_w, torch.float32, (T, k))):
         _need(t, name, dt, shp, dev)
     out = {
         "dx": torch.empty(T, H, dtype=torch.bfloat16, device=dev),
@@ -560,22 +544,12 @@ def moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offs
 
 
 def moe_grouped_fc2_mxfp8(h_q, h_sf, Wd_q, Wd_sf, group_offsets, ws: Workspace, y_perm, stream=None):
-    """A4 on MXFP8 operands, fp32 output (moe.h)."""
-    rows_cap, F = h_q.shape
-    E = group_offsets.shape[0] - 1
-    H = y_perm.shape[1]
-    _check("moe_grouped_fc2_mxfp8", load_library().moe_grouped_fc2_mxfp8(
-        _ptr(h_q), _ptr(h_sf), _ptr(Wd_q), _ptr(Wd_sf), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
-        _ptr(ws.buf), ws.nbytes, _stream(stream)))
-
-
-def moe_grouped_fc2_mxfp8_ybf16(h_q, h_sf, Wd_q, Wd_sf, group_offsets, ws: Workspace, y_perm, stream=None):
-    """A4 on MXFP8 operands, y_perm stored as bf16 (moe.h)."""
+    """A4 on MXFP8 operands, y_perm bf16 (moe.h)."""
     rows_cap, F = h_q.shape
     E = group_offsets.shape[0] - 1
     _need(y_perm, "y_perm", torch.bfloat16, None, h_q.device)
     H = y_perm.shape[1]
-    _check("moe_grouped_fc2_mxfp8_ybf16", load_library().moe_grouped_fc2_mxfp8_ybf16(
+    _check("moe_grouped_fc2_mxfp8", load_library().moe_grouped_fc2_mxfp8(
         _ptr(h_q), _ptr(h_sf), _ptr(Wd_q), _ptr(Wd_sf), _ptr(group_offsets), E, H, F, rows_cap, _ptr(y_perm),
         _ptr(ws.buf), ws.nbytes, _stream(stream)))
 
@@ -618,7 +592,7 @@ def moe_dequantize_weights_mxfp8(data: torch.Tensor, scales: torch.Tensor, E: in
 def moe_unpermute_combine_mxfp8(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w, out_q=None, out_sf=None,
                                 stream=None):
     """The combine with an MXFP8 output (moe.h): (codes uint8 [T, H], scales uint8 [T, H/32])."""
-    _need(y_perm, "y_perm", torch.float32)
+    _need(y_perm, "y_perm", torch.bfloat16)
     _need(dst_of_route, "dst_of_route", torch.int32)
     T, k = dst_of_route.shape
     H = y_perm.shape[1]

@@ -1,8 +1,9 @@
 // combine.cu -- A5: weighted unpermute / combine back to token order.
 //
-// One warp per token; each lane owns 8-column slices of the row (two 16-byte
-// fp32 loads per slot, or one of bf16 rows; one 16-byte bf16 store) and accumulates
-// w_j * y_perm[dst_j] over the k slots in slot order in fp32.  All slot loads
+// One warp per token; each lane owns 8-column slices of the row (one 16-byte load
+// of bf16 expert outputs per slot -- two of fp32 rows for the backward's
+// unpermute-sum --, one 16-byte bf16 store) and accumulates w_j * y_perm[dst_j]
+// over the k slots in slot order in fp32.  All slot loads
 // of a slice are issued before the FMAs, and each lane keeps several slices
 // in flight.  ("Add MoE + expert-parallel Python API surface, PyTorch
 // reference, and tests", Summary: per-top-k combine.)
@@ -72,7 +73,8 @@ struct Slice<uint4> {
     }
 };
 
-// Y = float4 (fp32 y_perm rows) or uint4 (bf16 rows, the MXFP8 forward's option).
+// Y = uint4 (bf16 y_perm rows, the forward's combine) or float4 (fp32 rows: the
+// backward's unpermute-sum of dx_perm).
 template <int KMAX, typename Y>
 __global__ void __launch_bounds__(kCombineWarps * 32)
 combine_kernel(const Y *__restrict__ y_perm, const int32_t *__restrict__ dst_of_route,
@@ -133,7 +135,7 @@ cudaError_t launch(const Y *y, const int32_t *dst, const float *w, int64_t T, in
 // shuffles (a block's lanes are all in range or all out, H % 32 == 0).
 template <int KMAX>
 __global__ void __launch_bounds__(kCombineWarps * 32)
-combine_mx_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__ dst_of_route,
+combine_mx_kernel(const uint4 *__restrict__ y_perm, const int32_t *__restrict__ dst_of_route,
                   const float *__restrict__ topk_w, int64_t T, int k, int slices, uint2 *__restrict__ out_q,
                   uint8_t *__restrict__ out_sf) {
     pdl_wait();
@@ -157,19 +159,15 @@ combine_mx_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__
     for (int s0 = 0; s0 < slices; s0 += 32) {
         const int s = s0 + lane;
         const bool in = s < slices;
-        F8 val[KMAX];
+        uint4 val[KMAX];
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)
-            if (in && dst[j] >= 0) {
-                const float4 *src = y_perm + ((int64_t)dst[j] * slices + s) * 2;
-                val[j].a = __ldg(src);
-                val[j].b = __ldg(src + 1);
-            }
+            if (in && dst[j] >= 0) val[j] = __ldg(y_perm + (int64_t)dst[j] * slices + s);
         float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         if (in) {
 #pragma unroll
             for (int j = 0; j < KMAX; ++j)
-                if (dst[j] >= 0) fma8(acc, w[j], val[j]);
+                if (dst[j] >= 0) Slice<uint4>::fma(acc, w[j], val[j]);
         }
         float a = 0.0f;
 #pragma unroll
@@ -185,11 +183,11 @@ combine_mx_kernel(const float4 *__restrict__ y_perm, const int32_t *__restrict__
 }
 
 template <int KMAX>
-cudaError_t launch_mx(const float *y, const int32_t *dst, const float *w, int64_t T, int k, int slices,
+cudaError_t launch_mx(const moe_bf16_t *y, const int32_t *dst, const float *w, int64_t T, int k, int slices,
                       uint8_t *out_q, uint8_t *out_sf, cudaStream_t s) {
     const int64_t blocks = (T + kCombineWarps - 1) / kCombineWarps;
     launch_k(combine_mx_kernel<KMAX>, dim3((unsigned)blocks), dim3(kCombineWarps * 32), 0, s,
-             reinterpret_cast<const float4 *>(y), dst, w, T, k, slices, reinterpret_cast<uint2 *>(out_q), out_sf);
+             reinterpret_cast<const uint4 *>(y), dst, w, T, k, slices, reinterpret_cast<uint2 *>(out_q), out_sf);
     return cudaGetLastError();
 }
 
@@ -214,20 +212,9 @@ cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int
 
 }  // namespace moe
 
-extern "C" moe_status_t moe_unpermute_combine(const float *y_perm, const int32_t *dst_of_route,
+extern "C" moe_status_t moe_unpermute_combine(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                               const float *topk_w, int64_t T, int H, int k,
                                               moe_bf16_t *out, moe_stream_t stream) {
-    if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
-    if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
-    if (T == 0) return MOE_OK;
-    if (!y_perm || !dst_of_route || !out) return MOE_ERR_INVALID_ARG;   // topk_w may be null: plain sum
-    if (!moe::all_aligned16({y_perm, out})) return MOE_ERR_UNSUPPORTED;
-    return moe::cuda_status(moe::combine_rows(y_perm, dst_of_route, topk_w, T, H, k, out, (cudaStream_t)stream));
-}
-
-extern "C" moe_status_t moe_unpermute_combine_ybf16(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
-                                                    const float *topk_w, int64_t T, int H, int k,
-                                                    moe_bf16_t *out, moe_stream_t stream) {
     if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
     if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
@@ -237,7 +224,7 @@ extern "C" moe_status_t moe_unpermute_combine_ybf16(const moe_bf16_t *y_perm, co
                                                 H, k, out, (cudaStream_t)stream));
 }
 
-extern "C" moe_status_t moe_unpermute_combine_mxfp8(const float *y_perm, const int32_t *dst_of_route,
+extern "C" moe_status_t moe_unpermute_combine_mxfp8(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                                     const float *topk_w, int64_t T, int H, int k, uint8_t *out_q,
                                                     uint8_t *out_sf, moe_stream_t stream) {
     using namespace moe;
@@ -246,7 +233,7 @@ extern "C" moe_status_t moe_unpermute_combine_mxfp8(const float *y_perm, const i
     if (T == 0) return MOE_OK;
     if (!y_perm || !dst_of_route || !out_q || !out_sf) return MOE_ERR_INVALID_ARG;   // topk_w may be null
     if (reinterpret_cast<uintptr_t>(y_perm) % 16 || reinterpret_cast<uintptr_t>(out_q) % 8)
-        return MOE_ERR_UNSUPPORTED;
+        return MOE_ERR_UNSUPPORTED;   // 16-byte row loads, 8-byte code stores
     cudaStream_t s = (cudaStream_t)stream;
     const int sl = H / 8;
     cudaError_t e;

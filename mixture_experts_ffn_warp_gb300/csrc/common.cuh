@@ -2,6 +2,7 @@
 #pragma once
 
 #include <initializer_list>
+#include <mutex>
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
@@ -51,6 +52,36 @@ inline moe_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_O
 inline moe_status_t launch_status() { return cuda_status(cudaGetLastError()); }
 
 int device_sm_count();
+
+// Per-device launch set-up of one kernel (its shared-memory attribute, an occupancy
+// query), done once per device and read by every later launch on it.  Indexed by device
+// ordinal and filled under a mutex, so that host threads driving different GPUs through
+// the library never race on it.
+struct PerDeviceOnce {
+    static constexpr int kMaxDevices = 128;
+    std::mutex lock;
+    bool done[kMaxDevices] = {};
+    int value[kMaxDevices] = {};
+
+    // The value for the current device, computing it with init(&value) -> moe_status_t
+    // the first time; init failing leaves the device unset (retried by the next launch).
+    template <typename Init>
+    moe_status_t get(Init &&init, int *out) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+        if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+        std::lock_guard<std::mutex> g(lock);
+        if (!done[dev]) {
+            int v = 0;
+            const moe_status_t st = init(&v);
+            if (st != MOE_OK) return st;
+            value[dev] = v;
+            done[dev] = true;
+        }
+        *out = value[dev];
+        return MOE_OK;
+    }
+};
 
 // out[t] = bf16(sum_j w[t,j] * y[dst[t,j]]) over fp32 rows of y (w == nullptr: weights 1).
 cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int64_t T, int H, int k,

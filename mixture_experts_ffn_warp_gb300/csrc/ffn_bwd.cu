@@ -24,7 +24,7 @@ constexpr int kBwdWarps = 8;
 
 template <int KMAX>
 __global__ void __launch_bounds__(kBwdWarps * 32)
-combine_bwd_kernel(const uint4 *__restrict__ dY, const float4 *__restrict__ y_perm,
+combine_bwd_kernel(const uint4 *__restrict__ dY, const uint4 *__restrict__ y_perm,
                    const int32_t *__restrict__ dst_of_route, const float *__restrict__ topk_w, int64_t T,
                    int k, int slices, uint4 *__restrict__ dy_perm, float *__restrict__ d_topk_w) {
     pdl_wait();
@@ -65,11 +65,15 @@ combine_bwd_kernel(const uint4 *__restrict__ dY, const float4 *__restrict__ y_pe
 #pragma unroll
             for (int i = 0; i < 4; ++i) op[i] = __floats2bfloat162_rn(w[j] * d[2 * i], w[j] * d[2 * i + 1]);
             dy_perm[(int64_t)dst[j] * slices + s] = o;
-            if (want_dot) {
-                const float4 *yr = y_perm + ((int64_t)dst[j] * slices + s) * 2;
-                const float4 a = __ldg(yr), b = __ldg(yr + 1);
-                dot[j] += d[0] * a.x + d[1] * a.y + d[2] * a.z + d[3] * a.w + d[4] * b.x + d[5] * b.y +
-                          d[6] * b.z + d[7] * b.w;
+            if (want_dot) {   // bf16 expert output of the route, widened exactly
+                const uint4 yv = __ldg(y_perm + (int64_t)dst[j] * slices + s);
+                const __nv_bfloat162 *yp = reinterpret_cast<const __nv_bfloat162 *>(&yv);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(yp[i]);
+                    dot[j] = fmaf(d[2 * i], f.x, dot[j]);
+                    dot[j] = fmaf(d[2 * i + 1], f.y, dot[j]);
+                }
             }
         }
     }
@@ -96,11 +100,11 @@ __global__ void zero_pad_rows_kernel(const int32_t *__restrict__ group_sizes,
 }
 
 template <int KMAX>
-cudaError_t launch_combine_bwd(const moe_bf16_t *dY, const float *y_perm, const int32_t *dst, const float *w,
+cudaError_t launch_combine_bwd(const moe_bf16_t *dY, const moe_bf16_t *y_perm, const int32_t *dst, const float *w,
                                int64_t T, int H, int k, moe_bf16_t *dy_perm, float *d_topk_w, cudaStream_t s) {
     const int64_t blocks = (T + kBwdWarps - 1) / kBwdWarps;
     launch_k(combine_bwd_kernel<KMAX>, dim3((unsigned)blocks), dim3(kBwdWarps * 32), 0, s,
-             reinterpret_cast<const uint4 *>(dY), reinterpret_cast<const float4 *>(y_perm), dst, w, T, k, H / 8,
+             reinterpret_cast<const uint4 *>(dY), reinterpret_cast<const uint4 *>(y_perm), dst, w, T, k, H / 8,
              reinterpret_cast<uint4 *>(dy_perm), d_topk_w);
     return cudaGetLastError();
 }
@@ -118,7 +122,7 @@ int64_t token_block_bound(int64_t rows_cap, int E) { return (rows_cap + gp::BT -
 
 }  // namespace
 
-extern "C" moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const float *y_perm, const int32_t *dst_of_route,
+extern "C" moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                         const float *topk_w, const int32_t *group_sizes,
                                         const int32_t *group_offsets, int64_t T, int H, int E, int k,
                                         int64_t rows_cap, moe_bf16_t *dy_perm, float *d_topk_w,
@@ -366,7 +370,7 @@ extern "C" moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *d
 
 extern "C" moe_status_t moe_grouped_ffn_bwd(
     const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
-    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const float *y_perm,
+    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const moe_bf16_t *y_perm,
     const int32_t *dst_of_route, const int32_t *group_sizes, const int32_t *group_offsets, const float *topk_w,
     int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm, moe_bf16_t *dgu,
     float *dx_perm, moe_bf16_t *dx, float *dW_gate, float *dW_up, float *dW_down, float *d_topk_w, void *ws,

@@ -63,16 +63,16 @@ moe_status_t fc1_impl(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const 
 
 moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32_t *group_offsets,
                       const int32_t *src_of_row, const float *topk_w, int E, int H, int F, int64_t rows_cap,
-                      float *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream) {
+                      moe_bf16_t *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream) {
     moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!h || !W_down || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
-    // h [rows, F] x W_down [F, H] -> y_perm [rows, H]
+    // h [rows, F] x W_down [F, H] -> y_perm [rows, H], fp32 accumulation stored as bf16
     if (H % 256 == 0) {
         // CTA pairs: 256 output columns (M) x up to 256 tokens (N) per pair tile
         CUtensorMap tW, tX, tOut;
         if (!tmap_bf16_3d(&tW, W_down, H, F, E, 64, 64) || !tmap_bf16_2d(&tX, h, F, rows_cap, F, 64, 128) ||
-            !tmap_store_plain(&tOut, y_perm, 4, H, rows_cap, H, 32, 16))
+            !tmap_store_plain(&tOut, y_perm, 2, H, rows_cap, H, 32, 16))
             return MOE_ERR_UNSUPPORTED;
         gp::Args a{};
         a.group_offsets = group_offsets;
@@ -81,7 +81,7 @@ moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32
         a.N_out = H;
         a.n_fb = H / 256;
         a.rows_cap = rows_cap;
-        a.y = y_perm;
+        a.y16 = reinterpret_cast<__nv_bfloat16 *>(y_perm);
         a.route_w = topk_w;
         a.src_of_row = src_of_row;
         a.err = ws_error_word(ws);
@@ -91,7 +91,7 @@ moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32
     const int bn = 128;
     CUtensorMap tA, tB, tC;
     if (!tmap_bf16_2d(&tA, h, F, rows_cap, F, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, 64) ||
-        !tmap_store_2d(&tC, y_perm, 4, H, rows_cap, H))
+        !tmap_store_2d(&tC, y_perm, 2, H, rows_cap, H))
         return MOE_ERR_UNSUPPORTED;
     gg::Args b{};
     b.group_offsets = group_offsets;
@@ -100,7 +100,7 @@ moe_status_t fc2_impl(const moe_bf16_t *h, const moe_bf16_t *W_down, const int32
     b.K = F;
     b.n_tiles = H / bn;
     b.rows_cap = rows_cap;
-    b.out_f32 = y_perm;
+    b.out0 = reinterpret_cast<__nv_bfloat16 *>(y_perm);
     b.ld0 = H;
     b.route_w = topk_w;
     b.src_of_row = src_of_row;
@@ -127,7 +127,7 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const m
 
 extern "C" moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W_down,
                                         const int32_t *group_offsets, int E, int H, int F,
-                                        int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
+                                        int64_t rows_cap, moe_bf16_t *y_perm, void *ws, size_t ws_bytes,
                                         moe_stream_t stream) {
     return fc2_impl(h, W_down, group_offsets, nullptr, nullptr, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
 }
@@ -146,7 +146,7 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_weighted(const moe_bf16_t *x_perm
 extern "C" moe_status_t moe_grouped_fc2_weighted(const moe_bf16_t *h, const moe_bf16_t *W_down,
                                                  const int32_t *group_offsets, const int32_t *src_of_row,
                                                  const float *topk_w, int E, int H, int F, int64_t rows_cap,
-                                                 float *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream) {
+                                                 moe_bf16_t *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream) {
     if (rows_cap > 0 && (!src_of_row || !topk_w)) return MOE_ERR_INVALID_ARG;
     return fc2_impl(h, W_down, group_offsets, src_of_row, topk_w, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
 }
@@ -154,7 +154,7 @@ extern "C" moe_status_t moe_grouped_fc2_weighted(const moe_bf16_t *h, const moe_
 extern "C" moe_status_t moe_grouped_ffn_fwd(const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
                                             const moe_bf16_t *W_up, const moe_bf16_t *W_down,
                                             const int32_t *group_offsets, int E, int H, int F,
-                                            int64_t rows_cap, moe_bf16_t *h, float *y_perm,
+                                            int64_t rows_cap, moe_bf16_t *h, moe_bf16_t *y_perm,
                                             moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
                                             moe_stream_t stream) {
     moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);

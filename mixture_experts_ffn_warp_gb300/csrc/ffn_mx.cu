@@ -94,18 +94,17 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8_clamped(
 
 namespace {
 
-// FC2_MX into fp32 (y_f32) or bf16 (y_bf16) rows of y_perm; exactly one is non-null.
+// FC2_MX: y_perm rows in bf16 (fp32 accumulation, one rounding per element).
 moe_status_t fc2_mx_impl(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q, const uint8_t *Wd_sf,
-                         const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap, float *y_f32,
-                         moe_bf16_t *y_bf16, void *ws, size_t ws_bytes, moe_stream_t stream) {
+                         const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap, moe_bf16_t *y_perm,
+                         void *ws, size_t ws_bytes, moe_stream_t stream) {
     moe_status_t st = check_mx(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
-    if (!h_q || !h_sf || !Wd_q || !Wd_sf || !group_offsets || (!y_f32 && !y_bf16)) return MOE_ERR_INVALID_ARG;
+    if (!h_q || !h_sf || !Wd_q || !Wd_sf || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
     if (!aligned16(h_sf) || !aligned16(Wd_sf) || !aligned16(Wd_q)) return MOE_ERR_UNSUPPORTED;
     const int bn = (H % 256 == 0) ? 256 : 128;
     CUtensorMap tA, tC;
-    if (!tmap_u8_2d(&tA, h_q, F, rows_cap, F, 128, 128) ||
-        !(y_bf16 ? tmap_store_2d(&tC, y_bf16, 2, H, rows_cap, H) : tmap_store_2d(&tC, y_f32, 4, H, rows_cap, H)))
+    if (!tmap_u8_2d(&tA, h_q, F, rows_cap, F, 128, 128) || !tmap_store_2d(&tC, y_perm, 2, H, rows_cap, H))
         return MOE_ERR_UNSUPPORTED;
     gg::Args a{};
     a.group_offsets = group_offsets;
@@ -118,8 +117,7 @@ moe_status_t fc2_mx_impl(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t 
     a.sfb0 = Wd_sf;
     a.b0_tiles = Wd_q;
     a.nb_rows = H;
-    a.out_f32 = y_f32;
-    a.out0 = reinterpret_cast<__nv_bfloat16 *>(y_bf16);
+    a.out0 = reinterpret_cast<__nv_bfloat16 *>(y_perm);
     a.ld0 = H;
     a.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
@@ -131,25 +129,16 @@ moe_status_t fc2_mx_impl(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t 
 
 extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
                                               const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H, int F,
-                                              int64_t rows_cap, float *y_perm, void *ws, size_t ws_bytes,
+                                              int64_t rows_cap, moe_bf16_t *y_perm, void *ws, size_t ws_bytes,
                                               moe_stream_t stream) {
-    return fc2_mx_impl(h_q, h_sf, Wd_q, Wd_sf, group_offsets, E, H, F, rows_cap, y_perm, nullptr, ws, ws_bytes,
-                       stream);
-}
-
-extern "C" moe_status_t moe_grouped_fc2_mxfp8_ybf16(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t *Wd_q,
-                                                    const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H,
-                                                    int F, int64_t rows_cap, moe_bf16_t *y_perm, void *ws,
-                                                    size_t ws_bytes, moe_stream_t stream) {
-    return fc2_mx_impl(h_q, h_sf, Wd_q, Wd_sf, group_offsets, E, H, F, rows_cap, nullptr, y_perm, ws, ws_bytes,
-                       stream);
+    return fc2_mx_impl(h_q, h_sf, Wd_q, Wd_sf, group_offsets, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
 }
 
 extern "C" moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t *Wg_q,
                                                   const uint8_t *Wg_sf, const uint8_t *Wu_q, const uint8_t *Wu_sf,
                                                   const uint8_t *Wd_q, const uint8_t *Wd_sf,
                                                   const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap,
-                                                  uint8_t *h_q, uint8_t *h_sf, float *y_perm, void *ws,
+                                                  uint8_t *h_q, uint8_t *h_sf, moe_bf16_t *y_perm, void *ws,
                                                   size_t ws_bytes, moe_stream_t stream) {
     moe_status_t st = moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, E, H, F,
                                                    rows_cap, h_q, h_sf, nullptr, ws, ws_bytes, stream);

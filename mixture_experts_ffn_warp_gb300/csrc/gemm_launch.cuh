@@ -14,14 +14,17 @@ moe_status_t launch(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorM
     using C = Cfg<OP, BN>;
     if (tiles_bound <= 0) return MOE_OK;
     auto kern = grouped_gemm_kernel<OP, BN>;
-    static int configured_dev = -1;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (configured_dev != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        configured_dev = dev;
-    }
+    static PerDeviceOnce once;   // per device: the smem attribute set
+    int unused = 0;
+    const moe_status_t st = once.get(
+        [&](int *) {
+            return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) ==
+                           cudaSuccess
+                       ? MOE_OK
+                       : MOE_ERR_CUDA;
+        },
+        &unused);
+    if (st != MOE_OK) return st;
     const int64_t sms = device_sm_count();
     const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
     launch_k(kern, dim3(grid), dim3(kThreads), C::SMEM_BYTES, s, a, b0, b1, c0, c1, args);

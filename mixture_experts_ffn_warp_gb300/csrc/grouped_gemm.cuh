@@ -14,14 +14,14 @@
 //
 // Ops (A row = one permuted route unless stated):
 //   FC1_SWIGLU     h = silu(x W_gate) * (x W_up)        M-grouped, K = H
-//   FC2            y = h W_down (fp32 out)              M-grouped, K = F
+//   FC2            y = h W_down (bf16 out)              M-grouped, K = F
 //   DGRAD_DSWIGLU  dh = dy W_down^T, then dSwiGLU       M-grouped, K = H
 //   DGRAD_FC1      dx = dg W_gate^T + du W_up^T (fp32)   M-grouped, K = 2F
 //   WGRAD_DOWN     dW_down[e] = h_e^T dy_e (fp32)        K-grouped (K = rows of e)
 //   WGRAD_GATEUP   [dW_gate|dW_up][e] = x_e^T [dg|du]_e K-grouped
 //   FC1_MX         FC1_SWIGLU on MXFP8 operands; h is quantised to MXFP8 (along F)
 //                  in the epilogue, scales written in the MMA tile layout
-//   FC2_MX         FC2 on MXFP8 operands (fp32 out)
+//   FC2_MX         FC2 on MXFP8 operands (bf16 out)
 // ("Add MoE + expert-parallel Python API surface, PyTorch reference, and
 // tests", Summary: SwiGLU experts, fc1_c stash, backward, MXFP8 operands;
 // "[Draft][JAX] MoE block optimization": fused grouped GEMM + SwiGLU and
@@ -66,8 +66,8 @@ struct Args {
     int k_split;      // DGRAD_FC1: K index where B switches from W_gate to W_up (= F)
     int n_split;      // WGRAD_GATEUP: column where output switches from out0 to out1 (= F)
     int64_t rows_cap; // rows of the permuted tensors
-    __nv_bfloat16 *out0;   // FC1: h; DSWIGLU: [dg | du]; FC2_MX: y_perm in bf16 (else out_f32)
-    float *out_f32;        // FC2: y_perm; DGRAD_FC1: dx_perm; WGRAD: dW_down / dW_gate (row pitch ld0)
+    __nv_bfloat16 *out0;   // FC1: h; DSWIGLU: [dg | du]; FC2, FC2_MX: y_perm
+    float *out_f32;        // DGRAD_FC1: dx_perm; WGRAD: dW_down / dW_gate (row pitch ld0)
     int64_t ld0;
     __nv_bfloat16 *out1;   // FC1, FC1_MX: fc1_c stash (nullable)
     float *out1_f32;       // WGRAD_GATEUP: dW_up (row pitch ld1)
@@ -701,8 +701,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                         stage_f32x32(d, second ? &tmC1 : &tmC0, second ? n - args.n_split : n, grow0);
                     }
                 }
-            } else {   // FC2, FC2_MX (y_perm) and DGRAD_FC1 (dx_perm): fp32 rows of the group
-                       // (FC2_MX with out0 set: bf16 rows)
+            } else {   // FC2, FC2_MX (y_perm: bf16 rows) and DGRAD_FC1 (dx_perm: fp32 rows)
                 static_assert(OP == Op::FC2 || OP == Op::FC2_MX || OP == Op::DGRAD_FC1, "unhandled op");
                 const int64_t row = tl.m0 + r;
                 const bool valid = row < tl.m_end && row < args.rows_cap;
@@ -722,7 +721,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     }
                     const int n = tl.n0 + c;
                     if (n < args.N) {
-                        if (OP == Op::FC2_MX && args.out0) {
+                        if constexpr (OP == Op::FC2 || OP == Op::FC2_MX) {
                             float v[32];
 #pragma unroll
                             for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(d[i]);

@@ -18,8 +18,8 @@
 //   warp 1      MMA issuer (one lane of the first CTA only); TMEM (512 columns, two
 //               accumulators of up to 256 columns) allocated by warp 1 of both CTAs
 //   warps 2..5  epilogue in each CTA: tcgen05.ld of its 128 lanes -> SwiGLU / scaling ->
-//               shared-memory staging -> TMA stores (row by row only at an expert's last
-//               token block)
+//               bf16 (h, y_perm) or fp32 (dx_perm) -> shared-memory staging -> TMA stores
+//               (row by row only at an expert's last token block)
 //
 // FC1: CTA c of the pair holds, for the 128 features [128 fb, 128 fb + 128) of the tile,
 // gate rows of features 128 fb + 64 c + [0, 64) in TMEM lanes 0..63 and the up rows of the
@@ -72,11 +72,12 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 // Epilogue shared memory: FC1 exchange buffers (2 warp pairs x 2 chunk parities x 2
 // directions x 16 tokens x 32 features fp32 = 16 KB) and output staging, two slots per
-// epilogue warp of 16 token rows (FC1 bf16 rows of 64 B, FC2 fp32 rows of 128 B).
+// epilogue warp of 16 token rows (FC1 and FC2 bf16 rows of 64 B, DGRAD_FC1 fp32 rows of
+// 128 B).
 template <Op OP>
 struct PCfg {
     static constexpr int XBUF_BYTES = OP == Op::FC1 ? 2 * 2 * 2 * 16 * 32 * 4 : 0;
-    static constexpr int SLOT_BYTES = OP == Op::FC1 ? 16 * 64 : 16 * 128;   // WGRAD: 32 rows x 64 B
+    static constexpr int SLOT_BYTES = (OP == Op::FC1 || OP == Op::FC2) ? 16 * 64 : 16 * 128;   // WGRAD: 32 rows x 64 B
     static constexpr int STG_BYTES = 4 * 2 * SLOT_BYTES;
     // WGRAD: the K-tail buffer, outside the ring: 2 operands x 2 MN chunks x 16 K rows x 128 B
     static constexpr int TAIL_BYTES = OP == Op::WGRAD ? 2 * 2 * 16 * 128 : 0;
@@ -104,7 +105,8 @@ struct Args {
     int64_t rows_cap;  // rows of the permuted tensors
     __nv_bfloat16 *h;        // FC1: h [rows, F]
     __nv_bfloat16 *stash;    // FC1: [g | u] bf16 [rows, 2F] (nullable)
-    float *y;                // FC2: y_perm [rows, H]; DGRAD_FC1: dx_perm [rows, H]
+    __nv_bfloat16 *y16;      // FC2: y_perm bf16 [rows, H]
+    float *y;                // DGRAD_FC1: dx_perm fp32 [rows, H]
     // router weight of each row's route applied in the epilogue (padding rows get 0); null = unweighted
     const float *route_w;
     const int32_t *src_of_row;
@@ -725,7 +727,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                     store_bf16x16(hv, &tmOut, args.h, F, fcol, tl.t0 + tok0, nv);
                 }
                 if (!alive) break;
-            } else {   // FC2 (y_perm) and DGRAD_FC1 (dx_perm): fp32 rows
+            } else {   // FC2 (y_perm, bf16 rows) and DGRAD_FC1 (dx_perm, fp32 rows)
                 const int H = args.N_out;
                 const int hcol = tl.fb * 256 + (int)rank * 128 + q * 32;   // this warp's 32 output columns
 #pragma unroll 1
@@ -744,7 +746,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
 #pragma unroll
                             for (int t = 0; t < 16; ++t) v[t] *= route_weight(tl.t0 + tok0 + t, t < nv);
                         }
-                        if (nv >= 16) {
+                        if constexpr (OP == Op::FC2) {
+                            store_bf16x16(v, &tmOut, args.y16, H, hcol, tl.t0 + tok0, nv);
+                        } else if (nv >= 16) {
                             slot_open();
                             float *w = reinterpret_cast<float *>(stg + slot * SLOT_BYTES);
 #pragma unroll
@@ -793,29 +797,28 @@ moe_status_t launch(const CUtensorMap &w0, const CUtensorMap &w1, const CUtensor
     if (tiles_bound <= 0) return MOE_OK;
     auto kern = pair_gemm_kernel<OP>;
     constexpr int smem = PCfg<OP>::SMEM_BYTES;
-    static int configured_dev = -1;
-    static int max_clusters = 0;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (configured_dev != dev) {
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
-            return MOE_ERR_CUDA;
-        cudaLaunchConfig_t q{};
-        q.gridDim = dim3(2);
-        q.blockDim = dim3(kThreads);
-        q.dynamicSmemBytes = smem;
-        cudaLaunchAttribute qa[1];
-        qa[0].id = cudaLaunchAttributeClusterDimension;
-        qa[0].val.clusterDim.x = 2;
-        qa[0].val.clusterDim.y = 1;
-        qa[0].val.clusterDim.z = 1;
-        q.attrs = qa;
-        q.numAttrs = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess || n < 1) return MOE_ERR_CUDA;
-        max_clusters = n;
-        configured_dev = dev;
-    }
+    static PerDeviceOnce once;   // per device: the smem attribute set, resident clusters counted
+    int max_clusters = 0;
+    const moe_status_t st = once.get(
+        [&](int *n) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+                return MOE_ERR_CUDA;
+            cudaLaunchConfig_t q{};
+            q.gridDim = dim3(2);
+            q.blockDim = dim3(kThreads);
+            q.dynamicSmemBytes = smem;
+            cudaLaunchAttribute qa[1];
+            qa[0].id = cudaLaunchAttributeClusterDimension;
+            qa[0].val.clusterDim.x = 2;
+            qa[0].val.clusterDim.y = 1;
+            qa[0].val.clusterDim.z = 1;
+            q.attrs = qa;
+            q.numAttrs = 1;
+            if (cudaOccupancyMaxActiveClusters(n, kern, &q) != cudaSuccess || *n < 1) return MOE_ERR_CUDA;
+            return MOE_OK;
+        },
+        &max_clusters);
+    if (st != MOE_OK) return st;
     const int64_t G = tiles_bound < max_clusters ? tiles_bound : max_clusters;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((unsigned)(2 * G));

@@ -504,6 +504,8 @@ extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx
 
 #include <mutex>
 
+#include <cudaTypedefs.h>
+
 namespace moe {
 namespace {
 
@@ -516,21 +518,56 @@ static __device__ __align__(256) unsigned char g_permute_scratch[kStaticScratchB
 
 constexpr int kMaxScratchDevices = 128;
 std::mutex g_scratch_lock;
-void *g_scratch_addr[kMaxScratchDevices];   // device address of the array, per device
+struct ScratchSlot {
+    unsigned long long ctx_id;   // the context the address belongs to (0: none yet)
+    void *addr;                  // device address of the array in that context
+};
+ScratchSlot g_scratch[kMaxScratchDevices];
 
-// Device address of the array on the current device, looked up once per
-// device (the host-side name is only a stand-in and must not reach a kernel).
+// Id of the calling thread's current CUDA context (cuCtxGetId: unique within the process
+// and never reused, so a context created after a cudaDeviceReset gets a new one); false
+// when no context is current yet.  Driver entry points fetched once, under the lock.
+bool current_context_id(unsigned long long *id) {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    if (!get_current || !get_id) {
+        void *p = nullptr, *q = nullptr;
+        cudaDriverEntryPointQueryResult r1, r2;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &r1) != cudaSuccess ||
+            r1 != cudaDriverEntryPointSuccess ||
+            cudaGetDriverEntryPointByVersion("cuCtxGetId", &q, 12000, cudaEnableDefault, &r2) != cudaSuccess ||
+            r2 != cudaDriverEntryPointSuccess)
+            return false;
+        get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(q);
+    }
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || !ctx) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// Device address of the array in the current device's current context.  The host-side
+// name is only a stand-in and must not reach a kernel; the address is looked up with
+// cudaGetSymbolAddress the first time a context calls, and again whenever the device's
+// context changes (a cudaDeviceReset, or a caller that made another context current),
+// since the module then lives elsewhere.
 moe_status_t static_scratch(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (dev < 0 || dev >= kMaxScratchDevices) return MOE_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> guard(g_scratch_lock);
-    if (!g_scratch_addr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
-        g_scratch_addr[dev] = p;
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
+    if (have_ctx && g_scratch[dev].addr && g_scratch[dev].ctx_id == ctx) {
+        *out = g_scratch[dev].addr;
+        return MOE_OK;
     }
-    *out = g_scratch_addr[dev];
+    void *p = nullptr;   // the lookup also makes the device's primary context current if none was
+    if (cudaGetSymbolAddress(&p, g_permute_scratch) != cudaSuccess || !p) return MOE_ERR_CUDA;
+    if (!have_ctx && !current_context_id(&ctx)) return MOE_ERR_CUDA;
+    g_scratch[dev].ctx_id = ctx;
+    g_scratch[dev].addr = p;
+    *out = p;
     return MOE_OK;
 }
 

@@ -16,8 +16,7 @@ from ._binding import (SCORE_SIGMOID, SCORE_SOFTMAX, Permutation, PermutationMX,
                        moe_dequantize_rows_mxfp8, moe_dequantize_weights_mxfp8, moe_unpermute_combine_mxfp8,
                        moe_quantize_weights_mxfp8, mx_tile_scale_bytes,
                        moe_grouped_dgrad_fc2_dswiglu, moe_grouped_fc1_swiglu, moe_grouped_fc2,
-                       moe_grouped_wgrad, moe_permute, moe_route_topk, moe_unpermute_combine, moe_unpermute_combine_ybf16,
-                       moe_grouped_fc2_mxfp8_ybf16,
+                       moe_grouped_wgrad, moe_permute, moe_route_topk, moe_unpermute_combine,
                        moe_unpermute_sum, rows_capacity)
 
 
@@ -64,7 +63,7 @@ class MoeForward:
             group_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev),
             rows_cap=cap, align=align)
         self.h = torch.empty(cap, F, dtype=torch.bfloat16, device=dev)
-        self.y_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
+        self.y_perm = torch.empty(cap, H, dtype=torch.bfloat16, device=dev)
         self.fc1_c = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev) if keep_fc1_c else None
         _output_buffers(self, out_format, T, H, dev)
 
@@ -123,8 +122,7 @@ def _output_buffers(m, out_format: str, T: int, H: int, dev):
 
 def _combine(m, w, stream):
     if m.out_format == "bf16":
-        combine = moe_unpermute_combine_ybf16 if m.y_perm.dtype == torch.bfloat16 else moe_unpermute_combine
-        combine(m.y_perm, m.perm.dst_of_route, w, out=m.out, stream=stream)
+        moe_unpermute_combine(m.y_perm, m.perm.dst_of_route, w, out=m.out, stream=stream)
     else:
         moe_unpermute_combine_mxfp8(m.y_perm, m.perm.dst_of_route, w, out_q=m.out_q, out_sf=m.out_sf, stream=stream)
 
@@ -229,9 +227,8 @@ class MxWeights:
 class MoeForwardMX:
     """Pre-allocated MXFP8 forward: route -> quantising permute -> block-scaled
     FC1 + SwiGLU (h to MXFP8) -> block-scaled FC2 -> combine (bf16 out).
-    router / expert_bias / normalize as for MoeForward.  y_perm is stored as bf16
-    (moe_grouped_fc2_mxfp8_ybf16) unless the forward keeps what the backward reads
-    (keep_fc1_c) or encodes its output as MXFP8, which read fp32 y_perm."""
+    router / expert_bias / normalize as for MoeForward.  y_perm (the expert outputs)
+    is bf16, as on the bf16 path."""
 
     def __init__(self, T: int, H: int, F: int, E: int, k: int, device="cuda", router: str = "softmax",
                  expert_bias=None, normalize: bool = True, keep_fc1_c: bool = False, out_format: str = "bf16",
@@ -258,8 +255,7 @@ class MoeForwardMX:
             group_offsets=torch.empty(E + 1, dtype=torch.int32, device=dev), rows_cap=cap)
         self.h_q = torch.empty(cap, F, dtype=torch.uint8, device=dev)
         self.h_sf = torch.zeros(mx_tile_scale_bytes(cap, E, F), dtype=torch.uint8, device=dev)
-        y_bf16 = out_format == "bf16" and not keep_fc1_c
-        self.y_perm = torch.empty(cap, H, dtype=torch.bfloat16 if y_bf16 else torch.float32, device=dev)
+        self.y_perm = torch.empty(cap, H, dtype=torch.bfloat16, device=dev)
         _output_buffers(self, out_format, T, H, dev)
         self.fc1_c = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev) if keep_fc1_c else None
 
@@ -274,8 +270,8 @@ class MoeForwardMX:
                                      self.h_q, self.h_sf, fc1_c=self.fc1_c, stream=stream, clamp=self.swiglu_clamp)
 
     def fc2(self, w: MxWeights, stream=None):
-        fc2 = moe_grouped_fc2_mxfp8_ybf16 if self.y_perm.dtype == torch.bfloat16 else moe_grouped_fc2_mxfp8
-        fc2(self.h_q, self.h_sf, w.Wd_q, w.Wd_sf, self.perm.group_offsets, self.ws, self.y_perm, stream=stream)
+        moe_grouped_fc2_mxfp8(self.h_q, self.h_sf, w.Wd_q, w.Wd_sf, self.perm.group_offsets, self.ws, self.y_perm,
+                              stream=stream)
 
     def combine(self, stream=None):
         _combine(self, self.topk_w, stream)

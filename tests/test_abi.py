@@ -104,7 +104,6 @@ def test_host_validation_before_launch(lib):
     assert lib.moe_permute(fake, fake, 4, 16, 4, 2, 1, mis, 8, fake, fake, fake, fake, nul, 0, nul) == 2
     assert lib.moe_unpermute_combine(mis, fake, nul, 3, 16, 2, fake, nul) == 2
     assert lib.moe_unpermute_combine(fake, fake, nul, 3, 16, 2, mis, nul) == 2
-    assert lib.moe_unpermute_combine_ybf16(mis, fake, nul, 3, 16, 2, fake, nul) == 2
     assert lib.moe_unpermute_sum(mis, fake, 3, 16, 2, fake, nul) == 2
 
 

@@ -27,7 +27,7 @@ pytestmark = pytest.mark.gpu
 def test_combine_mxfp8_bit_exact(T, H, k, drop, plain):
     g = torch.Generator(device="cuda").manual_seed(T + H + k)
     rows = T * k
-    y = torch.randn(rows, H, generator=g, device="cuda") * 3.0
+    y = (torch.randn(rows, H, generator=g, device="cuda") * 3.0).to(torch.bfloat16)
     y[5] *= 1e-6                                             # a row of tiny values
     dst = torch.randperm(rows, generator=g, device="cuda").to(torch.int32).reshape(T, k)
     if drop:
@@ -37,7 +37,7 @@ def test_combine_mxfp8_bit_exact(T, H, k, drop, plain):
     q, sf = moe_unpermute_combine_mxfp8(y, dst, w)
     torch.cuda.synchronize()
     wn = np.ones((T, k), np.float32) if plain else w.cpu().numpy()
-    rq, rs = oracle.unpermute_combine_mxfp8(y.cpu().numpy(), dst.cpu().numpy(), wn)
+    rq, rs = oracle.unpermute_combine_mxfp8(y.float().cpu().numpy(), dst.cpu().numpy(), wn)
     assert np.array_equal(sf.cpu().numpy(), rs)
     assert np.array_equal(q.cpu().numpy(), rq)
 
@@ -60,7 +60,7 @@ def test_forward_with_mxfp8_output(mx_path):
     torch.cuda.synchronize()
     assert m.ws.read_error() == 0
     # codes and scales: the oracle's encoding of this layer's own expert outputs
-    rq, rs = oracle.unpermute_combine_mxfp8(m.y_perm.cpu().numpy(), m.perm.dst_of_route.cpu().numpy(),
+    rq, rs = oracle.unpermute_combine_mxfp8(m.y_perm.float().cpu().numpy(), m.perm.dst_of_route.cpu().numpy(),
                                             m.topk_w.cpu().numpy())
     assert np.array_equal(q.cpu().numpy(), rq) and np.array_equal(sf.cpu().numpy(), rs)
     vals = oracle.mx_dequantize(q.cpu().numpy(), sf.cpu().numpy())

@@ -155,7 +155,7 @@ def test_mxfp8_forward_parity_small(name):
                                round_mode=2, want_y=True)
     assert_close_rms(to_f64(out), ref["out"], tol=TOL_MXFP8, what="out", bf16_out=True)
     dst = torch.from_numpy(m.perm.dst_of_route.cpu().numpy().reshape(-1).astype(np.int64)).cuda()
-    assert_close_rms(m.y_perm[dst].double().cpu().numpy(), ref["y"], tol=TOL_MXFP8, what="y_perm")
+    assert_close_rms(to_f64(m.y_perm[dst]), ref["y"], tol=TOL_MXFP8, what="y_perm")
 
 
 def test_mxfp8_forward_dsv3_full_size_sampled():
@@ -186,23 +186,23 @@ def test_mxfp8_forward_dsv3_full_size_sampled():
     assert_close_rms(to_f64(out[torch.from_numpy(toks).cuda()]), ref["out"], tol=TOL_MXFP8, what="dsv3 out", bf16_out=True)
 
 
-def test_mxfp8_bf16_y_perm_is_the_rounded_fp32_one():
-    """The MXFP8 forward stores y_perm in bf16 unless it keeps what the backward reads:
-    the same inputs through both layers give the bf16 rows as the round-to-nearest-even
-    of the fp32 rows, bit for bit, and the combine over bf16 rows equals the fp32
-    combine of the same values widened (one fp32 slot-order sum)."""
-    shape = small_shape("ybf16", T=600, H=256, F=384, E=6, k=3, mxfp8=True)
+def test_mxfp8_stash_leaves_the_forward_unchanged():
+    """Keeping the bf16 g | u stash for the straight-through backward changes nothing in
+    the forward: y_perm and the output are bit-identical with and without it, and the
+    combine over the bf16 rows is the plain combine of the same rows."""
+    shape = small_shape("ystash", T=600, H=256, F=384, E=6, k=3, mxfp8=True)
     inp = gpu_inputs(shape, with_dy=False)
     w = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"])
-    m16 = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k)
-    m32 = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k, keep_fc1_c=True)
-    assert m16.y_perm.dtype == torch.bfloat16 and m32.y_perm.dtype == torch.float32
-    out16 = m16(inp["x"], inp["logits"], w)
-    m32(inp["x"], inp["logits"], w)
+    m0 = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k)
+    m1 = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k, keep_fc1_c=True)
+    assert m0.y_perm.dtype == torch.bfloat16 and m1.y_perm.dtype == torch.bfloat16
+    out0 = m0(inp["x"], inp["logits"], w)
+    out1 = m1(inp["x"], inp["logits"], w)
     torch.cuda.synchronize()
-    assert m16.ws.read_error() == 0 and m32.ws.read_error() == 0
-    rows = int(m16.perm.group_offsets[-1].item())
+    assert m0.ws.read_error() == 0 and m1.ws.read_error() == 0
+    rows = int(m0.perm.group_offsets[-1].item())
     assert rows == shape.T * shape.k
-    assert torch.equal(m16.y_perm[:rows], m32.y_perm[:rows].to(torch.bfloat16))
-    ref = moe_unpermute_combine(m16.y_perm.float(), m16.perm.dst_of_route, m16.topk_w)
-    assert torch.equal(out16, ref)
+    assert torch.equal(m0.y_perm[:rows], m1.y_perm[:rows])
+    assert torch.equal(out0, out1)
+    ref = moe_unpermute_combine(m0.y_perm, m0.perm.dst_of_route, m0.topk_w)
+    assert torch.equal(out0, ref)

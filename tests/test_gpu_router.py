@@ -28,17 +28,37 @@ def _inputs(T, E, k, seed):
     return logits, bias, dw
 
 
-def _check_selection(idx_gpu, idx_ref, keys, k):
-    """Equal rows must dominate; rows that differ must still be a valid top-k of
-    the double keys up to fp32 rounding of the keys."""
+def _check_selection(idx_gpu, idx_ref, keys, k, tol=1e-6):
+    """Equal rows must dominate.  A row that differs (two keys within fp32 rounding of each
+    other: the GPU ranks fp32 keys, the oracle double ones) must still be a valid ranked
+    top-k of the double keys up to `tol`: k distinct ids; every unselected key at most the
+    smallest selected one (+ tol); slots in descending key order (up to tol); and where two
+    keys are exactly equal in double, the lower id first, an unselected id never below a
+    selected one of the same key."""
     diff = np.nonzero((idx_gpu != idx_ref).any(1))[0]
     assert len(diff) <= max(2, len(idx_ref) // 500), f"{len(diff)} rows differ"
+    E = keys.shape[1]
     for t in diff:
         sel = idx_gpu[t]
-        assert len(set(sel.tolist())) == k and (sel >= 0).all() and (sel < keys.shape[1]).all()
-        kth = np.sort(keys[t])[::-1][k - 1]
-        assert (keys[t, sel] >= kth - 1e-6).all(), (t, keys[t, sel], kth)
+        assert len(set(sel.tolist())) == k and (sel >= 0).all() and (sel < E).all(), (t, sel)
+        ks = keys[t, sel]
+        rest = np.setdiff1d(np.arange(E), sel)
+        assert (keys[t, rest] <= ks.min() + tol).all(), (t, ks, keys[t, rest].max())
+        for j in range(k - 1):
+            assert ks[j] >= ks[j + 1] - tol, (t, j, ks)
+            if ks[j] == ks[j + 1]:
+                assert sel[j] < sel[j + 1], (t, j, sel)
+        for e in rest:
+            same = sel[ks == keys[t, e]]
+            assert (same < e).all(), (t, e, same)
     return diff
+
+
+def _sigmoid_weights_of(idx, lg, normalize):
+    """Weights of a given selection in double: the selected unbiased sigmoid scores,
+    divided by (their sum + 1e-20) when normalising."""
+    s = 1.0 / (1.0 + np.exp(-np.take_along_axis(lg.astype(np.float64), idx.astype(np.int64), axis=1)))
+    return s / (s.sum(1, keepdims=True) + 1e-20) if normalize else s
 
 
 @pytest.mark.parametrize("name", list(SHAPES))
@@ -57,6 +77,8 @@ def test_sigmoid_router_matches_oracle(name, use_bias, normalize):
     diff = _check_selection(idx, ref_idx, keys, k)
     same = np.setdiff1d(np.arange(T), diff)
     assert np.abs(w[same] - ref_w[same]).max() <= 2e-6
+    # every row's weights, those of differing rows included, from the GPU's own selection
+    assert np.abs(w - _sigmoid_weights_of(idx, lg, normalize)).max() <= 2e-6
 
 
 def test_sigmoid_router_special_rows():

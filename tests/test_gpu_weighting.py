@@ -45,8 +45,7 @@ def test_early_weighting_matches_oracle(name, at):
     if at == "fc1":
         assert_close_ulp(to_f64(m.h[torch.from_numpy(rows).cuda()]), ref["h"][routes], what="weighted h", slack=4e-3)
     else:
-        assert_close_rms(m.y_perm[torch.from_numpy(rows).cuda()].double().cpu().numpy(), ref["y"][routes],
-                         what="weighted y")
+        assert_close_ulp(to_f64(m.y_perm[torch.from_numpy(rows).cuda()]), ref["y"][routes], what="weighted y")
     pad = np.nonzero(src < 0)[0]
     if len(pad):   # padding rows inside the groups carry weight 0
         t = m.h if at == "fc1" else m.y_perm
@@ -55,7 +54,7 @@ def test_early_weighting_matches_oracle(name, at):
 
 def test_early_weighting_agrees_with_late_weighting():
     """The three placements are one function; on the GPU they agree to the bf16
-    rounding of h (fc2 and combine placements share every rounding)."""
+    roundings of the weighted h (FC1) or the weighted y (FC2) against the unweighted ones."""
     shape = small_shape("agree", T=400, H=256, F=256, E=8, k=3)
     inp = gpu_inputs(shape, with_dy=False)
     outs = {}
@@ -64,7 +63,7 @@ def test_early_weighting_agrees_with_late_weighting():
         outs[at] = to_f64(m(inp["x"], inp["logits"], inp["W_gate"], inp["W_up"], inp["W_down"]).clone())
     torch.cuda.synchronize()
     rms = np.sqrt((outs["combine"] ** 2).mean())
-    assert np.abs(outs["fc2"] - outs["combine"]).max() <= 2.0 ** -7 * np.abs(outs["combine"]).max() + 1e-3 * rms
+    assert np.abs(outs["fc2"] - outs["combine"]).max() <= 2.0 ** -7 * np.abs(outs["combine"]).max() + 2e-2 * rms
     assert np.abs(outs["fc1"] - outs["combine"]).max() <= 2.0 ** -7 * np.abs(outs["combine"]).max() + 2e-2 * rms
 
 

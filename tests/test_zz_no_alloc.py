@@ -15,6 +15,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from mixture_experts_ffn_warp_gb300 import Workspace, load_library, moe_permute, moe_route_topk
 
 pytestmark = pytest.mark.gpu
@@ -24,13 +25,9 @@ def _p(t):
     return C.c_void_p(t.data_ptr())
 
 
-def _static_permute(x, idx, E, align=1):
-    L = load_library()
-    T, H = x.shape
-    k = idx.shape[1]
+def _outputs(T, H, E, k, align, dev):
     cap = T * k + E * (align - 1)
-    dev = x.device
-    out = {
+    return {
         "x_perm": torch.zeros(cap, H, dtype=torch.bfloat16, device=dev),
         "dst_of_route": torch.empty(T, k, dtype=torch.int32, device=dev),
         "src_of_row": torch.full((cap,), -7, dtype=torch.int32, device=dev),
@@ -38,6 +35,15 @@ def _static_permute(x, idx, E, align=1):
         "group_offsets": torch.empty(E + 1, dtype=torch.int32, device=dev),
         "err": torch.full((1,), 0xFF, dtype=torch.int32, device=dev),
     }
+
+
+def _static_permute(x, idx, E, align=1, out=None):
+    L = load_library()
+    T, H = x.shape
+    k = idx.shape[1]
+    cap = T * k + E * (align - 1)
+    if out is None:
+        out = _outputs(T, H, E, k, align, x.device)
     st = L.moe_permute_static_scratch(
         _p(x), _p(idx), T, H, E, k, align, _p(out["x_perm"]), cap, _p(out["dst_of_route"]),
         _p(out["src_of_row"]), _p(out["group_sizes"]), _p(out["group_offsets"]), _p(out["err"]),
@@ -58,6 +64,12 @@ def _compare(x, idx, E, align=1):
     assert torch.equal(got["src_of_row"][:used], ref.src_of_row[:used])
     assert torch.equal(got["x_perm"][:used], ref.x_perm[:used])
     assert int(got["err"].item()) == ws.read_error()
+    # and the maps against the CPU oracle's stable counting sort
+    want = oracle.permute(idx.cpu().numpy(), E, align=align)
+    assert np.array_equal(got["group_sizes"].cpu().numpy(), want["group_sizes"])
+    assert np.array_equal(got["group_offsets"].cpu().numpy(), want["group_offsets"])
+    assert np.array_equal(got["dst_of_route"].cpu().numpy(), want["dst_of_route"])
+    assert np.array_equal(got["src_of_row"][:used].cpu().numpy(), want["src_of_row"][:used])
     return got
 
 
@@ -93,11 +105,40 @@ def test_static_scratch_reports_bad_ids_and_clears_them():
     assert int(got["err"].item()) == 0          # the shared error word restarts at zero
 
 
+def test_static_scratch_allocates_nothing():
+    """After a first call (the address lookup, and the lazy loading of the kernels it
+    launches), a second call of the same shape leaves the device's free memory unchanged:
+    no allocation by the library, torch's caching allocator idle in between."""
+    g = torch.Generator(device="cuda").manual_seed(13)
+    T, H, E, k = 4000, 256, 32, 4
+    x = torch.randn(T, H, generator=g, device="cuda", dtype=torch.bfloat16)
+    idx, _ = moe_route_topk(torch.randn(T, E, generator=g, device="cuda"), k)
+    out = _outputs(T, H, E, k, 1, x.device)
+    _static_permute(x, idx, E, out=out)
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    _static_permute(x, idx, E, out=out)
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0
+    assert int(out["err"].item()) == 0
+
+
 def test_static_scratch_rejects_problems_beyond_the_array():
+    """ceil(T*k / 2048) * E > 65472 -> MOE_ERR_UNSUPPORTED.  Every pointer is a real
+    device buffer of the rejected problem's size, so that a refusal that regressed would
+    still launch on valid memory."""
     L = load_library()
-    nul = C.c_void_p(16)
-    # ceil(T*k / 2048) * E > 65472  ->  MOE_ERR_UNSUPPORTED before any launch
-    T, E, k = 600000, 1024, 1
-    st = L.moe_permute_static_scratch(nul, nul, T, 64, E, k, 1, nul, T * k, nul, nul, nul, nul, None,
-                                      C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    T, H, E, k = 130000, 8, 1024, 1          # 64 chunks x 1024 experts = 65536 counts
+    assert -(-T * k // 2048) * E > 65472
+    dev = torch.device("cuda")
+    x = torch.zeros(T, H, dtype=torch.bfloat16, device=dev)
+    idx = torch.zeros(T, k, dtype=torch.int32, device=dev)
+    out = _outputs(T, H, E, k, 1, dev)
+    st = L.moe_permute_static_scratch(
+        _p(x), _p(idx), T, H, E, k, 1, _p(out["x_perm"]), T * k, _p(out["dst_of_route"]), _p(out["src_of_row"]),
+        _p(out["group_sizes"]), _p(out["group_offsets"]), _p(out["err"]),
+        C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
     assert st == 2
+    assert int(out["err"].item()) == 0xFF     # nothing was launched or copied
