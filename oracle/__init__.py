@@ -86,6 +86,12 @@ def lib():
         L.oracle_unpermute_combine.argtypes = [_f32p, _i32p, _f32p, _i64, _int, _int, _int, _f64p]
         L.oracle_unpermute_combine_mxfp8.restype = None
         L.oracle_unpermute_combine_mxfp8.argtypes = [_f32p, _i32p, _f32p, _i64, _int, _int, _u8p, _u8p]
+        L.oracle_nvfp4_encode.restype = None
+        L.oracle_nvfp4_encode.argtypes = [_f32p, _i64, _u8p, _u8p]
+        L.oracle_nvfp4_value.restype = C.c_double
+        L.oracle_nvfp4_value.argtypes = [C.c_uint8, C.c_uint8]
+        L.oracle_unpermute_combine_nvfp4.restype = None
+        L.oracle_unpermute_combine_nvfp4.argtypes = [_f32p, _i32p, _f32p, _i64, _int, _int, _u8p, _u8p]
         L.oracle_round_bf16_array.restype = None
         L.oracle_round_bf16_array.argtypes = [_f64p, _i64, _f64p]
         L.oracle_num_threads.restype = _int
@@ -257,6 +263,45 @@ def unpermute_combine_mxfp8(y_perm: np.ndarray, dst_of_route: np.ndarray, topk_w
     codes = np.empty((T, H), np.uint8)
     scales = np.empty((T, H // 32), np.uint8)
     lib().oracle_unpermute_combine_mxfp8(_p(yb, _f32p), _p(dst, _i32p), _p(tw, _f32p), T, H, k,
+                                         _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def nvfp4_encode(v: np.ndarray):
+    """NVFP4 encoding of an fp32 array [..., K] (K % 16 == 0) along its last axis
+    (moe_oracle.c, oracle_nvfp4_encode): returns (codes uint8 [..., K/2], two E2M1
+    codes per byte with the even element in the low nibble; scales uint8 [..., K/16],
+    E4M3 bytes)."""
+    a = _c(v, np.float32)
+    K = a.shape[-1]
+    nb = a.size // 16
+    codes = np.empty(a.shape[:-1] + (K // 2,), np.uint8)
+    scales = np.empty(a.shape[:-1] + (K // 16,), np.uint8)
+    lib().oracle_nvfp4_encode(_p(a, _f32p), nb, _p(codes, _u8p), _p(scales, _u8p))
+    return codes, scales
+
+
+def nvfp4_decode(codes: np.ndarray, scales: np.ndarray) -> np.ndarray:
+    """Values of NVFP4 codes [..., K/2] with their block scales [..., K/16] (float64 [..., K])."""
+    c = np.asarray(codes, np.uint8)
+    nib = np.stack([c & 0xF, c >> 4], axis=-1).reshape(c.shape[:-1] + (c.shape[-1] * 2,))
+    sc = np.repeat(np.asarray(scales, np.uint8), 16, axis=-1)
+    f = lib().oracle_nvfp4_value
+    return np.vectorize(lambda q, s: f(int(q), int(s)))(nib, sc).astype(np.float64)
+
+
+def unpermute_combine_nvfp4(y_perm: np.ndarray, dst_of_route: np.ndarray, topk_w: np.ndarray):
+    """The combine with an NVFP4 output (moe_oracle.c, oracle_unpermute_combine_nvfp4):
+    fp32 slot-order sum, then the NVFP4 encoding along H.  Returns (codes uint8
+    [T, H/2], scales uint8 [T, H/16])."""
+    yb = _c(y_perm, np.float32)
+    H = yb.shape[1]
+    dst = _c(dst_of_route, np.int32)
+    tw = _c(topk_w, np.float32)
+    T, k = dst.shape
+    codes = np.empty((T, H // 2), np.uint8)
+    scales = np.empty((T, H // 16), np.uint8)
+    lib().oracle_unpermute_combine_nvfp4(_p(yb, _f32p), _p(dst, _i32p), _p(tw, _f32p), T, H, k,
                                          _p(codes, _u8p), _p(scales, _u8p))
     return codes, scales
 

@@ -445,6 +445,92 @@ void oracle_unpermute_combine_mxfp8(const float *y_perm, const int32_t *dst_of_r
     free(acc);
 }
 
+/* The combine with an NVFP4 output encoding ("Add MoE + expert-parallel Python API
+ * surface, PyTorch reference, and tests", Summary: nvfp4 public outputs as block-scaled
+ * tensors in their logical layout; BlockScaledTensor: data plus one scale per block,
+ * block_size 16 for nvfp4, and no tensor-level scale in the bundle).  The pages fix
+ * neither the element nor the scale format beyond that; the reading taken here:
+ *   elements: FP4 E2M1 (sign, 2 exponent bits, 1 mantissa bit), magnitudes
+ *             0, 0.5, 1, 1.5, 2, 3, 4, 6, in blocks of 16 consecutive elements along H;
+ *   scale:    one FP8 E4M3 value s per block, the smallest positive finite E4M3 value
+ *             with 6 s >= amax (so no element clips); 448 when amax > 6 * 448 (those
+ *             elements saturate at 6 s); byte 0x00 (s = 0, every code 0) when amax = 0;
+ *   codes:    the E2M1 magnitude nearest to |v| / s, a tie going to the magnitude whose
+ *             mantissa bit is 0; sign bit set when v < 0; two codes per byte, element
+ *             2i in the low nibble.
+ * Decoded value: (-1)^sign * magnitude * s.  The sum is the combine's own fp32
+ * slot-order sum (fmaf, from +0, dropped routes skipped), as for the MXFP8 output.
+ * codes [T, H/2], scales [T, H/16] (E4M3 bytes, row-major). */
+static const double E2M1_MAG[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+/* smallest E4M3 code in [1, 0x7E] whose value s has 6 s >= amax; 0 for amax = 0 */
+static uint8_t nvfp4_scale_code(double amax)
+{
+    if (amax == 0.0) return 0;
+    for (int c = 1; c <= 0x7E; ++c)
+        if (6.0 * oracle_e4m3_to_double((uint8_t)c) >= amax) return (uint8_t)c;
+    return 0x7E;
+}
+
+/* 4-bit code of v at block scale s > 0: nearest magnitude, ties to the even index */
+static uint8_t nvfp4_code(double v, double s)
+{
+    const double a = fabs(v);
+    int best = 0;
+    double bd = a;
+    for (int m = 1; m < 8; ++m) {
+        const double d = fabs(a - s * E2M1_MAG[m]);
+        if (d < bd || (d == bd && (m & 1) == 0)) { bd = d; best = m; }
+    }
+    return (uint8_t)((v < 0 ? 8 : 0) | best);
+}
+
+void oracle_nvfp4_encode(const float *v, int64_t n_blocks, uint8_t *codes, uint8_t *scales)
+{
+    for (int64_t b = 0; b < n_blocks; ++b) {
+        double amax = 0.0;
+        for (int i = 0; i < 16; ++i) {
+            double a = fabs((double)v[b * 16 + i]);
+            if (a > amax) amax = a;
+        }
+        const uint8_t sc = nvfp4_scale_code(amax);
+        scales[b] = sc;
+        const double s = oracle_e4m3_to_double(sc);
+        for (int i = 0; i < 8; ++i) {
+            uint8_t lo = 0, hi = 0;
+            if (sc) {
+                lo = nvfp4_code((double)v[b * 16 + 2 * i], s);
+                hi = nvfp4_code((double)v[b * 16 + 2 * i + 1], s);
+            }
+            codes[b * 8 + i] = (uint8_t)(lo | (hi << 4));
+        }
+    }
+}
+
+double oracle_nvfp4_value(uint8_t code, uint8_t scale)
+{
+    const double m = E2M1_MAG[code & 7] * oracle_e4m3_to_double(scale);
+    return (code & 8) ? -m : m;
+}
+
+void oracle_unpermute_combine_nvfp4(const float *y_perm, const int32_t *dst_of_route,
+                                    const float *topk_w, int64_t T, int H, int k,
+                                    uint8_t *codes, uint8_t *scales)
+{
+    float *acc = (float *)malloc(sizeof(float) * (size_t)H);
+    for (int64_t t = 0; t < T; ++t) {
+        for (int n = 0; n < H; ++n) acc[n] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            int32_t row = dst_of_route[t * k + j];
+            if (row < 0) continue;
+            const float w = topk_w[t * k + j];
+            for (int n = 0; n < H; ++n) acc[n] = fmaf(w, y_perm[(int64_t)row * H + n], acc[n]);
+        }
+        oracle_nvfp4_encode(acc, H / 16, codes + t * (H / 2), scales + t * (H / 16));
+    }
+    free(acc);
+}
+
 /* ------------------------------------------------------------------ */
 /* A3/A4: one route through one expert                                  */
 /* ------------------------------------------------------------------ */
