@@ -364,6 +364,26 @@ MOE_API moe_status_t moe_unpermute_combine_mxfp8(const moe_bf16_t *y_perm, const
                                                  const float *topk_w, int64_t T, int H, int k, uint8_t *out_q,
                                                  uint8_t *out_sf, moe_stream_t stream);
 
+/* The combine with the output encoded as NVFP4 along H ("Add MoE + expert-parallel
+ * Python API surface, PyTorch reference, and tests", Summary: nvfp4 public outputs as
+ * block-scaled tensors, logical unswizzled layout; BlockScaledTensor: data plus one
+ * scale per block, block_size 16 for nvfp4, no tensor-level scale).  The pages fix no
+ * more of the format; the reading taken: the fp32 slot-order sum of
+ * moe_unpermute_combine, then per 16 consecutive elements of a token row one FP8 E4M3
+ * scale s = the smallest positive finite E4M3 value with 6 s >= the block's max |v|
+ * (448 beyond 6 * 448, where elements saturate; byte 0 for an all-zero block) and
+ * FP4 E2M1 elements = the magnitude in {0, 0.5, 1, 1.5, 2, 3, 4, 6} nearest |v| / s,
+ * ties to the even code, sign bit (bit 3) set for v < 0.  Decoded value:
+ * +-magnitude * s.
+ *   out_q   device uint8 [T, H/2]: two codes per byte, element 2i in the low nibble
+ *   out_sf  device uint8 [T, H/16]: the E4M3 scale bytes, row-major
+ * topk_w may be NULL (plain sum).  Limits: H % 16 == 0, 1 <= k <= 32; y_perm 16-byte
+ * and out_q 4-byte aligned (else MOE_ERR_UNSUPPORTED).  Errors as
+ * moe_unpermute_combine. */
+MOE_API moe_status_t moe_unpermute_combine_nvfp4(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
+                                                 const float *topk_w, int64_t T, int H, int k, uint8_t *out_q,
+                                                 uint8_t *out_sf, moe_stream_t stream);
+
 /* ------------------------------------------------------------------ */
 /* A6 + A7  MXFP8 path                                                  */
 /* ------------------------------------------------------------------ */

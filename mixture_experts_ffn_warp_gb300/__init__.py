@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     PermutationMX, moe_grouped_fc1_swiglu_mxfp8, moe_grouped_fc2_mxfp8, moe_grouped_quantize_mxfp8,
     moe_permute_mxfp8, moe_quantize_weights_mxfp8, mx_tile_scale_bytes,
     moe_dequantize_rows_mxfp8, moe_dequantize_weights_mxfp8, moe_unpermute_combine_mxfp8,
+    moe_unpermute_combine_nvfp4,
 )
 from ._binding import (  # noqa: F401
     SCORE_SIGMOID, SCORE_SOFTMAX, moe_route_topk_bwd, moe_route_topk_sigmoid,

@@ -70,6 +70,7 @@ SIGNATURES = {
     "moe_grouped_fc1_swiglu_mxfp8_clamped": (_st, [_vp] * 7 + [_int, _int, _int, _i64] + [C.c_float] * 4
                                              + [_vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_unpermute_combine_mxfp8": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp, _vp]),
+    "moe_unpermute_combine_nvfp4": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp, _vp]),
     "moe_dequantize_weights_mxfp8": (_st, [_vp, _vp, _int, _int, _int, _vp, _vp]),
     "moe_grouped_fc2_mxfp8": (_st, [_vp] * 5 + [_int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
 }
@@ -605,5 +606,26 @@ def moe_unpermute_combine_mxfp8(y_perm: torch.Tensor, dst_of_route: torch.Tensor
     _need(out_q, "out_q", torch.uint8, (T, H))
     _need(out_sf, "out_sf", torch.uint8, (T, H // 32))
     _check("moe_unpermute_combine_mxfp8", load_library().moe_unpermute_combine_mxfp8(
+        _ptr(y_perm), _ptr(dst_of_route), _ptr(topk_w), T, H, k, _ptr(out_q), _ptr(out_sf), _stream(stream)))
+    return out_q, out_sf
+
+
+def moe_unpermute_combine_nvfp4(y_perm: torch.Tensor, dst_of_route: torch.Tensor, topk_w, out_q=None, out_sf=None,
+                                stream=None):
+    """The combine with an NVFP4 output (moe.h): (codes uint8 [T, H/2], two E2M1 codes per
+    byte; scales uint8 [T, H/16], E4M3)."""
+    _need(y_perm, "y_perm", torch.bfloat16)
+    _need(dst_of_route, "dst_of_route", torch.int32)
+    T, k = dst_of_route.shape
+    H = y_perm.shape[1]
+    if topk_w is not None:
+        _need(topk_w, "topk_w", torch.float32, (T, k))
+    if out_q is None:
+        out_q = torch.empty(T, H // 2, dtype=torch.uint8, device=y_perm.device)
+    if out_sf is None:
+        out_sf = torch.empty(T, H // 16, dtype=torch.uint8, device=y_perm.device)
+    _need(out_q, "out_q", torch.uint8, (T, H // 2))
+    _need(out_sf, "out_sf", torch.uint8, (T, H // 16))
+    _check("moe_unpermute_combine_nvfp4", load_library().moe_unpermute_combine_nvfp4(
         _ptr(y_perm), _ptr(dst_of_route), _ptr(topk_w), T, H, k, _ptr(out_q), _ptr(out_sf), _stream(stream)))
     return out_q, out_sf

@@ -14,6 +14,7 @@ from ._binding import (SCORE_SIGMOID, SCORE_SOFTMAX, Permutation, PermutationMX,
                        moe_grouped_dgrad_fc1, moe_route_topk_bwd, moe_route_topk_sigmoid,
                        moe_grouped_fc1_swiglu_mxfp8, moe_grouped_fc2_mxfp8, moe_permute_mxfp8,
                        moe_dequantize_rows_mxfp8, moe_dequantize_weights_mxfp8, moe_unpermute_combine_mxfp8,
+                       moe_unpermute_combine_nvfp4,
                        moe_quantize_weights_mxfp8, mx_tile_scale_bytes,
                        moe_grouped_dgrad_fc2_dswiglu, moe_grouped_fc1_swiglu, moe_grouped_fc2,
                        moe_grouped_wgrad, moe_permute, moe_route_topk, moe_unpermute_combine,
@@ -29,8 +30,9 @@ class MoeForward:
     weight_at: where the router weight is applied: "combine" (default), "fc1"
     (h scaled before its bf16 rounding) or "fc2" (y scaled); the early placements
     are forward only.
-    out_format: "bf16" (out [T, H]) or "mxfp8" (out_q E4M3 [T, H] + out_sf UE8M0
-    [T, H/32], the block-scaled output of the same fp32 combine sum).
+    out_format: "bf16" (out [T, H]), "mxfp8" (out_q E4M3 [T, H] + out_sf UE8M0
+    [T, H/32]) or "nvfp4" (out_q two E2M1 codes per byte [T, H/2] + out_sf E4M3
+    [T, H/16]): block-scaled encodings of the same fp32 combine sum.
     swiglu_clamp: None or (gate_lo, gate_hi, up_lo, up_hi): the SwiGLU inputs clamped to
     those inclusive bounds (the optional DeepSeek-style clamp; a MoeBackward of this layer
     uses the same bounds)."""
@@ -98,7 +100,7 @@ class MoeForward:
         _combine(self, self.topk_w if self.weight_at == "combine" else None, stream)
 
     def __call__(self, x, logits, W_gate, W_up, W_down, stream=None):
-        """Returns out (bf16) or, with out_format "mxfp8", (out_q, out_sf)."""
+        """Returns out (bf16) or, with a block-scaled out_format, (out_q, out_sf)."""
         self.route(logits, stream)
         self.permute(x, stream)
         self.ffn(W_gate, W_up, W_down, stream)
@@ -107,24 +109,31 @@ class MoeForward:
 
 
 def _output_buffers(m, out_format: str, T: int, H: int, dev):
-    if out_format not in ("bf16", "mxfp8"):
-        raise ValueError("out_format must be 'bf16' or 'mxfp8'")
+    if out_format not in ("bf16", "mxfp8", "nvfp4"):
+        raise ValueError("out_format must be 'bf16', 'mxfp8' or 'nvfp4'")
     m.out_format = out_format
     m.out = m.out_q = m.out_sf = None
     if out_format == "bf16":
         m.out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    else:
+    elif out_format == "mxfp8":
         if H % 32:
             raise ValueError("an MXFP8 output needs H % 32 == 0")
         m.out_q = torch.empty(T, H, dtype=torch.uint8, device=dev)
         m.out_sf = torch.empty(T, H // 32, dtype=torch.uint8, device=dev)
+    else:
+        if H % 16:
+            raise ValueError("an NVFP4 output needs H % 16 == 0")
+        m.out_q = torch.empty(T, H // 2, dtype=torch.uint8, device=dev)
+        m.out_sf = torch.empty(T, H // 16, dtype=torch.uint8, device=dev)
 
 
 def _combine(m, w, stream):
     if m.out_format == "bf16":
         moe_unpermute_combine(m.y_perm, m.perm.dst_of_route, w, out=m.out, stream=stream)
-    else:
+    elif m.out_format == "mxfp8":
         moe_unpermute_combine_mxfp8(m.y_perm, m.perm.dst_of_route, w, out_q=m.out_q, out_sf=m.out_sf, stream=stream)
+    else:
+        moe_unpermute_combine_nvfp4(m.y_perm, m.perm.dst_of_route, w, out_q=m.out_q, out_sf=m.out_sf, stream=stream)
 
 
 def moe_forward(x, logits, W_gate, W_up, W_down, k: int, align: int = 1, keep_fc1_c: bool = False):
@@ -277,7 +286,7 @@ class MoeForwardMX:
         _combine(self, self.topk_w, stream)
 
     def __call__(self, x, logits, w: MxWeights, stream=None):
-        """Returns out (bf16) or, with out_format "mxfp8", (out_q, out_sf)."""
+        """Returns out (bf16) or, with a block-scaled out_format, (out_q, out_sf)."""
         self.route(logits, stream)
         self.permute(x, stream)
         self.fc1(w, stream)

@@ -74,6 +74,31 @@ def assert_close_rms_mx(got, ref, scale_bytes, tol=TOL_MXFP8, what=""):
     return err / rms if rms > 0 else 0.0
 
 
+def e2m1_half_step(values, scale_bytes) -> np.ndarray:
+    """Half the spacing of the NVFP4 grid around each value [rows, K] given the blocks'
+    E4M3 scale bytes [rows, K/16]: the E2M1 magnitudes are 0.5 apart below 2, 1 apart
+    from 2 to 4 and 2 apart from 4 to 6 (times the block scale s)."""
+    s = np.repeat(np.vectorize(oracle.e4m3_to_double)(np.asarray(scale_bytes, np.uint8)), 16, axis=-1)
+    q = np.abs(np.asarray(values, np.float64)) / np.where(s > 0, s, 1.0)
+    return np.where(q < 2, 0.25, np.where(q < 4, 0.5, 1.0)) * s
+
+
+def assert_close_rms_nvfp4(got, ref, scale_bytes, tol, what=""):
+    """max |got - ref| <= tol * RMS(ref) for an NVFP4-encoded output compared with the
+    exact value, the bar applied to the error beyond the encoding's own rounding (half a
+    step of the E2M1 grid at the block's scale, taken at the larger of |got| and |ref|)."""
+    got = np.asarray(got, dtype=np.float64)
+    ref = np.asarray(ref, dtype=np.float64)
+    assert got.shape == ref.shape, (what, got.shape, ref.shape)
+    assert np.isfinite(got).all(), f"{what}: non-finite values"
+    rms = float(np.sqrt(np.mean(ref ** 2)))
+    hs = np.maximum(e2m1_half_step(got, scale_bytes), e2m1_half_step(ref, scale_bytes))
+    dev = np.maximum(np.abs(got - ref) - hs, 0.0)
+    err = float(dev.max()) if got.size else 0.0
+    assert err <= tol * rms, f"{what}: max|err| beyond the encoding {err:.3e} > {tol} * RMS {rms:.3e}"
+    return err / rms if rms > 0 else 0.0
+
+
 def assert_close_ulp(got, ref, what="", slack=2e-3):
     """Element-wise check of a stored bf16 intermediate against the oracle that
     rounds at the same point: the two may round a value on either side of a
