@@ -91,6 +91,19 @@ MOE_API size_t moe_workspace_bytes(int64_t T, int E, int k);
 /* Zero the error word (and any state) of a workspace, on `stream`. */
 MOE_API moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* Limit, in ns, of the device spin waits of the grouped GEMMs that use this
+ * workspace (every pipeline mbarrier wait of moe_grouped_* and the calls built on
+ * them), written into the workspace header on `stream`; 0 restores the default of
+ * 2 s (as does moe_workspace_init).  A wait that runs past the limit sets
+ * MOE_DEVERR_TIMEOUT in the error word; the kernel then lets the copies and MMAs
+ * it has issued finish, frees its tensor memory and exits, leaving the call's
+ * outputs invalid and the context usable.  Failure detection ("[JAX] Expert
+ * Parallelism: JAX primitives + VJPs", commit log: kernel contracts are trusted and
+ * errors surface instead of being sanitised) and a short limit to exercise that
+ * path.  Errors: MOE_ERR_WORKSPACE (null or too small), MOE_ERR_CUDA. */
+MOE_API moe_status_t moe_workspace_set_wait_limit(void *ws, size_t ws_bytes, uint32_t limit_ns,
+                                                  moe_stream_t stream);
+
 /* Copy the device error word to *out (synchronises `stream`).  Returns
  * MOE_OK if the word is 0, MOE_ERR_DEVICE_DATA if any bit is set,
  * MOE_ERR_CUDA if the copy failed. */

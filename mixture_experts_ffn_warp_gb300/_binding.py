@@ -35,6 +35,7 @@ SIGNATURES = {
     "moe_abi_version": (_int, []),
     "moe_workspace_bytes": (_sz, [_i64, _int, _int]),
     "moe_workspace_init": (_st, [_vp, _sz, _vp]),
+    "moe_workspace_set_wait_limit": (_st, [_vp, _sz, C.c_uint32, _vp]),
     "moe_read_device_error": (_st, [_vp, _vp, C.POINTER(C.c_uint32)]),
     "moe_route_topk": (_st, [_vp, _i64, _int, _int, _vp, _vp, _vp]),
     "moe_route_topk_sigmoid": (_st, [_vp, _vp, _i64, _int, _int, _int, _vp, _vp, _vp]),
@@ -147,6 +148,11 @@ class Workspace:
 
     def reset(self, stream=None):
         _check("moe_workspace_init", load_library().moe_workspace_init(_ptr(self.buf), self.nbytes, _stream(stream)))
+
+    def set_wait_limit(self, limit_ns: int, stream=None):
+        """Limit of the GEMMs' device spin waits in ns (0: the default 2 s)."""
+        _check("moe_workspace_set_wait_limit", load_library().moe_workspace_set_wait_limit(
+            _ptr(self.buf), self.nbytes, int(limit_ns), _stream(stream)))
 
     def read_error(self, stream=None) -> int:
         """Device error word (synchronises the stream)."""

@@ -10,6 +10,12 @@ int device_sm_count() {
     return n > 0 ? n : 1;
 }
 
+// One word of a workspace header written in stream order (capturable, no host copy).
+__global__ void set_word_kernel(uint32_t *word, uint32_t value) {
+    pdl_wait();
+    *word = value;
+}
+
 }  // namespace moe
 
 extern "C" {
@@ -42,6 +48,12 @@ size_t moe_mx_tile_scale_bytes(int64_t rows_cap, int E, int K) {
 moe_status_t moe_workspace_init(void *ws, size_t ws_bytes, moe_stream_t stream) {
     if (!ws || ws_bytes < moe::kWsHeaderBytes) return MOE_ERR_WORKSPACE;
     return moe::cuda_status(cudaMemsetAsync(ws, 0, moe::kWsHeaderBytes, (cudaStream_t)stream));
+}
+
+moe_status_t moe_workspace_set_wait_limit(void *ws, size_t ws_bytes, uint32_t limit_ns, moe_stream_t stream) {
+    if (!ws || ws_bytes < moe::kWsHeaderBytes) return MOE_ERR_WORKSPACE;
+    moe::launch_k(moe::set_word_kernel, dim3(1), dim3(1), 0, (cudaStream_t)stream, moe::ws_wait_limit(ws), limit_ns);
+    return moe::launch_status();
 }
 
 moe_status_t moe_read_device_error(const void *ws, moe_stream_t stream, uint32_t *out) {

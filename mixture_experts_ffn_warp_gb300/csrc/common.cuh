@@ -42,6 +42,18 @@ inline size_t ws_mtile_bytes(int E) { return ((size_t)(E + 1) * sizeof(int32_t) 
 __global__ void mtile_prefix_kernel(const int32_t *__restrict__ group_offsets, int G, int32_t *__restrict__ mtile_start);
 
 inline uint32_t *ws_error_word(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
+
+// Limit of the GEMM pipelines' device spin waits (their mbarrier waits), in ns: the
+// workspace header's uint32 at offset 8 (0 = the default, 2 s), set with
+// moe_workspace_set_wait_limit.  A wait past it sets MOE_DEVERR_TIMEOUT and the kernel
+// winds down (it lets its issued copies and MMAs finish, frees TMEM and exits).
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;
+inline uint32_t *ws_wait_limit(void *ws) { return reinterpret_cast<uint32_t *>(ws) + 2; }
+// Read by the kernels after their programmatic-launch wait (the error word is header word 0).
+__device__ __forceinline__ uint64_t device_wait_limit(const uint32_t *err) {
+    const uint32_t v = err ? __ldcg(err + 2) : 0u;
+    return v ? (uint64_t)v : kDefaultWaitNs;
+}
 // Blocks of the permutation's counting pass that have finished (header offset 4); the last
 // one to finish runs the scan and sets it back to zero.
 inline uint32_t *ws_done_counter(void *ws) { return reinterpret_cast<uint32_t *>(ws) + 1; }

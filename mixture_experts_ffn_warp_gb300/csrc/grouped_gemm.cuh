@@ -42,7 +42,6 @@ constexpr int BM = 128;
 constexpr int UMMA_K = 16;
 constexpr int kThreads = 192;
 constexpr int kMaxE = 1024;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 template <Op OP>
 struct Traits {
@@ -259,6 +258,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // everything above is on-chip set-up; from here on the kernel reads what earlier
     // kernels on the stream wrote
     pdl_wait();
+    const uint64_t wait_ns = device_wait_limit(args.err);   // pipeline waits' limit
     const int E = args.E;
     for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = args.group_offsets[i];
     __syncthreads();
@@ -310,7 +310,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
                 const Tile tl = decode_tile<OP, BN>(t, args, s_off, s_start);
                 for (int kb = 0; kb < tl.kb; ++kb) {
-                    if (!sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, kWaitLimitNs)) {
+                    if (!sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -398,12 +398,12 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         for (int t = blockIdx.x; t < total_tiles && ok; t += gridDim.x) {
             const Tile tl = decode_tile<OP, BN>(t, args, s_off, s_start);
             if (tl.kb == 0) continue;   // empty K range: the epilogue writes zeros
-            const bool got_acc = sm100::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, kWaitLimitNs);
+            const bool got_acc = sm100::mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, wait_ns);
             if (__any_sync(0xFFFFFFFFu, !got_acc)) { ok = false; break; }
             sm100::tc_fence_after();
             const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
             for (int kb = 0; kb < tl.kb; ++kb) {
-                const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, kWaitLimitNs);
+                const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, wait_ns);
                 if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
                 const uint32_t sa = smem_base + stage * C::STAGE_BYTES;
                 const uint32_t sb = sa + C::A_BYTES;
@@ -554,7 +554,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     continue;
                 }
             }
-            const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, kWaitLimitNs);
+            const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, wait_ns);
             if (__any_sync(0xFFFFFFFFu, !got)) break;
             sm100::tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN);

@@ -68,7 +68,6 @@ constexpr int B_BYTES = 128 * 128;       // 128 token rows x 64 K
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int STAGES = 6;
 constexpr int TMEM_COLS = 512;           // two accumulators of BT fp32 columns
-constexpr uint64_t kWaitLimitNs = 2000000000ull;   // 2 s
 
 // Epilogue shared memory: FC1 exchange buffers (2 warp pairs x 2 chunk parities x 2
 // directions x 16 tokens x 32 features fp32 = 16 KB) and output staging, two slots per
@@ -251,6 +250,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
 
     // from here on the kernel reads what earlier kernels on the stream wrote
     pdl_wait();
+    const uint64_t wait_ns = device_wait_limit(args.err);   // pipeline waits' limit
     const int E = args.E;
     for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = args.group_offsets[i];
     __syncthreads();
@@ -330,7 +330,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
             }
             for (int kb = 0; kb < tl.kblocks; ++kb) {
                 bool got = true;
-                if (lane == 0) got = sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, kWaitLimitNs);
+                if (lane == 0) got = sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, wait_ns);
                 if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) { ok = false; break; }
                 if (lane == 0) {
                     const uint32_t sa = smem_base + stage * STAGE_BYTES, sb = sa + A_BYTES;
@@ -350,7 +350,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                 // the previous tail has been multiplied; then the layout the TMA loads give
                 // (128-byte swizzle), with the MN chunks 16 K rows apart
                 bool got = true;
-                if (lane == 0) got = sm100::mbar_wait(&tail_empty, tphase ^ 1u, abort, args.err, kWaitLimitNs);
+                if (lane == 0) got = sm100::mbar_wait(&tail_empty, tphase ^ 1u, abort, args.err, wait_ns);
                 if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) { ok = false; break; }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
@@ -386,7 +386,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                 const PTile tl = decode(p, args, s_off, s_start);
                 const int trow = tl.t0 + (int)rank * (tl.n >> 1);   // this CTA's half of the tokens
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    if (!sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, kWaitLimitNs)) {
+                    if (!sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, wait_ns)) {
                         ok = false;
                         break;
                     }
@@ -463,12 +463,12 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                     const int ntail = tl.rows - tl.full16;
                     if (tl.rows == 0) continue;   // the epilogue writes this tile's zeros alone
                     const bool got_acc =
-                        sm100::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, kWaitLimitNs);
+                        sm100::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, wait_ns);
                     if (__any_sync(0xFFFFFFFFu, !got_acc)) { ok = false; break; }
                     sm100::tc_fence_after();
                     const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BT);
                     for (int kb = 0; kb < tl.kblocks; ++kb) {
-                        const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, kWaitLimitNs);
+                        const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, wait_ns);
                         if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
                         sm100::tc_fence_after();
                         const uint64_t ad = wa0 + (uint64_t)stage * STAGE_STEP;
@@ -488,7 +488,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                     if (!ok) break;
                     if (ntail > 0) {   // the zero-padded tail written by both producers
                         const bool got =
-                            sm100::mbar_wait_cluster(&tail_full, tphase, abort, args.err, kWaitLimitNs);
+                            sm100::mbar_wait_cluster(&tail_full, tphase, abort, args.err, wait_ns);
                         if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
                         tphase ^= 1u;
                         sm100::tc_fence_after();
@@ -510,12 +510,12 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                 const PTile tl = decode(p, args, s_off, s_start);
                 const uint32_t idesc = sm100::idesc_bf16(256, tl.n, !a_kmajor<OP>(), false);
                 const bool got_acc =
-                    sm100::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, kWaitLimitNs);
+                    sm100::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, wait_ns);
                 if (__any_sync(0xFFFFFFFFu, !got_acc)) { ok = false; break; }
                 sm100::tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BT);
                 for (int kb = 0; kb < kblocks; ++kb) {
-                    const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, kWaitLimitNs);
+                    const bool got = sm100::mbar_wait(&full_bar[stage], phase, abort, args.err, wait_ns);
                     if (__any_sync(0xFFFFFFFFu, !got)) { ok = false; break; }
                     sm100::tc_fence_after();
                     const uint64_t ad = a_desc0 + (uint64_t)stage * STAGE_STEP;
@@ -614,7 +614,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                 const WTile tl = decode_w(p, args, s_off);
                 const bool mma = tl.rows > 0;   // else an expert without rows: exact zeros
                 if (mma) {
-                    const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, kWaitLimitNs);
+                    const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, wait_ns);
                     if (__any_sync(0xFFFFFFFFu, !got)) break;
                     sm100::tc_fence_after();
                 }
@@ -660,7 +660,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
             const int p = round_tile(r, cid, G, total);
             if (p < 0) continue;
             const PTile tl = decode(p, args, s_off, s_start);
-            const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, kWaitLimitNs);
+            const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, wait_ns);
             if (__any_sync(0xFFFFFFFFu, !got)) break;
             sm100::tc_fence_after();
             const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
@@ -706,7 +706,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                     }
                     uint64_t *xbr = &xbar[pr][chunk_parity];
                     sm100::mbar_arrive(xbr);
-                    const bool xok = sm100::mbar_wait(xbr, (xphase >> chunk_parity) & 1u, abort, args.err, kWaitLimitNs);
+                    const bool xok = sm100::mbar_wait(xbr, (xphase >> chunk_parity) & 1u, abort, args.err, wait_ns);
                     xphase ^= 1u << chunk_parity;
                     if (__any_sync(0xFFFFFFFFu, !xok)) { alive = false; break; }
                     float hv[16];

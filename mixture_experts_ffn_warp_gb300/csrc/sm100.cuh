@@ -52,14 +52,33 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the same phase condition.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Limits below this are polled with the non-blocking test_wait: try_wait may suspend the
+// thread for a hardware-chosen time and succeed within it, so a short limit would
+// otherwise go unobserved.
+constexpr uint64_t kPollBelowNs = 1000000ull;
+
 // Bounded wait: gives up after `limit_ns` (setting *abort and the timeout
 // bit of the error word) or as soon as another role has set *abort.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
                                           uint32_t *err, uint64_t limit_ns) {
-    if (mbar_try_wait(bar, parity)) return true;
+    const bool poll = limit_ns < kPollBelowNs;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
@@ -279,13 +298,26 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t pa
     return ok != 0;
 }
 
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Bounded wait as mbar_wait, with cluster-scope acquire.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity, volatile int *abort,
                                                   uint32_t *err, uint64_t limit_ns) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const bool poll = limit_ns < kPollBelowNs;
+    if (poll ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if (poll ? mbar_test_wait_cluster(bar, parity) : mbar_try_wait_cluster(bar, parity)) return true;
         if (*abort) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *abort = 1;
