@@ -40,6 +40,10 @@ METRIC = "MoE layer tokens/s & grouped-GEMM TFLOP/s (% of GB300 peak); permute/c
 UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
+# Dense MXFP8 (E4M3, UE8M0 per 32 along K) rate of the library block-scaled GEMM on this
+# pool's GB300, measured by `python bench.py --measure-peaks` (torch._scaled_mm, 8192^3,
+# best of 10 launches), or None while unmeasured (then the bf16 peak x FP8_OVER_BF16).
+MEASURED_MXFP8_TFLOPS = None
 
 # DRAM traffic (read + write bytes per launch) of a workload's dominant kernel from one
 # ncu capture (profiles/), with a hash of the kernel sources it was taken on.  Reported as
@@ -63,6 +67,55 @@ def profiled_traffic(workload: str, kernel: str):
     if t is None or t[1] != kernel_source_hash():
         return None
     return t[0]
+
+
+def measure_library_peaks(dev) -> dict:
+    """Dense rates of the library GEMMs on this GPU, as timing comparators for the
+    roofline's denominators: torch.matmul bf16 and torch._scaled_mm MXFP8 (E4M3 operands,
+    UE8M0 scales per 32 elements along K), both 8192^3.  Burst = best of 10 single
+    launches; sustained = back to back for about 3 s.  Only the timings are used."""
+    import torch
+    n = 8192
+    flop = 2.0 * n ** 3
+
+    def rate(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(10):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            torch.cuda.synchronize(dev)
+            best = min(best, a.elapsed_time(b))
+        reps = max(1, int(3000.0 / best))
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            fn()
+        b.record()
+        torch.cuda.synchronize(dev)
+        return flop / (best * 1e-3) / 1e12, flop * reps / (a.elapsed_time(b) * 1e-3) / 1e12
+
+    out = {"how": "8192^3; burst: best of 10 launches; sustained: back to back for ~3 s; CUDA events"}
+    x = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    y = torch.randn(n, n, device=dev, dtype=torch.bfloat16)
+    out["bf16_tflops"], out["bf16_tflops_sustained"] = rate(lambda: torch.matmul(x, y))
+    try:
+        a8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b8 = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()     # column-major [K, N]
+        rows = (n + 127) // 128 * 128
+        cols = ((n // 32) + 3) // 4 * 4
+        sa = torch.ones(rows, cols, device=dev).to(torch.float8_e8m0fnu)
+        sb = torch.ones(rows, cols, device=dev).to(torch.float8_e8m0fnu)
+        fn = lambda: torch._scaled_mm(a8, b8, sa, sb, out_dtype=torch.bfloat16)  # noqa: E731
+        out["mxfp8_tflops"], out["mxfp8_tflops_sustained"] = rate(fn)
+        out["mxfp8_call"] = "torch._scaled_mm(E4M3 [M,K], E4M3 [K,N] column-major, UE8M0 scales, bf16 out)"
+    except Exception as e:   # the library block-scaled GEMM is not available here
+        out["mxfp8_unavailable"] = f"{type(e).__name__}: {e}"[:300]
+    return out
 
 
 def peaks():
@@ -552,7 +605,9 @@ def run_gpu(args):
     ms_e2e = max_over_ranks(t0.elapsed_time(t1) / args.steps, dev)
 
     def peak_flops(g):
-        return pk["bf16_tflops"] * (FP8_OVER_BF16 if g.fp8 else 1.0)
+        if g.fp8:
+            return MEASURED_MXFP8_TFLOPS if MEASURED_MXFP8_TFLOPS else pk["bf16_tflops"] * FP8_OVER_BF16
+        return pk["bf16_tflops"]
 
     rates = {}
     for g in groups:
@@ -569,7 +624,9 @@ def run_gpu(args):
     tensor_bound = dom.flop > 0 and dom.flop / dom.nbytes >= ridge
     if tensor_bound:
         roof = {"bound": "tensor", "achieved": dom.flop / t_dom / 1e12, "peak": peak_flops(dom), "unit": "TFLOP/s",
-                "peak_source": f"{pk['source']} bf16 dense burst" + (" x 2 (nominal fp8/bf16)" if dom.fp8 else "")}
+                "peak_source": (("measured MXFP8 library GEMM burst (bench.py --measure-peaks)"
+                                 if MEASURED_MXFP8_TFLOPS else f"{pk['source']} bf16 dense burst x 2 (nominal fp8/bf16)")
+                                if dom.fp8 else f"{pk['source']} bf16 dense burst")}
     else:
         roof = {"bound": "hbm", "achieved": dom.nbytes / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "peak_source": f"{pk['source']} HBM copy"}
@@ -591,7 +648,7 @@ def run_gpu(args):
                         "(events between groups stop a launch from overlapping the previous group's tail, so "
                         "the groups sum to a little more than ms_per_step)",
         "ffn_tflops": ffn_flop / (ffn_ms / 1e3) / 1e12,
-        "ffn_frac_of_peak": ffn_flop / (ffn_ms / 1e3) / 1e12 / (pk["bf16_tflops"] * (FP8_OVER_BF16 if shape.mxfp8 else 1)),
+        "ffn_frac_of_peak": ffn_flop / (ffn_ms / 1e3) / 1e12 / peak_flops(ffn[0]),
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": args.steps * sum(g.launches for g in groups),
@@ -631,7 +688,13 @@ def main(argv=None):
     ap.add_argument("--ref-tokens", type=int, default=0)
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--measure-peaks", action="store_true",
+                    help="print the library GEMMs' dense bf16 and MXFP8 rates on this GPU and exit")
     args = ap.parse_args(argv)
+    if args.measure_peaks:
+        import torch
+        print(json.dumps(measure_library_peaks(torch.device("cuda", 0))), flush=True)
+        return 0
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":

@@ -475,10 +475,20 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                         const uint64_t bd = wb0 + (uint64_t)stage * STAGE_STEP;
                         const int left = (tl.full16 - kb * 64) >> 4;   // 16-row slices left
                         const int kk_end = left < 4 ? left : 4;
+                        // a whole stage as four straight-line MMAs (a runtime-bounded loop in
+                        // the elected lane measured ~195 cycles per MMA against 128)
+                        const uint32_t acc0 = kb != 0 ? 1u : 0u;
                         if (sm100::elect_one()) {
-                            for (int kk = 0; kk < kk_end; ++kk)
-                                sm100::mma_bf16_pair(d_tmem, ad + kk * KSTEP, bd + kk * KSTEP, idesc,
-                                                     (kb | kk) != 0 ? 1u : 0u);
+                            if (kk_end == 4) {
+                                sm100::mma_bf16_pair(d_tmem, ad, bd, idesc, acc0);
+                                sm100::mma_bf16_pair(d_tmem, ad + KSTEP, bd + KSTEP, idesc, 1u);
+                                sm100::mma_bf16_pair(d_tmem, ad + 2 * KSTEP, bd + 2 * KSTEP, idesc, 1u);
+                                sm100::mma_bf16_pair(d_tmem, ad + 3 * KSTEP, bd + 3 * KSTEP, idesc, 1u);
+                            } else {
+                                for (int kk = 0; kk < kk_end; ++kk)
+                                    sm100::mma_bf16_pair(d_tmem, ad + kk * KSTEP, bd + kk * KSTEP, idesc,
+                                                         (kb | kk) != 0 ? 1u : 0u);
+                            }
                             sm100::mma_commit_pair(&empty_bar[stage], 0x3);
                         }
                         __syncwarp();
