@@ -41,9 +41,10 @@ UNIT = "tokens/s"
 L2_FLUSH_BYTES = 256 << 20
 FP8_OVER_BF16 = 2.0   # nominal dense fp8 / bf16 tensor rate (4.5 / 2.25 PFLOP/s)
 # Dense MXFP8 (E4M3, UE8M0 per 32 along K) rate of the library block-scaled GEMM on this
-# pool's GB300, measured by `python bench.py --measure-peaks` (torch._scaled_mm, 8192^3,
-# best of 10 launches), or None while unmeasured (then the bf16 peak x FP8_OVER_BF16).
-MEASURED_MXFP8_TFLOPS = None
+# pool's GB300, measured by `python bench.py --measure-peaks` (torch._scaled_mm, 8192^3):
+# 2847 TFLOP/s best single launch, 3254 TFLOP/s back to back for ~3 s (bf16 torch.matmul
+# in the same run: 1913 / 1686).  The larger of the two is the denominator.
+MEASURED_MXFP8_TFLOPS = 3254.0
 
 # DRAM traffic (read + write bytes per launch) of a workload's dominant kernel from one
 # ncu capture (profiles/), with a hash of the kernel sources it was taken on.  Reported as
@@ -624,7 +625,7 @@ def run_gpu(args):
     tensor_bound = dom.flop > 0 and dom.flop / dom.nbytes >= ridge
     if tensor_bound:
         roof = {"bound": "tensor", "achieved": dom.flop / t_dom / 1e12, "peak": peak_flops(dom), "unit": "TFLOP/s",
-                "peak_source": (("measured MXFP8 library GEMM burst (bench.py --measure-peaks)"
+                "peak_source": (("measured MXFP8 library GEMM rate (bench.py --measure-peaks)"
                                  if MEASURED_MXFP8_TFLOPS else f"{pk['source']} bf16 dense burst x 2 (nominal fp8/bf16)")
                                 if dom.fp8 else f"{pk['source']} bf16 dense burst")}
     else:

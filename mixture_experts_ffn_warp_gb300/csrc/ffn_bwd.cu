@@ -283,7 +283,8 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
             const moe_bf16_t *A = down ? h : x_perm, *B = down ? dy_perm : dgu;
             const int M = down ? F : H, N = down ? H : 2 * F;
             CUtensorMap tA, tB, tC0, tC1;
-            if (!tmap_bf16_2d(&tA, A, M, rows, M, 64, 64) || !tmap_bf16_2d(&tB, B, N, rows, N, 64, 64))
+            // each operand's 128 columns of a 64-row K step in one load (two 64-column chunks)
+            if (!tmap_bf16_col_chunks(&tA, A, M, rows, M, 64) || !tmap_bf16_col_chunks(&tB, B, N, rows, N, 64))
                 return MOE_ERR_UNSUPPORTED;
             if (down ? !tmap_store_2d(&tC0, dW_down, 4, H, (uint64_t)E * F, H)
                      : (!tmap_store_2d(&tC0, dW_gate, 4, F, (uint64_t)E * H, F) ||

@@ -296,7 +296,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
         // ============================================================ producer, WGRAD (both CTAs)
         // Lane 0 issues the TMA loads of the whole 16-row slices: this CTA's 128 gradient rows
         // (two 64-wide MN chunks of the A rows) and 128 gradient columns (of the B rows), 64
-        // K rows (tokens) per stage.  An expert's last (rows mod 16) rows go into the tail
+        // K rows (tokens) per stage, one 3-D box per operand.  An expert's last (rows mod 16) rows go into the tail
         // buffer, written by the whole warp: rows zero-padded to a 16-row slice in the MMA's
         // swizzled layout, so the pair MMAs never multiply a row of the next expert.  The tail
         // buffer sits outside the ring, so it takes no stage from the loads' lead over the MMAs.
@@ -336,11 +336,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                     const uint32_t sa = smem_base + stage * STAGE_BYTES, sb = sa + A_BYTES;
                     const uint32_t fb_c = full0 + (uint32_t)(stage * sizeof(uint64_t));
                     if (rank == 0) sm100::mbar_arrive_expect_tx(&full_bar[stage], 2 * STAGE_BYTES);
+                    // one 3-D box per operand: its two 64-column chunks of 64 K rows (measured
+                    // on mixtral: 677 cycles per K step against 782 with four 2-D boxes)
                     const int krow = tl.row0 + kb * 64;
-                    sm100::tma_load_2d_pair(sa, &tmW0, fb_c, m0, krow);
-                    sm100::tma_load_2d_pair(sa + 8192, &tmW0, fb_c, m0 + 64, krow);
-                    sm100::tma_load_2d_pair(sb, &tmX, fb_c, n0, krow);
-                    sm100::tma_load_2d_pair(sb + 8192, &tmX, fb_c, n0 + 64, krow);
+                    sm100::tma_load_3d_pair(sa, &tmW0, fb_c, 0, krow, m0 / 64);
+                    sm100::tma_load_3d_pair(sb, &tmX, fb_c, 0, krow, n0 / 64);
                 }
                 ++issued;
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -475,8 +475,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                         const uint64_t bd = wb0 + (uint64_t)stage * STAGE_STEP;
                         const int left = (tl.full16 - kb * 64) >> 4;   // 16-row slices left
                         const int kk_end = left < 4 ? left : 4;
-                        // a whole stage as four straight-line MMAs (a runtime-bounded loop in
-                        // the elected lane measured ~195 cycles per MMA against 128)
+                        // a whole stage as four straight-line MMAs, as the other ops issue them
                         const uint32_t acc0 = kb != 0 ? 1u : 0u;
                         if (sm100::elect_one()) {
                             if (kk_end == 4) {

@@ -63,6 +63,19 @@ inline bool tmap_bf16_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t
     return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
 }
 
+// A row-major bf16 matrix [rows, cols] (row pitch ld elements, cols % 64 == 0) seen as the
+// 3-D tensor [cols / 64][rows][64] -- dimension 2 steps 64 columns (128 bytes) --, with
+// boxes {64, box_rows, 2}: one load brings two adjacent 64-column chunks of box_rows rows,
+// chunk after chunk, each a 128-byte-swizzled block (the MN-major operand layout with
+// chunks box_rows * 128 bytes apart).
+inline bool tmap_bf16_col_chunks(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows, uint64_t ld,
+                                 uint32_t box_rows) {
+    const uint64_t dims[3] = {64, rows, cols / 64};
+    const uint64_t strides[2] = {ld * 2, 128};
+    const uint32_t box[3] = {64, box_rows, 2};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box);
+}
+
 // Store map of the GEMM epilogue: 2-D row-major [outer, inner] of `elem_bytes`-byte
 // elements (bf16, fp32 or bytes), row pitch `ld` elements; boxes of 64 bytes x 32 rows
 // in the 64-byte swizzle (the epilogue's staging slots).
