@@ -3,6 +3,7 @@
 //   B1 combine_bwd      dy_perm[row(t,j)] = bf16(w[t,j] * dY[t]); d_topk_w[t,j] = <dY[t], y(t,j)>
 //   B2+B3 dgrad FC2     dh = dy_perm W_down^T (fp32 in TMEM), then dSwiGLU from the fc1_c
 //                       stash in the epilogue: dg = dh*u*s*(1+g*(1-s)), du = dh*g*s -> bf16
+//                       (CTA pairs with tokens on M when F % 256 == 0)
 //   B4 dgrad FC1        dx_perm = [dg|du] [W_gate; W_up]^T (K = 2F), fp32
 //   B5 wgrad            dW_down[e] = h_e^T dy_e;  dW_gate|dW_up[e] = x_e^T [dg|du]_e  (fp32;
 //                       K = the rows of group e, read on the device; 0-token experts -> 0)
@@ -157,7 +158,34 @@ moe_status_t dgrad_fc2_impl(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down,
     moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!dy_perm || !W_down || !fc1_c || !group_offsets || !dgu) return MOE_ERR_INVALID_ARG;
-    const int bn = (F % 256 == 0) ? 256 : 128;
+    if (F % 256 == 0) {
+        // CTA pairs: 256 token rows (M, 128 per CTA) x 256 features (N) per pair tile, both
+        // operands K-major (dy_perm rows, W_down rows); the epilogue reads the stash rows
+        CUtensorMap tW, tX, tOut;
+        if (!tmap_bf16_3d(&tW, W_down, H, F, E, 64, 128) || !tmap_bf16_2d(&tX, dy_perm, H, rows_cap, H, 64, 128) ||
+            !tmap_store_2d(&tOut, dgu, 2, 2 * (uint64_t)F, rows_cap, 2 * (uint64_t)F))
+            return MOE_ERR_UNSUPPORTED;
+        gp::Args a{};
+        a.group_offsets = group_offsets;
+        a.E = E;
+        a.K = H;
+        a.N_out = F;
+        a.n_fb = F / 256;
+        a.rows_cap = rows_cap;
+        a.y16 = reinterpret_cast<__nv_bfloat16 *>(dgu);
+        a.aux = reinterpret_cast<const __nv_bfloat16 *>(fc1_c);
+        if (clamp) {
+            a.clamp = 1;
+            a.gate_lo = clamp[0];
+            a.gate_hi = clamp[1];
+            a.up_lo = clamp[2];
+            a.up_hi = clamp[3];
+        }
+        a.err = ws_error_word(ws);
+        return gp::launch<gp::Op::DSWIGLU>(tW, tW, tX, tOut, tOut, a, token_block_bound(rows_cap, E) * a.n_fb,
+                                           (cudaStream_t)stream);
+    }
+    const int bn = 128;
     // A = dy_perm [rows, H] (K-major), B = W_down[e] as [F rows][H] (K-major)
     CUtensorMap tA, tB, tC;
     if (!tmap_bf16_2d(&tA, dy_perm, H, rows_cap, H, 64, 128) || !tmap_bf16_3d(&tB, W_down, H, F, E, 64, bn) ||
@@ -183,7 +211,6 @@ moe_status_t dgrad_fc2_impl(const moe_bf16_t *dy_perm, const moe_bf16_t *W_down,
     }
     a.err = ws_error_word(ws);
     const int64_t bound = mblock_bound(rows_cap, E) * a.n_tiles;
-    if (bn == 256) return gg::launch<Op::DGRAD_DSWIGLU, 256>(tA, tB, tB, tC, tC, a, bound, (cudaStream_t)stream);
     return gg::launch<Op::DGRAD_DSWIGLU, 128>(tA, tB, tB, tC, tC, a, bound, (cudaStream_t)stream);
 }
 

@@ -43,14 +43,20 @@
 namespace moe {
 namespace gp {
 
-enum class Op : int { FC1, FC2, DGRAD_FC1, WGRAD };
+enum class Op : int { FC1, FC2, DGRAD_FC1, WGRAD, DSWIGLU };
 
 // DGRAD_FC1 (the backward's dx_perm = [dg|du] [W_gate; W_up]^T, M = H, K = 2F, fp32 out)
-// reads the weights K-major: their rows are the MMA's M rows.  (The dSwiGLU dgrad stays on
-// the one-CTA kernel: with tokens on N its epilogue must transpose the token-major stash
-// and outputs through shared memory, and measured slower.)
+// reads the weights K-major: their rows are the MMA's M rows.
+//
+// DSWIGLU (the backward's dh = dy_perm W_down^T followed by the dSwiGLU, M = tokens, N = F,
+// K = H) puts the routed tokens on M instead: a pair tile is 256 token rows of one expert
+// (128 per CTA, both operands K-major: dy_perm rows and W_down rows) x 256 features, so each
+// CTA's TMEM lanes are its 128 token rows and the epilogue reads the token-major fc1_c stash
+// and writes the token-major [dg | du] rows directly.  The rows of an expert's last token
+// block past its end are multiplied and never stored.  (With tokens on N the epilogue had to
+// transpose the stash and the outputs through shared memory and measured slower.)
 template <Op OP>
-constexpr bool a_kmajor() { return OP == Op::DGRAD_FC1; }
+constexpr bool a_kmajor() { return OP == Op::DGRAD_FC1 || OP == Op::DSWIGLU; }
 
 // WGRAD (the backward's weight gradients, K-grouped: K = the rows of each expert):
 //   dW_down[e] = h_e^T dy_e          M = F, N = H
@@ -76,7 +82,8 @@ constexpr int TMEM_COLS = 512;           // two accumulators of BT fp32 columns
 template <Op OP>
 struct PCfg {
     static constexpr int XBUF_BYTES = OP == Op::FC1 ? 2 * 2 * 2 * 16 * 32 * 4 : 0;
-    static constexpr int SLOT_BYTES = (OP == Op::FC1 || OP == Op::FC2) ? 16 * 64 : 16 * 128;   // WGRAD: 32 rows x 64 B
+    // WGRAD, DSWIGLU: 32 rows x 64 B (16 fp32 or 32 bf16 columns in the 64-byte swizzle)
+    static constexpr int SLOT_BYTES = (OP == Op::FC1 || OP == Op::FC2) ? 16 * 64 : 16 * 128;
     static constexpr int STG_BYTES = 4 * 2 * SLOT_BYTES;
     // WGRAD: the K-tail buffer, outside the ring: 2 operands x 2 MN chunks x 16 K rows x 128 B
     static constexpr int TAIL_BYTES = OP == Op::WGRAD ? 2 * 2 * 16 * 128 : 0;
@@ -104,8 +111,9 @@ struct Args {
     int64_t rows_cap;  // rows of the permuted tensors
     __nv_bfloat16 *h;        // FC1: h [rows, F]
     __nv_bfloat16 *stash;    // FC1: [g | u] bf16 [rows, 2F] (nullable)
-    __nv_bfloat16 *y16;      // FC2: y_perm bf16 [rows, H]
+    __nv_bfloat16 *y16;      // FC2: y_perm bf16 [rows, H]; DSWIGLU: [dg | du] bf16 [rows, 2F]
     float *y;                // DGRAD_FC1: dx_perm fp32 [rows, H]
+    const __nv_bfloat16 *aux;   // DSWIGLU: the fc1_c stash [g | u] bf16 [rows, 2F]
     // router weight of each row's route applied in the epilogue (padding rows get 0); null = unweighted
     const float *route_w;
     const int32_t *src_of_row;
@@ -157,6 +165,33 @@ __device__ __forceinline__ PTile decode(int p, const Args &a, const int *s_off, 
     const int left = rows - tb * bs;
     t.nvalid = left < bs ? left : bs;
     t.n = (t.nvalid + 15) & ~15;
+    return t;
+}
+
+// DSWIGLU pair tile p -> (expert, 256-token block, 256-feature block): within an expert the
+// token blocks vary fastest, so the clusters working at once share the feature block's W_down
+// rows and cover all of the expert's dy rows (tens of MB, held in the L2).
+struct MTile {
+    int e, fb;
+    int m0;      // first permuted row of the token block (CTA r holds rows m0 + 128 r + [0, 128))
+    int m_end;   // end of the expert's rows
+};
+
+__device__ __forceinline__ MTile decode_m(int p, const Args &a, const int *s_off, const int *s_start) {
+    int lo = 0, hi = a.E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_start[mid] <= p) lo = mid; else hi = mid - 1;
+    }
+    MTile t;
+    t.e = lo;
+    const int rows = s_off[lo + 1] - s_off[lo];
+    const int nmb = (rows + BT - 1) / BT;
+    const int local = p - s_start[lo];
+    const int mb = local % nmb;
+    t.fb = local / nmb;
+    t.m0 = s_off[lo] + mb * BT;
+    t.m_end = s_off[lo + 1];
     return t;
 }
 
@@ -380,7 +415,28 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
             uint32_t phase = 0;
             int issued = 0;
             bool ok = true;
-            for (int r = 0; r < rounds && ok && OP != Op::WGRAD; ++r) {
+            for (int r = 0; r < rounds && ok && OP == Op::DSWIGLU; ++r) {
+                const int p = round_tile(r, cid, G, total);
+                if (p < 0) continue;
+                const MTile tl = decode_m(p, args, s_off, s_start);
+                const int arow = tl.m0 + (int)rank * 128;          // this CTA's 128 token rows
+                const int brow = tl.fb * BT + (int)rank * 128;     // and its 128 rows (features) of W_down
+                for (int kb = 0; kb < kblocks; ++kb) {
+                    if (!sm100::mbar_wait(&empty_bar[stage], phase ^ 1u, abort, args.err, wait_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_base + stage * STAGE_BYTES, sb = sa + A_BYTES;
+                    const uint32_t fb_c = full0 + (uint32_t)(stage * sizeof(uint64_t));
+                    if (rank == 0) sm100::mbar_arrive_expect_tx(&full_bar[stage], 2 * STAGE_BYTES);
+                    const int k0 = kb * 64;
+                    sm100::tma_load_2d_pair(sa, &tmX, fb_c, k0, arow);          // dy_perm, K-major
+                    sm100::tma_load_3d_pair(sb, &tmW0, fb_c, k0, brow, tl.e);   // W_down [E][F][H], K-major
+                    ++issued;
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            for (int r = 0; r < rounds && ok && OP != Op::WGRAD && OP != Op::DSWIGLU; ++r) {
                 const int p = round_tile(r, cid, G, total);
                 if (p < 0) continue;
                 const PTile tl = decode(p, args, s_off, s_start);
@@ -516,8 +572,9 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
             for (int r = 0; r < rounds && ok && OP != Op::WGRAD; ++r) {
                 const int p = round_tile(r, cid, G, total);
                 if (p < 0) continue;
-                const PTile tl = decode(p, args, s_off, s_start);
-                const uint32_t idesc = sm100::idesc_bf16(256, tl.n, !a_kmajor<OP>(), false);
+                // tokens on N: the token block's width rounded up to 16; DSWIGLU: 256 features
+                const int n_mma = OP == Op::DSWIGLU ? BT : decode(p, args, s_off, s_start).n;
+                const uint32_t idesc = sm100::idesc_bf16(256, n_mma, !a_kmajor<OP>(), false);
                 const bool got_acc =
                     sm100::mbar_wait_cluster(&tempty_bar[acc], acc_phase ^ 1u, abort, args.err, wait_ns);
                 if (__any_sync(0xFFFFFFFFu, !got_acc)) { ok = false; break; }
@@ -662,6 +719,103 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                     if (lane == 0) sm100::mbar_arrive_cluster(tempty0 + (uint32_t)(acc * sizeof(uint64_t)));
                     if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
                 }
+            }
+            alive = false;   // the loop below is the other ops'
+        }
+        if constexpr (OP == Op::DSWIGLU) {
+            // this thread's token row: per 32-feature chunk, dh from TMEM, g and u from the stash,
+            // dg and du (bf16) staged as 32 rows x 64 B in the 64-byte swizzle and stored by TMA
+            // in boxes of 32 columns x 32 rows -- row by row for a warp whose rows leave the expert
+            auto put_h = [&](int j, uint4 v) {
+                *reinterpret_cast<uint4 *>(stg + slot * SLOT_BYTES + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
+            };
+            auto pack8 = [](const float *v) {
+                uint4 pk;
+                __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                return pk;
+            };
+            auto load8 = [](const __nv_bfloat16 *src, float *v) {
+                const uint4 pk = __ldg(reinterpret_cast<const uint4 *>(src));
+                const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&pk);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float2 f = __bfloat1622float2(h2[i]);
+                    v[2 * i] = f.x;
+                    v[2 * i + 1] = f.y;
+                }
+            };
+            const int F = args.N_out;
+            const int64_t ld = 2 * (int64_t)F;   // stash and output row pitch
+            for (int r = 0; r < rounds && alive; ++r) {
+                const int p = round_tile(r, cid, G, total);
+                if (p < 0) continue;
+                const MTile tl = decode_m(p, args, s_off, s_start);
+                const bool got = sm100::mbar_wait(&tfull_bar[acc], acc_phase, abort, args.err, wait_ns);
+                if (__any_sync(0xFFFFFFFFu, !got)) break;
+                sm100::tc_fence_after();
+                const uint32_t tacc = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BT);
+                const int64_t wrow0 = (int64_t)tl.m0 + (int)rank * 128 + q * 32;   // this warp's first row
+                const int64_t row = wrow0 + lane;
+                const bool whole = wrow0 + 32 <= tl.m_end && wrow0 + 32 <= args.rows_cap;   // warp-uniform
+                const bool valid = row < tl.m_end && row < args.rows_cap;
+#pragma unroll 1
+                for (int c0 = 0; c0 < BT; c0 += 32) {
+                    uint32_t d[32];
+                    sm100::tmem_ld32(tacc + c0, d);
+                    sm100::tmem_ld_wait();
+                    const int f = tl.fb * BT + c0;   // feature of this chunk's first column
+                    float dg[32], du[32];
+                    if (whole || valid) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            float gv[8], uv[8];
+                            load8(args.aux + row * ld + f + c, gv);
+                            load8(args.aux + row * ld + F + f + c, uv);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float dh = __uint_as_float(d[c + i]);
+                                const float G = gv[i], U = uv[i];
+                                if (args.clamp) {   // clamped inputs; zero derivative outside the bounds
+                                    const float gc = fminf(fmaxf(G, args.gate_lo), args.gate_hi);
+                                    const float uc = fminf(fmaxf(U, args.up_lo), args.up_hi);
+                                    const float sg = __fdividef(1.0f, 1.0f + __expf(-gc));
+                                    const bool gin = G >= args.gate_lo && G <= args.gate_hi;
+                                    const bool uin = U >= args.up_lo && U <= args.up_hi;
+                                    dg[c + i] = gin ? dh * uc * sg * (1.0f + gc * (1.0f - sg)) : 0.0f;
+                                    du[c + i] = uin ? dh * gc * sg : 0.0f;
+                                } else {
+                                    const float sg = __fdividef(1.0f, 1.0f + __expf(-G));
+                                    dg[c + i] = dh * U * sg * (1.0f + G * (1.0f - sg));
+                                    du[c + i] = dh * G * sg;
+                                }
+                            }
+                        }
+                    }
+                    if (whole) {
+#pragma unroll
+                        for (int half = 0; half < 2; ++half) {   // dg to columns f.., du to F + f..
+                            const float *v = half ? du : dg;
+                            slot_open();
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) put_h(j, pack8(v + 8 * j));
+                            slot_store(&tmOut, half ? F + f : f, (int)wrow0);
+                        }
+                    } else if (valid) {
+                        uint4 *dgr = reinterpret_cast<uint4 *>(args.y16 + row * ld + f);
+                        uint4 *dur = reinterpret_cast<uint4 *>(args.y16 + row * ld + F + f);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            dgr[j] = pack8(dg + 8 * j);
+                            dur[j] = pack8(du + 8 * j);
+                        }
+                    }
+                }
+                sm100::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) sm100::mbar_arrive_cluster(tempty0 + (uint32_t)(acc * sizeof(uint64_t)));
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
             }
             alive = false;   // the loop below is the other ops'
         }
