@@ -318,6 +318,7 @@ cudaError_t combine_rows(const float *y, const int32_t *dst, const float *w, int
 extern "C" moe_status_t moe_unpermute_combine(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                               const float *topk_w, int64_t T, int H, int k,
                                               moe_bf16_t *out, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_unpermute_combine");
     if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
     if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
@@ -330,6 +331,7 @@ extern "C" moe_status_t moe_unpermute_combine(const moe_bf16_t *y_perm, const in
 extern "C" moe_status_t moe_unpermute_combine_mxfp8(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                                     const float *topk_w, int64_t T, int H, int k, uint8_t *out_q,
                                                     uint8_t *out_sf, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_unpermute_combine_mxfp8");
     using namespace moe;
     if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
     if (k < 1 || k > 32 || H % 32 != 0) return MOE_ERR_UNSUPPORTED;
@@ -352,6 +354,7 @@ extern "C" moe_status_t moe_unpermute_combine_mxfp8(const moe_bf16_t *y_perm, co
 extern "C" moe_status_t moe_unpermute_combine_nvfp4(const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                                     const float *topk_w, int64_t T, int H, int k, uint8_t *out_q,
                                                     uint8_t *out_sf, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_unpermute_combine_nvfp4");
     using namespace moe;
     if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
     if (k < 1 || k > 32 || H % 16 != 0) return MOE_ERR_UNSUPPORTED;

@@ -4,6 +4,8 @@
 #include <initializer_list>
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stdint.h>
@@ -40,6 +42,17 @@ inline size_t ws_mtile_bytes(int E) { return ((size_t)(E + 1) * sizeof(int32_t) 
 
 // mtile_start[g] = sum over g' < g of ceil(rows(g') / 128) from group offsets (one block, G <= 1024).
 __global__ void mtile_prefix_kernel(const int32_t *__restrict__ group_offsets, int G, int32_t *__restrict__ mtile_start);
+
+// NVTX range around each entry point of the C ABI (named after the call), so that a
+// timeline tool shows which call enqueued which kernels.  Without a tool attached an NVTX
+// call returns at once.
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
+#define MOE_NVTX_RANGE(name) ::moe::NvtxRange moe_nvtx_range_(name)
 
 inline uint32_t *ws_error_word(void *ws) { return reinterpret_cast<uint32_t *>(ws); }
 

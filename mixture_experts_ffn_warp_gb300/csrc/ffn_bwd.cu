@@ -128,6 +128,7 @@ extern "C" moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const moe_bf16_t *
                                         const int32_t *group_offsets, int64_t T, int H, int E, int k,
                                         int64_t rows_cap, moe_bf16_t *dy_perm, float *d_topk_w,
                                         moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_combine_bwd");
     if (T < 0 || H < 1 || E < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
     if (k < 1 || k > 32 || H % 8 != 0 || E > gg::kMaxE) return MOE_ERR_UNSUPPORTED;
     if (!group_sizes || !group_offsets || !dy_perm) return MOE_ERR_INVALID_ARG;
@@ -220,6 +221,7 @@ extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu(const moe_bf16_t *dy_perm,
                                                       const moe_bf16_t *fc1_c, const int32_t *group_offsets,
                                                       int E, int H, int F, int64_t rows_cap, moe_bf16_t *dgu,
                                                       void *ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_dgrad_fc2_dswiglu");
     return dgrad_fc2_impl(dy_perm, W_down, fc1_c, group_offsets, E, H, F, rows_cap, dgu, ws, ws_bytes, stream,
                           nullptr);
 }
@@ -230,6 +232,7 @@ extern "C" moe_status_t moe_grouped_dgrad_fc2_dswiglu_clamped(const moe_bf16_t *
                                                               float gate_hi, float up_lo, float up_hi,
                                                               moe_bf16_t *dgu, void *ws, size_t ws_bytes,
                                                               moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_dgrad_fc2_dswiglu_clamped");
     if (!(gate_lo <= gate_hi && up_lo <= up_hi)) return MOE_ERR_INVALID_ARG;   // also rejects NaN
     const float c[4] = {gate_lo, gate_hi, up_lo, up_hi};
     return dgrad_fc2_impl(dy_perm, W_down, fc1_c, group_offsets, E, H, F, rows_cap, dgu, ws, ws_bytes, stream, c);
@@ -239,6 +242,7 @@ extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_b
                                               const moe_bf16_t *W_up, const int32_t *group_offsets, int E, int H,
                                               int F, int64_t rows_cap, float *dx_perm, void *ws, size_t ws_bytes,
                                               moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_dgrad_fc1");
     moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!dgu || !W_gate || !W_up || !group_offsets || !dx_perm) return MOE_ERR_INVALID_ARG;
@@ -288,6 +292,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
                                           const moe_bf16_t *dgu, const int32_t *group_offsets, int E, int H, int F,
                                           int64_t rows_cap, float *dW_gate, float *dW_up, float *dW_down, void *ws,
                                           size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_wgrad");
     moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK) return st;
     if (!group_offsets || !dW_gate || !dW_up || !dW_down) return MOE_ERR_INVALID_ARG;
@@ -388,6 +393,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
 
 extern "C" moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *dst_of_route, int64_t T, int H, int k,
                                           moe_bf16_t *dx, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_unpermute_sum");
     if (T < 0 || H < 1) return MOE_ERR_INVALID_ARG;
     if (k < 1 || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
     if (T == 0) return MOE_OK;
@@ -403,6 +409,7 @@ extern "C" moe_status_t moe_grouped_ffn_bwd(
     int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm, moe_bf16_t *dgu,
     float *dx_perm, moe_bf16_t *dx, float *dW_gate, float *dW_up, float *dW_down, float *d_topk_w, void *ws,
     size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_ffn_bwd");
     moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK) return st;
     st = moe_combine_bwd(dY, y_perm, dst_of_route, topk_w, group_sizes, group_offsets, T, H, E, k, rows_cap,

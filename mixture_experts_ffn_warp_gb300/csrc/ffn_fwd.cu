@@ -121,6 +121,7 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu(const moe_bf16_t *x_perm, const m
                                                int E, int H, int F, int64_t rows_cap, moe_bf16_t *h,
                                                moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
                                                moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_fc1_swiglu");
     return fc1_impl(x_perm, W_gate, W_up, group_offsets, nullptr, nullptr, E, H, F, rows_cap, h, fc1_c, ws,
                     ws_bytes, stream);
 }
@@ -129,6 +130,7 @@ extern "C" moe_status_t moe_grouped_fc2(const moe_bf16_t *h, const moe_bf16_t *W
                                         const int32_t *group_offsets, int E, int H, int F,
                                         int64_t rows_cap, moe_bf16_t *y_perm, void *ws, size_t ws_bytes,
                                         moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_fc2");
     return fc2_impl(h, W_down, group_offsets, nullptr, nullptr, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
 }
 
@@ -138,6 +140,7 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_weighted(const moe_bf16_t *x_perm
                                                         int H, int F, int64_t rows_cap, moe_bf16_t *h,
                                                         moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
                                                         moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_fc1_swiglu_weighted");
     if (rows_cap > 0 && (!src_of_row || !topk_w)) return MOE_ERR_INVALID_ARG;
     return fc1_impl(x_perm, W_gate, W_up, group_offsets, src_of_row, topk_w, E, H, F, rows_cap, h, fc1_c, ws,
                     ws_bytes, stream);
@@ -147,6 +150,7 @@ extern "C" moe_status_t moe_grouped_fc2_weighted(const moe_bf16_t *h, const moe_
                                                  const int32_t *group_offsets, const int32_t *src_of_row,
                                                  const float *topk_w, int E, int H, int F, int64_t rows_cap,
                                                  moe_bf16_t *y_perm, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_fc2_weighted");
     if (rows_cap > 0 && (!src_of_row || !topk_w)) return MOE_ERR_INVALID_ARG;
     return fc2_impl(h, W_down, group_offsets, src_of_row, topk_w, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
 }
@@ -157,6 +161,7 @@ extern "C" moe_status_t moe_grouped_ffn_fwd(const moe_bf16_t *x_perm, const moe_
                                             int64_t rows_cap, moe_bf16_t *h, moe_bf16_t *y_perm,
                                             moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
                                             moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_ffn_fwd");
     moe_status_t st = check_common(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!x_perm || !W_gate || !W_up || !W_down || !group_offsets || !h || !y_perm) return MOE_ERR_INVALID_ARG;
@@ -172,6 +177,7 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_clamped(const moe_bf16_t *x_perm,
                                                        int F, int64_t rows_cap, float gate_lo, float gate_hi,
                                                        float up_lo, float up_hi, moe_bf16_t *h, moe_bf16_t *fc1_c,
                                                        void *ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_fc1_swiglu_clamped");
     if (!clamp_bounds_ok(gate_lo, gate_hi, up_lo, up_hi)) return MOE_ERR_INVALID_ARG;
     if (rows_cap > 0 && (src_of_row == nullptr) != (topk_w == nullptr)) return MOE_ERR_INVALID_ARG;
     const float c[4] = {gate_lo, gate_hi, up_lo, up_hi};

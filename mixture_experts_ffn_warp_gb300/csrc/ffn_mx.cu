@@ -77,6 +77,7 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8(const uint8_t *x_q, const u
                                                      int64_t rows_cap, uint8_t *h_q, uint8_t *h_sf,
                                                      moe_bf16_t *fc1_c, void *ws, size_t ws_bytes,
                                                      moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_fc1_swiglu_mxfp8");
     return fc1_mx_impl(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, E, H, F, rows_cap, h_q, h_sf, fc1_c, ws,
                        ws_bytes, stream, nullptr);
 }
@@ -86,6 +87,7 @@ extern "C" moe_status_t moe_grouped_fc1_swiglu_mxfp8_clamped(
     const uint8_t *Wu_sf, const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap, float gate_lo,
     float gate_hi, float up_lo, float up_hi, uint8_t *h_q, uint8_t *h_sf, moe_bf16_t *fc1_c, void *ws,
     size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_fc1_swiglu_mxfp8_clamped");
     if (!(gate_lo <= gate_hi && up_lo <= up_hi)) return MOE_ERR_INVALID_ARG;   // also rejects NaN
     const float c[4] = {gate_lo, gate_hi, up_lo, up_hi};
     return fc1_mx_impl(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, E, H, F, rows_cap, h_q, h_sf, fc1_c, ws,
@@ -131,6 +133,7 @@ extern "C" moe_status_t moe_grouped_fc2_mxfp8(const uint8_t *h_q, const uint8_t 
                                               const uint8_t *Wd_sf, const int32_t *group_offsets, int E, int H, int F,
                                               int64_t rows_cap, moe_bf16_t *y_perm, void *ws, size_t ws_bytes,
                                               moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_fc2_mxfp8");
     return fc2_mx_impl(h_q, h_sf, Wd_q, Wd_sf, group_offsets, E, H, F, rows_cap, y_perm, ws, ws_bytes, stream);
 }
 
@@ -140,6 +143,7 @@ extern "C" moe_status_t moe_grouped_ffn_fwd_mxfp8(const uint8_t *x_q, const uint
                                                   const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap,
                                                   uint8_t *h_q, uint8_t *h_sf, moe_bf16_t *y_perm, void *ws,
                                                   size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_ffn_fwd_mxfp8");
     moe_status_t st = moe_grouped_fc1_swiglu_mxfp8(x_q, x_sf, Wg_q, Wg_sf, Wu_q, Wu_sf, group_offsets, E, H, F,
                                                    rows_cap, h_q, h_sf, nullptr, ws, ws_bytes, stream);
     if (st != MOE_OK) return st;

@@ -736,8 +736,7 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                 for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
                 return pk;
             };
-            auto load8 = [](const __nv_bfloat16 *src, float *v) {
-                const uint4 pk = __ldg(reinterpret_cast<const uint4 *>(src));
+            auto unpack8 = [](const uint4 &pk, float *v) {
                 const __nv_bfloat162 *h2 = reinterpret_cast<const __nv_bfloat162 *>(&pk);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -760,8 +759,23 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                 const int64_t row = wrow0 + lane;
                 const bool whole = wrow0 + 32 <= tl.m_end && wrow0 + 32 <= args.rows_cap;   // warp-uniform
                 const bool valid = row < tl.m_end && row < args.rows_cap;
+                // the stash values of a chunk are loaded one chunk ahead of their use
+                uint4 gq[4] = {}, uq[4] = {}, gn[4] = {}, un[4] = {};
+                auto load_stash = [&](int c0, uint4 (&g)[4], uint4 (&u)[4]) {
+                    if (whole || valid) {
+                        const uint4 *gs = reinterpret_cast<const uint4 *>(args.aux + row * ld + tl.fb * BT + c0);
+                        const uint4 *us = reinterpret_cast<const uint4 *>(args.aux + row * ld + F + tl.fb * BT + c0);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            g[j] = __ldg(gs + j);
+                            u[j] = __ldg(us + j);
+                        }
+                    }
+                };
+                load_stash(0, gq, uq);
 #pragma unroll 1
                 for (int c0 = 0; c0 < BT; c0 += 32) {
+                    if (c0 + 32 < BT) load_stash(c0 + 32, gn, un);
                     uint32_t d[32];
                     sm100::tmem_ld32(tacc + c0, d);
                     sm100::tmem_ld_wait();
@@ -771,8 +785,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
                             float gv[8], uv[8];
-                            load8(args.aux + row * ld + f + c, gv);
-                            load8(args.aux + row * ld + F + f + c, uv);
+                            unpack8(gq[c / 8], gv);
+                            unpack8(uq[c / 8], uv);
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
                                 const float dh = __uint_as_float(d[c + i]);
@@ -810,6 +824,11 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                             dgr[j] = pack8(dg + 8 * j);
                             dur[j] = pack8(du + 8 * j);
                         }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        gq[j] = gn[j];
+                        uq[j] = un[j];
                     }
                 }
                 sm100::tc_fence_before();

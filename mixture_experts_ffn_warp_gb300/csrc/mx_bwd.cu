@@ -118,6 +118,7 @@ dequantize_weights_kernel(const uint8_t *__restrict__ data, const uint8_t *__res
 extern "C" moe_status_t moe_dequantize_rows_mxfp8(const uint8_t *codes, const uint8_t *tile_scales,
                                                   const int32_t *group_offsets, int G, int64_t rows, int K,
                                                   moe_bf16_t *out, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_dequantize_rows_mxfp8");
     using namespace moe;
     if (rows < 0 || K < 1 || G < 1) return MOE_ERR_INVALID_ARG;
     if (K % 128 != 0 || G > 1024 || rows >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
@@ -137,6 +138,7 @@ extern "C" moe_status_t moe_dequantize_rows_mxfp8(const uint8_t *codes, const ui
 
 extern "C" moe_status_t moe_dequantize_weights_mxfp8(const uint8_t *data, const uint8_t *scales, int E, int K, int N,
                                                      moe_bf16_t *W, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_dequantize_weights_mxfp8");
     using namespace moe;
     if (E < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
     if (K % 128 != 0 || N % 128 != 0 || E > 65535 || K / 32 > 65535) return MOE_ERR_UNSUPPORTED;

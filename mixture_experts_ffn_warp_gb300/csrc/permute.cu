@@ -460,6 +460,7 @@ extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx
                                     int32_t *dst_of_route, int32_t *src_of_row,
                                     int32_t *group_sizes, int32_t *group_offsets, void *ws,
                                     size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_permute");
     using namespace moe;
     if (T < 0 || H < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
     if (E < 1 || E > 1024 || k < 1 || k > 32 || align < 1 || align > 1024 || H % 8 != 0)
@@ -580,6 +581,7 @@ extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const in
                                                    int32_t *src_of_row, int32_t *group_sizes,
                                                    int32_t *group_offsets, uint32_t *error_word,
                                                    moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_permute_static_scratch");
     using namespace moe;
     if (T < 0 || H < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
     if (E < 1 || E > 1024 || k < 1 || k > 32 || align < 1 || align > 1024 || H % 8 != 0)
@@ -754,6 +756,7 @@ extern "C" moe_status_t moe_permute_mxfp8(const moe_bf16_t *x, const int32_t *to
                                           int k, uint8_t *x_q, uint8_t *x_sf, int64_t rows_cap,
                                           int32_t *dst_of_route, int32_t *src_of_row, int32_t *group_sizes,
                                           int32_t *group_offsets, void *ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_permute_mxfp8");
     using namespace moe;
     if (T < 0 || H < 1 || rows_cap < 0) return MOE_ERR_INVALID_ARG;
     if (E < 1 || E > 1024 || k < 1 || k > 32 || H % 128 != 0) return MOE_ERR_UNSUPPORTED;

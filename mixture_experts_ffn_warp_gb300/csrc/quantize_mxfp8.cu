@@ -164,6 +164,7 @@ extern "C" moe_status_t moe_grouped_quantize_mxfp8(const moe_bf16_t *in, int64_t
                                                    const int32_t *group_offsets, int G, uint8_t *data,
                                                    uint8_t *scale_rowmajor, uint8_t *scale_tiles, void *ws,
                                                    size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_quantize_mxfp8");
     using namespace moe;
     if (rows < 0 || K < 1) return MOE_ERR_INVALID_ARG;
     if (K % 128 != 0 || rows >= 0x7FFFFFFF) return MOE_ERR_UNSUPPORTED;
@@ -185,6 +186,7 @@ extern "C" moe_status_t moe_grouped_quantize_mxfp8(const moe_bf16_t *in, int64_t
 
 extern "C" moe_status_t moe_quantize_weights_mxfp8(const moe_bf16_t *W, int E, int K, int N, uint8_t *data,
                                                    uint8_t *scales, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_quantize_weights_mxfp8");
     if (E < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
     if (K % 128 != 0 || N % 128 != 0 || E > 65535 || K / 32 > 65535) return MOE_ERR_UNSUPPORTED;
     if (!W || !data || !scales) return MOE_ERR_INVALID_ARG;

@@ -231,6 +231,7 @@ moe_status_t check_route(int64_t T, int E, int k) {
 
 extern "C" moe_status_t moe_route_topk(const float *logits, int64_t T, int E, int k,
                                        int32_t *topk_idx, float *topk_w, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_route_topk");
     moe_status_t st = check_route(T, E, k);
     if (st != MOE_OK || T == 0) return st;
     if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -240,6 +241,7 @@ extern "C" moe_status_t moe_route_topk(const float *logits, int64_t T, int E, in
 extern "C" moe_status_t moe_route_topk_sigmoid(const float *logits, const float *expert_bias, int64_t T, int E,
                                                int k, int normalize, int32_t *topk_idx, float *topk_w,
                                                moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_route_topk_sigmoid");
     moe_status_t st = check_route(T, E, k);
     if (st != MOE_OK || T == 0) return st;
     if (!logits || !topk_idx || !topk_w) return MOE_ERR_INVALID_ARG;
@@ -250,6 +252,7 @@ extern "C" moe_status_t moe_route_topk_sigmoid(const float *logits, const float 
 extern "C" moe_status_t moe_route_topk_bwd(const float *logits, const int32_t *topk_idx, const float *d_topk_w,
                                            int64_t T, int E, int k, int score_fn, int normalize, float *d_logits,
                                            moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_route_topk_bwd");
     moe_status_t st = check_route(T, E, k);
     if (st != MOE_OK || T == 0) return st;
     if (score_fn != MOE_SCORE_SOFTMAX && score_fn != MOE_SCORE_SIGMOID) return MOE_ERR_INVALID_ARG;
