@@ -64,6 +64,9 @@ typedef enum {
 #define MOE_DEVERR_BAD_EXPERT_ID 0x1u  /* a topk id outside [-1, E): route treated as dropped */
 #define MOE_DEVERR_TIMEOUT       0x2u  /* a bounded device wait gave up; outputs are invalid */
 #define MOE_DEVERR_CAPACITY      0x4u  /* routed rows exceed rows_cap; extra rows not written */
+#define MOE_DEVERR_BOUNDS        0x8u  /* bounds-check builds only (-DMOE_BOUNDS_CHECK): group
+                                          offsets that a GEMM read were not non-decreasing within
+                                          [0, rows_cap]; the GEMM computed nothing */
 
 /* Alignment: the kernels move 16-byte vectors.  The row tensors of moe_permute (x, x_perm),
  * moe_permute_static_scratch, moe_unpermute_combine (y_perm, out), moe_combine_bwd

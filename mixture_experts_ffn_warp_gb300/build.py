@@ -48,18 +48,23 @@ def _fingerprint(extra: list[str]) -> str:
     return h.hexdigest()
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out_dir: str | None = None) -> str:
+    """Compile the library (into out_dir, default _build/) and return its path.  extra_flags
+    are added to every nvcc command, e.g. ["-DMOE_BOUNDS_CHECK"] for the bounds-check build."""
     extra = list(extra_flags or [])
-    os.makedirs(OUT_DIR, exist_ok=True)
-    stamp = os.path.join(OUT_DIR, "fingerprint.txt")
+    out = out_dir or OUT_DIR
+    lib = os.path.join(out, LIB_NAME)
+    os.makedirs(out, exist_ok=True)
+    stamp = os.path.join(out, "fingerprint.txt")
     fp = _fingerprint(extra)
-    if not force and os.path.exists(LIB) and os.path.exists(stamp) and open(stamp).read() == fp:
-        return LIB
+    if not force and os.path.exists(lib) and os.path.exists(stamp) and open(stamp).read() == fp:
+        return lib
     nvcc = _nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out, os.path.basename(src)[:-3] + ".o")
         cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
@@ -73,15 +78,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = _sources()
     with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".{os.getpid()}.tmp"
+    tmp = lib + f".{os.getpid()}.tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
     with open(stamp, "w") as f:
         f.write(fp)
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

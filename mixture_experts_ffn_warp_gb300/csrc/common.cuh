@@ -116,6 +116,28 @@ __device__ __forceinline__ void raise_device_error(uint32_t *err, uint32_t bits)
     if (err) atomicOr(err, bits);
 }
 
+// Bounds-check builds (-DMOE_BOUNDS_CHECK; compute-sanitizer is not available for this
+// library's tests): a GEMM first checks the group offsets it read from device memory -- the
+// one data-dependent extent its loads, MMAs and stores trust -- and on a violation raises
+// MOE_DEVERR_BOUNDS and computes nothing.  Called by one whole warp over s_off[0..G]; true
+// when 0 <= s_off[0] <= ... <= s_off[G] <= rows_cap.  Always true in other builds.
+__device__ __forceinline__ bool group_offsets_in_bounds(const int *s_off, int G, int64_t rows_cap, int lane,
+                                                        uint32_t *err) {
+#ifdef MOE_BOUNDS_CHECK
+    bool bad = false;
+    for (int i = lane; i <= G; i += 32) {
+        const int v = s_off[i];
+        if (v < 0 || v > rows_cap || (i < G && v > s_off[i + 1])) bad = true;
+    }
+    bad = __any_sync(0xFFFFFFFFu, bad);
+    if (bad && lane == 0) raise_device_error(err, MOE_DEVERR_BOUNDS);
+    return !bad;
+#else
+    (void)s_off; (void)G; (void)rows_cap; (void)lane; (void)err;
+    return true;
+#endif
+}
+
 // ---------------------------------------------------------------- programmatic dependent launch
 // Every kernel of the library is launched with programmatic stream serialization, so the
 // GPU may schedule it as the kernel before it on the stream drains, instead of after that

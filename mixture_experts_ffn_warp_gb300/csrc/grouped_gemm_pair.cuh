@@ -315,7 +315,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                 run += tiles_of(e0 + i);
             }
         }
-        if (lane == 31) s_start[E] = incl;
+        const bool offs_ok = group_offsets_in_bounds(s_off, E, args.rows_cap, lane, args.err);
+        if (lane == 31) s_start[E] = offs_ok ? incl : 0;   // no tiles for offsets out of bounds
     }
     sm100::tc_fence_before();
     __syncthreads();
