@@ -49,9 +49,15 @@ MEASURED_MXFP8_TFLOPS = 3254.0
 # DRAM traffic (read + write bytes per launch) of a workload's dominant kernel from one
 # ncu capture (profiles/), with a hash of the kernel sources it was taken on.  Reported as
 # null once those sources change.
-PROFILED_TRAFFIC = {("fine_grained", "fc1_swiglu"): (903.9e6, "0f30777fdba1d6a4")}
+PROFILED_TRAFFIC = {
+    ("fine_grained", "fc1_swiglu"): (903.9e6, "70500fbdff034b1a"),
+    # captured at F = 2048 (both launches: 1199.9 MB) and scaled to F = 14336: reads by each
+    # launch's measured/operand-byte ratio, writes = fp32 gradient bytes less the measured
+    # L2-resident residue
+    ("mixtral", "wgrad"): (7282.7e6, "70500fbdff034b1a"),
+}
 KERNEL_SOURCES = ["common.cuh", "sm100.cuh", "grouped_gemm.cuh", "grouped_gemm_pair.cuh", "gemm_launch.cuh", "tmap.cuh",
-                  "ffn_fwd.cu"]
+                  "ffn_fwd.cu", "ffn_bwd.cu"]
 
 
 def kernel_source_hash() -> str:
