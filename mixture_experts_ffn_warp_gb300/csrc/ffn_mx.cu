@@ -1,9 +1,11 @@
 // ffn_mx.cu -- A7: the grouped expert FFN on MXFP8 operands (E4M3 data, UE8M0 scales
 // per 32 K elements) with block-scaled tcgen05 MMAs.  FC1 quantises h to MXFP8
-// along F in its epilogue; FC2 writes fp32 expert outputs.  Activation tiles come
-// in by TMA; weight tiles (pre-swizzled 16 KB blocks from moe_quantize_weights_mxfp8)
-// and all scale atoms by plain bulk copies.
+// along F in its epilogue; FC2 writes bf16 expert outputs.  FC1 runs on CTA pairs with the
+// tokens on N (grouped_gemm_pair_mx.cuh) unless the bf16 g | u stash is asked for; FC2, and
+// FC1 with the stash, on the one-CTA kernel (grouped_gemm.cuh), whose weight tiles and scale
+// atoms come in by plain bulk copies.
 #include "gemm_launch.cuh"
+#include "grouped_gemm_pair_mx.cuh"
 
 using namespace moe;
 using gg::Op;
@@ -18,6 +20,10 @@ moe_status_t check_mx(int E, int H, int F, int64_t rows_cap, void *ws, size_t ws
 }
 
 int64_t mblock_bound(int64_t rows_cap, int E) { return (rows_cap + gg::BM - 1) / gg::BM + E; }
+// upper bound of the pair GEMMs' token blocks over all experts
+int64_t token_block_bound(int64_t rows_cap, int E) { return (rows_cap + gpm::BT - 1) / gpm::BT + E; }
+// 128-row scale tiles of the tile layout (moe_mx_tile_scale_bytes)
+uint64_t scale_tiles(int64_t rows_cap, int E) { return (uint64_t)((rows_cap + 127) / 128 + E); }
 
 bool aligned16(const void *p) { return reinterpret_cast<uintptr_t>(p) % 16 == 0; }
 
@@ -36,27 +42,62 @@ moe_status_t fc1_mx_impl(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t 
         return MOE_ERR_INVALID_ARG;
     if (!aligned16(x_sf) || !aligned16(Wg_sf) || !aligned16(Wu_sf) || !aligned16(Wg_q) || !aligned16(Wu_q))
         return MOE_ERR_UNSUPPORTED;
-    CUtensorMap tA, tC;
-    if (!tmap_u8_2d(&tA, x_q, H, rows_cap, H, 128, 128) || !tmap_store_2d(&tC, h_q, 1, F, rows_cap, F))
+    if (fc1_c) {
+        // with the g | u stash: one CTA per tile, tokens on M, so that each epilogue thread
+        // holds one token's row and writes the stash rows with 16-byte stores (the pair kernel
+        // holds one feature per thread and measured slower with the stash: 2.07 against 1.94 ms
+        // on the DeepSeek-V3 shape)
+        CUtensorMap tA, tC;
+        if (!tmap_u8_2d(&tA, x_q, H, rows_cap, H, 128, 128) || !tmap_store_2d(&tC, h_q, 1, F, rows_cap, F))
+            return MOE_ERR_UNSUPPORTED;
+        gg::Args b{};
+        b.group_offsets = group_offsets;
+        b.E = E;
+        b.N = F;
+        b.K = H;
+        b.n_tiles = F / 128;
+        b.rows_cap = rows_cap;
+        b.sfa = x_sf;
+        b.sfb0 = Wg_sf;
+        b.sfb1 = Wu_sf;
+        b.b0_tiles = Wg_q;
+        b.b1_tiles = Wu_q;
+        b.nb_rows = F;
+        b.out_q = h_q;
+        b.ld0 = F;
+        b.out_sf = h_sf;
+        b.out1 = reinterpret_cast<__nv_bfloat16 *>(fc1_c);
+        b.ld1 = 2 * (int64_t)F;
+        if (clamp) {
+            b.clamp = 1;
+            b.gate_lo = clamp[0];
+            b.gate_hi = clamp[1];
+            b.up_lo = clamp[2];
+            b.up_hi = clamp[3];
+        }
+        b.err = ws_error_word(ws);
+        return gg::launch<Op::FC1_MX, 256>(tA, tA, tA, tC, tC, b, mblock_bound(rows_cap, E) * b.n_tiles,
+                                           (cudaStream_t)stream);
+    }
+    // without it: CTA pairs, per pair tile the gate (first CTA) and up (second CTA) weight
+    // blocks of 128 features (M = 256) x up to 256 tokens (N)
+    const uint64_t wblocks = (uint64_t)E * (H / 128) * (F / 128);
+    CUtensorMap tA0, tA1, tSA0, tSA1, tX, tX32, tSB;
+    if (!tmap_u8_rows(&tA0, Wg_q, 128, wblocks * 128, 128) || !tmap_u8_rows(&tA1, Wu_q, 128, wblocks * 128, 128) ||
+        !tmap_u8_rows(&tSA0, Wg_sf, 16, wblocks * 32, 32) || !tmap_u8_rows(&tSA1, Wu_sf, 16, wblocks * 32, 32) ||
+        !tmap_u8_2d(&tX, x_q, H, rows_cap, H, 128, 128) || !tmap_u8_2d(&tX32, x_q, H, rows_cap, H, 128, 32) ||
+        !tmap_sf_tile_pairs(&tSB, x_sf, H / 128, scale_tiles(rows_cap, E)))
         return MOE_ERR_UNSUPPORTED;
-    gg::Args a{};
+    if (reinterpret_cast<uintptr_t>(h_q) % 16 != 0) return MOE_ERR_UNSUPPORTED;   // 16-byte code stores
+    gpm::Args a{};
     a.group_offsets = group_offsets;
     a.E = E;
-    a.N = F;
     a.K = H;
-    a.n_tiles = F / 128;
+    a.N_out = F;
+    a.n_fb = F / 128;
     a.rows_cap = rows_cap;
-    a.sfa = x_sf;
-    a.sfb0 = Wg_sf;
-    a.sfb1 = Wu_sf;
-    a.b0_tiles = Wg_q;
-    a.b1_tiles = Wu_q;
-    a.nb_rows = F;
-    a.out_q = h_q;
-    a.ld0 = F;
-    a.out_sf = h_sf;
-    a.out1 = reinterpret_cast<__nv_bfloat16 *>(fc1_c);   // nullable: the g | u stash
-    a.ld1 = 2 * (int64_t)F;
+    a.h_q = h_q;
+    a.h_sf = h_sf;
     if (clamp) {
         a.clamp = 1;
         a.gate_lo = clamp[0];
@@ -65,8 +106,8 @@ moe_status_t fc1_mx_impl(const uint8_t *x_q, const uint8_t *x_sf, const uint8_t 
         a.up_hi = clamp[3];
     }
     a.err = ws_error_word(ws);
-    return gg::launch<Op::FC1_MX, 256>(tA, tA, tA, tC, tC, a, mblock_bound(rows_cap, E) * a.n_tiles,
-                                       (cudaStream_t)stream);
+    return gpm::launch(tA0, tA1, tSA0, tSA1, tX, tX32, tSB, a,
+                                     token_block_bound(rows_cap, E) * a.n_fb, (cudaStream_t)stream);
 }
 
 }  // namespace
@@ -104,6 +145,7 @@ moe_status_t fc2_mx_impl(const uint8_t *h_q, const uint8_t *h_sf, const uint8_t 
     if (st != MOE_OK || rows_cap == 0) return st;
     if (!h_q || !h_sf || !Wd_q || !Wd_sf || !group_offsets || !y_perm) return MOE_ERR_INVALID_ARG;
     if (!aligned16(h_sf) || !aligned16(Wd_sf) || !aligned16(Wd_q)) return MOE_ERR_UNSUPPORTED;
+    // one CTA per tile: 128 tokens (M) x 256 (or 128) output columns (N)
     const int bn = (H % 256 == 0) ? 256 : 128;
     CUtensorMap tA, tC;
     if (!tmap_u8_2d(&tA, h_q, F, rows_cap, F, 128, 128) || !tmap_store_2d(&tC, y_perm, 2, H, rows_cap, H))

@@ -91,11 +91,13 @@ inline bool tmap_store_2d(CUtensorMap *m, const void *base, int elem_bytes, uint
 }
 
 // Store map without swizzle: 2-D row-major [outer, inner] of `elem_bytes`-byte elements
-// (bf16 or fp32), row pitch `ld` elements, boxes of box_inner x box_rows (dense rows in
+// (bf16, fp32 or bytes), row pitch `ld` elements, boxes of box_inner x box_rows (dense rows in
 // shared memory).
 inline bool tmap_store_plain(CUtensorMap *m, const void *base, int elem_bytes, uint64_t inner, uint64_t outer,
                              uint64_t ld, uint32_t box_inner, uint32_t box_rows) {
-    const CUtensorMapDataType dt = elem_bytes == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType dt = elem_bytes == 4   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                   : elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     const uint64_t dims[2] = {inner, outer};
     const uint64_t strides[1] = {ld * (uint64_t)elem_bytes};
     const uint32_t box[2] = {box_inner, box_rows};
@@ -118,6 +120,27 @@ inline bool tmap_u8_3d(CUtensorMap *m, const void *base, uint64_t d0, uint64_t d
     const uint64_t strides[2] = {d0, d0 * d1};
     const uint32_t box[3] = {box0, box1, 1};
     return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box);
+}
+
+// Blocks of `row_bytes`-byte rows stored one after another (the pre-swizzled MXFP8 weight
+// blocks, rows of 128 bytes; the 512-byte scale atoms, rows of 16 bytes) as a 2-D byte
+// tensor [rows, row_bytes] without swizzle, boxes of box_rows rows: a load copies the bytes
+// as they are.
+inline bool tmap_u8_rows(CUtensorMap *m, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows) {
+    const uint64_t dims[2] = {row_bytes, rows};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {(uint32_t)row_bytes, box_rows};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// MXFP8 row scales in the tile layout ([tile][K/128] atoms of 32 x 16 bytes) as the 4-D byte
+// tensor [tiles][K/128][32][16]; a box holds the atoms of one K block of two consecutive
+// tiles (1 KB), tiles past the end read as zeros.
+inline bool tmap_sf_tile_pairs(CUtensorMap *m, const void *base, uint64_t kblocks, uint64_t tiles) {
+    const uint64_t dims[4] = {16, 32, kblocks, tiles};
+    const uint64_t strides[3] = {16, 512, kblocks * 512};
+    const uint32_t box[4] = {16, 32, 1, 2};
+    return encode_tmap(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 }  // namespace moe

@@ -13,7 +13,7 @@ from mixture_experts_ffn_warp_gb300 import (MoeForwardMX, MxWeights, Workspace, 
                                             moe_permute, moe_permute_mxfp8, moe_quantize_weights_mxfp8,
                                             moe_route_topk, moe_unpermute_combine)
 from mixture_experts_ffn_warp_gb300.synthetic import CONFIGS, small_shape
-from helpers import TOL_MXFP8, assert_close_rms, bits, gpu_inputs, to_f64
+from helpers import TOL_MXFP8, assert_close_rms, assert_close_rms_mx, bits, gpu_inputs, to_f64
 
 pytestmark = pytest.mark.gpu
 
@@ -137,6 +137,9 @@ SMALL = {
     "ragged": small_shape("ragged", T=300, H=256, F=384, E=5, k=2),
     "h384": small_shape("h384", T=257, H=384, F=256, E=7, k=3),   # FC2 with 128-wide tiles
     "many": small_shape("many", T=512, H=256, F=128, E=64, k=4, skew=True),
+    # experts of 1011, 25, 317, 1400, 1367 and 80 rows: several 256-token blocks, last blocks
+    # of every kind (one CTA's half of at most 32 tokens, or more)
+    "blocks": small_shape("blocks", T=1400, H=256, F=384, E=6, k=3, skew=True),
 }
 
 
@@ -206,3 +209,38 @@ def test_mxfp8_stash_leaves_the_forward_unchanged():
     assert torch.equal(out0, out1)
     ref = moe_unpermute_combine(m0.y_perm, m0.perm.dst_of_route, m0.topk_w)
     assert torch.equal(out0, ref)
+
+
+def _e4m3_values() -> np.ndarray:
+    return np.array([oracle.e4m3_to_double(c) for c in range(256)])
+
+
+def test_mxfp8_h_codes_over_token_blocks():
+    """The FC1 epilogue's h codes and scales on experts cut into several 256-token blocks:
+    decoded, they are the exact h of the MXFP8 operands within the encoding's own rounding
+    (oracle, fp64), and every 32-feature block's scale is the smallest power of two that
+    keeps the block within E4M3's 448 (its largest code is at least 224 in magnitude)."""
+    shape = SMALL["blocks"]
+    inp = gpu_inputs(shape, with_dy=False)
+    w = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"])
+    m = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k)
+    m(inp["x"], inp["logits"], w)
+    torch.cuda.synchronize()
+    assert m.ws.read_error() == 0
+    sizes = m.perm.group_sizes.cpu().numpy()
+    tail = sizes % 256
+    assert (sizes > 512).any() and ((tail > 0) & (tail <= 64)).any() and (tail > 64).any(), sizes
+    go = m.perm.group_offsets.cpu().numpy()
+    used = int(go[-1])
+    codes = m.h_q[:used].cpu().numpy()
+    sc = tiles_to_rowmajor(m.h_sf.cpu().numpy(), go, used, shape.F)
+    vals = _e4m3_values()
+    mag = np.abs(vals[codes]).reshape(used, shape.F // 32, 32).max(axis=2)
+    assert np.all((mag >= 224) | (sc == 0)), "a block scale is not the smallest that fits"
+    got = oracle.mx_dequantize(codes, sc)
+    idx, tw = m.topk_idx.cpu().numpy(), m.topk_w.cpu().numpy()
+    xq = oracle.mx_roundtrip_rows(bits(inp["x"]))
+    wg, wu, wd = oracle.mx_roundtrip_weights(bits(inp["W_gate"]), bits(inp["W_up"]), bits(inp["W_down"]))
+    ref = oracle.moe_fwd(xq, wg, wu, wd, idx, tw, round_mode=0, want_h=True)
+    dst = m.perm.dst_of_route.cpu().numpy().reshape(-1)
+    assert_close_rms_mx(got[dst], ref["h"], sc[dst], what="h (MXFP8) over token blocks")
