@@ -240,7 +240,17 @@ class Group:
         self.name, self.run, self.flop, self.nbytes, self.launches, self.fp8 = name, run, flop, nbytes, launches, fp8
 
 
-def build_workload(shape, dev, stream):
+def group_align(shape, requested=None) -> int:
+    """Rows each expert's group is padded to (with zero rows) in the permutation.  The bf16
+    forward + backward pads to 16, so that every expert's rows are whole 16-row K slices of
+    the weight-gradient GEMM (no zero-padded tail slice to build per expert); the padding rows
+    carry zeros through every GEMM and change no result."""
+    if requested is not None:
+        return requested
+    return 16 if (shape.backward and not shape.mxfp8) else 1
+
+
+def build_workload(shape, dev, stream, align=1):
     """Inputs, pre-allocated layer objects and the step's kernel groups."""
     import torch
     from mixture_experts_ffn_warp_gb300 import MoeBackward, MoeBackwardMX, MoeForward, MoeForwardMX, MxWeights
@@ -265,7 +275,8 @@ def build_workload(shape, dev, stream):
             w["bwd"] = w["make_bwd"](m)
             w["bwd_weights"] = mw.dequantized(stream)
     else:
-        w["make_layer"] = lambda: MoeForward(T, H, F, E, k, device=dev, keep_fc1_c=shape.backward,  # noqa: E731
+        w["make_layer"] = lambda: MoeForward(T, H, F, E, k, device=dev, align=align,  # noqa: E731
+                                             keep_fc1_c=shape.backward,
                                              router="sigmoid" if sigmoid else "softmax",
                                              expert_bias=inp.get("expert_bias"), weight_at=shape.weight_at)
         w["make_bwd"] = lambda f: MoeBackward(f, want_d_logits=True)  # noqa: E731
@@ -296,7 +307,7 @@ def build_workload(shape, dev, stream):
         stash = R * 2 * F * 2 if shape.backward else 0
         g += [
             Group("permute", lambda: m.permute(inp["x"], stream), nbytes=T * H * 2 + R * H * 2 + R * 8,
-                  launches=2),
+                  launches=3 if align > 1 else 2),   # + the zero fill of the padding rows
             Group("fc1_swiglu", lambda: m.fc1(inp["W_gate"], inp["W_up"], stream), flop=4.0 * R * H * F,
                   nbytes=R * H * 2 + 2 * wbytes + R * F * 2 + stash),
             Group("fc2", lambda: m.fc2(inp["W_down"], stream), flop=2.0 * R * H * F,
@@ -544,7 +555,8 @@ def run_gpu(args):
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
 
     with torch.cuda.stream(stream):
-        w = build_workload(shape, dev, stream)
+        align = group_align(shape, args.align)
+        w = build_workload(shape, dev, stream, align)
     groups = w["groups"]
     m = w["layer"]
 
@@ -671,6 +683,7 @@ def run_gpu(args):
         "roofline": roof,
         "clocks": clk,
         "gpu_launches": args.steps * sum(g.launches for g in groups),
+        "group_align": align,
         "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": ms_e2e,
                 "how": "HostPipeline (two slots; upload, compute and download streams): K steps from the first "
@@ -695,6 +708,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="mixtral",
                     choices=["tiny", "fine_grained", "mixtral", "skewed", "dsv3_mxfp8"])
+    ap.add_argument("--align", type=int, default=None,
+                    help="pad each expert's rows to a multiple of this (default: 16 for the bf16 "
+                         "forward + backward, else 1)")
     ap.add_argument("--shape", default="",
                     help="override sizes of the workload, e.g. 'T=2048,F=4096' (same kind of pass)")
     ap.add_argument("--router", default="softmax", choices=["softmax", "sigmoid"],
