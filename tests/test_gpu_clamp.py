@@ -91,3 +91,32 @@ def test_clamped_mxfp8_forward_and_straight_through_backward():
     assert_close_rms(to_f64(b.dx), ref["dx"], tol=TOL_MXFP8, what="dx", bf16_out=True)
     for n in ("dW_gate", "dW_up", "dW_down"):
         assert_close_rms(getattr(b, n).double().cpu().numpy(), ref[n], tol=TOL_MXFP8, what=n)
+
+
+def test_clamped_mxfp8_forward_on_cta_pairs():
+    """Without the stash the MXFP8 FC1 runs on CTA pairs: the clamped forward there matches the
+    clamped oracle, and its expert outputs are the ones of the one-CTA kernel (which runs when
+    the stash is kept), bit for bit."""
+    from mixture_experts_ffn_warp_gb300 import MoeForwardMX, MxWeights
+    from helpers import TOL_MXFP8
+    shape = small_shape("mxclamp_pairs", T=700, H=256, F=384, E=5, k=2, mxfp8=True)
+    clamp = (-0.3, 0.2, -0.25, 0.25)
+    inp = gpu_inputs(shape, with_dy=False)
+    mw = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"])
+    m0 = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k, swiglu_clamp=clamp)
+    m1 = MoeForwardMX(shape.T, shape.H, shape.F, shape.E, shape.k, keep_fc1_c=True, swiglu_clamp=clamp)
+    out0 = m0(inp["x"], inp["logits"], mw)
+    m1(inp["x"], inp["logits"], mw)
+    torch.cuda.synchronize()
+    assert m0.ws.read_error() == 0 and m1.ws.read_error() == 0
+    rows = int(m0.perm.group_offsets[-1].item())
+    assert torch.equal(m0.h_q[:rows], m1.h_q[:rows])
+    assert torch.equal(m0.h_sf, m1.h_sf)
+    assert torch.equal(m0.y_perm[:rows], m1.y_perm[:rows])
+    idx, w = m0.topk_idx.cpu().numpy(), m0.topk_w.cpu().numpy()
+    hb = {n: bits(inp[n]) for n in ("x", "W_gate", "W_up", "W_down")}
+    xq = oracle.mx_roundtrip_rows(hb["x"])
+    wg, wu, wd = oracle.mx_roundtrip_weights(hb["W_gate"], hb["W_up"], hb["W_down"])
+    with oracle.swiglu_clamp(*clamp):
+        ref_out = oracle.moe_fwd(xq, wg, wu, wd, idx, w, round_mode=2, h_mx=True)["out"]
+    assert_close_rms(to_f64(out0), ref_out, tol=TOL_MXFP8, what="clamped MXFP8 out (CTA pairs)", bf16_out=True)
