@@ -307,7 +307,7 @@ def build_workload(shape, dev, stream, align=1):
         stash = R * 2 * F * 2 if shape.backward else 0
         g += [
             Group("permute", lambda: m.permute(inp["x"], stream), nbytes=T * H * 2 + R * H * 2 + R * 8,
-                  launches=3 if align > 1 else 2),   # + the zero fill of the padding rows
+                  launches=2),
             Group("fc1_swiglu", lambda: m.fc1(inp["W_gate"], inp["W_up"], stream), flop=4.0 * R * H * F,
                   nbytes=R * H * 2 + 2 * wbytes + R * F * 2 + stash),
             Group("fc2", lambda: m.fc2(inp["W_down"], stream), flop=2.0 * R * H * F,

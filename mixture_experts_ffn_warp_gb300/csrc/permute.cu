@@ -353,14 +353,17 @@ moe_status_t count_and_scan(const int32_t *topk_idx, int64_t R, int E, int align
 // kernel runs after the counting pass, which triggers it early: the token row's first
 // 32 * PRE 16-byte vectors are loaded before the wait (x was complete before the counting
 // pass passed its own wait; the loads go to the L2, the point of coherence, past the SM's L1),
-// the maps after it.  PRE = 8 (4 KB rows: H <= 2048), 16 for wider rows.
+// the maps after it.  PRE = 8 (4 KB rows: H <= 2048), 16 for wider rows.  Blocks from
+// token_blocks on (one per expert, aligned groups only) fill expert e's padding rows instead:
+// src_of_row = -1 and zero data.
 template <int KMAX, int PRE>
 __global__ void __launch_bounds__(kScatterWarps * 32)
 permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ topk_idx,
                        int64_t T, int k, int E, int row_vecs,
                        const int32_t *__restrict__ chunk_first, int32_t *__restrict__ dst_of_route,
                        int32_t *__restrict__ src_of_row, uint4 *__restrict__ x_perm,
-                       int64_t rows_cap, uint32_t *err) {
+                       int64_t rows_cap, const int32_t *__restrict__ group_sizes,
+                       const int32_t *__restrict__ group_offsets, int64_t token_blocks, uint32_t *err) {
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kScatterWarps + (threadIdx.x >> 5);
     const uint4 *src = x + (t < T ? t : 0) * row_vecs;
@@ -371,6 +374,16 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
             if (lane + 32 * u < row_vecs) pre[u] = __ldcg(src + lane + 32 * u);   // from the L2, not L1
     }
     pdl_wait();
+    if ((int64_t)blockIdx.x >= token_blocks) {   // an expert's padding rows
+        const int e = (int)(blockIdx.x - token_blocks);
+        const int64_t first = (int64_t)group_offsets[e] + group_sizes[e];
+        const int64_t last = group_offsets[e + 1] < rows_cap ? group_offsets[e + 1] : rows_cap;
+        for (int64_t row = first; row < last; ++row) {
+            if (threadIdx.x == 0) src_of_row[row] = -1;
+            for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) x_perm[row * row_vecs + v] = make_uint4(0, 0, 0, 0);
+        }
+        return;
+    }
     if (t >= T) return;
     int my_dst = -1;
     if (lane < k) {
@@ -418,15 +431,21 @@ permute_scatter_kernel(const uint4 *__restrict__ x, const int32_t *__restrict__ 
     }
 }
 
-void launch_scatter(int64_t blocks, cudaStream_t s, const uint4 *x, const int32_t *topk_idx, int64_t T, int k,
-                    int E, int row_vecs, const int32_t *chunk_first, int32_t *dst_of_route, int32_t *src_of_row,
-                    uint4 *x_perm, int64_t rows_cap, uint32_t *err) {
+// The scatter of T tokens, plus one block per expert filling its padding rows when `pad`.
+void launch_scatter(cudaStream_t s, const uint4 *x, const int32_t *topk_idx, int64_t T, int k, int E, int row_vecs,
+                    const int32_t *chunk_first, int32_t *dst_of_route, int32_t *src_of_row, uint4 *x_perm,
+                    int64_t rows_cap, const int32_t *group_sizes, const int32_t *group_offsets, bool pad,
+                    uint32_t *err) {
+    const int64_t tb = (T + kScatterWarps - 1) / kScatterWarps;
+    const unsigned blocks = (unsigned)(tb + (pad ? E : 0));
 #define MOE_SCATTER(KM)                                                                                        \
     (row_vecs > 256                                                                                            \
-         ? launch_k(permute_scatter_kernel<KM, 16>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s, x,   \
-                    topk_idx, T, k, E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, err)   \
-         : launch_k(permute_scatter_kernel<KM, 8>, dim3((unsigned)blocks), dim3(kScatterWarps * 32), 0, s, x,    \
-                    topk_idx, T, k, E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, err))
+         ? launch_k(permute_scatter_kernel<KM, 16>, dim3(blocks), dim3(kScatterWarps * 32), 0, s, x, topk_idx,  \
+                    T, k, E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, group_sizes,     \
+                    group_offsets, tb, err)                                                                      \
+         : launch_k(permute_scatter_kernel<KM, 8>, dim3(blocks), dim3(kScatterWarps * 32), 0, s, x, topk_idx,   \
+                    T, k, E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, group_sizes,     \
+                    group_offsets, tb, err))
     if (k <= 1) MOE_SCATTER(1);
     else if (k <= 2) MOE_SCATTER(2);
     else if (k <= 4) MOE_SCATTER(4);
@@ -436,21 +455,6 @@ void launch_scatter(int64_t blocks, cudaStream_t s, const uint4 *x, const int32_
 #undef MOE_SCATTER
 }
 
-// Padding rows of aligned groups: src_of_row = -1 and zero data.
-__global__ void permute_pad_kernel(const int32_t *__restrict__ group_sizes,
-                                   const int32_t *__restrict__ group_offsets, int E, int row_vecs,
-                                   int32_t *__restrict__ src_of_row, uint4 *__restrict__ x_perm,
-                                   int64_t rows_cap) {
-    pdl_wait();
-    const int e = blockIdx.x;
-    const int64_t first = (int64_t)group_offsets[e] + group_sizes[e];
-    const int64_t last = group_offsets[e + 1] < rows_cap ? group_offsets[e + 1] : rows_cap;
-    for (int64_t row = first; row < last; ++row) {
-        if (threadIdx.x == 0) src_of_row[row] = -1;
-        for (int v = threadIdx.x; v < row_vecs; v += blockDim.x)
-            x_perm[row * row_vecs + v] = make_uint4(0, 0, 0, 0);
-    }
-}
 
 }  // namespace
 }  // namespace moe
@@ -483,15 +487,10 @@ extern "C" moe_status_t moe_permute(const moe_bf16_t *x, const int32_t *topk_idx
                        ws_done_counter(ws), err, s) != MOE_OK)
         return MOE_ERR_CUDA;
     const int row_vecs = H / 8;
-    if (T > 0) {
-        const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
-        launch_scatter(blocks, s, reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts,
-                       dst_of_route, src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, err);
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    }
-    if (align > 1) {
-        launch_k(permute_pad_kernel, dim3(E), dim3(256), 0, s, group_sizes, group_offsets, E, row_vecs, src_of_row,
-                 reinterpret_cast<uint4 *>(x_perm), rows_cap);
+    if (T > 0) {   // (with no tokens there are no padding rows either)
+        launch_scatter(s, reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts, dst_of_route,
+                       src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, group_sizes, group_offsets,
+                       align > 1, err);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     return MOE_OK;
@@ -610,15 +609,10 @@ extern "C" moe_status_t moe_permute_static_scratch(const moe_bf16_t *x, const in
                        err + 1, err, s) != MOE_OK)
         return MOE_ERR_CUDA;
     const int row_vecs = H / 8;
-    if (T > 0) {
-        const int64_t blocks = (T + kScatterWarps - 1) / kScatterWarps;
-        launch_scatter(blocks, s, reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts,
-                       dst_of_route, src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, err);
-        if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
-    }
-    if (align > 1) {
-        launch_k(permute_pad_kernel, dim3(E), dim3(256), 0, s, group_sizes, group_offsets, E, row_vecs, src_of_row,
-                 reinterpret_cast<uint4 *>(x_perm), rows_cap);
+    if (T > 0) {   // (with no tokens there are no padding rows either)
+        launch_scatter(s, reinterpret_cast<const uint4 *>(x), topk_idx, T, k, E, row_vecs, counts, dst_of_route,
+                       src_of_row, reinterpret_cast<uint4 *>(x_perm), rows_cap, group_sizes, group_offsets,
+                       align > 1, err);
         if (launch_status() != MOE_OK) return MOE_ERR_CUDA;
     }
     if (error_word &&
