@@ -111,12 +111,13 @@ def _edge_or_random(rng, n):
 
 def test_backward_parity_mixtral_full_size_sampled():
     """Mixtral-like fwd+bwd at full size (T=8192, H=4096, F=14336, E=8, top-2),
-    in the bench's launch configuration: dx and d_topk_w of 64 sampled tokens, and
-    entries of every weight gradient of every expert -- most on the edges of the 256 x 256
-    gradient tiles (each entry sums over all of its expert's rows, the K tail included) --
-    against the oracle.  The tolerance scale is the RMS of the oracle's own values."""
+    in the bench's launch configuration (expert groups padded to 16 rows): dx and d_topk_w of
+    64 sampled tokens, and entries of every weight gradient of every expert -- most on the
+    edges of the 256 x 256 gradient tiles (each entry sums over all of its expert's rows and
+    its zero padding rows) -- against the oracle.  The tolerance scale is the RMS of the
+    oracle's own values.  (The K tail of unpadded groups: test_wgrad_group_sizes_on_cta_pairs.)"""
     shape = CONFIGS["mixtral"]
-    inp, m, b = _run(shape)
+    inp, m, b = _run(shape, align=16)
     idx, w = m.topk_idx.cpu().numpy(), m.topk_w.cpu().numpy()
     E, H, F = shape.E, shape.H, shape.F
     Wg, Wu, Wd = (host_experts(inp[n], range(E)) for n in ("W_gate", "W_up", "W_down"))
