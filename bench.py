@@ -324,7 +324,7 @@ def build_workload(shape, dev, stream, align=1):
                            nbytes=R * (H + F) * (1 + 1 / 32) + R * (H + F) * 2, launches=4))
         g += [
             Group("combine_bwd", lambda: b.combine_bwd(inp["dY"], stream),
-                  nbytes=T * H * 2 + R * H * ysz + R * H * 2 + R * 8, launches=2),
+                  nbytes=T * H * 2 + R * H * ysz + R * H * 2 + R * 8),
             Group("route_bwd", lambda: b.router_bwd(inp["logits"], stream), nbytes=R * 4 + R * 8 + T * E * 4),
             Group("dgrad_fc2_dswiglu", lambda: b.dgrad_fc2(Wd_b, stream), flop=2.0 * R * H * F,
                   nbytes=R * H * 2 + wb16 + R * 2 * F * 2 * 2),

@@ -27,8 +27,20 @@ template <int KMAX>
 __global__ void __launch_bounds__(kBwdWarps * 32)
 combine_bwd_kernel(const uint4 *__restrict__ dY, const uint4 *__restrict__ y_perm,
                    const int32_t *__restrict__ dst_of_route, const float *__restrict__ topk_w, int64_t T,
-                   int k, int slices, uint4 *__restrict__ dy_perm, float *__restrict__ d_topk_w) {
+                   int k, int slices, uint4 *__restrict__ dy_perm, float *__restrict__ d_topk_w,
+                   const int32_t *__restrict__ group_sizes, const int32_t *__restrict__ group_offsets,
+                   int64_t rows_cap, int64_t token_blocks) {
     pdl_wait();
+    if ((int64_t)blockIdx.x >= token_blocks) {
+        // one block per expert: its padding rows (aligned groups) get a zero gradient row,
+        // never uninitialised memory
+        const int e = (int)(blockIdx.x - token_blocks);
+        const int64_t first = (int64_t)group_offsets[e] + group_sizes[e];
+        const int64_t last = group_offsets[e + 1] < rows_cap ? group_offsets[e + 1] : rows_cap;
+        for (int64_t row = first; row < last; ++row)
+            for (int v = threadIdx.x; v < slices; v += blockDim.x) dy_perm[row * slices + v] = make_uint4(0, 0, 0, 0);
+        return;
+    }
     const int lane = threadIdx.x & 31;
     const int64_t t = (int64_t)blockIdx.x * kBwdWarps + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -88,25 +100,16 @@ combine_bwd_kernel(const uint4 *__restrict__ dY, const uint4 *__restrict__ y_per
     }
 }
 
-// Padding rows of aligned groups get a zero gradient row (never uninitialised memory).
-__global__ void zero_pad_rows_kernel(const int32_t *__restrict__ group_sizes,
-                                     const int32_t *__restrict__ group_offsets, int row_vecs,
-                                     uint4 *__restrict__ rows, int64_t rows_cap) {
-    pdl_wait();
-    const int e = blockIdx.x;
-    const int64_t first = (int64_t)group_offsets[e] + group_sizes[e];
-    const int64_t last = group_offsets[e + 1] < rows_cap ? group_offsets[e + 1] : rows_cap;
-    for (int64_t row = first; row < last; ++row)
-        for (int v = threadIdx.x; v < row_vecs; v += blockDim.x) rows[row * row_vecs + v] = make_uint4(0, 0, 0, 0);
-}
-
 template <int KMAX>
+// T tokens' blocks plus one block per expert for the padding rows.
 cudaError_t launch_combine_bwd(const moe_bf16_t *dY, const moe_bf16_t *y_perm, const int32_t *dst, const float *w,
-                               int64_t T, int H, int k, moe_bf16_t *dy_perm, float *d_topk_w, cudaStream_t s) {
+                               int64_t T, int H, int E, int k, moe_bf16_t *dy_perm, float *d_topk_w,
+                               const int32_t *group_sizes, const int32_t *group_offsets, int64_t rows_cap,
+                               cudaStream_t s) {
     const int64_t blocks = (T + kBwdWarps - 1) / kBwdWarps;
-    launch_k(combine_bwd_kernel<KMAX>, dim3((unsigned)blocks), dim3(kBwdWarps * 32), 0, s,
+    launch_k(combine_bwd_kernel<KMAX>, dim3((unsigned)(blocks + E)), dim3(kBwdWarps * 32), 0, s,
              reinterpret_cast<const uint4 *>(dY), reinterpret_cast<const uint4 *>(y_perm), dst, w, T, k, H / 8,
-             reinterpret_cast<uint4 *>(dy_perm), d_topk_w);
+             reinterpret_cast<uint4 *>(dy_perm), d_topk_w, group_sizes, group_offsets, rows_cap, blocks);
     return cudaGetLastError();
 }
 
@@ -135,19 +138,21 @@ extern "C" moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const moe_bf16_t *
     if (T > 0 && (!dY || !dst_of_route || !topk_w || (d_topk_w && !y_perm))) return MOE_ERR_INVALID_ARG;
     if (!all_aligned16({dY, y_perm, dy_perm})) return MOE_ERR_UNSUPPORTED;
     cudaStream_t s = (cudaStream_t)stream;
-    if (T > 0) {
+    if (T > 0) {   // (with no tokens every group is empty: no padding rows either)
         cudaError_t e;
-        if (k <= 1) e = launch_combine_bwd<1>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
-        else if (k <= 2) e = launch_combine_bwd<2>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
-        else if (k <= 4) e = launch_combine_bwd<4>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
-        else if (k <= 8) e = launch_combine_bwd<8>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
-        else if (k <= 16) e = launch_combine_bwd<16>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
-        else e = launch_combine_bwd<32>(dY, y_perm, dst_of_route, topk_w, T, H, k, dy_perm, d_topk_w, s);
+#define MOE_COMBINE_BWD(KM) \
+    launch_combine_bwd<KM>(dY, y_perm, dst_of_route, topk_w, T, H, E, k, dy_perm, d_topk_w, group_sizes, \
+                           group_offsets, rows_cap, s)
+        if (k <= 1) e = MOE_COMBINE_BWD(1);
+        else if (k <= 2) e = MOE_COMBINE_BWD(2);
+        else if (k <= 4) e = MOE_COMBINE_BWD(4);
+        else if (k <= 8) e = MOE_COMBINE_BWD(8);
+        else if (k <= 16) e = MOE_COMBINE_BWD(16);
+        else e = MOE_COMBINE_BWD(32);
+#undef MOE_COMBINE_BWD
         if (e != cudaSuccess) return MOE_ERR_CUDA;
     }
-    launch_k(zero_pad_rows_kernel, dim3(E), dim3(256), 0, s, group_sizes, group_offsets, H / 8,
-             reinterpret_cast<uint4 *>(dy_perm), rows_cap);
-    return launch_status();
+    return MOE_OK;
 }
 
 namespace {
