@@ -250,7 +250,7 @@ def group_align(shape, requested=None) -> int:
     return 16 if (shape.backward and not shape.mxfp8) else 1
 
 
-def build_workload(shape, dev, stream, align=1):
+def build_workload(shape, dev, stream, align=1, dw_bf16=False):
     """Inputs, pre-allocated layer objects and the step's kernel groups."""
     import torch
     from mixture_experts_ffn_warp_gb300 import MoeBackward, MoeBackwardMX, MoeForward, MoeForwardMX, MxWeights
@@ -259,13 +259,14 @@ def build_workload(shape, dev, stream, align=1):
     T, H, F, E, k = shape.T, shape.H, shape.F, shape.E, shape.k
     R = T * k
     sigmoid = shape.router == "sigmoid"
+    dw_dtype = torch.bfloat16 if dw_bf16 else torch.float32
     inp = make_inputs(shape, device=dev, with_dy=shape.backward, with_expert_bias=sigmoid)
     w = {"inp": inp, "shape": shape}
     if shape.mxfp8:
         mw = MxWeights(inp["W_gate"], inp["W_up"], inp["W_down"], stream)
         w["make_layer"] = lambda: MoeForwardMX(T, H, F, E, k, device=dev, router=shape.router,  # noqa: E731
                                                expert_bias=inp.get("expert_bias"), keep_fc1_c=shape.backward)
-        w["make_bwd"] = lambda f: MoeBackwardMX(f, want_d_logits=True)  # noqa: E731
+        w["make_bwd"] = lambda f: MoeBackwardMX(f, want_d_logits=True, dw_dtype=dw_dtype)  # noqa: E731
         m = w["make_layer"]()
         w.update(layer=m, mw=mw)
         m(inp["x"], inp["logits"], mw, stream)
@@ -279,7 +280,7 @@ def build_workload(shape, dev, stream, align=1):
                                              keep_fc1_c=shape.backward,
                                              router="sigmoid" if sigmoid else "softmax",
                                              expert_bias=inp.get("expert_bias"), weight_at=shape.weight_at)
-        w["make_bwd"] = lambda f: MoeBackward(f, want_d_logits=True)  # noqa: E731
+        w["make_bwd"] = lambda f: MoeBackward(f, want_d_logits=True, dw_dtype=dw_dtype)  # noqa: E731
         m = w["make_layer"]()
         w.update(layer=m)
         m(inp["x"], inp["logits"], inp["W_gate"], inp["W_up"], inp["W_down"], stream)
@@ -331,7 +332,7 @@ def build_workload(shape, dev, stream, align=1):
             Group("dgrad_fc1", lambda: b.dgrad_fc1(Wg_b, Wu_b, stream), flop=4.0 * R * H * F,
                   nbytes=R * 2 * F * 2 + 2 * wb16 + R * H * 4),
             Group("wgrad", lambda: b.wgrad(stream), flop=6.0 * R * H * F,
-                  nbytes=R * (F + H + H + 2 * F) * 2 + 3 * E * H * F * 4, launches=2),
+                  nbytes=R * (F + H + H + 2 * F) * 2 + 3 * E * H * F * (2 if dw_bf16 else 4), launches=2),
             Group("unpermute_sum", lambda: b.unpermute_sum(stream), nbytes=R * H * 4 + T * H * 2 + R * 8),
         ]
     w["groups"] = g
@@ -556,7 +557,7 @@ def run_gpu(args):
 
     with torch.cuda.stream(stream):
         align = group_align(shape, args.align)
-        w = build_workload(shape, dev, stream, align)
+        w = build_workload(shape, dev, stream, align, args.wgrad_dtype == "bf16")
     groups = w["groups"]
     m = w["layer"]
 
@@ -661,7 +662,7 @@ def run_gpu(args):
     else:
         roof = {"bound": "hbm", "achieved": dom.nbytes / t_dom / 1e9, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "peak_source": f"{pk['source']} HBM copy"}
-    roof.update(kernel=dom.name, frac=roof["achieved"] / roof["peak"], traffic=profiled_traffic(shape.name, dom.name),
+    roof.update(kernel=dom.name, frac=roof["achieved"] / roof["peak"], traffic=profiled_traffic(shape.name + ("_dwbf16" if args.wgrad_dtype == "bf16" else ""), dom.name),
                 algorithmic_bytes=dom.nbytes, algorithmic_flop=dom.flop)
 
     ffn = [g for g in groups if g.flop]
@@ -684,6 +685,7 @@ def run_gpu(args):
         "clocks": clk,
         "gpu_launches": args.steps * sum(g.launches for g in groups),
         "group_align": align,
+        "weight_grads": args.wgrad_dtype if shape.backward else None,
         "e2e": {"value": tokens / (ms_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": ms_e2e,
                 "how": "HostPipeline (two slots; upload, compute and download streams): K steps from the first "
@@ -708,6 +710,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="mixtral",
                     choices=["tiny", "fine_grained", "mixtral", "skewed", "dsv3_mxfp8"])
+    ap.add_argument("--wgrad-dtype", default="fp32", choices=["fp32", "bf16"],
+                    help="dtype the weight gradients are stored in (fp32 accumulation either way)")
     ap.add_argument("--align", type=int, default=None,
                     help="pad each expert's rows to a multiple of this (default: 16 for the bf16 "
                          "forward + backward, else 1)")

@@ -529,12 +529,25 @@ MOE_API moe_status_t moe_grouped_ffn_bwd(
     moe_bf16_t *dgu, float *dx_perm, moe_bf16_t *dx, float *dW_gate, float *dW_up, float *dW_down,
     float *d_topk_w, void *ws, size_t ws_bytes, moe_stream_t stream);
 
+/* moe_grouped_ffn_bwd with the weight gradients stored as bf16 (the fp32 accumulators rounded
+ * to nearest even once, the values moe_grouped_ffn_bwd stores rounded): dW_gate, dW_up bf16
+ * [E, H, F], dW_down bf16 [E, F, H] ("[JAX] Expert Parallelism", commit log: outputs in the
+ * input dtype).  Everything else as moe_grouped_ffn_bwd. */
+MOE_API moe_status_t moe_grouped_ffn_bwd_bf16(
+    const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
+    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const moe_bf16_t *y_perm,
+    const int32_t *dst_of_route, const int32_t *group_sizes, const int32_t *group_offsets,
+    const float *topk_w, int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm,
+    moe_bf16_t *dgu, float *dx_perm, moe_bf16_t *dx, moe_bf16_t *dW_gate, moe_bf16_t *dW_up,
+    moe_bf16_t *dW_down, float *d_topk_w, void *ws, size_t ws_bytes, moe_stream_t stream);
+
 /* The steps of moe_grouped_ffn_bwd, callable on their own (same arguments,
  * limits and errors; each reads what the previous steps wrote):
  *   moe_combine_bwd               dY -> dy_perm (+ zero padding rows), d_topk_w
  *   moe_grouped_dgrad_fc2_dswiglu dy_perm, fc1_c -> dgu
  *   moe_grouped_dgrad_fc1         dgu -> dx_perm
  *   moe_grouped_wgrad             x_perm, h, dy_perm, dgu -> dW_gate, dW_up, dW_down
+ *                                 (moe_grouped_wgrad_bf16: the same gradients stored as bf16)
  *   moe_unpermute_sum             dx_perm -> dx */
 MOE_API moe_status_t moe_combine_bwd(const moe_bf16_t *dY, const moe_bf16_t *y_perm, const int32_t *dst_of_route,
                                      const float *topk_w, const int32_t *group_sizes,
@@ -559,6 +572,11 @@ MOE_API moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf16_
                                        const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap,
                                        float *dW_gate, float *dW_up, float *dW_down, void *ws,
                                        size_t ws_bytes, moe_stream_t stream);
+MOE_API moe_status_t moe_grouped_wgrad_bf16(const moe_bf16_t *x_perm, const moe_bf16_t *h,
+                                            const moe_bf16_t *dy_perm, const moe_bf16_t *dgu,
+                                            const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap,
+                                            moe_bf16_t *dW_gate, moe_bf16_t *dW_up, moe_bf16_t *dW_down, void *ws,
+                                            size_t ws_bytes, moe_stream_t stream);
 MOE_API moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *dst_of_route, int64_t T, int H,
                                        int k, moe_bf16_t *dx, moe_stream_t stream);
 

@@ -51,6 +51,7 @@ SIGNATURES = {
     "moe_grouped_fc2_weighted": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_unpermute_combine": (_st, [_vp, _vp, _vp, _i64, _int, _int, _vp, _vp]),
     "moe_grouped_ffn_bwd": (_st, [_vp] * 12 + [_i64, _int, _int, _int, _int, _i64] + [_vp] * 8 + [_vp, _sz, _vp]),
+    "moe_grouped_ffn_bwd_bf16": (_st, [_vp] * 12 + [_i64, _int, _int, _int, _int, _i64] + [_vp] * 8 + [_vp, _sz, _vp]),
     "moe_combine_bwd": (_st, [_vp, _vp, _vp, _vp, _vp, _vp, _i64, _int, _int, _int, _i64, _vp, _vp, _vp]),
     "moe_grouped_dgrad_fc2_dswiglu": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_grouped_dgrad_fc2_dswiglu_clamped": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64] + [C.c_float] * 4
@@ -59,6 +60,7 @@ SIGNATURES = {
                                        + [_vp, _vp, _vp, _sz, _vp]),
     "moe_grouped_dgrad_fc1": (_st, [_vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _sz, _vp]),
     "moe_grouped_wgrad": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_grouped_wgrad_bf16": (_st, [_vp, _vp, _vp, _vp, _vp, _int, _int, _int, _i64, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_unpermute_sum": (_st, [_vp, _vp, _i64, _int, _int, _vp, _vp]),
     "moe_mx_tile_scale_bytes": (_sz, [_i64, _int, _int]),
     "moe_grouped_quantize_mxfp8": (_st, [_vp, _i64, _int, _vp, _int, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -405,10 +407,15 @@ def moe_grouped_dgrad_fc1(dgu, W_gate, W_up, group_offsets, ws: Workspace, dx_pe
 
 def moe_grouped_wgrad(x_perm, h, dy_perm, dgu, group_offsets, ws: Workspace, dW_gate, dW_up, dW_down,
                       stream=None):
-    """fp32 weight gradients per expert, K = the group's rows (moe.h)."""
+    """Weight gradients per expert, K = the group's rows (moe.h): fp32 accumulation, stored in
+    the dtype of the dW tensors (fp32, or bf16 through moe_grouped_wgrad_bf16)."""
     rows_cap, H = x_perm.shape
     E, _, F = dW_gate.shape
-    _check("moe_grouped_wgrad", load_library().moe_grouped_wgrad(
+    fn = "moe_grouped_wgrad_bf16" if dW_gate.dtype == torch.bfloat16 else "moe_grouped_wgrad"
+    for name, t in (("dW_gate", dW_gate), ("dW_up", dW_up), ("dW_down", dW_down)):
+        if t.dtype != dW_gate.dtype or t.dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError(f"{name}: fp32 or bf16, all three the same dtype")
+    _check(fn, getattr(load_library(), fn)(
         _ptr(x_perm), _ptr(h), _ptr(dy_perm), _ptr(dgu), _ptr(group_offsets), E, H, F, rows_cap,
         _ptr(dW_gate), _ptr(dW_up), _ptr(dW_down), _ptr(ws.buf), ws.nbytes, _stream(stream)))
 
@@ -422,9 +429,12 @@ def moe_unpermute_sum(dx_perm, dst_of_route, dx, stream=None):
 
 
 def moe_grouped_ffn_bwd(dY, x_perm, W_gate, W_up, W_down, fc1_c, h, y_perm, perm: "Permutation", topk_w,
-                        ws: Workspace, want_d_topk_w: bool = True, stream=None):
-    """The whole backward in one call (moe.h); allocates its outputs and scratch.
+                        ws: Workspace, want_d_topk_w: bool = True, stream=None, dw_dtype=torch.float32):
+    """The whole backward in one call (moe.h); allocates its outputs and scratch.  dw_dtype:
+    fp32 weight gradients (moe_grouped_ffn_bwd) or bf16 (moe_grouped_ffn_bwd_bf16).
     Returns dict(dx, dW_gate, dW_up, dW_down, d_topk_w)."""
+    if dw_dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("dw_dtype: torch.float32 or torch.bfloat16")
     dev = dY.device
     T, H = dY.shape
     E, _, F = W_gate.shape
@@ -438,15 +448,16 @@ def moe_grouped_ffn_bwd(dY, x_perm, W_gate, W_up, W_down, fc1_c, h, y_perm, perm
         _need(t, name, dt, shp, dev)
     out = {
         "dx": torch.empty(T, H, dtype=torch.bfloat16, device=dev),
-        "dW_gate": torch.empty(E, H, F, dtype=torch.float32, device=dev),
-        "dW_up": torch.empty(E, H, F, dtype=torch.float32, device=dev),
-        "dW_down": torch.empty(E, F, H, dtype=torch.float32, device=dev),
+        "dW_gate": torch.empty(E, H, F, dtype=dw_dtype, device=dev),
+        "dW_up": torch.empty(E, H, F, dtype=dw_dtype, device=dev),
+        "dW_down": torch.empty(E, F, H, dtype=dw_dtype, device=dev),
         "d_topk_w": torch.empty(T, k, dtype=torch.float32, device=dev) if want_d_topk_w else None,
     }
     dy_perm = torch.empty(cap, H, dtype=torch.bfloat16, device=dev)
     dgu = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev)
     dx_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
-    _check("moe_grouped_ffn_bwd", load_library().moe_grouped_ffn_bwd(
+    fn = "moe_grouped_ffn_bwd_bf16" if dw_dtype == torch.bfloat16 else "moe_grouped_ffn_bwd"
+    _check(fn, getattr(load_library(), fn)(
         _ptr(dY), _ptr(x_perm), _ptr(W_gate), _ptr(W_up), _ptr(W_down), _ptr(fc1_c), _ptr(h), _ptr(y_perm),
         _ptr(perm.dst_of_route), _ptr(perm.group_sizes), _ptr(perm.group_offsets), _ptr(topk_w),
         T, H, F, E, k, cap, _ptr(dy_perm), _ptr(dgu), _ptr(dx_perm), _ptr(out["dx"]), _ptr(out["dW_gate"]),

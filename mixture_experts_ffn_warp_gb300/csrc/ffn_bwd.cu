@@ -293,17 +293,19 @@ extern "C" moe_status_t moe_grouped_dgrad_fc1(const moe_bf16_t *dgu, const moe_b
     return gg::launch<Op::DGRAD_FC1, 128>(tA, tB0, tB1, tC, tC, a, bound, (cudaStream_t)stream);
 }
 
-extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf16_t *h, const moe_bf16_t *dy_perm,
-                                          const moe_bf16_t *dgu, const int32_t *group_offsets, int E, int H, int F,
-                                          int64_t rows_cap, float *dW_gate, float *dW_up, float *dW_down, void *ws,
-                                          size_t ws_bytes, moe_stream_t stream) {
-    MOE_NVTX_RANGE("moe_grouped_wgrad");
+namespace {
+
+// The weight gradients, stored as fp32 (elem = 4) or bf16 (elem = 2); fp32 accumulation either way.
+moe_status_t wgrad_impl(const moe_bf16_t *x_perm, const moe_bf16_t *h, const moe_bf16_t *dy_perm,
+                        const moe_bf16_t *dgu, const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap,
+                        void *dW_gate, void *dW_up, void *dW_down, int elem, void *ws, size_t ws_bytes,
+                        moe_stream_t stream) {
     moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK) return st;
     if (!group_offsets || !dW_gate || !dW_up || !dW_down) return MOE_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;
     if (rows_cap == 0) {   // no rows at all: every expert's gradient is zero
-        const size_t n = (size_t)E * H * F * sizeof(float);
+        const size_t n = (size_t)E * H * F * (size_t)elem;
         if (cudaMemsetAsync(dW_gate, 0, n, s) != cudaSuccess || cudaMemsetAsync(dW_up, 0, n, s) != cudaSuccess ||
             cudaMemsetAsync(dW_down, 0, n, s) != cudaSuccess)
             return MOE_ERR_CUDA;
@@ -323,9 +325,9 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
             // each operand's 128 columns of a 64-row K step in one load (two 64-column chunks)
             if (!tmap_bf16_col_chunks(&tA, A, M, rows, M, 64) || !tmap_bf16_col_chunks(&tB, B, N, rows, N, 64))
                 return MOE_ERR_UNSUPPORTED;
-            if (down ? !tmap_store_2d(&tC0, dW_down, 4, H, (uint64_t)E * F, H)
-                     : (!tmap_store_2d(&tC0, dW_gate, 4, F, (uint64_t)E * H, F) ||
-                        !tmap_store_2d(&tC1, dW_up, 4, F, (uint64_t)E * H, F)))
+            if (down ? !tmap_store_2d(&tC0, dW_down, elem, H, (uint64_t)E * F, H)
+                     : (!tmap_store_2d(&tC0, dW_gate, elem, F, (uint64_t)E * H, F) ||
+                        !tmap_store_2d(&tC1, dW_up, elem, F, (uint64_t)E * H, F)))
                 return MOE_ERR_UNSUPPORTED;
             if (down) tC1 = tC0;
             gp::Args a{};
@@ -341,6 +343,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
             a.b_rows = reinterpret_cast<const __nv_bfloat16 *>(B);
             a.ldb = N;
             a.rows_cap = rows_cap;
+            a.w_bf16 = elem == 2;
             a.err = ws_error_word(ws);
             st = gp::launch<gp::Op::WGRAD>(tA, tA, tB, tC0, tC1, a, (int64_t)E * a.nt_m * a.nt_n, s);
             if (st != MOE_OK) return st;
@@ -351,7 +354,7 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
         const int bn = (H % 256 == 0) ? 256 : 128;
         CUtensorMap tA, tB, tC;
         if (!tmap_bf16_2d(&tA, h, F, rows, F, 64, 64) || !tmap_bf16_2d(&tB, dy_perm, H, rows, H, 64, 64) ||
-            !tmap_store_2d(&tC, dW_down, 4, H, (uint64_t)E * F, H))
+            !tmap_store_2d(&tC, dW_down, elem, H, (uint64_t)E * F, H))
             return MOE_ERR_UNSUPPORTED;
         gg::Args a{};
         a.group_offsets = group_offsets;
@@ -361,7 +364,9 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
         a.m_tiles = F / gg::BM;
         a.n_tiles = H / bn;
         a.rows_cap = rows_cap;
-        a.out_f32 = dW_down;
+        a.out_f32 = static_cast<float *>(dW_down);
+        a.out0 = static_cast<__nv_bfloat16 *>(dW_down);
+        a.w_bf16 = elem == 2;
         a.ld0 = H;
         a.expert_stride = (int64_t)F * H;
         a.err = ws_error_word(ws);
@@ -374,7 +379,8 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
         CUtensorMap tA, tB, tC0, tC1;
         if (!tmap_bf16_2d(&tA, x_perm, H, rows, H, 64, 64) ||
             !tmap_bf16_2d(&tB, dgu, 2 * (uint64_t)F, rows, 2 * (uint64_t)F, 64, 64) ||
-            !tmap_store_2d(&tC0, dW_gate, 4, F, (uint64_t)E * H, F) || !tmap_store_2d(&tC1, dW_up, 4, F, (uint64_t)E * H, F))
+            !tmap_store_2d(&tC0, dW_gate, elem, F, (uint64_t)E * H, F) ||
+            !tmap_store_2d(&tC1, dW_up, elem, F, (uint64_t)E * H, F))
             return MOE_ERR_UNSUPPORTED;
         gg::Args a{};
         a.group_offsets = group_offsets;
@@ -385,15 +391,39 @@ extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf
         a.m_tiles = H / gg::BM;
         a.n_tiles = 2 * F / 256;
         a.rows_cap = rows_cap;
-        a.out_f32 = dW_gate;
+        a.out_f32 = static_cast<float *>(dW_gate);
+        a.out0 = static_cast<__nv_bfloat16 *>(dW_gate);
         a.ld0 = F;
-        a.out1_f32 = dW_up;
+        a.out1_f32 = static_cast<float *>(dW_up);
+        a.out1 = static_cast<__nv_bfloat16 *>(dW_up);
         a.ld1 = F;
+        a.w_bf16 = elem == 2;
         a.expert_stride = (int64_t)H * F;
         a.err = ws_error_word(ws);
         const int64_t tiles = (int64_t)E * a.m_tiles * a.n_tiles;
         return gg::launch<Op::WGRAD_GATEUP, 256>(tA, tB, tB, tC0, tC1, a, tiles, s);
     }
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_wgrad(const moe_bf16_t *x_perm, const moe_bf16_t *h, const moe_bf16_t *dy_perm,
+                                          const moe_bf16_t *dgu, const int32_t *group_offsets, int E, int H, int F,
+                                          int64_t rows_cap, float *dW_gate, float *dW_up, float *dW_down, void *ws,
+                                          size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_wgrad");
+    return wgrad_impl(x_perm, h, dy_perm, dgu, group_offsets, E, H, F, rows_cap, dW_gate, dW_up, dW_down, 4, ws,
+                      ws_bytes, stream);
+}
+
+extern "C" moe_status_t moe_grouped_wgrad_bf16(const moe_bf16_t *x_perm, const moe_bf16_t *h,
+                                               const moe_bf16_t *dy_perm, const moe_bf16_t *dgu,
+                                               const int32_t *group_offsets, int E, int H, int F, int64_t rows_cap,
+                                               moe_bf16_t *dW_gate, moe_bf16_t *dW_up, moe_bf16_t *dW_down, void *ws,
+                                               size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_wgrad_bf16");
+    return wgrad_impl(x_perm, h, dy_perm, dgu, group_offsets, E, H, F, rows_cap, dW_gate, dW_up, dW_down, 2, ws,
+                      ws_bytes, stream);
 }
 
 extern "C" moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *dst_of_route, int64_t T, int H, int k,
@@ -407,14 +437,15 @@ extern "C" moe_status_t moe_unpermute_sum(const float *dx_perm, const int32_t *d
     return cuda_status(combine_rows(dx_perm, dst_of_route, nullptr, T, H, k, dx, (cudaStream_t)stream));
 }
 
-extern "C" moe_status_t moe_grouped_ffn_bwd(
-    const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
-    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const moe_bf16_t *y_perm,
-    const int32_t *dst_of_route, const int32_t *group_sizes, const int32_t *group_offsets, const float *topk_w,
-    int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm, moe_bf16_t *dgu,
-    float *dx_perm, moe_bf16_t *dx, float *dW_gate, float *dW_up, float *dW_down, float *d_topk_w, void *ws,
-    size_t ws_bytes, moe_stream_t stream) {
-    MOE_NVTX_RANGE("moe_grouped_ffn_bwd");
+namespace {
+
+moe_status_t ffn_bwd_impl(const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate,
+                          const moe_bf16_t *W_up, const moe_bf16_t *W_down, const moe_bf16_t *fc1_c,
+                          const moe_bf16_t *h, const moe_bf16_t *y_perm, const int32_t *dst_of_route,
+                          const int32_t *group_sizes, const int32_t *group_offsets, const float *topk_w, int64_t T,
+                          int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm, moe_bf16_t *dgu,
+                          float *dx_perm, moe_bf16_t *dx, void *dW_gate, void *dW_up, void *dW_down, int elem,
+                          float *d_topk_w, void *ws, size_t ws_bytes, moe_stream_t stream) {
     moe_status_t st = check_sizes(E, H, F, rows_cap, ws, ws_bytes);
     if (st != MOE_OK) return st;
     st = moe_combine_bwd(dY, y_perm, dst_of_route, topk_w, group_sizes, group_offsets, T, H, E, k, rows_cap,
@@ -428,8 +459,36 @@ extern "C" moe_status_t moe_grouped_ffn_bwd(
                                    stream);
         if (st != MOE_OK) return st;
     }
-    st = moe_grouped_wgrad(x_perm, h, dy_perm, dgu, group_offsets, E, H, F, rows_cap, dW_gate, dW_up, dW_down, ws,
-                           ws_bytes, stream);
+    st = wgrad_impl(x_perm, h, dy_perm, dgu, group_offsets, E, H, F, rows_cap, dW_gate, dW_up, dW_down, elem, ws,
+                    ws_bytes, stream);
     if (st != MOE_OK) return st;
     return moe_unpermute_sum(dx_perm, dst_of_route, T, H, k, dx, stream);
+}
+
+}  // namespace
+
+extern "C" moe_status_t moe_grouped_ffn_bwd(
+    const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
+    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const moe_bf16_t *y_perm,
+    const int32_t *dst_of_route, const int32_t *group_sizes, const int32_t *group_offsets, const float *topk_w,
+    int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm, moe_bf16_t *dgu,
+    float *dx_perm, moe_bf16_t *dx, float *dW_gate, float *dW_up, float *dW_down, float *d_topk_w, void *ws,
+    size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_ffn_bwd");
+    return ffn_bwd_impl(dY, x_perm, W_gate, W_up, W_down, fc1_c, h, y_perm, dst_of_route, group_sizes, group_offsets,
+                        topk_w, T, H, F, E, k, rows_cap, dy_perm, dgu, dx_perm, dx, dW_gate, dW_up, dW_down, 4,
+                        d_topk_w, ws, ws_bytes, stream);
+}
+
+extern "C" moe_status_t moe_grouped_ffn_bwd_bf16(
+    const moe_bf16_t *dY, const moe_bf16_t *x_perm, const moe_bf16_t *W_gate, const moe_bf16_t *W_up,
+    const moe_bf16_t *W_down, const moe_bf16_t *fc1_c, const moe_bf16_t *h, const moe_bf16_t *y_perm,
+    const int32_t *dst_of_route, const int32_t *group_sizes, const int32_t *group_offsets, const float *topk_w,
+    int64_t T, int H, int F, int E, int k, int64_t rows_cap, moe_bf16_t *dy_perm, moe_bf16_t *dgu,
+    float *dx_perm, moe_bf16_t *dx, moe_bf16_t *dW_gate, moe_bf16_t *dW_up, moe_bf16_t *dW_down, float *d_topk_w,
+    void *ws, size_t ws_bytes, moe_stream_t stream) {
+    MOE_NVTX_RANGE("moe_grouped_ffn_bwd_bf16");
+    return ffn_bwd_impl(dY, x_perm, W_gate, W_up, W_down, fc1_c, h, y_perm, dst_of_route, group_sizes, group_offsets,
+                        topk_w, T, H, F, E, k, rows_cap, dy_perm, dgu, dx_perm, dx, dW_gate, dW_up, dW_down, 2,
+                        d_topk_w, ws, ws_bytes, stream);
 }

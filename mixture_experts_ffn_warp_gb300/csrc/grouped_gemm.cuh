@@ -17,7 +17,7 @@
 //   FC2            y = h W_down (bf16 out)              M-grouped, K = F
 //   DGRAD_DSWIGLU  dh = dy W_down^T, then dSwiGLU       M-grouped, K = H
 //   DGRAD_FC1      dx = dg W_gate^T + du W_up^T (fp32)   M-grouped, K = 2F
-//   WGRAD_DOWN     dW_down[e] = h_e^T dy_e (fp32)        K-grouped (K = rows of e)
+//   WGRAD_DOWN     dW_down[e] = h_e^T dy_e (fp32 / bf16) K-grouped (K = rows of e)
 //   WGRAD_GATEUP   [dW_gate|dW_up][e] = x_e^T [dg|du]_e K-grouped
 //   FC1_MX         FC1_SWIGLU on MXFP8 operands; h is quantised to MXFP8 (along F)
 //                  in the epilogue, scales written in the MMA tile layout
@@ -91,6 +91,9 @@ struct Args {
     // [gate_lo, gate_hi] and u to [up_lo, up_hi] before SwiGLU, inclusive bounds
     int clamp;
     float gate_lo, gate_hi, up_lo, up_hi;
+    // WGRAD_*: the gradients are stored as bf16 in out0 / out1 (row pitch ld0 / ld1) instead of
+    // fp32 in out_f32 / out1_f32
+    int w_bf16;
     uint32_t *err;
 };
 
@@ -545,12 +548,13 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     for (int c = 0; c < BN; c += 32) {
                         const int n = tl.n0 + c;
                         if (n >= args.N) break;
-                        float *dst = (OP == Op::WGRAD_GATEUP && n >= args.n_split)
-                                         ? args.out1_f32 + eoff + (size_t)row * args.ld1 + (n - args.n_split)
-                                         : args.out_f32 + eoff + (size_t)row * args.ld0 + n;
-                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                        for (int q4 = 0; q4 < 8; ++q4) d4[q4] = make_uint4(0, 0, 0, 0);
+                        const bool second = OP == Op::WGRAD_GATEUP && n >= args.n_split;
+                        const size_t off = eoff + (size_t)row * (second ? args.ld1 : args.ld0) +
+                                           (second ? n - args.n_split : n);
+                        uint4 *d4 = args.w_bf16 ? reinterpret_cast<uint4 *>((second ? args.out1 : args.out0) + off)
+                                                : reinterpret_cast<uint4 *>((second ? args.out1_f32 : args.out_f32) + off);
+                        const int nq = args.w_bf16 ? 4 : 8;   // 32 columns: 64 or 128 bytes
+                        for (int q4 = 0; q4 < nq; ++q4) d4[q4] = make_uint4(0, 0, 0, 0);
                     }
                     continue;
                 }
@@ -699,7 +703,14 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     const int n = tl.n0 + c;
                     if (n < args.N) {
                         const bool second = OP == Op::WGRAD_GATEUP && n >= args.n_split;
-                        stage_f32x32(d, second ? &tmC1 : &tmC0, second ? n - args.n_split : n, grow0);
+                        if (args.w_bf16) {
+                            float v[32];
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(d[i]);
+                            stage_bf16x32(v, second ? &tmC1 : &tmC0, second ? n - args.n_split : n, grow0);
+                        } else {
+                            stage_f32x32(d, second ? &tmC1 : &tmC0, second ? n - args.n_split : n, grow0);
+                        }
                     }
                 }
             } else {   // FC2, FC2_MX (y_perm: bf16 rows) and DGRAD_FC1 (dx_perm: fp32 rows)

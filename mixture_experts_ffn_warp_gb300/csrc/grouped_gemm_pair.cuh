@@ -104,6 +104,7 @@ struct Args {
     // within an expert (M blocks fastest or N blocks fastest), the column where the output
     // switches to the second matrix (0: none), and the operands' row tensors for the K tail
     int M, nt_m, nt_n, m_fastest, n_split;
+    int w_bf16;        // WGRAD: the gradients are stored as bf16 (else fp32)
     const __nv_bfloat16 *a_rows;   // [rows, M]
     int64_t lda;
     const __nv_bfloat16 *b_rows;   // [rows, N]
@@ -670,8 +671,8 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
         uint32_t xphase = 0;   // bit b: parity of the next wait on xbar[pair][b]
         bool alive = true;
         if constexpr (OP == Op::WGRAD) {
-            // this thread's gradient row; 32 fp32 columns at a time staged as 32 rows x 64 B
-            // (64-byte swizzle) and stored by TMA in boxes of 16 columns x 32 rows
+            // this thread's gradient row; 32 columns at a time staged as 32 rows x 64 B (64-byte
+            // swizzle) and stored by TMA in boxes of 16 fp32 or 32 bf16 columns x 32 rows
             auto put_w = [&](int j, uint4 v) {
                 *reinterpret_cast<uint4 *>(stg + slot * SLOT_BYTES + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v;
             };
@@ -703,6 +704,19 @@ pair_gemm_kernel(const __grid_constant__ CUtensorMap tmW0, const __grid_constant
                     const int ncol = tl.n0 + c0;
                     const bool second = args.n_split > 0 && ncol >= args.n_split;
                     const int col = second ? ncol - args.n_split : ncol;
+                    if (args.w_bf16) {   // 32 bf16 columns: one 32-row x 64-byte slot, one TMA store
+                        slot_open();
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            uint4 pk;
+                            __nv_bfloat162 *h2 = reinterpret_cast<__nv_bfloat162 *>(&pk);
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) h2[i] = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+                            put_w(j, pk);
+                        }
+                        slot_store(second ? &tmStash : &tmOut, col, (int)grow0);
+                        continue;
+                    }
 #pragma unroll
                     for (int hf = 0; hf < 2; ++hf) {
                         slot_open();

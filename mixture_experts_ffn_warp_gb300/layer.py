@@ -151,9 +151,14 @@ class MoeBackward:
     following the backward contract of "Add MoE + expert-parallel Python API
     surface, PyTorch reference, and tests" (FP32 weight and route gradients);
     with want_d_logits also the fp32 router-logits gradient ("[JAX] Expert
-    Parallelism: JAX primitives + VJPs", commit log: the router backward)."""
+    Parallelism: JAX primitives + VJPs", commit log: the router backward).
+    dw_dtype=torch.bfloat16 stores the weight gradients as bf16 instead (the
+    same fp32 accumulators, rounded once)."""
 
-    def __init__(self, fwd: MoeForward, want_d_topk_w: bool = True, want_d_logits: bool = False):
+    def __init__(self, fwd: MoeForward, want_d_topk_w: bool = True, want_d_logits: bool = False,
+                 dw_dtype=torch.float32):
+        if dw_dtype not in (torch.float32, torch.bfloat16):
+            raise ValueError("dw_dtype: torch.float32 or torch.bfloat16")
         if want_d_logits and not want_d_topk_w:
             raise ValueError("the logits gradient needs d_topk_w")
         if fwd.fc1_c is None:
@@ -166,9 +171,9 @@ class MoeBackward:
         self.dgu = torch.empty(cap, 2 * F, dtype=torch.bfloat16, device=dev)
         self.dx_perm = torch.empty(cap, H, dtype=torch.float32, device=dev)
         self.dx = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-        self.dW_gate = torch.empty(E, H, F, dtype=torch.float32, device=dev)
-        self.dW_up = torch.empty(E, H, F, dtype=torch.float32, device=dev)
-        self.dW_down = torch.empty(E, F, H, dtype=torch.float32, device=dev)
+        self.dW_gate = torch.empty(E, H, F, dtype=dw_dtype, device=dev)
+        self.dW_up = torch.empty(E, H, F, dtype=dw_dtype, device=dev)
+        self.dW_down = torch.empty(E, F, H, dtype=dw_dtype, device=dev)
         self.d_topk_w = torch.empty(T, k, dtype=torch.float32, device=dev) if want_d_topk_w else None
         self.d_logits = torch.empty(T, E, dtype=torch.float32, device=dev) if want_d_logits else None
 
@@ -304,8 +309,9 @@ class MoeBackwardMX(MoeBackward):
     (MxWeights.dequantized) -- with the g | u stash of the MXFP8 FC1.  Outputs as
     MoeBackward (gradients with respect to the unquantised x and weights)."""
 
-    def __init__(self, fwd: MoeForwardMX, want_d_topk_w: bool = True, want_d_logits: bool = False):
-        super().__init__(fwd, want_d_topk_w, want_d_logits)
+    def __init__(self, fwd: MoeForwardMX, want_d_topk_w: bool = True, want_d_logits: bool = False,
+                 dw_dtype=torch.float32):
+        super().__init__(fwd, want_d_topk_w, want_d_logits, dw_dtype)
         cap, dev = fwd.rows_cap, fwd.device
         self.x_deq = torch.empty(cap, fwd.H, dtype=torch.bfloat16, device=dev)
         self.h_deq = torch.empty(cap, fwd.F, dtype=torch.bfloat16, device=dev)

@@ -177,3 +177,50 @@ def test_wgrad_group_sizes_on_cta_pairs():
                 continue
             err = (got - want[n]).abs().max().item()
             assert err <= 1e-4 * want[n].abs().max().item(), (e, n, err)   # fp32 accumulation
+
+
+@pytest.mark.parametrize("sizes", [[0, 5, 16, 1100, 4077, 1000, 37, 2000],   # CTA pairs (>= 1024 rows on average)
+                                   [0, 5, 16, 300, 77, 129, 37, 200]])       # the one-CTA kernels
+def test_wgrad_bf16_is_the_rounded_fp32(sizes):
+    """moe_grouped_wgrad_bf16 stores the same fp32 accumulators as moe_grouped_wgrad, each rounded
+    to the nearest bf16 (ties to even) once: bit for bit, on both weight-gradient kernels, with
+    experts of no rows (exact zeros), of fewer than 16 rows and of ragged tails."""
+    H, F = 256, 512
+    E, R = len(sizes), sum(sizes)
+    g = torch.Generator(device="cuda").manual_seed(12)
+    x = torch.randn(R, H, generator=g, device="cuda").to(torch.bfloat16)
+    h = torch.randn(R, F, generator=g, device="cuda").to(torch.bfloat16)
+    dy = torch.randn(R, H, generator=g, device="cuda").to(torch.bfloat16)
+    dgu = torch.randn(R, 2 * F, generator=g, device="cuda").to(torch.bfloat16)
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(sizes)]), dtype=torch.int32, device="cuda")
+    ws = Workspace(R, E, 1)
+    out = {}
+    for dt in (torch.float32, torch.bfloat16):
+        dWg = torch.full((E, H, F), float("nan"), device="cuda", dtype=dt)
+        dWu = torch.full((E, H, F), float("nan"), device="cuda", dtype=dt)
+        dWd = torch.full((E, F, H), float("nan"), device="cuda", dtype=dt)
+        moe_grouped_wgrad(x, h, dy, dgu, offs, ws, dWg, dWu, dWd)
+        out[dt] = (dWg, dWu, dWd)
+    torch.cuda.synchronize()
+    assert ws.read_error() == 0
+    for f32, b16 in zip(out[torch.float32], out[torch.bfloat16]):
+        assert torch.equal(f32.to(torch.bfloat16), b16)
+    assert torch.count_nonzero(out[torch.bfloat16][0][0]) == 0   # the expert without rows
+
+
+def test_one_call_backward_with_bf16_weight_gradients():
+    """moe_grouped_ffn_bwd_bf16: dx and d_topk_w as moe_grouped_ffn_bwd, the weight gradients its
+    fp32 ones rounded to bf16."""
+    shape = SHAPES["ragged"]
+    inp, m, b = _run(shape)
+    res = {}
+    for dt in (torch.float32, torch.bfloat16):
+        res[dt] = moe_grouped_ffn_bwd(inp["dY"], m.perm.x_perm, inp["W_gate"], inp["W_up"], inp["W_down"], m.fc1_c,
+                                      m.h, m.y_perm, m.perm, m.topk_w, m.ws, dw_dtype=dt)
+    torch.cuda.synchronize()
+    assert m.ws.read_error() == 0
+    f, q = res[torch.float32], res[torch.bfloat16]
+    assert torch.equal(f["dx"], q["dx"]) and torch.equal(f["d_topk_w"], q["d_topk_w"])
+    for n in ("dW_gate", "dW_up", "dW_down"):
+        assert q[n].dtype == torch.bfloat16
+        assert torch.equal(f[n].to(torch.bfloat16), q[n])
