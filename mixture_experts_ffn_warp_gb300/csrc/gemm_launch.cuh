@@ -27,7 +27,7 @@ moe_status_t launch(const CUtensorMap &a, const CUtensorMap &b0, const CUtensorM
     if (st != MOE_OK) return st;
     const int64_t sms = device_sm_count();
     const int grid = (int)(tiles_bound < sms ? tiles_bound : sms);
-    launch_k(kern, dim3(grid), dim3(kThreads), C::SMEM_BYTES, s, a, b0, b1, c0, c1, args);
+    launch_k(kern, dim3(grid), dim3(C::THREADS), C::SMEM_BYTES, s, a, b0, b1, c0, c1, args);
     return launch_status();
 }
 

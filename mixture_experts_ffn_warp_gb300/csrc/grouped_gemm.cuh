@@ -1,7 +1,7 @@
 // grouped_gemm.cuh -- persistent, warp-specialised grouped GEMM on tcgen05 for the
 // expert FFN (forward, backward and the MXFP8 forward).
 //
-// One CTA per SM, 6 warps:
+// One CTA per SM, 6 or 10 warps:
 //   warp 0      TMA producer (one lane): A and B tiles (and, for MXFP8, their
 //               block scales) -> a ring of smem stages
 //   warp 1      MMA issuer (one elected lane issues tcgen05.mma, M=128 x N=BN; K=16 per
@@ -9,7 +9,7 @@
 //               TMEM (double-buffered for bf16, single for MXFP8, whose scales
 //               take the other half of TMEM)
 //   warps 2..5  epilogue: tcgen05.ld -> fused activation -> swizzled smem slots ->
-//               TMA stores (row by row only for a warp whose rows cross a group end)
+//   (or 2..9)   TMA stores (row by row only for a warp whose rows cross a group end)
 // Tiles are scheduled on the device from group_offsets (no host round trip).
 //
 // Ops (A row = one permuted route unless stated):
@@ -40,7 +40,6 @@ enum class Op : int { FC1_SWIGLU, FC2, DGRAD_DSWIGLU, DGRAD_FC1, WGRAD_DOWN, WGR
 
 constexpr int BM = 128;
 constexpr int UMMA_K = 16;
-constexpr int kThreads = 192;
 constexpr int kMaxE = 1024;
 
 template <Op OP>
@@ -104,7 +103,14 @@ struct Cfg {
     static constexpr int B_BYTES = BN * 128;
     static constexpr int SF_BYTES = MX ? 512 + (BN / 128) * 512 : 0;
     static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + SF_BYTES + 1023) / 1024 * 1024;
-    static constexpr int STG_BYTES = 4 * 4096;   // epilogue staging: 2 x 2 KB per epilogue warp
+    // Epilogue warps: eight (two per TMEM lane quarter, alternate 32-column chunks) for the ops
+    // whose chunks are independent stores -- FC2, FC2_MX, DGRAD_FC1 and the weight gradients,
+    // where the epilogue is exposed (the MXFP8 single accumulator) or outweighs a short K loop
+    // (experts with few rows) -- with one 2 KB staging slot each; four with two slots otherwise.
+    static constexpr int EPI = (Traits<OP>::k_grouped || OP == Op::FC2 || OP == Op::FC2_MX || OP == Op::DGRAD_FC1) ? 8 : 4;
+    static constexpr int THREADS = 64 + 32 * EPI;
+    static constexpr int SLOTS = EPI == 8 ? 1 : 2;
+    static constexpr int STG_BYTES = EPI * SLOTS * 2048;
     // dynamic shared memory: 227 KB per CTA less ~9 KB of static tables and barriers
     static constexpr int DYN_BUDGET = 232448 - 9216;
     static constexpr int FIT = (DYN_BUDGET - STG_BYTES - 1024) / STAGE_BYTES;
@@ -215,7 +221,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Args &a, const int *s_o
 }
 
 template <Op OP, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<OP, BN>::THREADS, 1)
 grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                     const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmC0,
                     const __grid_constant__ CUtensorMap tmC1, const Args args) {
@@ -243,7 +249,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int b = 0; b < 2; ++b) {
             sm100::mbar_init(&tfull_bar[b], 1);
-            sm100::mbar_init(&tempty_bar[b], 4 * 32);
+            sm100::mbar_init(&tempty_bar[b], C::EPI * 32);
         }
         sm100::mbar_init(&drain_bar, 1);
         s_abort = 0;
@@ -263,7 +269,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     pdl_wait();
     const uint64_t wait_ns = device_wait_limit(args.err);   // pipeline waits' limit
     const int E = args.E;
-    for (int i = threadIdx.x; i <= E; i += kThreads) s_off[i] = args.group_offsets[i];
+    for (int i = threadIdx.x; i <= E; i += blockDim.x) s_off[i] = args.group_offsets[i];
     __syncthreads();
     if (warp == 2) {
         // s_start[e] = tiles before expert e (M-grouped: m-blocks x n_tiles)
@@ -491,14 +497,17 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         // ============================================================ epilogue
         const int q = warp & 3;            // TMEM lane quarter this warp may access
         const int r = q * 32 + lane;       // accumulator row of this thread
+        const int ew = warp - 2;           // epilogue warp
+        const int sub = ew >> 2;           // which of the quarter's warps (eight epilogue warps)
+        constexpr int NSUB = C::EPI / 4;
         // Output staging of this warp: two 2 KB slots of 32 rows x 64 bytes in the 64-byte
         // swizzle (16-byte chunk j of row i at chunk j ^ ((i / 2) % 4): conflict-free
         // 16-byte writes), each written back by one TMA store while the other fills.
-        uint8_t *stg = smem + S * C::STAGE_BYTES + q * 4096;
-        const uint32_t stg_s = smem_base + S * C::STAGE_BYTES + q * 4096;
+        uint8_t *stg = smem + S * C::STAGE_BYTES + ew * C::SLOTS * 2048;
+        const uint32_t stg_s = smem_base + S * C::STAGE_BYTES + ew * C::SLOTS * 2048;
         int slot = 0;
         auto slot_open = [&]() {
-            if (lane == 0) sm100::bulk_wait_read<1>();   // the store that last used this slot has read it
+            if (lane == 0) sm100::bulk_wait_read<C::SLOTS - 1>();   // the store that last used this slot has read it
             __syncwarp();
         };
         auto slot_put = [&](int j, uint4 v) {
@@ -511,7 +520,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 sm100::tma_store_2d(tm, stg_s + slot * 2048, col, (int)row0);
                 sm100::bulk_commit();
             }
-            slot ^= 1;
+            slot = slot + 1 == C::SLOTS ? 0 : slot + 1;
         };
         auto stage_bf16x32 = [&](const float (&v)[32], const CUtensorMap *tm, int col, int64_t row0) {
             slot_open();
@@ -545,7 +554,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 const size_t eoff = (size_t)tl.e * (size_t)args.expert_stride;
                 if (tl.kb == 0) {
                     // expert with no routes: its weight gradient is exactly zero
-                    for (int c = 0; c < BN; c += 32) {
+                    for (int c = 32 * sub; c < BN; c += 32 * NSUB) {
                         const int n = tl.n0 + c;
                         if (n >= args.N) break;
                         const bool second = OP == Op::WGRAD_GATEUP && n >= args.n_split;
@@ -696,7 +705,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // rows of the [E * M, N] view of the expert-stacked gradient
                 const int64_t grow0 = (int64_t)tl.e * args.M + tl.m0 + q * 32;
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = 32 * sub; c < BN; c += 32 * NSUB) {
                     uint32_t d[32];
                     sm100::tmem_ld32(tacc + c, d);
                     sm100::tmem_ld_wait();
@@ -723,7 +732,7 @@ grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                     rw = src >= 0 ? args.route_w[src] : 0.0f;
                 }
 #pragma unroll 1
-                for (int c = 0; c < BN; c += 32) {
+                for (int c = 32 * sub; c < BN; c += 32 * NSUB) {
                     uint32_t d[32];
                     sm100::tmem_ld32(tacc + c, d);
                     sm100::tmem_ld_wait();
