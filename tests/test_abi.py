@@ -105,6 +105,12 @@ def test_host_validation_before_launch(lib):
     assert lib.moe_unpermute_combine(mis, fake, nul, 3, 16, 2, fake, nul) == 2
     assert lib.moe_unpermute_combine(fake, fake, nul, 3, 16, 2, mis, nul) == 2
     assert lib.moe_unpermute_sum(mis, fake, 3, 16, 2, fake, nul) == 2
+    # weight gradients, fp32 and bf16: null outputs, sizes, workspace -- refused before a launch
+    for wg in (lib.moe_grouped_wgrad, lib.moe_grouped_wgrad_bf16):
+        assert wg(fake, fake, fake, fake, fake, 4, 128, 128, 64, nul, fake, fake, fake, 256, nul) == 1
+        assert wg(fake, fake, fake, fake, fake, 4, 100, 128, 64, fake, fake, fake, fake, 256, nul) == 2
+        assert wg(fake, fake, fake, fake, fake, 4, 128, 128, 64, fake, fake, fake, nul, 0, nul) == 5
+    assert lib.moe_grouped_ffn_bwd_bf16(*([fake] * 12), 4, 100, 128, 4, 2, 8, *([fake] * 8), fake, 256, nul) == 2
 
 
 def test_product_path_has_no_oracle_dependency():
