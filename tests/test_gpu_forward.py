@@ -142,6 +142,34 @@ def test_permute_aligned_groups(align):
     assert_close_rms(to_f64(out), refo["out"], what="out", bf16_out=True)
 
 
+@pytest.mark.parametrize("T,k,E,align", [
+    (2000, 8, 40, 1),      # 16000 routes: one cluster of 8 CTAs exchanging counts on chip
+    (4096, 8, 256, 128),   # 32768 routes, 16 warps a CTA: the cluster pass's largest problem
+    (1000, 32, 1024, 1),   # 32000 routes, a [16][1024] count table a CTA, in one cluster
+    (4097, 8, 256, 16),    # 32776 routes: chunk counts and the last block's scan
+    (3000, 32, 1024, 8),   # 96000 routes over 1024 experts: chunk counts
+])
+def test_permute_counting_paths(T, k, E, align):
+    """Both counting passes (one cluster while the routes fit it, chunk counts otherwise)
+    give the oracle's maps, group sizes and offsets and copy the rows bit for bit, with a
+    skewed load, dropped routes and padded groups."""
+    H = 64
+    g = torch.Generator(device="cuda").manual_seed(T + k + E)
+    x = torch.randn(T, H, generator=g, device="cuda", dtype=torch.bfloat16)
+    # a Zipf-like load: expert e drawn with weight 1 / (e + 1)
+    wts = 1.0 / torch.arange(1, E + 1, device="cuda", dtype=torch.float32)
+    idx = torch.multinomial(wts.expand(T, E), k, replacement=False, generator=g).to(torch.int32)
+    idx[::97, 0] = -1                     # dropped routes
+    ws = Workspace(T, E, k)
+    p = moe_permute(x, idx, E, ws, align=align)
+    torch.cuda.synchronize()
+    assert ws.read_error() == 0
+    ref = oracle.permute(idx.cpu().numpy(), E, align=align)
+    _check_perm(p, ref, T * k)
+    used = int(ref["group_offsets"][-1])
+    assert np.array_equal(bits(p.x_perm[:used]), oracle.gather_rows(bits(x), k, ref["src_of_row"], used))
+
+
 def test_permute_dropped_and_invalid_ids():
     T, H, E, k = 700, 64, 6, 3
     g = torch.Generator(device="cuda").manual_seed(3)

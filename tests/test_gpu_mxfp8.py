@@ -103,8 +103,10 @@ def test_quantize_weights_bit_exact():
         assert np.array_equal(rs_all[e], rs)
 
 
-def test_permute_mxfp8_bit_exact():
-    shape = small_shape("perm", T=1500, H=384, F=128, E=16, k=4)
+@pytest.mark.parametrize("T,H,E,k", [(1500, 384, 16, 4),    # counted in one cluster
+                                     (8500, 128, 16, 8)])   # 68000 routes: chunk counts
+def test_permute_mxfp8_bit_exact(T, H, E, k):
+    shape = small_shape("perm", T=T, H=H, F=128, E=E, k=k)
     inp = gpu_inputs(shape, with_dy=False)
     idx, _ = moe_route_topk(inp["logits"], shape.k)
     ws = Workspace(shape.T, shape.E, shape.k)
