@@ -60,33 +60,42 @@ combine_bwd_kernel(const uint4 *__restrict__ dY, const uint4 *__restrict__ y_per
         dot[j] = 0.0f;
     }
     const bool want_dot = d_topk_w != nullptr;
-    for (int s = lane; s < slices; s += 32) {
-        const uint4 g = __ldg(dY + t * slices + s);
-        const __nv_bfloat162 *gp = reinterpret_cast<const __nv_bfloat162 *>(&g);
-        float d[8];
+    // U 16-byte slices a lane per pass: the U dY loads, then per route the U y loads, are
+    // in flight together (one slice at a time left the loop bound by load latency)
+    constexpr int U = 4;
+    for (int s0 = lane; s0 < slices; s0 += 32 * U) {
+        uint4 g[U];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const float2 f = __bfloat1622float2(gp[i]);
-            d[2 * i] = f.x;
-            d[2 * i + 1] = f.y;
-        }
+        for (int u = 0; u < U; ++u)
+            if (s0 + 32 * u < slices) g[u] = __ldg(dY + t * slices + s0 + 32 * u);
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {
             if (dst[j] < 0) continue;
-            uint4 o;
-            __nv_bfloat162 *op = reinterpret_cast<__nv_bfloat162 *>(&o);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) op[i] = __floats2bfloat162_rn(w[j] * d[2 * i], w[j] * d[2 * i + 1]);
-            dy_perm[(int64_t)dst[j] * slices + s] = o;
+            const uint4 *yrow = y_perm + (int64_t)dst[j] * slices;
+            uint4 *orow = dy_perm + (int64_t)dst[j] * slices;
+            uint4 yv[U];
             if (want_dot) {   // bf16 expert output of the route, widened exactly
-                const uint4 yv = __ldg(y_perm + (int64_t)dst[j] * slices + s);
-                const __nv_bfloat162 *yp = reinterpret_cast<const __nv_bfloat162 *>(&yv);
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    if (s0 + 32 * u < slices) yv[u] = __ldg(yrow + s0 + 32 * u);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (s0 + 32 * u >= slices) continue;
+                const __nv_bfloat162 *gp = reinterpret_cast<const __nv_bfloat162 *>(&g[u]);
+                uint4 o;
+                __nv_bfloat162 *op = reinterpret_cast<__nv_bfloat162 *>(&o);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
-                    const float2 f = __bfloat1622float2(yp[i]);
-                    dot[j] = fmaf(d[2 * i], f.x, dot[j]);
-                    dot[j] = fmaf(d[2 * i + 1], f.y, dot[j]);
+                    const float2 d = __bfloat1622float2(gp[i]);
+                    op[i] = __floats2bfloat162_rn(w[j] * d.x, w[j] * d.y);
+                    if (want_dot) {
+                        const float2 f = __bfloat1622float2(reinterpret_cast<const __nv_bfloat162 *>(&yv[u])[i]);
+                        dot[j] = fmaf(d.x, f.x, dot[j]);
+                        dot[j] = fmaf(d.y, f.y, dot[j]);
+                    }
                 }
+                orow[s0 + 32 * u] = o;
             }
         }
     }
