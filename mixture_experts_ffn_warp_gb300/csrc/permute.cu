@@ -525,16 +525,21 @@ moe_status_t count_and_scan(const int32_t *topk_idx, int64_t R, int E, int align
     // The cluster pass takes all the shared memory a CTA may have, so that no scatter CTA
     // (launched early, loading its token rows) shares an SM with it: measured on GB300, the
     // counting CTAs' shared-memory and global accesses otherwise queue behind those loads.
+    // Where the cluster cannot be launched (its attribute refused, or no eight whole SMs of one
+    // GPC available to this context) the chunked pass below runs instead.
     int dev = 0, optin = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
         return MOE_ERR_CUDA;
     const size_t dyn = optin > 1024 ? (size_t)optin - 1024 : 0;   // (static arrays: 256 bytes)
-    if (const int w = cluster_count_warps(R, E, dyn)) {
-        const int ctas = (int)(chunks < kClusterCtas ? chunks : kClusterCtas);
+    const int w = cluster_count_warps(R, E, dyn);
+    if (w > 0) {
         if (cudaFuncSetAttribute(permute_count_cluster_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)dyn) != cudaSuccess)
-            return MOE_ERR_CUDA;
+                                 (int)dyn) != cudaSuccess) {
+            (void)cudaGetLastError();   // refused: not this call's error, the chunked pass runs
+            goto chunked;
+        }
+        const int ctas = (int)(chunks < kClusterCtas ? chunks : kClusterCtas);
         cudaLaunchConfig_t cfg{};
         cfg.gridDim = dim3((unsigned)ctas);
         cfg.blockDim = dim3((unsigned)(w * 32));
@@ -549,12 +554,14 @@ moe_status_t count_and_scan(const int32_t *topk_idx, int64_t R, int E, int align
         attr[1].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 2;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, permute_count_cluster_kernel, topk_idx, R, E, align, rows_cap,
-                                                 dst_of_route, src_of_row, group_sizes, group_offsets, mtile, err);
-        if (e != cudaSuccess) return cuda_status(e);
-        *final_rows = true;
-        return launch_status();
+        if (cudaLaunchKernelEx(&cfg, permute_count_cluster_kernel, topk_idx, R, E, align, rows_cap, dst_of_route,
+                               src_of_row, group_sizes, group_offsets, mtile, err) == cudaSuccess) {
+            *final_rows = true;
+            return launch_status();
+        }
+        (void)cudaGetLastError();   // refused: not this call's error, the chunked pass runs
     }
+chunked:
     if (chunks > 0) {
         // the final scan stages the count matrix in shared memory when it fits
         const int64_t mat = chunks * E;
