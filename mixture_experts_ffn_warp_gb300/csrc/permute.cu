@@ -12,6 +12,7 @@
 // (One-GPU counterpart of the expert-major dispatch layout with device-side
 // group sizes: "[JAX] Expert Parallelism: JAX primitives + VJPs", commit log;
 // "MoE training optimization": problem sizes supplied from device buffers.)
+#include "carveout.cuh"
 #include "common.cuh"
 
 namespace moe {
@@ -671,7 +672,9 @@ void launch_scatter(cudaStream_t s, const uint4 *x, const int32_t *topk_idx, int
     const int64_t tb = (T + kScatterWarps - 1) / kScatterWarps;
     const unsigned blocks = (unsigned)(tb + (pad ? E : 0));
 #define MOE_SCATTER(KM)                                                                                        \
-    (row_vecs > 256                                                                                            \
+    (prefer_max_smem_carveout<permute_scatter_kernel<KM, 16>>(),                                               \
+     prefer_max_smem_carveout<permute_scatter_kernel<KM, 8>>(),                                                \
+     row_vecs > 256                                                                                            \
          ? launch_k(permute_scatter_kernel<KM, 16>, dim3(blocks), dim3(kScatterWarps * 32), 0, s, x, topk_idx,  \
                     T, k, E, row_vecs, chunk_first, dst_of_route, src_of_row, x_perm, rows_cap, group_sizes,     \
                     group_offsets, tb, err)                                                                      \

@@ -12,6 +12,7 @@
 // log: fused_topk_with_score_function on fp32 logits, sigmoid scores with an
 // expert routing bias, the kernel's sum + 1e-20 normalisation, and its backward
 // giving the fp32 logits cotangent).
+#include "carveout.cuh"
 #include "common.cuh"
 
 namespace moe {
@@ -113,6 +114,7 @@ template <int VPL, bool SIGMOID>
 cudaError_t launch(const float *logits, const float *bias, int64_t T, int E, int k, int normalize, int32_t *idx,
                    float *w, cudaStream_t s) {
     int64_t blocks = (T + kRouteWarps - 1) / kRouteWarps;
+    prefer_max_smem_carveout<route_topk_kernel<VPL, SIGMOID>>();   // the counting pass runs next
     return launch_k(route_topk_kernel<VPL, SIGMOID>, dim3((unsigned)blocks), dim3(kRouteWarps * 32), 0, s, logits,
                     bias, T, E, k, normalize, idx, w);
 }
