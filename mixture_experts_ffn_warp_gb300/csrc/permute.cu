@@ -5,10 +5,12 @@
 //               every route its stable rank among the chunk's routes to the
 //               same expert (bit-sliced warp ballots + per-warp running counts); the last
 //               block to finish turns the chunk counts into group sizes,
-//               (aligned) group offsets and each chunk's first row per expert;
-//   2. scatter: one warp per token writes dst_of_route / src_of_row and
-//               copies the token's row once from HBM into its k destinations
-//               with 16-byte loads and stores.
+//               (aligned) group offsets and each chunk's first row per expert.  Up to
+//               32768 routes one thread-block cluster does the same with the counts
+//               exchanged in distributed shared memory, and writes the final rows;
+//   2. scatter: one warp per token writes dst_of_route / src_of_row (unless the
+//               cluster pass wrote them) and copies the token's row once from HBM
+//               into its k destinations with 16-byte loads and stores.
 // (One-GPU counterpart of the expert-major dispatch layout with device-side
 // group sizes: "[JAX] Expert Parallelism: JAX primitives + VJPs", commit log;
 // "MoE training optimization": problem sizes supplied from device buffers.)
